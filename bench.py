@@ -1,0 +1,442 @@
+#!/usr/bin/env python3
+"""Benchmark of the quaternion cumulative-product scan, forward + backward.
+
+One step = one forward scan (``quat_cumprod_fwd``) and one backward
+(``quat_cumprod_bwd``) over one batch of seeded synthetic inputs, through the C
+ABI.  Metric: elements per second, elements = B*S*H*J, with inputs resident in
+HBM when the timed region starts; ``e2e`` is the same metric with the inputs
+copied from pinned host memory and the outputs copied back inside each step.
+
+``--impl reference`` times the fp64 CPU oracle (the only reference
+implementation of this scan) on the host cores, on a bounded lane sample of the
+same workload.
+
+Multi-GPU (torchrun): every rank runs its own independent batch (lanes are
+independent; no collective on the data path), timing is the max over ranks,
+``value`` is the total over ranks (weak scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from quaternion_cumulative_product_gb300 import workloads  # noqa: E402
+
+METRIC = "quat-scan fwd+bwd elements/s (B*S*H*J)"
+UNIT = "elements/s"
+DEFAULT_WORKLOAD = "mamba3"
+FWD_BYTES_PER_ELEMENT = 32      # read q, write cum
+BWD_BYTES_PER_ELEMENT = 48      # read q and d_cum, write d_q
+L2_BYTES = 126 * (1 << 20)
+FALLBACK_HBM_GBS = 6800.0
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+KERNEL_SOURCES = [os.path.join(ROOT, "quaternion_cumulative_product_gb300", "csrc", f)
+                  for f in ("quat_scan.cu", "quat_device.cuh")]
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for p in KERNEL_SOURCES:
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peak_hbm():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "measured (MEASURED_PEAKS.json hbm_gbs)"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback (6.8 TB/s, earlier GB300 measurement)"
+
+
+def recorded_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it matches the current source."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            for line in f:
+                parts = line.split()
+                if len(parts) >= 4 and parts[0] == kernel and parts[1] == workload:
+                    fields = dict(p.split("=", 1) for p in parts[2:] if "=" in p)
+                    if fields.get("source_hash") == kernel_source_hash():
+                        return float(fields["dram_bytes_per_launch"])
+    except (OSError, ValueError, KeyError):
+        pass
+    return None
+
+
+# ---------------------------------------------------------------------------
+# Distributed helpers (host logic; tested with gloo on CPU).
+# ---------------------------------------------------------------------------
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return world, rank, local
+
+
+def rank_seed(base_seed: int, rank: int) -> int:
+    """Each rank draws its own independent batch (weak scaling)."""
+    return base_seed + 1000 * rank
+
+
+def reduce_max(value: float, device=None) -> float:
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(device=None):
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
+        if device is not None and device.type == "cuda":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+# ---------------------------------------------------------------------------
+# Clocks sampler (nvidia-smi during the timed region).
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(prefix="qs_clocks_", suffix=".csv")
+            os.close(fd)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_index), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.2)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                p = [x.strip() for x in line.split(",")]
+                if len(p) >= 9:
+                    rows.append(p)
+        os.unlink(self.path)
+        if not rows:
+            return None
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        pw = [num(r[3]) for r in rows if num(r[3]) is not None]
+        loaded = [s for s, p in zip(sm, pw) if p is not None and p > 200] or sm
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            for name, val in zip(names, r[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(loaded) if loaded else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(rows),
+                "power_w_max": max(pw) if pw else None}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle baseline (bounded lane sample).
+# ---------------------------------------------------------------------------
+def oracle_sample(w, max_lanes: int, arrays=None):
+    """A bounded lane sample of workload ``w`` for the CPU oracle (fp64 arrays)."""
+    import numpy as np
+    if arrays is None:
+        arrays = workloads.make_inputs(w) if w.elements <= (1 << 26) else _sample_inputs(w, max_lanes)
+    q, init, d_cum = arrays
+    H, J = q.shape[2], q.shape[3]
+    avail = q.shape[0] * H * J
+    lanes = min(max_lanes, avail)
+    rng = np.random.default_rng(0)
+    pick = np.sort(rng.choice(avail, lanes, replace=False))
+    sq, si, sd = workloads.sample_lanes((q, init, d_cum), pick, H, J)
+    return tuple(a.astype(np.float64) for a in (sq, si, sd)), lanes
+
+
+def time_oracle(sample, target_s: float):
+    """Runs oracle fwd+bwd on the sample until ``target_s`` elapsed (at least once).
+
+    Returns (elements/s, threads used, repetitions, seconds).
+    """
+    import oracle
+    sq, si, sd = sample
+    cores = os.cpu_count() or 1
+    done, elapsed, reps = 0, 0.0, 0
+    while elapsed < target_s or reps == 0:
+        t0 = time.perf_counter()
+        oracle.fwd(sq, si, nthreads=cores)
+        oracle.bwd(sq, si, sd, nthreads=cores)
+        elapsed += time.perf_counter() - t0
+        done += sq.shape[1] * sq.shape[2]
+        reps += 1
+    return done / elapsed, cores, reps, elapsed
+
+
+def sample_description(w, lanes, reps, cores):
+    return (f"{lanes} of {w.lanes} lanes (full S={w.S}) of {w.describe()}, fwd+bwd, "
+            f"{reps} repetition(s), fp64 C oracle, {cores} threads")
+
+
+def _sample_inputs(w, max_lanes):
+    # Workloads too large to draw on the host in full: the same recipe on fewer
+    # batch entries (same distributions and seed).
+    B = max(1, min(w.B, max_lanes // max(1, w.H * w.J)))
+    small = workloads.custom(w.name, B, w.S, w.H, w.J, q_kind=w.q_kind, theta_max=w.theta_max,
+                             init_kind=w.init_kind, dcum_sigma=w.dcum_sigma, seed=w.seed)
+    return workloads.make_inputs(small)
+
+
+# ---------------------------------------------------------------------------
+# Arms.
+# ---------------------------------------------------------------------------
+def run_reference(args, w, world, rank):
+    if rank != 0:
+        return 0
+    sample, lanes = oracle_sample(w, args.cpu_lanes)
+    for _ in range(args.warmup):
+        time_oracle(sample, 0.0)
+    rates, t_all, reps_all, cores = [], 0.0, 0, os.cpu_count() or 1
+    for _ in range(args.steps):
+        rate, cores, reps, secs = time_oracle(sample, 0.0)
+        rates.append(rate)
+        t_all += secs
+        reps_all += reps
+    value = sum(rates) / len(rates)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t_all / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded generator, workloads.py)",
+        "config": {"workload": w.describe(), "B": w.B, "S": w.S, "H": w.H, "J": w.J,
+                   "elements": w.elements},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": sample_description(w, lanes, 1, cores) + " per step"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args, w, world, rank, local):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    import quaternion_cumulative_product_gb300 as qs
+
+    if not torch.cuda.is_available():
+        raise RuntimeError("bench.py needs a CUDA device (the scan has no CPU path)")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group("nccl", device_id=dev)
+    qs.load_library()
+
+    wr = workloads.custom(w.name, w.B, w.S, w.H, w.J, q_kind=w.q_kind, theta_max=w.theta_max,
+                          init_kind=w.init_kind, dcum_sigma=w.dcum_sigma, seed=rank_seed(w.seed, rank))
+    q_np, init_np, dcum_np = workloads.make_inputs(wr)
+    q = torch.from_numpy(q_np).to(dev)
+    init = torch.from_numpy(init_np).to(dev)
+    d_cum = torch.from_numpy(dcum_np).to(dev)
+    cum = torch.empty_like(q)
+    d_q = torch.empty_like(q)
+    d_init = torch.empty_like(init)
+    tensor_bytes = q.numel() * 4
+    flush = tensor_bytes < 2 * L2_BYTES
+    scratch = torch.empty(2 * L2_BYTES // 4, device=dev) if flush else None
+    stream = torch.cuda.current_stream(dev)
+    launches = [0]
+
+    def step():
+        qs.quat_cumprod_fwd(q, init, cum)
+        qs.quat_cumprod_bwd(q, init, d_cum, d_q, d_init)
+        launches[0] += 2
+
+    for _ in range(args.warmup):
+        step()
+    st = qs.quat_cumprod_status(device=dev)
+    if st != qs.QS_OK:
+        raise RuntimeError(f"device status after warm-up: {qs.quat_cumprod_strerror(st)}")
+
+    # ---- device-timed region -------------------------------------------------
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    torch.cuda.synchronize(dev)
+    barrier(dev)
+    sampler.start()
+    launches[0] = 0
+    torch.cuda.synchronize(dev)
+    for i in range(args.steps):
+        if flush:
+            scratch.zero_()
+        e0, e1, e2 = ev[i]
+        e0.record(stream)
+        qs.quat_cumprod_fwd(q, init, cum)
+        e1.record(stream)
+        qs.quat_cumprod_bwd(q, init, d_cum, d_q, d_init)
+        e2.record(stream)
+        launches[0] += 2
+    torch.cuda.synchronize(dev)
+    clocks = sampler.stop()
+    barrier(dev)
+    st = qs.quat_cumprod_status(device=dev)
+    if st != qs.QS_OK:
+        raise RuntimeError(f"device status after timed region: {qs.quat_cumprod_strerror(st)}")
+    fwd_ms = [a.elapsed_time(b) for a, b, _ in ev]
+    bwd_ms = [b.elapsed_time(c) for _, b, c in ev]
+    step_ms_local = sum(f + b for f, b in zip(fwd_ms, bwd_ms)) / args.steps
+    step_ms = reduce_max(step_ms_local, dev)
+    E = w.elements
+    value = world * E / (step_ms * 1e-3)
+
+    # ---- end to end through the public API with pinned host buffers ---------
+    h_q = torch.from_numpy(q_np).pin_memory()
+    h_init = torch.from_numpy(init_np).pin_memory()
+    h_dcum = torch.from_numpy(dcum_np).pin_memory()
+    o_cum = torch.empty(q.shape, dtype=torch.float32).pin_memory()
+    o_dq = torch.empty(q.shape, dtype=torch.float32).pin_memory()
+    o_di = torch.empty(init.shape, dtype=torch.float32).pin_memory()
+
+    def e2e_step():
+        dq_ = h_q.to(dev, non_blocking=True)
+        di_ = h_init.to(dev, non_blocking=True)
+        dd_ = h_dcum.to(dev, non_blocking=True)
+        c_ = qs.quat_cumprod_fwd(dq_, di_)
+        gq_, gi_ = qs.quat_cumprod_bwd(dq_, di_, dd_)
+        o_cum.copy_(c_, non_blocking=True)
+        o_dq.copy_(gq_, non_blocking=True)
+        o_di.copy_(gi_, non_blocking=True)
+
+    del cum, d_q
+    for _ in range(min(args.warmup, 3)):
+        e2e_step()
+    e2e_steps = max(1, min(args.steps, args.e2e_steps))
+    torch.cuda.synchronize(dev)
+    barrier(dev)
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = reduce_max(a.elapsed_time(b) / e2e_steps, dev)
+    st = qs.quat_cumprod_status(device=dev)
+    if st != qs.QS_OK:
+        raise RuntimeError(f"device status after e2e: {qs.quat_cumprod_strerror(st)}")
+    h2d = (h_q.numel() + h_init.numel() + h_dcum.numel()) * 4
+    d2h = (o_cum.numel() + o_dq.numel() + o_di.numel()) * 4
+
+    if rank != 0:
+        return 0
+    peak, peak_src = measured_peak_hbm()
+    bwd_avg = statistics.mean(bwd_ms)
+    fwd_avg = statistics.mean(fwd_ms)
+    bwd_gbs = BWD_BYTES_PER_ELEMENT * E / (bwd_avg * 1e-3) / 1e9
+    fwd_gbs = FWD_BYTES_PER_ELEMENT * E / (fwd_avg * 1e-3) / 1e9
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        sample, lanes = oracle_sample(w, args.cpu_lanes, (q_np, init_np, dcum_np))
+        rate, cores, reps, _ = time_oracle(sample, args.cpu_seconds)
+        cpu = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle",
+               "sample": sample_description(w, lanes, reps, cores)}
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded generator, workloads.py)",
+        "config": {"workload": w.describe(), "B": w.B, "S": w.S, "H": w.H, "J": w.J,
+                   "elements": E, "bytes_per_tensor": tensor_bytes,
+                   "l2": ("L2 flushed (2x126 MB write) before every step" if flush else
+                          f"inputs larger than L2 ({tensor_bytes / 1e6:.0f} MB per tensor > 126 MB), no flush"),
+                   "parallelism": ("one independent batch per GPU, no collective" if world > 1
+                                   else "single GPU")},
+        "roofline": {"bound": "hbm", "kernel": "quat_scan_bwd_kernel", "achieved": bwd_gbs, "peak": peak,
+                     "unit": "GB/s", "frac": bwd_gbs / peak, "peak_source": peak_src,
+                     "traffic": recorded_traffic("quat_scan_bwd_kernel", w.name),
+                     "algorithmic_bytes_per_launch": BWD_BYTES_PER_ELEMENT * E,
+                     "avg_launch_ms": bwd_avg},
+        "roofline_fwd": {"bound": "hbm", "kernel": "quat_scan_fwd_kernel", "achieved": fwd_gbs, "peak": peak,
+                         "unit": "GB/s", "frac": fwd_gbs / peak,
+                         "traffic": recorded_traffic("quat_scan_fwd_kernel", w.name),
+                         "algorithmic_bytes_per_launch": FWD_BYTES_PER_ELEMENT * E,
+                         "avg_launch_ms": fwd_avg},
+        "cpu_baseline": cpu,
+        "e2e": {"value": world * E / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "steps": e2e_steps},
+        "gpu_launches": launches[0],
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main(argv=None):
+    p = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", choices=sorted(workloads.WORKLOADS), default=DEFAULT_WORKLOAD)
+    p.add_argument("--e2e-steps", type=int, default=5)
+    p.add_argument("--cpu-seconds", type=float, default=10.0)
+    p.add_argument("--cpu-lanes", type=int, default=512)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    args = p.parse_args(argv)
+    if args.warmup < 3:
+        p.error("--warmup must be >= 3")
+    world, rank, local = dist_env()
+    if args.gpus != world and world > 1:
+        p.error(f"--gpus {args.gpus} does not match WORLD_SIZE {world}")
+    w = workloads.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, w, world, rank)
+    return run_ours(args, w, world, rank, local)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,136 @@
+/*
+ * quat_cumprod.h -- C ABI of the GB300 (sm_103a) quaternion cumulative-product
+ * scan and its recompute-based backward.
+ *
+ * The operation is the one defined in burn-mamba `mamba3/quat_scan/backward.rs`,
+ * module documentation, section "Gradient math":
+ *
+ *     cum[t] = q_t (x) cum[t-1],     cum[-1] = init            (forward)
+ *
+ * and, for a cotangent d_cum of cum, the vector-Jacobian product
+ *
+ *     G[t]   = d_cum[t] + conj(q_{t+1}) (x) G[t+1]               (reverse recurrence)
+ *     d_q[t] = G[t] (x) conj(cum[t-1])
+ *     d_init = conj(q_0) (x) G[0]   (= the page's S[0] for unit q_0)
+ *
+ * which for unit quaternions is the page's closed form with the prefix product
+ * P_t = q_t (x) ... (x) q_0 and the suffix sum S[t] = sum_{s>=t} conj(P_s) (x) d_cum[s].
+ * (x) is the Hamilton product (i^2 = j^2 = k^2 = ijk = -1); a quaternion is four
+ * floats [w, x, y, z].  As on the page, the backward takes only the leaves
+ * (q, init) and the cotangent: nothing is saved between forward and backward.
+ * The backward is exact for all quaternions, not only unit ones.
+ *
+ * Layout (all tensors): contiguous row-major fp32.
+ *   q, cum, d_cum, d_q : [B, S, H, J, 4]   element (b,s,h,j) at float offset
+ *                                          (((b*S + s)*H + h)*J + j)*4
+ *   init, d_init       : [B, H, J, 4]
+ * A "lane" is one (b, h, j); lanes are independent, the scan runs along s.
+ *
+ * Pointers: device pointers (cudaMalloc / torch CUDA memory) on the current
+ * device, owned by the caller, never freed or retained by the library, each
+ * aligned to 16 bytes.  Outputs must not overlap inputs.
+ *
+ * Streams: `stream` is a cudaStream_t (NULL = the legacy default stream).
+ * Every call is asynchronous: it validates arguments, enqueues its work on
+ * `stream` and returns.  Launch failures are returned at once; a failure that
+ * happens on the device (a cross-tile wait that ran out) is recorded in a
+ * per-stream device word and reported by quat_cumprod_status().
+ *
+ * Scratch memory: both calls use a library-owned workspace per (device,
+ * stream) for cross-tile carries and flags.  The first call on a stream, and
+ * any later call that needs a larger workspace, allocates it (cudaMalloc) and
+ * synchronizes that stream; issue such a call before capturing the stream
+ * into a CUDA graph.  Calls on one stream are ordered by the stream; calls on
+ * different streams use different workspaces and may run concurrently.
+ *
+ * Sizes: B, S, H, J >= 0.  Any zero size makes the call a no-op that returns
+ * QS_OK (except that quat_cumprod_bwd with S == 0 writes d_init = 0).
+ * Limits: S*H*J*16 < 2^40 bytes per batch entry, H*J*4 < 2^32, the number of
+ * work tiles below 2^31.
+ */
+#ifndef QUAT_CUMPROD_H
+#define QUAT_CUMPROD_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes returned by every entry point. */
+enum {
+    QS_OK = 0,
+    QS_ERR_NULL = -1,        /* a required pointer is NULL                      */
+    QS_ERR_DIMS = -2,        /* a size is negative or beyond the limits above   */
+    QS_ERR_MISALIGNED = -3,  /* a pointer is not 16-byte aligned                */
+    QS_ERR_ALIAS = -4,       /* an output overlaps an input                     */
+    QS_ERR_CUDA = -5,        /* a CUDA runtime call failed (launch, memset...)  */
+    QS_ERR_TIMEOUT = -6,     /* a cross-tile wait on the device ran out         */
+    QS_ERR_NOMEM = -7,       /* workspace allocation failed, or it would have to
+                                grow while the stream is being captured         */
+    QS_ERR_DEVICE = -8       /* the current device is not compute capability 10.3 */
+};
+
+/*
+ * Forward scan.  Reads q [B,S,H,J,4] and init [B,H,J,4]; writes
+ * cum [B,S,H,J,4] with cum[b,s,h,j] = q[b,s,h,j] (x) cum[b,s-1,h,j] and
+ * cum[b,-1,h,j] = init[b,h,j].
+ * Definition: burn-mamba `mamba3/quat_scan/backward.rs`, "Gradient math"
+ * (the scan), and `Mamba3QuatScanBackendExt::quat_cumprod(q_bshj4, init_bhj4)`.
+ */
+int quat_cumprod_fwd(const float *q, const float *init, float *cum,
+                     int64_t B, int64_t S, int64_t H, int64_t J, void *stream);
+
+/*
+ * Backward (vector-Jacobian product) of the forward scan, recomputed from the
+ * leaves.  Reads q, init and d_cum (the cotangent of cum, same shape as q);
+ * writes d_q [B,S,H,J,4] and d_init [B,H,J,4] as defined at the top of this
+ * file.  A cotangent of a "final carry" cum[:, S-1] must already be added
+ * into d_cum[:, S-1] by the caller, as the page's module documentation says.
+ * Definition: burn-mamba `mamba3/quat_scan/backward.rs`, "Gradient math"
+ * (VJP rule, reverse recurrence, closed form) and `quat_scan_backward`.
+ */
+int quat_cumprod_bwd(const float *q, const float *init, const float *d_cum,
+                     float *d_q, float *d_init,
+                     int64_t B, int64_t S, int64_t H, int64_t J, void *stream);
+
+/*
+ * Synchronizes `stream`, then returns QS_ERR_TIMEOUT if any call enqueued on it
+ * since the previous quat_cumprod_status() recorded a device-side timeout
+ * (its outputs are then invalid), QS_ERR_CUDA if the synchronization failed,
+ * and QS_OK otherwise.  Clears the recorded error.
+ */
+int quat_cumprod_status(void *stream);
+
+/* Static, human-readable description of a status code. */
+const char *quat_cumprod_strerror(int status);
+
+/*
+ * Test hooks.  quat_cumprod_debug_set_timeout_ns sets the limit of every
+ * cross-tile wait on the device (default 2 s; values <= 0 restore it).
+ * quat_cumprod_debug_stall_tile(k) makes work tile k of every later call skip
+ * publishing its carry (k < 0 disables), so that the tiles waiting on it run
+ * out their limit and the call reports QS_ERR_TIMEOUT instead of hanging.
+ * Both are process-wide settings; both return QS_OK.
+ */
+int quat_cumprod_debug_set_timeout_ns(int64_t ns);
+int quat_cumprod_debug_stall_tile(int64_t tile);
+
+/*
+ * Tuning / inspection hooks of the backward schedule.  The backward processes
+ * lanes in batches whose q fits the L2 cache between the batch's two passes;
+ * quat_cumprod_debug_set_batch_bytes sets the target q bytes per batch
+ * (default 24 MiB; <= 0 restores it; process-wide; returns QS_OK).
+ * quat_cumprod_debug_check_schedule verifies on the host, without a GPU, that
+ * the backward work-item order for these sizes visits every item once and
+ * puts every item after the items it waits on (QS_OK, QS_ERR_DIMS for sizes
+ * too large to check, or a negative code naming the violated property).
+ */
+int quat_cumprod_debug_set_batch_bytes(int64_t bytes);
+int quat_cumprod_debug_check_schedule(int64_t B, int64_t S, int64_t H, int64_t J);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QUAT_CUMPROD_H */

@@ -1,0 +1,177 @@
+"""Quaternion cumulative-product scan on GB300 (sm_103a).
+
+Thin ctypes binding over the C ABI in ``include/quat_cumprod.h`` (library
+``libquatscan.so`` next to this file).  The binding only checks and marshals
+arguments: every step of the scan runs in the library's CUDA kernels.  PyTorch
+provides device memory and the current stream.  There is no CPU fallback: if
+the library is missing or the device is not sm_103, calls raise.
+
+Operation (burn-mamba ``mamba3/quat_scan/backward.rs``, "Gradient math"):
+``cum[t] = q_t (x) cum[t-1]`` with ``cum[-1] = init`` over ``[B,S,H,J,4]``
+fp32 tensors, and its vector-Jacobian product ``(d_q, d_init)`` recomputed
+from ``(q, init, d_cum)``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+__all__ = [
+    "QS_OK", "QS_ERR_NULL", "QS_ERR_DIMS", "QS_ERR_MISALIGNED", "QS_ERR_ALIAS",
+    "QS_ERR_CUDA", "QS_ERR_TIMEOUT", "QS_ERR_NOMEM", "QS_ERR_DEVICE",
+    "QuatScanError", "library_path", "load_library", "quat_cumprod_fwd",
+    "quat_cumprod_bwd", "quat_cumprod_status", "quat_cumprod_strerror",
+]
+
+QS_OK = 0
+QS_ERR_NULL = -1
+QS_ERR_DIMS = -2
+QS_ERR_MISALIGNED = -3
+QS_ERR_ALIAS = -4
+QS_ERR_CUDA = -5
+QS_ERR_TIMEOUT = -6
+QS_ERR_NOMEM = -7
+QS_ERR_DEVICE = -8
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_NAME = "libquatscan.so"
+_lock = threading.Lock()
+_lib = None
+
+
+class QuatScanError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {quat_cumprod_strerror(status)} (status {status})")
+
+
+def library_path() -> str:
+    return os.path.join(_HERE, _LIB_NAME)
+
+
+def load_library():
+    """Loads ``libquatscan.so`` (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = library_path()
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"{path} is missing: build it with `python -c 'import __graft_entry__ as g; g.build()'` "
+                "(there is no CPU fallback)")
+        lib = ctypes.CDLL(path)
+        vp, i64 = ctypes.c_void_p, ctypes.c_int64
+        lib.quat_cumprod_fwd.argtypes = [vp, vp, vp, i64, i64, i64, i64, vp]
+        lib.quat_cumprod_fwd.restype = ctypes.c_int
+        lib.quat_cumprod_bwd.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, vp]
+        lib.quat_cumprod_bwd.restype = ctypes.c_int
+        lib.quat_cumprod_status.argtypes = [vp]
+        lib.quat_cumprod_status.restype = ctypes.c_int
+        lib.quat_cumprod_strerror.argtypes = [ctypes.c_int]
+        lib.quat_cumprod_strerror.restype = ctypes.c_char_p
+        lib.quat_cumprod_debug_set_timeout_ns.argtypes = [i64]
+        lib.quat_cumprod_debug_set_timeout_ns.restype = ctypes.c_int
+        lib.quat_cumprod_debug_stall_tile.argtypes = [i64]
+        lib.quat_cumprod_debug_stall_tile.restype = ctypes.c_int
+        _lib = lib
+        return lib
+
+
+def quat_cumprod_strerror(status: int) -> str:
+    return load_library().quat_cumprod_strerror(int(status)).decode()
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _stream_handle(stream, device):
+    torch = _torch()
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check_tensor(name, t, shape, device=None):
+    torch = _torch()
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != torch.float32:
+        raise TypeError(f"{name} must be float32, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (there is no CPU path)")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _dims(q, init):
+    if q.dim() != 5 or q.shape[-1] != 4:
+        raise ValueError(f"q must be [B,S,H,J,4], got {tuple(q.shape)}")
+    B, S, H, J, _ = q.shape
+    _check_tensor("q", q, (B, S, H, J, 4))
+    _check_tensor("init", init, (B, H, J, 4), q.device)
+    return B, S, H, J
+
+
+def quat_cumprod_fwd(q, init, cum=None, stream=None):
+    """cum[b,t,h,j] = q[b,t,h,j] (x) cum[b,t-1,h,j], cum[b,-1,h,j] = init[b,h,j].
+
+    ``q``: [B,S,H,J,4] float32 CUDA, ``init``: [B,H,J,4]; ``cum`` (optional
+    output) has the shape of ``q``.  Enqueued on ``stream`` (default: the
+    current torch stream).  Returns ``cum``.
+    """
+    torch = _torch()
+    B, S, H, J = _dims(q, init)
+    if cum is None:
+        cum = torch.empty_like(q)
+    else:
+        _check_tensor("cum", cum, q.shape, q.device)
+    with torch.cuda.device(q.device):
+        rc = load_library().quat_cumprod_fwd(
+            ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(init.data_ptr()),
+            ctypes.c_void_p(cum.data_ptr()), B, S, H, J, _stream_handle(stream, q.device))
+    if rc != QS_OK:
+        raise QuatScanError(rc, "quat_cumprod_fwd")
+    return cum
+
+
+def quat_cumprod_bwd(q, init, d_cum, d_q=None, d_init=None, stream=None):
+    """(d_q, d_init): vector-Jacobian product of the scan for the cotangent ``d_cum``.
+
+    Recomputed from the leaves ``q``, ``init`` (nothing is saved by the forward).
+    Returns ``(d_q, d_init)`` with the shapes of ``q`` and ``init``.
+    """
+    torch = _torch()
+    B, S, H, J = _dims(q, init)
+    _check_tensor("d_cum", d_cum, q.shape, q.device)
+    if d_q is None:
+        d_q = torch.empty_like(q)
+    else:
+        _check_tensor("d_q", d_q, q.shape, q.device)
+    if d_init is None:
+        d_init = torch.empty_like(init)
+    else:
+        _check_tensor("d_init", d_init, init.shape, q.device)
+    with torch.cuda.device(q.device):
+        rc = load_library().quat_cumprod_bwd(
+            ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(init.data_ptr()),
+            ctypes.c_void_p(d_cum.data_ptr()), ctypes.c_void_p(d_q.data_ptr()),
+            ctypes.c_void_p(d_init.data_ptr()), B, S, H, J, _stream_handle(stream, q.device))
+    if rc != QS_OK:
+        raise QuatScanError(rc, "quat_cumprod_bwd")
+    return d_q, d_init
+
+
+def quat_cumprod_status(stream=None, device=None):
+    """Synchronizes the stream and returns its recorded status (QS_OK or an error code)."""
+    torch = _torch()
+    device = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    with torch.cuda.device(device):
+        return load_library().quat_cumprod_status(_stream_handle(stream, device))

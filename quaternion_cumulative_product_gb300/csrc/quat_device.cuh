@@ -1,0 +1,119 @@
+// quat_device.cuh -- device-side building blocks of the quaternion scan:
+// Hamilton-product arithmetic on float4 and the sm_100-family PTX used by the
+// kernels (mbarrier, TMA tensor loads, acquire/release flags, global timer).
+//
+// Quaternion layout: float4 (x, y, z, w) holds [w, x, y, z] of the quaternion,
+// i.e. .x is the real part and .y/.z/.w are the i/j/k parts, matching the
+// [..., 4] = [w, x, y, z] memory layout of the tensors.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+
+namespace qs {
+
+// ---------------------------------------------------------------------------
+// Quaternion arithmetic (Hamilton convention, i^2 = j^2 = k^2 = ijk = -1).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float4 q_ident() { return make_float4(1.f, 0.f, 0.f, 0.f); }
+__device__ __forceinline__ float4 q_zero() { return make_float4(0.f, 0.f, 0.f, 0.f); }
+__device__ __forceinline__ float4 q_nan() {
+    const float n = __int_as_float(0x7fc00000);
+    return make_float4(n, n, n, n);
+}
+
+__device__ __forceinline__ float4 q_conj(const float4 a) { return make_float4(a.x, -a.y, -a.z, -a.w); }
+
+__device__ __forceinline__ float4 q_add(const float4 a, const float4 b) {
+    return make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
+}
+
+// a (x) b
+__device__ __forceinline__ float4 q_mul(const float4 a, const float4 b) {
+    float4 r;
+    r.x = a.x * b.x - a.y * b.y - a.z * b.z - a.w * b.w;
+    r.y = a.x * b.y + a.y * b.x + a.z * b.w - a.w * b.z;
+    r.z = a.x * b.z - a.y * b.w + a.z * b.x + a.w * b.y;
+    r.w = a.x * b.w + a.y * b.z - a.z * b.y + a.w * b.x;
+    return r;
+}
+
+// conj(a) (x) b  and  a (x) conj(b); the negations fold into the FMAs.
+__device__ __forceinline__ float4 q_mul_cl(const float4 a, const float4 b) { return q_mul(q_conj(a), b); }
+__device__ __forceinline__ float4 q_mul_cr(const float4 a, const float4 b) { return q_mul(a, q_conj(b)); }
+
+// ---------------------------------------------------------------------------
+// Shared-memory addresses, mbarriers and TMA.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// 3-D tiled TMA load of the box at (x, y, z) into shared memory; completion is
+// signalled on `bar` as transaction bytes.
+__device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, int x, int y, int z,
+                                            uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_addr(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// GPU-scope flags and the global timer.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long *p) {
+    unsigned long long v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_release_u64(unsigned long long *p, unsigned long long v) {
+    asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ uint32_t ld_volatile_u32(const unsigned int *p) {
+    return *reinterpret_cast<const volatile unsigned int *>(p);
+}
+
+__device__ __forceinline__ unsigned long long global_timer_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+}  // namespace qs

@@ -1,0 +1,173 @@
+"""Host-side tests of the C ABI (no GPU needed).
+
+The library must load and export every function ``include/*.h`` declares; the
+argument checks that run before any CUDA call must return the documented
+status codes; the backward work-item schedule must be valid (every item once,
+every wait on an earlier item) for the named workloads and for edge sizes.
+"""
+from __future__ import annotations
+
+import ctypes
+import glob
+import os
+import re
+import subprocess
+
+import pytest
+
+import quaternion_cumulative_product_gb300 as qs
+from quaternion_cumulative_product_gb300 import build as qbuild
+from quaternion_cumulative_product_gb300 import workloads
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    qbuild.build()
+    return qs.load_library()
+
+
+def _declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"^\s*(?:const\s+)?\w+\s*\*?\s*(quat_\w+)\s*\(", text, flags=re.M):
+            names.add(m.group(1))
+    return names
+
+
+def test_header_declares_the_boundary():
+    names = _declared_functions()
+    for required in ("quat_cumprod_fwd", "quat_cumprod_bwd", "quat_cumprod_status",
+                     "quat_cumprod_strerror"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", qs.library_path()],
+                         capture_output=True, text=True, check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
+    missing = _declared_functions() - exported
+    assert not missing, f"declared but not exported: {sorted(missing)}"
+    for name in _declared_functions():
+        assert hasattr(lib, name)
+
+
+def test_strerror_covers_all_codes(lib):
+    seen = set()
+    for code in (qs.QS_OK, qs.QS_ERR_NULL, qs.QS_ERR_DIMS, qs.QS_ERR_MISALIGNED, qs.QS_ERR_ALIAS,
+                 qs.QS_ERR_CUDA, qs.QS_ERR_TIMEOUT, qs.QS_ERR_NOMEM, qs.QS_ERR_DEVICE):
+        msg = qs.quat_cumprod_strerror(code)
+        assert msg and msg != "unknown status"
+        seen.add(msg)
+    assert len(seen) == 9
+    assert qs.quat_cumprod_strerror(12345) == "unknown status"
+
+
+def _p(addr):
+    return ctypes.c_void_p(addr)
+
+
+def test_fwd_argument_checks_before_any_cuda_call(lib):
+    A, Bp, Cp = 0x10000, 0x20000000, 0x40000000
+    # negative sizes
+    assert lib.quat_cumprod_fwd(_p(A), _p(Bp), _p(Cp), -1, 4, 1, 1, None) == qs.QS_ERR_DIMS
+    assert lib.quat_cumprod_fwd(_p(A), _p(Bp), _p(Cp), 1, -4, 1, 1, None) == qs.QS_ERR_DIMS
+    # sizes beyond the limits
+    assert lib.quat_cumprod_fwd(_p(A), _p(Bp), _p(Cp), 1, 1 << 32, 1, 1, None) == qs.QS_ERR_DIMS
+    assert lib.quat_cumprod_fwd(_p(A), _p(Bp), _p(Cp), 1, 1 << 20, 1 << 12, 1 << 10, None) == qs.QS_ERR_DIMS
+    # empty problems are no-ops (NULL pointers allowed)
+    for dims in [(0, 4, 1, 1), (1, 0, 1, 1), (1, 4, 0, 1), (1, 4, 1, 0)]:
+        assert lib.quat_cumprod_fwd(None, None, None, *dims, None) == qs.QS_OK
+    # NULL pointers
+    assert lib.quat_cumprod_fwd(None, _p(Bp), _p(Cp), 1, 4, 1, 1, None) == qs.QS_ERR_NULL
+    assert lib.quat_cumprod_fwd(_p(A), None, _p(Cp), 1, 4, 1, 1, None) == qs.QS_ERR_NULL
+    assert lib.quat_cumprod_fwd(_p(A), _p(Bp), None, 1, 4, 1, 1, None) == qs.QS_ERR_NULL
+    # 16-byte alignment
+    assert lib.quat_cumprod_fwd(_p(A + 4), _p(Bp), _p(Cp), 1, 4, 1, 1, None) == qs.QS_ERR_MISALIGNED
+    assert lib.quat_cumprod_fwd(_p(A), _p(Bp + 8), _p(Cp), 1, 4, 1, 1, None) == qs.QS_ERR_MISALIGNED
+    assert lib.quat_cumprod_fwd(_p(A), _p(Bp), _p(Cp + 12), 1, 4, 1, 1, None) == qs.QS_ERR_MISALIGNED
+    # outputs overlapping inputs (q is 1*4*1*1*16 = 64 bytes)
+    assert lib.quat_cumprod_fwd(_p(A), _p(Bp), _p(A + 48), 1, 4, 1, 1, None) == qs.QS_ERR_ALIAS
+    assert lib.quat_cumprod_fwd(_p(A), _p(Bp), _p(Bp - 48), 1, 4, 1, 1, None) == qs.QS_ERR_ALIAS
+    # adjacent but not overlapping is not aliasing: the call then goes on to
+    # the device (not exercised here)
+
+
+def test_bwd_argument_checks_before_any_cuda_call(lib):
+    q, i, d, gq, gi = 0x10000, 0x20000, 0x30000, 0x40000, 0x50000
+    f = lib.quat_cumprod_bwd
+    assert f(_p(q), _p(i), _p(d), _p(gq), _p(gi), 1, -1, 1, 1, None) == qs.QS_ERR_DIMS
+    assert f(None, None, None, None, None, 0, 5, 2, 2, None) == qs.QS_OK
+    assert f(None, None, None, None, None, 2, 5, 0, 2, None) == qs.QS_OK
+    # S == 0 with lanes: d_init must be written -> needs a valid pointer
+    assert f(None, None, None, None, None, 2, 0, 2, 2, None) == qs.QS_ERR_NULL
+    assert f(None, None, None, None, _p(gi + 4), 2, 0, 2, 2, None) == qs.QS_ERR_MISALIGNED
+    for k in range(5):
+        ptrs = [_p(q), _p(i), _p(d), _p(gq), _p(gi)]
+        ptrs[k] = None
+        assert f(*ptrs, 1, 4, 1, 1, None) == qs.QS_ERR_NULL
+        ptrs = [_p(q), _p(i), _p(d), _p(gq), _p(gi)]
+        ptrs[k] = _p([q, i, d, gq, gi][k] + 4)
+        assert f(*ptrs, 1, 4, 1, 1, None) == qs.QS_ERR_MISALIGNED
+    # q/d_cum/d_q are 64 bytes, init/d_init 16 bytes
+    assert f(_p(q), _p(i), _p(d), _p(q + 16), _p(gi), 1, 4, 1, 1, None) == qs.QS_ERR_ALIAS
+    assert f(_p(q), _p(i), _p(d), _p(d), _p(gi), 1, 4, 1, 1, None) == qs.QS_ERR_ALIAS
+    assert f(_p(q), _p(i), _p(d), _p(gq), _p(i), 1, 4, 1, 1, None) == qs.QS_ERR_ALIAS
+    assert f(_p(q), _p(i), _p(d), _p(gq), _p(gq + 32), 1, 4, 1, 1, None) == qs.QS_ERR_ALIAS
+
+
+def test_debug_hooks_return_ok(lib):
+    assert lib.quat_cumprod_debug_set_timeout_ns(1000) == qs.QS_OK
+    assert lib.quat_cumprod_debug_set_timeout_ns(0) == qs.QS_OK
+    assert lib.quat_cumprod_debug_stall_tile(3) == qs.QS_OK
+    assert lib.quat_cumprod_debug_stall_tile(-1) == qs.QS_OK
+    lib.quat_cumprod_debug_set_batch_bytes.argtypes = [ctypes.c_int64]
+    assert lib.quat_cumprod_debug_set_batch_bytes(1 << 20) == qs.QS_OK
+    assert lib.quat_cumprod_debug_set_batch_bytes(0) == qs.QS_OK
+
+
+def _check_schedule(lib, B, S, H, J):
+    f = lib.quat_cumprod_debug_check_schedule
+    f.argtypes = [ctypes.c_int64] * 4
+    f.restype = ctypes.c_int
+    return f(B, S, H, J)
+
+
+@pytest.mark.parametrize("name", ["tiny", "small", "mamba3", "large", "long"])
+def test_backward_schedule_named_workloads(lib, name):
+    w = workloads.WORKLOADS[name]
+    assert _check_schedule(lib, w.B, w.S, w.H, w.J) == qs.QS_OK
+
+
+@pytest.mark.parametrize("batch_bytes", [1, 1 << 16, 1 << 20, 0])
+@pytest.mark.parametrize("dims", [(1, 1, 1, 1), (1, 33, 1, 1), (3, 100, 5, 8), (2, 31, 40, 1),
+                                  (7, 257, 3, 11), (1, 4096, 16, 16), (5, 64, 64, 2)])
+def test_backward_schedule_edge_sizes(lib, dims, batch_bytes):
+    lib.quat_cumprod_debug_set_batch_bytes.argtypes = [ctypes.c_int64]
+    lib.quat_cumprod_debug_set_batch_bytes(batch_bytes)
+    try:
+        assert _check_schedule(lib, *dims) == qs.QS_OK
+    finally:
+        lib.quat_cumprod_debug_set_batch_bytes(0)
+
+
+def test_workload_generator_is_seeded_and_shaped():
+    w = workloads.WORKLOADS["tiny"]
+    a = workloads.make_inputs(w)
+    b = workloads.make_inputs(w)
+    for x, y in zip(a, b):
+        assert x.dtype.name == "float32" and (x == y).all()
+    q, init, d_cum = a
+    assert q.shape == (1, 64, 2, 4, 4) and init.shape == (1, 2, 4, 4) and d_cum.shape == q.shape
+    import numpy as np
+    assert np.allclose(np.linalg.norm(q, axis=-1), 1, atol=1e-6)
+    w3 = workloads.custom("c", 2, 10, 1, 3, q_kind="rotation", theta_max=0.1, init_kind="identity")
+    q3, i3, _ = workloads.make_inputs(w3)
+    assert np.all(q3[..., 0] >= np.cos(0.05) - 1e-6) and np.all(i3[..., 0] == 1)
+    lanes = [0, 4, 5]
+    sq, si, sd = workloads.sample_lanes(a, lanes, 2, 4)
+    assert sq.shape == (1, 64, 3, 1, 4) and si.shape == (1, 3, 1, 4)
+    assert (sq[0, :, 1, 0] == q[0, :, 1, 0]).all() and (si[0, 2, 0] == init[0, 1, 1]).all()

@@ -1,0 +1,259 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle.
+
+Tolerance: for every output tensor, the normwise relative error
+``max_i |gpu_i - ref_i| / max_i |ref_i|`` must be <= 1e-4 (fp32 I/O and fp32
+arithmetic against the exact-input fp64 oracle).  Workloads are the seeded
+synthetic ones of ``workloads.py``; the two largest are run at full size in the
+benchmark's launch configuration and compared on whole sampled lanes (lanes
+are independent, so the oracle on a lane subset is exact).
+"""
+from __future__ import annotations
+
+import ctypes
+
+import numpy as np
+import pytest
+
+import oracle
+import quaternion_cumulative_product_gb300 as qs
+from quaternion_cumulative_product_gb300 import workloads
+
+torch = pytest.importorskip("torch")
+
+pytestmark = pytest.mark.gpu
+
+TOL = 1e-4
+
+
+@pytest.fixture(scope="module")
+def dev():
+    if not torch.cuda.is_available():
+        pytest.fail("CUDA device required for -m gpu tests")
+    qs.load_library()
+    return torch.device("cuda", 0)
+
+
+@pytest.fixture(autouse=True)
+def reset_hooks():
+    lib = qs.load_library()
+    yield
+    lib.quat_cumprod_debug_set_timeout_ns(0)
+    lib.quat_cumprod_debug_stall_tile(-1)
+    lib.quat_cumprod_debug_set_batch_bytes.argtypes = [ctypes.c_int64]
+    lib.quat_cumprod_debug_set_batch_bytes(0)
+
+
+def normwise(got, ref):
+    scale = float(np.abs(ref).max()) if ref.size else 0.0
+    return float(np.abs(got.astype(np.float64) - ref).max()) / (scale if scale > 0 else 1.0) if ref.size else 0.0
+
+
+def run_gpu(dev, q, init, d_cum, stream=None):
+    tq, ti, td = (torch.from_numpy(np.ascontiguousarray(a)).to(dev) for a in (q, init, d_cum))
+    cum = qs.quat_cumprod_fwd(tq, ti, stream=stream)
+    d_q, d_init = qs.quat_cumprod_bwd(tq, ti, td, stream=stream)
+    st = qs.quat_cumprod_status(stream=stream, device=dev)
+    assert st == qs.QS_OK, qs.quat_cumprod_strerror(st)
+    return cum.cpu().numpy(), d_q.cpu().numpy(), d_init.cpu().numpy()
+
+
+def assert_parity(got, ref, what):
+    err = normwise(got, ref)
+    assert err <= TOL, f"{what}: normwise relative error {err:.3e} > {TOL}"
+    return err
+
+
+def check_against_oracle(dev, q, init, d_cum, stream=None):
+    cum, d_q, d_init = run_gpu(dev, q, init, d_cum, stream)
+    ref_cum = oracle.fwd(q, init)
+    ref_dq, ref_di = oracle.bwd(q, init, d_cum)
+    return (assert_parity(cum, ref_cum, "cum"), assert_parity(d_q, ref_dq, "d_q"),
+            assert_parity(d_init, ref_di, "d_init"))
+
+
+# ---------------------------------------------------------------------------
+# Named workloads.
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("name", ["tiny", "small", "mamba3"])
+def test_named_workload_full_parity(dev, name):
+    w = workloads.WORKLOADS[name]
+    check_against_oracle(dev, *workloads.make_inputs(w))
+
+
+def _sampled_lane_parity(dev, w, nlanes, seed):
+    q, init, d_cum = workloads.make_inputs(w)
+    tq, ti, td = (torch.from_numpy(a).to(dev) for a in (q, init, d_cum))
+    cum = qs.quat_cumprod_fwd(tq, ti)
+    d_q, d_init = qs.quat_cumprod_bwd(tq, ti, td)
+    assert qs.quat_cumprod_status(device=dev) == qs.QS_OK
+    rng = np.random.default_rng(seed)
+    HJ = w.H * w.J
+    lanes = np.unique(np.concatenate([[0, 31, 32, HJ - 1, w.lanes - 1],
+                                      rng.choice(w.lanes, nlanes, replace=False)]))
+    b = torch.from_numpy(lanes // HJ).to(dev)
+    hj = torch.from_numpy(lanes % HJ).to(dev)
+    g_cum = cum.view(w.B, w.S, HJ, 4)[b, :, hj].cpu().numpy()        # [n, S, 4]
+    g_dq = d_q.view(w.B, w.S, HJ, 4)[b, :, hj].cpu().numpy()
+    g_di = d_init.view(w.B, HJ, 4)[b, hj].cpu().numpy()
+    del cum, d_q, d_init, tq, td
+    sq, si, sd = workloads.sample_lanes((q, init, d_cum), lanes, w.H, w.J)
+    ref_cum = oracle.fwd(sq, si)[0, :, :, 0].transpose(1, 0, 2)
+    ref_dq, ref_di = oracle.bwd(sq, si, sd)
+    assert_parity(g_cum, ref_cum, "cum (sampled lanes)")
+    assert_parity(g_dq, ref_dq[0, :, :, 0].transpose(1, 0, 2), "d_q (sampled lanes)")
+    assert_parity(g_di, ref_di[0, :, 0], "d_init (sampled lanes)")
+
+
+def test_large_full_size_sampled_lanes(dev):
+    _sampled_lane_parity(dev, workloads.WORKLOADS["large"], 48, 5)
+
+
+def test_long_sequence_full_size(dev):
+    w = workloads.WORKLOADS["long"]
+    _sampled_lane_parity(dev, w, 60, 6)
+
+
+def test_mamba3_full_size_sampled_lanes(dev):
+    _sampled_lane_parity(dev, workloads.WORKLOADS["mamba3"], 64, 7)
+
+
+# ---------------------------------------------------------------------------
+# Edge shapes: ragged sequence tails, lane counts that are not multiples of
+# 32 (partial lane groups, groups of several batch entries), S < tile, S = 1.
+# ---------------------------------------------------------------------------
+EDGE = [(1, 1, 1, 1), (1, 2, 1, 1), (2, 33, 1, 1), (1, 100, 2, 3), (3, 257, 5, 8),
+        (2, 31, 40, 1), (1, 64, 4, 8), (2, 500, 1, 32), (1, 1000, 3, 17), (4, 65, 2, 16),
+        (1, 4099, 1, 33), (2, 129, 8, 8)]
+
+
+@pytest.mark.parametrize("dims", EDGE)
+def test_edge_shapes(dev, dims):
+    B, S, H, J = dims
+    w = workloads.custom("edge", B, S, H, J, seed=sum(dims))
+    check_against_oracle(dev, *workloads.make_inputs(w))
+
+
+def test_non_unit_quaternions(dev):
+    """The backward is exact for all quaternions (no unit assumption)."""
+    rng = np.random.default_rng(3)
+    B, S, H, J = 2, 700, 2, 20
+    q = rng.standard_normal((B, S, H, J, 4))
+    q /= np.linalg.norm(q, axis=-1, keepdims=True)
+    q *= rng.uniform(0.995, 1.005, (B, S, H, J, 1))
+    init = (rng.standard_normal((B, H, J, 4)) * 2).astype(np.float32)
+    d_cum = rng.standard_normal((B, S, H, J, 4)).astype(np.float32)
+    check_against_oracle(dev, q.astype(np.float32), init, d_cum)
+    # strongly non-unit on a short sequence
+    q2 = (rng.standard_normal((1, 24, 3, 7, 4)) * 1.5).astype(np.float32)
+    check_against_oracle(dev, q2, init[:1, :3, :7].copy(), rng.standard_normal(q2.shape).astype(np.float32))
+
+
+def test_identity_q_is_reverse_cumsum(dev):
+    rng = np.random.default_rng(4)
+    B, S, H, J = 2, 300, 1, 40
+    q = np.zeros((B, S, H, J, 4), np.float32)
+    q[..., 0] = 1
+    init = rng.standard_normal((B, H, J, 4)).astype(np.float32)
+    d_cum = rng.standard_normal((B, S, H, J, 4)).astype(np.float32)
+    cum, d_q, d_init = run_gpu(dev, q, init, d_cum)
+    np.testing.assert_array_equal(cum, np.broadcast_to(init[:, None], cum.shape))
+    G = np.flip(np.cumsum(np.flip(d_cum.astype(np.float64), 1), 1), 1)
+    assert_parity(d_init, G[:, 0], "d_init")
+
+
+def test_empty_sizes(dev):
+    z = torch.zeros(0, device=dev)
+    for B, S, H, J in [(0, 5, 2, 2), (2, 5, 0, 2), (2, 5, 2, 0)]:
+        q = torch.zeros(B, S, H, J, 4, device=dev)
+        init = torch.zeros(B, H, J, 4, device=dev)
+        assert qs.quat_cumprod_fwd(q, init).shape == q.shape
+        gq, gi = qs.quat_cumprod_bwd(q, init, q)
+        assert gq.shape == q.shape and gi.shape == init.shape
+    q = torch.zeros(3, 0, 2, 2, 4, device=dev)
+    init = torch.randn(3, 2, 2, 4, device=dev)
+    gi = torch.full_like(init, 7.0)
+    qs.quat_cumprod_bwd(q, init, q, d_init=gi)
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(gi).item() == 0
+    del z
+
+
+@pytest.mark.parametrize("batch_bytes", [1, 1 << 20])
+def test_backward_many_batches(dev, batch_bytes):
+    """Small batches exercise the interleaved A/C schedule with many batches."""
+    lib = qs.load_library()
+    lib.quat_cumprod_debug_set_batch_bytes.argtypes = [ctypes.c_int64]
+    lib.quat_cumprod_debug_set_batch_bytes(batch_bytes)
+    w = workloads.custom("batches", 3, 1500, 4, 24, q_kind="rotation", theta_max=0.4, seed=9)
+    check_against_oracle(dev, *workloads.make_inputs(w))
+
+
+def test_repeated_calls_and_side_stream(dev):
+    w = workloads.WORKLOADS["small"]
+    q, init, d_cum = workloads.make_inputs(w)
+    s = torch.cuda.Stream(device=dev)
+    for _ in range(3):
+        check_against_oracle(dev, q, init, d_cum)
+    with torch.cuda.stream(s):
+        check_against_oracle(dev, q, init, d_cum, stream=s)
+
+
+def test_unaligned_base_views(dev):
+    """Tensors that start 16 bytes into an allocation (TMA base alignment is 16 B)."""
+    w = workloads.custom("view", 2, 77, 3, 5, seed=12)
+    q, init, d_cum = workloads.make_inputs(w)
+    n = q.size
+    big = torch.zeros(n + 4, device=dev)
+    big[4:] = torch.from_numpy(q.ravel()).to(dev)
+    tq = big[4:].view(q.shape)
+    ti = torch.from_numpy(init).to(dev)
+    bigd = torch.zeros(n + 8, device=dev)
+    bigd[8:] = torch.from_numpy(d_cum.ravel()).to(dev)
+    td = bigd[8:].view(q.shape)
+    cum = qs.quat_cumprod_fwd(tq, ti)
+    d_q, d_init = qs.quat_cumprod_bwd(tq, ti, td)
+    assert qs.quat_cumprod_status(device=dev) == qs.QS_OK
+    assert_parity(cum.cpu().numpy(), oracle.fwd(q, init), "cum")
+    rq, ri = oracle.bwd(q, init, d_cum)
+    assert_parity(d_q.cpu().numpy(), rq, "d_q")
+    assert_parity(d_init.cpu().numpy(), ri, "d_init")
+
+
+def test_binding_rejects_bad_tensors(dev):
+    q = torch.zeros(1, 4, 1, 1, 4, device=dev)
+    init = torch.zeros(1, 1, 1, 4, device=dev)
+    with pytest.raises(TypeError):
+        qs.quat_cumprod_fwd(q.double(), init)
+    with pytest.raises(ValueError):
+        qs.quat_cumprod_fwd(q.cpu(), init)
+    with pytest.raises(ValueError):
+        qs.quat_cumprod_fwd(q, init[:, :, :, :3])
+    with pytest.raises(ValueError):
+        qs.quat_cumprod_fwd(torch.zeros(1, 4, 1, 2, 4, device=dev)[:, :, :, :1], init)
+    with pytest.raises(qs.QuatScanError) as ei:
+        qs.quat_cumprod_fwd(q, init, cum=q)
+    assert ei.value.status == qs.QS_ERR_ALIAS
+
+
+# ---------------------------------------------------------------------------
+# Failure detection: a tile that never publishes makes its dependents' bounded
+# waits run out; the call reports QS_ERR_TIMEOUT and the next call is clean.
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("which", ["fwd", "bwd"])
+def test_stalled_tile_reports_timeout_then_recovers(dev, which):
+    lib = qs.load_library()
+    w = workloads.custom("stall", 2, 600, 2, 16, seed=21)
+    q, init, d_cum = workloads.make_inputs(w)
+    tq, ti, td = (torch.from_numpy(a).to(dev) for a in (q, init, d_cum))
+    assert qs.quat_cumprod_status(device=dev) == qs.QS_OK
+    lib.quat_cumprod_debug_set_timeout_ns(50_000_000)    # 50 ms
+    lib.quat_cumprod_debug_stall_tile(0)
+    if which == "fwd":
+        qs.quat_cumprod_fwd(tq, ti)
+    else:
+        qs.quat_cumprod_bwd(tq, ti, td)
+    assert qs.quat_cumprod_status(device=dev) == qs.QS_ERR_TIMEOUT
+    assert qs.quat_cumprod_status(device=dev) == qs.QS_OK   # cleared
+    lib.quat_cumprod_debug_stall_tile(-1)
+    lib.quat_cumprod_debug_set_timeout_ns(0)
+    check_against_oracle(dev, q, init, d_cum)
