@@ -37,7 +37,8 @@
  * per-stream device word and reported by quat_cumprod_status().
  *
  * Scratch memory: both calls use a library-owned workspace per (device,
- * stream) for cross-tile carries and flags.  The first call on a stream, and
+ * stream) for per-chunk aggregates, carries and flags (about 32 bytes (forward)
+ * or 64 bytes (backward) per lane and chunk of 32 steps).  The first call on a stream, and
  * any later call that needs a larger workspace, allocates it (cudaMalloc) and
  * synchronizes that stream; issue such a call before capturing the stream
  * into a CUDA graph.  Calls on one stream are ordered by the stream; calls on
@@ -108,8 +109,8 @@ const char *quat_cumprod_strerror(int status);
 /*
  * Test hooks.  quat_cumprod_debug_set_timeout_ns sets the limit of every
  * cross-tile wait on the device (default 2 s; values <= 0 restore it).
- * quat_cumprod_debug_stall_tile(k) makes work tile k of every later call skip
- * publishing its carry (k < 0 disables), so that the tiles waiting on it run
+ * quat_cumprod_debug_stall_tile(k) makes work item k of every later call skip
+ * publishing its result (k < 0 disables), so that the items waiting on it run
  * out their limit and the call reports QS_ERR_TIMEOUT instead of hanging.
  * Both are process-wide settings; both return QS_OK.
  */
@@ -117,16 +118,20 @@ int quat_cumprod_debug_set_timeout_ns(int64_t ns);
 int quat_cumprod_debug_stall_tile(int64_t tile);
 
 /*
- * Tuning / inspection hooks of the backward schedule.  The backward processes
- * lanes in batches whose q fits the L2 cache between the batch's two passes;
- * quat_cumprod_debug_set_batch_bytes sets the target q bytes per batch
- * (default 24 MiB; <= 0 restores it; process-wide; returns QS_OK).
- * quat_cumprod_debug_check_schedule verifies on the host, without a GPU, that
- * the backward work-item order for these sizes visits every item once and
- * puts every item after the items it waits on (QS_OK, QS_ERR_DIMS for sizes
- * too large to check, or a negative code naming the violated property).
+ * Tuning / inspection hooks.  Both directions process lane groups in batches
+ * whose inputs fit the L2 cache between the two passes over a batch;
+ * quat_cumprod_debug_set_batch_bytes sets the target input bytes per batch
+ * (default 24 MiB; <= 0 restores it).  quat_cumprod_debug_set_variant selects
+ * a compiled tile configuration (index into the library's variant table, -1 =
+ * automatic; QS_ERR_DIMS for an unknown index).  Both are process-wide and
+ * return QS_OK.  quat_cumprod_debug_check_schedule verifies on the host,
+ * without a GPU, that the work-item order of both directions for these sizes
+ * visits every item once and puts every item after the items it waits on
+ * (QS_OK, QS_ERR_DIMS for sizes too large to check, or a negative code naming
+ * the violated property).
  */
 int quat_cumprod_debug_set_batch_bytes(int64_t bytes);
+int quat_cumprod_debug_set_variant(int fwd_variant, int bwd_variant);
 int quat_cumprod_debug_check_schedule(int64_t B, int64_t S, int64_t H, int64_t J);
 
 #ifdef __cplusplus

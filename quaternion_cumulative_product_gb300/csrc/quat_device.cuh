@@ -1,6 +1,7 @@
 // quat_device.cuh -- device-side building blocks of the quaternion scan:
 // Hamilton-product arithmetic on float4 and the sm_100-family PTX used by the
-// kernels (mbarrier, TMA tensor loads, acquire/release flags, global timer).
+// kernels (mbarrier, TMA tensor loads and stores, bulk async-groups,
+// acquire/release flags, global timer).
 //
 // Quaternion layout: float4 (x, y, z, w) holds [w, x, y, z] of the quaternion,
 // i.e. .x is the real part and .y/.z/.w are the i/j/k parts, matching the
@@ -88,6 +89,27 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, i
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_addr(bar))
         : "memory");
 }
+
+// 3-D tiled TMA store of a shared-memory box to (x, y, z); out-of-range parts
+// of the box are not written.  Completion is tracked by bulk async-groups.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, const void *src, int x, int y, int z) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
+            reinterpret_cast<uint64_t>(map)),
+        "r"(x), "r"(y), "r"(z), "r"(smem_addr(src))
+        : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+// Waits until at most N of this thread's bulk groups are still reading shared memory.
+template <int N>
+__device__ __forceinline__ void bulk_wait_group_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+
+// Waits until all of this thread's bulk groups have completed.
+__device__ __forceinline__ void bulk_wait_group_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");

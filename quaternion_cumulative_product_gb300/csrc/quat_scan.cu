@@ -9,40 +9,43 @@
 //
 // Design (one GPU, HBM-bound; no tensor cores -- there is no dense contraction):
 //
-//  * A tile is LT = 32 lanes x T consecutive steps.  Its rows (one step, 32
-//    lanes = 512 contiguous bytes) are staged into shared memory by one 3-D TMA
-//    load per operand, double/triple buffered in a persistent CTA that claims
-//    tiles from a global counter.  Inside the tile, thread (seg, lane) owns N
-//    consecutive steps of one lane; 8 segments per tile.
+//  * Tile = LT lanes x T consecutive steps of one lane group (LT lanes of one
+//    batch entry, contiguous in memory).  One 3-D TMA load stages a tile (one
+//    per operand) into shared memory; thread (seg, lane) owns N consecutive
+//    steps of one lane, NSEG = 256 / LT segments per tile.
 //
-//  * Forward: per-thread sequential products give the segment-local prefixes,
-//    warp 0 scans the 8 segment aggregates, and a decoupled look-back over the
-//    tiles of the same lane group (earlier chunks) gives the carry cum[t0-1].
-//    Tile aggregate = L_c = local product of the chunk; inclusive value =
-//    cum at the chunk's last step.  Output cum[t] = local_t (x) carry.
+//  * Chunk aggregates (the page's factorisation):
+//      L_c = q_{t1-1} (x) ... (x) q_{t0}                      (chunk product)
+//      W_c = sum_{s in c} conj(local_s) (x) d_cum[s]          (backward only)
+//    with local_s = q_s (x) ... (x) q_{t0}.  With H[t] = conj(q_t) (x) G[t]
+//    (the cotangent step t hands to cum[t-1]), a chunk maps the H entering
+//    from its right end to the H at its first step by
+//      H_c = W_c + conj(L_c) (x) H_{c+1},
+//    which is the page's suffix-sum factorisation
+//    conj(P_s) = conj(P_{c-1}) (x) conj(local_s), and composes the literal
+//    reverse recurrence, so it is exact for all quaternions.  d_init = H_0.
+//    The forward carry into chunk c is F_c = cum[t0-1] = L_{c-1} (x) F_{c-1},
+//    F_0 = init.
 //
-//  * Backward: the page's per-chunk aggregates are the chunk product L_c and the
-//    weighted sum W_c = sum_{s in c} conj(local_s) (x) d_cum[s].  Writing
-//    H[t] = conj(q_t) (x) G[t] (the cotangent that step t hands to cum[t-1]),
-//    a chunk maps the H entering at its end to the H at its start by the affine
-//    map  H_c = W_c + conj(L_c) (x) H_{c+1}.  This is exactly the page's
-//    factorisation conj(P_s) = conj(P_{c-1}) (x) conj(local_s) of the suffix
-//    sum, and it is exact for all quaternions (no unit assumption), because it
-//    composes the literal reverse recurrence.  d_init = H_0.
-//    d_q needs both directions: the forward carry cum[t0-1] (from earlier
-//    chunks) and H_{c+1} (from later chunks).  One persistent kernel runs two
-//    kinds of work items from one queue: "A" items (read q only, forward
-//    look-back, publish cum at each chunk end) and "C" items (read q and d_cum,
-//    reverse look-back over the affine aggregates, wait for the A carry of the
-//    previous chunk, write d_q).  Lanes are processed in batches small enough
-//    that a batch's q stays in L2 between its A pass and its C pass; the queue
-//    runs A(0), A(1), C(0), A(2), C(1), ...  Every wait is on an item claimed
-//    earlier from the queue, so the schedule cannot deadlock; every wait is also
-//    bounded in time and reports QS_ERR_TIMEOUT instead of hanging.
+//  * One persistent kernel per direction runs three kinds of work items from
+//    one queue (no look-back chains):
+//      P1 (chunk, group): read the tile, publish L_c (and W_c);
+//      SC (group):        once all P1 items of the group are published, scan
+//                         its chunk aggregates (8-16 threads per lane) into the
+//                         carries F_c (and H_{c+1}, and d_init);
+//      P3 (chunk, group): read the tile again, apply the carries, write cum (or
+//                         d_q) into shared memory and store it with one TMA store.
+//    Lane groups are processed in batches whose inputs fit the L2 cache; the
+//    queue runs P1(0) SC(0) | P1(1) SC(1) P3(0) | P1(2) SC(2) P3(1) | ... so
+//    the P3 pass of a batch re-reads its tiles from L2: DRAM traffic stays
+//    near the minimum (32 B per element forward, 48 B backward).
+//    Every wait is on an item claimed earlier from the queue (no deadlock);
+//    every wait is bounded in time and reports QS_ERR_TIMEOUT instead of hanging.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cstddef>
 #include <cstdint>
 #include <cstring>
 #include <map>
@@ -55,11 +58,7 @@
 
 namespace qs {
 
-constexpr int LT = 32;                 // lanes per tile (= warp width)
 constexpr int NTHREADS = 256;          // threads per CTA
-constexpr int NSEG = NTHREADS / LT;    // sequence segments per tile
-constexpr uint32_t ST_AGG = 1;         // flag: tile aggregate published
-constexpr uint32_t ST_INCL = 2;        // flag: inclusive carry published
 
 // Per-workspace control block (device memory, zero-initialised, epoch = 1).
 struct __align__(256) WsHeader {
@@ -89,23 +88,111 @@ struct Control {
     unsigned long long timeout_ns;
 };
 
-struct BwdArrays {
-    unsigned long long *a_flags;  // [CA*NG]
-    float4 *a_agg;                // [CA*NG*LT]   chunk product L_c
-    float4 *a_incl;               // [CA*NG*LT]   cum at the chunk's last step
-    unsigned long long *c_flags;  // [C*NG]
-    float4 *c_agg;                // [C*NG*LT*2]  affine map (conj(L_c), W_c)
-    float4 *c_incl;               // [C*NG*LT]    H at the chunk's first step
+struct Arrays {
+    unsigned long long *p1_flags;   // [C*NG]   P1 item published
+    unsigned long long *sc_flags;   // [NG]     SC item published
+    float4 *aggL;                   // [C*NG*LT] chunk product L_c
+    float4 *aggW;                   // [C*NG*LT] chunk weighted sum W_c (backward)
+    float4 *carF;                   // [C*NG*LT] forward carry cum[t0-1]
+    float4 *carH;                   // [C*NG*LT] H entering the chunk from the right (backward)
 };
 
+// Batches of lane groups: batch k holds groups [k*GB, k*GB + gk).
 struct Schedule {
-    int CA;   // chunks with an A item (C - 1)
     int GB;   // lane groups per batch
     int NB;   // batches
 };
 
-__device__ __forceinline__ unsigned long long pack_flag(uint32_t epoch, uint32_t st) {
-    return (static_cast<unsigned long long>(epoch) << 2) | st;
+enum : int { KIND_P1 = 0, KIND_SC = 1, KIND_P3 = 2 };
+
+struct Work {
+    int kind;
+    int chunk;   // P1/P3
+    int g;       // lane group
+};
+
+// Queue order: block 0 = P1(0) SC(0); block k (1..NB-1) = P1(k) SC(k) P3(k-1);
+// block NB = P3(NB-1).  Inside P1/P3 of a batch: chunk-major (all groups of
+// the batch at chunk c, then chunk c+1).
+__host__ __device__ inline Work decode_item(int id, int NG, int C, const Schedule &s) {
+    const int last_g = NG - (s.NB - 1) * s.GB;
+    const long long full = 2ll * C * s.GB + s.GB;   // block with full P1, SC, P3
+    Work w;
+    int k, kind;
+    long long local;
+    long long r = id;
+    const int g0 = (s.NB == 1) ? last_g : s.GB;
+    const long long b0 = (long long)C * g0 + g0;
+    if (r < b0) {
+        k = 0;
+        if (r < (long long)C * g0) {
+            kind = KIND_P1;
+            local = r;
+        } else {
+            kind = KIND_SC;
+            local = r - (long long)C * g0;
+        }
+    } else {
+        r -= b0;
+        const long long nfull = s.NB > 2 ? s.NB - 2 : 0;   // blocks 1..NB-2
+        if (r < nfull * full) {
+            const int blk = 1 + (int)(r / full);
+            r %= full;
+            if (r < (long long)C * s.GB) {
+                kind = KIND_P1;
+                k = blk;
+                local = r;
+            } else if (r < (long long)C * s.GB + s.GB) {
+                kind = KIND_SC;
+                k = blk;
+                local = r - (long long)C * s.GB;
+            } else {
+                kind = KIND_P3;
+                k = blk - 1;
+                local = r - (long long)C * s.GB - s.GB;
+            }
+        } else {
+            r -= nfull * full;
+            if (s.NB >= 2) {
+                // block NB-1: P1(NB-1) [C*last_g], SC(NB-1) [last_g], P3(NB-2) [C*GB]
+                if (r < (long long)C * last_g) {
+                    kind = KIND_P1;
+                    k = s.NB - 1;
+                    local = r;
+                } else if (r < (long long)C * last_g + last_g) {
+                    kind = KIND_SC;
+                    k = s.NB - 1;
+                    local = r - (long long)C * last_g;
+                } else if (r < (long long)C * last_g + last_g + (long long)C * s.GB) {
+                    kind = KIND_P3;
+                    k = s.NB - 2;
+                    local = r - (long long)C * last_g - last_g;
+                } else {
+                    kind = KIND_P3;
+                    k = s.NB - 1;
+                    local = r - (long long)C * last_g - last_g - (long long)C * s.GB;
+                }
+            } else {
+                kind = KIND_P3;
+                k = 0;
+                local = r;
+            }
+        }
+    }
+    const int gk = (k == s.NB - 1) ? last_g : s.GB;
+    w.kind = kind;
+    if (kind == KIND_SC) {
+        w.chunk = 0;
+        w.g = k * s.GB + (int)local;
+    } else {
+        w.chunk = (int)(local / gk);
+        w.g = k * s.GB + (int)(local % gk);
+    }
+    return w;
+}
+
+__device__ __forceinline__ unsigned long long pack_flag(uint32_t epoch) {
+    return static_cast<unsigned long long>(epoch);
 }
 
 __device__ __forceinline__ unsigned char *align1024(unsigned char *p) {
@@ -118,38 +205,30 @@ __device__ void record_error(WsHeader *h, uint32_t epoch, int item) {
     atomicExch(&h->err_epoch, epoch);
 }
 
-// Waits until `flag` carries this launch's epoch with a status >= need.
-// Bounded: gives up after ctl.timeout_ns (records the error) or as soon as
-// another CTA of this launch has given up; `failed` is then set.
-__device__ __noinline__ uint32_t wait_flag(const unsigned long long *flag, uint32_t epoch,
-                                           const Control &ctl, int item, uint32_t need, bool &failed) {
-    unsigned long long f = ld_acquire_u64(flag);
-    if (static_cast<uint32_t>(f >> 2) == epoch && static_cast<uint32_t>(f & 3u) >= need)
-        return static_cast<uint32_t>(f & 3u);
+// Waits until `flag` carries this launch's epoch.  Bounded: gives up after
+// ctl.timeout_ns (records the error) or as soon as another CTA of this launch
+// has given up.  Returns false if it gave up.
+__device__ __noinline__ bool wait_flag(const unsigned long long *flag, uint32_t epoch, const Control &ctl,
+                                       int item) {
+    if (ld_acquire_u64(flag) == pack_flag(epoch)) return true;
     const unsigned long long t0 = global_timer_ns();
     unsigned ns = 32;
     for (;;) {
         __nanosleep(ns);
         if (ns < 256) ns <<= 1;
-        f = ld_acquire_u64(flag);
-        if (static_cast<uint32_t>(f >> 2) == epoch && static_cast<uint32_t>(f & 3u) >= need)
-            return static_cast<uint32_t>(f & 3u);
-        if (ld_volatile_u32(&ctl.hdr->err_epoch) == epoch) {
-            failed = true;
-            return ST_INCL;
-        }
+        if (ld_acquire_u64(flag) == pack_flag(epoch)) return true;
+        if (ld_volatile_u32(&ctl.hdr->err_epoch) == epoch) return false;
         if (global_timer_ns() - t0 > ctl.timeout_ns) {
             record_error(ctl.hdr, epoch, item);
-            failed = true;
-            return ST_INCL;
+            return false;
         }
     }
 }
 
 // Waits for a TMA stage; bounded like wait_flag (a TMA copy completes in
 // microseconds, so running out here means the device is in trouble).
-__device__ __forceinline__ void wait_stage(uint64_t *bar, uint32_t parity, const Control &ctl,
-                                           uint32_t epoch, int item) {
+__device__ __forceinline__ void wait_stage(uint64_t *bar, uint32_t parity, const Control &ctl, uint32_t epoch,
+                                           int item) {
     if (mbar_try_wait(bar, parity)) return;
     const unsigned long long t0 = global_timer_ns();
     while (!mbar_try_wait(bar, parity)) {
@@ -158,123 +237,6 @@ __device__ __forceinline__ void wait_stage(uint64_t *bar, uint32_t parity, const
             return;
         }
     }
-}
-
-// Warp 0 publishes one quaternion per lane, then the flag (release).
-__device__ __forceinline__ void publish1(float4 *vals, unsigned long long *flag, long long idx, int lane,
-                                         float4 v, unsigned long long fv) {
-    __stcg(vals + idx * LT + lane, v);
-    __threadfence();
-    __syncwarp();
-    if (lane == 0) st_release_u64(flag, fv);
-}
-
-__device__ __forceinline__ void publish2(float4 *vals, unsigned long long *flag, long long idx, int lane,
-                                         float4 m, float4 v, unsigned long long fv) {
-    __stcg(vals + (idx * LT + lane) * 2, m);
-    __stcg(vals + (idx * LT + lane) * 2 + 1, v);
-    __threadfence();
-    __syncwarp();
-    if (lane == 0) st_release_u64(flag, fv);
-}
-
-// Decoupled look-back in the forward direction.  Tile (chunk, g) needs the
-// exclusive carry cum[t0-1] = L_{chunk-1} (x) ... (x) L_0 (x) init, combined
-// from the nearest tiles before it: each published aggregate (L) or inclusive
-// value (cum at that tile's end, which ends the walk).  Segment `seg` of the
-// block reads predecessor chunk-1-seg, so one round looks NSEG tiles back.
-// All threads call it; the result is valid in threads with seg == 0.
-__device__ float4 lookback_prod(const unsigned long long *flags, const float4 *agg, const float4 *incl,
-                                int chunk, int g, int NG, float4 init_v, uint32_t epoch, const Control &ctl,
-                                int item, int seg, int lane, float4 (*s_lb)[LT], uint32_t *s_st, int *s_done) {
-    float4 acc = q_ident();
-    int base = chunk - 1;
-    for (;;) {
-        const int pc = base - seg;
-        float4 v;
-        uint32_t st;
-        if (pc < 0) {
-            st = ST_INCL;   // before the first chunk: cum[-1] = init
-            v = init_v;
-        } else {
-            const long long pidx = static_cast<long long>(pc) * NG + g;
-            bool failed = false;
-            st = wait_flag(flags + pidx, epoch, ctl, item, ST_AGG, failed);
-            if (failed)
-                v = q_nan();
-            else
-                v = (st == ST_INCL) ? __ldcg(incl + pidx * LT + lane) : __ldcg(agg + pidx * LT + lane);
-        }
-        s_lb[seg][lane] = v;
-        if (lane == 0) s_st[seg] = st;
-        __syncthreads();
-        if (seg == 0) {
-            int done = 0;
-            for (int k = 0; k < NSEG; ++k) {
-                acc = q_mul(acc, s_lb[k][lane]);
-                if (s_st[k] == ST_INCL) {
-                    done = 1;
-                    break;
-                }
-            }
-            if (lane == 0) *s_done = done;
-        }
-        __syncthreads();
-        if (*s_done) break;
-        base -= NSEG;
-    }
-    return acc;
-}
-
-// Decoupled look-back in the reverse direction over affine maps
-// x -> V + M (x) x (M = conj(L_c), V = W_c for an aggregate; an inclusive value
-// is H at that tile's first step and ends the walk).  Returns H_{chunk+1}, the
-// cotangent entering tile `chunk` from the right; valid in threads seg == 0.
-__device__ float4 lookback_affine(const unsigned long long *flags, const float4 *agg2, const float4 *incl,
-                                  int chunk, int C, int g, int NG, uint32_t epoch, const Control &ctl, int item,
-                                  int seg, int lane, float4 (*s_lb)[LT][2], uint32_t *s_st, int *s_done) {
-    float4 accM = q_ident(), accV = q_zero();
-    int base = chunk + 1;
-    for (;;) {
-        const int pc = base + seg;
-        float4 m = q_zero(), v = q_zero();
-        uint32_t st;
-        if (pc >= C) {
-            st = ST_INCL;   // past the last step: nothing flows back
-        } else {
-            const long long pidx = static_cast<long long>(pc) * NG + g;
-            bool failed = false;
-            st = wait_flag(flags + pidx, epoch, ctl, item, ST_AGG, failed);
-            if (failed) {
-                v = q_nan();
-            } else if (st == ST_INCL) {
-                v = __ldcg(incl + pidx * LT + lane);
-            } else {
-                m = __ldcg(agg2 + (pidx * LT + lane) * 2);
-                v = __ldcg(agg2 + (pidx * LT + lane) * 2 + 1);
-            }
-        }
-        s_lb[seg][lane][0] = m;
-        s_lb[seg][lane][1] = v;
-        if (lane == 0) s_st[seg] = st;
-        __syncthreads();
-        if (seg == 0) {
-            int done = 0;
-            for (int k = 0; k < NSEG; ++k) {
-                accV = q_add(accV, q_mul(accM, s_lb[k][lane][1]));
-                if (s_st[k] == ST_INCL) {
-                    done = 1;
-                    break;
-                }
-                accM = q_mul(accM, s_lb[k][lane][0]);
-            }
-            if (lane == 0) *s_done = done;
-        }
-        __syncthreads();
-        if (*s_done) break;
-        base += NSEG;
-    }
-    return accV;
 }
 
 // The last CTA to finish resets the queue and advances the epoch, so that the
@@ -294,114 +256,56 @@ __device__ __forceinline__ void finish_launch(const Control &ctl, uint32_t epoch
 }
 
 // ---------------------------------------------------------------------------
-// Backward work-item schedule: A(0), [A(1), C(0)], [A(2), C(1)], ..., C(NB-1).
-// Within A(k) items are chunk-major in increasing chunk order; within C(k)
-// chunk-major in decreasing chunk order.  Batch k holds lane groups
-// [k*GB, k*GB + gk).
+// The scan kernel.  BWD = false: forward (q -> cum).  BWD = true: backward
+// ((q, d_cum) -> (d_q, d_init)).
 // ---------------------------------------------------------------------------
-struct Work {
-    int phase;   // 0 = A item, 1 = C item
-    int chunk;
-    int g;
-};
-
-__host__ __device__ inline Work decode_bwd(int id, int NG, int C, const Schedule &s) {
-    const int last_g = NG - (s.NB - 1) * s.GB;
-    const int fullA = s.CA * s.GB, fullC = C * s.GB;
-    const int nA0 = s.CA * (s.NB == 1 ? last_g : s.GB);
-    int phase, k, local;
-    int r = id;
-    if (r < nA0) {
-        phase = 0;
-        k = 0;
-        local = r;
-    } else {
-        r -= nA0;
-        const int nfull = s.NB > 2 ? s.NB - 2 : 0;   // pairs [A(k), C(k-1)] for k = 1..NB-2
-        const long long pair = static_cast<long long>(fullA) + fullC;
-        if (static_cast<long long>(r) < nfull * pair) {
-            k = 1 + static_cast<int>(r / pair);
-            r = static_cast<int>(r % pair);
-            if (r < fullA) {
-                phase = 0;
-                local = r;
-            } else {
-                phase = 1;
-                k -= 1;
-                local = r - fullA;
-            }
-        } else {
-            r -= static_cast<int>(nfull * pair);
-            if (s.NB >= 2) {
-                const int kk = s.NB - 1;
-                const int nAk = s.CA * last_g;
-                if (r < nAk) {
-                    phase = 0;
-                    k = kk;
-                    local = r;
-                } else if (r - nAk < fullC) {
-                    phase = 1;
-                    k = kk - 1;
-                    local = r - nAk;
-                } else {
-                    phase = 1;
-                    k = kk;
-                    local = r - nAk - fullC;
-                }
-            } else {
-                phase = 1;
-                k = 0;
-                local = r;
-            }
-        }
-    }
-    const int gk = (k == s.NB - 1) ? last_g : s.GB;
-    Work w;
-    w.phase = phase;
-    w.g = k * s.GB + local % gk;
-    w.chunk = (phase == 0) ? local / gk : C - 1 - local / gk;
-    return w;
-}
-
-// ---------------------------------------------------------------------------
-// Forward kernel.
-// ---------------------------------------------------------------------------
-template <int N, int NST>
+template <bool BWD, int LT, int N, int NSTAGE>
 __global__ void __launch_bounds__(NTHREADS)
-    quat_scan_fwd_kernel(const __grid_constant__ CUtensorMap qmap, const float4 *__restrict__ init,
-                         float4 *__restrict__ cum, unsigned long long *flags, float4 *agg, float4 *incl,
-                         const Geometry geo, const Control ctl) {
-    static_assert(NST >= 2, "at least double buffering");
+    quat_scan_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap dmap,
+                     const __grid_constant__ CUtensorMap omap, const float4 *__restrict__ init,
+                     float4 *__restrict__ d_init, const Arrays arr, const Geometry geo, const Schedule sch,
+                     const Control ctl) {
+    static_assert(NSTAGE >= 3, "ring of at least three stages");
+    static_assert(LT == 16 || LT == 32, "lane group width");
+    constexpr int NSEG = NTHREADS / LT;
     constexpr int T = NSEG * N;
-    constexpr uint32_t STAGE_BYTES = T * LT * 16;
+    constexpr int PD = NSTAGE - 2;                       // items prefetched ahead
+    constexpr uint32_t HALF = T * LT * 16;               // one operand of a stage
+    constexpr uint32_t STAGE = BWD ? 2 * HALF : HALF;
+    constexpr unsigned SEG0_MASK = (LT == 32) ? 0xffffffffu : 0x0000ffffu;
+
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem = align1024(smem_raw);
-    __shared__ __align__(8) uint64_t bar[NST];
-    __shared__ int s_items[NST];
-    __shared__ float4 s_seg[NSEG][LT];
-    __shared__ float4 s_lb[NSEG][LT];
-    __shared__ uint32_t s_st[NSEG];
-    __shared__ float4 s_carry[LT];
-    __shared__ int s_done;
+    __shared__ __align__(8) uint64_t bar[NSTAGE];
+    __shared__ int s_items[NSTAGE];
+    __shared__ float4 s_a[NSEG][LT];   // segment products, then exclusive prefixes
+    __shared__ float4 s_w[NSEG][LT];   // segment weighted sums, then V of the suffix maps
+    __shared__ float4 s_m[NSEG][LT];   // M of the suffix maps
 
     const int tid = threadIdx.x, lane = tid % LT, seg = tid / LT;
     const uint32_t epoch = ld_volatile_u32(&ctl.hdr->epoch);
     const uint32_t box_bytes = static_cast<uint32_t>(geo.boxw) * geo.boxh * 16u;
     const long long S = geo.S;
-    const int HJ = geo.HJ, NG = geo.NG;
+    const int HJ = geo.HJ, NG = geo.NG, C = geo.C, boxw = geo.boxw;
+    const unsigned long long flag_val = pack_flag(epoch);
 
     auto issue = [&](int it, int stage) {
-        const int chunk = it / NG, g = it % NG;
-        const int b = g / geo.NGb, hj0 = (g % geo.NGb) * LT;
-        mbar_arrive_expect_tx(&bar[stage], box_bytes);
-        tma_load_3d(smem + stage * STAGE_BYTES, &qmap, hj0 * 4, chunk * T, b, &bar[stage]);
+        const Work w = decode_item(it, NG, C, sch);
+        if (w.kind == KIND_SC) return;
+        const int b = w.g / geo.NGb, x = (w.g % geo.NGb) * LT * 4, y = w.chunk * T;
+        unsigned char *dst = smem + stage * STAGE;
+        mbar_arrive_expect_tx(&bar[stage], BWD ? 2 * box_bytes : box_bytes);
+        tma_load_3d(dst, &qmap, x, y, b, &bar[stage]);
+        if (BWD) tma_load_3d(dst + HALF, &dmap, x, y, b, &bar[stage]);
     };
 
     if (tid == 0) {
         prefetch_tensormap(&qmap);
-        for (int s = 0; s < NST; ++s) mbar_init(&bar[s], 1);
+        if (BWD) prefetch_tensormap(&dmap);
+        prefetch_tensormap(&omap);
+        for (int s = 0; s < NSTAGE; ++s) mbar_init(&bar[s], 1);
         fence_mbar_init();
-        for (int s = 0; s < NST - 1; ++s) {
+        for (int s = 0; s < PD; ++s) {
             const int it = static_cast<int>(atomicAdd(&ctl.hdr->counter, 1u));
             s_items[s] = it;
             if (it < ctl.nitems) issue(it, s);
@@ -410,280 +314,219 @@ __global__ void __launch_bounds__(NTHREADS)
     __syncthreads();
 
     uint32_t phases = 0;
-    int head = 0;
-    for (;;) {
-        const int item = s_items[head];
+    for (int n = 0;; ++n) {
+        const int stage = n % NSTAGE;
+        const int item = s_items[stage];
         if (item >= ctl.nitems) break;
         if (tid == 0) {
             const int nx = static_cast<int>(atomicAdd(&ctl.hdr->counter, 1u));
-            const int st = (head + NST - 1) % NST;
-            s_items[st] = nx;
+            const int ns = (n + PD) % NSTAGE;
+            s_items[ns] = nx;
+            bulk_wait_group_read<1>();   // stage ns was last stored from two items ago
             if (nx < ctl.nitems) {
                 fence_proxy_async_smem();
-                issue(nx, st);
+                issue(nx, ns);
             }
         }
-        wait_stage(&bar[head], (phases >> head) & 1u, ctl, epoch, item);
-        phases ^= 1u << head;
-
-        const int chunk = item / NG, g = item % NG;
+        const Work w = decode_item(item, NG, C, sch);
+        const int g = w.g, chunk = w.chunk;
         const int b = g / geo.NGb, hj = (g % geo.NGb) * LT + lane;
-        const bool lane_ok = lane < geo.boxw && hj < HJ;
-        const float4 *tile = reinterpret_cast<const float4 *>(smem + head * STAGE_BYTES);
+        const bool in_box = lane < boxw;
+        const bool lane_ok = in_box && hj < HJ;
+        const long long idx = static_cast<long long>(chunk) * NG + g;   // (chunk, group) slot
+        float4 *Qt = reinterpret_cast<float4 *>(smem + stage * STAGE);
+        float4 *Dt = reinterpret_cast<float4 *>(smem + stage * STAGE + HALF);
         const long long t0 = static_cast<long long>(chunk) * T + seg * N;
 
-        // Segment-local prefix products: x[i] = q_{t0+i} (x) ... (x) q_{t0}.
-        float4 x[N];
-        float4 loc = q_ident();
-#pragma unroll
-        for (int i = 0; i < N; ++i) {
-            float4 v = tile[(seg * N + i) * geo.boxw + lane];
-            if (t0 + i >= S) v = q_zero();
-            loc = q_mul(v, loc);
-            x[i] = loc;
+        if (w.kind != KIND_SC) {
+            wait_stage(&bar[stage], (phases >> stage) & 1u, ctl, epoch, item);
+            phases ^= 1u << stage;
         }
-        s_seg[seg][lane] = loc;
-        __syncthreads();
 
-        float4 Lc = q_ident();
-        if (seg == 0) {
-            // Exclusive prefixes of the segment aggregates (in place), chunk product L_c.
-            float4 e = q_ident();
-#pragma unroll
-            for (int k = 0; k < NSEG; ++k) {
-                const float4 a = s_seg[k][lane];
-                s_seg[k][lane] = e;
-                e = q_mul(a, e);
-            }
-            Lc = e;
-            if (chunk > 0 && item != ctl.stall_item)
-                publish1(agg, flags + item, item, lane, Lc, pack_flag(epoch, ST_AGG));
-        }
-        const float4 init_v = lane_ok ? init[static_cast<long long>(b) * HJ + hj] : q_ident();
-        float4 carry = init_v;
-        if (chunk > 0)
-            carry = lookback_prod(flags, agg, incl, chunk, g, NG, init_v, epoch, ctl, item, seg, lane, s_lb, s_st,
-                                  &s_done);
-        if (seg == 0) {
-            if (item != ctl.stall_item)
-                publish1(incl, flags + item, item, lane, q_mul(Lc, carry), pack_flag(epoch, ST_INCL));
-            s_carry[lane] = carry;
-        }
-        __syncthreads();
-
-        const float4 X = q_mul(s_seg[seg][lane], s_carry[lane]);   // cum just before this segment
-        if (lane_ok) {
-            float4 *out = cum + (static_cast<long long>(b) * S + t0) * HJ + hj;
-#pragma unroll
-            for (int i = 0; i < N; ++i)
-                if (t0 + i < S) __stcs(out + static_cast<long long>(i) * HJ, q_mul(x[i], X));
-        }
-        __syncthreads();
-        head = (head + 1) % NST;
-    }
-    finish_launch(ctl, epoch);
-}
-
-// ---------------------------------------------------------------------------
-// Backward kernel (A and C items from one queue).
-// ---------------------------------------------------------------------------
-template <int N, int NST>
-__global__ void __launch_bounds__(NTHREADS)
-    quat_scan_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap dmap,
-                         const float4 *__restrict__ init, float4 *__restrict__ d_q, float4 *__restrict__ d_init,
-                         const BwdArrays arr, const Geometry geo, const Schedule sch, const Control ctl) {
-    static_assert(NST >= 2, "at least double buffering");
-    constexpr int T = NSEG * N;
-    constexpr uint32_t HALF_BYTES = T * LT * 16;    // one operand of a stage
-    constexpr uint32_t STAGE_BYTES = 2 * HALF_BYTES;
-    extern __shared__ unsigned char smem_raw[];
-    unsigned char *smem = align1024(smem_raw);
-    __shared__ __align__(8) uint64_t bar[NST];
-    __shared__ int s_items[NST];
-    __shared__ float4 s_seg[NSEG][LT];   // segment products, then exclusive prefixes
-    __shared__ float4 s_w[NSEG][LT];     // segment weighted sums, then V of the suffix map
-    __shared__ float4 s_m[NSEG][LT];     // M of the suffix map
-    __shared__ float4 s_lb[NSEG][LT][2];
-    __shared__ uint32_t s_st[NSEG];
-    __shared__ float4 s_carry[LT];
-    __shared__ float4 s_h[LT];
-    __shared__ int s_done;
-
-    const int tid = threadIdx.x, lane = tid % LT, seg = tid / LT;
-    const uint32_t epoch = ld_volatile_u32(&ctl.hdr->epoch);
-    const uint32_t box_bytes = static_cast<uint32_t>(geo.boxw) * geo.boxh * 16u;
-    const long long S = geo.S;
-    const int HJ = geo.HJ, NG = geo.NG, C = geo.C;
-
-    auto issue = [&](int it, int stage) {
-        const Work w = decode_bwd(it, NG, C, sch);
-        const int b = w.g / geo.NGb, hj0 = (w.g % geo.NGb) * LT;
-        unsigned char *dst = smem + stage * STAGE_BYTES;
-        if (w.phase == 0) {
-            mbar_arrive_expect_tx(&bar[stage], box_bytes);
-            tma_load_3d(dst, &qmap, hj0 * 4, w.chunk * T, b, &bar[stage]);
-        } else {
-            mbar_arrive_expect_tx(&bar[stage], 2 * box_bytes);
-            tma_load_3d(dst, &qmap, hj0 * 4, w.chunk * T, b, &bar[stage]);
-            tma_load_3d(dst + HALF_BYTES, &dmap, hj0 * 4, w.chunk * T, b, &bar[stage]);
-        }
-    };
-
-    if (tid == 0) {
-        prefetch_tensormap(&qmap);
-        prefetch_tensormap(&dmap);
-        for (int s = 0; s < NST; ++s) mbar_init(&bar[s], 1);
-        fence_mbar_init();
-        for (int s = 0; s < NST - 1; ++s) {
-            const int it = static_cast<int>(atomicAdd(&ctl.hdr->counter, 1u));
-            s_items[s] = it;
-            if (it < ctl.nitems) issue(it, s);
-        }
-    }
-    __syncthreads();
-
-    uint32_t phases = 0;
-    int head = 0;
-    for (;;) {
-        const int item = s_items[head];
-        if (item >= ctl.nitems) break;
-        if (tid == 0) {
-            const int nx = static_cast<int>(atomicAdd(&ctl.hdr->counter, 1u));
-            const int st = (head + NST - 1) % NST;
-            s_items[st] = nx;
-            if (nx < ctl.nitems) {
-                fence_proxy_async_smem();
-                issue(nx, st);
-            }
-        }
-        wait_stage(&bar[head], (phases >> head) & 1u, ctl, epoch, item);
-        phases ^= 1u << head;
-
-        const Work w = decode_bwd(item, NG, C, sch);
-        const int chunk = w.chunk, g = w.g;
-        const int b = g / geo.NGb, hj = (g % geo.NGb) * LT + lane;
-        const bool lane_ok = lane < geo.boxw && hj < HJ;
-        const long long idx = static_cast<long long>(chunk) * NG + g;
-        const float4 *Qt = reinterpret_cast<const float4 *>(smem + head * STAGE_BYTES);
-        const float4 *Dt = reinterpret_cast<const float4 *>(smem + head * STAGE_BYTES + HALF_BYTES);
-        const long long t0 = static_cast<long long>(chunk) * T + seg * N;
-        const float4 init_v = lane_ok ? init[static_cast<long long>(b) * HJ + hj] : q_ident();
-
-        if (w.phase == 0) {
-            // ---- A item: forward carry at the end of this chunk ----------------
-            float4 loc = q_ident();
-#pragma unroll
-            for (int i = 0; i < N; ++i) {
-                float4 v = Qt[(seg * N + i) * geo.boxw + lane];
-                if (t0 + i >= S) v = q_zero();
-                loc = q_mul(v, loc);
-            }
-            s_seg[seg][lane] = loc;
-            __syncthreads();
-            float4 Lc = q_ident();
-            if (seg == 0) {
-#pragma unroll
-                for (int k = 0; k < NSEG; ++k) Lc = q_mul(s_seg[k][lane], Lc);
-                if (chunk > 0 && item != ctl.stall_item)
-                    publish1(arr.a_agg, arr.a_flags + idx, idx, lane, Lc, pack_flag(epoch, ST_AGG));
-            }
-            float4 carry = init_v;
-            if (chunk > 0)
-                carry = lookback_prod(arr.a_flags, arr.a_agg, arr.a_incl, chunk, g, NG, init_v, epoch, ctl, item,
-                                      seg, lane, reinterpret_cast<float4(*)[LT]>(&s_lb[0][0][0]), s_st, &s_done);
-            if (seg == 0 && item != ctl.stall_item)
-                publish1(arr.a_incl, arr.a_flags + idx, idx, lane, q_mul(Lc, carry), pack_flag(epoch, ST_INCL));
-        } else {
-            // ---- C item: cotangents of this chunk ------------------------------
-            // Forward local pass: lp[i] = product of the segment's steps before i,
-            // W = sum_i conj(local_i) (x) d_cum[t0+i].
-            float4 lp[N];
+        if (w.kind == KIND_P1) {
+            // ---- chunk aggregates ------------------------------------------------
             float4 loc = q_ident(), W = q_zero();
 #pragma unroll
             for (int i = 0; i < N; ++i) {
-                const int row = seg * N + i;
-                float4 qv = Qt[row * geo.boxw + lane], dv = Dt[row * geo.boxw + lane];
-                if (t0 + i >= S) {
-                    qv = q_zero();
-                    dv = q_zero();
-                }
-                lp[i] = loc;
+                const int cell = (seg * N + i) * boxw + lane;
+                const bool live = in_box && t0 + i < S;
+                const float4 qv = live ? Qt[cell] : q_zero();
                 loc = q_mul(qv, loc);
-                W = q_add(W, q_mul_cl(loc, dv));
-            }
-            s_seg[seg][lane] = loc;
-            s_w[seg][lane] = W;
-            __syncthreads();
-
-            float4 Mt = q_ident(), Vt = q_zero();
-            if (seg == 0) {
-                // Suffix maps: segment k receives H = V_k + M_k (x) H_{chunk+1}.
-                float4 M = q_ident(), V = q_zero();
-#pragma unroll
-                for (int k = NSEG - 1; k >= 0; --k) {
-                    const float4 Lk = s_seg[k][lane], Wk = s_w[k][lane];
-                    s_m[k][lane] = M;
-                    s_w[k][lane] = V;
-                    V = q_add(Wk, q_mul_cl(Lk, V));
-                    M = q_mul_cl(Lk, M);
+                if (BWD) {
+                    const float4 dv = live ? Dt[cell] : q_zero();
+                    W = q_add(W, q_mul_cl(loc, dv));
                 }
-                Mt = M;   // conj(L_c)
-                Vt = V;   // W_c
-                // Exclusive forward prefixes of the segment products (in place).
-                float4 e = q_ident();
+            }
+            s_a[seg][lane] = loc;
+            if (BWD) s_w[seg][lane] = W;
+            __syncthreads();
+            if (seg == 0) {
+                float4 L = q_ident();
+#pragma unroll
+                for (int k = 0; k < NSEG; ++k) L = q_mul(s_a[k][lane], L);
+                __stcg(arr.aggL + idx * LT + lane, L);
+                if (BWD) {
+                    float4 V = q_zero();
+#pragma unroll
+                    for (int k = NSEG - 1; k >= 0; --k) V = q_add(s_w[k][lane], q_mul_cl(s_a[k][lane], V));
+                    __stcg(arr.aggW + idx * LT + lane, V);
+                }
+                __threadfence();
+                __syncwarp(SEG0_MASK);
+                if (lane == 0 && item != ctl.stall_item) st_release_u64(arr.p1_flags + idx, flag_val);
+            }
+        } else if (w.kind == KIND_SC) {
+            // ---- scan of one lane group's chunk aggregates ------------------------
+            for (int c = tid; c < C; c += NTHREADS)
+                wait_flag(arr.p1_flags + static_cast<long long>(c) * NG + g, epoch, ctl, item);
+            __syncthreads();
+            const int R = (C + NSEG - 1) / NSEG;
+            const int c_lo = min(C, seg * R), c_hi = min(C, c_lo + R);
+            auto at = [&](int c) { return (static_cast<long long>(c) * NG + g) * LT + lane; };
+            // Pass 1: aggregates of this thread's chunk range.
+            float4 P = q_ident(), M = q_ident(), V = q_zero();
+            for (int c = c_lo; c < c_hi; ++c) P = q_mul(__ldcg(arr.aggL + at(c)), P);
+            if (BWD) {
+                for (int c = c_hi - 1; c >= c_lo; --c) {
+                    const float4 L = __ldcg(arr.aggL + at(c)), Wc = __ldcg(arr.aggW + at(c));
+                    V = q_add(Wc, q_mul_cl(L, V));
+                    M = q_mul_cl(L, M);
+                }
+            }
+            s_a[seg][lane] = P;
+            if (BWD) {
+                s_m[seg][lane] = M;
+                s_w[seg][lane] = V;
+            }
+            __syncthreads();
+            if (seg == 0) {
+                float4 e = lane_ok ? init[static_cast<long long>(b) * HJ + hj] : q_ident();
 #pragma unroll
                 for (int k = 0; k < NSEG; ++k) {
-                    const float4 a = s_seg[k][lane];
-                    s_seg[k][lane] = e;
+                    const float4 a = s_a[k][lane];
+                    s_a[k][lane] = e;
                     e = q_mul(a, e);
                 }
-                if (chunk < C - 1 && item != ctl.stall_item)
-                    publish2(arr.c_agg, arr.c_flags + idx, idx, lane, Mt, Vt, pack_flag(epoch, ST_AGG));
-            }
-            float4 Hnext = q_zero();
-            if (chunk < C - 1)
-                Hnext = lookback_affine(arr.c_flags, arr.c_agg, arr.c_incl, chunk, C, g, NG, epoch, ctl, item,
-                                        seg, lane, s_lb, s_st, &s_done);
-            if (seg == 0) {
-                const float4 Hc = q_add(Vt, q_mul(Mt, Hnext));
-                if (item != ctl.stall_item)
-                    publish1(arr.c_incl, arr.c_flags + idx, idx, lane, Hc, pack_flag(epoch, ST_INCL));
-                if (chunk == 0 && lane_ok) d_init[static_cast<long long>(b) * HJ + hj] = Hc;
-                float4 F = init_v;
-                if (chunk > 0) {
-                    const long long aidx = idx - NG;   // A item of chunk - 1
-                    bool failed = false;
-                    wait_flag(arr.a_flags + aidx, epoch, ctl, item, ST_INCL, failed);
-                    F = failed ? q_nan() : __ldcg(arr.a_incl + aidx * LT + lane);
+                if (BWD) {
+                    float4 h = q_zero();
+#pragma unroll
+                    for (int k = NSEG - 1; k >= 0; --k) {
+                        const float4 Vk = s_w[k][lane], Mk = s_m[k][lane];
+                        s_w[k][lane] = h;   // H entering range k from the right
+                        h = q_add(Vk, q_mul(Mk, h));
+                    }
+                    if (lane_ok) d_init[static_cast<long long>(b) * HJ + hj] = h;   // H_0
                 }
-                s_carry[lane] = F;
-                s_h[lane] = Hnext;
             }
             __syncthreads();
-
-            // Reverse pass: G = d_cum + H_next, d_q = G (x) conj(cum[t-1]),
-            // H = conj(q_t) (x) G handed to step t-1.
-            const float4 X = q_mul(s_seg[seg][lane], s_carry[lane]);
-            float4 Hn = q_add(s_w[seg][lane], q_mul(s_m[seg][lane], s_h[lane]));
-            float4 *out = d_q + (static_cast<long long>(b) * S + t0) * HJ + hj;
-#pragma unroll
-            for (int i = N - 1; i >= 0; --i) {
-                const int row = seg * N + i;
-                float4 qv = Qt[row * geo.boxw + lane], dv = Dt[row * geo.boxw + lane];
-                const bool t_ok = t0 + i < S;
-                if (!t_ok) {
-                    qv = q_zero();
-                    dv = q_zero();
-                }
-                const float4 G = q_add(dv, Hn);
-                const float4 cp = q_mul(lp[i], X);
-                if (lane_ok && t_ok) __stcs(out + static_cast<long long>(i) * HJ, q_mul_cr(G, cp));
-                Hn = q_mul_cl(qv, G);
+            // Pass 2: per-chunk carries.
+            float4 carry = s_a[seg][lane];
+            for (int c = c_lo; c < c_hi; ++c) {
+                __stcg(arr.carF + at(c), carry);
+                carry = q_mul(__ldcg(arr.aggL + at(c)), carry);
             }
+            if (BWD) {
+                float4 h = s_w[seg][lane];
+                for (int c = c_hi - 1; c >= c_lo; --c) {
+                    __stcg(arr.carH + at(c), h);
+                    h = q_add(__ldcg(arr.aggW + at(c)), q_mul_cl(__ldcg(arr.aggL + at(c)), h));
+                }
+            }
+            __threadfence();
+            __syncthreads();
+            if (tid == 0 && item != ctl.stall_item) st_release_u64(arr.sc_flags + g, flag_val);
+        } else {
+            // ---- apply the carries, write the outputs -----------------------------
+            const bool ok = wait_flag(arr.sc_flags + g, epoch, ctl, item);
+            const float4 F = ok ? __ldcg(arr.carF + idx * LT + lane) : q_nan();
+            if (!BWD) {
+                float4 x[N];
+                float4 loc = q_ident();
+#pragma unroll
+                for (int i = 0; i < N; ++i) {
+                    const bool live = in_box && t0 + i < S;
+                    const float4 qv = live ? Qt[(seg * N + i) * boxw + lane] : q_zero();
+                    loc = q_mul(qv, loc);
+                    x[i] = loc;
+                }
+                s_a[seg][lane] = loc;
+                __syncthreads();
+                if (seg == 0) {
+                    float4 e = q_ident();
+#pragma unroll
+                    for (int k = 0; k < NSEG; ++k) {
+                        const float4 a = s_a[k][lane];
+                        s_a[k][lane] = e;
+                        e = q_mul(a, e);
+                    }
+                }
+                __syncthreads();
+                const float4 X = q_mul(s_a[seg][lane], F);   // cum just before this segment
+                if (in_box) {
+#pragma unroll
+                    for (int i = 0; i < N; ++i) Qt[(seg * N + i) * boxw + lane] = q_mul(x[i], X);
+                }
+            } else {
+                const float4 Hc = ok ? __ldcg(arr.carH + idx * LT + lane) : q_nan();
+                // Forward local pass: lp[i] = product of the segment's steps before i.
+                float4 lp[N];
+                float4 loc = q_ident(), W = q_zero();
+#pragma unroll
+                for (int i = 0; i < N; ++i) {
+                    const int cell = (seg * N + i) * boxw + lane;
+                    const bool live = in_box && t0 + i < S;
+                    const float4 qv = live ? Qt[cell] : q_zero(), dv = live ? Dt[cell] : q_zero();
+                    lp[i] = loc;
+                    loc = q_mul(qv, loc);
+                    W = q_add(W, q_mul_cl(loc, dv));
+                }
+                s_a[seg][lane] = loc;
+                s_w[seg][lane] = W;
+                __syncthreads();
+                if (seg == 0) {
+                    // Suffix maps: segment k receives H = V_k + M_k (x) H_c.
+                    float4 Mk = q_ident(), Vk = q_zero();
+#pragma unroll
+                    for (int k = NSEG - 1; k >= 0; --k) {
+                        const float4 Lk = s_a[k][lane], Wk = s_w[k][lane];
+                        s_m[k][lane] = Mk;
+                        s_w[k][lane] = Vk;
+                        Vk = q_add(Wk, q_mul_cl(Lk, Vk));
+                        Mk = q_mul_cl(Lk, Mk);
+                    }
+                    float4 e = q_ident();
+#pragma unroll
+                    for (int k = 0; k < NSEG; ++k) {
+                        const float4 a = s_a[k][lane];
+                        s_a[k][lane] = e;
+                        e = q_mul(a, e);
+                    }
+                }
+                __syncthreads();
+                // Reverse pass: G = d_cum + H, d_q = G (x) conj(cum[t-1]),
+                // H = conj(q_t) (x) G handed to step t-1.
+                const float4 X = q_mul(s_a[seg][lane], F);
+                float4 Hn = q_add(s_w[seg][lane], q_mul(s_m[seg][lane], Hc));
+#pragma unroll
+                for (int i = N - 1; i >= 0; --i) {
+                    const int cell = (seg * N + i) * boxw + lane;
+                    const bool live = in_box && t0 + i < S;
+                    const float4 qv = live ? Qt[cell] : q_zero(), dv = live ? Dt[cell] : q_zero();
+                    const float4 G = q_add(dv, Hn);
+                    const float4 cp = q_mul(lp[i], X);
+                    if (in_box) Dt[cell] = q_mul_cr(G, cp);
+                    Hn = q_mul_cl(qv, G);
+                }
+            }
+            fence_proxy_async_smem();
+            __syncthreads();
+            if (tid == 0)
+                tma_store_3d(&omap, BWD ? (const void *)Dt : (const void *)Qt, (g % geo.NGb) * LT * 4, chunk * T, b);
         }
+        if (tid == 0) bulk_commit_group();   // one bulk group per item (empty unless P3)
         __syncthreads();
-        head = (head + 1) % NST;
     }
+    if (tid == 0) bulk_wait_group_all();
     finish_launch(ctl, epoch);
 }
 
@@ -694,31 +537,54 @@ __global__ void __launch_bounds__(NTHREADS)
 // ===========================================================================
 namespace {
 
-using qs::LT;
-using qs::NSEG;
 using qs::NTHREADS;
 
-// Kernel variants (steps per thread N, pipeline stages NST).
-constexpr int FWD_N = 8, FWD_NST = 2;
-constexpr int BWD_N = 4, BWD_NST = 2;
-constexpr int FWD_T = NSEG * FWD_N;
-constexpr int BWD_T = NSEG * BWD_N;
-constexpr size_t FWD_SMEM = size_t(FWD_NST) * FWD_T * LT * 16 + 1024;
-constexpr size_t BWD_SMEM = size_t(BWD_NST) * 2 * BWD_T * LT * 16 + 1024;
-// Target bytes of q per backward batch: small enough that the batch's q is
-// still in L2 when its C items re-read it.
-constexpr long long BWD_BATCH_Q_BYTES = 24ll << 20;
-long long g_batch_q_bytes = BWD_BATCH_Q_BYTES;
 constexpr unsigned long long DEFAULT_TIMEOUT_NS = 2000000000ull;
+// Target input bytes per batch of lane groups (q for the forward, q + d_cum for
+// the backward): about two batches plus the streamed outputs must stay in L2.
+constexpr long long DEFAULT_BATCH_BYTES = 24ll << 20;
+
+using KernelFn = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, const float4 *, float4 *, qs::Arrays,
+                          qs::Geometry, qs::Schedule, qs::Control);
+
+struct Variant {
+    KernelFn fn;
+    bool bwd;
+    int lt, n, nstage;
+    int T() const { return (NTHREADS / lt) * n; }
+    size_t smem() const { return size_t(nstage) * (bwd ? 2 : 1) * T() * lt * 16 + 1024; }
+};
+
+#define QS_VARIANT(B, LT, N, NS) \
+    Variant { reinterpret_cast<KernelFn>(qs::quat_scan_kernel<B, LT, N, NS>), B, LT, N, NS }
+const Variant kFwdVariants[] = {
+    QS_VARIANT(false, 32, 4, 4),
+    QS_VARIANT(false, 32, 8, 4),
+    QS_VARIANT(false, 32, 8, 3),
+    QS_VARIANT(false, 16, 4, 4),
+};
+const Variant kBwdVariants[] = {
+    QS_VARIANT(true, 32, 4, 4),
+    QS_VARIANT(true, 32, 4, 3),
+    QS_VARIANT(true, 32, 2, 4),
+    QS_VARIANT(true, 16, 4, 4),
+    QS_VARIANT(true, 32, 8, 3),
+};
+#undef QS_VARIANT
+constexpr int kNumFwd = sizeof(kFwdVariants) / sizeof(kFwdVariants[0]);
+constexpr int kNumBwd = sizeof(kBwdVariants) / sizeof(kBwdVariants[0]);
 
 std::mutex g_mu;
 unsigned long long g_timeout_ns = DEFAULT_TIMEOUT_NS;
 int g_stall_item = -1;
+long long g_batch_bytes = DEFAULT_BATCH_BYTES;
+int g_fwd_variant = -1, g_bwd_variant = -1;   // -1: automatic
 
 struct DevInfo {
     int sms = 0;
     int major = 0, minor = 0;
-    int fwd_blocks = 0, bwd_blocks = 0;   // resident CTAs per SM
+    int fwd_blocks[kNumFwd] = {};
+    int bwd_blocks[kNumBwd] = {};
 };
 std::map<int, DevInfo> g_dev;
 
@@ -787,18 +653,23 @@ int device_info(DevInfo **out, int *dev_out) {
             return QS_ERR_CUDA;
         }
         if (d.major == 10 && d.minor == 3) {
-            auto fk = qs::quat_scan_fwd_kernel<FWD_N, FWD_NST>;
-            auto bk = qs::quat_scan_bwd_kernel<BWD_N, BWD_NST>;
-            if (cudaFuncSetAttribute(fk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)FWD_SMEM) != cudaSuccess ||
-                cudaFuncSetAttribute(bk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)BWD_SMEM) != cudaSuccess ||
-                cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.fwd_blocks, fk, NTHREADS, FWD_SMEM) != cudaSuccess ||
-                cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.bwd_blocks, bk, NTHREADS, BWD_SMEM) != cudaSuccess) {
+            auto setup = [&](const Variant &v, int *blocks) {
+                const void *f = reinterpret_cast<const void *>(v.fn);
+                if (cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)v.smem()) !=
+                        cudaSuccess ||
+                    cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, f, NTHREADS, v.smem()) != cudaSuccess)
+                    return false;
+                *blocks = std::max(*blocks, 1);
+                return true;
+            };
+            bool ok = true;
+            for (int i = 0; i < kNumFwd; ++i) ok = ok && setup(kFwdVariants[i], &d.fwd_blocks[i]);
+            for (int i = 0; i < kNumBwd; ++i) ok = ok && setup(kBwdVariants[i], &d.bwd_blocks[i]);
+            if (!ok) {
                 cudaGetLastError();
                 d.sms = 0;
                 return QS_ERR_CUDA;
             }
-            d.fwd_blocks = std::max(d.fwd_blocks, 1);
-            d.bwd_blocks = std::max(d.bwd_blocks, 1);
         }
     }
     if (!(d.major == 10 && d.minor == 3)) return QS_ERR_DEVICE;
@@ -866,32 +737,120 @@ int make_map(CUtensorMap *m, const float *ptr, int64_t B, int64_t S, int64_t HJ,
     return r == CUDA_SUCCESS ? QS_OK : QS_ERR_CUDA;
 }
 
-qs::Geometry geometry(int64_t B, int64_t S, int64_t HJ, int T) {
-    qs::Geometry g;
+// Everything a launch needs, derived from the sizes alone (no device calls).
+struct Plan {
+    const Variant *v = nullptr;
+    int vidx = 0;
+    qs::Geometry geo{};
+    qs::Schedule sch{};
+    long long nitems = 0;
+    size_t o_p1 = 0, o_sc = 0, o_L = 0, o_W = 0, o_F = 0, o_H = 0, ws_bytes = 0;
+};
+
+int pick_variant(bool bwd, int64_t HJ) {
+    int forced;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        forced = bwd ? g_bwd_variant : g_fwd_variant;
+    }
+    if (forced >= 0) return forced;
+    // Narrow lane groups when a batch entry has few lanes.
+    if (HJ <= 16) return 3;
+    return 0;
+}
+
+int make_plan(bool bwd, int64_t B, int64_t S, int64_t HJ, Plan *pl) {
+    pl->vidx = pick_variant(bwd, HJ);
+    if (pl->vidx < 0 || pl->vidx >= (bwd ? kNumBwd : kNumFwd)) return QS_ERR_DIMS;
+    pl->v = bwd ? &kBwdVariants[pl->vidx] : &kFwdVariants[pl->vidx];
+    const int LT = pl->v->lt, T = pl->v->T();
+    qs::Geometry &g = pl->geo;
     g.S = S;
     g.HJ = (int)HJ;
     g.NGb = (int)((HJ + LT - 1) / LT);
-    g.NG = (int)(B * g.NGb);
-    g.C = (int)((S + T - 1) / T);
+    const long long NG = (long long)B * g.NGb;
+    const long long C = (S + T - 1) / T;
+    if (NG >= (1ll << 30) || C >= (1ll << 30)) return QS_ERR_DIMS;
+    g.NG = (int)NG;
+    g.C = (int)C;
     g.boxw = (int)std::min<int64_t>(LT, HJ);
     g.boxh = (int)std::min<int64_t>(T, S);
-    return g;
-}
-
-qs::Schedule bwd_schedule(const qs::Geometry &g) {
-    qs::Schedule s;
-    s.CA = g.C - 1;
-    const long long q_per_group = (long long)LT * g.S * 16;
     long long batch_bytes;
     {
         std::lock_guard<std::mutex> lk(g_mu);
-        batch_bytes = g_batch_q_bytes;
+        batch_bytes = g_batch_bytes;
     }
-    long long gb = batch_bytes / std::max<long long>(q_per_group, 1);
-    gb = std::max<long long>(1, std::min<long long>(gb, g.NG));
-    s.GB = (int)gb;
-    s.NB = (g.NG + s.GB - 1) / s.GB;
-    return s;
+    const long long in_per_group = (long long)LT * S * 16 * (bwd ? 2 : 1);
+    long long gb = batch_bytes / std::max<long long>(in_per_group, 1);
+    gb = std::max<long long>(1, std::min<long long>(gb, NG));
+    pl->sch.GB = (int)gb;
+    pl->sch.NB = (int)((NG + gb - 1) / gb);
+    const long long slots = C * NG;
+    pl->nitems = 2 * slots + NG;
+    if (pl->nitems >= (1ll << 31) - (1 << 20)) return QS_ERR_DIMS;
+    size_t off = sizeof(qs::WsHeader);
+    pl->o_p1 = off;
+    off = align_up(off + slots * 8, 256);
+    pl->o_sc = off;
+    off = align_up(off + NG * 8, 256);
+    const size_t per = (size_t)slots * LT * 16;
+    pl->o_L = off;
+    off = align_up(off + per, 256);
+    pl->o_F = off;
+    off = align_up(off + per, 256);
+    if (bwd) {
+        pl->o_W = off;
+        off = align_up(off + per, 256);
+        pl->o_H = off;
+        off = align_up(off + per, 256);
+    }
+    pl->ws_bytes = off;
+    return QS_OK;
+}
+
+int launch(bool bwd, const float *q, const float *d_cum, float *out, const float *init, float *d_init, int64_t B,
+           int64_t S, int64_t HJ, cudaStream_t stream) {
+    DevInfo *di = nullptr;
+    int dev = 0;
+    int rc = device_info(&di, &dev);
+    if (rc != QS_OK) return rc;
+    Plan pl;
+    rc = make_plan(bwd, B, S, HJ, &pl);
+    if (rc != QS_OK) return rc;
+    unsigned char *ws = nullptr;
+    rc = ensure_workspace(dev, stream, pl.ws_bytes, &ws);
+    if (rc != QS_OK) return rc;
+    CUtensorMap qmap, dmap, omap;
+    rc = make_map(&qmap, q, B, S, HJ, pl.geo.boxw, pl.geo.boxh);
+    if (rc == QS_OK) rc = make_map(&omap, out, B, S, HJ, pl.geo.boxw, pl.geo.boxh);
+    if (rc == QS_OK) rc = make_map(&dmap, bwd ? d_cum : q, B, S, HJ, pl.geo.boxw, pl.geo.boxh);
+    if (rc != QS_OK) return rc;
+    qs::Arrays arr;
+    arr.p1_flags = reinterpret_cast<unsigned long long *>(ws + pl.o_p1);
+    arr.sc_flags = reinterpret_cast<unsigned long long *>(ws + pl.o_sc);
+    arr.aggL = reinterpret_cast<float4 *>(ws + pl.o_L);
+    arr.carF = reinterpret_cast<float4 *>(ws + pl.o_F);
+    arr.aggW = bwd ? reinterpret_cast<float4 *>(ws + pl.o_W) : nullptr;
+    arr.carH = bwd ? reinterpret_cast<float4 *>(ws + pl.o_H) : nullptr;
+    qs::Control ctl;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        ctl.timeout_ns = g_timeout_ns;
+        ctl.stall_item = g_stall_item;
+    }
+    ctl.hdr = reinterpret_cast<qs::WsHeader *>(ws);
+    ctl.nitems = (int)pl.nitems;
+    const int blocks = bwd ? di->bwd_blocks[pl.vidx] : di->fwd_blocks[pl.vidx];
+    const int grid = (int)std::min<long long>(pl.nitems, (long long)di->sms * blocks);
+    const float4 *init4 = reinterpret_cast<const float4 *>(init);
+    float4 *dinit4 = reinterpret_cast<float4 *>(d_init);
+    void *args[] = {&qmap, &dmap, &omap, (void *)&init4, (void *)&dinit4, &arr, &pl.geo, &pl.sch, &ctl};
+    if (cudaLaunchKernel(reinterpret_cast<const void *>(pl.v->fn), dim3(grid), dim3(NTHREADS), args, pl.v->smem(),
+                         stream) != cudaSuccess) {
+        cudaGetLastError();
+        return QS_ERR_CUDA;
+    }
+    return QS_OK;
 }
 
 }  // namespace
@@ -906,46 +865,7 @@ extern "C" int quat_cumprod_fwd(const float *q, const float *init, float *cum, i
     const int64_t HJ = H * J;
     const size_t big = (size_t)B * S * HJ * 16, small = (size_t)B * HJ * 16;
     if (overlaps(cum, big, q, big) || overlaps(cum, big, init, small)) return QS_ERR_ALIAS;
-
-    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
-    DevInfo *di = nullptr;
-    int dev = 0;
-    int rc = device_info(&di, &dev);
-    if (rc != QS_OK) return rc;
-
-    const qs::Geometry geo = geometry(B, S, HJ, FWD_T);
-    const long long nitems = (long long)geo.C * geo.NG;
-    if (nitems >= (1ll << 31) - (1 << 20)) return QS_ERR_DIMS;
-    size_t off = sizeof(qs::WsHeader);
-    const size_t o_flags = off;
-    off = align_up(off + nitems * 8, 256);
-    const size_t o_agg = off;
-    off = align_up(off + nitems * LT * 16, 256);
-    const size_t o_incl = off;
-    off = align_up(off + nitems * LT * 16, 256);
-    unsigned char *ws = nullptr;
-    rc = ensure_workspace(dev, stream, off, &ws);
-    if (rc != QS_OK) return rc;
-
-    CUtensorMap qmap;
-    rc = make_map(&qmap, q, B, S, HJ, geo.boxw, geo.boxh);
-    if (rc != QS_OK) return rc;
-
-    qs::Control ctl;
-    {
-        std::lock_guard<std::mutex> lk(g_mu);
-        ctl.timeout_ns = g_timeout_ns;
-        ctl.stall_item = g_stall_item;
-    }
-    ctl.hdr = reinterpret_cast<qs::WsHeader *>(ws);
-    ctl.nitems = (int)nitems;
-    const int grid = (int)std::min<long long>(nitems, (long long)di->sms * di->fwd_blocks);
-    qs::quat_scan_fwd_kernel<FWD_N, FWD_NST><<<grid, NTHREADS, FWD_SMEM, stream>>>(
-        qmap, reinterpret_cast<const float4 *>(init), reinterpret_cast<float4 *>(cum),
-        reinterpret_cast<unsigned long long *>(ws + o_flags), reinterpret_cast<float4 *>(ws + o_agg),
-        reinterpret_cast<float4 *>(ws + o_incl), geo, ctl);
-    if (cudaGetLastError() != cudaSuccess) return QS_ERR_CUDA;
-    return QS_OK;
+    return launch(false, q, nullptr, cum, init, nullptr, B, S, HJ, static_cast<cudaStream_t>(stream_));
 }
 
 extern "C" int quat_cumprod_bwd(const float *q, const float *init, const float *d_cum, float *d_q, float *d_init,
@@ -974,60 +894,7 @@ extern "C" int quat_cumprod_bwd(const float *q, const float *init, const float *
         overlaps(d_init, small, q, big) || overlaps(d_init, small, init, small) ||
         overlaps(d_init, small, d_cum, big) || overlaps(d_q, big, d_init, small))
         return QS_ERR_ALIAS;
-
-    DevInfo *di = nullptr;
-    int dev = 0;
-    int rc = device_info(&di, &dev);
-    if (rc != QS_OK) return rc;
-
-    const qs::Geometry geo = geometry(B, S, HJ, BWD_T);
-    const qs::Schedule sch = bwd_schedule(geo);
-    const long long nA = (long long)sch.CA * geo.NG, nC = (long long)geo.C * geo.NG;
-    const long long nitems = nA + nC;
-    if (nitems >= (1ll << 31) - (1 << 20)) return QS_ERR_DIMS;
-    size_t off = sizeof(qs::WsHeader);
-    const size_t o_af = off;
-    off = align_up(off + nA * 8, 256);
-    const size_t o_aa = off;
-    off = align_up(off + nA * LT * 16, 256);
-    const size_t o_ai = off;
-    off = align_up(off + nA * LT * 16, 256);
-    const size_t o_cf = off;
-    off = align_up(off + nC * 8, 256);
-    const size_t o_ca = off;
-    off = align_up(off + nC * LT * 32, 256);
-    const size_t o_ci = off;
-    off = align_up(off + nC * LT * 16, 256);
-    unsigned char *ws = nullptr;
-    rc = ensure_workspace(dev, stream, off, &ws);
-    if (rc != QS_OK) return rc;
-
-    CUtensorMap qmap, dmap;
-    rc = make_map(&qmap, q, B, S, HJ, geo.boxw, geo.boxh);
-    if (rc == QS_OK) rc = make_map(&dmap, d_cum, B, S, HJ, geo.boxw, geo.boxh);
-    if (rc != QS_OK) return rc;
-
-    qs::BwdArrays arr;
-    arr.a_flags = reinterpret_cast<unsigned long long *>(ws + o_af);
-    arr.a_agg = reinterpret_cast<float4 *>(ws + o_aa);
-    arr.a_incl = reinterpret_cast<float4 *>(ws + o_ai);
-    arr.c_flags = reinterpret_cast<unsigned long long *>(ws + o_cf);
-    arr.c_agg = reinterpret_cast<float4 *>(ws + o_ca);
-    arr.c_incl = reinterpret_cast<float4 *>(ws + o_ci);
-    qs::Control ctl;
-    {
-        std::lock_guard<std::mutex> lk(g_mu);
-        ctl.timeout_ns = g_timeout_ns;
-        ctl.stall_item = g_stall_item;
-    }
-    ctl.hdr = reinterpret_cast<qs::WsHeader *>(ws);
-    ctl.nitems = (int)nitems;
-    const int grid = (int)std::min<long long>(nitems, (long long)di->sms * di->bwd_blocks);
-    qs::quat_scan_bwd_kernel<BWD_N, BWD_NST><<<grid, NTHREADS, BWD_SMEM, stream>>>(
-        qmap, dmap, reinterpret_cast<const float4 *>(init), reinterpret_cast<float4 *>(d_q),
-        reinterpret_cast<float4 *>(d_init), arr, geo, sch, ctl);
-    if (cudaGetLastError() != cudaSuccess) return QS_ERR_CUDA;
-    return QS_OK;
+    return launch(true, q, d_cum, d_q, init, d_init, B, S, HJ, stream);
 }
 
 extern "C" int quat_cumprod_status(void *stream_) {
@@ -1091,48 +958,54 @@ extern "C" int quat_cumprod_debug_stall_tile(int64_t tile) {
 
 extern "C" int quat_cumprod_debug_set_batch_bytes(int64_t bytes) {
     std::lock_guard<std::mutex> lk(g_mu);
-    g_batch_q_bytes = bytes > 0 ? (long long)bytes : BWD_BATCH_Q_BYTES;
+    g_batch_bytes = bytes > 0 ? (long long)bytes : DEFAULT_BATCH_BYTES;
     return QS_OK;
 }
 
-// Host-side check of the backward work-item schedule for these sizes: every
-// (phase, chunk, group) item appears exactly once, A items of a group come in
-// increasing chunk order, C items in decreasing chunk order, and the A item of
-// chunk c precedes the C item of chunk c+1 (the only cross-phase wait).
+extern "C" int quat_cumprod_debug_set_variant(int fwd_variant, int bwd_variant) {
+    if (fwd_variant >= kNumFwd || bwd_variant >= kNumBwd) return QS_ERR_DIMS;
+    std::lock_guard<std::mutex> lk(g_mu);
+    g_fwd_variant = fwd_variant < 0 ? -1 : fwd_variant;
+    g_bwd_variant = bwd_variant < 0 ? -1 : bwd_variant;
+    return QS_OK;
+}
+
+// Host-side check of the work-item schedule for these sizes (both
+// directions): every P1 (chunk, group), SC (group) and P3 (chunk, group) item
+// appears exactly once, and every item comes after the items it waits on
+// (SC after all P1 items of its group, P3 after the SC item of its group).
 extern "C" int quat_cumprod_debug_check_schedule(int64_t B, int64_t S, int64_t H, int64_t J) {
     const int dc = check_dims(B, S, H, J);
     if (dc == 1) return QS_OK;
     if (dc != QS_OK) return dc;
-    const qs::Geometry geo = geometry(B, S, H * J, BWD_T);
-    const qs::Schedule sch = bwd_schedule(geo);
-    const long long nA = (long long)sch.CA * geo.NG, nC = (long long)geo.C * geo.NG;
-    if (nA + nC > (1ll << 26)) return QS_ERR_DIMS;   // keep the check cheap
-    std::vector<int> posA(nA > 0 ? nA : 1, -1), posC(nC, -1);
-    for (long long id = 0; id < nA + nC; ++id) {
-        const qs::Work w = qs::decode_bwd((int)id, geo.NG, geo.C, sch);
-        if (w.g < 0 || w.g >= geo.NG || w.chunk < 0) return -100;
-        if (w.phase == 0) {
-            if (w.chunk >= sch.CA) return -101;
-            int &p = posA[(long long)w.chunk * geo.NG + w.g];
-            if (p != -1) return -102;
-            p = (int)id;
-        } else {
-            if (w.chunk >= geo.C) return -103;
-            int &p = posC[(long long)w.chunk * geo.NG + w.g];
-            if (p != -1) return -104;
-            p = (int)id;
+    for (int bwd = 0; bwd < 2; ++bwd) {
+        Plan pl;
+        const int rc = make_plan(bwd != 0, B, S, H * J, &pl);
+        if (rc != QS_OK) return rc;
+        const long long C = pl.geo.C, NG = pl.geo.NG;
+        if (pl.nitems > (1ll << 26)) return QS_ERR_DIMS;   // keep the check cheap
+        std::vector<long long> p1(C * NG, -1), p3(C * NG, -1), sc(NG, -1);
+        for (long long id = 0; id < pl.nitems; ++id) {
+            const qs::Work w = qs::decode_item((int)id, pl.geo.NG, pl.geo.C, pl.sch);
+            if (w.g < 0 || w.g >= NG) return -100;
+            if (w.kind == qs::KIND_SC) {
+                if (sc[w.g] != -1) return -101;
+                sc[w.g] = id;
+                continue;
+            }
+            if (w.chunk < 0 || w.chunk >= C) return -102;
+            std::vector<long long> &v = (w.kind == qs::KIND_P1) ? p1 : p3;
+            long long &slot = v[(long long)w.chunk * NG + w.g];
+            if (slot != -1) return -103;
+            slot = id;
         }
-    }
-    for (int g = 0; g < geo.NG; ++g) {
-        for (int c = 0; c < geo.C; ++c) {
-            const int pc = posC[(long long)c * geo.NG + g];
-            if (pc < 0) return -105;
-            if (c + 1 < geo.C && posC[(long long)(c + 1) * geo.NG + g] > pc) return -106;
-            if (c < sch.CA) {
-                const int pa = posA[(long long)c * geo.NG + g];
-                if (pa < 0) return -107;
-                if (c > 0 && posA[(long long)(c - 1) * geo.NG + g] > pa) return -108;
-                if (pa > posC[(long long)(c + 1) * geo.NG + g]) return -109;
+        for (long long g = 0; g < NG; ++g) {
+            if (sc[g] < 0) return -104;
+            for (long long c = 0; c < C; ++c) {
+                const long long a = p1[c * NG + g], z = p3[c * NG + g];
+                if (a < 0 || z < 0) return -105;
+                if (a > sc[g]) return -106;
+                if (sc[g] > z) return -107;
             }
         }
     }

@@ -39,8 +39,8 @@ def reset_hooks():
     yield
     lib.quat_cumprod_debug_set_timeout_ns(0)
     lib.quat_cumprod_debug_stall_tile(-1)
-    lib.quat_cumprod_debug_set_batch_bytes.argtypes = [ctypes.c_int64]
     lib.quat_cumprod_debug_set_batch_bytes(0)
+    lib.quat_cumprod_debug_set_variant(-1, -1)
 
 
 def normwise(got, ref):
@@ -145,7 +145,8 @@ def test_non_unit_quaternions(dev):
     check_against_oracle(dev, q.astype(np.float32), init, d_cum)
     # strongly non-unit on a short sequence
     q2 = (rng.standard_normal((1, 24, 3, 7, 4)) * 1.5).astype(np.float32)
-    check_against_oracle(dev, q2, init[:1, :3, :7].copy(), rng.standard_normal(q2.shape).astype(np.float32))
+    init2 = rng.standard_normal((1, 3, 7, 4)).astype(np.float32)
+    check_against_oracle(dev, q2, init2, rng.standard_normal(q2.shape).astype(np.float32))
 
 
 def test_identity_q_is_reverse_cumsum(dev):
@@ -180,12 +181,34 @@ def test_empty_sizes(dev):
 
 @pytest.mark.parametrize("batch_bytes", [1, 1 << 20])
 def test_backward_many_batches(dev, batch_bytes):
-    """Small batches exercise the interleaved A/C schedule with many batches."""
+    """Small batches exercise the interleaved P1/SC/P3 schedule with many batches."""
     lib = qs.load_library()
-    lib.quat_cumprod_debug_set_batch_bytes.argtypes = [ctypes.c_int64]
     lib.quat_cumprod_debug_set_batch_bytes(batch_bytes)
     w = workloads.custom("batches", 3, 1500, 4, 24, q_kind="rotation", theta_max=0.4, seed=9)
     check_against_oracle(dev, *workloads.make_inputs(w))
+
+
+N_FWD_VARIANTS, N_BWD_VARIANTS = 4, 5
+
+
+@pytest.mark.parametrize("variant", range(max(N_FWD_VARIANTS, N_BWD_VARIANTS)))
+@pytest.mark.parametrize("dims", [(2, 333, 3, 16), (1, 70, 5, 9), (3, 1100, 1, 40)])
+def test_every_compiled_variant(dev, variant, dims):
+    """Each compiled tile configuration (lane-group width, steps per thread, stages)."""
+    lib = qs.load_library()
+    fv = variant if variant < N_FWD_VARIANTS else -1
+    bv = variant if variant < N_BWD_VARIANTS else -1
+    assert lib.quat_cumprod_debug_set_variant(fv, bv) == qs.QS_OK
+    lib.quat_cumprod_debug_set_batch_bytes(1 << 16)   # several batches even at these sizes
+    B, S, H, J = dims
+    w = workloads.custom("variant", B, S, H, J, q_kind="rotation", theta_max=0.5, seed=variant)
+    check_against_oracle(dev, *workloads.make_inputs(w))
+
+
+def test_unknown_variant_is_rejected(dev):
+    lib = qs.load_library()
+    assert lib.quat_cumprod_debug_set_variant(N_FWD_VARIANTS, 0) == qs.QS_ERR_DIMS
+    assert lib.quat_cumprod_debug_set_variant(0, N_BWD_VARIANTS) == qs.QS_ERR_DIMS
 
 
 def test_repeated_calls_and_side_stream(dev):
