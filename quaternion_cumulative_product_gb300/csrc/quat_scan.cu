@@ -113,64 +113,65 @@ struct Work {
 
 // Queue order: block 0 = P1(0) SC(0); block k (1..NB-1) = P1(k) SC(k) P3(k-1);
 // block NB = P3(NB-1).  Inside P1/P3 of a batch: chunk-major (all groups of
-// the batch at chunk c, then chunk c+1).
+// the batch at chunk c, then chunk c+1).  Item counts stay below 2^31, so the
+// arithmetic is 32-bit.
 __host__ __device__ inline Work decode_item(int id, int NG, int C, const Schedule &s) {
-    const int last_g = NG - (s.NB - 1) * s.GB;
-    const long long full = 2ll * C * s.GB + s.GB;   // block with full P1, SC, P3
-    Work w;
+    const unsigned uC = static_cast<unsigned>(C), GB = static_cast<unsigned>(s.GB);
+    const unsigned last_g = static_cast<unsigned>(NG - (s.NB - 1) * s.GB);
+    const unsigned g0 = (s.NB == 1) ? last_g : GB;
+    const unsigned b0 = uC * g0 + g0;
+    unsigned r = static_cast<unsigned>(id), local;
     int k, kind;
-    long long local;
-    long long r = id;
-    const int g0 = (s.NB == 1) ? last_g : s.GB;
-    const long long b0 = (long long)C * g0 + g0;
     if (r < b0) {
         k = 0;
-        if (r < (long long)C * g0) {
+        if (r < uC * g0) {
             kind = KIND_P1;
             local = r;
         } else {
             kind = KIND_SC;
-            local = r - (long long)C * g0;
+            local = r - uC * g0;
         }
     } else {
         r -= b0;
-        const long long nfull = s.NB > 2 ? s.NB - 2 : 0;   // blocks 1..NB-2
+        const unsigned full = 2u * uC * GB + GB;   // block with full P1, SC, P3
+        const unsigned nfull = s.NB > 2 ? static_cast<unsigned>(s.NB - 2) : 0u;   // blocks 1..NB-2
         if (r < nfull * full) {
-            const int blk = 1 + (int)(r / full);
-            r %= full;
-            if (r < (long long)C * s.GB) {
+            const unsigned blk = 1u + r / full;
+            r -= (blk - 1u) * full;
+            if (r < uC * GB) {
                 kind = KIND_P1;
-                k = blk;
+                k = static_cast<int>(blk);
                 local = r;
-            } else if (r < (long long)C * s.GB + s.GB) {
+            } else if (r < uC * GB + GB) {
                 kind = KIND_SC;
-                k = blk;
-                local = r - (long long)C * s.GB;
+                k = static_cast<int>(blk);
+                local = r - uC * GB;
             } else {
                 kind = KIND_P3;
-                k = blk - 1;
-                local = r - (long long)C * s.GB - s.GB;
+                k = static_cast<int>(blk) - 1;
+                local = r - uC * GB - GB;
             }
         } else {
             r -= nfull * full;
             if (s.NB >= 2) {
                 // block NB-1: P1(NB-1) [C*last_g], SC(NB-1) [last_g], P3(NB-2) [C*GB]
-                if (r < (long long)C * last_g) {
+                const unsigned a1 = uC * last_g, a2 = a1 + last_g, a3 = a2 + uC * GB;
+                if (r < a1) {
                     kind = KIND_P1;
                     k = s.NB - 1;
                     local = r;
-                } else if (r < (long long)C * last_g + last_g) {
+                } else if (r < a2) {
                     kind = KIND_SC;
                     k = s.NB - 1;
-                    local = r - (long long)C * last_g;
-                } else if (r < (long long)C * last_g + last_g + (long long)C * s.GB) {
+                    local = r - a1;
+                } else if (r < a3) {
                     kind = KIND_P3;
                     k = s.NB - 2;
-                    local = r - (long long)C * last_g - last_g;
+                    local = r - a2;
                 } else {
                     kind = KIND_P3;
                     k = s.NB - 1;
-                    local = r - (long long)C * last_g - last_g - (long long)C * s.GB;
+                    local = r - a3;
                 }
             } else {
                 kind = KIND_P3;
@@ -179,14 +180,15 @@ __host__ __device__ inline Work decode_item(int id, int NG, int C, const Schedul
             }
         }
     }
-    const int gk = (k == s.NB - 1) ? last_g : s.GB;
+    const unsigned gk = (k == s.NB - 1) ? last_g : GB;
+    Work w;
     w.kind = kind;
     if (kind == KIND_SC) {
         w.chunk = 0;
-        w.g = k * s.GB + (int)local;
+        w.g = k * s.GB + static_cast<int>(local);
     } else {
-        w.chunk = (int)(local / gk);
-        w.g = k * s.GB + (int)(local % gk);
+        w.chunk = static_cast<int>(local / gk);
+        w.g = k * s.GB + static_cast<int>(local - (local / gk) * gk);
     }
     return w;
 }
@@ -217,6 +219,48 @@ __device__ __noinline__ bool wait_flag(const unsigned long long *flag, uint32_t 
         __nanosleep(ns);
         if (ns < 256) ns <<= 1;
         if (ld_acquire_u64(flag) == pack_flag(epoch)) return true;
+        if (ld_volatile_u32(&ctl.hdr->err_epoch) == epoch) return false;
+        if (global_timer_ns() - t0 > ctl.timeout_ns) {
+            record_error(ctl.hdr, epoch, item);
+            return false;
+        }
+    }
+}
+
+// Waits until the flags base[c*stride] for c = begin, begin+step, ... < end all
+// carry this launch's epoch.  The flags are polled with relaxed loads issued
+// eight at a time and acquired by one fence once all have been seen; bounded
+// like wait_flag.  Returns false if it gave up.
+__device__ __noinline__ bool wait_flags(const unsigned long long *base, long long stride, int begin, int end,
+                                        int step, uint32_t epoch, const Control &ctl, int item) {
+    const unsigned long long want = pack_flag(epoch);
+    unsigned long long t0 = 0;
+    unsigned ns = 32;
+    int c = begin;
+    for (int round = 0;; ++round) {
+        while (c < end) {
+            unsigned long long f[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int cc = c + u * step;
+                f[u] = cc < end ? ld_relaxed_u64(base + cc * stride) : want;
+            }
+            int ready = 0;
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                if (f[u] != want) break;
+                ++ready;
+            }
+            c += ready * step;
+            if (ready < 8) break;
+        }
+        if (c >= end) {
+            fence_acquire_gpu();
+            return true;
+        }
+        if (round == 0) t0 = global_timer_ns();
+        __nanosleep(ns);
+        if (ns < 256) ns <<= 1;
         if (ld_volatile_u32(&ctl.hdr->err_epoch) == epoch) return false;
         if (global_timer_ns() - t0 > ctl.timeout_ns) {
             record_error(ctl.hdr, epoch, item);
@@ -258,6 +302,14 @@ __device__ __forceinline__ void finish_launch(const Control &ctl, uint32_t epoch
 // ---------------------------------------------------------------------------
 // The scan kernel.  BWD = false: forward (q -> cum).  BWD = true: backward
 // ((q, d_cum) -> (d_q, d_init)).
+//
+// Per item the threads meet at two block barriers: after the segment-local
+// pass (segment results in shared memory) and before the item's shared memory
+// may be reused (P1: after the publishing segment has read the results; P3:
+// before the TMA store).  Each segment combines the results of the other
+// segments it needs itself, so no segment runs a serial scan for the others;
+// global waits (flags) and fences are done by one segment while the others
+// carry on.
 // ---------------------------------------------------------------------------
 template <bool BWD, int LT, int N, int NSTAGE>
 __global__ void __launch_bounds__(NTHREADS)
@@ -278,9 +330,10 @@ __global__ void __launch_bounds__(NTHREADS)
     unsigned char *smem = align1024(smem_raw);
     __shared__ __align__(8) uint64_t bar[NSTAGE];
     __shared__ int s_items[NSTAGE];
-    __shared__ float4 s_a[NSEG][LT];   // segment products, then exclusive prefixes
-    __shared__ float4 s_w[NSEG][LT];   // segment weighted sums, then V of the suffix maps
-    __shared__ float4 s_m[NSEG][LT];   // M of the suffix maps
+    __shared__ float4 s_a[NSEG][LT];   // segment products
+    __shared__ float4 s_w[BWD ? NSEG : 1][LT];   // segment weighted sums (backward)
+    __shared__ float4 s_cf[LT];        // carries of the current P3 item
+    __shared__ float4 s_ch[BWD ? LT : 1];
 
     const int tid = threadIdx.x, lane = tid % LT, seg = tid / LT;
     const uint32_t epoch = ld_volatile_u32(&ctl.hdr->epoch);
@@ -288,11 +341,14 @@ __global__ void __launch_bounds__(NTHREADS)
     const long long S = geo.S;
     const int HJ = geo.HJ, NG = geo.NG, C = geo.C, boxw = geo.boxw;
     const unsigned long long flag_val = pack_flag(epoch);
+    // Without partial boxes every staged cell is data or TMA zero fill, and
+    // zero steps are exactly what the padded tail of a chunk must be.
+    const bool masked = boxw < LT || geo.boxh < T;
 
     auto issue = [&](int it, int stage) {
         const Work w = decode_item(it, NG, C, sch);
         if (w.kind == KIND_SC) return;
-        const int b = w.g / geo.NGb, x = (w.g % geo.NGb) * LT * 4, y = w.chunk * T;
+        const int b = w.g / geo.NGb, x = (w.g - b * geo.NGb) * LT * 4, y = w.chunk * T;
         unsigned char *dst = smem + stage * STAGE;
         mbar_arrive_expect_tx(&bar[stage], BWD ? 2 * box_bytes : box_bytes);
         tma_load_3d(dst, &qmap, x, y, b, &bar[stage]);
@@ -330,106 +386,134 @@ __global__ void __launch_bounds__(NTHREADS)
         }
         const Work w = decode_item(item, NG, C, sch);
         const int g = w.g, chunk = w.chunk;
-        const int b = g / geo.NGb, hj = (g % geo.NGb) * LT + lane;
+        const int b = g / geo.NGb, gx = g - b * geo.NGb, hj = gx * LT + lane;
         const bool in_box = lane < boxw;
         const bool lane_ok = in_box && hj < HJ;
         const long long idx = static_cast<long long>(chunk) * NG + g;   // (chunk, group) slot
         float4 *Qt = reinterpret_cast<float4 *>(smem + stage * STAGE);
         float4 *Dt = reinterpret_cast<float4 *>(smem + stage * STAGE + HALF);
         const long long t0 = static_cast<long long>(chunk) * T + seg * N;
+        const int row0 = seg * N * boxw + lane;   // cell of this thread's first step
 
         if (w.kind != KIND_SC) {
             wait_stage(&bar[stage], (phases >> stage) & 1u, ctl, epoch, item);
             phases ^= 1u << stage;
         }
 
+        // Staged value of step i of this thread (zero outside the data).
+        auto cell_ok = [&](int i) { return !masked || (in_box && t0 + i < S); };
+
         if (w.kind == KIND_P1) {
             // ---- chunk aggregates ------------------------------------------------
             float4 loc = q_ident(), W = q_zero();
 #pragma unroll
             for (int i = 0; i < N; ++i) {
-                const int cell = (seg * N + i) * boxw + lane;
-                const bool live = in_box && t0 + i < S;
-                const float4 qv = live ? Qt[cell] : q_zero();
+                const bool ok = cell_ok(i);
+                const float4 qv = ok ? Qt[row0 + i * boxw] : q_zero();
                 loc = q_mul(qv, loc);
                 if (BWD) {
-                    const float4 dv = live ? Dt[cell] : q_zero();
+                    const float4 dv = ok ? Dt[row0 + i * boxw] : q_zero();
                     W = q_add(W, q_mul_cl(loc, dv));
                 }
             }
             s_a[seg][lane] = loc;
             if (BWD) s_w[seg][lane] = W;
             __syncthreads();
+            float4 L = q_ident(), V = q_zero();
             if (seg == 0) {
-                float4 L = q_ident();
 #pragma unroll
                 for (int k = 0; k < NSEG; ++k) L = q_mul(s_a[k][lane], L);
-                __stcg(arr.aggL + idx * LT + lane, L);
                 if (BWD) {
-                    float4 V = q_zero();
 #pragma unroll
                     for (int k = NSEG - 1; k >= 0; --k) V = q_add(s_w[k][lane], q_mul_cl(s_a[k][lane], V));
-                    __stcg(arr.aggW + idx * LT + lane, V);
                 }
+            }
+            __syncthreads();   // segment results consumed; the next item may overwrite them
+            if (seg == 0) {
+                __stcg(arr.aggL + idx * LT + lane, L);
+                if (BWD) __stcg(arr.aggW + idx * LT + lane, V);
                 __threadfence();
                 __syncwarp(SEG0_MASK);
                 if (lane == 0 && item != ctl.stall_item) st_release_u64(arr.p1_flags + idx, flag_val);
             }
         } else if (w.kind == KIND_SC) {
             // ---- scan of one lane group's chunk aggregates ------------------------
-            for (int c = tid; c < C; c += NTHREADS)
-                wait_flag(arr.p1_flags + static_cast<long long>(c) * NG + g, epoch, ctl, item);
+            wait_flags(arr.p1_flags + g, NG, tid, C, NTHREADS, epoch, ctl, item);
             __syncthreads();
+            constexpr int U = 8;   // aggregates loaded per batch (independent loads)
             const int R = (C + NSEG - 1) / NSEG;
             const int c_lo = min(C, seg * R), c_hi = min(C, c_lo + R);
             auto at = [&](int c) { return (static_cast<long long>(c) * NG + g) * LT + lane; };
             // Pass 1: aggregates of this thread's chunk range.
             float4 P = q_ident(), M = q_ident(), V = q_zero();
-            for (int c = c_lo; c < c_hi; ++c) P = q_mul(__ldcg(arr.aggL + at(c)), P);
+            for (int c0 = c_lo; c0 < c_hi; c0 += U) {
+                float4 Lb[U];
+#pragma unroll
+                for (int u = 0; u < U; ++u) Lb[u] = (c0 + u < c_hi) ? __ldcg(arr.aggL + at(c0 + u)) : q_ident();
+#pragma unroll
+                for (int u = 0; u < U; ++u) P = q_mul(Lb[u], P);
+            }
             if (BWD) {
-                for (int c = c_hi - 1; c >= c_lo; --c) {
-                    const float4 L = __ldcg(arr.aggL + at(c)), Wc = __ldcg(arr.aggW + at(c));
-                    V = q_add(Wc, q_mul_cl(L, V));
-                    M = q_mul_cl(L, M);
+                for (int c1 = c_hi; c1 > c_lo; c1 -= U) {
+                    float4 Lb[U], Wb[U];
+#pragma unroll
+                    for (int u = 0; u < U; ++u) {
+                        const int c = c1 - 1 - u;
+                        const bool in = c >= c_lo;
+                        Lb[u] = in ? __ldcg(arr.aggL + at(c)) : q_ident();
+                        Wb[u] = in ? __ldcg(arr.aggW + at(c)) : q_zero();
+                    }
+#pragma unroll
+                    for (int u = 0; u < U; ++u) {
+                        V = q_add(Wb[u], q_mul_cl(Lb[u], V));
+                        M = q_mul_cl(Lb[u], M);
+                    }
                 }
             }
             s_a[seg][lane] = P;
+            __shared__ float4 s_m[BWD ? NSEG : 1][LT];
             if (BWD) {
                 s_m[seg][lane] = M;
                 s_w[seg][lane] = V;
             }
             __syncthreads();
-            if (seg == 0) {
-                float4 e = lane_ok ? init[static_cast<long long>(b) * HJ + hj] : q_ident();
-#pragma unroll
-                for (int k = 0; k < NSEG; ++k) {
-                    const float4 a = s_a[k][lane];
-                    s_a[k][lane] = e;
-                    e = q_mul(a, e);
-                }
-                if (BWD) {
-                    float4 h = q_zero();
-#pragma unroll
-                    for (int k = NSEG - 1; k >= 0; --k) {
-                        const float4 Vk = s_w[k][lane], Mk = s_m[k][lane];
-                        s_w[k][lane] = h;   // H entering range k from the right
-                        h = q_add(Vk, q_mul(Mk, h));
-                    }
-                    if (lane_ok) d_init[static_cast<long long>(b) * HJ + hj] = h;   // H_0
-                }
+            // Carry into this thread's first chunk: ranges before it (forward),
+            // ranges after it (backward).
+            float4 carry = lane_ok ? init[static_cast<long long>(b) * HJ + hj] : q_ident();
+            for (int k = 0; k < seg; ++k) carry = q_mul(s_a[k][lane], carry);
+            float4 h = q_zero();
+            if (BWD) {
+                for (int k = NSEG - 1; k > seg; --k) h = q_add(s_w[k][lane], q_mul(s_m[k][lane], h));
+                if (seg == 0 && lane_ok)   // H_0 = V_0 + M_0 (x) (H entering range 0)
+                    d_init[static_cast<long long>(b) * HJ + hj] = q_add(V, q_mul(M, h));
             }
-            __syncthreads();
             // Pass 2: per-chunk carries.
-            float4 carry = s_a[seg][lane];
-            for (int c = c_lo; c < c_hi; ++c) {
-                __stcg(arr.carF + at(c), carry);
-                carry = q_mul(__ldcg(arr.aggL + at(c)), carry);
+            for (int c0 = c_lo; c0 < c_hi; c0 += U) {
+                float4 Lb[U];
+#pragma unroll
+                for (int u = 0; u < U; ++u) Lb[u] = (c0 + u < c_hi) ? __ldcg(arr.aggL + at(c0 + u)) : q_ident();
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    if (c0 + u < c_hi) __stcg(arr.carF + at(c0 + u), carry);
+                    carry = q_mul(Lb[u], carry);
+                }
             }
             if (BWD) {
-                float4 h = s_w[seg][lane];
-                for (int c = c_hi - 1; c >= c_lo; --c) {
-                    __stcg(arr.carH + at(c), h);
-                    h = q_add(__ldcg(arr.aggW + at(c)), q_mul_cl(__ldcg(arr.aggL + at(c)), h));
+                for (int c1 = c_hi; c1 > c_lo; c1 -= U) {
+                    float4 Lb[U], Wb[U];
+#pragma unroll
+                    for (int u = 0; u < U; ++u) {
+                        const int c = c1 - 1 - u;
+                        const bool in = c >= c_lo;
+                        Lb[u] = in ? __ldcg(arr.aggL + at(c)) : q_ident();
+                        Wb[u] = in ? __ldcg(arr.aggW + at(c)) : q_zero();
+                    }
+#pragma unroll
+                    for (int u = 0; u < U; ++u) {
+                        const int c = c1 - 1 - u;
+                        if (c >= c_lo) __stcg(arr.carH + at(c), h);
+                        h = q_add(Wb[u], q_mul_cl(Lb[u], h));
+                    }
                 }
             }
             __threadfence();
@@ -437,45 +521,40 @@ __global__ void __launch_bounds__(NTHREADS)
             if (tid == 0 && item != ctl.stall_item) st_release_u64(arr.sc_flags + g, flag_val);
         } else {
             // ---- apply the carries, write the outputs -----------------------------
-            const bool ok = wait_flag(arr.sc_flags + g, epoch, ctl, item);
-            const float4 F = ok ? __ldcg(arr.carF + idx * LT + lane) : q_nan();
+            // Segment 0 fetches the chunk's carries while the others start on
+            // their local products; all read them after the first barrier.
+            if (seg == 0) {
+                const bool ok = wait_flag(arr.sc_flags + g, epoch, ctl, item);
+                s_cf[lane] = ok ? __ldcg(arr.carF + idx * LT + lane) : q_nan();
+                if (BWD) s_ch[lane] = ok ? __ldcg(arr.carH + idx * LT + lane) : q_nan();
+            }
             if (!BWD) {
                 float4 x[N];
                 float4 loc = q_ident();
 #pragma unroll
                 for (int i = 0; i < N; ++i) {
-                    const bool live = in_box && t0 + i < S;
-                    const float4 qv = live ? Qt[(seg * N + i) * boxw + lane] : q_zero();
+                    const float4 qv = cell_ok(i) ? Qt[row0 + i * boxw] : q_zero();
                     loc = q_mul(qv, loc);
                     x[i] = loc;
                 }
                 s_a[seg][lane] = loc;
                 __syncthreads();
-                if (seg == 0) {
-                    float4 e = q_ident();
-#pragma unroll
-                    for (int k = 0; k < NSEG; ++k) {
-                        const float4 a = s_a[k][lane];
-                        s_a[k][lane] = e;
-                        e = q_mul(a, e);
-                    }
-                }
-                __syncthreads();
-                const float4 X = q_mul(s_a[seg][lane], F);   // cum just before this segment
+                // cum just before this segment = (segments before it) (x) carry.
+                float4 X = s_cf[lane];
+                for (int k = 0; k < seg; ++k) X = q_mul(s_a[k][lane], X);
                 if (in_box) {
 #pragma unroll
-                    for (int i = 0; i < N; ++i) Qt[(seg * N + i) * boxw + lane] = q_mul(x[i], X);
+                    for (int i = 0; i < N; ++i) Qt[row0 + i * boxw] = q_mul(x[i], X);
                 }
             } else {
-                const float4 Hc = ok ? __ldcg(arr.carH + idx * LT + lane) : q_nan();
                 // Forward local pass: lp[i] = product of the segment's steps before i.
                 float4 lp[N];
                 float4 loc = q_ident(), W = q_zero();
 #pragma unroll
                 for (int i = 0; i < N; ++i) {
-                    const int cell = (seg * N + i) * boxw + lane;
-                    const bool live = in_box && t0 + i < S;
-                    const float4 qv = live ? Qt[cell] : q_zero(), dv = live ? Dt[cell] : q_zero();
+                    const bool ok = cell_ok(i);
+                    const float4 qv = ok ? Qt[row0 + i * boxw] : q_zero();
+                    const float4 dv = ok ? Dt[row0 + i * boxw] : q_zero();
                     lp[i] = loc;
                     loc = q_mul(qv, loc);
                     W = q_add(W, q_mul_cl(loc, dv));
@@ -483,48 +562,30 @@ __global__ void __launch_bounds__(NTHREADS)
                 s_a[seg][lane] = loc;
                 s_w[seg][lane] = W;
                 __syncthreads();
-                if (seg == 0) {
-                    // Suffix maps: segment k receives H = V_k + M_k (x) H_c.
-                    float4 Mk = q_ident(), Vk = q_zero();
-#pragma unroll
-                    for (int k = NSEG - 1; k >= 0; --k) {
-                        const float4 Lk = s_a[k][lane], Wk = s_w[k][lane];
-                        s_m[k][lane] = Mk;
-                        s_w[k][lane] = Vk;
-                        Vk = q_add(Wk, q_mul_cl(Lk, Vk));
-                        Mk = q_mul_cl(Lk, Mk);
-                    }
-                    float4 e = q_ident();
-#pragma unroll
-                    for (int k = 0; k < NSEG; ++k) {
-                        const float4 a = s_a[k][lane];
-                        s_a[k][lane] = e;
-                        e = q_mul(a, e);
-                    }
-                }
-                __syncthreads();
+                // cum just before this segment, and the H entering its last step
+                // (segments after it composed onto the chunk's right carry).
+                float4 X = s_cf[lane];
+                for (int k = 0; k < seg; ++k) X = q_mul(s_a[k][lane], X);
+                float4 Hn = s_ch[lane];
+                for (int k = NSEG - 1; k > seg; --k) Hn = q_add(s_w[k][lane], q_mul_cl(s_a[k][lane], Hn));
                 // Reverse pass: G = d_cum + H, d_q = G (x) conj(cum[t-1]),
                 // H = conj(q_t) (x) G handed to step t-1.
-                const float4 X = q_mul(s_a[seg][lane], F);
-                float4 Hn = q_add(s_w[seg][lane], q_mul(s_m[seg][lane], Hc));
 #pragma unroll
                 for (int i = N - 1; i >= 0; --i) {
-                    const int cell = (seg * N + i) * boxw + lane;
-                    const bool live = in_box && t0 + i < S;
-                    const float4 qv = live ? Qt[cell] : q_zero(), dv = live ? Dt[cell] : q_zero();
+                    const bool ok = cell_ok(i);
+                    const float4 qv = ok ? Qt[row0 + i * boxw] : q_zero();
+                    const float4 dv = ok ? Dt[row0 + i * boxw] : q_zero();
                     const float4 G = q_add(dv, Hn);
-                    const float4 cp = q_mul(lp[i], X);
-                    if (in_box) Dt[cell] = q_mul_cr(G, cp);
+                    if (in_box) Dt[row0 + i * boxw] = q_mul_cr(G, q_mul(lp[i], X));
                     Hn = q_mul_cl(qv, G);
                 }
             }
             fence_proxy_async_smem();
-            __syncthreads();
+            __syncthreads();   // outputs staged; segment results consumed
             if (tid == 0)
-                tma_store_3d(&omap, BWD ? (const void *)Dt : (const void *)Qt, (g % geo.NGb) * LT * 4, chunk * T, b);
+                tma_store_3d(&omap, BWD ? (const void *)Dt : (const void *)Qt, gx * LT * 4, chunk * T, b);
         }
         if (tid == 0) bulk_commit_group();   // one bulk group per item (empty unless P3)
-        __syncthreads();
     }
     if (tid == 0) bulk_wait_group_all();
     finish_launch(ctl, epoch);
@@ -754,9 +815,11 @@ int pick_variant(bool bwd, int64_t HJ) {
         forced = bwd ? g_bwd_variant : g_fwd_variant;
     }
     if (forced >= 0) return forced;
-    // Narrow lane groups when a batch entry has few lanes.
+    // Narrow lane groups when a batch entry has few lanes; otherwise the
+    // measured fastest: 64-step tiles, 3 stages (forward), 32-step tiles,
+    // 3 stages (backward).
     if (HJ <= 16) return 3;
-    return 0;
+    return bwd ? 1 : 2;
 }
 
 int make_plan(bool bwd, int64_t B, int64_t S, int64_t HJ, Plan *pl) {
