@@ -10,9 +10,9 @@
 // Design (one GPU, HBM-bound; no tensor cores -- there is no dense contraction):
 //
 //  * Tile = LT lanes x T consecutive steps of one lane group (LT lanes of one
-//    batch entry, contiguous in memory).  One 3-D TMA load stages a tile (one
-//    per operand) into shared memory; thread (seg, lane) owns N consecutive
-//    steps of one lane, NSEG = 256 / LT segments per tile.
+//    batch entry, contiguous in memory), staged into shared memory by 3-D TMA
+//    loads of boxes of up to 64 lanes.  Compute thread (seg, lane) owns N
+//    consecutive steps of one lane; NSEG = 256 / LT segments per tile.
 //
 //  * Chunk aggregates (the page's factorisation):
 //      L_c = q_{t1-1} (x) ... (x) q_{t0}                      (chunk product)
@@ -28,19 +28,27 @@
 //    F_0 = init.
 //
 //  * One persistent kernel per direction runs three kinds of work items from
-//    one queue (no look-back chains):
+//    one global queue:
 //      P1 (chunk, group): read the tile, publish L_c (and W_c);
-//      SC (group):        once all P1 items of the group are published, scan
-//                         its chunk aggregates (8-16 threads per lane) into the
-//                         carries F_c (and H_{c+1}, and d_init);
+//      SC (group, 32-lane block): once all P1 items of the group are published,
+//                         scan its chunk aggregates (8 threads per lane) into
+//                         the carries F_c (and H_{c+1}, and d_init);
 //      P3 (chunk, group): read the tile again, apply the carries, write cum (or
-//                         d_q) into shared memory and store it with one TMA store.
+//                         d_q) into shared memory, store it with TMA.
 //    Lane groups are processed in batches whose inputs fit the L2 cache; the
 //    queue runs P1(0) SC(0) | P1(1) SC(1) P3(0) | P1(2) SC(2) P3(1) | ... so
-//    the P3 pass of a batch re-reads its tiles from L2: DRAM traffic stays
-//    near the minimum (32 B per element forward, 48 B backward).
-//    Every wait is on an item claimed earlier from the queue (no deadlock);
-//    every wait is bounded in time and reports QS_ERR_TIMEOUT instead of hanging.
+//    the P3 pass of a batch re-reads its tiles from L2.
+//
+//  * Warp roles inside a CTA (10 warps): 8 compute warps run the items; a
+//    producer warp claims items, issues TMA loads several stages ahead and
+//    fetches the carries of P3 items; a publisher warp writes P1 aggregates
+//    out (fence, flag), issues the TMA stores of P3 outputs and frees stages.
+//    They hand stages over through mbarriers (full / done / empty), so no
+//    global-memory latency sits on the compute warps' path.
+//
+//  * Every cross-CTA wait is on an item claimed earlier from the queue (no
+//    deadlock) and is bounded in time: it reports QS_ERR_TIMEOUT instead of
+//    hanging.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -58,7 +66,11 @@
 
 namespace qs {
 
-constexpr int NTHREADS = 256;          // threads per CTA
+constexpr int NCOMPUTE = 256;            // compute threads per CTA (8 warps)
+constexpr int PRODUCER_WARP = 8;
+constexpr int PUBLISHER_WARP = 9;
+constexpr int NTHREADS = NCOMPUTE + 64;  // + producer warp + publisher warp
+constexpr int CLAIM = 2;                 // items claimed per atomic
 
 // Per-workspace control block (device memory, zero-initialised, epoch = 1).
 struct __align__(256) WsHeader {
@@ -77,8 +89,6 @@ struct Geometry {
     int NGb;       // lane groups per batch entry
     int NG;        // lane groups in total
     int C;         // chunks along the sequence
-    int boxw;      // lanes per TMA box row (min(LT, HJ))
-    int boxh;      // rows per TMA box (min(T, S))
 };
 
 struct Control {
@@ -89,8 +99,8 @@ struct Control {
 };
 
 struct Arrays {
-    unsigned long long *p1_flags;   // [C*NG]   P1 item published
-    unsigned long long *sc_flags;   // [NG]     SC item published
+    unsigned long long *p1_flags;   // [C*NG]       P1 item published
+    unsigned long long *sc_flags;   // [NG*NSB]     SC item published
     float4 *aggL;                   // [C*NG*LT] chunk product L_c
     float4 *aggW;                   // [C*NG*LT] chunk weighted sum W_c (backward)
     float4 *carF;                   // [C*NG*LT] forward carry cum[t0-1]
@@ -99,8 +109,9 @@ struct Arrays {
 
 // Batches of lane groups: batch k holds groups [k*GB, k*GB + gk).
 struct Schedule {
-    int GB;   // lane groups per batch
-    int NB;   // batches
+    int GB;    // lane groups per batch
+    int NB;    // batches
+    int NSB;   // 32-lane blocks per group (SC items per group)
 };
 
 enum : int { KIND_P1 = 0, KIND_SC = 1, KIND_P3 = 2 };
@@ -109,6 +120,7 @@ struct Work {
     int kind;
     int chunk;   // P1/P3
     int g;       // lane group
+    int sb;      // 32-lane block (SC)
 };
 
 // Queue order: block 0 = P1(0) SC(0); block k (1..NB-1) = P1(k) SC(k) P3(k-1);
@@ -117,9 +129,10 @@ struct Work {
 // arithmetic is 32-bit.
 __host__ __device__ inline Work decode_item(int id, int NG, int C, const Schedule &s) {
     const unsigned uC = static_cast<unsigned>(C), GB = static_cast<unsigned>(s.GB);
+    const unsigned NSB = static_cast<unsigned>(s.NSB);
     const unsigned last_g = static_cast<unsigned>(NG - (s.NB - 1) * s.GB);
     const unsigned g0 = (s.NB == 1) ? last_g : GB;
-    const unsigned b0 = uC * g0 + g0;
+    const unsigned b0 = uC * g0 + g0 * NSB;
     unsigned r = static_cast<unsigned>(id), local;
     int k, kind;
     if (r < b0) {
@@ -133,7 +146,7 @@ __host__ __device__ inline Work decode_item(int id, int NG, int C, const Schedul
         }
     } else {
         r -= b0;
-        const unsigned full = 2u * uC * GB + GB;   // block with full P1, SC, P3
+        const unsigned full = 2u * uC * GB + GB * NSB;   // block with full P1, SC, P3
         const unsigned nfull = s.NB > 2 ? static_cast<unsigned>(s.NB - 2) : 0u;   // blocks 1..NB-2
         if (r < nfull * full) {
             const unsigned blk = 1u + r / full;
@@ -142,20 +155,20 @@ __host__ __device__ inline Work decode_item(int id, int NG, int C, const Schedul
                 kind = KIND_P1;
                 k = static_cast<int>(blk);
                 local = r;
-            } else if (r < uC * GB + GB) {
+            } else if (r < uC * GB + GB * NSB) {
                 kind = KIND_SC;
                 k = static_cast<int>(blk);
                 local = r - uC * GB;
             } else {
                 kind = KIND_P3;
                 k = static_cast<int>(blk) - 1;
-                local = r - uC * GB - GB;
+                local = r - uC * GB - GB * NSB;
             }
         } else {
             r -= nfull * full;
             if (s.NB >= 2) {
-                // block NB-1: P1(NB-1) [C*last_g], SC(NB-1) [last_g], P3(NB-2) [C*GB]
-                const unsigned a1 = uC * last_g, a2 = a1 + last_g, a3 = a2 + uC * GB;
+                // block NB-1: P1(NB-1) [C*last_g], SC(NB-1) [last_g*NSB], P3(NB-2) [C*GB]
+                const unsigned a1 = uC * last_g, a2 = a1 + last_g * NSB, a3 = a2 + uC * GB;
                 if (r < a1) {
                     kind = KIND_P1;
                     k = s.NB - 1;
@@ -185,10 +198,13 @@ __host__ __device__ inline Work decode_item(int id, int NG, int C, const Schedul
     w.kind = kind;
     if (kind == KIND_SC) {
         w.chunk = 0;
-        w.g = k * s.GB + static_cast<int>(local);
+        w.g = k * s.GB + static_cast<int>(local / NSB);
+        w.sb = static_cast<int>(local - (local / NSB) * NSB);
     } else {
-        w.chunk = static_cast<int>(local / gk);
-        w.g = k * s.GB + static_cast<int>(local - (local / gk) * gk);
+        const unsigned c = local / gk;
+        w.chunk = static_cast<int>(c);
+        w.g = k * s.GB + static_cast<int>(local - c * gk);
+        w.sb = 0;
     }
     return w;
 }
@@ -207,30 +223,17 @@ __device__ void record_error(WsHeader *h, uint32_t epoch, int item) {
     atomicExch(&h->err_epoch, epoch);
 }
 
-// Waits until `flag` carries this launch's epoch.  Bounded: gives up after
-// ctl.timeout_ns (records the error) or as soon as another CTA of this launch
-// has given up.  Returns false if it gave up.
-__device__ __noinline__ bool wait_flag(const unsigned long long *flag, uint32_t epoch, const Control &ctl,
-                                       int item) {
-    if (ld_acquire_u64(flag) == pack_flag(epoch)) return true;
-    const unsigned long long t0 = global_timer_ns();
-    unsigned ns = 32;
-    for (;;) {
-        __nanosleep(ns);
-        if (ns < 256) ns <<= 1;
-        if (ld_acquire_u64(flag) == pack_flag(epoch)) return true;
-        if (ld_volatile_u32(&ctl.hdr->err_epoch) == epoch) return false;
-        if (global_timer_ns() - t0 > ctl.timeout_ns) {
-            record_error(ctl.hdr, epoch, item);
-            return false;
-        }
-    }
+// True once this launch has recorded a timeout: every wait then gives up at
+// once so that the launch drains quickly (its outputs are invalid anyway).
+__device__ __forceinline__ bool launch_failed(const Control &ctl, uint32_t epoch) {
+    return ld_volatile_u32(&ctl.hdr->err_epoch) == epoch;
 }
 
 // Waits until the flags base[c*stride] for c = begin, begin+step, ... < end all
 // carry this launch's epoch.  The flags are polled with relaxed loads issued
-// eight at a time and acquired by one fence once all have been seen; bounded
-// like wait_flag.  Returns false if it gave up.
+// eight at a time and acquired by one fence once all have been seen.  Bounded:
+// gives up after ctl.timeout_ns (records the error) or as soon as another CTA
+// of this launch has given up.  Returns false if it gave up.
 __device__ __noinline__ bool wait_flags(const unsigned long long *base, long long stride, int begin, int end,
                                         int step, uint32_t epoch, const Control &ctl, int item) {
     const unsigned long long want = pack_flag(epoch);
@@ -261,7 +264,7 @@ __device__ __noinline__ bool wait_flags(const unsigned long long *base, long lon
         if (round == 0) t0 = global_timer_ns();
         __nanosleep(ns);
         if (ns < 256) ns <<= 1;
-        if (ld_volatile_u32(&ctl.hdr->err_epoch) == epoch) return false;
+        if (launch_failed(ctl, epoch)) return false;
         if (global_timer_ns() - t0 > ctl.timeout_ns) {
             record_error(ctl.hdr, epoch, item);
             return false;
@@ -269,18 +272,20 @@ __device__ __noinline__ bool wait_flags(const unsigned long long *base, long lon
     }
 }
 
-// Waits for a TMA stage; bounded like wait_flag (a TMA copy completes in
-// microseconds, so running out here means the device is in trouble).
-__device__ __forceinline__ void wait_stage(uint64_t *bar, uint32_t parity, const Control &ctl, uint32_t epoch,
-                                           int item) {
-    if (mbar_try_wait(bar, parity)) return;
+// Waits for a phase of an intra-CTA mbarrier.  These phases depend only on
+// this CTA's own warps and TMA copies, so they complete unless something is
+// broken; the wait is still bounded (records the error, returns false).
+__device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, unsigned long long limit_ns,
+                                         const Control &ctl, uint32_t epoch, int item) {
+    if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = global_timer_ns();
     while (!mbar_try_wait(bar, parity)) {
-        if (global_timer_ns() - t0 > ctl.timeout_ns) {
+        if (global_timer_ns() - t0 > limit_ns) {
             record_error(ctl.hdr, epoch, item);
-            return;
+            return false;
         }
     }
+    return true;
 }
 
 // The last CTA to finish resets the queue and advances the epoch, so that the
@@ -299,295 +304,432 @@ __device__ __forceinline__ void finish_launch(const Control &ctl, uint32_t epoch
     }
 }
 
+// Shared-memory footprint of one kernel configuration (dynamic part).
+__host__ __device__ constexpr size_t smem_bytes(bool bwd, int lt, int n, int nst) {
+    return 1024                                                        // alignment slack
+           + size_t(nst) * (bwd ? 2 : 1) * (NCOMPUTE / lt) * n * lt * 16  // stages
+           + size_t(2) * nst * (bwd ? 2 : 1) * lt * 16                  // P1 results, P3 carries
+           + size_t(2) * NCOMPUTE * 16 * (bwd ? 2 : 1);                  // segment results (2 parities)
+}
+
 // ---------------------------------------------------------------------------
 // The scan kernel.  BWD = false: forward (q -> cum).  BWD = true: backward
 // ((q, d_cum) -> (d_q, d_init)).
-//
-// Per item the threads meet at two block barriers: after the segment-local
-// pass (segment results in shared memory) and before the item's shared memory
-// may be reused (P1: after the publishing segment has read the results; P3:
-// before the TMA store).  Each segment combines the results of the other
-// segments it needs itself, so no segment runs a serial scan for the others;
-// global waits (flags) and fences are done by one segment while the others
-// carry on.
 // ---------------------------------------------------------------------------
-template <bool BWD, int LT, int N, int NSTAGE>
-__global__ void __launch_bounds__(NTHREADS)
+template <bool BWD, int LT, int N, int NST>
+__global__ void __launch_bounds__(NTHREADS, 1)
     quat_scan_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap dmap,
                      const __grid_constant__ CUtensorMap omap, const float4 *__restrict__ init,
                      float4 *__restrict__ d_init, const Arrays arr, const Geometry geo, const Schedule sch,
                      const Control ctl) {
-    static_assert(NSTAGE >= 3, "ring of at least three stages");
-    static_assert(LT == 16 || LT == 32, "lane group width");
-    constexpr int NSEG = NTHREADS / LT;
+    static_assert(NST >= 3, "at least three stages");
+    static_assert(LT == 32 || LT == 64 || LT == 128, "lane group width");
+    constexpr int NSEG = NCOMPUTE / LT;
     constexpr int T = NSEG * N;
-    constexpr int PD = NSTAGE - 2;                       // items prefetched ahead
-    constexpr uint32_t HALF = T * LT * 16;               // one operand of a stage
+    static_assert(T <= 256, "TMA box height");
+    static_assert(smem_bytes(BWD, LT, N, NST) <= 226 * 1024, "shared memory per CTA");
+    constexpr int BW = LT < 64 ? LT : 64;                  // lanes per TMA box
+    constexpr int NBOX = LT / BW;
+    constexpr uint32_t BOXB = T * BW * 16;                  // bytes of one box
+    constexpr uint32_t HALF = NBOX * BOXB;                  // one operand of a stage
     constexpr uint32_t STAGE = BWD ? 2 * HALF : HALF;
-    constexpr unsigned SEG0_MASK = (LT == 32) ? 0xffffffffu : 0x0000ffffu;
+    constexpr int NRES = BWD ? 2 : 1;
 
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem = align1024(smem_raw);
-    __shared__ __align__(8) uint64_t bar[NSTAGE];
-    __shared__ int s_items[NSTAGE];
-    __shared__ float4 s_a[NSEG][LT];   // segment products
-    __shared__ float4 s_w[BWD ? NSEG : 1][LT];   // segment weighted sums (backward)
-    __shared__ float4 s_cf[LT];        // carries of the current P3 item
-    __shared__ float4 s_ch[BWD ? LT : 1];
+    // [stages][P1 results][P3 carries][segment results]
+    float4 *s_res = reinterpret_cast<float4 *>(smem + size_t(NST) * STAGE);       // [NST][NRES][LT]
+    float4 *s_car = s_res + NST * NRES * LT;                                      // [NST][NRES][LT]
+    float4 *s_seg = s_car + NST * NRES * LT;                                      // [2][NRES][NSEG][LT]
+    __shared__ __align__(8) uint64_t full_bar[NST], done_bar[NST], empty_bar[NST];
+    __shared__ int s_items[NST];
+    __shared__ int s_end_seq;
+    __shared__ int s_abort;   // set when an intra-CTA wait ran out: every role stops
 
-    const int tid = threadIdx.x, lane = tid % LT, seg = tid / LT;
+    const int tid = threadIdx.x, warp = tid >> 5, wl = tid & 31;
     const uint32_t epoch = ld_volatile_u32(&ctl.hdr->epoch);
-    const uint32_t box_bytes = static_cast<uint32_t>(geo.boxw) * geo.boxh * 16u;
-    const long long S = geo.S;
-    const int HJ = geo.HJ, NG = geo.NG, C = geo.C, boxw = geo.boxw;
+    const int HJ = geo.HJ, NG = geo.NG, C = geo.C;
     const unsigned long long flag_val = pack_flag(epoch);
-    // Without partial boxes every staged cell is data or TMA zero fill, and
-    // zero steps are exactly what the padded tail of a chunk must be.
-    const bool masked = boxw < LT || geo.boxh < T;
-
-    auto issue = [&](int it, int stage) {
-        const Work w = decode_item(it, NG, C, sch);
-        if (w.kind == KIND_SC) return;
-        const int b = w.g / geo.NGb, x = (w.g - b * geo.NGb) * LT * 4, y = w.chunk * T;
-        unsigned char *dst = smem + stage * STAGE;
-        mbar_arrive_expect_tx(&bar[stage], BWD ? 2 * box_bytes : box_bytes);
-        tma_load_3d(dst, &qmap, x, y, b, &bar[stage]);
-        if (BWD) tma_load_3d(dst + HALF, &dmap, x, y, b, &bar[stage]);
-    };
 
     if (tid == 0) {
-        prefetch_tensormap(&qmap);
-        if (BWD) prefetch_tensormap(&dmap);
-        prefetch_tensormap(&omap);
-        for (int s = 0; s < NSTAGE; ++s) mbar_init(&bar[s], 1);
-        fence_mbar_init();
-        for (int s = 0; s < PD; ++s) {
-            const int it = static_cast<int>(atomicAdd(&ctl.hdr->counter, 1u));
-            s_items[s] = it;
-            if (it < ctl.nitems) issue(it, s);
+        for (int s = 0; s < NST; ++s) {
+            mbar_init(&full_bar[s], 2);                 // issue + fetch
+            mbar_init(&done_bar[s], NCOMPUTE / 32);     // one per compute warp
+            mbar_init(&empty_bar[s], 1);                // publisher
         }
+        s_end_seq = -1;
+        s_abort = 0;
+        fence_mbar_init();
     }
     __syncthreads();
 
-    uint32_t phases = 0;
-    for (int n = 0;; ++n) {
-        const int stage = n % NSTAGE;
-        const int item = s_items[stage];
-        if (item >= ctl.nitems) break;
-        if (tid == 0) {
-            const int nx = static_cast<int>(atomicAdd(&ctl.hdr->counter, 1u));
-            const int ns = (n + PD) % NSTAGE;
-            s_items[ns] = nx;
-            bulk_wait_group_read<1>();   // stage ns was last stored from two items ago
-            if (nx < ctl.nitems) {
-                fence_proxy_async_smem();
-                issue(nx, ns);
-            }
+    auto nboxes = [&](int gx) {   // boxes of group column gx that hold lanes
+        const int rem = HJ - gx * LT;
+        return rem >= LT ? NBOX : (rem + BW - 1) / BW;
+    };
+
+    if (warp == PRODUCER_WARP) {
+        // ================= producer: claims, TMA loads, carries =================
+        if (wl == 0) {
+            prefetch_tensormap(&qmap);
+            if (BWD) prefetch_tensormap(&dmap);
         }
-        const Work w = decode_item(item, NG, C, sch);
-        const int g = w.g, chunk = w.chunk;
-        const int b = g / geo.NGb, gx = g - b * geo.NGb, hj = gx * LT + lane;
-        const bool in_box = lane < boxw;
-        const bool lane_ok = in_box && hj < HJ;
-        const long long idx = static_cast<long long>(chunk) * NG + g;   // (chunk, group) slot
-        float4 *Qt = reinterpret_cast<float4 *>(smem + stage * STAGE);
-        float4 *Dt = reinterpret_cast<float4 *>(smem + stage * STAGE + HALF);
-        const long long t0 = static_cast<long long>(chunk) * T + seg * N;
-        const int row0 = seg * N * boxw + lane;   // cell of this thread's first step
-
-        if (w.kind != KIND_SC) {
-            wait_stage(&bar[stage], (phases >> stage) & 1u, ctl, epoch, item);
-            phases ^= 1u << stage;
-        }
-
-        // Staged value of step i of this thread (zero outside the data).
-        auto cell_ok = [&](int i) { return !masked || (in_box && t0 + i < S); };
-
-        if (w.kind == KIND_P1) {
-            // ---- chunk aggregates ------------------------------------------------
-            float4 loc = q_ident(), W = q_zero();
-#pragma unroll
-            for (int i = 0; i < N; ++i) {
-                const bool ok = cell_ok(i);
-                const float4 qv = ok ? Qt[row0 + i * boxw] : q_zero();
-                loc = q_mul(qv, loc);
-                if (BWD) {
-                    const float4 dv = ok ? Dt[row0 + i * boxw] : q_zero();
-                    W = q_add(W, q_mul_cl(loc, dv));
-                }
-            }
-            s_a[seg][lane] = loc;
-            if (BWD) s_w[seg][lane] = W;
-            __syncthreads();
-            float4 L = q_ident(), V = q_zero();
-            if (seg == 0) {
-#pragma unroll
-                for (int k = 0; k < NSEG; ++k) L = q_mul(s_a[k][lane], L);
-                if (BWD) {
-#pragma unroll
-                    for (int k = NSEG - 1; k >= 0; --k) V = q_add(s_w[k][lane], q_mul_cl(s_a[k][lane], V));
-                }
-            }
-            __syncthreads();   // segment results consumed; the next item may overwrite them
-            if (seg == 0) {
-                __stcg(arr.aggL + idx * LT + lane, L);
-                if (BWD) __stcg(arr.aggW + idx * LT + lane, V);
-                __threadfence();
-                __syncwarp(SEG0_MASK);
-                if (lane == 0 && item != ctl.stall_item) st_release_u64(arr.p1_flags + idx, flag_val);
-            }
-        } else if (w.kind == KIND_SC) {
-            // ---- scan of one lane group's chunk aggregates ------------------------
-            wait_flags(arr.p1_flags + g, NG, tid, C, NTHREADS, epoch, ctl, item);
-            __syncthreads();
-            constexpr int U = 8;   // aggregates loaded per batch (independent loads)
-            const int R = (C + NSEG - 1) / NSEG;
-            const int c_lo = min(C, seg * R), c_hi = min(C, c_lo + R);
-            auto at = [&](int c) { return (static_cast<long long>(c) * NG + g) * LT + lane; };
-            // Pass 1: aggregates of this thread's chunk range.
-            float4 P = q_ident(), M = q_ident(), V = q_zero();
-            for (int c0 = c_lo; c0 < c_hi; c0 += U) {
-                float4 Lb[U];
-#pragma unroll
-                for (int u = 0; u < U; ++u) Lb[u] = (c0 + u < c_hi) ? __ldcg(arr.aggL + at(c0 + u)) : q_ident();
-#pragma unroll
-                for (int u = 0; u < U; ++u) P = q_mul(Lb[u], P);
-            }
-            if (BWD) {
-                for (int c1 = c_hi; c1 > c_lo; c1 -= U) {
-                    float4 Lb[U], Wb[U];
-#pragma unroll
-                    for (int u = 0; u < U; ++u) {
-                        const int c = c1 - 1 - u;
-                        const bool in = c >= c_lo;
-                        Lb[u] = in ? __ldcg(arr.aggL + at(c)) : q_ident();
-                        Wb[u] = in ? __ldcg(arr.aggW + at(c)) : q_zero();
+        int seq_issue = 0, seq_fetch = 0, claim_next = 0, claim_left = 0;
+        bool ended = false;
+        unsigned long long idle_since = 0, stuck_since = 0;
+        int spins = 0;
+        for (;;) {
+            if (*reinterpret_cast<volatile int *>(&s_abort)) break;
+            bool prog = false;
+            // -- issue the next item into a free stage --
+            if (!ended) {
+                const int s = seq_issue % NST;
+                const bool free_stage =
+                    seq_issue < NST || mbar_test_wait(&empty_bar[s], ((seq_issue / NST) - 1) & 1);
+                if (free_stage) {
+                    if (claim_left == 0) {
+                        int c0 = 0;
+                        if (wl == 0) c0 = static_cast<int>(atomicAdd(&ctl.hdr->counter, (unsigned)CLAIM));
+                        claim_next = __shfl_sync(0xffffffffu, c0, 0);
+                        claim_left = CLAIM;
                     }
-#pragma unroll
-                    for (int u = 0; u < U; ++u) {
-                        V = q_add(Wb[u], q_mul_cl(Lb[u], V));
-                        M = q_mul_cl(Lb[u], M);
+                    const int it = claim_next++;
+                    --claim_left;
+                    if (it >= ctl.nitems) {
+                        ended = true;
+                        if (wl == 0) {
+                            s_items[s] = -1;
+                            s_end_seq = seq_issue;
+                            mbar_arrive(&full_bar[s]);
+                            mbar_arrive(&full_bar[s]);
+                        }
+                    } else {
+                        const Work w = decode_item(it, NG, C, sch);
+                        if (wl == 0) {
+                            s_items[s] = it;
+                            if (w.kind == KIND_SC) {
+                                mbar_arrive(&full_bar[s]);
+                            } else {
+                                const int b = w.g / geo.NGb, gx = w.g - b * geo.NGb, nb = nboxes(gx);
+                                unsigned char *dst = smem + size_t(s) * STAGE;
+                                mbar_arrive_expect_tx(&full_bar[s], (BWD ? 2u : 1u) * nb * BOXB);
+                                for (int j = 0; j < nb; ++j) {
+                                    const int x = (gx * LT + j * BW) * 4;
+                                    tma_load_3d(dst + j * BOXB, &qmap, x, w.chunk * T, b, &full_bar[s]);
+                                    if (BWD) tma_load_3d(dst + HALF + j * BOXB, &dmap, x, w.chunk * T, b, &full_bar[s]);
+                                }
+                            }
+                        }
+                        ++seq_issue;
                     }
+                    __syncwarp();
+                    prog = true;
                 }
             }
-            s_a[seg][lane] = P;
-            __shared__ float4 s_m[BWD ? NSEG : 1][LT];
-            if (BWD) {
-                s_m[seg][lane] = M;
-                s_w[seg][lane] = V;
-            }
-            __syncthreads();
-            // Carry into this thread's first chunk: ranges before it (forward),
-            // ranges after it (backward).
-            float4 carry = lane_ok ? init[static_cast<long long>(b) * HJ + hj] : q_ident();
-            for (int k = 0; k < seg; ++k) carry = q_mul(s_a[k][lane], carry);
-            float4 h = q_zero();
-            if (BWD) {
-                for (int k = NSEG - 1; k > seg; --k) h = q_add(s_w[k][lane], q_mul(s_m[k][lane], h));
-                if (seg == 0 && lane_ok)   // H_0 = V_0 + M_0 (x) (H entering range 0)
-                    d_init[static_cast<long long>(b) * HJ + hj] = q_add(V, q_mul(M, h));
-            }
-            // Pass 2: per-chunk carries.
-            for (int c0 = c_lo; c0 < c_hi; c0 += U) {
-                float4 Lb[U];
-#pragma unroll
-                for (int u = 0; u < U; ++u) Lb[u] = (c0 + u < c_hi) ? __ldcg(arr.aggL + at(c0 + u)) : q_ident();
-#pragma unroll
-                for (int u = 0; u < U; ++u) {
-                    if (c0 + u < c_hi) __stcg(arr.carF + at(c0 + u), carry);
-                    carry = q_mul(Lb[u], carry);
-                }
-            }
-            if (BWD) {
-                for (int c1 = c_hi; c1 > c_lo; c1 -= U) {
-                    float4 Lb[U], Wb[U];
-#pragma unroll
-                    for (int u = 0; u < U; ++u) {
-                        const int c = c1 - 1 - u;
-                        const bool in = c >= c_lo;
-                        Lb[u] = in ? __ldcg(arr.aggL + at(c)) : q_ident();
-                        Wb[u] = in ? __ldcg(arr.aggW + at(c)) : q_zero();
+            // -- complete the next issued item: carries of P3 items --
+            if (seq_fetch < seq_issue) {
+                const int s = seq_fetch % NST;
+                const int it = s_items[s];
+                const Work w = decode_item(it, NG, C, sch);
+                bool ready = true;
+                if (w.kind == KIND_P3) {
+                    // all 32-lane blocks of the group must have been scanned
+                    const unsigned long long f =
+                        wl < sch.NSB ? ld_relaxed_u64(arr.sc_flags + static_cast<long long>(w.g) * sch.NSB + wl)
+                                     : flag_val;
+                    ready = __all_sync(0xffffffffu, f == flag_val);
+                    bool give_up = false;
+                    if (!ready && spins > 64) {
+                        if (idle_since == 0) idle_since = global_timer_ns();
+                        if (launch_failed(ctl, epoch)) give_up = true;
+                        else if (global_timer_ns() - idle_since > ctl.timeout_ns) {
+                            if (wl == 0) record_error(ctl.hdr, epoch, it);
+                            give_up = true;
+                        }
                     }
-#pragma unroll
-                    for (int u = 0; u < U; ++u) {
-                        const int c = c1 - 1 - u;
-                        if (c >= c_lo) __stcg(arr.carH + at(c), h);
-                        h = q_add(Wb[u], q_mul_cl(Lb[u], h));
+                    if (ready || give_up) {
+                        fence_acquire_gpu();
+                        const long long base = (static_cast<long long>(w.chunk) * NG + w.g) * LT;
+                        for (int l = wl; l < LT; l += 32) {
+                            s_car[(s * NRES + 0) * LT + l] = give_up ? q_nan() : __ldcg(arr.carF + base + l);
+                            if (BWD) s_car[(s * NRES + 1) * LT + l] = give_up ? q_nan() : __ldcg(arr.carH + base + l);
+                        }
+                        ready = true;
+                        idle_since = 0;
                     }
                 }
-            }
-            __threadfence();
-            __syncthreads();
-            if (tid == 0 && item != ctl.stall_item) st_release_u64(arr.sc_flags + g, flag_val);
-        } else {
-            // ---- apply the carries, write the outputs -----------------------------
-            // Segment 0 fetches the chunk's carries while the others start on
-            // their local products; all read them after the first barrier.
-            if (seg == 0) {
-                const bool ok = wait_flag(arr.sc_flags + g, epoch, ctl, item);
-                s_cf[lane] = ok ? __ldcg(arr.carF + idx * LT + lane) : q_nan();
-                if (BWD) s_ch[lane] = ok ? __ldcg(arr.carH + idx * LT + lane) : q_nan();
-            }
-            if (!BWD) {
-                float4 x[N];
-                float4 loc = q_ident();
-#pragma unroll
-                for (int i = 0; i < N; ++i) {
-                    const float4 qv = cell_ok(i) ? Qt[row0 + i * boxw] : q_zero();
-                    loc = q_mul(qv, loc);
-                    x[i] = loc;
+                if (ready) {
+                    __syncwarp();
+                    if (wl == 0) mbar_arrive(&full_bar[s]);
+                    ++seq_fetch;
+                    prog = true;
                 }
-                s_a[seg][lane] = loc;
-                __syncthreads();
-                // cum just before this segment = (segments before it) (x) carry.
-                float4 X = s_cf[lane];
-                for (int k = 0; k < seg; ++k) X = q_mul(s_a[k][lane], X);
-                if (in_box) {
-#pragma unroll
-                    for (int i = 0; i < N; ++i) Qt[row0 + i * boxw] = q_mul(x[i], X);
-                }
+            }
+            if (ended && seq_fetch == seq_issue) break;
+            if (prog) {
+                spins = 0;
+                stuck_since = 0;
             } else {
-                // Forward local pass: lp[i] = product of the segment's steps before i.
-                float4 lp[N];
+                ++spins;
+                __nanosleep(32);
+                if ((spins & 255) == 0) {
+                    const unsigned long long now = global_timer_ns();
+                    if (stuck_since == 0) {
+                        stuck_since = now;
+                    } else if (now - stuck_since > 4 * ctl.timeout_ns) {
+                        if (wl == 0) {
+                            record_error(ctl.hdr, epoch, -1);
+                            s_abort = 1;
+                        }
+                        __syncwarp();
+                        break;
+                    }
+                }
+            }
+        }
+        // Never leave with TMA loads in flight: complete the second arrival of
+        // issued items that were not fetched, then wait (bounded) for every
+        // stage's last issued phase.
+        if (*reinterpret_cast<volatile int *>(&s_abort) && wl == 0) {
+            for (int q = seq_fetch; q < seq_issue; ++q) mbar_arrive(&full_bar[q % NST]);
+            for (int q = seq_issue - NST; q < seq_issue; ++q)
+                if (q >= 0) wait_bar(&full_bar[q % NST], (q / NST) & 1, 10000000ull, ctl, epoch, -1);
+        }
+    } else if (warp == PUBLISHER_WARP) {
+        // ================= publisher: P1 aggregates, P3 stores, free stages =====
+        if (wl == 0) prefetch_tensormap(&omap);
+        for (int seq = 0;; ++seq) {
+            const int s = seq % NST;
+            const uint32_t par = (seq / NST) & 1;
+            bool have = false;
+            unsigned long long t0 = 0;
+            for (int spin = 0;; ++spin) {
+                if (mbar_test_wait(&done_bar[s], par)) {
+                    have = true;
+                    break;
+                }
+                if (*reinterpret_cast<volatile int *>(&s_end_seq) == seq) break;
+                if (*reinterpret_cast<volatile int *>(&s_abort)) break;
+                __nanosleep(32);
+                if (spin == 64) t0 = global_timer_ns();
+                if (spin > 64 && (spin & 63) == 0 && global_timer_ns() - t0 > 4 * ctl.timeout_ns) {
+                    if (wl == 0) {
+                        record_error(ctl.hdr, epoch, -1);
+                        s_abort = 1;
+                    }
+                    break;
+                }
+            }
+            if (!have) break;
+            const int it = s_items[s];
+            const Work w = decode_item(it, NG, C, sch);
+            if (w.kind == KIND_P1) {
+                const long long base = (static_cast<long long>(w.chunk) * NG + w.g) * LT;
+                for (int l = wl; l < LT; l += 32) {
+                    __stcg(arr.aggL + base + l, s_res[(s * NRES + 0) * LT + l]);
+                    if (BWD) __stcg(arr.aggW + base + l, s_res[(s * NRES + 1) * LT + l]);
+                }
+                __threadfence();
+                __syncwarp();
+                if (wl == 0 && it != ctl.stall_item)
+                    st_release_u64(arr.p1_flags + static_cast<long long>(w.chunk) * NG + w.g, flag_val);
+            } else if (w.kind == KIND_P3 && wl == 0) {
+                const int b = w.g / geo.NGb, gx = w.g - b * geo.NGb, nb = nboxes(gx);
+                const unsigned char *src = smem + size_t(s) * STAGE + (BWD ? HALF : 0);
+                for (int j = 0; j < nb; ++j)
+                    tma_store_3d(&omap, src + j * BOXB, (gx * LT + j * BW) * 4, w.chunk * T, b);
+            }
+            if (wl == 0) {
+                bulk_commit_group();            // one bulk group per item
+                if (seq >= 1) {
+                    bulk_wait_group_read<1>();  // the previous item's store has read its stage
+                    mbar_arrive(&empty_bar[(seq - 1) % NST]);
+                }
+            }
+            __syncwarp();
+        }
+        if (wl == 0) bulk_wait_group_all();
+    } else {
+        // ================= compute warps =========================================
+        const int ctid = tid;                  // 0..255
+        const int lane = ctid % LT, seg = ctid / LT;
+        const int box = lane / BW, col = lane - box * BW;
+        for (int seq = 0;; ++seq) {
+            const int s = seq % NST;
+            const bool ok = wait_bar(&full_bar[s], (seq / NST) & 1, 4 * ctl.timeout_ns, ctl, epoch, -1);
+            // All compute warps leave together if any wait ran out.
+            if (named_bar_or(2, NCOMPUTE, !ok || *reinterpret_cast<volatile int *>(&s_abort))) {
+                if (ctid == 0) s_abort = 1;
+                break;
+            }
+            const int item = s_items[s];
+            if (item < 0) break;
+            const Work w = decode_item(item, NG, C, sch);
+            const int par = seq & 1;
+            float4 *sa = s_seg + (par * NRES + 0) * NCOMPUTE;      // [NSEG][LT]
+            float4 *sw = s_seg + (par * NRES + (BWD ? 1 : 0)) * NCOMPUTE;
+            float4 *Qt = reinterpret_cast<float4 *>(smem + size_t(s) * STAGE);
+            float4 *Dt = reinterpret_cast<float4 *>(smem + size_t(s) * STAGE + HALF);
+            const int cell0 = box * (T * BW) + seg * N * BW + col;   // this thread's first step
+
+            if (w.kind == KIND_P1) {
+                // ---- chunk aggregates --------------------------------------------
                 float4 loc = q_ident(), W = q_zero();
 #pragma unroll
                 for (int i = 0; i < N; ++i) {
-                    const bool ok = cell_ok(i);
-                    const float4 qv = ok ? Qt[row0 + i * boxw] : q_zero();
-                    const float4 dv = ok ? Dt[row0 + i * boxw] : q_zero();
-                    lp[i] = loc;
-                    loc = q_mul(qv, loc);
-                    W = q_add(W, q_mul_cl(loc, dv));
+                    loc = q_mul(Qt[cell0 + i * BW], loc);
+                    if (BWD) W = q_add(W, q_mul_cl(loc, Dt[cell0 + i * BW]));
                 }
-                s_a[seg][lane] = loc;
-                s_w[seg][lane] = W;
-                __syncthreads();
-                // cum just before this segment, and the H entering its last step
-                // (segments after it composed onto the chunk's right carry).
-                float4 X = s_cf[lane];
-                for (int k = 0; k < seg; ++k) X = q_mul(s_a[k][lane], X);
-                float4 Hn = s_ch[lane];
-                for (int k = NSEG - 1; k > seg; --k) Hn = q_add(s_w[k][lane], q_mul_cl(s_a[k][lane], Hn));
-                // Reverse pass: G = d_cum + H, d_q = G (x) conj(cum[t-1]),
-                // H = conj(q_t) (x) G handed to step t-1.
+                sa[seg * LT + lane] = loc;
+                if (BWD) sw[seg * LT + lane] = W;
+                named_bar_sync(1, NCOMPUTE);
+                if (seg == 0) {
+                    float4 L = q_ident();
 #pragma unroll
-                for (int i = N - 1; i >= 0; --i) {
-                    const bool ok = cell_ok(i);
-                    const float4 qv = ok ? Qt[row0 + i * boxw] : q_zero();
-                    const float4 dv = ok ? Dt[row0 + i * boxw] : q_zero();
-                    const float4 G = q_add(dv, Hn);
-                    if (in_box) Dt[row0 + i * boxw] = q_mul_cr(G, q_mul(lp[i], X));
-                    Hn = q_mul_cl(qv, G);
+                    for (int k = 0; k < NSEG; ++k) L = q_mul(sa[k * LT + lane], L);
+                    s_res[(s * NRES + 0) * LT + lane] = L;
+                    if (BWD) {
+                        float4 V = q_zero();
+#pragma unroll
+                        for (int k = NSEG - 1; k >= 0; --k) V = q_add(sw[k * LT + lane], q_mul_cl(sa[k * LT + lane], V));
+                        s_res[(s * NRES + 1) * LT + lane] = V;
+                    }
                 }
+            } else if (w.kind == KIND_SC) {
+                // ---- scan of one 32-lane block's chunk aggregates ----------------
+                wait_flags(arr.p1_flags + w.g, NG, ctid, C, NCOMPUTE, epoch, ctl, item);
+                named_bar_sync(1, NCOMPUTE);
+                constexpr int U = 8;    // aggregates loaded per batch (independent loads)
+                constexpr int RT = NCOMPUTE / 32;   // threads per lane (chunk ranges)
+                const int sl = ctid & 31, rg = ctid >> 5;   // lane in the block, range
+                const int l = w.sb * 32 + sl;               // lane in the group
+                const int b = w.g / geo.NGb, hj = (w.g - b * geo.NGb) * LT + l;
+                const bool lane_ok = hj < HJ;
+                const int R = (C + RT - 1) / RT;
+                const int c_lo = min(C, rg * R), c_hi = min(C, c_lo + R);
+                auto at = [&](int c) { return (static_cast<long long>(c) * NG + w.g) * LT + l; };
+                float4 *xa = sa;                       // [RT][32] range products
+                float4 *xm = s_seg + (par ^ 1) * NRES * NCOMPUTE;   // [RT][32] (other parity is free here)
+                float4 *xv = sw;
+                float4 P = q_ident(), M = q_ident(), V = q_zero();
+                for (int c0 = c_lo; c0 < c_hi; c0 += U) {
+                    float4 Lb[U];
+#pragma unroll
+                    for (int u = 0; u < U; ++u) Lb[u] = (c0 + u < c_hi) ? __ldcg(arr.aggL + at(c0 + u)) : q_ident();
+#pragma unroll
+                    for (int u = 0; u < U; ++u) P = q_mul(Lb[u], P);
+                }
+                if (BWD) {
+                    for (int c1 = c_hi; c1 > c_lo; c1 -= U) {
+                        float4 Lb[U], Wb[U];
+#pragma unroll
+                        for (int u = 0; u < U; ++u) {
+                            const int c = c1 - 1 - u;
+                            const bool in = c >= c_lo;
+                            Lb[u] = in ? __ldcg(arr.aggL + at(c)) : q_ident();
+                            Wb[u] = in ? __ldcg(arr.aggW + at(c)) : q_zero();
+                        }
+#pragma unroll
+                        for (int u = 0; u < U; ++u) {
+                            V = q_add(Wb[u], q_mul_cl(Lb[u], V));
+                            M = q_mul_cl(Lb[u], M);
+                        }
+                    }
+                }
+                xa[rg * 32 + sl] = P;
+                if (BWD) {
+                    xm[rg * 32 + sl] = M;
+                    xv[rg * 32 + sl] = V;
+                }
+                named_bar_sync(1, NCOMPUTE);
+                float4 carry = lane_ok ? init[static_cast<long long>(b) * HJ + hj] : q_ident();
+                for (int k = 0; k < rg; ++k) carry = q_mul(xa[k * 32 + sl], carry);
+                float4 h = q_zero();
+                if (BWD) {
+                    for (int k = RT - 1; k > rg; --k) h = q_add(xv[k * 32 + sl], q_mul(xm[k * 32 + sl], h));
+                    if (rg == 0 && lane_ok) d_init[static_cast<long long>(b) * HJ + hj] = q_add(V, q_mul(M, h));
+                }
+                for (int c0 = c_lo; c0 < c_hi; c0 += U) {
+                    float4 Lb[U];
+#pragma unroll
+                    for (int u = 0; u < U; ++u) Lb[u] = (c0 + u < c_hi) ? __ldcg(arr.aggL + at(c0 + u)) : q_ident();
+#pragma unroll
+                    for (int u = 0; u < U; ++u) {
+                        if (c0 + u < c_hi) __stcg(arr.carF + at(c0 + u), carry);
+                        carry = q_mul(Lb[u], carry);
+                    }
+                }
+                if (BWD) {
+                    for (int c1 = c_hi; c1 > c_lo; c1 -= U) {
+                        float4 Lb[U], Wb[U];
+#pragma unroll
+                        for (int u = 0; u < U; ++u) {
+                            const int c = c1 - 1 - u;
+                            const bool in = c >= c_lo;
+                            Lb[u] = in ? __ldcg(arr.aggL + at(c)) : q_ident();
+                            Wb[u] = in ? __ldcg(arr.aggW + at(c)) : q_zero();
+                        }
+#pragma unroll
+                        for (int u = 0; u < U; ++u) {
+                            const int c = c1 - 1 - u;
+                            if (c >= c_lo) __stcg(arr.carH + at(c), h);
+                            h = q_add(Wb[u], q_mul_cl(Lb[u], h));
+                        }
+                    }
+                }
+                __threadfence();
+                named_bar_sync(1, NCOMPUTE);
+                if (ctid == 0 && item != ctl.stall_item)
+                    st_release_u64(arr.sc_flags + static_cast<long long>(w.g) * sch.NSB + w.sb, flag_val);
+            } else {
+                // ---- apply the carries, write the outputs in place ---------------
+                const float4 F = s_car[(s * NRES + 0) * LT + lane];
+                if (!BWD) {
+                    float4 x[N];
+                    float4 loc = q_ident();
+#pragma unroll
+                    for (int i = 0; i < N; ++i) {
+                        loc = q_mul(Qt[cell0 + i * BW], loc);
+                        x[i] = loc;
+                    }
+                    sa[seg * LT + lane] = loc;
+                    named_bar_sync(1, NCOMPUTE);
+                    float4 X = F;   // cum just before this segment
+                    for (int k = 0; k < seg; ++k) X = q_mul(sa[k * LT + lane], X);
+#pragma unroll
+                    for (int i = 0; i < N; ++i) Qt[cell0 + i * BW] = q_mul(x[i], X);
+                } else {
+                    float4 lp[N];
+                    float4 loc = q_ident(), W = q_zero();
+#pragma unroll
+                    for (int i = 0; i < N; ++i) {
+                        lp[i] = loc;
+                        loc = q_mul(Qt[cell0 + i * BW], loc);
+                        W = q_add(W, q_mul_cl(loc, Dt[cell0 + i * BW]));
+                    }
+                    sa[seg * LT + lane] = loc;
+                    sw[seg * LT + lane] = W;
+                    named_bar_sync(1, NCOMPUTE);
+                    float4 X = F;
+                    for (int k = 0; k < seg; ++k) X = q_mul(sa[k * LT + lane], X);
+                    float4 Hn = s_car[(s * NRES + 1) * LT + lane];
+                    for (int k = NSEG - 1; k > seg; --k) Hn = q_add(sw[k * LT + lane], q_mul_cl(sa[k * LT + lane], Hn));
+                    // Reverse pass: G = d_cum + H, d_q = G (x) conj(cum[t-1]),
+                    // H = conj(q_t) (x) G handed to step t-1.
+#pragma unroll
+                    for (int i = N - 1; i >= 0; --i) {
+                        const float4 qv = Qt[cell0 + i * BW];
+                        const float4 G = q_add(Dt[cell0 + i * BW], Hn);
+                        Dt[cell0 + i * BW] = q_mul_cr(G, q_mul(lp[i], X));
+                        Hn = q_mul_cl(qv, G);
+                    }
+                }
+                fence_proxy_async_smem();
             }
-            fence_proxy_async_smem();
-            __syncthreads();   // outputs staged; segment results consumed
-            if (tid == 0)
-                tma_store_3d(&omap, BWD ? (const void *)Dt : (const void *)Qt, gx * LT * 4, chunk * T, b);
+            __syncwarp();
+            if (wl == 0) mbar_arrive(&done_bar[s]);
         }
-        if (tid == 0) bulk_commit_group();   // one bulk group per item (empty unless P3)
     }
-    if (tid == 0) bulk_wait_group_all();
     finish_launch(ctl, epoch);
 }
 
@@ -608,28 +750,29 @@ constexpr long long DEFAULT_BATCH_BYTES = 24ll << 20;
 using KernelFn = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, const float4 *, float4 *, qs::Arrays,
                           qs::Geometry, qs::Schedule, qs::Control);
 
+// One compiled configuration: lane-group width LT, steps per thread N, stages.
 struct Variant {
     KernelFn fn;
     bool bwd;
     int lt, n, nstage;
-    int T() const { return (NTHREADS / lt) * n; }
-    size_t smem() const { return size_t(nstage) * (bwd ? 2 : 1) * T() * lt * 16 + 1024; }
+    int T() const { return (qs::NCOMPUTE / lt) * n; }
+    int bw() const { return lt < 64 ? lt : 64; }
+    size_t smem() const { return qs::smem_bytes(bwd, lt, n, nstage); }
 };
 
 #define QS_VARIANT(B, LT, N, NS) \
     Variant { reinterpret_cast<KernelFn>(qs::quat_scan_kernel<B, LT, N, NS>), B, LT, N, NS }
 const Variant kFwdVariants[] = {
-    QS_VARIANT(false, 32, 4, 4),
-    QS_VARIANT(false, 32, 8, 4),
-    QS_VARIANT(false, 32, 8, 3),
-    QS_VARIANT(false, 16, 4, 4),
+    QS_VARIANT(false, 128, 8, 5),   // 16-step chunks, 32 KiB stages
+    QS_VARIANT(false, 64, 8, 5),    // 32-step chunks
+    QS_VARIANT(false, 32, 8, 4),    // 64-step chunks
+    QS_VARIANT(false, 128, 16, 3),  // 32-step chunks, 64 KiB stages
 };
 const Variant kBwdVariants[] = {
-    QS_VARIANT(true, 32, 4, 4),
-    QS_VARIANT(true, 32, 4, 3),
-    QS_VARIANT(true, 32, 2, 4),
-    QS_VARIANT(true, 16, 4, 4),
-    QS_VARIANT(true, 32, 8, 3),
+    QS_VARIANT(true, 128, 4, 5),    // 8-step chunks, 32 KiB stages
+    QS_VARIANT(true, 64, 4, 5),     // 16-step chunks
+    QS_VARIANT(true, 32, 4, 5),     // 32-step chunks
+    QS_VARIANT(true, 128, 4, 4),    // 8-step chunks, four stages
 };
 #undef QS_VARIANT
 constexpr int kNumFwd = sizeof(kFwdVariants) / sizeof(kFwdVariants[0]);
@@ -784,7 +927,9 @@ int ensure_workspace(int dev, cudaStream_t stream, size_t need, unsigned char **
     return QS_OK;
 }
 
-// 3-D view [B][S][HJ*4 floats] of a [B,S,H,J,4] tensor; box = boxw lanes x boxh steps.
+// 3-D view [B][S][HJ*4 floats] of a [B,S,H,J,4] tensor; box = boxw lanes x boxh
+// steps (boxes may reach past the tensor: TMA fills those cells with zeros on
+// loads and skips them on stores).
 int make_map(CUtensorMap *m, const float *ptr, int64_t B, int64_t S, int64_t HJ, int boxw, int boxh) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return QS_ERR_CUDA;
@@ -818,8 +963,9 @@ int pick_variant(bool bwd, int64_t HJ) {
     // Narrow lane groups when a batch entry has few lanes; otherwise the
     // measured fastest: 64-step tiles, 3 stages (forward), 32-step tiles,
     // 3 stages (backward).
-    if (HJ <= 16) return 3;
-    return bwd ? 1 : 2;
+    if (HJ <= 32) return 2;
+    if (HJ <= 64) return 1;
+    return 0;
 }
 
 int make_plan(bool bwd, int64_t B, int64_t S, int64_t HJ, Plan *pl) {
@@ -836,8 +982,6 @@ int make_plan(bool bwd, int64_t B, int64_t S, int64_t HJ, Plan *pl) {
     if (NG >= (1ll << 30) || C >= (1ll << 30)) return QS_ERR_DIMS;
     g.NG = (int)NG;
     g.C = (int)C;
-    g.boxw = (int)std::min<int64_t>(LT, HJ);
-    g.boxh = (int)std::min<int64_t>(T, S);
     long long batch_bytes;
     {
         std::lock_guard<std::mutex> lk(g_mu);
@@ -848,14 +992,15 @@ int make_plan(bool bwd, int64_t B, int64_t S, int64_t HJ, Plan *pl) {
     gb = std::max<long long>(1, std::min<long long>(gb, NG));
     pl->sch.GB = (int)gb;
     pl->sch.NB = (int)((NG + gb - 1) / gb);
+    pl->sch.NSB = LT / 32;
     const long long slots = C * NG;
-    pl->nitems = 2 * slots + NG;
+    pl->nitems = 2 * slots + NG * pl->sch.NSB;
     if (pl->nitems >= (1ll << 31) - (1 << 20)) return QS_ERR_DIMS;
     size_t off = sizeof(qs::WsHeader);
     pl->o_p1 = off;
     off = align_up(off + slots * 8, 256);
     pl->o_sc = off;
-    off = align_up(off + NG * 8, 256);
+    off = align_up(off + NG * pl->sch.NSB * 8, 256);
     const size_t per = (size_t)slots * LT * 16;
     pl->o_L = off;
     off = align_up(off + per, 256);
@@ -884,9 +1029,10 @@ int launch(bool bwd, const float *q, const float *d_cum, float *out, const float
     rc = ensure_workspace(dev, stream, pl.ws_bytes, &ws);
     if (rc != QS_OK) return rc;
     CUtensorMap qmap, dmap, omap;
-    rc = make_map(&qmap, q, B, S, HJ, pl.geo.boxw, pl.geo.boxh);
-    if (rc == QS_OK) rc = make_map(&omap, out, B, S, HJ, pl.geo.boxw, pl.geo.boxh);
-    if (rc == QS_OK) rc = make_map(&dmap, bwd ? d_cum : q, B, S, HJ, pl.geo.boxw, pl.geo.boxh);
+    const int bw = pl.v->bw(), T = pl.v->T();
+    rc = make_map(&qmap, q, B, S, HJ, bw, T);
+    if (rc == QS_OK) rc = make_map(&omap, out, B, S, HJ, bw, T);
+    if (rc == QS_OK) rc = make_map(&dmap, bwd ? d_cum : q, B, S, HJ, bw, T);
     if (rc != QS_OK) return rc;
     qs::Arrays arr;
     arr.p1_flags = reinterpret_cast<unsigned long long *>(ws + pl.o_p1);
@@ -1034,9 +1180,10 @@ extern "C" int quat_cumprod_debug_set_variant(int fwd_variant, int bwd_variant) 
 }
 
 // Host-side check of the work-item schedule for these sizes (both
-// directions): every P1 (chunk, group), SC (group) and P3 (chunk, group) item
-// appears exactly once, and every item comes after the items it waits on
-// (SC after all P1 items of its group, P3 after the SC item of its group).
+// directions): every P1 (chunk, group), SC (group, 32-lane block) and P3
+// (chunk, group) item appears exactly once, and every item comes after the
+// items it waits on (SC after all P1 items of its group, P3 after all SC
+// items of its group).
 extern "C" int quat_cumprod_debug_check_schedule(int64_t B, int64_t S, int64_t H, int64_t J) {
     const int dc = check_dims(B, S, H, J);
     if (dc == 1) return QS_OK;
@@ -1047,13 +1194,14 @@ extern "C" int quat_cumprod_debug_check_schedule(int64_t B, int64_t S, int64_t H
         if (rc != QS_OK) return rc;
         const long long C = pl.geo.C, NG = pl.geo.NG;
         if (pl.nitems > (1ll << 26)) return QS_ERR_DIMS;   // keep the check cheap
-        std::vector<long long> p1(C * NG, -1), p3(C * NG, -1), sc(NG, -1);
+        const long long NSB = pl.sch.NSB;
+        std::vector<long long> p1(C * NG, -1), p3(C * NG, -1), sc(NG * NSB, -1);
         for (long long id = 0; id < pl.nitems; ++id) {
             const qs::Work w = qs::decode_item((int)id, pl.geo.NG, pl.geo.C, pl.sch);
             if (w.g < 0 || w.g >= NG) return -100;
             if (w.kind == qs::KIND_SC) {
-                if (sc[w.g] != -1) return -101;
-                sc[w.g] = id;
+                if (w.sb < 0 || w.sb >= NSB || sc[w.g * NSB + w.sb] != -1) return -101;
+                sc[w.g * NSB + w.sb] = id;
                 continue;
             }
             if (w.chunk < 0 || w.chunk >= C) return -102;
@@ -1063,12 +1211,18 @@ extern "C" int quat_cumprod_debug_check_schedule(int64_t B, int64_t S, int64_t H
             slot = id;
         }
         for (long long g = 0; g < NG; ++g) {
-            if (sc[g] < 0) return -104;
+            long long first_sc = -1, last_sc = -1;
+            for (long long k = 0; k < NSB; ++k) {
+                const long long v = sc[g * NSB + k];
+                if (v < 0) return -104;
+                first_sc = (first_sc < 0 || v < first_sc) ? v : first_sc;
+                last_sc = v > last_sc ? v : last_sc;
+            }
             for (long long c = 0; c < C; ++c) {
                 const long long a = p1[c * NG + g], z = p3[c * NG + g];
                 if (a < 0 || z < 0) return -105;
-                if (a > sc[g]) return -106;
-                if (sc[g] > z) return -107;
+                if (a > first_sc) return -106;
+                if (last_sc > z) return -107;
             }
         }
     }
