@@ -70,7 +70,7 @@ constexpr int NCOMPUTE = 256;            // compute threads per CTA (8 warps)
 constexpr int PRODUCER_WARP = 8;
 constexpr int PUBLISHER_WARP = 9;
 constexpr int NTHREADS = NCOMPUTE + 64;  // + producer warp + publisher warp
-constexpr int CLAIM = 2;                 // items claimed per atomic
+constexpr int CLAIM = 4;                 // items claimed per atomic
 
 // Per-workspace control block (device memory, zero-initialised, epoch = 1).
 struct __align__(256) WsHeader {
@@ -96,10 +96,13 @@ struct Control {
     int nitems;
     int stall_item;
     unsigned long long timeout_ns;
+    int ctr_cap;   // entries of each P1 counter array
 };
 
 struct Arrays {
-    unsigned long long *p1_flags;   // [C*NG]       P1 item published
+    unsigned int *p1_count;         // [2][ctr_cap] P1 items published per lane group;
+                                    // array (epoch & 1) counts this launch, the other
+                                    // one is cleared for the next launch
     unsigned long long *sc_flags;   // [NG*NSB]     SC item published
     float4 *aggL;                   // [C*NG*LT] chunk product L_c
     float4 *aggW;                   // [C*NG*LT] chunk weighted sum W_c (backward)
@@ -272,6 +275,30 @@ __device__ __noinline__ bool wait_flags(const unsigned long long *base, long lon
     }
 }
 
+// Waits until the counter reaches `target` (relaxed polling, then one acquire
+// fence); bounded like wait_flags.
+__device__ __noinline__ bool wait_count(const unsigned int *ctr, unsigned target, uint32_t epoch,
+                                        const Control &ctl, int item) {
+    unsigned long long t0 = 0;
+    unsigned ns = 32;
+    for (int round = 0;; ++round) {
+        unsigned v;
+        asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
+        if (v >= target) {
+            fence_acquire_gpu();
+            return true;
+        }
+        if (round == 0) t0 = global_timer_ns();
+        __nanosleep(ns);
+        if (ns < 256) ns <<= 1;
+        if (launch_failed(ctl, epoch)) return false;
+        if (global_timer_ns() - t0 > ctl.timeout_ns) {
+            record_error(ctl.hdr, epoch, item);
+            return false;
+        }
+    }
+}
+
 // Waits for a phase of an intra-CTA mbarrier.  These phases depend only on
 // this CTA's own warps and TMA copies, so they complete unless something is
 // broken; the wait is still bounded (records the error, returns false).
@@ -343,6 +370,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     float4 *s_seg = s_car + NST * NRES * LT;                                      // [2][NRES][NSEG][LT]
     __shared__ __align__(8) uint64_t full_bar[NST], done_bar[NST], empty_bar[NST];
     __shared__ int s_items[NST];
+    __shared__ int4 s_work[NST];   // decoded item: kind, chunk, group, 32-lane block
     __shared__ int s_end_seq;
     __shared__ int s_abort;   // set when an intra-CTA wait ran out: every role stops
 
@@ -351,6 +379,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int HJ = geo.HJ, NG = geo.NG, C = geo.C;
     const unsigned long long flag_val = pack_flag(epoch);
 
+    {   // clear the other counter array for the next launch on this workspace
+        unsigned int *next = arr.p1_count + ((epoch + 1u) & 1u) * ctl.ctr_cap;
+        for (int i = blockIdx.x * NTHREADS + tid; i < ctl.ctr_cap; i += gridDim.x * NTHREADS) next[i] = 0u;
+    }
     if (tid == 0) {
         for (int s = 0; s < NST; ++s) {
             mbar_init(&full_bar[s], 2);                 // issue + fetch
@@ -407,6 +439,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                         const Work w = decode_item(it, NG, C, sch);
                         if (wl == 0) {
                             s_items[s] = it;
+                            s_work[s] = make_int4(w.kind, w.chunk, w.g, w.sb);
                             if (w.kind == KIND_SC) {
                                 mbar_arrive(&full_bar[s]);
                             } else {
@@ -430,7 +463,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             if (seq_fetch < seq_issue) {
                 const int s = seq_fetch % NST;
                 const int it = s_items[s];
-                const Work w = decode_item(it, NG, C, sch);
+                const int4 wk = s_work[s];
+                const Work w{wk.x, wk.y, wk.z, wk.w};
                 bool ready = true;
                 if (w.kind == KIND_P3) {
                     // all 32-lane blocks of the group must have been scanned
@@ -498,6 +532,19 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     } else if (warp == PUBLISHER_WARP) {
         // ================= publisher: P1 aggregates, P3 stores, free stages =====
         if (wl == 0) prefetch_tensormap(&omap);
+        unsigned int *cnt = arr.p1_count + (epoch & 1u) * ctl.ctr_cap;
+        int pend[NST + 1];   // lane groups of P1 items written but not yet counted
+        int npend = 0;
+        // One fence makes every aggregate written so far visible, then each
+        // pending P1 item is counted for its lane group.
+        auto flush_pending = [&]() {
+            if (npend == 0) return;
+            __threadfence();
+            __syncwarp();
+            if (wl == 0)
+                for (int k = 0; k < npend; ++k) atomicAdd(cnt + pend[k], 1u);
+            npend = 0;
+        };
         for (int seq = 0;; ++seq) {
             const int s = seq % NST;
             const uint32_t par = (seq / NST) & 1;
@@ -508,6 +555,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     have = true;
                     break;
                 }
+                flush_pending();   // nothing else to do: publish what is pending
                 if (*reinterpret_cast<volatile int *>(&s_end_seq) == seq) break;
                 if (*reinterpret_cast<volatile int *>(&s_abort)) break;
                 __nanosleep(32);
@@ -522,23 +570,23 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             }
             if (!have) break;
             const int it = s_items[s];
-            const Work w = decode_item(it, NG, C, sch);
+            const int4 wk = s_work[s];
+            const Work w{wk.x, wk.y, wk.z, wk.w};
             if (w.kind == KIND_P1) {
                 const long long base = (static_cast<long long>(w.chunk) * NG + w.g) * LT;
                 for (int l = wl; l < LT; l += 32) {
                     __stcg(arr.aggL + base + l, s_res[(s * NRES + 0) * LT + l]);
                     if (BWD) __stcg(arr.aggW + base + l, s_res[(s * NRES + 1) * LT + l]);
                 }
-                __threadfence();
-                __syncwarp();
-                if (wl == 0 && it != ctl.stall_item)
-                    st_release_u64(arr.p1_flags + static_cast<long long>(w.chunk) * NG + w.g, flag_val);
+                // Counted (and fenced) later, in a batch: see flush_pending.
+                if (it != ctl.stall_item) pend[npend++] = w.g;
             } else if (w.kind == KIND_P3 && wl == 0) {
                 const int b = w.g / geo.NGb, gx = w.g - b * geo.NGb, nb = nboxes(gx);
                 const unsigned char *src = smem + size_t(s) * STAGE + (BWD ? HALF : 0);
                 for (int j = 0; j < nb; ++j)
                     tma_store_3d(&omap, src + j * BOXB, (gx * LT + j * BW) * 4, w.chunk * T, b);
             }
+            if (npend >= NST) flush_pending();
             if (wl == 0) {
                 bulk_commit_group();            // one bulk group per item
                 if (seq >= 1) {
@@ -548,6 +596,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             }
             __syncwarp();
         }
+        flush_pending();
         if (wl == 0) bulk_wait_group_all();
     } else {
         // ================= compute warps =========================================
@@ -564,7 +613,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             }
             const int item = s_items[s];
             if (item < 0) break;
-            const Work w = decode_item(item, NG, C, sch);
+            const int4 wk = s_work[s];
+            const Work w{wk.x, wk.y, wk.z, wk.w};
             const int par = seq & 1;
             float4 *sa = s_seg + (par * NRES + 0) * NCOMPUTE;      // [NSEG][LT]
             float4 *sw = s_seg + (par * NRES + (BWD ? 1 : 0)) * NCOMPUTE;
@@ -597,9 +647,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 }
             } else if (w.kind == KIND_SC) {
                 // ---- scan of one 32-lane block's chunk aggregates ----------------
-                wait_flags(arr.p1_flags + w.g, NG, ctid, C, NCOMPUTE, epoch, ctl, item);
+                wait_count(arr.p1_count + (epoch & 1u) * ctl.ctr_cap + w.g, static_cast<unsigned>(C), epoch, ctl,
+                           item);
                 named_bar_sync(1, NCOMPUTE);
-                constexpr int U = 8;    // aggregates loaded per batch (independent loads)
+                constexpr int U = BWD ? 8 : 16;   // aggregates loaded per batch (independent loads)
                 constexpr int RT = NCOMPUTE / 32;   // threads per lane (chunk ranges)
                 const int sl = ctid & 31, rg = ctid >> 5;   // lane in the block, range
                 const int l = w.sb * 32 + sl;               // lane in the group
@@ -763,16 +814,16 @@ struct Variant {
 #define QS_VARIANT(B, LT, N, NS) \
     Variant { reinterpret_cast<KernelFn>(qs::quat_scan_kernel<B, LT, N, NS>), B, LT, N, NS }
 const Variant kFwdVariants[] = {
-    QS_VARIANT(false, 128, 8, 5),   // 16-step chunks, 32 KiB stages
-    QS_VARIANT(false, 64, 8, 5),    // 32-step chunks
-    QS_VARIANT(false, 32, 8, 4),    // 64-step chunks
     QS_VARIANT(false, 128, 16, 3),  // 32-step chunks, 64 KiB stages
+    QS_VARIANT(false, 64, 16, 3),   // 64-step chunks, 64 KiB stages
+    QS_VARIANT(false, 32, 8, 4),    // 64-step chunks, 32 KiB stages
+    QS_VARIANT(false, 128, 8, 5),   // 16-step chunks, 32 KiB stages
 };
 const Variant kBwdVariants[] = {
-    QS_VARIANT(true, 128, 4, 5),    // 8-step chunks, 32 KiB stages
-    QS_VARIANT(true, 64, 4, 5),     // 16-step chunks
-    QS_VARIANT(true, 32, 4, 5),     // 32-step chunks
-    QS_VARIANT(true, 128, 4, 4),    // 8-step chunks, four stages
+    QS_VARIANT(true, 64, 8, 3),     // 32-step chunks, 64 KiB stages
+    QS_VARIANT(true, 32, 8, 3),     // 64-step chunks, 64 KiB stages
+    QS_VARIANT(true, 64, 4, 5),     // 16-step chunks, 32 KiB stages
+    QS_VARIANT(true, 32, 4, 5),     // 32-step chunks, 32 KiB stages
 };
 #undef QS_VARIANT
 constexpr int kNumFwd = sizeof(kFwdVariants) / sizeof(kFwdVariants[0]);
@@ -792,10 +843,16 @@ struct DevInfo {
 };
 std::map<int, DevInfo> g_dev;
 
+// Library-owned scratch of one (device, stream): control block, the two P1
+// counter arrays (fixed capacity, so that a launch can clear the array of
+// the next launch whatever its sizes), then the per-launch arrays.
 struct Workspace {
     unsigned char *base = nullptr;
     size_t bytes = 0;
+    int ctr_cap = 0;
 };
+
+size_t counters_end(int ctr_cap) { return 256 + ((size_t(8) * ctr_cap + 255) / 256) * 256; }
 std::map<std::pair<int, uintptr_t>, Workspace> g_ws;
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
@@ -882,14 +939,19 @@ int device_info(DevInfo **out, int *dev_out) {
     return QS_OK;
 }
 
-// Returns the workspace of (device, stream) with at least `need` bytes.
-int ensure_workspace(int dev, cudaStream_t stream, size_t need, unsigned char **out) {
+// Returns the workspace of (device, stream) with room for `plan_bytes` of
+// per-launch arrays and at least `ng` counters per array.
+int ensure_workspace(int dev, cudaStream_t stream, size_t plan_bytes, int ng, unsigned char **out, int *ctr_cap) {
     std::lock_guard<std::mutex> lk(g_mu);
     Workspace &w = g_ws[{dev, reinterpret_cast<uintptr_t>(stream)}];
-    if (w.bytes >= need) {
+    if (w.ctr_cap >= ng && w.bytes >= counters_end(w.ctr_cap) + plan_bytes) {
         *out = w.base;
+        *ctr_cap = w.ctr_cap;
         return QS_OK;
     }
+    int cap = std::max(w.ctr_cap, 4096);
+    while (cap < ng) cap *= 2;
+    const size_t need = counters_end(cap) + plan_bytes;
     cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
     if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) {
         cudaGetLastError();
@@ -923,7 +985,9 @@ int ensure_workspace(int dev, cudaStream_t stream, size_t need, unsigned char **
     }
     w.base = static_cast<unsigned char *>(p);
     w.bytes = bytes;
+    w.ctr_cap = cap;
     *out = w.base;
+    *ctr_cap = cap;
     return QS_OK;
 }
 
@@ -950,7 +1014,7 @@ struct Plan {
     qs::Geometry geo{};
     qs::Schedule sch{};
     long long nitems = 0;
-    size_t o_p1 = 0, o_sc = 0, o_L = 0, o_W = 0, o_F = 0, o_H = 0, ws_bytes = 0;
+    size_t o_sc = 0, o_L = 0, o_W = 0, o_F = 0, o_H = 0, ws_bytes = 0;   // offsets past the counters
 };
 
 int pick_variant(bool bwd, int64_t HJ) {
@@ -963,8 +1027,8 @@ int pick_variant(bool bwd, int64_t HJ) {
     // Narrow lane groups when a batch entry has few lanes; otherwise the
     // measured fastest: 64-step tiles, 3 stages (forward), 32-step tiles,
     // 3 stages (backward).
-    if (HJ <= 32) return 2;
-    if (HJ <= 64) return 1;
+    if (HJ <= 32) return bwd ? 1 : 2;
+    if (HJ <= 64) return bwd ? 0 : 1;
     return 0;
 }
 
@@ -996,9 +1060,7 @@ int make_plan(bool bwd, int64_t B, int64_t S, int64_t HJ, Plan *pl) {
     const long long slots = C * NG;
     pl->nitems = 2 * slots + NG * pl->sch.NSB;
     if (pl->nitems >= (1ll << 31) - (1 << 20)) return QS_ERR_DIMS;
-    size_t off = sizeof(qs::WsHeader);
-    pl->o_p1 = off;
-    off = align_up(off + slots * 8, 256);
+    size_t off = 0;
     pl->o_sc = off;
     off = align_up(off + NG * pl->sch.NSB * 8, 256);
     const size_t per = (size_t)slots * LT * 16;
@@ -1026,8 +1088,10 @@ int launch(bool bwd, const float *q, const float *d_cum, float *out, const float
     rc = make_plan(bwd, B, S, HJ, &pl);
     if (rc != QS_OK) return rc;
     unsigned char *ws = nullptr;
-    rc = ensure_workspace(dev, stream, pl.ws_bytes, &ws);
+    int ctr_cap = 0;
+    rc = ensure_workspace(dev, stream, pl.ws_bytes, pl.geo.NG, &ws, &ctr_cap);
     if (rc != QS_OK) return rc;
+    unsigned char *data = ws + counters_end(ctr_cap);
     CUtensorMap qmap, dmap, omap;
     const int bw = pl.v->bw(), T = pl.v->T();
     rc = make_map(&qmap, q, B, S, HJ, bw, T);
@@ -1035,12 +1099,12 @@ int launch(bool bwd, const float *q, const float *d_cum, float *out, const float
     if (rc == QS_OK) rc = make_map(&dmap, bwd ? d_cum : q, B, S, HJ, bw, T);
     if (rc != QS_OK) return rc;
     qs::Arrays arr;
-    arr.p1_flags = reinterpret_cast<unsigned long long *>(ws + pl.o_p1);
-    arr.sc_flags = reinterpret_cast<unsigned long long *>(ws + pl.o_sc);
-    arr.aggL = reinterpret_cast<float4 *>(ws + pl.o_L);
-    arr.carF = reinterpret_cast<float4 *>(ws + pl.o_F);
-    arr.aggW = bwd ? reinterpret_cast<float4 *>(ws + pl.o_W) : nullptr;
-    arr.carH = bwd ? reinterpret_cast<float4 *>(ws + pl.o_H) : nullptr;
+    arr.p1_count = reinterpret_cast<unsigned int *>(ws + 256);
+    arr.sc_flags = reinterpret_cast<unsigned long long *>(data + pl.o_sc);
+    arr.aggL = reinterpret_cast<float4 *>(data + pl.o_L);
+    arr.carF = reinterpret_cast<float4 *>(data + pl.o_F);
+    arr.aggW = bwd ? reinterpret_cast<float4 *>(data + pl.o_W) : nullptr;
+    arr.carH = bwd ? reinterpret_cast<float4 *>(data + pl.o_H) : nullptr;
     qs::Control ctl;
     {
         std::lock_guard<std::mutex> lk(g_mu);
@@ -1049,6 +1113,7 @@ int launch(bool bwd, const float *q, const float *d_cum, float *out, const float
     }
     ctl.hdr = reinterpret_cast<qs::WsHeader *>(ws);
     ctl.nitems = (int)pl.nitems;
+    ctl.ctr_cap = ctr_cap;
     const int blocks = bwd ? di->bwd_blocks[pl.vidx] : di->fwd_blocks[pl.vidx];
     const int grid = (int)std::min<long long>(pl.nitems, (long long)di->sms * blocks);
     const float4 *init4 = reinterpret_cast<const float4 *>(init);
