@@ -123,7 +123,8 @@ int quat_cumprod_debug_stall_tile(int64_t tile);
  * quat_cumprod_debug_set_batch_bytes sets the target input bytes per batch
  * (default 24 MiB; <= 0 restores it).  quat_cumprod_debug_set_variant selects
  * a compiled tile configuration (index into the library's variant table, -1 =
- * automatic; QS_ERR_DIMS for an unknown index).  Both are process-wide and
+ * automatic; QS_ERR_DIMS for an unknown index; a configuration that does not
+ * apply to a call's sizes is replaced by the automatic choice).  Both are process-wide and
  * return QS_OK.  quat_cumprod_debug_check_schedule verifies on the host,
  * without a GPU, that the work-item order of both directions for these sizes
  * visits every item once and puts every item after the items it waits on

@@ -335,7 +335,7 @@ __device__ __forceinline__ void finish_launch(const Control &ctl, uint32_t epoch
 __host__ __device__ constexpr size_t smem_bytes(bool bwd, int lt, int n, int nst) {
     return 1024                                                        // alignment slack
            + size_t(nst) * (bwd ? 2 : 1) * (NCOMPUTE / lt) * n * lt * 16  // stages
-           + size_t(2) * nst * (bwd ? 2 : 1) * lt * 16                  // P1 results, P3 carries
+           + size_t(nst) * (bwd ? 2 : 1) * lt * 16                      // per-stage result / carry slot
            + size_t(2) * NCOMPUTE * 16 * (bwd ? 2 : 1);                  // segment results (2 parities)
 }
 
@@ -355,19 +355,20 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     constexpr int T = NSEG * N;
     static_assert(T <= 256, "TMA box height");
     static_assert(smem_bytes(BWD, LT, N, NST) <= 226 * 1024, "shared memory per CTA");
-    constexpr int BW = LT < 64 ? LT : 64;                  // lanes per TMA box
-    constexpr int NBOX = LT / BW;
-    constexpr uint32_t BOXB = T * BW * 16;                  // bytes of one box
-    constexpr uint32_t HALF = NBOX * BOXB;                  // one operand of a stage
+    // One TMA box per operand: [T rows][LT lanes], row-major.  128-lane groups
+    // use a 4-D view (64-lane blocks), narrower groups a 3-D view.
+    constexpr bool MAP4 = LT == 128;
+    constexpr uint32_t HALF = T * LT * 16;                  // one operand of a stage
     constexpr uint32_t STAGE = BWD ? 2 * HALF : HALF;
     constexpr int NRES = BWD ? 2 : 1;
 
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem = align1024(smem_raw);
     // [stages][P1 results][P3 carries][segment results]
-    float4 *s_res = reinterpret_cast<float4 *>(smem + size_t(NST) * STAGE);       // [NST][NRES][LT]
-    float4 *s_car = s_res + NST * NRES * LT;                                      // [NST][NRES][LT]
-    float4 *s_seg = s_car + NST * NRES * LT;                                      // [2][NRES][NSEG][LT]
+    // Per-stage slot: the P1 results of a stage's item (compute -> publisher),
+    // or the carries of its P3 item (producer -> compute).
+    float4 *s_rc = reinterpret_cast<float4 *>(smem + size_t(NST) * STAGE);        // [NST][NRES][LT]
+    float4 *s_seg = s_rc + NST * NRES * LT;                                       // [2][NRES][NSEG][LT]
     __shared__ __align__(8) uint64_t full_bar[NST], done_bar[NST], empty_bar[NST];
     __shared__ int s_items[NST];
     __shared__ int4 s_work[NST];   // decoded item: kind, chunk, group, 32-lane block
@@ -395,10 +396,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
     __syncthreads();
 
-    auto nboxes = [&](int gx) {   // boxes of group column gx that hold lanes
-        const int rem = HJ - gx * LT;
-        return rem >= LT ? NBOX : (rem + BW - 1) / BW;
-    };
 
     if (warp == PRODUCER_WARP) {
         // ================= producer: claims, TMA loads, carries =================
@@ -413,12 +410,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         for (;;) {
             if (*reinterpret_cast<volatile int *>(&s_abort)) break;
             bool prog = false;
-            // -- issue the next item into a free stage --
-            if (!ended) {
+            // -- issue items into free stages --
+            while (!ended) {
                 const int s = seq_issue % NST;
                 const bool free_stage =
                     seq_issue < NST || mbar_test_wait(&empty_bar[s], ((seq_issue / NST) - 1) & 1);
-                if (free_stage) {
+                if (!free_stage) break;
+                {
                     if (claim_left == 0) {
                         int c0 = 0;
                         if (wl == 0) c0 = static_cast<int>(atomicAdd(&ctl.hdr->counter, (unsigned)CLAIM));
@@ -443,13 +441,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                             if (w.kind == KIND_SC) {
                                 mbar_arrive(&full_bar[s]);
                             } else {
-                                const int b = w.g / geo.NGb, gx = w.g - b * geo.NGb, nb = nboxes(gx);
+                                const int b = w.g / geo.NGb, gx = w.g - b * geo.NGb;
                                 unsigned char *dst = smem + size_t(s) * STAGE;
-                                mbar_arrive_expect_tx(&full_bar[s], (BWD ? 2u : 1u) * nb * BOXB);
-                                for (int j = 0; j < nb; ++j) {
-                                    const int x = (gx * LT + j * BW) * 4;
-                                    tma_load_3d(dst + j * BOXB, &qmap, x, w.chunk * T, b, &full_bar[s]);
-                                    if (BWD) tma_load_3d(dst + HALF + j * BOXB, &dmap, x, w.chunk * T, b, &full_bar[s]);
+                                mbar_arrive_expect_tx(&full_bar[s], STAGE);
+                                if (MAP4) {
+                                    tma_load_4d(dst, &qmap, 0, gx * 2, w.chunk * T, b, &full_bar[s]);
+                                    if (BWD) tma_load_4d(dst + HALF, &dmap, 0, gx * 2, w.chunk * T, b, &full_bar[s]);
+                                } else {
+                                    tma_load_3d(dst, &qmap, gx * LT * 4, w.chunk * T, b, &full_bar[s]);
+                                    if (BWD) tma_load_3d(dst + HALF, &dmap, gx * LT * 4, w.chunk * T, b, &full_bar[s]);
                                 }
                             }
                         }
@@ -485,8 +485,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                         fence_acquire_gpu();
                         const long long base = (static_cast<long long>(w.chunk) * NG + w.g) * LT;
                         for (int l = wl; l < LT; l += 32) {
-                            s_car[(s * NRES + 0) * LT + l] = give_up ? q_nan() : __ldcg(arr.carF + base + l);
-                            if (BWD) s_car[(s * NRES + 1) * LT + l] = give_up ? q_nan() : __ldcg(arr.carH + base + l);
+                            s_rc[(s * NRES + 0) * LT + l] = give_up ? q_nan() : __ldcg(arr.carF + base + l);
+                            if (BWD) s_rc[(s * NRES + 1) * LT + l] = give_up ? q_nan() : __ldcg(arr.carH + base + l);
                         }
                         ready = true;
                         idle_since = 0;
@@ -575,24 +575,26 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             if (w.kind == KIND_P1) {
                 const long long base = (static_cast<long long>(w.chunk) * NG + w.g) * LT;
                 for (int l = wl; l < LT; l += 32) {
-                    __stcg(arr.aggL + base + l, s_res[(s * NRES + 0) * LT + l]);
-                    if (BWD) __stcg(arr.aggW + base + l, s_res[(s * NRES + 1) * LT + l]);
+                    __stcg(arr.aggL + base + l, s_rc[(s * NRES + 0) * LT + l]);
+                    if (BWD) __stcg(arr.aggW + base + l, s_rc[(s * NRES + 1) * LT + l]);
                 }
                 // Counted (and fenced) later, in a batch: see flush_pending.
                 if (it != ctl.stall_item) pend[npend++] = w.g;
             } else if (w.kind == KIND_P3 && wl == 0) {
-                const int b = w.g / geo.NGb, gx = w.g - b * geo.NGb, nb = nboxes(gx);
+                const int b = w.g / geo.NGb, gx = w.g - b * geo.NGb;
                 const unsigned char *src = smem + size_t(s) * STAGE + (BWD ? HALF : 0);
-                for (int j = 0; j < nb; ++j)
-                    tma_store_3d(&omap, src + j * BOXB, (gx * LT + j * BW) * 4, w.chunk * T, b);
+                if (MAP4)
+                    tma_store_4d(&omap, src, 0, gx * 2, w.chunk * T, b);
+                else
+                    tma_store_3d(&omap, src, gx * LT * 4, w.chunk * T, b);
             }
             if (npend >= NST) flush_pending();
             if (wl == 0) {
-                bulk_commit_group();            // one bulk group per item
-                if (seq >= 1) {
-                    bulk_wait_group_read<1>();  // the previous item's store has read its stage
-                    mbar_arrive(&empty_bar[(seq - 1) % NST]);
+                if (w.kind == KIND_P3) {
+                    bulk_commit_group();
+                    bulk_wait_group_read<0>();  // the store has read the stage
                 }
+                mbar_arrive(&empty_bar[s]);
             }
             __syncwarp();
         }
@@ -602,7 +604,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         // ================= compute warps =========================================
         const int ctid = tid;                  // 0..255
         const int lane = ctid % LT, seg = ctid / LT;
-        const int box = lane / BW, col = lane - box * BW;
         for (int seq = 0;; ++seq) {
             const int s = seq % NST;
             const bool ok = wait_bar(&full_bar[s], (seq / NST) & 1, 4 * ctl.timeout_ns, ctl, epoch, -1);
@@ -620,15 +621,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             float4 *sw = s_seg + (par * NRES + (BWD ? 1 : 0)) * NCOMPUTE;
             float4 *Qt = reinterpret_cast<float4 *>(smem + size_t(s) * STAGE);
             float4 *Dt = reinterpret_cast<float4 *>(smem + size_t(s) * STAGE + HALF);
-            const int cell0 = box * (T * BW) + seg * N * BW + col;   // this thread's first step
+            const int cell0 = seg * N * LT + lane;   // this thread's first step
 
             if (w.kind == KIND_P1) {
                 // ---- chunk aggregates --------------------------------------------
                 float4 loc = q_ident(), W = q_zero();
 #pragma unroll
                 for (int i = 0; i < N; ++i) {
-                    loc = q_mul(Qt[cell0 + i * BW], loc);
-                    if (BWD) W = q_add(W, q_mul_cl(loc, Dt[cell0 + i * BW]));
+                    loc = q_mul(Qt[cell0 + i * LT], loc);
+                    if (BWD) W = q_add(W, q_mul_cl(loc, Dt[cell0 + i * LT]));
                 }
                 sa[seg * LT + lane] = loc;
                 if (BWD) sw[seg * LT + lane] = W;
@@ -637,12 +638,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     float4 L = q_ident();
 #pragma unroll
                     for (int k = 0; k < NSEG; ++k) L = q_mul(sa[k * LT + lane], L);
-                    s_res[(s * NRES + 0) * LT + lane] = L;
+                    s_rc[(s * NRES + 0) * LT + lane] = L;
                     if (BWD) {
                         float4 V = q_zero();
 #pragma unroll
                         for (int k = NSEG - 1; k >= 0; --k) V = q_add(sw[k * LT + lane], q_mul_cl(sa[k * LT + lane], V));
-                        s_res[(s * NRES + 1) * LT + lane] = V;
+                        s_rc[(s * NRES + 1) * LT + lane] = V;
                     }
                 }
             } else if (w.kind == KIND_SC) {
@@ -734,13 +735,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     st_release_u64(arr.sc_flags + static_cast<long long>(w.g) * sch.NSB + w.sb, flag_val);
             } else {
                 // ---- apply the carries, write the outputs in place ---------------
-                const float4 F = s_car[(s * NRES + 0) * LT + lane];
+                const float4 F = s_rc[(s * NRES + 0) * LT + lane];
                 if (!BWD) {
                     float4 x[N];
                     float4 loc = q_ident();
 #pragma unroll
                     for (int i = 0; i < N; ++i) {
-                        loc = q_mul(Qt[cell0 + i * BW], loc);
+                        loc = q_mul(Qt[cell0 + i * LT], loc);
                         x[i] = loc;
                     }
                     sa[seg * LT + lane] = loc;
@@ -748,30 +749,30 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     float4 X = F;   // cum just before this segment
                     for (int k = 0; k < seg; ++k) X = q_mul(sa[k * LT + lane], X);
 #pragma unroll
-                    for (int i = 0; i < N; ++i) Qt[cell0 + i * BW] = q_mul(x[i], X);
+                    for (int i = 0; i < N; ++i) Qt[cell0 + i * LT] = q_mul(x[i], X);
                 } else {
                     float4 lp[N];
                     float4 loc = q_ident(), W = q_zero();
 #pragma unroll
                     for (int i = 0; i < N; ++i) {
                         lp[i] = loc;
-                        loc = q_mul(Qt[cell0 + i * BW], loc);
-                        W = q_add(W, q_mul_cl(loc, Dt[cell0 + i * BW]));
+                        loc = q_mul(Qt[cell0 + i * LT], loc);
+                        W = q_add(W, q_mul_cl(loc, Dt[cell0 + i * LT]));
                     }
                     sa[seg * LT + lane] = loc;
                     sw[seg * LT + lane] = W;
                     named_bar_sync(1, NCOMPUTE);
                     float4 X = F;
                     for (int k = 0; k < seg; ++k) X = q_mul(sa[k * LT + lane], X);
-                    float4 Hn = s_car[(s * NRES + 1) * LT + lane];
+                    float4 Hn = s_rc[(s * NRES + 1) * LT + lane];
                     for (int k = NSEG - 1; k > seg; --k) Hn = q_add(sw[k * LT + lane], q_mul_cl(sa[k * LT + lane], Hn));
                     // Reverse pass: G = d_cum + H, d_q = G (x) conj(cum[t-1]),
                     // H = conj(q_t) (x) G handed to step t-1.
 #pragma unroll
                     for (int i = N - 1; i >= 0; --i) {
-                        const float4 qv = Qt[cell0 + i * BW];
-                        const float4 G = q_add(Dt[cell0 + i * BW], Hn);
-                        Dt[cell0 + i * BW] = q_mul_cr(G, q_mul(lp[i], X));
+                        const float4 qv = Qt[cell0 + i * LT];
+                        const float4 G = q_add(Dt[cell0 + i * LT], Hn);
+                        Dt[cell0 + i * LT] = q_mul_cr(G, q_mul(lp[i], X));
                         Hn = q_mul_cl(qv, G);
                     }
                 }
@@ -807,23 +808,23 @@ struct Variant {
     bool bwd;
     int lt, n, nstage;
     int T() const { return (qs::NCOMPUTE / lt) * n; }
-    int bw() const { return lt < 64 ? lt : 64; }
     size_t smem() const { return qs::smem_bytes(bwd, lt, n, nstage); }
 };
 
 #define QS_VARIANT(B, LT, N, NS) \
     Variant { reinterpret_cast<KernelFn>(qs::quat_scan_kernel<B, LT, N, NS>), B, LT, N, NS }
+// 128-lane configurations need H*J to be a multiple of 64 (4-D TMA view).
 const Variant kFwdVariants[] = {
-    QS_VARIANT(false, 128, 16, 3),  // 32-step chunks, 64 KiB stages
-    QS_VARIANT(false, 64, 16, 3),   // 64-step chunks, 64 KiB stages
-    QS_VARIANT(false, 32, 8, 4),    // 64-step chunks, 32 KiB stages
-    QS_VARIANT(false, 128, 8, 5),   // 16-step chunks, 32 KiB stages
+    QS_VARIANT(false, 128, 8, 6),   // 16-step chunks, 6 x 32 KiB stages
+    QS_VARIANT(false, 64, 8, 6),    // 32-step chunks, 6 x 32 KiB stages
+    QS_VARIANT(false, 32, 8, 6),    // 64-step chunks, 6 x 32 KiB stages
+    QS_VARIANT(false, 128, 16, 3),  // 32-step chunks, 3 x 64 KiB stages
 };
 const Variant kBwdVariants[] = {
-    QS_VARIANT(true, 64, 8, 3),     // 32-step chunks, 64 KiB stages
-    QS_VARIANT(true, 32, 8, 3),     // 64-step chunks, 64 KiB stages
-    QS_VARIANT(true, 64, 4, 5),     // 16-step chunks, 32 KiB stages
-    QS_VARIANT(true, 32, 4, 5),     // 32-step chunks, 32 KiB stages
+    QS_VARIANT(true, 64, 4, 6),     // 16-step chunks, 6 x 32 KiB stages
+    QS_VARIANT(true, 32, 4, 6),     // 32-step chunks, 6 x 32 KiB stages
+    QS_VARIANT(true, 128, 4, 5),    // 8-step chunks, 5 x 32 KiB stages
+    QS_VARIANT(true, 64, 8, 3),     // 32-step chunks, 3 x 64 KiB stages
 };
 #undef QS_VARIANT
 constexpr int kNumFwd = sizeof(kFwdVariants) / sizeof(kFwdVariants[0]);
@@ -991,10 +992,25 @@ int ensure_workspace(int dev, cudaStream_t stream, size_t plan_bytes, int ng, un
     return QS_OK;
 }
 
-// 3-D view [B][S][HJ*4 floats] of a [B,S,H,J,4] tensor; box = boxw lanes x boxh
-// steps (boxes may reach past the tensor: TMA fills those cells with zeros on
-// loads and skips them on stores).
-int make_map(CUtensorMap *m, const float *ptr, int64_t B, int64_t S, int64_t HJ, int boxw, int boxh) {
+// View of a [B,S,H,J,4] tensor for TMA boxes of `lt` lanes x `boxh` steps.
+// lt <= 64: 3-D view [B][S][HJ*4 floats].  lt == 128 (HJ a multiple of 64):
+// 4-D view [B][S][HJ/64][64*4 floats], boxes of two 64-lane blocks.  Boxes may
+// reach past the tensor: TMA fills those cells with zeros on loads and skips
+// them on stores.
+int make_map(CUtensorMap *m, const float *ptr, int64_t B, int64_t S, int64_t HJ, int lt, int boxh) {
+    if (lt == 128) {
+        EncodeTiledFn fn = encode_fn();
+        if (!fn) return QS_ERR_CUDA;
+        cuuint64_t dims[4] = {256, (cuuint64_t)(HJ / 64), (cuuint64_t)S, (cuuint64_t)B};
+        cuuint64_t strides[3] = {1024, (cuuint64_t)(HJ * 16), (cuuint64_t)(S * HJ * 16)};
+        cuuint32_t box[4] = {256, 2, (cuuint32_t)boxh, 1};
+        cuuint32_t estr[4] = {1, 1, 1, 1};
+        CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<float *>(ptr), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        return r == CUDA_SUCCESS ? QS_OK : QS_ERR_CUDA;
+    }
+    const int boxw = lt;
     EncodeTiledFn fn = encode_fn();
     if (!fn) return QS_ERR_CUDA;
     cuuint64_t dims[3] = {(cuuint64_t)(HJ * 4), (cuuint64_t)S, (cuuint64_t)B};
@@ -1023,14 +1039,14 @@ int pick_variant(bool bwd, int64_t HJ) {
         std::lock_guard<std::mutex> lk(g_mu);
         forced = bwd ? g_bwd_variant : g_fwd_variant;
     }
-    if (forced >= 0) return forced;
-    // Narrow lane groups when a batch entry has few lanes; otherwise the
-    // measured fastest: 64-step tiles, 3 stages (forward), 32-step tiles,
-    // 3 stages (backward).
-    if (HJ <= 32) return bwd ? 1 : 2;
-    if (HJ <= 64) return bwd ? 0 : 1;
-    return 0;
+    const Variant *table = bwd ? kBwdVariants : kFwdVariants;
+    const int count = bwd ? kNumBwd : kNumFwd;
+    if (forced >= 0 && forced < count && (table[forced].lt != 128 || HJ % 64 == 0)) return forced;
+    if (!bwd && HJ >= 128 && HJ % 64 == 0) return 0;
+    if (HJ >= 64) return bwd ? 0 : 1;
+    return bwd ? 1 : 2;
 }
+
 
 int make_plan(bool bwd, int64_t B, int64_t S, int64_t HJ, Plan *pl) {
     pl->vidx = pick_variant(bwd, HJ);
@@ -1093,10 +1109,10 @@ int launch(bool bwd, const float *q, const float *d_cum, float *out, const float
     if (rc != QS_OK) return rc;
     unsigned char *data = ws + counters_end(ctr_cap);
     CUtensorMap qmap, dmap, omap;
-    const int bw = pl.v->bw(), T = pl.v->T();
-    rc = make_map(&qmap, q, B, S, HJ, bw, T);
-    if (rc == QS_OK) rc = make_map(&omap, out, B, S, HJ, bw, T);
-    if (rc == QS_OK) rc = make_map(&dmap, bwd ? d_cum : q, B, S, HJ, bw, T);
+    const int lt = pl.v->lt, T = pl.v->T();
+    rc = make_map(&qmap, q, B, S, HJ, lt, T);
+    if (rc == QS_OK) rc = make_map(&omap, out, B, S, HJ, lt, T);
+    if (rc == QS_OK) rc = make_map(&dmap, bwd ? d_cum : q, B, S, HJ, lt, T);
     if (rc != QS_OK) return rc;
     qs::Arrays arr;
     arr.p1_count = reinterpret_cast<unsigned int *>(ws + 256);
