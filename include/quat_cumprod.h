@@ -33,12 +33,12 @@
  * Streams: `stream` is a cudaStream_t (NULL = the legacy default stream).
  * Every call is asynchronous: it validates arguments, enqueues its work on
  * `stream` and returns.  Launch failures are returned at once; a failure that
- * happens on the device (a cross-tile wait that ran out) is recorded in a
- * per-stream device word and reported by quat_cumprod_status().
+ * happens on the device (a wait that ran out) is recorded in a per-stream
+ * device word and reported by quat_cumprod_status().
  *
  * Scratch memory: both calls use a library-owned workspace per (device,
- * stream) for per-chunk aggregates, carries and flags (about 32 bytes (forward)
- * or 64 bytes (backward) per lane and chunk of 32 steps).  The first call on a stream, and
+ * stream) for per-chunk aggregates and carries (32 bytes per lane and chunk
+ * of 64 steps forward, 64 bytes backward).  The first call on a stream, and
  * any later call that needs a larger workspace, allocates it (cudaMalloc) and
  * synchronizes that stream; issue such a call before capturing the stream
  * into a CUDA graph.  Calls on one stream are ordered by the stream; calls on
@@ -66,7 +66,7 @@ enum {
     QS_ERR_MISALIGNED = -3,  /* a pointer is not 16-byte aligned                */
     QS_ERR_ALIAS = -4,       /* an output overlaps an input                     */
     QS_ERR_CUDA = -5,        /* a CUDA runtime call failed (launch, memset...)  */
-    QS_ERR_TIMEOUT = -6,     /* a cross-tile wait on the device ran out         */
+    QS_ERR_TIMEOUT = -6,     /* a wait on the device ran out                    */
     QS_ERR_NOMEM = -7,       /* workspace allocation failed, or it would have to
                                 grow while the stream is being captured         */
     QS_ERR_DEVICE = -8       /* the current device is not compute capability 10.3 */
@@ -108,32 +108,18 @@ const char *quat_cumprod_strerror(int status);
 
 /*
  * Test hooks.  quat_cumprod_debug_set_timeout_ns sets the limit of every
- * cross-tile wait on the device (default 2 s; values <= 0 restore it).
- * quat_cumprod_debug_stall_tile(k) makes work item k of every later call skip
- * publishing its result (k < 0 disables), so that the items waiting on it run
- * out their limit and the call reports QS_ERR_TIMEOUT instead of hanging.
- * Both are process-wide settings; both return QS_OK.
+ * device-side wait (default 2 s; values <= 0 restore it).
+ * quat_cumprod_debug_stall_tile(k) makes the first kernel of every later call
+ * wait in tile k for bytes that never arrive (k < 0 disables), so that the
+ * wait runs out its limit and the call reports QS_ERR_TIMEOUT instead of
+ * hanging.  quat_cumprod_debug_set_variant selects a compiled tile
+ * configuration for each direction (index into the library's variant table,
+ * -1 = default; QS_ERR_DIMS for an unknown index).  All three are
+ * process-wide settings and return QS_OK unless stated.
  */
 int quat_cumprod_debug_set_timeout_ns(int64_t ns);
 int quat_cumprod_debug_stall_tile(int64_t tile);
-
-/*
- * Tuning / inspection hooks.  Both directions process lane groups in batches
- * whose inputs fit the L2 cache between the two passes over a batch;
- * quat_cumprod_debug_set_batch_bytes sets the target input bytes per batch
- * (default 24 MiB; <= 0 restores it).  quat_cumprod_debug_set_variant selects
- * a compiled tile configuration (index into the library's variant table, -1 =
- * automatic; QS_ERR_DIMS for an unknown index; a configuration that does not
- * apply to a call's sizes is replaced by the automatic choice).  Both are process-wide and
- * return QS_OK.  quat_cumprod_debug_check_schedule verifies on the host,
- * without a GPU, that the work-item order of both directions for these sizes
- * visits every item once and puts every item after the items it waits on
- * (QS_OK, QS_ERR_DIMS for sizes too large to check, or a negative code naming
- * the violated property).
- */
-int quat_cumprod_debug_set_batch_bytes(int64_t bytes);
 int quat_cumprod_debug_set_variant(int fwd_variant, int bwd_variant);
-int quat_cumprod_debug_check_schedule(int64_t B, int64_t S, int64_t H, int64_t J);
 
 #ifdef __cplusplus
 }

@@ -75,12 +75,8 @@ def load_library():
         lib.quat_cumprod_debug_set_timeout_ns.restype = ctypes.c_int
         lib.quat_cumprod_debug_stall_tile.argtypes = [i64]
         lib.quat_cumprod_debug_stall_tile.restype = ctypes.c_int
-        lib.quat_cumprod_debug_set_batch_bytes.argtypes = [i64]
-        lib.quat_cumprod_debug_set_batch_bytes.restype = ctypes.c_int
         lib.quat_cumprod_debug_set_variant.argtypes = [ctypes.c_int, ctypes.c_int]
         lib.quat_cumprod_debug_set_variant.restype = ctypes.c_int
-        lib.quat_cumprod_debug_check_schedule.argtypes = [i64, i64, i64, i64]
-        lib.quat_cumprod_debug_check_schedule.restype = ctypes.c_int
         _lib = lib
         return lib
 
