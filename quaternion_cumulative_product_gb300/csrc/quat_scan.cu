@@ -98,6 +98,15 @@ __device__ __forceinline__ void wait_tile(uint64_t *bar, const Control &ctl, int
     }
 }
 
+// Thread 0 initialises the tile's barrier; the barrier must be visible to the
+// whole CTA (and to the TMA unit) before the copy is issued.
+__device__ __forceinline__ void init_tile_bar(uint64_t *bar) {
+    if (threadIdx.x == 0) {
+        mbar_init(bar, 1);
+        fence_mbar_init();
+    }
+}
+
 // Thread 0 stages the tile (q, and d_cum for the backward) of lane group g,
 // chunk c.  The test hook makes the barrier expect 16 bytes that never come.
 template <bool BWD, int LT, int T>
@@ -106,8 +115,6 @@ __device__ __forceinline__ void stage_tile(unsigned char *dst, uint64_t *bar, co
                                            const Control &ctl, int tile) {
     constexpr uint32_t BYTES = T * LT * 16;
     if (threadIdx.x == 0) {
-        mbar_init(bar, 1);
-        fence_mbar_init();
         const int b = g / geo.NGb, x = (g - b * geo.NGb) * LT * 4;
         const uint32_t extra = (tile == ctl.stall_tile) ? 16u : 0u;
         mbar_arrive_expect_tx(bar, (BWD ? 2 : 1) * BYTES + extra);
@@ -137,8 +144,9 @@ __global__ void __launch_bounds__(NTHREADS)
     const int tile = blockIdx.x;
     const int c = tile / geo.NG, g = tile - c * geo.NG;
     const int lane = threadIdx.x % LT, seg = threadIdx.x / LT;
-    stage_tile<BWD, LT, T>(smem, &bar, &qmap, &dmap, geo, c, g, ctl, tile);
+    init_tile_bar(&bar);
     __syncthreads();
+    stage_tile<BWD, LT, T>(smem, &bar, &qmap, &dmap, geo, c, g, ctl, tile);
     wait_tile(&bar, ctl, tile);
 
     const int cell0 = seg * N * LT + lane;
@@ -291,13 +299,14 @@ __global__ void __launch_bounds__(NTHREADS)
     const int tile = static_cast<int>(gridDim.x) - 1 - static_cast<int>(blockIdx.x);   // reverse order
     const int c = tile / geo.NG, g = tile - c * geo.NG;
     const int lane = threadIdx.x % LT, seg = threadIdx.x / LT;
+    init_tile_bar(&bar);
+    __syncthreads();
     stage_tile<BWD, LT, T>(smem, &bar, &qmap, &dmap, geo, c, g, ctl, -1);
     const long long o = static_cast<long long>(c) * geo.NL + static_cast<long long>(g) * LT + lane;
     if (seg == 0) {   // carries of this chunk (their loads overlap the tile load)
         s_cf[lane] = __ldg(carF + o);
         if (BWD) s_ch[lane] = __ldg(carH + o);
     }
-    __syncthreads();
     wait_tile(&bar, ctl, tile);
 
     const int b = g / geo.NGb, hj = (g - b * geo.NGb) * LT + lane;
