@@ -108,7 +108,8 @@ __device__ __forceinline__ void init_tile_bar(uint64_t *bar) {
 }
 
 // Thread 0 stages the tile (q, and d_cum for the backward) of lane group g,
-// chunk c.  The test hook makes the barrier expect 16 bytes that never come.
+// chunk c.  The test hook makes the barrier of tile `tile` (>= 0; the apply
+// kernel passes -1) expect 16 bytes that never come.
 template <bool BWD, int LT, int T>
 __device__ __forceinline__ void stage_tile(unsigned char *dst, uint64_t *bar, const CUtensorMap *qmap,
                                            const CUtensorMap *dmap, const Geometry &geo, int c, int g,
@@ -116,7 +117,7 @@ __device__ __forceinline__ void stage_tile(unsigned char *dst, uint64_t *bar, co
     constexpr uint32_t BYTES = T * LT * 16;
     if (threadIdx.x == 0) {
         const int b = g / geo.NGb, x = (g - b * geo.NGb) * LT * 4;
-        const uint32_t extra = (tile == ctl.stall_tile) ? 16u : 0u;
+        const uint32_t extra = (tile >= 0 && tile == ctl.stall_tile) ? 16u : 0u;
         mbar_arrive_expect_tx(bar, (BWD ? 2 : 1) * BYTES + extra);
         tma_load_3d(dst, qmap, x, c * T, b, bar);
         if (BWD) tma_load_3d(dst + BYTES, dmap, x, c * T, b, bar);
