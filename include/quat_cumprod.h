@@ -69,7 +69,9 @@ enum {
     QS_ERR_TIMEOUT = -6,     /* a wait on the device ran out                    */
     QS_ERR_NOMEM = -7,       /* workspace allocation failed, or it would have to
                                 grow while the stream is being captured         */
-    QS_ERR_DEVICE = -8       /* the current device is not compute capability 10.3 */
+    QS_ERR_DEVICE = -8,      /* the current device is not compute capability 10.3 */
+    QS_ERR_SCRATCH = -9      /* quat_cumprod_bwd_noalloc: the sizes need more
+                                scratch than its fixed array holds              */
 };
 
 /*
@@ -94,6 +96,52 @@ int quat_cumprod_fwd(const float *q, const float *init, float *cum,
 int quat_cumprod_bwd(const float *q, const float *init, const float *d_cum,
                      float *d_q, float *d_init,
                      int64_t B, int64_t S, int64_t H, int64_t J, void *stream);
+
+/*
+ * Backward without allocation: computes exactly what quat_cumprod_bwd
+ * computes, with the same arguments, layout, ownership and checks, but never
+ * allocates device memory.  The paper has no counterpart: this entry point
+ * exists for callers that cannot call cudaMalloc at the point where they need
+ * the gradient, for example
+ *   - code whose device memory is all handed out by another allocator (a
+ *     framework's caching allocator, or a runtime with a fixed memory budget
+ *     reserved at start-up), where a raw cudaMalloc can fail or fragment that
+ *     allocator's pool;
+ *   - latency-critical loops that cannot afford the device-wide
+ *     synchronization that cudaFree implies (quat_cumprod_bwd may free and
+ *     re-allocate its workspace when a call needs a larger one).
+ * It calls no cudaMalloc, no cudaFree and no other allocating routine.
+ *
+ * Scratch: one fixed array of this library in device memory (a file-scope
+ * __device__ variable), 16 MiB + 256 bytes on every device where the
+ * library's kernels are loaded.  It holds a status block and the per-chunk
+ * aggregates and carries of one call, so the sizes are limited to
+ *     B * ceil(H*J / 32) * ceil(S / 64) <= QS_NOALLOC_MAX_TILES (8192)
+ * work tiles (for example B=8, S=4096, H=16, J=32 fits exactly); larger sizes
+ * return QS_ERR_SCRATCH before anything is enqueued.
+ *
+ * Every call on a device shares that one array.  Each call clears the status
+ * block on `stream` before its kernels run; everything else it reads it has
+ * written earlier in the same call.  Calls whose work can overlap on the GPU
+ * (calls on different streams without an ordering between them, or from
+ * several host threads onto unordered streams) RACE on the array and give
+ * wrong results; calls on one stream are ordered and safe.
+ *
+ * Set-up: the first call on each device looks up the array's address on that
+ * device (cudaGetSymbolAddress, with that device current) and prepares the
+ * kernels' attributes; later calls reuse both.  Make that first call on each
+ * device before any stream capture begins.
+ *
+ * Errors as for quat_cumprod_bwd, plus QS_ERR_SCRATCH.  A device-side wait
+ * that runs out (possible only if a tile's copy never lands) is recorded in
+ * the array's status block, not in the per-stream word that
+ * quat_cumprod_status() reads, so quat_cumprod_status() does not report it
+ * for this entry point.  The debug stall hook does not apply to it.
+ */
+#define QS_NOALLOC_MAX_TILES 8192
+int quat_cumprod_bwd_noalloc(const float *q, const float *init, const float *d_cum,
+                             float *d_q, float *d_init,
+                             int64_t B, int64_t S, int64_t H, int64_t J, void *stream);
 
 /*
  * Synchronizes `stream`, then returns QS_ERR_TIMEOUT if any call enqueued on it

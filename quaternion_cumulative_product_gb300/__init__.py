@@ -19,9 +19,9 @@ import threading
 
 __all__ = [
     "QS_OK", "QS_ERR_NULL", "QS_ERR_DIMS", "QS_ERR_MISALIGNED", "QS_ERR_ALIAS",
-    "QS_ERR_CUDA", "QS_ERR_TIMEOUT", "QS_ERR_NOMEM", "QS_ERR_DEVICE",
-    "QuatScanError", "library_path", "load_library", "quat_cumprod_fwd",
-    "quat_cumprod_bwd", "quat_cumprod_status", "quat_cumprod_strerror",
+    "QS_ERR_CUDA", "QS_ERR_TIMEOUT", "QS_ERR_NOMEM", "QS_ERR_DEVICE", "QS_ERR_SCRATCH",
+    "QS_NOALLOC_MAX_TILES", "QuatScanError", "library_path", "load_library", "quat_cumprod_fwd",
+    "quat_cumprod_bwd", "quat_cumprod_bwd_noalloc", "quat_cumprod_status", "quat_cumprod_strerror",
 ]
 
 QS_OK = 0
@@ -33,6 +33,11 @@ QS_ERR_CUDA = -5
 QS_ERR_TIMEOUT = -6
 QS_ERR_NOMEM = -7
 QS_ERR_DEVICE = -8
+QS_ERR_SCRATCH = -9
+
+# Work tiles (B * ceil(H*J/32) * ceil(S/64)) that quat_cumprod_bwd_noalloc's
+# fixed scratch array holds.
+QS_NOALLOC_MAX_TILES = 8192
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_NAME = "libquatscan.so"
@@ -67,6 +72,8 @@ def load_library():
         lib.quat_cumprod_fwd.restype = ctypes.c_int
         lib.quat_cumprod_bwd.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, vp]
         lib.quat_cumprod_bwd.restype = ctypes.c_int
+        lib.quat_cumprod_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, vp]
+        lib.quat_cumprod_bwd_noalloc.restype = ctypes.c_int
         lib.quat_cumprod_status.argtypes = [vp]
         lib.quat_cumprod_status.restype = ctypes.c_int
         lib.quat_cumprod_strerror.argtypes = [ctypes.c_int]
@@ -168,6 +175,31 @@ def quat_cumprod_bwd(q, init, d_cum, d_q=None, d_init=None, stream=None):
             ctypes.c_void_p(d_init.data_ptr()), B, S, H, J, _stream_handle(stream, q.device))
     if rc != QS_OK:
         raise QuatScanError(rc, "quat_cumprod_bwd")
+    return d_q, d_init
+
+
+def quat_cumprod_bwd_noalloc(q, init, d_cum, d_q, d_init, stream=None):
+    """``quat_cumprod_bwd`` into caller-owned ``d_q`` and ``d_init``, with no allocation.
+
+    For callers that must not allocate device memory at this point: the
+    library call uses a fixed scratch array of the library instead of a
+    cudaMalloc'ed workspace, and this wrapper allocates no tensor either.  The
+    sizes must satisfy ``B * ceil(H*J/32) * ceil(S/64) <= QS_NOALLOC_MAX_TILES``.
+    All calls on one device share the scratch: calls whose work can overlap on
+    the GPU (unordered streams) race.  Returns ``(d_q, d_init)``.
+    """
+    torch = _torch()
+    B, S, H, J = _dims(q, init)
+    _check_tensor("d_cum", d_cum, q.shape, q.device)
+    _check_tensor("d_q", d_q, q.shape, q.device)
+    _check_tensor("d_init", d_init, init.shape, q.device)
+    with torch.cuda.device(q.device):
+        rc = load_library().quat_cumprod_bwd_noalloc(
+            ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(init.data_ptr()),
+            ctypes.c_void_p(d_cum.data_ptr()), ctypes.c_void_p(d_q.data_ptr()),
+            ctypes.c_void_p(d_init.data_ptr()), B, S, H, J, _stream_handle(stream, q.device))
+    if rc != QS_OK:
+        raise QuatScanError(rc, "quat_cumprod_bwd_noalloc")
     return d_q, d_init
 
 

@@ -751,6 +751,9 @@ extern "C" const char *quat_cumprod_strerror(int status) {
         case QS_ERR_TIMEOUT: return "a device-side wait ran out (outputs are invalid)";
         case QS_ERR_NOMEM: return "workspace allocation failed or would be needed during stream capture";
         case QS_ERR_DEVICE: return "the current device is not compute capability 10.3 (sm_103)";
+        case QS_ERR_SCRATCH:
+            return "the sizes need more scratch than quat_cumprod_bwd_noalloc's fixed array holds "
+                   "(B * ceil(H*J/32) * ceil(S/64) must not exceed QS_NOALLOC_MAX_TILES = 8192)";
         default: return "unknown status";
     }
 }
@@ -773,4 +776,152 @@ extern "C" int quat_cumprod_debug_set_variant(int fwd_variant, int bwd_variant) 
     g_fwd_variant = fwd_variant < 0 ? -1 : fwd_variant;
     g_bwd_variant = bwd_variant < 0 ? -1 : bwd_variant;
     return QS_OK;
+}
+
+// ===========================================================================
+// quat_cumprod_bwd_noalloc: the backward of quat_cumprod_bwd with its scratch
+// (status block, chunk aggregates and carries) in one fixed device array of
+// this file instead of the cudaMalloc'ed per-stream workspace.  Same kernels,
+// always the 32-lane x 64-step tile, so that the size limit is fixed too.
+// ===========================================================================
+namespace {
+
+constexpr int NA_LT = 32, NA_N = 8;
+constexpr int NA_T = (NTHREADS / NA_LT) * NA_N;                                  // 64 steps per chunk
+constexpr size_t NA_ARRAY_BYTES = size_t(QS_NOALLOC_MAX_TILES) * NA_LT * 16;   // one aggregate or carry array
+constexpr size_t NA_SCRATCH_BYTES = sizeof(qs::WsHeader) + 4 * NA_ARRAY_BYTES;
+static_assert(sizeof(qs::WsHeader) == 256, "the arrays after the status block stay 256-byte aligned");
+static_assert(NA_SCRATCH_BYTES == (size_t(16) << 20) + 256, "the header states 16 MiB + 256 bytes");
+
+}  // namespace
+
+// The scratch every quat_cumprod_bwd_noalloc call on a device shares (one copy
+// per device, like every __device__ variable).
+static __device__ __align__(256) unsigned char g_noalloc_scratch[NA_SCRATCH_BYTES];
+
+namespace {
+
+std::map<int, unsigned char *> g_noalloc_ptr;   // device -> address of g_noalloc_scratch
+
+// Address of the scratch on the current device `dev`, looked up once per
+// device (the lookup loads this library's device code on that device).
+int noalloc_scratch(int dev, unsigned char **out) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto it = g_noalloc_ptr.find(dev);
+    if (it != g_noalloc_ptr.end()) {
+        *out = it->second;
+        return QS_OK;
+    }
+    void *p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess || p == nullptr) {
+        cudaGetLastError();
+        return QS_ERR_CUDA;
+    }
+    g_noalloc_ptr[dev] = static_cast<unsigned char *>(p);
+    *out = static_cast<unsigned char *>(p);
+    return QS_OK;
+}
+
+// Work tiles of the fixed tile for these sizes (exact; no overflow for any
+// sizes that passed check_dims).
+long long noalloc_tiles(int64_t B, int64_t S, int64_t HJ) {
+    const __int128 t = (__int128)B * ((HJ + NA_LT - 1) / NA_LT) * ((S + NA_T - 1) / NA_T);
+    return t > (__int128)INT64_MAX ? INT64_MAX : (long long)t;
+}
+
+int noalloc_launch(const float *q, const float *init, const float *d_cum, float *d_q, float *d_init, int64_t B,
+                   int64_t S, int64_t HJ, cudaStream_t stream) {
+    DevInfo *di = nullptr;
+    int dev = 0;
+    int rc = device_info(&di, &dev);
+    if (rc != QS_OK) return rc;
+    unsigned char *ws = nullptr;
+    rc = noalloc_scratch(dev, &ws);
+    if (rc != QS_OK) return rc;
+
+    qs::Geometry geo;
+    geo.S = S;
+    geo.HJ = (int)HJ;
+    geo.NGb = (int)((HJ + NA_LT - 1) / NA_LT);
+    geo.NG = (int)(B * geo.NGb);
+    geo.C = (int)((S + NA_T - 1) / NA_T);
+    geo.NL = geo.NG * NA_LT;
+    const int tiles = geo.NG * geo.C;
+    const size_t per = (size_t)tiles * NA_LT * 16;
+    float4 *aggL = reinterpret_cast<float4 *>(ws + sizeof(qs::WsHeader));
+    float4 *carF = aggL + per / 16;
+    float4 *aggW = carF + per / 16;
+    float4 *carH = aggW + per / 16;
+
+    // The status block must start at zero; every aggregate and carry slot a
+    // call reads is written earlier in the same call.
+    if (cudaMemsetAsync(ws, 0, sizeof(qs::WsHeader), stream) != cudaSuccess) {
+        cudaGetLastError();
+        return QS_ERR_CUDA;
+    }
+    CUtensorMap qmap, dmap;
+    rc = make_map(&qmap, q, B, S, HJ, NA_LT, NA_T);
+    if (rc == QS_OK) rc = make_map(&dmap, d_cum, B, S, HJ, NA_LT, NA_T);
+    if (rc != QS_OK) return rc;
+    qs::Control ctl;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        ctl.timeout_ns = g_timeout_ns;
+    }
+    ctl.stall_tile = -1;
+    ctl.hdr = reinterpret_cast<qs::WsHeader *>(ws);
+    const float4 *init4 = reinterpret_cast<const float4 *>(init);
+    float4 *dinit4 = reinterpret_cast<float4 *>(d_init);
+    float4 *out4 = reinterpret_cast<float4 *>(d_q);
+    const float4 *aggL_c = aggL, *aggW_c = aggW, *carF_c = carF, *carH_c = carH;
+    int lt = NA_LT;
+    const int carry_lb = geo.C > 256 ? 8 : 32;
+    const void *agg_fn = reinterpret_cast<const void *>(qs::quat_agg_kernel<true, NA_LT, NA_N>);
+    const void *apply_fn = reinterpret_cast<const void *>(qs::quat_apply_kernel<true, NA_LT, NA_N>);
+    const void *carry_fn = carry_lb == 8 ? reinterpret_cast<const void *>(qs::quat_carry_kernel<true, 8>)
+                                         : reinterpret_cast<const void *>(qs::quat_carry_kernel<true, 32>);
+    const size_t smem = qs::tile_smem_bytes(true, NA_LT, NA_N);
+    void *agg_args[] = {&qmap, &dmap, &aggL, &aggW, &geo, &ctl};
+    void *carry_args[] = {&aggL_c, &aggW_c, &init4, &carF, &carH, &dinit4, &geo, &lt};
+    void *apply_args[] = {&qmap, &dmap, &carF_c, &carH_c, &out4, &geo, &ctl};
+    const int carry_blocks = (geo.NL + carry_lb - 1) / carry_lb;
+    if (cudaLaunchKernel(agg_fn, dim3(tiles), dim3(NTHREADS), agg_args, smem, stream) != cudaSuccess ||
+        cudaLaunchKernel(carry_fn, dim3(carry_blocks), dim3(NTHREADS), carry_args, 0, stream) != cudaSuccess ||
+        cudaLaunchKernel(apply_fn, dim3(tiles), dim3(NTHREADS), apply_args, smem, stream) != cudaSuccess) {
+        cudaGetLastError();
+        return QS_ERR_CUDA;
+    }
+    return QS_OK;
+}
+
+}  // namespace
+
+extern "C" int quat_cumprod_bwd_noalloc(const float *q, const float *init, const float *d_cum, float *d_q,
+                                        float *d_init, int64_t B, int64_t S, int64_t H, int64_t J, void *stream_) {
+    const int dc = check_dims(B, S, H, J);
+    if (dc != QS_OK && dc != 1) return dc;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+    const int64_t HJ = H * J;
+    if (dc == 1) {
+        if (S == 0 && B > 0 && HJ > 0) {   // no steps: the gradient of init is zero
+            if (!d_init) return QS_ERR_NULL;
+            if (misaligned(d_init)) return QS_ERR_MISALIGNED;
+            if (cudaMemsetAsync(d_init, 0, (size_t)B * HJ * 16, stream) != cudaSuccess) {
+                cudaGetLastError();
+                return QS_ERR_CUDA;
+            }
+        }
+        return QS_OK;
+    }
+    if (!q || !init || !d_cum || !d_q || !d_init) return QS_ERR_NULL;
+    if (misaligned(q) || misaligned(init) || misaligned(d_cum) || misaligned(d_q) || misaligned(d_init))
+        return QS_ERR_MISALIGNED;
+    const size_t big = (size_t)B * S * HJ * 16, small = (size_t)B * HJ * 16;
+    if (overlaps(d_q, big, q, big) || overlaps(d_q, big, init, small) || overlaps(d_q, big, d_cum, big) ||
+        overlaps(d_init, small, q, big) || overlaps(d_init, small, init, small) ||
+        overlaps(d_init, small, d_cum, big) || overlaps(d_q, big, d_init, small))
+        return QS_ERR_ALIAS;
+    if (noalloc_tiles(B, S, HJ) > QS_NOALLOC_MAX_TILES) return QS_ERR_SCRATCH;
+    return noalloc_launch(q, init, d_cum, d_q, d_init, B, S, HJ, stream);
 }
