@@ -38,14 +38,15 @@ UNIT = "elements/s"
 DEFAULT_WORKLOAD = "mamba3"
 FWD_BYTES_PER_ELEMENT = 32      # read q, write cum
 BWD_BYTES_PER_ELEMENT = 48      # read q and d_cum, write d_q
-# Each call launches three kernels (aggregate, carry, apply).
-KERNELS_PER_CALL = 3
-KERNELS_PER_STEP = 2 * KERNELS_PER_CALL
 L2_BYTES = 126 * (1 << 20)
 FALLBACK_HBM_GBS = 6800.0
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.txt")
 KERNEL_SOURCES = [os.path.join(ROOT, "quaternion_cumulative_product_gb300", "csrc", f)
                   for f in ("quat_scan.cu", "quat_device.cuh")]
+
+
+def design_name(call: str, kernels: int) -> str:
+    return f"{call} ({'walk kernel' if kernels == 1 else 'aggregate + carry + apply kernels'})"
 
 
 def kernel_source_hash() -> str:
@@ -293,11 +294,16 @@ def run_ours(args, w, world, rank, local):
     scratch = torch.empty(2 * L2_BYTES // 4, device=dev) if flush else None
     stream = torch.cuda.current_stream(dev)
     launches = [0]
+    # The library picks one design per call (a single walk kernel, or the
+    # aggregate / carry / apply kernels); count the kernels it launches.
+    fwd_variant, fwd_kernels = qs.quat_cumprod_plan(False, w.B, w.S, w.H, w.J, device=dev)
+    bwd_variant, bwd_kernels = qs.quat_cumprod_plan(True, w.B, w.S, w.H, w.J, device=dev)
+    kernels_per_step = fwd_kernels + bwd_kernels
 
     def step():
         qs.quat_cumprod_fwd(q, init, cum)
         qs.quat_cumprod_bwd(q, init, d_cum, d_q, d_init)
-        launches[0] += KERNELS_PER_STEP
+        launches[0] += kernels_per_step
 
     for _ in range(args.warmup):
         step()
@@ -323,7 +329,7 @@ def run_ours(args, w, world, rank, local):
         e1.record(stream)
         qs.quat_cumprod_bwd(q, init, d_cum, d_q, d_init)
         e2.record(stream)
-        launches[0] += KERNELS_PER_STEP
+        launches[0] += kernels_per_step
     torch.cuda.synchronize(dev)
     clocks = sampler.stop()
     barrier(dev)
@@ -398,13 +404,15 @@ def run_ours(args, w, world, rank, local):
                           f"inputs larger than L2 ({tensor_bytes / 1e6:.0f} MB per tensor > 126 MB), no flush"),
                    "parallelism": ("one independent batch per GPU, no collective" if world > 1
                                    else "single GPU")},
-        "roofline": {"bound": "hbm", "kernel": "quat_cumprod_bwd (aggregate + carry + apply kernels)",
+        "roofline": {"bound": "hbm", "kernel": design_name("quat_cumprod_bwd", bwd_kernels),
+                     "variant": bwd_variant,
                      "achieved": bwd_gbs, "peak": peak,
                      "unit": "GB/s", "frac": bwd_gbs / peak, "peak_source": peak_src,
                      "traffic": recorded_traffic("quat_cumprod_bwd", w.name),
                      "algorithmic_bytes_per_launch": BWD_BYTES_PER_ELEMENT * E,
                      "avg_launch_ms": bwd_avg},
-        "roofline_fwd": {"bound": "hbm", "kernel": "quat_cumprod_fwd (aggregate + carry + apply kernels)",
+        "roofline_fwd": {"bound": "hbm", "kernel": design_name("quat_cumprod_fwd", fwd_kernels),
+                         "variant": fwd_variant,
                          "achieved": fwd_gbs, "peak": peak,
                          "unit": "GB/s", "frac": fwd_gbs / peak,
                          "traffic": recorded_traffic("quat_cumprod_fwd", w.name),

@@ -151,6 +151,18 @@ int quat_cumprod_bwd_noalloc(const float *q, const float *init, const float *d_c
  */
 int quat_cumprod_status(void *stream);
 
+/*
+ * Which compiled configuration a call with these sizes would use on the
+ * current device, and how many kernels it launches: 1 for a walk (one CTA
+ * per lane group streams the whole sequence), 3 for aggregate / carry /
+ * apply (the sequence split into independent tiles, chosen when there are
+ * too few lane groups to fill the GPU).  `bwd` selects the backward.  Writes
+ * *variant = -1 and *kernels = 0 when the call would launch nothing.  Returns
+ * the status the call's argument and device checks would return.  Nothing is
+ * enqueued.
+ */
+int quat_cumprod_plan(int bwd, int64_t B, int64_t S, int64_t H, int64_t J, int *variant, int *kernels);
+
 /* Static, human-readable description of a status code. */
 const char *quat_cumprod_strerror(int status);
 

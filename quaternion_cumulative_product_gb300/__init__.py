@@ -21,7 +21,8 @@ __all__ = [
     "QS_OK", "QS_ERR_NULL", "QS_ERR_DIMS", "QS_ERR_MISALIGNED", "QS_ERR_ALIAS",
     "QS_ERR_CUDA", "QS_ERR_TIMEOUT", "QS_ERR_NOMEM", "QS_ERR_DEVICE", "QS_ERR_SCRATCH",
     "QS_NOALLOC_MAX_TILES", "QuatScanError", "library_path", "load_library", "quat_cumprod_fwd",
-    "quat_cumprod_bwd", "quat_cumprod_bwd_noalloc", "quat_cumprod_status", "quat_cumprod_strerror",
+    "quat_cumprod_bwd", "quat_cumprod_bwd_noalloc", "quat_cumprod_plan", "quat_cumprod_status",
+    "quat_cumprod_strerror",
 ]
 
 QS_OK = 0
@@ -74,6 +75,9 @@ def load_library():
         lib.quat_cumprod_bwd.restype = ctypes.c_int
         lib.quat_cumprod_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, vp]
         lib.quat_cumprod_bwd_noalloc.restype = ctypes.c_int
+        ip = ctypes.POINTER(ctypes.c_int)
+        lib.quat_cumprod_plan.argtypes = [ctypes.c_int, i64, i64, i64, i64, ip, ip]
+        lib.quat_cumprod_plan.restype = ctypes.c_int
         lib.quat_cumprod_status.argtypes = [vp]
         lib.quat_cumprod_status.restype = ctypes.c_int
         lib.quat_cumprod_strerror.argtypes = [ctypes.c_int]
@@ -201,6 +205,18 @@ def quat_cumprod_bwd_noalloc(q, init, d_cum, d_q, d_init, stream=None):
     if rc != QS_OK:
         raise QuatScanError(rc, "quat_cumprod_bwd_noalloc")
     return d_q, d_init
+
+
+def quat_cumprod_plan(bwd, B, S, H, J, device=None):
+    """(variant, kernels) a call with these sizes would use on ``device`` (launches nothing)."""
+    torch = _torch()
+    device = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    v, k = ctypes.c_int(0), ctypes.c_int(0)
+    with torch.cuda.device(device):
+        rc = load_library().quat_cumprod_plan(int(bool(bwd)), B, S, H, J, ctypes.byref(v), ctypes.byref(k))
+    if rc != QS_OK:
+        raise QuatScanError(rc, "quat_cumprod_plan")
+    return v.value, k.value
 
 
 def quat_cumprod_status(stream=None, device=None):

@@ -9,14 +9,14 @@
 //
 // Design (one GPU, HBM-bound; no tensor cores -- there is no dense contraction):
 //
-//  * Tile = LT lanes x T consecutive steps of one lane group (LT lanes of one
-//    batch entry, 16*LT contiguous bytes per step), staged into shared memory
-//    by one 3-D TMA load per operand.  Thread (seg, lane) owns N consecutive
-//    steps of one lane; NSEG = 256 / LT segments per tile.  TMA fills the
-//    parts of a tile past the sequence end or past the last lane with zeros,
-//    and a zero step is exactly the padding the scan needs.
+//  * Chunk = T consecutive steps of one lane group (LT lanes of one batch
+//    entry, 16*LT contiguous bytes per step), staged into shared memory by
+//    one 3-D TMA load per operand.  Thread (seg, lane) owns N consecutive
+//    steps of one lane; NSEG segments per chunk.  TMA fills the parts of a
+//    chunk past the sequence end or past the last lane with zeros, and a zero
+//    step is exactly the padding the scan needs.
 //
-//  * Chunk aggregates (the page's factorisation), one chunk = one tile:
+//  * Chunk aggregates (the page's factorisation):
 //      L_c = q_{t1-1} (x) ... (x) q_{t0}                      (chunk product)
 //      W_c = sum_{s in c} conj(local_s) (x) d_cum[s]          (backward only)
 //    with local_s = q_s (x) ... (x) q_{t0}.  With H[t] = conj(q_t) (x) G[t]
@@ -29,12 +29,19 @@
 //    The forward carry into chunk c is F_c = cum[t0-1] = L_{c-1} (x) F_{c-1},
 //    F_0 = init.
 //
-//  * Three kernels per call, none of which waits on another CTA:
+//  * Two designs; each call picks one from the number of lane groups.
+//    Walk (one kernel): one CTA per lane group streams the whole sequence
+//    through a TMA ring and keeps the carries between chunks itself -- the
+//    forward reads q once and writes cum once; the backward walks forward
+//    over q for the carries, then backward over q and d_cum.
+//    Aggregate / carry / apply (three kernels), for too few lane groups to
+//    fill the GPU: every chunk is an independent tile --
 //      aggregate: one tile per CTA -> L_c (and W_c);
 //      carry:     per lane, chunk aggregates -> carries F_c (and H_{c+1},
 //                 d_init), with 8 to 32 threads per lane over chunk ranges;
 //      apply:     one tile per CTA, tiles in reverse order (the most recently
 //                 read tiles are still in L2) -> cum (or d_q).
+//    No kernel waits on another CTA.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -51,7 +58,7 @@
 
 namespace qs {
 
-constexpr int NTHREADS = 256;   // threads per CTA of every kernel
+constexpr int NTHREADS = 256;   // threads per CTA of the aggregate, carry and apply kernels
 
 // Device status of one (device, stream) workspace.
 struct __align__(256) WsHeader {
@@ -358,11 +365,300 @@ __global__ void __launch_bounds__(NTHREADS)
     }
 }
 
+// ---------------------------------------------------------------------------
+// Walk kernels.  One CTA walks one lane group (LT lanes of one batch entry)
+// along the whole sequence, chunk by chunk: chunk c = T steps x LT lanes is
+// staged by one TMA load per operand through an NST-deep ring, thread
+// (seg, lane) owns N consecutive steps of one lane (NSEG segments per chunk),
+// and the carry between chunks stays in the CTA.  Nothing waits on another
+// CTA.  One block barrier per chunk: what a chunk needs from the one before
+// it (the carry, and in the backward the right-hand cotangent) is published
+// one chunk ahead in double-buffered shared slots, and the segment aggregates
+// are double-buffered as well.
+//
+// Forward: one pass, cum[t] = local_t (x) F_c, 32 bytes per element.
+// Backward: a forward walk over q that stores the carries F_c (q loaded with
+// the L2 evict-last policy), then a reverse walk over q and d_cum
+// (evict-first) that folds the affine chunk maps H_c = W_c + conj(L_c) (x)
+// H_{c+1} and writes d_q.  The reverse walk starts with the chunks the
+// forward walk read last, so as much of q as L2 holds is read from L2 the
+// second time: 48 to 64 bytes of DRAM traffic per element.
+// ---------------------------------------------------------------------------
+
+// Bounded wait on one stage of a ring; false if the wait ran out (the error is
+// recorded by thread 0).
+__device__ __forceinline__ bool wait_stage(uint64_t *bar, uint32_t parity, const Control &ctl, int item) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = global_timer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (global_timer_ns() - t0 > ctl.timeout_ns) {
+            if (threadIdx.x == 0) record_error(ctl.hdr, item);
+            return false;
+        }
+    }
+    return true;
+}
+
+__device__ __forceinline__ int ld_volatile_int(const int *p) { return *reinterpret_cast<const volatile int *>(p); }
+
+// After a wait ran out, the ring's barriers are no longer in step with the
+// loads; the kernel stops issuing loads and, before it exits, gives the loads
+// it did issue a bounded time to land (so that none writes into the shared
+// memory of a later CTA).
+template <int NS>
+__device__ __forceinline__ void drain_ring(uint64_t *bars, const int *issued, const Control &ctl) {
+    if (threadIdx.x != 0) return;
+    for (int s = 0; s < NS; ++s) {
+        if (issued[s] == 0) continue;
+        const uint32_t parity = static_cast<uint32_t>(issued[s] - 1) & 1u;
+        const unsigned long long t0 = global_timer_ns();
+        while (!mbar_try_wait(&bars[s], parity) && global_timer_ns() - t0 <= ctl.timeout_ns) {
+        }
+    }
+}
+
+template <int LT, int NSEG, int N, int NST>
+__global__ void __launch_bounds__(LT *NSEG)
+    quat_walk_fwd_kernel(const __grid_constant__ CUtensorMap qmap, const float4 *__restrict__ init,
+                         float4 *__restrict__ out, const Geometry geo, const Control ctl) {
+    constexpr int T = NSEG * N;
+    constexpr uint32_t BYTES = T * LT * 16;
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char *ring = align128(smem_raw);
+    __shared__ __align__(8) uint64_t full[NST];
+    __shared__ int issued[NST];   // loads issued per stage (thread 0)
+    __shared__ int s_broken;
+    __shared__ float4 s_a[2][NSEG][LT];   // segment products of chunk i (slot i & 1)
+    __shared__ float4 s_x[2][LT];         // carry into chunk i (slot i & 1)
+
+    const int g = static_cast<int>(blockIdx.x);
+    const int b = g / geo.NGb, x0 = (g - b * geo.NGb) * LT * 4;
+    const int lane = threadIdx.x % LT, seg = threadIdx.x / LT;
+    const int hj = (g - b * geo.NGb) * LT + lane;
+    const bool lane_ok = hj < geo.HJ;
+    const int C = geo.C;
+
+    float4 R = q_ident();   // carry into the next chunk (segment-0 threads)
+    if (seg == 0 && lane_ok) R = init[static_cast<long long>(b) * geo.HJ + hj];
+    if (seg == 0) s_x[0][lane] = R;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < NST; ++s) {
+            mbar_init(&full[s], 1);
+            issued[s] = 0;
+        }
+        fence_mbar_init();
+        s_broken = 0;
+    }
+    __syncthreads();
+    auto issue = [&](int c) {   // thread 0: chunk c into stage c % NST
+        const int st = c % NST;
+        ++issued[st];
+        mbar_arrive_expect_tx(&full[st], BYTES + (c * geo.NG + g == ctl.stall_tile ? 16u : 0u));
+        tma_load_3d(ring + st * BYTES, &qmap, x0, c * T, b, &full[st]);
+    };
+    if (threadIdx.x == 0)
+        for (int c = 0; c < NST && c < C; ++c) issue(c);
+
+    const long long row0 = static_cast<long long>(b) * geo.S;
+    for (int c = 0; c < C; ++c) {
+        const int st = c % NST, sl = c & 1;
+        const float4 *Qt = reinterpret_cast<const float4 *>(ring + st * BYTES);
+        if (!ld_volatile_int(&s_broken) && !wait_stage(&full[st], (c / NST) & 1, ctl, c * geo.NG + g))
+            s_broken = 1;
+        float4 x[N];
+        float4 loc = q_ident();
+#pragma unroll
+        for (int k = 0; k < N; ++k) {
+            loc = q_mul(Qt[(seg * N + k) * LT + lane], loc);
+            x[k] = loc;
+        }
+        s_a[sl][seg][lane] = loc;
+        __syncthreads();
+        if (threadIdx.x == 0 && !s_broken && c + NST < C) issue(c + NST);
+        float4 P = q_ident();   // product of the earlier segments of the chunk
+        for (int k = 0; k < seg; ++k) P = q_mul(s_a[sl][k][lane], P);
+        const float4 Y = q_mul(P, s_x[sl][lane]);
+        if (seg == 0) {
+            float4 L = q_ident();
+#pragma unroll
+            for (int k = 0; k < NSEG; ++k) L = q_mul(s_a[sl][k][lane], L);
+            R = q_mul(L, R);
+            s_x[sl ^ 1][lane] = R;
+        }
+        if (lane_ok) {
+            const long long t0 = static_cast<long long>(c) * T + seg * N;
+            float4 *dst = out + (row0 + t0) * geo.HJ + hj;
+#pragma unroll
+            for (int k = 0; k < N; ++k)
+                if (t0 + k < geo.S) __stcs(dst + static_cast<long long>(k) * geo.HJ, q_mul(x[k], Y));
+        }
+    }
+    if (s_broken) drain_ring<NST>(full, issued, ctl);
+}
+
+template <int LT, int NSEG, int N, int NSTF, int NSTB>
+__global__ void __launch_bounds__(LT *NSEG)
+    quat_walk_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap dmap,
+                         const float4 *__restrict__ init, float4 *__restrict__ carF, float4 *__restrict__ d_q,
+                         float4 *__restrict__ d_init, const Geometry geo, const Control ctl) {
+    constexpr int T = NSEG * N;
+    constexpr uint32_t BQ = T * LT * 16;   // one operand of one chunk
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char *ring = align128(smem_raw);
+    __shared__ __align__(8) uint64_t fullF[NSTF];
+    __shared__ __align__(8) uint64_t fullB[NSTB];
+    __shared__ int issuedF[NSTF], issuedB[NSTB];
+    __shared__ int s_broken;
+    __shared__ float4 s_a[2][NSEG][LT];   // segment products
+    __shared__ float4 s_w[2][NSEG][LT];   // segment weighted sums (reverse walk)
+    __shared__ float4 s_cf[2][LT];        // carry F_c of the chunk (reverse walk)
+    __shared__ float4 s_ch[2][LT];        // H entering the chunk from the right
+
+    const int g = static_cast<int>(blockIdx.x);
+    const int b = g / geo.NGb, x0 = (g - b * geo.NGb) * LT * 4;
+    const int lane = threadIdx.x % LT, seg = threadIdx.x / LT;
+    const int hj = (g - b * geo.NGb) * LT + lane;
+    const bool lane_ok = hj < geo.HJ;
+    const int C = geo.C;
+    const long long NL = geo.NL;
+    const long long col = static_cast<long long>(g) * LT + lane;   // padded lane of this thread
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < NSTF; ++s) {
+            mbar_init(&fullF[s], 1);
+            issuedF[s] = 0;
+        }
+        for (int s = 0; s < NSTB; ++s) {
+            mbar_init(&fullB[s], 1);
+            issuedB[s] = 0;
+        }
+        fence_mbar_init();
+        s_broken = 0;
+    }
+    __syncthreads();
+    const uint64_t keep = l2_policy_evict_last(), drop = l2_policy_evict_first();
+
+    // ---- forward walk over q: carries F_c --------------------------------
+    auto issueF = [&](int c) {
+        const int st = c % NSTF;
+        ++issuedF[st];
+        mbar_arrive_expect_tx(&fullF[st], BQ + (c * geo.NG + g == ctl.stall_tile ? 16u : 0u));
+        tma_load_3d_hint(ring + st * BQ, &qmap, x0, c * T, b, &fullF[st], keep);
+    };
+    if (threadIdx.x == 0)
+        for (int c = 0; c < NSTF && c < C; ++c) issueF(c);
+
+    float4 R = q_ident();
+    if (seg == 0 && lane_ok) R = init[static_cast<long long>(b) * geo.HJ + hj];
+    for (int c = 0; c < C; ++c) {
+        const int st = c % NSTF, sl = c & 1;
+        const float4 *Qt = reinterpret_cast<const float4 *>(ring + st * BQ);
+        if (!ld_volatile_int(&s_broken) && !wait_stage(&fullF[st], (c / NSTF) & 1, ctl, c * geo.NG + g))
+            s_broken = 1;
+        float4 loc = q_ident();
+#pragma unroll
+        for (int k = 0; k < N; ++k) loc = q_mul(Qt[(seg * N + k) * LT + lane], loc);
+        s_a[sl][seg][lane] = loc;
+        __syncthreads();
+        if (threadIdx.x == 0 && !s_broken && c + NSTF < C) issueF(c + NSTF);
+        if (seg == 0) {
+            float4 L = q_ident();
+#pragma unroll
+            for (int k = 0; k < NSEG; ++k) L = q_mul(s_a[sl][k][lane], L);
+            carF[static_cast<long long>(c) * NL + col] = R;
+            R = q_mul(L, R);
+        }
+    }
+    __syncthreads();   // every read of the forward ring is done before the reverse ring reuses it
+
+    // ---- reverse walk over q and d_cum: d_q, d_init --------------------------
+    auto issueB = [&](int j) {   // reverse step j covers chunk C-1-j
+        const int st = j % NSTB, c = C - 1 - j;
+        ++issuedB[st];
+        unsigned char *dst = ring + st * 2 * BQ;
+        mbar_arrive_expect_tx(&fullB[st], 2 * BQ);
+        tma_load_3d_hint(dst, &qmap, x0, c * T, b, &fullB[st], drop);
+        tma_load_3d_hint(dst + BQ, &dmap, x0, c * T, b, &fullB[st], drop);
+    };
+    if (threadIdx.x == 0 && !s_broken)
+        for (int j = 0; j < NSTB && j < C; ++j) issueB(j);
+    float4 Hc = q_zero();   // H entering the current chunk from the right (segment-0 threads)
+    if (seg == 0) {
+        s_ch[0][lane] = Hc;
+        s_cf[0][lane] = carF[static_cast<long long>(C - 1) * NL + col];   // written by this thread
+    }
+    __syncthreads();
+
+    const long long row0 = static_cast<long long>(b) * geo.S;
+    for (int j = 0; j < C; ++j) {
+        const int c = C - 1 - j;
+        const int st = j % NSTB, sl = j & 1;
+        float4 cf_next = q_ident();
+        if (seg == 0 && c > 0) cf_next = carF[static_cast<long long>(c - 1) * NL + col];
+        const float4 *Qt = reinterpret_cast<const float4 *>(ring + st * 2 * BQ);
+        const float4 *Dt = Qt + T * LT;
+        if (!ld_volatile_int(&s_broken) && !wait_stage(&fullB[st], (j / NSTB) & 1, ctl, c * geo.NG + g))
+            s_broken = 1;
+        const int cell0 = seg * N * LT + lane;
+        float4 qv[N], dv[N], lp[N];
+        float4 loc = q_ident(), W = q_zero();
+#pragma unroll
+        for (int k = 0; k < N; ++k) {
+            qv[k] = Qt[cell0 + k * LT];
+            dv[k] = Dt[cell0 + k * LT];
+            lp[k] = loc;
+            loc = q_mul(qv[k], loc);
+            W = q_add(W, q_mul_cl(loc, dv[k]));
+        }
+        s_a[sl][seg][lane] = loc;
+        s_w[sl][seg][lane] = W;
+        __syncthreads();
+        if (threadIdx.x == 0 && !s_broken && j + NSTB < C) issueB(j + NSTB);
+        float4 P = q_ident();   // earlier segments
+        for (int k = 0; k < seg; ++k) P = q_mul(s_a[sl][k][lane], P);
+        float4 V = q_zero(), M = q_ident();   // later segments as h -> V + M (x) h
+        for (int k = NSEG - 1; k > seg; --k) {
+            V = q_add(s_w[sl][k][lane], q_mul_cl(s_a[sl][k][lane], V));
+            M = q_mul_cl(s_a[sl][k][lane], M);
+        }
+        const float4 X = q_mul(P, s_cf[sl][lane]);   // cum just before this segment
+        float4 Hn = q_add(V, q_mul(M, s_ch[sl][lane]));
+        if (seg == 0) {   // the whole chunk's map, applied to the H from the right
+            Hc = q_add(q_add(s_w[sl][0][lane], q_mul_cl(s_a[sl][0][lane], V)),
+                       q_mul(q_mul_cl(s_a[sl][0][lane], M), Hc));
+            s_ch[sl ^ 1][lane] = Hc;
+            s_cf[sl ^ 1][lane] = cf_next;
+            if (c == 0 && lane_ok) d_init[static_cast<long long>(b) * geo.HJ + hj] = Hc;
+        }
+        const long long t0 = static_cast<long long>(c) * T + seg * N;
+        float4 *dst = d_q + (row0 + t0) * geo.HJ + hj;
+#pragma unroll
+        for (int k = N - 1; k >= 0; --k) {
+            const float4 G = q_add(dv[k], Hn);
+            if (lane_ok && t0 + k < geo.S)
+                __stcs(dst + static_cast<long long>(k) * geo.HJ, q_mul_cr(G, q_mul(lp[k], X)));
+            Hn = q_mul_cl(qv[k], G);
+        }
+    }
+    if (s_broken) {
+        drain_ring<NSTF>(fullF, issuedF, ctl);
+        drain_ring<NSTB>(fullB, issuedB, ctl);
+    }
+}
+
 // Shared memory of a tile kernel (dynamic part).
 __host__ __device__ constexpr size_t tile_smem_bytes(bool bwd, int lt, int n) {
     return 128 + size_t(bwd ? 2 : 1) * (NTHREADS / lt) * n * lt * 16;
 }
 
+// Dynamic shared memory of the walk kernels: the forward ring, or the larger
+// of the backward's two rings (one operand per stage forward, two reverse).
+__host__ __device__ constexpr size_t walk_fwd_smem_bytes(int lt, int nseg, int n, int nst) {
+    return 128 + size_t(nst) * nseg * n * lt * 16;
+}
+__host__ __device__ constexpr size_t walk_bwd_smem_bytes(int lt, int nseg, int n, int nstf, int nstb) {
+    return 128 + size_t(nstf > 2 * nstb ? nstf : 2 * nstb) * nseg * n * lt * 16;
+}
 }  // namespace qs
 
 // ===========================================================================
@@ -374,34 +670,66 @@ using qs::NTHREADS;
 
 constexpr unsigned long long DEFAULT_TIMEOUT_NS = 2000000000ull;
 
-// One compiled tile configuration: lane-group width LT, steps per thread N.
+// One compiled configuration: lane-group width LT, segments per chunk NSEG
+// (threads per CTA = LT * NSEG), steps per thread N.
 struct Variant {
-    const void *agg;
-    const void *apply;
+    bool walk;           // walk kernel (else aggregate / carry / apply)
+    const void *agg;     // the walk kernel, or the aggregate kernel
+    const void *apply;   // the apply kernel (three-kernel variants)
     bool bwd;
-    int lt, n;
-    int T() const { return (NTHREADS / lt) * n; }
-    size_t smem() const { return qs::tile_smem_bytes(bwd, lt, n); }
+    int lt, nseg, n;
+    size_t smem_bytes;   // dynamic shared memory per CTA
+    int T() const { return nseg * n; }
+    int threads() const { return lt * nseg; }
+    size_t smem() const { return smem_bytes; }
 };
 
 #define QS_VARIANT(B, LT, N)                                                                        \
     Variant {                                                                                       \
-        reinterpret_cast<const void *>(qs::quat_agg_kernel<B, LT, N>),                              \
-            reinterpret_cast<const void *>(qs::quat_apply_kernel<B, LT, N>), B, LT, N               \
+        false, reinterpret_cast<const void *>(qs::quat_agg_kernel<B, LT, N>),                       \
+            reinterpret_cast<const void *>(qs::quat_apply_kernel<B, LT, N>), B, LT, NTHREADS / (LT), N, \
+            qs::tile_smem_bytes(B, LT, N)                                                           \
+    }
+#define QS_WALK_FWD(LT, NSEG, N, NST)                                                               \
+    Variant {                                                                                       \
+        true, reinterpret_cast<const void *>(qs::quat_walk_fwd_kernel<LT, NSEG, N, NST>), nullptr,  \
+            false, LT, NSEG, N, qs::walk_fwd_smem_bytes(LT, NSEG, N, NST)                           \
+    }
+#define QS_WALK_BWD(LT, NSEG, N, NSTF, NSTB)                                                        \
+    Variant {                                                                                       \
+        true, reinterpret_cast<const void *>(qs::quat_walk_bwd_kernel<LT, NSEG, N, NSTF, NSTB>),    \
+            nullptr, true, LT, NSEG, N, qs::walk_bwd_smem_bytes(LT, NSEG, N, NSTF, NSTB)            \
     }
 const Variant kFwdVariants[] = {
-    QS_VARIANT(false, 32, 8),    // 64-step chunks, 32 KiB tiles
-    QS_VARIANT(false, 32, 4),    // 32-step chunks, 16 KiB tiles
-    QS_VARIANT(false, 64, 8),    // 32-step chunks, 32 KiB tiles
-    QS_VARIANT(false, 32, 16),   // 128-step chunks, 64 KiB tiles
+    QS_VARIANT(false, 32, 8),          // 0: three kernels, 64-step chunks, 32 KiB tiles
+    QS_VARIANT(false, 32, 4),          // 1: three kernels, 32-step chunks
+    QS_VARIANT(false, 64, 8),          // 2: three kernels, 64 lanes x 32 steps
+    QS_VARIANT(false, 32, 16),         // 3: three kernels, 128-step chunks
+    QS_WALK_FWD(32, 8, 8, 3),          // 4: walk, 32 lanes x 64 steps, 3 x 32 KiB ring
+    QS_WALK_FWD(16, 8, 8, 3),          // 5: walk, 16 lanes x 64 steps (128 threads), 3 x 16 KiB
+    QS_WALK_FWD(16, 16, 8, 3),         // 6: walk, 16 lanes x 128 steps (256 threads), 3 x 32 KiB
+    QS_WALK_FWD(32, 8, 4, 6),          // 7: walk, 32 lanes x 32 steps, 6 x 16 KiB
 };
 const Variant kBwdVariants[] = {
-    QS_VARIANT(true, 32, 8),     // 64-step chunks, 64 KiB tiles
-    QS_VARIANT(true, 32, 4),     // 32-step chunks, 32 KiB tiles
-    QS_VARIANT(true, 64, 4),     // 16-step chunks, 32 KiB tiles
-    QS_VARIANT(true, 64, 8),     // 32-step chunks, 64 KiB tiles
+    QS_VARIANT(true, 32, 8),           // 0: three kernels, 64-step chunks, 64 KiB tiles
+    QS_VARIANT(true, 32, 4),           // 1: three kernels, 32-step chunks
+    QS_VARIANT(true, 64, 4),           // 2: three kernels, 64 lanes x 16 steps
+    QS_VARIANT(true, 64, 8),           // 3: three kernels, 64 lanes x 32 steps
+    QS_WALK_BWD(16, 8, 8, 4, 2),       // 4: walk, 16 lanes x 64 steps (128 threads), 64 KiB rings
+    QS_WALK_BWD(16, 8, 8, 6, 3),       // 5: walk, 16 lanes x 64 steps, 96 KiB rings
+    QS_WALK_BWD(32, 8, 8, 6, 3),       // 6: walk, 32 lanes x 64 steps, 192 KiB rings
+    QS_WALK_BWD(32, 8, 4, 6, 3),       // 7: walk, 32 lanes x 32 steps, 96 KiB rings
 };
 #undef QS_VARIANT
+#undef QS_WALK_FWD
+#undef QS_WALK_BWD
+// Automatic choice between the two designs.  A walk keeps one CTA per lane
+// group for the whole sequence, so it needs enough lane groups to keep every
+// SM streaming (measured: 128 groups of 32 lanes forward and 256 groups of 16
+// lanes backward already beat the three-kernel path on 152 SMs).  With fewer
+// lanes -- long sequences of few lanes -- the three-kernel path, which splits
+// the sequence into independent tiles, is the faster one.
+constexpr int kWalkFwd = 4, kWalkBwd = 4, kThreeFwd = 0, kThreeBwd = 0;
 constexpr int kNumFwd = sizeof(kFwdVariants) / sizeof(kFwdVariants[0]);
 constexpr int kNumBwd = sizeof(kBwdVariants) / sizeof(kBwdVariants[0]);
 
@@ -487,9 +815,10 @@ int device_info(DevInfo **out, int *dev_out) {
             auto setup = [&](const Variant &v) {
                 ok = ok &&
                      cudaFuncSetAttribute(v.agg, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)v.smem()) ==
-                         cudaSuccess &&
-                     cudaFuncSetAttribute(v.apply, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)v.smem()) ==
                          cudaSuccess;
+                if (v.apply)
+                    ok = ok && cudaFuncSetAttribute(v.apply, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                    (int)v.smem()) == cudaSuccess;
             };
             for (const Variant &v : kFwdVariants) setup(v);
             for (const Variant &v : kBwdVariants) setup(v);
@@ -563,23 +892,32 @@ int make_map(CUtensorMap *m, const float *ptr, int64_t B, int64_t S, int64_t HJ,
     return r == CUDA_SUCCESS ? QS_OK : QS_ERR_CUDA;
 }
 
-int pick_variant(bool bwd) {
-    std::lock_guard<std::mutex> lk(g_mu);
-    const int forced = bwd ? g_bwd_variant : g_fwd_variant;
-    return forced >= 0 ? forced : 0;
+int pick_variant(bool bwd, int64_t B, int64_t HJ, int sms) {
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        const int forced = bwd ? g_bwd_variant : g_fwd_variant;
+        if (forced >= 0) return forced;
+    }
+    const Variant &w = bwd ? kBwdVariants[kWalkBwd] : kFwdVariants[kWalkFwd];
+    const long long groups = (long long)B * ((HJ + w.lt - 1) / w.lt);
+    const long long need = bwd ? 3ll * sms / 2 : 3ll * sms / 4;
+    if (groups >= need) return bwd ? kWalkBwd : kWalkFwd;
+    return bwd ? kThreeBwd : kThreeFwd;
 }
 
 // Everything a call needs, derived from the sizes alone (no device calls).
 struct Plan {
     const Variant *v = nullptr;
+    int vi = 0;   // index in the variant table
     qs::Geometry geo{};
     long long tiles = 0;
     int carry_lb = 32;   // lanes per block of the carry kernel
     size_t o_L = 0, o_W = 0, o_F = 0, o_H = 0, ws_bytes = 0;
 };
 
-int make_plan(bool bwd, int64_t B, int64_t S, int64_t HJ, Plan *pl) {
-    const int vi = pick_variant(bwd);
+int make_plan(bool bwd, int64_t B, int64_t S, int64_t HJ, int sms, Plan *pl) {
+    const int vi = pick_variant(bwd, B, HJ, sms);
+    pl->vi = vi;
     pl->v = bwd ? &kBwdVariants[vi] : &kFwdVariants[vi];
     const int LT = pl->v->lt, T = pl->v->T();
     qs::Geometry &g = pl->geo;
@@ -593,10 +931,19 @@ int make_plan(bool bwd, int64_t B, int64_t S, int64_t HJ, Plan *pl) {
     g.NG = (int)NG;
     g.C = (int)C;
     g.NL = (int)(NG * LT);
-    // More threads per lane when the chunk count is large.
-    pl->carry_lb = C > 256 ? 8 : 32;
     const size_t per = (size_t)pl->tiles * LT * 16;
     size_t off = sizeof(qs::WsHeader);
+    if (pl->v->walk) {
+        // Walk kernels: status block, then (backward) the carries F_c.
+        if (bwd) {
+            pl->o_F = off;
+            off = align_up(off + per, 256);
+        }
+        pl->ws_bytes = off;
+        return QS_OK;
+    }
+    // More threads per lane when the chunk count is large.
+    pl->carry_lb = C > 256 ? 8 : 32;
     pl->o_L = off;
     off = align_up(off + per, 256);
     pl->o_F = off;
@@ -618,7 +965,7 @@ int launch(bool bwd, const float *q, const float *d_cum, float *out, const float
     int rc = device_info(&di, &dev);
     if (rc != QS_OK) return rc;
     Plan pl;
-    rc = make_plan(bwd, B, S, HJ, &pl);
+    rc = make_plan(bwd, B, S, HJ, di->sms, &pl);
     if (rc != QS_OK) return rc;
     unsigned char *ws = nullptr;
     rc = ensure_workspace(dev, stream, pl.ws_bytes, &ws);
@@ -627,6 +974,27 @@ int launch(bool bwd, const float *q, const float *d_cum, float *out, const float
     rc = make_map(&qmap, q, B, S, HJ, pl.v->lt, pl.v->T());
     if (rc == QS_OK) rc = make_map(&dmap, bwd ? d_cum : q, B, S, HJ, pl.v->lt, pl.v->T());
     if (rc != QS_OK) return rc;
+    if (pl.v->walk) {
+        float4 *carF = bwd ? reinterpret_cast<float4 *>(ws + pl.o_F) : nullptr;
+        qs::Control ctl;
+        {
+            std::lock_guard<std::mutex> lk(g_mu);
+            ctl.timeout_ns = g_timeout_ns;
+            ctl.stall_tile = g_stall_tile;
+        }
+        ctl.hdr = reinterpret_cast<qs::WsHeader *>(ws);
+        const float4 *init4 = reinterpret_cast<const float4 *>(init);
+        float4 *dinit4 = reinterpret_cast<float4 *>(d_init);
+        float4 *out4 = reinterpret_cast<float4 *>(out);
+        void *fwd_args[] = {&qmap, &init4, &out4, &pl.geo, &ctl};
+        void *bwd_args[] = {&qmap, &dmap, &init4, &carF, &out4, &dinit4, &pl.geo, &ctl};
+        if (cudaLaunchKernel(pl.v->agg, dim3((unsigned)pl.geo.NG), dim3(pl.v->threads()),
+                             bwd ? bwd_args : fwd_args, pl.v->smem(), stream) != cudaSuccess) {
+            cudaGetLastError();
+            return QS_ERR_CUDA;
+        }
+        return QS_OK;
+    }
     float4 *aggL = reinterpret_cast<float4 *>(ws + pl.o_L);
     float4 *carF = reinterpret_cast<float4 *>(ws + pl.o_F);
     float4 *aggW = bwd ? reinterpret_cast<float4 *>(ws + pl.o_W) : nullptr;
@@ -738,6 +1106,27 @@ extern "C" int quat_cumprod_status(void *stream_) {
         return QS_ERR_CUDA;
     }
     return QS_ERR_TIMEOUT;
+}
+
+extern "C" int quat_cumprod_plan(int bwd, int64_t B, int64_t S, int64_t H, int64_t J, int *variant, int *kernels) {
+    if (!variant || !kernels) return QS_ERR_NULL;
+    const int dc = check_dims(B, S, H, J);
+    if (dc != QS_OK && dc != 1) return dc;
+    if (dc == 1) {   // nothing to launch (the backward may write d_init with a memset)
+        *variant = -1;
+        *kernels = 0;
+        return QS_OK;
+    }
+    DevInfo *di = nullptr;
+    int dev = 0;
+    int rc = device_info(&di, &dev);
+    if (rc != QS_OK) return rc;
+    Plan pl;
+    rc = make_plan(bwd != 0, B, S, H * J, di->sms, &pl);
+    if (rc != QS_OK) return rc;
+    *variant = pl.vi;
+    *kernels = pl.v->walk ? 1 : 3;
+    return QS_OK;
 }
 
 extern "C" const char *quat_cumprod_strerror(int status) {

@@ -145,3 +145,12 @@ def test_workload_generator_is_seeded_and_shaped():
     sq, si, sd = workloads.sample_lanes(a, lanes, 2, 4)
     assert sq.shape == (1, 64, 3, 1, 4) and si.shape == (1, 3, 1, 4)
     assert (sq[0, :, 1, 0] == q[0, :, 1, 0]).all() and (si[0, 2, 0] == init[0, 1, 1]).all()
+
+
+def test_plan_query_argument_checks(lib):
+    v, k = ctypes.c_int(7), ctypes.c_int(7)
+    assert lib.quat_cumprod_plan(0, 1, 4, 1, 1, None, ctypes.byref(k)) == qs.QS_ERR_NULL
+    assert lib.quat_cumprod_plan(1, 1, 4, 1, 1, ctypes.byref(v), None) == qs.QS_ERR_NULL
+    assert lib.quat_cumprod_plan(0, 1, -4, 1, 1, ctypes.byref(v), ctypes.byref(k)) == qs.QS_ERR_DIMS
+    assert lib.quat_cumprod_plan(1, 0, 4, 1, 1, ctypes.byref(v), ctypes.byref(k)) == qs.QS_OK
+    assert (v.value, k.value) == (-1, 0)

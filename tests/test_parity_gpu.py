@@ -178,13 +178,18 @@ def test_empty_sizes(dev):
     del z
 
 
-N_FWD_VARIANTS, N_BWD_VARIANTS = 4, 4
+# Variants 0-3: aggregate / carry / apply kernels; the rest: walk kernels.
+N_FWD_VARIANTS, N_BWD_VARIANTS = 8, 8
 
 
 @pytest.mark.parametrize("variant", range(max(N_FWD_VARIANTS, N_BWD_VARIANTS)))
-@pytest.mark.parametrize("dims", [(2, 333, 3, 16), (1, 70, 5, 9), (3, 1100, 1, 40)])
+@pytest.mark.parametrize("dims", [(2, 333, 3, 16), (1, 70, 5, 9), (3, 1100, 1, 40), (1, 5000, 2, 32)])
 def test_every_compiled_variant(dev, variant, dims):
-    """Each compiled tile configuration (lane-group width, steps per thread, stages)."""
+    """Each compiled configuration (lane-group width, steps per thread, cluster size, stages).
+
+    The sizes give chunk counts below, at and above the cluster sizes, ragged
+    lane groups and ragged last chunks.
+    """
     lib = qs.load_library()
     fv = variant if variant < N_FWD_VARIANTS else -1
     bv = variant if variant < N_BWD_VARIANTS else -1
@@ -252,9 +257,11 @@ def test_binding_rejects_bad_tensors(dev):
 # runs out its bounded wait; the call reports QS_ERR_TIMEOUT (no hang) and the
 # next call is clean.
 # ---------------------------------------------------------------------------
+@pytest.mark.parametrize("variant", [0, 4])   # aggregate / carry / apply, and walk
 @pytest.mark.parametrize("which", ["fwd", "bwd"])
-def test_stalled_tile_reports_timeout_then_recovers(dev, which):
+def test_stalled_tile_reports_timeout_then_recovers(dev, which, variant):
     lib = qs.load_library()
+    assert lib.quat_cumprod_debug_set_variant(variant, variant) == qs.QS_OK
     w = workloads.custom("stall", 2, 600, 2, 16, seed=21)
     q, init, d_cum = workloads.make_inputs(w)
     tq, ti, td = (torch.from_numpy(a).to(dev) for a in (q, init, d_cum))
@@ -270,3 +277,17 @@ def test_stalled_tile_reports_timeout_then_recovers(dev, which):
     lib.quat_cumprod_debug_stall_tile(-1)
     lib.quat_cumprod_debug_set_timeout_ns(0)
     check_against_oracle(dev, q, init, d_cum)
+
+
+# ---------------------------------------------------------------------------
+# Automatic choice of design: walk kernels when the lane groups fill the GPU,
+# the three-kernel path otherwise.
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("name,walk", [("mamba3", True), ("large", True), ("long", False),
+                                       ("small", False), ("tiny", False)])
+def test_plan_picks_the_design_by_lane_groups(dev, name, walk):
+    w = workloads.WORKLOADS[name]
+    for bwd in (False, True):
+        variant, kernels = qs.quat_cumprod_plan(bwd, w.B, w.S, w.H, w.J, device=dev)
+        assert kernels == (1 if walk else 3), (name, bwd, variant, kernels)
+    assert qs.quat_cumprod_plan(True, 2, 0, 3, 4, device=dev) == (-1, 0)
