@@ -43,6 +43,20 @@ __device__ __forceinline__ float4 q_mul(const float4 a, const float4 b) {
 __device__ __forceinline__ float4 q_mul_cl(const float4 a, const float4 b) { return q_mul(q_conj(a), b); }
 __device__ __forceinline__ float4 q_mul_cr(const float4 a, const float4 b) { return q_mul(a, q_conj(b)); }
 
+// acc + a (x) b and acc + conj(a) (x) b, accumulated term by term into acc
+// (four fused multiply-adds per component).
+__device__ __forceinline__ float4 q_fma(const float4 acc, const float4 a, const float4 b) {
+    float4 r;
+    r.x = fmaf(-a.w, b.w, fmaf(-a.z, b.z, fmaf(-a.y, b.y, fmaf(a.x, b.x, acc.x))));
+    r.y = fmaf(-a.w, b.z, fmaf(a.z, b.w, fmaf(a.y, b.x, fmaf(a.x, b.y, acc.y))));
+    r.z = fmaf(a.w, b.y, fmaf(a.z, b.x, fmaf(-a.y, b.w, fmaf(a.x, b.z, acc.z))));
+    r.w = fmaf(a.w, b.x, fmaf(-a.z, b.y, fmaf(a.y, b.z, fmaf(a.x, b.w, acc.w))));
+    return r;
+}
+__device__ __forceinline__ float4 q_fma_cl(const float4 acc, const float4 a, const float4 b) {
+    return q_fma(acc, q_conj(a), b);
+}
+
 // ---------------------------------------------------------------------------
 // Shared-memory addresses, mbarriers and TMA.
 // ---------------------------------------------------------------------------

@@ -509,10 +509,10 @@ __global__ void __launch_bounds__(LT *NSEG)
     __shared__ __align__(8) uint64_t fullB[NSTB];
     __shared__ int issuedF[NSTF], issuedB[NSTB];
     __shared__ int s_broken;
-    __shared__ float4 s_a[2][NSEG][LT];   // segment products
-    __shared__ float4 s_w[2][NSEG][LT];   // segment weighted sums (reverse walk)
-    __shared__ float4 s_cf[2][LT];        // carry F_c of the chunk (reverse walk)
-    __shared__ float4 s_ch[2][LT];        // H entering the chunk from the right
+    __shared__ float4 s_a[2][NSEG][LT];   // segment products (forward walk: slot c & 1)
+    __shared__ float4 s_w[NSEG][LT];      // segment weighted sums (reverse walk)
+    __shared__ float4 s_x[NSEG][LT];      // cum just before each segment (reverse walk)
+    __shared__ float4 s_h[NSEG][LT];      // H entering each segment from the right
 
     const int g = static_cast<int>(blockIdx.x);
     const int b = g / geo.NGb, x0 = (g - b * geo.NGb) * LT * 4;
@@ -561,12 +561,10 @@ __global__ void __launch_bounds__(LT *NSEG)
         s_a[sl][seg][lane] = loc;
         __syncthreads();
         if (threadIdx.x == 0 && !s_broken && c + NSTF < C) issueF(c + NSTF);
-        if (seg == 0) {
-            float4 L = q_ident();
-#pragma unroll
-            for (int k = 0; k < NSEG; ++k) L = q_mul(s_a[sl][k][lane], L);
+        if (seg == 0) {   // segment 0 carries the lane through the chunk
             carF[static_cast<long long>(c) * NL + col] = R;
-            R = q_mul(L, R);
+#pragma unroll
+            for (int k = 0; k < NSEG; ++k) R = q_mul(s_a[sl][k][lane], R);
         }
     }
     __syncthreads();   // every read of the forward ring is done before the reverse ring reuses it
@@ -582,19 +580,18 @@ __global__ void __launch_bounds__(LT *NSEG)
     };
     if (threadIdx.x == 0 && !s_broken)
         for (int j = 0; j < NSTB && j < C; ++j) issueB(j);
-    float4 Hc = q_zero();   // H entering the current chunk from the right (segment-0 threads)
-    if (seg == 0) {
-        s_ch[0][lane] = Hc;
-        s_cf[0][lane] = carF[static_cast<long long>(C - 1) * NL + col];   // written by this thread
-    }
-    __syncthreads();
 
+    float4 Hc = q_zero();   // H entering the current chunk from the right (segment-0 threads)
+    // Carry into the chunk, written by this thread in the forward walk; loaded
+    // one chunk ahead.
+    float4 F_next = q_ident();
+    if (seg == 0) F_next = carF[static_cast<long long>(C - 1) * NL + col];
     const long long row0 = static_cast<long long>(b) * geo.S;
     for (int j = 0; j < C; ++j) {
         const int c = C - 1 - j;
-        const int st = j % NSTB, sl = j & 1;
-        float4 cf_next = q_ident();
-        if (seg == 0 && c > 0) cf_next = carF[static_cast<long long>(c - 1) * NL + col];
+        const int st = j % NSTB;
+        const float4 F = F_next;
+        if (seg == 0 && c > 0) F_next = carF[static_cast<long long>(c - 1) * NL + col];
         const float4 *Qt = reinterpret_cast<const float4 *>(ring + st * 2 * BQ);
         const float4 *Dt = Qt + T * LT;
         if (!ld_volatile_int(&s_broken) && !wait_stage(&fullB[st], (j / NSTB) & 1, ctl, c * geo.NG + g))
@@ -608,36 +605,46 @@ __global__ void __launch_bounds__(LT *NSEG)
             dv[k] = Dt[cell0 + k * LT];
             lp[k] = loc;
             loc = q_mul(qv[k], loc);
-            W = q_add(W, q_mul_cl(loc, dv[k]));
+            W = q_fma_cl(W, loc, dv[k]);
         }
-        s_a[sl][seg][lane] = loc;
-        s_w[sl][seg][lane] = W;
+        s_a[0][seg][lane] = loc;
+        s_w[seg][lane] = W;
         __syncthreads();
         if (threadIdx.x == 0 && !s_broken && j + NSTB < C) issueB(j + NSTB);
-        float4 P = q_ident();   // earlier segments
-        for (int k = 0; k < seg; ++k) P = q_mul(s_a[sl][k][lane], P);
-        float4 V = q_zero(), M = q_ident();   // later segments as h -> V + M (x) h
-        for (int k = NSEG - 1; k > seg; --k) {
-            V = q_add(s_w[sl][k][lane], q_mul_cl(s_a[sl][k][lane], V));
-            M = q_mul_cl(s_a[sl][k][lane], M);
-        }
-        const float4 X = q_mul(P, s_cf[sl][lane]);   // cum just before this segment
-        float4 Hn = q_add(V, q_mul(M, s_ch[sl][lane]));
-        if (seg == 0) {   // the whole chunk's map, applied to the H from the right
-            Hc = q_add(q_add(s_w[sl][0][lane], q_mul_cl(s_a[sl][0][lane], V)),
-                       q_mul(q_mul_cl(s_a[sl][0][lane], M), Hc));
-            s_ch[sl ^ 1][lane] = Hc;
-            s_cf[sl ^ 1][lane] = cf_next;
+        if (seg == 0) {
+            // The carry forward through the segments, and H backward through
+            // them: two independent chains of NSEG products.
+            float4 X = F, h = Hc;
+#pragma unroll
+            for (int k = 0; k < NSEG; ++k) {
+                const int kr = NSEG - 1 - k;
+                s_x[k][lane] = X;
+                s_h[kr][lane] = h;
+                X = q_mul(s_a[0][k][lane], X);
+                h = q_fma_cl(s_w[kr][lane], s_a[0][kr][lane], h);
+            }
+            Hc = h;
             if (c == 0 && lane_ok) d_init[static_cast<long long>(b) * geo.HJ + hj] = Hc;
         }
+        __syncthreads();
+        const float4 X = s_x[seg][lane];   // cum just before this segment
+        float4 Hn = s_h[seg][lane];         // H entering this segment from the right
         const long long t0 = static_cast<long long>(c) * T + seg * N;
         float4 *dst = d_q + (row0 + t0) * geo.HJ + hj;
+        if (lane_ok && t0 + N <= geo.S) {
 #pragma unroll
-        for (int k = N - 1; k >= 0; --k) {
-            const float4 G = q_add(dv[k], Hn);
-            if (lane_ok && t0 + k < geo.S)
+            for (int k = N - 1; k >= 0; --k) {
+                const float4 G = q_add(dv[k], Hn);
                 __stcs(dst + static_cast<long long>(k) * geo.HJ, q_mul_cr(G, q_mul(lp[k], X)));
-            Hn = q_mul_cl(qv[k], G);
+                Hn = q_mul_cl(qv[k], G);
+            }
+        } else if (lane_ok) {
+#pragma unroll
+            for (int k = N - 1; k >= 0; --k) {
+                const float4 G = q_add(dv[k], Hn);
+                if (t0 + k < geo.S) __stcs(dst + static_cast<long long>(k) * geo.HJ, q_mul_cr(G, q_mul(lp[k], X)));
+                Hn = q_mul_cl(qv[k], G);
+            }
         }
     }
     if (s_broken) {
