@@ -97,6 +97,11 @@ def rank_seed(base_seed: int, rank: int) -> int:
     return base_seed + 1000 * rank
 
 
+def weak_scaling_value(world: int, elements_per_rank: int, step_ms: float) -> float:
+    """Whole-job elements/s: every rank processes its own batch in ``step_ms`` (max over ranks)."""
+    return world * elements_per_rank / (step_ms * 1e-3)
+
+
 def reduce_max(value: float, device=None) -> float:
     import torch
     import torch.distributed as dist
@@ -341,7 +346,7 @@ def run_ours(args, w, world, rank, local):
     step_ms_local = sum(f + b for f, b in zip(fwd_ms, bwd_ms)) / args.steps
     step_ms = reduce_max(step_ms_local, dev)
     E = w.elements
-    value = world * E / (step_ms * 1e-3)
+    value = weak_scaling_value(world, E, step_ms)
 
     # ---- end to end through the public API with pinned host buffers ---------
     h_q = torch.from_numpy(q_np).pin_memory()
@@ -419,7 +424,7 @@ def run_ours(args, w, world, rank, local):
                          "algorithmic_bytes_per_launch": FWD_BYTES_PER_ELEMENT * E,
                          "avg_launch_ms": fwd_avg},
         "cpu_baseline": cpu,
-        "e2e": {"value": world * E / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+        "e2e": {"value": weak_scaling_value(world, E, e2e_ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "steps": e2e_steps},
         "gpu_launches": launches[0],
         "clocks": clocks,
