@@ -496,7 +496,14 @@ __global__ void __launch_bounds__(LT *NSEG)
     if (s_broken) drain_ring<NST>(full, issued, ctl);
 }
 
-template <int LT, int NSEG, int N, int NSTF, int NSTB>
+// SELF = false: after a chunk's segment aggregates are in shared memory, the
+// segment-0 thread of each lane folds them once (two chains of NSEG products)
+// and a second block barrier hands each segment its carry and cotangent.
+// SELF = true: every thread folds its own carry (through the earlier
+// segments) and cotangent (through the later ones), about NSEG-1 products,
+// and the chunk needs no second barrier; segment 0 publishes the cotangent
+// entering the next chunk one chunk ahead.
+template <int LT, int NSEG, int N, int NSTF, int NSTB, bool SELF>
 __global__ void __launch_bounds__(LT *NSEG)
     quat_walk_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap dmap,
                          const float4 *__restrict__ init, float4 *__restrict__ carF, float4 *__restrict__ d_q,
@@ -509,10 +516,10 @@ __global__ void __launch_bounds__(LT *NSEG)
     __shared__ __align__(8) uint64_t fullB[NSTB];
     __shared__ int issuedF[NSTF], issuedB[NSTB];
     __shared__ int s_broken;
-    __shared__ float4 s_a[2][NSEG][LT];   // segment products (forward walk: slot c & 1)
-    __shared__ float4 s_w[NSEG][LT];      // segment weighted sums (reverse walk)
-    __shared__ float4 s_x[NSEG][LT];      // cum just before each segment (reverse walk)
-    __shared__ float4 s_h[NSEG][LT];      // H entering each segment from the right
+    __shared__ float4 s_a[2][NSEG][LT];             // segment products (slot: chunk parity)
+    __shared__ float4 s_w[SELF ? 2 : 1][NSEG][LT];  // segment weighted sums (reverse walk)
+    __shared__ float4 s_x[SELF ? 1 : NSEG][LT];     // cum just before each segment
+    __shared__ float4 s_h[SELF ? 2 : NSEG][LT];     // H entering each segment / the next chunk
 
     const int g = static_cast<int>(blockIdx.x);
     const int b = g / geo.NGb, x0 = (g - b * geo.NGb) * LT * 4;
@@ -582,16 +589,18 @@ __global__ void __launch_bounds__(LT *NSEG)
         for (int j = 0; j < NSTB && j < C; ++j) issueB(j);
 
     float4 Hc = q_zero();   // H entering the current chunk from the right (segment-0 threads)
-    // Carry into the chunk, written by this thread in the forward walk; loaded
-    // one chunk ahead.
+    // Carry into the chunk, written by this lane's segment-0 thread in the
+    // forward walk; loaded one chunk ahead.
     float4 F_next = q_ident();
-    if (seg == 0) F_next = carF[static_cast<long long>(C - 1) * NL + col];
+    if (SELF || seg == 0) F_next = carF[static_cast<long long>(C - 1) * NL + col];
+    if (SELF && seg == 0) s_h[0][lane] = Hc;
+    if (SELF) __syncthreads();
     const long long row0 = static_cast<long long>(b) * geo.S;
     for (int j = 0; j < C; ++j) {
         const int c = C - 1 - j;
-        const int st = j % NSTB;
+        const int st = j % NSTB, sl = j & 1;
         const float4 F = F_next;
-        if (seg == 0 && c > 0) F_next = carF[static_cast<long long>(c - 1) * NL + col];
+        if ((SELF || seg == 0) && c > 0) F_next = carF[static_cast<long long>(c - 1) * NL + col];
         const float4 *Qt = reinterpret_cast<const float4 *>(ring + st * 2 * BQ);
         const float4 *Dt = Qt + T * LT;
         if (!ld_volatile_int(&s_broken) && !wait_stage(&fullB[st], (j / NSTB) & 1, ctl, c * geo.NG + g))
@@ -607,28 +616,42 @@ __global__ void __launch_bounds__(LT *NSEG)
             loc = q_mul(qv[k], loc);
             W = q_fma_cl(W, loc, dv[k]);
         }
-        s_a[0][seg][lane] = loc;
-        s_w[seg][lane] = W;
+        const int ws = SELF ? sl : 0;
+        s_a[sl][seg][lane] = loc;
+        s_w[ws][seg][lane] = W;
         __syncthreads();
         if (threadIdx.x == 0 && !s_broken && j + NSTB < C) issueB(j + NSTB);
-        if (seg == 0) {
-            // The carry forward through the segments, and H backward through
-            // them: two independent chains of NSEG products.
-            float4 X = F, h = Hc;
-#pragma unroll
-            for (int k = 0; k < NSEG; ++k) {
-                const int kr = NSEG - 1 - k;
-                s_x[k][lane] = X;
-                s_h[kr][lane] = h;
-                X = q_mul(s_a[0][k][lane], X);
-                h = q_fma_cl(s_w[kr][lane], s_a[0][kr][lane], h);
+        float4 X, Hn;
+        if constexpr (SELF) {
+            X = F;   // through the earlier segments
+            for (int k = 0; k < seg; ++k) X = q_mul(s_a[sl][k][lane], X);
+            Hn = s_h[sl][lane];   // through the later segments
+            for (int k = NSEG - 1; k > seg; --k) Hn = q_fma_cl(s_w[ws][k][lane], s_a[sl][k][lane], Hn);
+            if (seg == 0) {
+                Hc = q_fma_cl(s_w[ws][0][lane], s_a[sl][0][lane], Hn);
+                s_h[sl ^ 1][lane] = Hc;
+                if (c == 0 && lane_ok) d_init[static_cast<long long>(b) * geo.HJ + hj] = Hc;
             }
-            Hc = h;
-            if (c == 0 && lane_ok) d_init[static_cast<long long>(b) * geo.HJ + hj] = Hc;
+        } else {
+            if (seg == 0) {
+                // The carry forward through the segments, and H backward
+                // through them: two independent chains of NSEG products.
+                float4 Xs = F, h = Hc;
+#pragma unroll
+                for (int k = 0; k < NSEG; ++k) {
+                    const int kr = NSEG - 1 - k;
+                    s_x[k][lane] = Xs;
+                    s_h[kr][lane] = h;
+                    Xs = q_mul(s_a[sl][k][lane], Xs);
+                    h = q_fma_cl(s_w[0][kr][lane], s_a[sl][kr][lane], h);
+                }
+                Hc = h;
+                if (c == 0 && lane_ok) d_init[static_cast<long long>(b) * geo.HJ + hj] = Hc;
+            }
+            __syncthreads();
+            X = s_x[seg][lane];    // cum just before this segment
+            Hn = s_h[seg][lane];   // H entering this segment from the right
         }
-        __syncthreads();
-        const float4 X = s_x[seg][lane];   // cum just before this segment
-        float4 Hn = s_h[seg][lane];         // H entering this segment from the right
         const long long t0 = static_cast<long long>(c) * T + seg * N;
         float4 *dst = d_q + (row0 + t0) * geo.HJ + hj;
         if (lane_ok && t0 + N <= geo.S) {
@@ -702,9 +725,9 @@ struct Variant {
         true, reinterpret_cast<const void *>(qs::quat_walk_fwd_kernel<LT, NSEG, N, NST>), nullptr,  \
             false, LT, NSEG, N, qs::walk_fwd_smem_bytes(LT, NSEG, N, NST)                           \
     }
-#define QS_WALK_BWD(LT, NSEG, N, NSTF, NSTB)                                                        \
+#define QS_WALK_BWD(LT, NSEG, N, NSTF, NSTB, SELF)                                                  \
     Variant {                                                                                       \
-        true, reinterpret_cast<const void *>(qs::quat_walk_bwd_kernel<LT, NSEG, N, NSTF, NSTB>),    \
+        true, reinterpret_cast<const void *>(qs::quat_walk_bwd_kernel<LT, NSEG, N, NSTF, NSTB, SELF>), \
             nullptr, true, LT, NSEG, N, qs::walk_bwd_smem_bytes(LT, NSEG, N, NSTF, NSTB)            \
     }
 const Variant kFwdVariants[] = {
@@ -722,10 +745,12 @@ const Variant kBwdVariants[] = {
     QS_VARIANT(true, 32, 4),           // 1: three kernels, 32-step chunks
     QS_VARIANT(true, 64, 4),           // 2: three kernels, 64 lanes x 16 steps
     QS_VARIANT(true, 64, 8),           // 3: three kernels, 64 lanes x 32 steps
-    QS_WALK_BWD(16, 8, 8, 4, 2),       // 4: walk, 16 lanes x 64 steps (128 threads), 64 KiB rings
-    QS_WALK_BWD(16, 8, 8, 6, 3),       // 5: walk, 16 lanes x 64 steps, 96 KiB rings
-    QS_WALK_BWD(32, 8, 8, 6, 3),       // 6: walk, 32 lanes x 64 steps, 192 KiB rings
-    QS_WALK_BWD(32, 8, 4, 6, 3),       // 7: walk, 32 lanes x 32 steps, 96 KiB rings
+    QS_WALK_BWD(16, 8, 8, 4, 2, false),   // 4: walk, 16 lanes x 64 steps (128 threads), 64 KiB rings, one fold per lane
+    QS_WALK_BWD(16, 8, 8, 6, 3, false),   // 5: walk, 16 lanes x 64 steps, 96 KiB rings
+    QS_WALK_BWD(32, 8, 8, 6, 3, false),   // 6: walk, 32 lanes x 64 steps, 192 KiB rings
+    QS_WALK_BWD(32, 8, 4, 6, 3, false),   // 7: walk, 32 lanes x 32 steps, 96 KiB rings
+    QS_WALK_BWD(16, 8, 8, 4, 2, true),    // 8: walk, 16 lanes x 64 steps, each thread folds its own carries
+    QS_WALK_BWD(32, 8, 8, 6, 3, true),    // 9: walk, 32 lanes x 64 steps, each thread folds its own carries
 };
 #undef QS_VARIANT
 #undef QS_WALK_FWD

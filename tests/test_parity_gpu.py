@@ -179,7 +179,7 @@ def test_empty_sizes(dev):
 
 
 # Variants 0-3: aggregate / carry / apply kernels; the rest: walk kernels.
-N_FWD_VARIANTS, N_BWD_VARIANTS = 8, 8
+N_FWD_VARIANTS, N_BWD_VARIANTS = 8, 10
 
 
 @pytest.mark.parametrize("variant", range(max(N_FWD_VARIANTS, N_BWD_VARIANTS)))
