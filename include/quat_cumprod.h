@@ -144,6 +144,44 @@ int quat_cumprod_bwd_noalloc(const float *q, const float *init, const float *d_c
                              int64_t B, int64_t S, int64_t H, int64_t J, void *stream);
 
 /*
+ * Chunk carries.  A training step that keeps something between forward and
+ * backward can skip the backward's recomputation of the forward carries: the
+ * forward below also writes the state entering every QS_CARRY_STEPS-step
+ * chunk,
+ *
+ *     carries[b, c, h, j] = cum[b, c*QS_CARRY_STEPS - 1, h, j]   (init for c = 0),
+ *
+ * an extra [B, ceil(S / QS_CARRY_STEPS), H, J, 4] fp32 tensor (1/64 of q),
+ * and the backward below takes it in place of init.  The page's autodiff node
+ * deliberately keeps only q and init (burn-mamba `mamba3/quat_scan/backward.rs`,
+ * `QuatScanBackward` / `State`: the leaves, no scan intermediates); these two
+ * calls are the variant that keeps the carries as well, so that the backward
+ * reads q once instead of twice.  Results equal quat_cumprod_fwd and
+ * quat_cumprod_bwd (with init = carries[:, 0]) up to rounding order.
+ */
+#define QS_CARRY_STEPS 64
+
+/*
+ * Forward scan that also writes `carries` (device, caller-owned, 16-byte
+ * aligned, overlapping nothing else).  Arguments, layout and errors otherwise
+ * as quat_cumprod_fwd.
+ */
+int quat_cumprod_fwd_carries(const float *q, const float *init, float *cum, float *carries,
+                             int64_t B, int64_t S, int64_t H, int64_t J, void *stream);
+
+/*
+ * Backward from the carries written by quat_cumprod_fwd_carries for the same
+ * q and init: writes d_q and d_init as quat_cumprod_bwd(q, carries[:, 0],
+ * d_cum) would.  When the lane groups are too few for a walk (see
+ * quat_cumprod_plan) the carries serve only as init and the backward
+ * recomputes the rest.  Arguments, layout and errors otherwise as
+ * quat_cumprod_bwd.
+ */
+int quat_cumprod_bwd_carries(const float *q, const float *carries, const float *d_cum,
+                             float *d_q, float *d_init,
+                             int64_t B, int64_t S, int64_t H, int64_t J, void *stream);
+
+/*
  * Synchronizes `stream`, then returns QS_ERR_TIMEOUT if any call enqueued on it
  * since the previous quat_cumprod_status() recorded a device-side timeout
  * (its outputs are then invalid), QS_ERR_CUDA if the synchronization failed,
@@ -156,12 +194,14 @@ int quat_cumprod_status(void *stream);
  * current device, and how many kernels it launches: 1 for a walk (one CTA
  * per lane group streams the whole sequence), 3 for aggregate / carry /
  * apply (the sequence split into independent tiles, chosen when there are
- * too few lane groups to fill the GPU).  `bwd` selects the backward.  Writes
+ * too few lane groups to fill the GPU), plus 1 when the forward exports its
+ * carries from that path.  `call`: 0 quat_cumprod_fwd, 1 quat_cumprod_bwd,
+ * 2 quat_cumprod_fwd_carries, 3 quat_cumprod_bwd_carries.  Writes
  * *variant = -1 and *kernels = 0 when the call would launch nothing.  Returns
- * the status the call's argument and device checks would return.  Nothing is
- * enqueued.
+ * the status the call's size and device checks would return (QS_ERR_DIMS for
+ * an unknown `call`).  Nothing is enqueued.
  */
-int quat_cumprod_plan(int bwd, int64_t B, int64_t S, int64_t H, int64_t J, int *variant, int *kernels);
+int quat_cumprod_plan(int call, int64_t B, int64_t S, int64_t H, int64_t J, int *variant, int *kernels);
 
 /* Static, human-readable description of a status code. */
 const char *quat_cumprod_strerror(int status);

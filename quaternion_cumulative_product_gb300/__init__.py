@@ -20,9 +20,9 @@ import threading
 __all__ = [
     "QS_OK", "QS_ERR_NULL", "QS_ERR_DIMS", "QS_ERR_MISALIGNED", "QS_ERR_ALIAS",
     "QS_ERR_CUDA", "QS_ERR_TIMEOUT", "QS_ERR_NOMEM", "QS_ERR_DEVICE", "QS_ERR_SCRATCH",
-    "QS_NOALLOC_MAX_TILES", "QuatScanError", "library_path", "load_library", "quat_cumprod_fwd",
-    "quat_cumprod_bwd", "quat_cumprod_bwd_noalloc", "quat_cumprod_plan", "quat_cumprod_status",
-    "quat_cumprod_strerror",
+    "QS_NOALLOC_MAX_TILES", "QS_CARRY_STEPS", "QuatScanError", "library_path", "load_library",
+    "quat_cumprod_fwd", "quat_cumprod_bwd", "quat_cumprod_fwd_carries", "quat_cumprod_bwd_carries",
+    "quat_cumprod_bwd_noalloc", "quat_cumprod_plan", "quat_cumprod_status", "quat_cumprod_strerror",
 ]
 
 QS_OK = 0
@@ -35,6 +35,9 @@ QS_ERR_TIMEOUT = -6
 QS_ERR_NOMEM = -7
 QS_ERR_DEVICE = -8
 QS_ERR_SCRATCH = -9
+
+# Steps per chunk of the carries written by quat_cumprod_fwd_carries.
+QS_CARRY_STEPS = 64
 
 # Work tiles (B * ceil(H*J/32) * ceil(S/64)) that quat_cumprod_bwd_noalloc's
 # fixed scratch array holds.
@@ -75,6 +78,10 @@ def load_library():
         lib.quat_cumprod_bwd.restype = ctypes.c_int
         lib.quat_cumprod_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, vp]
         lib.quat_cumprod_bwd_noalloc.restype = ctypes.c_int
+        lib.quat_cumprod_fwd_carries.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, vp]
+        lib.quat_cumprod_fwd_carries.restype = ctypes.c_int
+        lib.quat_cumprod_bwd_carries.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, vp]
+        lib.quat_cumprod_bwd_carries.restype = ctypes.c_int
         ip = ctypes.POINTER(ctypes.c_int)
         lib.quat_cumprod_plan.argtypes = [ctypes.c_int, i64, i64, i64, i64, ip, ip]
         lib.quat_cumprod_plan.restype = ctypes.c_int
@@ -182,6 +189,66 @@ def quat_cumprod_bwd(q, init, d_cum, d_q=None, d_init=None, stream=None):
     return d_q, d_init
 
 
+def _carries_shape(q):
+    B, S, H, J, _ = q.shape
+    return (B, (S + QS_CARRY_STEPS - 1) // QS_CARRY_STEPS, H, J, 4)
+
+
+def quat_cumprod_fwd_carries(q, init, cum=None, carries=None, stream=None):
+    """``quat_cumprod_fwd`` that also returns the chunk carries.
+
+    ``carries[b, c] = cum[b, c*QS_CARRY_STEPS - 1]`` (``init`` for ``c = 0``),
+    shape ``[B, ceil(S/64), H, J, 4]``.  Returns ``(cum, carries)``.
+    """
+    torch = _torch()
+    B, S, H, J = _dims(q, init)
+    if cum is None:
+        cum = torch.empty_like(q)
+    else:
+        _check_tensor("cum", cum, q.shape, q.device)
+    if carries is None:
+        carries = torch.empty(_carries_shape(q), dtype=q.dtype, device=q.device)
+    else:
+        _check_tensor("carries", carries, _carries_shape(q), q.device)
+    with torch.cuda.device(q.device):
+        rc = load_library().quat_cumprod_fwd_carries(
+            ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(init.data_ptr()), ctypes.c_void_p(cum.data_ptr()),
+            ctypes.c_void_p(carries.data_ptr()), B, S, H, J, _stream_handle(stream, q.device))
+    if rc != QS_OK:
+        raise QuatScanError(rc, "quat_cumprod_fwd_carries")
+    return cum, carries
+
+
+def quat_cumprod_bwd_carries(q, carries, d_cum, d_q=None, d_init=None, stream=None):
+    """``quat_cumprod_bwd`` from the carries of ``quat_cumprod_fwd_carries``.
+
+    Returns ``(d_q, d_init)``; ``d_init`` has the shape ``[B, H, J, 4]``.
+    """
+    torch = _torch()
+    if q.dim() != 5 or q.shape[-1] != 4:
+        raise ValueError(f"q must be [B,S,H,J,4], got {tuple(q.shape)}")
+    B, S, H, J, _ = q.shape
+    _check_tensor("q", q, q.shape)
+    _check_tensor("carries", carries, _carries_shape(q), q.device)
+    _check_tensor("d_cum", d_cum, q.shape, q.device)
+    if d_q is None:
+        d_q = torch.empty_like(q)
+    else:
+        _check_tensor("d_q", d_q, q.shape, q.device)
+    if d_init is None:
+        d_init = torch.empty((B, H, J, 4), dtype=q.dtype, device=q.device)
+    else:
+        _check_tensor("d_init", d_init, (B, H, J, 4), q.device)
+    with torch.cuda.device(q.device):
+        rc = load_library().quat_cumprod_bwd_carries(
+            ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(carries.data_ptr()),
+            ctypes.c_void_p(d_cum.data_ptr()), ctypes.c_void_p(d_q.data_ptr()),
+            ctypes.c_void_p(d_init.data_ptr()), B, S, H, J, _stream_handle(stream, q.device))
+    if rc != QS_OK:
+        raise QuatScanError(rc, "quat_cumprod_bwd_carries")
+    return d_q, d_init
+
+
 def quat_cumprod_bwd_noalloc(q, init, d_cum, d_q, d_init, stream=None):
     """``quat_cumprod_bwd`` into caller-owned ``d_q`` and ``d_init``, with no allocation.
 
@@ -207,13 +274,21 @@ def quat_cumprod_bwd_noalloc(q, init, d_cum, d_q, d_init, stream=None):
     return d_q, d_init
 
 
-def quat_cumprod_plan(bwd, B, S, H, J, device=None):
-    """(variant, kernels) a call with these sizes would use on ``device`` (launches nothing)."""
+_PLAN_CALLS = {"fwd": 0, "bwd": 1, "fwd_carries": 2, "bwd_carries": 3}
+
+
+def quat_cumprod_plan(call, B, S, H, J, device=None):
+    """(variant, kernels) a call with these sizes would use on ``device`` (launches nothing).
+
+    ``call``: ``"fwd"``, ``"bwd"``, ``"fwd_carries"``, ``"bwd_carries"`` (or
+    False / True for the first two).
+    """
     torch = _torch()
     device = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    code = _PLAN_CALLS[call] if isinstance(call, str) else int(bool(call))
     v, k = ctypes.c_int(0), ctypes.c_int(0)
     with torch.cuda.device(device):
-        rc = load_library().quat_cumprod_plan(int(bool(bwd)), B, S, H, J, ctypes.byref(v), ctypes.byref(k))
+        rc = load_library().quat_cumprod_plan(code, B, S, H, J, ctypes.byref(v), ctypes.byref(k))
     if rc != QS_OK:
         raise QuatScanError(rc, "quat_cumprod_plan")
     return v.value, k.value

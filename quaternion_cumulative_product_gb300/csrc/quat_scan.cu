@@ -417,10 +417,13 @@ __device__ __forceinline__ void drain_ring(uint64_t *bars, const int *issued, co
     }
 }
 
+// `carries` (optional, may be null): [B, C, H*J] float4, the state entering
+// every chunk, carries[b, c] = cum[b, c*T - 1] (init for c = 0).
 template <int LT, int NSEG, int N, int NST>
 __global__ void __launch_bounds__(LT *NSEG)
     quat_walk_fwd_kernel(const __grid_constant__ CUtensorMap qmap, const float4 *__restrict__ init,
-                         float4 *__restrict__ out, const Geometry geo, const Control ctl) {
+                         float4 *__restrict__ out, float4 *__restrict__ carries, const Geometry geo,
+                         const Control ctl) {
     constexpr int T = NSEG * N;
     constexpr uint32_t BYTES = T * LT * 16;
     extern __shared__ unsigned char smem_raw[];
@@ -479,6 +482,8 @@ __global__ void __launch_bounds__(LT *NSEG)
         for (int k = 0; k < seg; ++k) P = q_mul(s_a[sl][k][lane], P);
         const float4 Y = q_mul(P, s_x[sl][lane]);
         if (seg == 0) {
+            if (carries != nullptr && lane_ok)
+                carries[(static_cast<long long>(b) * C + c) * geo.HJ + hj] = R;   // state entering chunk c
             float4 L = q_ident();
 #pragma unroll
             for (int k = 0; k < NSEG; ++k) L = q_mul(s_a[sl][k][lane], L);
@@ -503,11 +508,16 @@ __global__ void __launch_bounds__(LT *NSEG)
 // segments) and cotangent (through the later ones), about NSEG-1 products,
 // and the chunk needs no second barrier; segment 0 publishes the cotangent
 // entering the next chunk one chunk ahead.
-template <int LT, int NSEG, int N, int NSTF, int NSTB, bool SELF>
+//
+// GIVEN = true: the chunk carries come from the caller, `given` = [B, C, H*J]
+// float4 with given[b, c] = cum[b, c*T - 1] (what the forward walk writes as
+// `carries`); the forward walk is skipped and `init` and `carF` are unused.
+template <int LT, int NSEG, int N, int NSTF, int NSTB, bool SELF, bool GIVEN>
 __global__ void __launch_bounds__(LT *NSEG)
     quat_walk_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap dmap,
-                         const float4 *__restrict__ init, float4 *__restrict__ carF, float4 *__restrict__ d_q,
-                         float4 *__restrict__ d_init, const Geometry geo, const Control ctl) {
+                         const float4 *__restrict__ init, float4 *__restrict__ carF,
+                         const float4 *__restrict__ given, float4 *__restrict__ d_q, float4 *__restrict__ d_init,
+                         const Geometry geo, const Control ctl) {
     constexpr int T = NSEG * N;
     constexpr uint32_t BQ = T * LT * 16;   // one operand of one chunk
     extern __shared__ unsigned char smem_raw[];
@@ -543,35 +553,38 @@ __global__ void __launch_bounds__(LT *NSEG)
         s_broken = 0;
     }
     __syncthreads();
-    const uint64_t keep = l2_policy_evict_last(), drop = l2_policy_evict_first();
+    const uint64_t drop = l2_policy_evict_first();
 
-    // ---- forward walk over q: carries F_c --------------------------------
-    auto issueF = [&](int c) {
-        const int st = c % NSTF;
-        ++issuedF[st];
-        mbar_arrive_expect_tx(&fullF[st], BQ + (c * geo.NG + g == ctl.stall_tile ? 16u : 0u));
-        tma_load_3d_hint(ring + st * BQ, &qmap, x0, c * T, b, &fullF[st], keep);
-    };
-    if (threadIdx.x == 0)
-        for (int c = 0; c < NSTF && c < C; ++c) issueF(c);
+    if constexpr (!GIVEN) {
+        // ---- forward walk over q: carries F_c --------------------------------
+        const uint64_t keep = l2_policy_evict_last();
+        auto issueF = [&](int c) {
+            const int st = c % NSTF;
+            ++issuedF[st];
+            mbar_arrive_expect_tx(&fullF[st], BQ + (c * geo.NG + g == ctl.stall_tile ? 16u : 0u));
+            tma_load_3d_hint(ring + st * BQ, &qmap, x0, c * T, b, &fullF[st], keep);
+        };
+        if (threadIdx.x == 0)
+            for (int c = 0; c < NSTF && c < C; ++c) issueF(c);
 
-    float4 R = q_ident();
-    if (seg == 0 && lane_ok) R = init[static_cast<long long>(b) * geo.HJ + hj];
-    for (int c = 0; c < C; ++c) {
-        const int st = c % NSTF, sl = c & 1;
-        const float4 *Qt = reinterpret_cast<const float4 *>(ring + st * BQ);
-        if (!ld_volatile_int(&s_broken) && !wait_stage(&fullF[st], (c / NSTF) & 1, ctl, c * geo.NG + g))
-            s_broken = 1;
-        float4 loc = q_ident();
+        float4 R = q_ident();
+        if (seg == 0 && lane_ok) R = init[static_cast<long long>(b) * geo.HJ + hj];
+        for (int c = 0; c < C; ++c) {
+            const int st = c % NSTF, sl = c & 1;
+            const float4 *Qt = reinterpret_cast<const float4 *>(ring + st * BQ);
+            if (!ld_volatile_int(&s_broken) && !wait_stage(&fullF[st], (c / NSTF) & 1, ctl, c * geo.NG + g))
+                s_broken = 1;
+            float4 loc = q_ident();
 #pragma unroll
-        for (int k = 0; k < N; ++k) loc = q_mul(Qt[(seg * N + k) * LT + lane], loc);
-        s_a[sl][seg][lane] = loc;
-        __syncthreads();
-        if (threadIdx.x == 0 && !s_broken && c + NSTF < C) issueF(c + NSTF);
-        if (seg == 0) {   // segment 0 carries the lane through the chunk
-            carF[static_cast<long long>(c) * NL + col] = R;
+            for (int k = 0; k < N; ++k) loc = q_mul(Qt[(seg * N + k) * LT + lane], loc);
+            s_a[sl][seg][lane] = loc;
+            __syncthreads();
+            if (threadIdx.x == 0 && !s_broken && c + NSTF < C) issueF(c + NSTF);
+            if (seg == 0) {   // segment 0 carries the lane through the chunk
+                carF[static_cast<long long>(c) * NL + col] = R;
 #pragma unroll
-            for (int k = 0; k < NSEG; ++k) R = q_mul(s_a[sl][k][lane], R);
+                for (int k = 0; k < NSEG; ++k) R = q_mul(s_a[sl][k][lane], R);
+            }
         }
     }
     __syncthreads();   // every read of the forward ring is done before the reverse ring reuses it
@@ -591,8 +604,12 @@ __global__ void __launch_bounds__(LT *NSEG)
     float4 Hc = q_zero();   // H entering the current chunk from the right (segment-0 threads)
     // Carry into the chunk, written by this lane's segment-0 thread in the
     // forward walk; loaded one chunk ahead.
+    auto carry_of = [&](int c) -> float4 {
+        if constexpr (GIVEN) return lane_ok ? given[(static_cast<long long>(b) * C + c) * geo.HJ + hj] : q_ident();
+        else return carF[static_cast<long long>(c) * NL + col];
+    };
     float4 F_next = q_ident();
-    if (SELF || seg == 0) F_next = carF[static_cast<long long>(C - 1) * NL + col];
+    if (SELF || seg == 0) F_next = carry_of(C - 1);
     if (SELF && seg == 0) s_h[0][lane] = Hc;
     if (SELF) __syncthreads();
     const long long row0 = static_cast<long long>(b) * geo.S;
@@ -600,7 +617,7 @@ __global__ void __launch_bounds__(LT *NSEG)
         const int c = C - 1 - j;
         const int st = j % NSTB, sl = j & 1;
         const float4 F = F_next;
-        if ((SELF || seg == 0) && c > 0) F_next = carF[static_cast<long long>(c - 1) * NL + col];
+        if ((SELF || seg == 0) && c > 0) F_next = carry_of(c - 1);
         const float4 *Qt = reinterpret_cast<const float4 *>(ring + st * 2 * BQ);
         const float4 *Dt = Qt + T * LT;
         if (!ld_volatile_int(&s_broken) && !wait_stage(&fullB[st], (j / NSTB) & 1, ctl, c * geo.NG + g))
@@ -676,6 +693,20 @@ __global__ void __launch_bounds__(LT *NSEG)
     }
 }
 
+// Copies the chunk carries the carry kernel left in the workspace
+// (chunk-major, padded lanes) to the caller's [B, C, H*J] layout.
+__global__ void __launch_bounds__(NTHREADS)
+    quat_export_carries_kernel(const float4 *__restrict__ carF, float4 *__restrict__ carries, const Geometry geo,
+                               int LT, long long total) {
+    const long long i = static_cast<long long>(blockIdx.x) * NTHREADS + threadIdx.x;
+    if (i >= total) return;
+    const long long bc = i / geo.HJ;
+    const int hj = static_cast<int>(i - bc * geo.HJ);
+    const int b = static_cast<int>(bc / geo.C), c = static_cast<int>(bc - static_cast<long long>(b) * geo.C);
+    const long long g = static_cast<long long>(b) * geo.NGb + hj / LT;
+    carries[i] = carF[static_cast<long long>(c) * geo.NL + g * LT + hj % LT];
+}
+
 // Shared memory of a tile kernel (dynamic part).
 __host__ __device__ constexpr size_t tile_smem_bytes(bool bwd, int lt, int n) {
     return 128 + size_t(bwd ? 2 : 1) * (NTHREADS / lt) * n * lt * 16;
@@ -727,7 +758,7 @@ struct Variant {
     }
 #define QS_WALK_BWD(LT, NSEG, N, NSTF, NSTB, SELF)                                                  \
     Variant {                                                                                       \
-        true, reinterpret_cast<const void *>(qs::quat_walk_bwd_kernel<LT, NSEG, N, NSTF, NSTB, SELF>), \
+        true, reinterpret_cast<const void *>(qs::quat_walk_bwd_kernel<LT, NSEG, N, NSTF, NSTB, SELF, false>), \
             nullptr, true, LT, NSEG, N, qs::walk_bwd_smem_bytes(LT, NSEG, N, NSTF, NSTB)            \
     }
 const Variant kFwdVariants[] = {
@@ -752,6 +783,15 @@ const Variant kBwdVariants[] = {
     QS_WALK_BWD(16, 8, 8, 4, 2, true),    // 8: walk, 16 lanes x 64 steps, each thread folds its own carries
     QS_WALK_BWD(32, 8, 8, 6, 3, true),    // 9: walk, 32 lanes x 64 steps, each thread folds its own carries
 };
+// The backward from caller-provided carries: the reverse walk alone.
+const Variant kBwdGiven = Variant{true,
+                                  reinterpret_cast<const void *>(qs::quat_walk_bwd_kernel<16, 8, 8, 1, 2, false, true>),
+                                  nullptr,
+                                  true,
+                                  16,
+                                  8,
+                                  8,
+                                  qs::walk_bwd_smem_bytes(16, 8, 8, 1, 2)};
 #undef QS_VARIANT
 #undef QS_WALK_FWD
 #undef QS_WALK_BWD
@@ -854,6 +894,7 @@ int device_info(DevInfo **out, int *dev_out) {
             };
             for (const Variant &v : kFwdVariants) setup(v);
             for (const Variant &v : kBwdVariants) setup(v);
+            setup(kBwdGiven);
             if (!ok) {
                 cudaGetLastError();
                 d.sms = 0;
@@ -938,19 +979,34 @@ int pick_variant(bool bwd, int64_t B, int64_t HJ, int sms) {
 }
 
 // Everything a call needs, derived from the sizes alone (no device calls).
+// What a call computes besides its outputs.
+enum class Mode {
+    PLAIN,          // quat_cumprod_fwd / quat_cumprod_bwd
+    SAVE_CARRIES,   // forward that also writes the chunk carries
+    FROM_CARRIES,   // backward from caller-provided chunk carries
+};
+
 struct Plan {
     const Variant *v = nullptr;
     int vi = 0;   // index in the variant table
     qs::Geometry geo{};
     long long tiles = 0;
     int carry_lb = 32;   // lanes per block of the carry kernel
-    size_t o_L = 0, o_W = 0, o_F = 0, o_H = 0, ws_bytes = 0;
+    size_t o_L = 0, o_W = 0, o_F = 0, o_H = 0, o_I = 0, ws_bytes = 0;
 };
 
-int make_plan(bool bwd, int64_t B, int64_t S, int64_t HJ, int sms, Plan *pl) {
-    const int vi = pick_variant(bwd, B, HJ, sms);
+int make_plan(bool bwd, int64_t B, int64_t S, int64_t HJ, int sms, Plan *pl, Mode mode = Mode::PLAIN) {
+    int vi = pick_variant(bwd, B, HJ, sms);
+    const Variant *v = bwd ? &kBwdVariants[vi] : &kFwdVariants[vi];
+    if (mode != Mode::PLAIN && v->T() != QS_CARRY_STEPS) {
+        // The carries are defined on QS_CARRY_STEPS-step chunks: keep the
+        // design, take its default configuration (which has that chunk).
+        vi = v->walk ? (bwd ? kWalkBwd : kWalkFwd) : (bwd ? kThreeBwd : kThreeFwd);
+        v = bwd ? &kBwdVariants[vi] : &kFwdVariants[vi];
+    }
+    if (mode == Mode::FROM_CARRIES && v->walk) v = &kBwdGiven;
     pl->vi = vi;
-    pl->v = bwd ? &kBwdVariants[vi] : &kFwdVariants[vi];
+    pl->v = v;
     const int LT = pl->v->lt, T = pl->v->T();
     qs::Geometry &g = pl->geo;
     g.S = S;
@@ -967,7 +1023,7 @@ int make_plan(bool bwd, int64_t B, int64_t S, int64_t HJ, int sms, Plan *pl) {
     size_t off = sizeof(qs::WsHeader);
     if (pl->v->walk) {
         // Walk kernels: status block, then (backward) the carries F_c.
-        if (bwd) {
+        if (bwd && mode != Mode::FROM_CARRIES) {
             pl->o_F = off;
             off = align_up(off + per, 256);
         }
@@ -986,18 +1042,24 @@ int make_plan(bool bwd, int64_t B, int64_t S, int64_t HJ, int sms, Plan *pl) {
         pl->o_H = off;
         off = align_up(off + per, 256);
     }
+    if (mode == Mode::FROM_CARRIES) {   // init = carries[:, 0], made contiguous
+        pl->o_I = off;
+        off = align_up(off + (size_t)B * HJ * 16, 256);
+    }
     pl->ws_bytes = off;
     return QS_OK;
 }
 
+// `carries`: written (Mode::SAVE_CARRIES) or read (Mode::FROM_CARRIES),
+// [B, ceil(S / QS_CARRY_STEPS), H*J] float4; unused otherwise.
 int launch(bool bwd, const float *q, const float *d_cum, float *out, const float *init, float *d_init, int64_t B,
-           int64_t S, int64_t HJ, cudaStream_t stream) {
+           int64_t S, int64_t HJ, cudaStream_t stream, Mode mode = Mode::PLAIN, float *carries = nullptr) {
     DevInfo *di = nullptr;
     int dev = 0;
     int rc = device_info(&di, &dev);
     if (rc != QS_OK) return rc;
     Plan pl;
-    rc = make_plan(bwd, B, S, HJ, di->sms, &pl);
+    rc = make_plan(bwd, B, S, HJ, di->sms, &pl, mode);
     if (rc != QS_OK) return rc;
     unsigned char *ws = nullptr;
     rc = ensure_workspace(dev, stream, pl.ws_bytes, &ws);
@@ -1018,8 +1080,10 @@ int launch(bool bwd, const float *q, const float *d_cum, float *out, const float
         const float4 *init4 = reinterpret_cast<const float4 *>(init);
         float4 *dinit4 = reinterpret_cast<float4 *>(d_init);
         float4 *out4 = reinterpret_cast<float4 *>(out);
-        void *fwd_args[] = {&qmap, &init4, &out4, &pl.geo, &ctl};
-        void *bwd_args[] = {&qmap, &dmap, &init4, &carF, &out4, &dinit4, &pl.geo, &ctl};
+        float4 *save4 = mode == Mode::SAVE_CARRIES ? reinterpret_cast<float4 *>(carries) : nullptr;
+        const float4 *given4 = mode == Mode::FROM_CARRIES ? reinterpret_cast<const float4 *>(carries) : nullptr;
+        void *fwd_args[] = {&qmap, &init4, &out4, &save4, &pl.geo, &ctl};
+        void *bwd_args[] = {&qmap, &dmap, &init4, &carF, &given4, &out4, &dinit4, &pl.geo, &ctl};
         if (cudaLaunchKernel(pl.v->agg, dim3((unsigned)pl.geo.NG), dim3(pl.v->threads()),
                              bwd ? bwd_args : fwd_args, pl.v->smem(), stream) != cudaSuccess) {
             cudaGetLastError();
@@ -1039,6 +1103,16 @@ int launch(bool bwd, const float *q, const float *d_cum, float *out, const float
     }
     ctl.hdr = reinterpret_cast<qs::WsHeader *>(ws);
     const float4 *init4 = reinterpret_cast<const float4 *>(init);
+    if (mode == Mode::FROM_CARRIES) {
+        // init = carries[:, 0]: one row of H*J quaternions per batch entry.
+        const size_t row = (size_t)HJ * 16;
+        if (cudaMemcpy2DAsync(ws + pl.o_I, row, carries, row * pl.geo.C, row, (size_t)B, cudaMemcpyDeviceToDevice,
+                              stream) != cudaSuccess) {
+            cudaGetLastError();
+            return QS_ERR_CUDA;
+        }
+        init4 = reinterpret_cast<const float4 *>(ws + pl.o_I);
+    }
     float4 *dinit4 = reinterpret_cast<float4 *>(d_init);
     float4 *out4 = reinterpret_cast<float4 *>(out);
     const float4 *aggL_c = aggL, *aggW_c = aggW, *carF_c = carF, *carH_c = carH;
@@ -1061,6 +1135,17 @@ int launch(bool bwd, const float *q, const float *d_cum, float *out, const float
             cudaSuccess) {
         cudaGetLastError();
         return QS_ERR_CUDA;
+    }
+    if (mode == Mode::SAVE_CARRIES) {
+        long long total = (long long)B * pl.geo.C * HJ;
+        float4 *dst = reinterpret_cast<float4 *>(carries);
+        void *exp_args[] = {&carF_c, &dst, &pl.geo, &lt, &total};
+        const unsigned blocks = (unsigned)((total + NTHREADS - 1) / NTHREADS);
+        if (cudaLaunchKernel(reinterpret_cast<const void *>(qs::quat_export_carries_kernel), dim3(blocks),
+                             dim3(NTHREADS), exp_args, 0, stream) != cudaSuccess) {
+            cudaGetLastError();
+            return QS_ERR_CUDA;
+        }
     }
     return QS_OK;
 }
@@ -1109,6 +1194,53 @@ extern "C" int quat_cumprod_bwd(const float *q, const float *init, const float *
     return launch(true, q, d_cum, d_q, init, d_init, B, S, HJ, stream);
 }
 
+extern "C" int quat_cumprod_fwd_carries(const float *q, const float *init, float *cum, float *carries, int64_t B,
+                                        int64_t S, int64_t H, int64_t J, void *stream_) {
+    const int dc = check_dims(B, S, H, J);
+    if (dc == 1) return QS_OK;
+    if (dc != QS_OK) return dc;
+    if (!q || !init || !cum || !carries) return QS_ERR_NULL;
+    if (misaligned(q) || misaligned(init) || misaligned(cum) || misaligned(carries)) return QS_ERR_MISALIGNED;
+    const int64_t HJ = H * J;
+    const size_t big = (size_t)B * S * HJ * 16, small = (size_t)B * HJ * 16;
+    const size_t ncar = (size_t)B * ((S + QS_CARRY_STEPS - 1) / QS_CARRY_STEPS) * HJ * 16;
+    if (overlaps(cum, big, q, big) || overlaps(cum, big, init, small) || overlaps(carries, ncar, q, big) ||
+        overlaps(carries, ncar, init, small) || overlaps(carries, ncar, cum, big))
+        return QS_ERR_ALIAS;
+    return launch(false, q, nullptr, cum, init, nullptr, B, S, HJ, static_cast<cudaStream_t>(stream_),
+                  Mode::SAVE_CARRIES, carries);
+}
+
+extern "C" int quat_cumprod_bwd_carries(const float *q, const float *carries, const float *d_cum, float *d_q,
+                                        float *d_init, int64_t B, int64_t S, int64_t H, int64_t J, void *stream_) {
+    const int dc = check_dims(B, S, H, J);
+    if (dc != QS_OK && dc != 1) return dc;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+    const int64_t HJ = H * J;
+    if (dc == 1) {
+        if (S == 0 && B > 0 && HJ > 0) {   // no steps: the gradient of init is zero
+            if (!d_init) return QS_ERR_NULL;
+            if (misaligned(d_init)) return QS_ERR_MISALIGNED;
+            if (cudaMemsetAsync(d_init, 0, (size_t)B * HJ * 16, stream) != cudaSuccess) {
+                cudaGetLastError();
+                return QS_ERR_CUDA;
+            }
+        }
+        return QS_OK;
+    }
+    if (!q || !carries || !d_cum || !d_q || !d_init) return QS_ERR_NULL;
+    if (misaligned(q) || misaligned(carries) || misaligned(d_cum) || misaligned(d_q) || misaligned(d_init))
+        return QS_ERR_MISALIGNED;
+    const size_t big = (size_t)B * S * HJ * 16, small = (size_t)B * HJ * 16;
+    const size_t ncar = (size_t)B * ((S + QS_CARRY_STEPS - 1) / QS_CARRY_STEPS) * HJ * 16;
+    if (overlaps(d_q, big, q, big) || overlaps(d_q, big, carries, ncar) || overlaps(d_q, big, d_cum, big) ||
+        overlaps(d_init, small, q, big) || overlaps(d_init, small, carries, ncar) ||
+        overlaps(d_init, small, d_cum, big) || overlaps(d_q, big, d_init, small))
+        return QS_ERR_ALIAS;
+    return launch(true, q, d_cum, d_q, nullptr, d_init, B, S, HJ, stream, Mode::FROM_CARRIES,
+                  const_cast<float *>(carries));
+}
+
 extern "C" int quat_cumprod_status(void *stream_) {
     cudaStream_t stream = static_cast<cudaStream_t>(stream_);
     if (cudaStreamSynchronize(stream) != cudaSuccess) {
@@ -1140,8 +1272,11 @@ extern "C" int quat_cumprod_status(void *stream_) {
     return QS_ERR_TIMEOUT;
 }
 
-extern "C" int quat_cumprod_plan(int bwd, int64_t B, int64_t S, int64_t H, int64_t J, int *variant, int *kernels) {
+extern "C" int quat_cumprod_plan(int call, int64_t B, int64_t S, int64_t H, int64_t J, int *variant, int *kernels) {
     if (!variant || !kernels) return QS_ERR_NULL;
+    if (call < 0 || call > 3) return QS_ERR_DIMS;
+    const bool bwd = (call & 1) != 0;
+    const Mode mode = call == 2 ? Mode::SAVE_CARRIES : call == 3 ? Mode::FROM_CARRIES : Mode::PLAIN;
     const int dc = check_dims(B, S, H, J);
     if (dc != QS_OK && dc != 1) return dc;
     if (dc == 1) {   // nothing to launch (the backward may write d_init with a memset)
@@ -1154,10 +1289,10 @@ extern "C" int quat_cumprod_plan(int bwd, int64_t B, int64_t S, int64_t H, int64
     int rc = device_info(&di, &dev);
     if (rc != QS_OK) return rc;
     Plan pl;
-    rc = make_plan(bwd != 0, B, S, H * J, di->sms, &pl);
+    rc = make_plan(bwd, B, S, H * J, di->sms, &pl, mode);
     if (rc != QS_OK) return rc;
     *variant = pl.vi;
-    *kernels = pl.v->walk ? 1 : 3;
+    *kernels = pl.v->walk ? 1 : (mode == Mode::SAVE_CARRIES ? 4 : 3);
     return QS_OK;
 }
 

@@ -154,3 +154,40 @@ def test_plan_query_argument_checks(lib):
     assert lib.quat_cumprod_plan(0, 1, -4, 1, 1, ctypes.byref(v), ctypes.byref(k)) == qs.QS_ERR_DIMS
     assert lib.quat_cumprod_plan(1, 0, 4, 1, 1, ctypes.byref(v), ctypes.byref(k)) == qs.QS_OK
     assert (v.value, k.value) == (-1, 0)
+
+
+def test_carry_calls_argument_checks_before_any_cuda_call(lib):
+    # [1, 100, 1, 1, 4]: q / cum / d_cum are 1600 bytes, carries 2 chunks = 32 bytes
+    q, i, c, car, d, gq, gi = (k << 20 for k in range(1, 8))
+    f = lib.quat_cumprod_fwd_carries
+    assert f(_p(q), _p(i), _p(c), _p(car), 1, -1, 1, 1, None) == qs.QS_ERR_DIMS
+    assert f(None, None, None, None, 0, 100, 1, 1, None) == qs.QS_OK
+    for k in range(4):
+        ptrs = [_p(q), _p(i), _p(c), _p(car)]
+        ptrs[k] = None
+        assert f(*ptrs, 1, 100, 1, 1, None) == qs.QS_ERR_NULL
+        ptrs = [_p(q), _p(i), _p(c), _p(car)]
+        ptrs[k] = _p([q, i, c, car][k] + 8)
+        assert f(*ptrs, 1, 100, 1, 1, None) == qs.QS_ERR_MISALIGNED
+    assert f(_p(q), _p(i), _p(c), _p(c + 16), 1, 100, 1, 1, None) == qs.QS_ERR_ALIAS     # carries in cum
+    assert f(_p(q), _p(i), _p(c), _p(q + 1584), 1, 100, 1, 1, None) == qs.QS_ERR_ALIAS   # carries in q
+    assert f(_p(q), _p(i), _p(c), _p(i - 16), 1, 100, 1, 1, None) == qs.QS_ERR_ALIAS     # overlaps init
+    g = lib.quat_cumprod_bwd_carries
+    assert g(_p(q), _p(car), _p(d), _p(gq), _p(gi), 1, -1, 1, 1, None) == qs.QS_ERR_DIMS
+    assert g(None, None, None, None, None, 2, 0, 2, 2, None) == qs.QS_ERR_NULL   # S == 0 writes d_init
+    for k in range(5):
+        ptrs = [_p(q), _p(car), _p(d), _p(gq), _p(gi)]
+        ptrs[k] = None
+        assert g(*ptrs, 1, 100, 1, 1, None) == qs.QS_ERR_NULL
+        ptrs = [_p(q), _p(car), _p(d), _p(gq), _p(gi)]
+        ptrs[k] = _p([q, car, d, gq, gi][k] + 4)
+        assert g(*ptrs, 1, 100, 1, 1, None) == qs.QS_ERR_MISALIGNED
+    assert g(_p(q), _p(car), _p(d), _p(car - 1584), _p(gi), 1, 100, 1, 1, None) == qs.QS_ERR_ALIAS
+    assert g(_p(q), _p(car), _p(d), _p(gq), _p(car + 16), 1, 100, 1, 1, None) == qs.QS_ERR_ALIAS
+
+
+def test_plan_rejects_unknown_call(lib):
+    v, k = ctypes.c_int(0), ctypes.c_int(0)
+    assert lib.quat_cumprod_plan(4, 1, 4, 1, 1, ctypes.byref(v), ctypes.byref(k)) == qs.QS_ERR_DIMS
+    assert lib.quat_cumprod_plan(-1, 1, 4, 1, 1, ctypes.byref(v), ctypes.byref(k)) == qs.QS_ERR_DIMS
+    assert lib.quat_cumprod_plan(3, 0, 4, 1, 1, ctypes.byref(v), ctypes.byref(k)) == qs.QS_OK
