@@ -380,6 +380,37 @@ def run_ours(args, w, world, rank, local):
     cstep_ms = reduce_max(cfwd_ms + cbwd_ms, dev)
     del carries
 
+    # ---- the same step with bfloat16 tensors (fp32 arithmetic) ---------------
+    bq, bi, bd = q.to(torch.bfloat16), init.to(torch.bfloat16), d_cum.to(torch.bfloat16)
+    bcum, bdq, bdi = torch.empty_like(bq), torch.empty_like(bq), torch.empty_like(bi)
+    even = (w.H * w.J) % 2 == 0
+    if even:
+        for _ in range(args.warmup):
+            qs.quat_cumprod_fwd_bf16(bq, bi, bcum)
+            qs.quat_cumprod_bwd_bf16(bq, bi, bd, bdq, bdi)
+        bev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+                torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        torch.cuda.synchronize(dev)
+        barrier(dev)
+        for i in range(args.steps):
+            if flush:
+                scratch.zero_()
+            e0, e1, e2 = bev[i]
+            e0.record(stream)
+            qs.quat_cumprod_fwd_bf16(bq, bi, bcum)
+            e1.record(stream)
+            qs.quat_cumprod_bwd_bf16(bq, bi, bd, bdq, bdi)
+            e2.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(dev)
+        st = qs.quat_cumprod_status(device=dev)
+        if st != qs.QS_OK:
+            raise RuntimeError(f"device status after the bf16 region: {qs.quat_cumprod_strerror(st)}")
+        bfwd_ms = statistics.mean(a.elapsed_time(b) for a, b, _ in bev)
+        bbwd_ms = statistics.mean(b.elapsed_time(c) for _, b, c in bev)
+        bstep_ms = reduce_max(bfwd_ms + bbwd_ms, dev)
+    del bq, bi, bd, bcum, bdq, bdi
+
     # ---- end to end through the public API with pinned host buffers ---------
     h_q = torch.from_numpy(q_np).pin_memory()
     h_init = torch.from_numpy(init_np).pin_memory()
@@ -463,6 +494,15 @@ def run_ours(args, w, world, rank, local):
             "bwd_achieved_gbs": BWD_BYTES_PER_ELEMENT * E / (cbwd_ms * 1e-3) / 1e9,
             "bwd_frac": BWD_BYTES_PER_ELEMENT * E / (cbwd_ms * 1e-3) / 1e9 / peak,
             "kernels_per_step": cfwd_kernels + cbwd_kernels},
+        "bf16": None if not even else {
+            "note": "every tensor bfloat16, fp32 arithmetic; algorithmic bytes 16 (fwd) / 24 (bwd) per element",
+            "value": weak_scaling_value(world, E, bstep_ms), "unit": UNIT, "ms_per_step": bstep_ms,
+            "fwd_ms": bfwd_ms, "bwd_ms": bbwd_ms,
+            "fwd_achieved_gbs": 16 * E / (bfwd_ms * 1e-3) / 1e9,
+            "fwd_frac": 16 * E / (bfwd_ms * 1e-3) / 1e9 / peak,
+            "bwd_achieved_gbs": 24 * E / (bbwd_ms * 1e-3) / 1e9,
+            "bwd_frac": 24 * E / (bbwd_ms * 1e-3) / 1e9 / peak,
+            "kernels_per_step": 2},
         "cpu_baseline": cpu,
         "e2e": {"value": weak_scaling_value(world, E, e2e_ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "steps": e2e_steps},

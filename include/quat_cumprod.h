@@ -182,6 +182,26 @@ int quat_cumprod_bwd_carries(const float *q, const float *carries, const float *
                              int64_t B, int64_t S, int64_t H, int64_t J, void *stream);
 
 /*
+ * bfloat16 I/O.  The same scan and backward with every tensor (q, init, cum,
+ * d_cum, d_q, d_init) in bfloat16: a quaternion is four bfloat16 bit patterns
+ * [w, x, y, z] (8 bytes, passed as uint16_t), laid out as above.  The
+ * arithmetic is fp32 throughout (chunk carries included); each output is
+ * rounded to the nearest bfloat16 (ties to even) once, when it is stored, so
+ * an output differs from the exact result for the bfloat16 inputs by at most
+ * half a bfloat16 ulp (2^-8 of its magnitude) plus the fp32 error of the fp32
+ * calls.  Requires
+ * H*J even (TMA row strides are multiples of 16 bytes; QS_ERR_DIMS
+ * otherwise); pointers 16-byte aligned.  Uses the walk kernels for every size.
+ * The pages define the scan in full precision; this halves the bytes moved
+ * (8 bytes per quaternion instead of 16).
+ */
+int quat_cumprod_fwd_bf16(const uint16_t *q, const uint16_t *init, uint16_t *cum,
+                          int64_t B, int64_t S, int64_t H, int64_t J, void *stream);
+int quat_cumprod_bwd_bf16(const uint16_t *q, const uint16_t *init, const uint16_t *d_cum,
+                          uint16_t *d_q, uint16_t *d_init,
+                          int64_t B, int64_t S, int64_t H, int64_t J, void *stream);
+
+/*
  * Synchronizes `stream`, then returns QS_ERR_TIMEOUT if any call enqueued on it
  * since the previous quat_cumprod_status() recorded a device-side timeout
  * (its outputs are then invalid), QS_ERR_CUDA if the synchronization failed,
@@ -196,7 +216,8 @@ int quat_cumprod_status(void *stream);
  * apply (the sequence split into independent tiles, chosen when there are
  * too few lane groups to fill the GPU), plus 1 when the forward exports its
  * carries from that path.  `call`: 0 quat_cumprod_fwd, 1 quat_cumprod_bwd,
- * 2 quat_cumprod_fwd_carries, 3 quat_cumprod_bwd_carries.  Writes
+ * 2 quat_cumprod_fwd_carries, 3 quat_cumprod_bwd_carries, 4 quat_cumprod_fwd_bf16,
+ * 5 quat_cumprod_bwd_bf16.  Writes
  * *variant = -1 and *kernels = 0 when the call would launch nothing.  Returns
  * the status the call's size and device checks would return (QS_ERR_DIMS for
  * an unknown `call`).  Nothing is enqueued.

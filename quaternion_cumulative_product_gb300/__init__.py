@@ -22,6 +22,7 @@ __all__ = [
     "QS_ERR_CUDA", "QS_ERR_TIMEOUT", "QS_ERR_NOMEM", "QS_ERR_DEVICE", "QS_ERR_SCRATCH",
     "QS_NOALLOC_MAX_TILES", "QS_CARRY_STEPS", "QuatScanError", "library_path", "load_library",
     "quat_cumprod_fwd", "quat_cumprod_bwd", "quat_cumprod_fwd_carries", "quat_cumprod_bwd_carries",
+    "quat_cumprod_fwd_bf16", "quat_cumprod_bwd_bf16",
     "quat_cumprod_bwd_noalloc", "quat_cumprod_plan", "quat_cumprod_status", "quat_cumprod_strerror",
 ]
 
@@ -78,6 +79,10 @@ def load_library():
         lib.quat_cumprod_bwd.restype = ctypes.c_int
         lib.quat_cumprod_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, vp]
         lib.quat_cumprod_bwd_noalloc.restype = ctypes.c_int
+        lib.quat_cumprod_fwd_bf16.argtypes = [vp, vp, vp, i64, i64, i64, i64, vp]
+        lib.quat_cumprod_fwd_bf16.restype = ctypes.c_int
+        lib.quat_cumprod_bwd_bf16.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, vp]
+        lib.quat_cumprod_bwd_bf16.restype = ctypes.c_int
         lib.quat_cumprod_fwd_carries.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, vp]
         lib.quat_cumprod_fwd_carries.restype = ctypes.c_int
         lib.quat_cumprod_bwd_carries.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, vp]
@@ -115,12 +120,13 @@ def _stream_handle(stream, device):
     return ctypes.c_void_p(stream.cuda_stream)
 
 
-def _check_tensor(name, t, shape, device=None):
+def _check_tensor(name, t, shape, device=None, dtype=None):
     torch = _torch()
+    dtype = torch.float32 if dtype is None else dtype
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
-    if t.dtype != torch.float32:
-        raise TypeError(f"{name} must be float32, got {t.dtype}")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
     if not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor (there is no CPU path)")
     if device is not None and t.device != device:
@@ -131,12 +137,12 @@ def _check_tensor(name, t, shape, device=None):
         raise ValueError(f"{name} must be contiguous")
 
 
-def _dims(q, init):
+def _dims(q, init, dtype=None):
     if q.dim() != 5 or q.shape[-1] != 4:
         raise ValueError(f"q must be [B,S,H,J,4], got {tuple(q.shape)}")
     B, S, H, J, _ = q.shape
-    _check_tensor("q", q, (B, S, H, J, 4))
-    _check_tensor("init", init, (B, H, J, 4), q.device)
+    _check_tensor("q", q, (B, S, H, J, 4), dtype=dtype)
+    _check_tensor("init", init, (B, H, J, 4), q.device, dtype)
     return B, S, H, J
 
 
@@ -186,6 +192,46 @@ def quat_cumprod_bwd(q, init, d_cum, d_q=None, d_init=None, stream=None):
             ctypes.c_void_p(d_init.data_ptr()), B, S, H, J, _stream_handle(stream, q.device))
     if rc != QS_OK:
         raise QuatScanError(rc, "quat_cumprod_bwd")
+    return d_q, d_init
+
+
+def quat_cumprod_fwd_bf16(q, init, cum=None, stream=None):
+    """``quat_cumprod_fwd`` on bfloat16 tensors (fp32 arithmetic, outputs rounded once)."""
+    torch = _torch()
+    B, S, H, J = _dims(q, init, torch.bfloat16)
+    if cum is None:
+        cum = torch.empty_like(q)
+    else:
+        _check_tensor("cum", cum, q.shape, q.device, torch.bfloat16)
+    with torch.cuda.device(q.device):
+        rc = load_library().quat_cumprod_fwd_bf16(
+            ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(init.data_ptr()),
+            ctypes.c_void_p(cum.data_ptr()), B, S, H, J, _stream_handle(stream, q.device))
+    if rc != QS_OK:
+        raise QuatScanError(rc, "quat_cumprod_fwd_bf16")
+    return cum
+
+
+def quat_cumprod_bwd_bf16(q, init, d_cum, d_q=None, d_init=None, stream=None):
+    """``quat_cumprod_bwd`` on bfloat16 tensors.  Returns ``(d_q, d_init)`` (bfloat16)."""
+    torch = _torch()
+    B, S, H, J = _dims(q, init, torch.bfloat16)
+    _check_tensor("d_cum", d_cum, q.shape, q.device, torch.bfloat16)
+    if d_q is None:
+        d_q = torch.empty_like(q)
+    else:
+        _check_tensor("d_q", d_q, q.shape, q.device, torch.bfloat16)
+    if d_init is None:
+        d_init = torch.empty_like(init)
+    else:
+        _check_tensor("d_init", d_init, init.shape, q.device, torch.bfloat16)
+    with torch.cuda.device(q.device):
+        rc = load_library().quat_cumprod_bwd_bf16(
+            ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(init.data_ptr()),
+            ctypes.c_void_p(d_cum.data_ptr()), ctypes.c_void_p(d_q.data_ptr()),
+            ctypes.c_void_p(d_init.data_ptr()), B, S, H, J, _stream_handle(stream, q.device))
+    if rc != QS_OK:
+        raise QuatScanError(rc, "quat_cumprod_bwd_bf16")
     return d_q, d_init
 
 
@@ -274,7 +320,7 @@ def quat_cumprod_bwd_noalloc(q, init, d_cum, d_q, d_init, stream=None):
     return d_q, d_init
 
 
-_PLAN_CALLS = {"fwd": 0, "bwd": 1, "fwd_carries": 2, "bwd_carries": 3}
+_PLAN_CALLS = {"fwd": 0, "bwd": 1, "fwd_carries": 2, "bwd_carries": 3, "fwd_bf16": 4, "bwd_bf16": 5}
 
 
 def quat_cumprod_plan(call, B, S, H, J, device=None):

@@ -10,6 +10,7 @@
 
 #include <cstdint>
 #include <cuda.h>
+#include <cuda_bf16.h>
 
 namespace qs {
 
@@ -56,6 +57,34 @@ __device__ __forceinline__ float4 q_fma(const float4 acc, const float4 a, const 
 __device__ __forceinline__ float4 q_fma_cl(const float4 acc, const float4 a, const float4 b) {
     return q_fma(acc, q_conj(a), b);
 }
+
+// ---------------------------------------------------------------------------
+// Element types of the tensors in memory.  Arithmetic is always fp32; an I/O
+// type says how one quaternion is stored and converts it.
+// ---------------------------------------------------------------------------
+struct IoF32 {             // four fp32, 16 bytes
+    using elem = float4;
+    static constexpr uint32_t bytes = 16;
+    __device__ __forceinline__ static float4 get(const elem &v) { return v; }
+    __device__ __forceinline__ static elem put(const float4 v) { return v; }
+};
+
+struct IoBF16 {            // four bfloat16 [w, x, y, z], 8 bytes
+    using elem = uint2;
+    static constexpr uint32_t bytes = 8;
+    __device__ __forceinline__ static float4 get(const elem &v) {
+        const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&v.x));
+        const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&v.y));
+        return make_float4(a.x, a.y, b.x, b.y);
+    }
+    __device__ __forceinline__ static elem put(const float4 v) {   // round to nearest even
+        const __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y), b = __floats2bfloat162_rn(v.z, v.w);
+        elem r;
+        r.x = *reinterpret_cast<const uint32_t *>(&a);
+        r.y = *reinterpret_cast<const uint32_t *>(&b);
+        return r;
+    }
+};
 
 // ---------------------------------------------------------------------------
 // Shared-memory addresses, mbarriers and TMA.

@@ -419,13 +419,14 @@ __device__ __forceinline__ void drain_ring(uint64_t *bars, const int *issued, co
 
 // `carries` (optional, may be null): [B, C, H*J] float4, the state entering
 // every chunk, carries[b, c] = cum[b, c*T - 1] (init for c = 0).
-template <int LT, int NSEG, int N, int NST>
+template <typename IO, int LT, int NSEG, int N, int NST>
 __global__ void __launch_bounds__(LT *NSEG)
-    quat_walk_fwd_kernel(const __grid_constant__ CUtensorMap qmap, const float4 *__restrict__ init,
-                         float4 *__restrict__ out, float4 *__restrict__ carries, const Geometry geo,
+    quat_walk_fwd_kernel(const __grid_constant__ CUtensorMap qmap, const typename IO::elem *__restrict__ init,
+                         typename IO::elem *__restrict__ out, float4 *__restrict__ carries, const Geometry geo,
                          const Control ctl) {
+    using E = typename IO::elem;
     constexpr int T = NSEG * N;
-    constexpr uint32_t BYTES = T * LT * 16;
+    constexpr uint32_t BYTES = T * LT * IO::bytes;
     extern __shared__ unsigned char smem_raw[];
     unsigned char *ring = align128(smem_raw);
     __shared__ __align__(8) uint64_t full[NST];
@@ -442,7 +443,7 @@ __global__ void __launch_bounds__(LT *NSEG)
     const int C = geo.C;
 
     float4 R = q_ident();   // carry into the next chunk (segment-0 threads)
-    if (seg == 0 && lane_ok) R = init[static_cast<long long>(b) * geo.HJ + hj];
+    if (seg == 0 && lane_ok) R = IO::get(init[static_cast<long long>(b) * geo.HJ + hj]);
     if (seg == 0) s_x[0][lane] = R;
     if (threadIdx.x == 0) {
         for (int s = 0; s < NST; ++s) {
@@ -465,14 +466,14 @@ __global__ void __launch_bounds__(LT *NSEG)
     const long long row0 = static_cast<long long>(b) * geo.S;
     for (int c = 0; c < C; ++c) {
         const int st = c % NST, sl = c & 1;
-        const float4 *Qt = reinterpret_cast<const float4 *>(ring + st * BYTES);
+        const E *Qt = reinterpret_cast<const E *>(ring + st * BYTES);
         if (!ld_volatile_int(&s_broken) && !wait_stage(&full[st], (c / NST) & 1, ctl, c * geo.NG + g))
             s_broken = 1;
         float4 x[N];
         float4 loc = q_ident();
 #pragma unroll
         for (int k = 0; k < N; ++k) {
-            loc = q_mul(Qt[(seg * N + k) * LT + lane], loc);
+            loc = q_mul(IO::get(Qt[(seg * N + k) * LT + lane]), loc);
             x[k] = loc;
         }
         s_a[sl][seg][lane] = loc;
@@ -492,10 +493,10 @@ __global__ void __launch_bounds__(LT *NSEG)
         }
         if (lane_ok) {
             const long long t0 = static_cast<long long>(c) * T + seg * N;
-            float4 *dst = out + (row0 + t0) * geo.HJ + hj;
+            E *dst = out + (row0 + t0) * geo.HJ + hj;
 #pragma unroll
             for (int k = 0; k < N; ++k)
-                if (t0 + k < geo.S) __stcs(dst + static_cast<long long>(k) * geo.HJ, q_mul(x[k], Y));
+                if (t0 + k < geo.S) __stcs(dst + static_cast<long long>(k) * geo.HJ, IO::put(q_mul(x[k], Y)));
         }
     }
     if (s_broken) drain_ring<NST>(full, issued, ctl);
@@ -512,14 +513,15 @@ __global__ void __launch_bounds__(LT *NSEG)
 // GIVEN = true: the chunk carries come from the caller, `given` = [B, C, H*J]
 // float4 with given[b, c] = cum[b, c*T - 1] (what the forward walk writes as
 // `carries`); the forward walk is skipped and `init` and `carF` are unused.
-template <int LT, int NSEG, int N, int NSTF, int NSTB, bool SELF, bool GIVEN>
+template <typename IO, int LT, int NSEG, int N, int NSTF, int NSTB, bool SELF, bool GIVEN>
 __global__ void __launch_bounds__(LT *NSEG)
     quat_walk_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap dmap,
-                         const float4 *__restrict__ init, float4 *__restrict__ carF,
-                         const float4 *__restrict__ given, float4 *__restrict__ d_q, float4 *__restrict__ d_init,
-                         const Geometry geo, const Control ctl) {
+                         const typename IO::elem *__restrict__ init, float4 *__restrict__ carF,
+                         const float4 *__restrict__ given, typename IO::elem *__restrict__ d_q,
+                         typename IO::elem *__restrict__ d_init, const Geometry geo, const Control ctl) {
+    using E = typename IO::elem;
     constexpr int T = NSEG * N;
-    constexpr uint32_t BQ = T * LT * 16;   // one operand of one chunk
+    constexpr uint32_t BQ = T * LT * IO::bytes;   // one operand of one chunk
     extern __shared__ unsigned char smem_raw[];
     unsigned char *ring = align128(smem_raw);
     __shared__ __align__(8) uint64_t fullF[NSTF];
@@ -568,15 +570,15 @@ __global__ void __launch_bounds__(LT *NSEG)
             for (int c = 0; c < NSTF && c < C; ++c) issueF(c);
 
         float4 R = q_ident();
-        if (seg == 0 && lane_ok) R = init[static_cast<long long>(b) * geo.HJ + hj];
+        if (seg == 0 && lane_ok) R = IO::get(init[static_cast<long long>(b) * geo.HJ + hj]);
         for (int c = 0; c < C; ++c) {
             const int st = c % NSTF, sl = c & 1;
-            const float4 *Qt = reinterpret_cast<const float4 *>(ring + st * BQ);
+            const E *Qt = reinterpret_cast<const E *>(ring + st * BQ);
             if (!ld_volatile_int(&s_broken) && !wait_stage(&fullF[st], (c / NSTF) & 1, ctl, c * geo.NG + g))
                 s_broken = 1;
             float4 loc = q_ident();
 #pragma unroll
-            for (int k = 0; k < N; ++k) loc = q_mul(Qt[(seg * N + k) * LT + lane], loc);
+            for (int k = 0; k < N; ++k) loc = q_mul(IO::get(Qt[(seg * N + k) * LT + lane]), loc);
             s_a[sl][seg][lane] = loc;
             __syncthreads();
             if (threadIdx.x == 0 && !s_broken && c + NSTF < C) issueF(c + NSTF);
@@ -618,8 +620,8 @@ __global__ void __launch_bounds__(LT *NSEG)
         const int st = j % NSTB, sl = j & 1;
         const float4 F = F_next;
         if ((SELF || seg == 0) && c > 0) F_next = carry_of(c - 1);
-        const float4 *Qt = reinterpret_cast<const float4 *>(ring + st * 2 * BQ);
-        const float4 *Dt = Qt + T * LT;
+        const E *Qt = reinterpret_cast<const E *>(ring + st * 2 * BQ);
+        const E *Dt = Qt + T * LT;
         if (!ld_volatile_int(&s_broken) && !wait_stage(&fullB[st], (j / NSTB) & 1, ctl, c * geo.NG + g))
             s_broken = 1;
         const int cell0 = seg * N * LT + lane;
@@ -627,8 +629,8 @@ __global__ void __launch_bounds__(LT *NSEG)
         float4 loc = q_ident(), W = q_zero();
 #pragma unroll
         for (int k = 0; k < N; ++k) {
-            qv[k] = Qt[cell0 + k * LT];
-            dv[k] = Dt[cell0 + k * LT];
+            qv[k] = IO::get(Qt[cell0 + k * LT]);
+            dv[k] = IO::get(Dt[cell0 + k * LT]);
             lp[k] = loc;
             loc = q_mul(qv[k], loc);
             W = q_fma_cl(W, loc, dv[k]);
@@ -647,7 +649,7 @@ __global__ void __launch_bounds__(LT *NSEG)
             if (seg == 0) {
                 Hc = q_fma_cl(s_w[ws][0][lane], s_a[sl][0][lane], Hn);
                 s_h[sl ^ 1][lane] = Hc;
-                if (c == 0 && lane_ok) d_init[static_cast<long long>(b) * geo.HJ + hj] = Hc;
+                if (c == 0 && lane_ok) d_init[static_cast<long long>(b) * geo.HJ + hj] = IO::put(Hc);
             }
         } else {
             if (seg == 0) {
@@ -663,26 +665,26 @@ __global__ void __launch_bounds__(LT *NSEG)
                     h = q_fma_cl(s_w[0][kr][lane], s_a[sl][kr][lane], h);
                 }
                 Hc = h;
-                if (c == 0 && lane_ok) d_init[static_cast<long long>(b) * geo.HJ + hj] = Hc;
+                if (c == 0 && lane_ok) d_init[static_cast<long long>(b) * geo.HJ + hj] = IO::put(Hc);
             }
             __syncthreads();
             X = s_x[seg][lane];    // cum just before this segment
             Hn = s_h[seg][lane];   // H entering this segment from the right
         }
         const long long t0 = static_cast<long long>(c) * T + seg * N;
-        float4 *dst = d_q + (row0 + t0) * geo.HJ + hj;
+        E *dst = d_q + (row0 + t0) * geo.HJ + hj;
         if (lane_ok && t0 + N <= geo.S) {
 #pragma unroll
             for (int k = N - 1; k >= 0; --k) {
                 const float4 G = q_add(dv[k], Hn);
-                __stcs(dst + static_cast<long long>(k) * geo.HJ, q_mul_cr(G, q_mul(lp[k], X)));
+                __stcs(dst + static_cast<long long>(k) * geo.HJ, IO::put(q_mul_cr(G, q_mul(lp[k], X))));
                 Hn = q_mul_cl(qv[k], G);
             }
         } else if (lane_ok) {
 #pragma unroll
             for (int k = N - 1; k >= 0; --k) {
                 const float4 G = q_add(dv[k], Hn);
-                if (t0 + k < geo.S) __stcs(dst + static_cast<long long>(k) * geo.HJ, q_mul_cr(G, q_mul(lp[k], X)));
+                if (t0 + k < geo.S) __stcs(dst + static_cast<long long>(k) * geo.HJ, IO::put(q_mul_cr(G, q_mul(lp[k], X))));
                 Hn = q_mul_cl(qv[k], G);
             }
         }
@@ -714,11 +716,11 @@ __host__ __device__ constexpr size_t tile_smem_bytes(bool bwd, int lt, int n) {
 
 // Dynamic shared memory of the walk kernels: the forward ring, or the larger
 // of the backward's two rings (one operand per stage forward, two reverse).
-__host__ __device__ constexpr size_t walk_fwd_smem_bytes(int lt, int nseg, int n, int nst) {
-    return 128 + size_t(nst) * nseg * n * lt * 16;
+__host__ __device__ constexpr size_t walk_fwd_smem_bytes(int lt, int nseg, int n, int nst, int eb = 16) {
+    return 128 + size_t(nst) * nseg * n * lt * eb;
 }
-__host__ __device__ constexpr size_t walk_bwd_smem_bytes(int lt, int nseg, int n, int nstf, int nstb) {
-    return 128 + size_t(nstf > 2 * nstb ? nstf : 2 * nstb) * nseg * n * lt * 16;
+__host__ __device__ constexpr size_t walk_bwd_smem_bytes(int lt, int nseg, int n, int nstf, int nstb, int eb = 16) {
+    return 128 + size_t(nstf > 2 * nstb ? nstf : 2 * nstb) * nseg * n * lt * eb;
 }
 }  // namespace qs
 
@@ -753,12 +755,12 @@ struct Variant {
     }
 #define QS_WALK_FWD(LT, NSEG, N, NST)                                                               \
     Variant {                                                                                       \
-        true, reinterpret_cast<const void *>(qs::quat_walk_fwd_kernel<LT, NSEG, N, NST>), nullptr,  \
+        true, reinterpret_cast<const void *>(qs::quat_walk_fwd_kernel<qs::IoF32, LT, NSEG, N, NST>), nullptr, \
             false, LT, NSEG, N, qs::walk_fwd_smem_bytes(LT, NSEG, N, NST)                           \
     }
 #define QS_WALK_BWD(LT, NSEG, N, NSTF, NSTB, SELF)                                                  \
     Variant {                                                                                       \
-        true, reinterpret_cast<const void *>(qs::quat_walk_bwd_kernel<LT, NSEG, N, NSTF, NSTB, SELF, false>), \
+        true, reinterpret_cast<const void *>(qs::quat_walk_bwd_kernel<qs::IoF32, LT, NSEG, N, NSTF, NSTB, SELF, false>), \
             nullptr, true, LT, NSEG, N, qs::walk_bwd_smem_bytes(LT, NSEG, N, NSTF, NSTB)            \
     }
 const Variant kFwdVariants[] = {
@@ -785,13 +787,32 @@ const Variant kBwdVariants[] = {
 };
 // The backward from caller-provided carries: the reverse walk alone.
 const Variant kBwdGiven = Variant{true,
-                                  reinterpret_cast<const void *>(qs::quat_walk_bwd_kernel<16, 8, 8, 1, 2, false, true>),
+                                  reinterpret_cast<const void *>(qs::quat_walk_bwd_kernel<qs::IoF32, 16, 8, 8, 1, 2, false, true>),
                                   nullptr,
                                   true,
                                   16,
                                   8,
                                   8,
                                   qs::walk_bwd_smem_bytes(16, 8, 8, 1, 2)};
+// bf16 I/O (fp32 arithmetic): walk kernels only, with rings of the same depth
+// in steps and half the bytes per stage.
+const Variant kFwdBf16 = Variant{true,
+                                 reinterpret_cast<const void *>(qs::quat_walk_fwd_kernel<qs::IoBF16, 32, 8, 8, 6>),
+                                 nullptr,
+                                 false,
+                                 32,
+                                 8,
+                                 8,
+                                 qs::walk_fwd_smem_bytes(32, 8, 8, 6, 8)};
+const Variant kBwdBf16 =
+    Variant{true,
+            reinterpret_cast<const void *>(qs::quat_walk_bwd_kernel<qs::IoBF16, 16, 8, 8, 8, 4, false, false>),
+            nullptr,
+            true,
+            16,
+            8,
+            8,
+            qs::walk_bwd_smem_bytes(16, 8, 8, 8, 4, 8)};
 #undef QS_VARIANT
 #undef QS_WALK_FWD
 #undef QS_WALK_BWD
@@ -895,6 +916,8 @@ int device_info(DevInfo **out, int *dev_out) {
             for (const Variant &v : kFwdVariants) setup(v);
             for (const Variant &v : kBwdVariants) setup(v);
             setup(kBwdGiven);
+            setup(kFwdBf16);
+            setup(kBwdBf16);
             if (!ok) {
                 cudaGetLastError();
                 d.sms = 0;
@@ -952,14 +975,16 @@ int ensure_workspace(int dev, cudaStream_t stream, size_t need, unsigned char **
 // 3-D view [B][S][HJ*4 floats] of a [B,S,H,J,4] tensor for TMA boxes of `lt`
 // lanes x `boxh` steps.  Boxes may reach past the tensor: TMA fills those
 // cells with zeros.
-int make_map(CUtensorMap *m, const float *ptr, int64_t B, int64_t S, int64_t HJ, int lt, int boxh) {
+// `eb`: bytes of one quaternion (16 fp32, 8 bf16).
+int make_map(CUtensorMap *m, const void *ptr, int64_t B, int64_t S, int64_t HJ, int lt, int boxh, int eb = 16) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return QS_ERR_CUDA;
     cuuint64_t dims[3] = {(cuuint64_t)(HJ * 4), (cuuint64_t)S, (cuuint64_t)B};
-    cuuint64_t strides[2] = {(cuuint64_t)(HJ * 16), (cuuint64_t)(S * HJ * 16)};
+    cuuint64_t strides[2] = {(cuuint64_t)(HJ * eb), (cuuint64_t)(S * HJ * eb)};
     cuuint32_t box[3] = {(cuuint32_t)(lt * 4), (cuuint32_t)boxh, 1};
     cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float *>(ptr), dims, strides, box, estr,
+    const CUtensorMapDataType dt = eb == 8 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+    CUresult r = fn(m, dt, 3, const_cast<void *>(ptr), dims, strides, box, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? QS_OK : QS_ERR_CUDA;
@@ -995,9 +1020,10 @@ struct Plan {
     size_t o_L = 0, o_W = 0, o_F = 0, o_H = 0, o_I = 0, ws_bytes = 0;
 };
 
-int make_plan(bool bwd, int64_t B, int64_t S, int64_t HJ, int sms, Plan *pl, Mode mode = Mode::PLAIN) {
-    int vi = pick_variant(bwd, B, HJ, sms);
-    const Variant *v = bwd ? &kBwdVariants[vi] : &kFwdVariants[vi];
+int make_plan(bool bwd, int64_t B, int64_t S, int64_t HJ, int sms, Plan *pl, Mode mode = Mode::PLAIN,
+              bool bf16 = false) {
+    int vi = bf16 ? 0 : pick_variant(bwd, B, HJ, sms);
+    const Variant *v = bf16 ? (bwd ? &kBwdBf16 : &kFwdBf16) : bwd ? &kBwdVariants[vi] : &kFwdVariants[vi];
     if (mode != Mode::PLAIN && v->T() != QS_CARRY_STEPS) {
         // The carries are defined on QS_CARRY_STEPS-step chunks: keep the
         // design, take its default configuration (which has that chunk).
@@ -1052,21 +1078,24 @@ int make_plan(bool bwd, int64_t B, int64_t S, int64_t HJ, int sms, Plan *pl, Mod
 
 // `carries`: written (Mode::SAVE_CARRIES) or read (Mode::FROM_CARRIES),
 // [B, ceil(S / QS_CARRY_STEPS), H*J] float4; unused otherwise.
-int launch(bool bwd, const float *q, const float *d_cum, float *out, const float *init, float *d_init, int64_t B,
-           int64_t S, int64_t HJ, cudaStream_t stream, Mode mode = Mode::PLAIN, float *carries = nullptr) {
+// `bf16`: the tensors hold bfloat16 quaternions (8 bytes); walk kernels only.
+int launch(bool bwd, const void *q, const void *d_cum, void *out, const void *init, void *d_init, int64_t B,
+           int64_t S, int64_t HJ, cudaStream_t stream, Mode mode = Mode::PLAIN, float *carries = nullptr,
+           bool bf16 = false) {
     DevInfo *di = nullptr;
     int dev = 0;
     int rc = device_info(&di, &dev);
     if (rc != QS_OK) return rc;
     Plan pl;
-    rc = make_plan(bwd, B, S, HJ, di->sms, &pl, mode);
+    rc = make_plan(bwd, B, S, HJ, di->sms, &pl, mode, bf16);
     if (rc != QS_OK) return rc;
     unsigned char *ws = nullptr;
     rc = ensure_workspace(dev, stream, pl.ws_bytes, &ws);
     if (rc != QS_OK) return rc;
     CUtensorMap qmap, dmap;
-    rc = make_map(&qmap, q, B, S, HJ, pl.v->lt, pl.v->T());
-    if (rc == QS_OK) rc = make_map(&dmap, bwd ? d_cum : q, B, S, HJ, pl.v->lt, pl.v->T());
+    const int eb = bf16 ? 8 : 16;
+    rc = make_map(&qmap, q, B, S, HJ, pl.v->lt, pl.v->T(), eb);
+    if (rc == QS_OK) rc = make_map(&dmap, bwd ? d_cum : q, B, S, HJ, pl.v->lt, pl.v->T(), eb);
     if (rc != QS_OK) return rc;
     if (pl.v->walk) {
         float4 *carF = bwd ? reinterpret_cast<float4 *>(ws + pl.o_F) : nullptr;
@@ -1077,9 +1106,9 @@ int launch(bool bwd, const float *q, const float *d_cum, float *out, const float
             ctl.stall_tile = g_stall_tile;
         }
         ctl.hdr = reinterpret_cast<qs::WsHeader *>(ws);
-        const float4 *init4 = reinterpret_cast<const float4 *>(init);
-        float4 *dinit4 = reinterpret_cast<float4 *>(d_init);
-        float4 *out4 = reinterpret_cast<float4 *>(out);
+        const void *init4 = init;   // element type of the kernel's I/O
+        void *dinit4 = d_init;
+        void *out4 = out;
         float4 *save4 = mode == Mode::SAVE_CARRIES ? reinterpret_cast<float4 *>(carries) : nullptr;
         const float4 *given4 = mode == Mode::FROM_CARRIES ? reinterpret_cast<const float4 *>(carries) : nullptr;
         void *fwd_args[] = {&qmap, &init4, &out4, &save4, &pl.geo, &ctl};
@@ -1241,6 +1270,51 @@ extern "C" int quat_cumprod_bwd_carries(const float *q, const float *carries, co
                   const_cast<float *>(carries));
 }
 
+extern "C" int quat_cumprod_fwd_bf16(const uint16_t *q, const uint16_t *init, uint16_t *cum, int64_t B, int64_t S,
+                                     int64_t H, int64_t J, void *stream_) {
+    const int dc = check_dims(B, S, H, J);
+    if (dc == 1) return QS_OK;
+    if (dc != QS_OK) return dc;
+    const int64_t HJ = H * J;
+    if (HJ % 2 != 0) return QS_ERR_DIMS;   // TMA row strides are multiples of 16 bytes
+    if (!q || !init || !cum) return QS_ERR_NULL;
+    if (misaligned(q) || misaligned(init) || misaligned(cum)) return QS_ERR_MISALIGNED;
+    const size_t big = (size_t)B * S * HJ * 8, small = (size_t)B * HJ * 8;
+    if (overlaps(cum, big, q, big) || overlaps(cum, big, init, small)) return QS_ERR_ALIAS;
+    return launch(false, q, nullptr, cum, init, nullptr, B, S, HJ, static_cast<cudaStream_t>(stream_), Mode::PLAIN,
+                  nullptr, true);
+}
+
+extern "C" int quat_cumprod_bwd_bf16(const uint16_t *q, const uint16_t *init, const uint16_t *d_cum,
+                                     uint16_t *d_q, uint16_t *d_init, int64_t B, int64_t S, int64_t H, int64_t J,
+                                     void *stream_) {
+    const int dc = check_dims(B, S, H, J);
+    if (dc != QS_OK && dc != 1) return dc;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+    const int64_t HJ = H * J;
+    if (dc == 1) {
+        if (S == 0 && B > 0 && HJ > 0) {   // no steps: the gradient of init is zero
+            if (!d_init) return QS_ERR_NULL;
+            if (misaligned(d_init)) return QS_ERR_MISALIGNED;
+            if (cudaMemsetAsync(d_init, 0, (size_t)B * HJ * 8, stream) != cudaSuccess) {
+                cudaGetLastError();
+                return QS_ERR_CUDA;
+            }
+        }
+        return QS_OK;
+    }
+    if (HJ % 2 != 0) return QS_ERR_DIMS;
+    if (!q || !init || !d_cum || !d_q || !d_init) return QS_ERR_NULL;
+    if (misaligned(q) || misaligned(init) || misaligned(d_cum) || misaligned(d_q) || misaligned(d_init))
+        return QS_ERR_MISALIGNED;
+    const size_t big = (size_t)B * S * HJ * 8, small = (size_t)B * HJ * 8;
+    if (overlaps(d_q, big, q, big) || overlaps(d_q, big, init, small) || overlaps(d_q, big, d_cum, big) ||
+        overlaps(d_init, small, q, big) || overlaps(d_init, small, init, small) ||
+        overlaps(d_init, small, d_cum, big) || overlaps(d_q, big, d_init, small))
+        return QS_ERR_ALIAS;
+    return launch(true, q, d_cum, d_q, init, d_init, B, S, HJ, stream, Mode::PLAIN, nullptr, true);
+}
+
 extern "C" int quat_cumprod_status(void *stream_) {
     cudaStream_t stream = static_cast<cudaStream_t>(stream_);
     if (cudaStreamSynchronize(stream) != cudaSuccess) {
@@ -1274,9 +1348,11 @@ extern "C" int quat_cumprod_status(void *stream_) {
 
 extern "C" int quat_cumprod_plan(int call, int64_t B, int64_t S, int64_t H, int64_t J, int *variant, int *kernels) {
     if (!variant || !kernels) return QS_ERR_NULL;
-    if (call < 0 || call > 3) return QS_ERR_DIMS;
+    if (call < 0 || call > 5) return QS_ERR_DIMS;
     const bool bwd = (call & 1) != 0;
+    const bool bf16 = call >= 4;
     const Mode mode = call == 2 ? Mode::SAVE_CARRIES : call == 3 ? Mode::FROM_CARRIES : Mode::PLAIN;
+    if (bf16 && (H * J) % 2 != 0 && B > 0 && S > 0 && H > 0 && J > 0) return QS_ERR_DIMS;
     const int dc = check_dims(B, S, H, J);
     if (dc != QS_OK && dc != 1) return dc;
     if (dc == 1) {   // nothing to launch (the backward may write d_init with a memset)
@@ -1289,7 +1365,7 @@ extern "C" int quat_cumprod_plan(int call, int64_t B, int64_t S, int64_t H, int6
     int rc = device_info(&di, &dev);
     if (rc != QS_OK) return rc;
     Plan pl;
-    rc = make_plan(bwd, B, S, H * J, di->sms, &pl, mode);
+    rc = make_plan(bwd, B, S, H * J, di->sms, &pl, mode, bf16);
     if (rc != QS_OK) return rc;
     *variant = pl.vi;
     *kernels = pl.v->walk ? 1 : (mode == Mode::SAVE_CARRIES ? 4 : 3);

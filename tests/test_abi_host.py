@@ -191,3 +191,16 @@ def test_plan_rejects_unknown_call(lib):
     assert lib.quat_cumprod_plan(4, 1, 4, 1, 1, ctypes.byref(v), ctypes.byref(k)) == qs.QS_ERR_DIMS
     assert lib.quat_cumprod_plan(-1, 1, 4, 1, 1, ctypes.byref(v), ctypes.byref(k)) == qs.QS_ERR_DIMS
     assert lib.quat_cumprod_plan(3, 0, 4, 1, 1, ctypes.byref(v), ctypes.byref(k)) == qs.QS_OK
+
+
+def test_bf16_calls_argument_checks_before_any_cuda_call(lib):
+    q, i, c, d, gq, gi = (k << 20 for k in range(1, 7))
+    f, g = lib.quat_cumprod_fwd_bf16, lib.quat_cumprod_bwd_bf16
+    assert f(_p(q), _p(i), _p(c), 1, 16, 3, 5, None) == qs.QS_ERR_DIMS        # H*J odd
+    assert g(_p(q), _p(i), _p(d), _p(gq), _p(gi), 1, 16, 1, 1, None) == qs.QS_ERR_DIMS
+    assert f(None, None, None, 0, 16, 2, 2, None) == qs.QS_OK
+    assert f(None, _p(i), _p(c), 1, 16, 2, 2, None) == qs.QS_ERR_NULL
+    assert f(_p(q + 8), _p(i), _p(c), 1, 16, 2, 2, None) == qs.QS_ERR_MISALIGNED
+    assert f(_p(q), _p(i), _p(q + 64), 1, 16, 2, 2, None) == qs.QS_ERR_ALIAS    # 1*16*4 quats * 8 B
+    assert g(None, None, None, None, None, 2, 0, 2, 2, None) == qs.QS_ERR_NULL
+    assert g(_p(q), _p(i), _p(d), _p(d + 256), _p(gi), 1, 16, 2, 2, None) == qs.QS_ERR_ALIAS

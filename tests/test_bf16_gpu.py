@@ -1,0 +1,114 @@
+"""GPU: the bfloat16-I/O calls against the fp64 oracle.
+
+The inputs are bfloat16, and the oracle runs on exactly those values
+(widened to fp64).  The kernels compute in fp32 and round each output once to
+the nearest bfloat16.
+
+Tolerance, normwise per output tensor:
+
+- bfloat16 has 8 significant bits, so rounding to nearest moves a value by at
+  most half an ulp, 2^-8 of its magnitude, hence at most 2^-8 of max|ref|.
+- The fp32 arithmetic before the rounding is within the fp32 calls'
+  tolerance of 1e-4.
+- So |out - ref| <= 2^-8 (1 + 1e-4) max|ref| + 1e-4 max|ref|, which gives
+  TOL_BF16 = 2^-8 + 1.1e-4 (about 4.0e-3).
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+
+import oracle
+import quaternion_cumulative_product_gb300 as qs
+from quaternion_cumulative_product_gb300 import workloads
+
+torch = pytest.importorskip("torch")
+
+pytestmark = pytest.mark.gpu
+
+TOL_BF16 = 2.0 ** -8 + 1.1e-4
+
+
+@pytest.fixture(scope="module")
+def dev():
+    if not torch.cuda.is_available():
+        pytest.fail("CUDA device required for -m gpu tests")
+    qs.load_library()
+    return torch.device("cuda", 0)
+
+
+def normwise(got, ref):
+    ref = np.asarray(ref, np.float64)
+    if ref.size == 0:
+        return 0.0
+    scale = float(np.abs(ref).max())
+    return float(np.abs(np.asarray(got, np.float64) - ref).max()) / (scale if scale > 0 else 1.0)
+
+
+def bf16_inputs(dev, w):
+    """The workload's inputs rounded to bfloat16, on the device, and the same values as fp64."""
+    arrays = workloads.make_inputs(w)
+    tb = [torch.from_numpy(a).to(dev).to(torch.bfloat16) for a in arrays]
+    exact = [t.float().cpu().numpy().astype(np.float64) for t in tb]
+    return tb, exact
+
+
+@pytest.mark.parametrize("dims", [(1, 64, 2, 4), (2, 333, 3, 16), (3, 1100, 1, 40), (1, 70, 5, 2),
+                                  (2, 1, 1, 2)])
+def test_bf16_matches_oracle(dev, dims):
+    w = workloads.custom("bf16", *dims, q_kind="rotation", theta_max=0.6, seed=61)
+    (tq, ti, td), (q, init, d_cum) = bf16_inputs(dev, w)
+    cum = qs.quat_cumprod_fwd_bf16(tq, ti)
+    d_q, d_init = qs.quat_cumprod_bwd_bf16(tq, ti, td)
+    assert qs.quat_cumprod_status(device=dev) == qs.QS_OK
+    assert cum.dtype == d_q.dtype == d_init.dtype == torch.bfloat16
+    ref_cum = oracle.fwd(q, init)
+    ref_dq, ref_di = oracle.bwd(q, init, d_cum)
+    for got, ref, name in ((cum, ref_cum, "cum"), (d_q, ref_dq, "d_q"), (d_init, ref_di, "d_init")):
+        err = normwise(got.float().cpu().numpy(), ref)
+        assert err <= TOL_BF16, f"{name}: {err:.3e} > {TOL_BF16:.3e}"
+
+
+def test_bf16_full_size_sampled_lanes(dev):
+    """mamba3 at full size (bench launch configuration) on sampled whole lanes."""
+    w = workloads.WORKLOADS["mamba3"]
+    (tq, ti, td), _ = bf16_inputs(dev, w)
+    cum = qs.quat_cumprod_fwd_bf16(tq, ti)
+    d_q, d_init = qs.quat_cumprod_bwd_bf16(tq, ti, td)
+    assert qs.quat_cumprod_status(device=dev) == qs.QS_OK
+    lanes = np.random.default_rng(3).choice(w.lanes, 24, replace=False)
+    host = [t.float().cpu().numpy() for t in (tq, ti, td, cum, d_q, d_init)]
+    sq, si, sd = (a.astype(np.float64) for a in workloads.sample_lanes(host[:3], lanes, w.H, w.J))
+    gc, gq, gi = workloads.sample_lanes(host[3:], lanes, w.H, w.J)
+    ref_dq, ref_di = oracle.bwd(sq, si, sd)
+    assert normwise(gc, oracle.fwd(sq, si)) <= TOL_BF16
+    assert normwise(gq, ref_dq) <= TOL_BF16
+    assert normwise(gi, ref_di) <= TOL_BF16
+
+
+def test_bf16_rounding_is_the_only_difference_from_fp32(dev):
+    """On bfloat16-representable inputs the bf16 call is the fp32 call rounded."""
+    w = workloads.custom("bf16fp32", 2, 500, 4, 4, q_kind="gauss4", seed=62)
+    (tq, ti, td), _ = bf16_inputs(dev, w)
+    c16 = qs.quat_cumprod_fwd_bf16(tq, ti).float()
+    c32 = qs.quat_cumprod_fwd(tq.float(), ti.float())
+    g16, i16 = qs.quat_cumprod_bwd_bf16(tq, ti, td)
+    g32, i32 = qs.quat_cumprod_bwd(tq.float(), ti.float(), td.float())
+    for a, b in ((c16, c32), (g16.float(), g32), (i16.float(), i32)):
+        assert normwise(a.cpu().numpy(), b.cpu().numpy().astype(np.float64)) <= 2.0 ** -8 + 1e-5
+
+
+def test_bf16_rejects_odd_lane_count_and_wrong_dtype(dev):
+    q = torch.zeros(1, 8, 3, 1, 4, device=dev, dtype=torch.bfloat16)
+    init = torch.zeros(1, 3, 1, 4, device=dev, dtype=torch.bfloat16)
+    with pytest.raises(qs.QuatScanError) as ei:
+        qs.quat_cumprod_fwd_bf16(q, init)
+    assert ei.value.status == qs.QS_ERR_DIMS
+    with pytest.raises(TypeError):
+        qs.quat_cumprod_fwd_bf16(q.float(), init.float())
+    # S == 0: d_init is zero
+    q0 = torch.zeros(2, 0, 2, 1, 4, device=dev, dtype=torch.bfloat16)
+    i0 = torch.ones(2, 2, 1, 4, device=dev, dtype=torch.bfloat16)
+    _, di = qs.quat_cumprod_bwd_bf16(q0, i0, q0.clone())
+    torch.cuda.synchronize(dev)
+    assert float(di.float().abs().max()) == 0.0
