@@ -241,6 +241,8 @@ const char *quat_cumprod_strerror(int status);
 int quat_cumprod_debug_set_timeout_ns(int64_t ns);
 int quat_cumprod_debug_stall_tile(int64_t tile);
 int quat_cumprod_debug_set_variant(int fwd_variant, int bwd_variant);
+/* The same for the bfloat16 calls (their own table of configurations). */
+int quat_cumprod_debug_set_variant_bf16(int fwd_variant, int bwd_variant);
 
 #ifdef __cplusplus
 }

@@ -100,6 +100,8 @@ def load_library():
         lib.quat_cumprod_debug_stall_tile.restype = ctypes.c_int
         lib.quat_cumprod_debug_set_variant.argtypes = [ctypes.c_int, ctypes.c_int]
         lib.quat_cumprod_debug_set_variant.restype = ctypes.c_int
+        lib.quat_cumprod_debug_set_variant_bf16.argtypes = [ctypes.c_int, ctypes.c_int]
+        lib.quat_cumprod_debug_set_variant_bf16.restype = ctypes.c_int
         _lib = lib
         return lib
 

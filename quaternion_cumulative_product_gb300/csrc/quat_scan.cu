@@ -794,25 +794,35 @@ const Variant kBwdGiven = Variant{true,
                                   8,
                                   8,
                                   qs::walk_bwd_smem_bytes(16, 8, 8, 1, 2)};
-// bf16 I/O (fp32 arithmetic): walk kernels only, with rings of the same depth
-// in steps and half the bytes per stage.
-const Variant kFwdBf16 = Variant{true,
-                                 reinterpret_cast<const void *>(qs::quat_walk_fwd_kernel<qs::IoBF16, 32, 8, 8, 6>),
-                                 nullptr,
-                                 false,
-                                 32,
-                                 8,
-                                 8,
-                                 qs::walk_fwd_smem_bytes(32, 8, 8, 6, 8)};
-const Variant kBwdBf16 =
-    Variant{true,
-            reinterpret_cast<const void *>(qs::quat_walk_bwd_kernel<qs::IoBF16, 16, 8, 8, 8, 4, false, false>),
-            nullptr,
-            true,
-            16,
-            8,
-            8,
-            qs::walk_bwd_smem_bytes(16, 8, 8, 8, 4, 8)};
+// bf16 I/O (fp32 arithmetic): walk kernels only.
+#define QS_WALK_FWD16(LT, NSEG, N, NST)                                                             \
+    Variant {                                                                                       \
+        true, reinterpret_cast<const void *>(qs::quat_walk_fwd_kernel<qs::IoBF16, LT, NSEG, N, NST>), \
+            nullptr, false, LT, NSEG, N, qs::walk_fwd_smem_bytes(LT, NSEG, N, NST, 8)               \
+    }
+#define QS_WALK_BWD16(LT, NSEG, N, NSTF, NSTB, SELF)                                                \
+    Variant {                                                                                       \
+        true,                                                                                       \
+            reinterpret_cast<const void *>(                                                         \
+                qs::quat_walk_bwd_kernel<qs::IoBF16, LT, NSEG, N, NSTF, NSTB, SELF, false>),        \
+            nullptr, true, LT, NSEG, N, qs::walk_bwd_smem_bytes(LT, NSEG, N, NSTF, NSTB, 8)         \
+    }
+const Variant kFwdBf16Variants[] = {
+    QS_WALK_FWD16(32, 8, 8, 6),            // 0: 32 lanes x 64 steps, 6 x 16 KiB ring
+    QS_WALK_FWD16(16, 8, 8, 6),            // 1: 16 lanes x 64 steps (128 threads), 6 x 8 KiB
+    QS_WALK_FWD16(16, 16, 8, 4),           // 2: 16 lanes x 128 steps (256 threads), 4 x 16 KiB
+    QS_WALK_FWD16(32, 16, 4, 6),           // 3: 32 lanes x 64 steps (512 threads), 6 x 16 KiB
+};
+const Variant kBwdBf16Variants[] = {
+    QS_WALK_BWD16(16, 8, 8, 8, 4, false),  // 0: 16 lanes x 64 steps (128 threads), 64 KiB rings
+    QS_WALK_BWD16(16, 8, 8, 8, 4, true),   // 1: the same, each thread folds its own carries
+    QS_WALK_BWD16(16, 16, 4, 8, 4, false), // 2: 16 lanes x 64 steps (256 threads), 64 KiB rings
+    QS_WALK_BWD16(32, 8, 8, 8, 4, false),  // 3: 32 lanes x 64 steps (256 threads), 128 KiB rings
+};
+#undef QS_WALK_FWD16
+#undef QS_WALK_BWD16
+constexpr int kNumFwdBf16 = sizeof(kFwdBf16Variants) / sizeof(kFwdBf16Variants[0]);
+constexpr int kNumBwdBf16 = sizeof(kBwdBf16Variants) / sizeof(kBwdBf16Variants[0]);
 #undef QS_VARIANT
 #undef QS_WALK_FWD
 #undef QS_WALK_BWD
@@ -830,6 +840,7 @@ std::mutex g_mu;
 unsigned long long g_timeout_ns = DEFAULT_TIMEOUT_NS;
 int g_stall_tile = -1;
 int g_fwd_variant = -1, g_bwd_variant = -1;   // -1: automatic
+int g_fwd_variant16 = -1, g_bwd_variant16 = -1;
 
 struct DevInfo {
     int sms = 0;
@@ -916,8 +927,8 @@ int device_info(DevInfo **out, int *dev_out) {
             for (const Variant &v : kFwdVariants) setup(v);
             for (const Variant &v : kBwdVariants) setup(v);
             setup(kBwdGiven);
-            setup(kFwdBf16);
-            setup(kBwdBf16);
+            for (const Variant &v : kFwdBf16Variants) setup(v);
+            for (const Variant &v : kBwdBf16Variants) setup(v);
             if (!ok) {
                 cudaGetLastError();
                 d.sms = 0;
@@ -1022,8 +1033,16 @@ struct Plan {
 
 int make_plan(bool bwd, int64_t B, int64_t S, int64_t HJ, int sms, Plan *pl, Mode mode = Mode::PLAIN,
               bool bf16 = false) {
-    int vi = bf16 ? 0 : pick_variant(bwd, B, HJ, sms);
-    const Variant *v = bf16 ? (bwd ? &kBwdBf16 : &kFwdBf16) : bwd ? &kBwdVariants[vi] : &kFwdVariants[vi];
+    int vi = 0;
+    if (bf16) {
+        std::lock_guard<std::mutex> lk(g_mu);
+        const int forced = bwd ? g_bwd_variant16 : g_fwd_variant16;
+        vi = forced >= 0 ? forced : 0;
+    } else {
+        vi = pick_variant(bwd, B, HJ, sms);
+    }
+    const Variant *v = bf16 ? (bwd ? &kBwdBf16Variants[vi] : &kFwdBf16Variants[vi])
+                            : bwd ? &kBwdVariants[vi] : &kFwdVariants[vi];
     if (mode != Mode::PLAIN && v->T() != QS_CARRY_STEPS) {
         // The carries are defined on QS_CARRY_STEPS-step chunks: keep the
         // design, take its default configuration (which has that chunk).
@@ -1399,6 +1418,14 @@ extern "C" int quat_cumprod_debug_set_timeout_ns(int64_t ns) {
 extern "C" int quat_cumprod_debug_stall_tile(int64_t tile) {
     std::lock_guard<std::mutex> lk(g_mu);
     g_stall_tile = (tile < 0 || tile > INT32_MAX) ? -1 : (int)tile;
+    return QS_OK;
+}
+
+extern "C" int quat_cumprod_debug_set_variant_bf16(int fwd_variant, int bwd_variant) {
+    if (fwd_variant >= kNumFwdBf16 || bwd_variant >= kNumBwdBf16) return QS_ERR_DIMS;
+    std::lock_guard<std::mutex> lk(g_mu);
+    g_fwd_variant16 = fwd_variant < 0 ? -1 : fwd_variant;
+    g_bwd_variant16 = bwd_variant < 0 ? -1 : bwd_variant;
     return QS_OK;
 }
 

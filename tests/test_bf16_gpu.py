@@ -53,9 +53,20 @@ def bf16_inputs(dev, w):
     return tb, exact
 
 
+N_BF16_VARIANTS = 4   # compiled configurations per direction
+
+
+@pytest.fixture(autouse=True)
+def reset_bf16_variant():
+    yield
+    qs.load_library().quat_cumprod_debug_set_variant_bf16(-1, -1)
+
+
+@pytest.mark.parametrize("variant", range(N_BF16_VARIANTS))
 @pytest.mark.parametrize("dims", [(1, 64, 2, 4), (2, 333, 3, 16), (3, 1100, 1, 40), (1, 70, 5, 2),
                                   (2, 1, 1, 2)])
-def test_bf16_matches_oracle(dev, dims):
+def test_bf16_matches_oracle(dev, dims, variant):
+    assert qs.load_library().quat_cumprod_debug_set_variant_bf16(variant, variant) == qs.QS_OK
     w = workloads.custom("bf16", *dims, q_kind="rotation", theta_max=0.6, seed=61)
     (tq, ti, td), (q, init, d_cum) = bf16_inputs(dev, w)
     cum = qs.quat_cumprod_fwd_bf16(tq, ti)
@@ -96,6 +107,12 @@ def test_bf16_rounding_is_the_only_difference_from_fp32(dev):
     g32, i32 = qs.quat_cumprod_bwd(tq.float(), ti.float(), td.float())
     for a, b in ((c16, c32), (g16.float(), g32), (i16.float(), i32)):
         assert normwise(a.cpu().numpy(), b.cpu().numpy().astype(np.float64)) <= 2.0 ** -8 + 1e-5
+
+
+def test_bf16_unknown_variant_is_rejected(dev):
+    lib = qs.load_library()
+    assert lib.quat_cumprod_debug_set_variant_bf16(N_BF16_VARIANTS, 0) == qs.QS_ERR_DIMS
+    assert lib.quat_cumprod_debug_set_variant_bf16(0, N_BF16_VARIANTS) == qs.QS_ERR_DIMS
 
 
 def test_bf16_rejects_odd_lane_count_and_wrong_dtype(dev):
