@@ -117,11 +117,11 @@ __device__ __forceinline__ void init_tile_bar(uint64_t *bar) {
 // Thread 0 stages the tile (q, and d_cum for the backward) of lane group g,
 // chunk c.  The test hook makes the barrier of tile `tile` (>= 0; the apply
 // kernel passes -1) expect 16 bytes that never come.
-template <bool BWD, int LT, int T>
+template <typename IO, bool BWD, int LT, int T>
 __device__ __forceinline__ void stage_tile(unsigned char *dst, uint64_t *bar, const CUtensorMap *qmap,
                                            const CUtensorMap *dmap, const Geometry &geo, int c, int g,
                                            const Control &ctl, int tile) {
-    constexpr uint32_t BYTES = T * LT * 16;
+    constexpr uint32_t BYTES = T * LT * IO::bytes;
     if (threadIdx.x == 0) {
         const int b = g / geo.NGb, x = (g - b * geo.NGb) * LT * 4;
         const uint32_t extra = (tile >= 0 && tile == ctl.stall_tile) ? 16u : 0u;
@@ -135,7 +135,7 @@ __device__ __forceinline__ void stage_tile(unsigned char *dst, uint64_t *bar, co
 // Aggregate kernel: one tile per CTA -> L_c (and W_c) of its LT lanes.
 // Tiles are numbered chunk-major: tile = c * NG + g.
 // ---------------------------------------------------------------------------
-template <bool BWD, int LT, int N>
+template <typename IO, bool BWD, int LT, int N>
 __global__ void __launch_bounds__(NTHREADS)
     quat_agg_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap dmap,
                     float4 *__restrict__ aggL, float4 *__restrict__ aggW, const Geometry geo, const Control ctl) {
@@ -143,8 +143,9 @@ __global__ void __launch_bounds__(NTHREADS)
     constexpr int T = NSEG * N;
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem = align128(smem_raw);
-    const float4 *Qt = reinterpret_cast<const float4 *>(smem);
-    const float4 *Dt = Qt + T * LT;
+    using E = typename IO::elem;
+    const E *Qt = reinterpret_cast<const E *>(smem);
+    const E *Dt = Qt + T * LT;
     __shared__ __align__(8) uint64_t bar;
     __shared__ float4 s_a[NSEG][LT];
     __shared__ float4 s_w[BWD ? NSEG : 1][LT];
@@ -154,15 +155,15 @@ __global__ void __launch_bounds__(NTHREADS)
     const int lane = threadIdx.x % LT, seg = threadIdx.x / LT;
     init_tile_bar(&bar);
     __syncthreads();
-    stage_tile<BWD, LT, T>(smem, &bar, &qmap, &dmap, geo, c, g, ctl, tile);
+    stage_tile<IO, BWD, LT, T>(smem, &bar, &qmap, &dmap, geo, c, g, ctl, tile);
     wait_tile(&bar, ctl, tile);
 
     const int cell0 = seg * N * LT + lane;
     float4 loc = q_ident(), W = q_zero();
 #pragma unroll
     for (int i = 0; i < N; ++i) {
-        loc = q_mul(Qt[cell0 + i * LT], loc);
-        if (BWD) W = q_add(W, q_mul_cl(loc, Dt[cell0 + i * LT]));
+        loc = q_mul(IO::get(Qt[cell0 + i * LT]), loc);
+        if (BWD) W = q_add(W, q_mul_cl(loc, IO::get(Dt[cell0 + i * LT])));
     }
     s_a[seg][lane] = loc;
     if (BWD) s_w[seg][lane] = W;
@@ -189,11 +190,11 @@ __global__ void __launch_bounds__(NTHREADS)
 // its range.  carF[c] = cum[t0-1]; carH[c] = H entering chunk c from the
 // right (H_{c+1}); d_init = H_0.
 // ---------------------------------------------------------------------------
-template <bool BWD, int LB>
+template <typename IO, bool BWD, int LB>
 __global__ void __launch_bounds__(NTHREADS)
     quat_carry_kernel(const float4 *__restrict__ aggL, const float4 *__restrict__ aggW,
-                      const float4 *__restrict__ init, float4 *__restrict__ carF, float4 *__restrict__ carH,
-                      float4 *__restrict__ d_init, const Geometry geo, int LT) {
+                      const typename IO::elem *__restrict__ init, float4 *__restrict__ carF,
+                      float4 *__restrict__ carH, typename IO::elem *__restrict__ d_init, const Geometry geo, int LT) {
     constexpr int RT = NTHREADS / LB;
     constexpr int U = 8;   // aggregates loaded per batch (independent loads)
     __shared__ float4 xa[RT][LB];
@@ -245,12 +246,12 @@ __global__ void __launch_bounds__(NTHREADS)
     }
     __syncthreads();
     if (!in_range) return;
-    float4 carry = lane_ok ? init[static_cast<long long>(b) * geo.HJ + hj] : q_ident();
+    float4 carry = lane_ok ? IO::get(init[static_cast<long long>(b) * geo.HJ + hj]) : q_ident();
     for (int k = 0; k < r; ++k) carry = q_mul(xa[k][l], carry);
     float4 h = q_zero();
     if (BWD) {
         for (int k = RT - 1; k > r; --k) h = q_add(xv[k][l], q_mul(xm[k][l], h));
-        if (r == 0 && lane_ok) d_init[static_cast<long long>(b) * geo.HJ + hj] = q_add(V, q_mul(M, h));
+        if (r == 0 && lane_ok) d_init[static_cast<long long>(b) * geo.HJ + hj] = IO::put(q_add(V, q_mul(M, h)));
     }
     for (int c0 = c_lo; c0 < c_hi; c0 += U) {
         float4 Lb[U];
@@ -287,17 +288,19 @@ __global__ void __launch_bounds__(NTHREADS)
 // cum[t] = local_t (x) F_c.  Backward: reverse pass G = d_cum + H,
 // d_q = G (x) conj(cum[t-1]), H = conj(q_t) (x) G.
 // ---------------------------------------------------------------------------
-template <bool BWD, int LT, int N>
+template <typename IO, bool BWD, int LT, int N>
 __global__ void __launch_bounds__(NTHREADS)
     quat_apply_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap dmap,
-                      const float4 *__restrict__ carF, const float4 *__restrict__ carH, float4 *__restrict__ out,
+                      const float4 *__restrict__ carF, const float4 *__restrict__ carH,
+                      typename IO::elem *__restrict__ out,
                       const Geometry geo, const Control ctl) {
     constexpr int NSEG = NTHREADS / LT;
     constexpr int T = NSEG * N;
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem = align128(smem_raw);
-    const float4 *Qt = reinterpret_cast<const float4 *>(smem);
-    const float4 *Dt = Qt + T * LT;
+    using E = typename IO::elem;
+    const E *Qt = reinterpret_cast<const E *>(smem);
+    const E *Dt = Qt + T * LT;
     __shared__ __align__(8) uint64_t bar;
     __shared__ float4 s_a[NSEG][LT];
     __shared__ float4 s_w[BWD ? NSEG : 1][LT];
@@ -309,7 +312,7 @@ __global__ void __launch_bounds__(NTHREADS)
     const int lane = threadIdx.x % LT, seg = threadIdx.x / LT;
     init_tile_bar(&bar);
     __syncthreads();
-    stage_tile<BWD, LT, T>(smem, &bar, &qmap, &dmap, geo, c, g, ctl, -1);
+    stage_tile<IO, BWD, LT, T>(smem, &bar, &qmap, &dmap, geo, c, g, ctl, -1);
     const long long o = static_cast<long long>(c) * geo.NL + static_cast<long long>(g) * LT + lane;
     if (seg == 0) {   // carries of this chunk (their loads overlap the tile load)
         s_cf[lane] = __ldg(carF + o);
@@ -321,13 +324,13 @@ __global__ void __launch_bounds__(NTHREADS)
     const bool lane_ok = hj < geo.HJ;
     const long long t0 = static_cast<long long>(c) * T + seg * N;
     const int cell0 = seg * N * LT + lane;
-    float4 *dst = out + (static_cast<long long>(b) * geo.S + t0) * geo.HJ + hj;
+    E *dst = out + (static_cast<long long>(b) * geo.S + t0) * geo.HJ + hj;
     if (!BWD) {
         float4 x[N];
         float4 loc = q_ident();
 #pragma unroll
         for (int i = 0; i < N; ++i) {
-            loc = q_mul(Qt[cell0 + i * LT], loc);
+            loc = q_mul(IO::get(Qt[cell0 + i * LT]), loc);
             x[i] = loc;
         }
         s_a[seg][lane] = loc;
@@ -337,7 +340,7 @@ __global__ void __launch_bounds__(NTHREADS)
         if (lane_ok) {
 #pragma unroll
             for (int i = 0; i < N; ++i)
-                if (t0 + i < geo.S) __stcs(dst + static_cast<long long>(i) * geo.HJ, q_mul(x[i], X));
+                if (t0 + i < geo.S) __stcs(dst + static_cast<long long>(i) * geo.HJ, IO::put(q_mul(x[i], X)));
         }
     } else {
         float4 lp[N];
@@ -345,8 +348,8 @@ __global__ void __launch_bounds__(NTHREADS)
 #pragma unroll
         for (int i = 0; i < N; ++i) {
             lp[i] = loc;
-            loc = q_mul(Qt[cell0 + i * LT], loc);
-            W = q_add(W, q_mul_cl(loc, Dt[cell0 + i * LT]));
+            loc = q_mul(IO::get(Qt[cell0 + i * LT]), loc);
+            W = q_add(W, q_mul_cl(loc, IO::get(Dt[cell0 + i * LT])));
         }
         s_a[seg][lane] = loc;
         s_w[seg][lane] = W;
@@ -357,10 +360,10 @@ __global__ void __launch_bounds__(NTHREADS)
         for (int k = NSEG - 1; k > seg; --k) Hn = q_add(s_w[k][lane], q_mul_cl(s_a[k][lane], Hn));
 #pragma unroll
         for (int i = N - 1; i >= 0; --i) {
-            const float4 G = q_add(Dt[cell0 + i * LT], Hn);
+            const float4 G = q_add(IO::get(Dt[cell0 + i * LT]), Hn);
             if (lane_ok && t0 + i < geo.S)
-                __stcs(dst + static_cast<long long>(i) * geo.HJ, q_mul_cr(G, q_mul(lp[i], X)));
-            Hn = q_mul_cl(Qt[cell0 + i * LT], G);
+                __stcs(dst + static_cast<long long>(i) * geo.HJ, IO::put(q_mul_cr(G, q_mul(lp[i], X))));
+            Hn = q_mul_cl(IO::get(Qt[cell0 + i * LT]), G);
         }
     }
 }
@@ -719,8 +722,8 @@ __global__ void __launch_bounds__(NTHREADS)
 }
 
 // Shared memory of a tile kernel (dynamic part).
-__host__ __device__ constexpr size_t tile_smem_bytes(bool bwd, int lt, int n) {
-    return 128 + size_t(bwd ? 2 : 1) * (NTHREADS / lt) * n * lt * 16;
+__host__ __device__ constexpr size_t tile_smem_bytes(bool bwd, int lt, int n, int eb = 16) {
+    return 128 + size_t(bwd ? 2 : 1) * (NTHREADS / lt) * n * lt * eb;
 }
 
 // Dynamic shared memory of the walk kernels: the forward ring, or the larger
@@ -758,9 +761,9 @@ struct Variant {
 
 #define QS_VARIANT(B, LT, N)                                                                        \
     Variant {                                                                                       \
-        false, reinterpret_cast<const void *>(qs::quat_agg_kernel<B, LT, N>),                       \
-            reinterpret_cast<const void *>(qs::quat_apply_kernel<B, LT, N>), B, LT, NTHREADS / (LT), N, \
-            qs::tile_smem_bytes(B, LT, N)                                                           \
+        false, reinterpret_cast<const void *>(qs::quat_agg_kernel<qs::IoF32, B, LT, N>),            \
+            reinterpret_cast<const void *>(qs::quat_apply_kernel<qs::IoF32, B, LT, N>), B, LT,      \
+            NTHREADS / (LT), N, qs::tile_smem_bytes(B, LT, N)                                       \
     }
 #define QS_WALK_FWD(LT, NSEG, N, NST)                                                               \
     Variant {                                                                                       \
@@ -816,22 +819,32 @@ const Variant kBwdGiven = Variant{true,
                 qs::quat_walk_bwd_kernel<qs::IoBF16, LT, NSEG, N, NSTF, NSTB, SELF, false>),        \
             nullptr, true, LT, NSEG, N, qs::walk_bwd_smem_bytes(LT, NSEG, N, NSTF, NSTB, 8)         \
     }
+#define QS_VARIANT16(B, LT, N)                                                                      \
+    Variant {                                                                                       \
+        false, reinterpret_cast<const void *>(qs::quat_agg_kernel<qs::IoBF16, B, LT, N>),           \
+            reinterpret_cast<const void *>(qs::quat_apply_kernel<qs::IoBF16, B, LT, N>), B, LT,     \
+            NTHREADS / (LT), N, qs::tile_smem_bytes(B, LT, N, 8)                                    \
+    }
 const Variant kFwdBf16Variants[] = {
     QS_WALK_FWD16(32, 8, 8, 6),            // 0: 32 lanes x 64 steps, 6 x 16 KiB ring
     QS_WALK_FWD16(16, 8, 8, 6),            // 1: 16 lanes x 64 steps (128 threads), 6 x 8 KiB
     QS_WALK_FWD16(16, 16, 8, 4),           // 2: 16 lanes x 128 steps (256 threads), 4 x 16 KiB
     QS_WALK_FWD16(32, 16, 4, 6),           // 3: 32 lanes x 64 steps (512 threads), 6 x 16 KiB
+    QS_VARIANT16(false, 32, 8),            // 4: three kernels, 64-step chunks (few lane groups)
 };
 const Variant kBwdBf16Variants[] = {
     QS_WALK_BWD16(16, 8, 8, 8, 4, false),  // 0: 16 lanes x 64 steps (128 threads), 64 KiB rings
     QS_WALK_BWD16(16, 8, 8, 8, 4, true),   // 1: the same, each thread folds its own carries
     QS_WALK_BWD16(16, 16, 4, 8, 4, false), // 2: 16 lanes x 64 steps (256 threads), 64 KiB rings
     QS_WALK_BWD16(32, 8, 8, 8, 4, false),  // 3: 32 lanes x 64 steps (256 threads), 128 KiB rings
+    QS_VARIANT16(true, 32, 8),             // 4: three kernels, 64-step chunks (few lane groups)
 };
+#undef QS_VARIANT16
 #undef QS_WALK_FWD16
 #undef QS_WALK_BWD16
 constexpr int kNumFwdBf16 = sizeof(kFwdBf16Variants) / sizeof(kFwdBf16Variants[0]);
-constexpr int kFwdBf16Default = 1, kBwdBf16Default = 0;   // fastest measured on 8x4096x16x32
+constexpr int kFwdBf16Default = 1, kBwdBf16Default = 0;   // walks; fastest measured on 8x4096x16x32
+constexpr int kFwdBf16Three = 4, kBwdBf16Three = 4;       // for too few lane groups
 constexpr int kNumBwdBf16 = sizeof(kBwdBf16Variants) / sizeof(kBwdBf16Variants[0]);
 #undef QS_VARIANT
 #undef QS_WALK_FWD
@@ -1045,9 +1058,20 @@ int make_plan(bool bwd, int64_t B, int64_t S, int64_t HJ, int sms, Plan *pl, Mod
               bool bf16 = false) {
     int vi = 0;
     if (bf16) {
-        std::lock_guard<std::mutex> lk(g_mu);
-        const int forced = bwd ? g_bwd_variant16 : g_fwd_variant16;
-        vi = forced >= 0 ? forced : (bwd ? kBwdBf16Default : kFwdBf16Default);
+        int forced;
+        {
+            std::lock_guard<std::mutex> lk(g_mu);
+            forced = bwd ? g_bwd_variant16 : g_fwd_variant16;
+        }
+        if (forced >= 0) {
+            vi = forced;
+        } else {   // the same rule as for fp32: a walk when the lane groups fill the GPU
+            const int wi = bwd ? kBwdBf16Default : kFwdBf16Default;
+            const Variant &w = bwd ? kBwdBf16Variants[wi] : kFwdBf16Variants[wi];
+            const long long groups = (long long)B * ((HJ + w.lt - 1) / w.lt);
+            const long long need = bwd ? 3ll * sms / 2 : 3ll * sms / 4;
+            vi = groups >= need ? wi : (bwd ? kBwdBf16Three : kFwdBf16Three);
+        }
     } else {
         vi = pick_variant(bwd, B, HJ, sms);
     }
@@ -1177,12 +1201,20 @@ int launch(bool bwd, const void *q, const void *d_cum, void *out, const void *in
     const int tiles = (int)pl.tiles;
     int lt = pl.v->lt;
     const void *carry_fn;
-    if (pl.carry_lb == 8)
-        carry_fn = bwd ? reinterpret_cast<const void *>(qs::quat_carry_kernel<true, 8>)
-                       : reinterpret_cast<const void *>(qs::quat_carry_kernel<false, 8>);
-    else
-        carry_fn = bwd ? reinterpret_cast<const void *>(qs::quat_carry_kernel<true, 32>)
-                       : reinterpret_cast<const void *>(qs::quat_carry_kernel<false, 32>);
+    if (bf16) {
+        if (pl.carry_lb == 8)
+            carry_fn = bwd ? reinterpret_cast<const void *>(qs::quat_carry_kernel<qs::IoBF16, true, 8>)
+                           : reinterpret_cast<const void *>(qs::quat_carry_kernel<qs::IoBF16, false, 8>);
+        else
+            carry_fn = bwd ? reinterpret_cast<const void *>(qs::quat_carry_kernel<qs::IoBF16, true, 32>)
+                           : reinterpret_cast<const void *>(qs::quat_carry_kernel<qs::IoBF16, false, 32>);
+    } else if (pl.carry_lb == 8) {
+        carry_fn = bwd ? reinterpret_cast<const void *>(qs::quat_carry_kernel<qs::IoF32, true, 8>)
+                       : reinterpret_cast<const void *>(qs::quat_carry_kernel<qs::IoF32, false, 8>);
+    } else {
+        carry_fn = bwd ? reinterpret_cast<const void *>(qs::quat_carry_kernel<qs::IoF32, true, 32>)
+                       : reinterpret_cast<const void *>(qs::quat_carry_kernel<qs::IoF32, false, 32>);
+    }
     void *agg_args[] = {&qmap, &dmap, &aggL, &aggW, &pl.geo, &ctl};
     void *carry_args[] = {&aggL_c, &aggW_c, &init4, &carF, &carH, &dinit4, &pl.geo, &lt};
     void *apply_args[] = {&qmap, &dmap, &carF_c, &carH_c, &out4, &pl.geo, &ctl};
@@ -1546,10 +1578,10 @@ int noalloc_launch(const float *q, const float *init, const float *d_cum, float 
     const float4 *aggL_c = aggL, *aggW_c = aggW, *carF_c = carF, *carH_c = carH;
     int lt = NA_LT;
     const int carry_lb = geo.C > 256 ? 8 : 32;
-    const void *agg_fn = reinterpret_cast<const void *>(qs::quat_agg_kernel<true, NA_LT, NA_N>);
-    const void *apply_fn = reinterpret_cast<const void *>(qs::quat_apply_kernel<true, NA_LT, NA_N>);
-    const void *carry_fn = carry_lb == 8 ? reinterpret_cast<const void *>(qs::quat_carry_kernel<true, 8>)
-                                         : reinterpret_cast<const void *>(qs::quat_carry_kernel<true, 32>);
+    const void *agg_fn = reinterpret_cast<const void *>(qs::quat_agg_kernel<qs::IoF32, true, NA_LT, NA_N>);
+    const void *apply_fn = reinterpret_cast<const void *>(qs::quat_apply_kernel<qs::IoF32, true, NA_LT, NA_N>);
+    const void *carry_fn = carry_lb == 8 ? reinterpret_cast<const void *>(qs::quat_carry_kernel<qs::IoF32, true, 8>)
+                                         : reinterpret_cast<const void *>(qs::quat_carry_kernel<qs::IoF32, true, 32>);
     const size_t smem = qs::tile_smem_bytes(true, NA_LT, NA_N);
     void *agg_args[] = {&qmap, &dmap, &aggL, &aggW, &geo, &ctl};
     void *carry_args[] = {&aggL_c, &aggW_c, &init4, &carF, &carH, &dinit4, &geo, &lt};

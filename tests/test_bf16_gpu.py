@@ -53,7 +53,7 @@ def bf16_inputs(dev, w):
     return tb, exact
 
 
-N_BF16_VARIANTS = 4   # compiled configurations per direction
+N_BF16_VARIANTS = 5   # compiled configurations per direction (0-3 walks, 4 three kernels)
 
 
 @pytest.fixture(autouse=True)
@@ -107,6 +107,30 @@ def test_bf16_rounding_is_the_only_difference_from_fp32(dev):
     g32, i32 = qs.quat_cumprod_bwd(tq.float(), ti.float(), td.float())
     for a, b in ((c16, c32), (g16.float(), g32), (i16.float(), i32)):
         assert normwise(a.cpu().numpy(), b.cpu().numpy().astype(np.float64)) <= 2.0 ** -8 + 1e-5
+
+
+@pytest.mark.parametrize("name,kernels", [("mamba3", 1), ("large", 1), ("long", 3), ("small", 3)])
+def test_bf16_plan_picks_the_design_by_lane_groups(dev, name, kernels):
+    w = workloads.WORKLOADS[name]
+    for call in ("fwd_bf16", "bwd_bf16"):
+        assert qs.quat_cumprod_plan(call, w.B, w.S, w.H, w.J, device=dev)[1] == kernels
+
+
+def test_bf16_long_sequence_sampled_lanes(dev):
+    """The long workload (few lanes: aggregate / carry / apply) at full size, sampled lanes."""
+    w = workloads.WORKLOADS["long"]
+    (tq, ti, td), _ = bf16_inputs(dev, w)
+    cum = qs.quat_cumprod_fwd_bf16(tq, ti)
+    d_q, d_init = qs.quat_cumprod_bwd_bf16(tq, ti, td)
+    assert qs.quat_cumprod_status(device=dev) == qs.QS_OK
+    lanes = np.random.default_rng(4).choice(w.lanes, 6, replace=False)
+    host = [t.float().cpu().numpy() for t in (tq, ti, td, cum, d_q, d_init)]
+    sq, si, sd = (a.astype(np.float64) for a in workloads.sample_lanes(host[:3], lanes, w.H, w.J))
+    gc, gq, gi = workloads.sample_lanes(host[3:], lanes, w.H, w.J)
+    ref_dq, ref_di = oracle.bwd(sq, si, sd)
+    assert normwise(gc, oracle.fwd(sq, si)) <= TOL_BF16
+    assert normwise(gq, ref_dq) <= TOL_BF16
+    assert normwise(gi, ref_di) <= TOL_BF16
 
 
 def test_bf16_unknown_variant_is_rejected(dev):
