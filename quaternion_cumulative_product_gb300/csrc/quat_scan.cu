@@ -284,6 +284,125 @@ __global__ void __launch_bounds__(NTHREADS)
 }
 
 // ---------------------------------------------------------------------------
+// Carry kernel for many chunks per lane: one block per padded lane, thread r
+// folds the chunk range r (about C / 256 chunks); the 256 range products (and
+// affine range maps) are combined by a log-depth scan in shared memory, then
+// every thread writes the carries of its range.  Same outputs as
+// quat_carry_kernel.
+// ---------------------------------------------------------------------------
+template <typename IO, bool BWD>
+__global__ void __launch_bounds__(NTHREADS)
+    quat_carry_scan_kernel(const float4 *__restrict__ aggL, const float4 *__restrict__ aggW,
+                           const typename IO::elem *__restrict__ init, float4 *__restrict__ carF,
+                           float4 *__restrict__ carH, typename IO::elem *__restrict__ d_init, const Geometry geo,
+                           int LT) {
+    constexpr int U = 8;   // aggregates loaded per batch (independent loads)
+    __shared__ float4 sP[NTHREADS];
+    __shared__ float4 sM[BWD ? NTHREADS : 1];
+    __shared__ float4 sV[BWD ? NTHREADS : 1];
+    const int gl = static_cast<int>(blockIdx.x);   // padded lane
+    const int r = threadIdx.x;
+    const int g = gl / LT, lig = gl - g * LT;
+    const int b = g / geo.NGb, hj = (g - b * geo.NGb) * LT + lig;
+    const bool lane_ok = hj < geo.HJ;
+    const int C = geo.C;
+    const long long NL = geo.NL;
+    const int R = (C + NTHREADS - 1) / NTHREADS;
+    const int c_lo = min(C, r * R), c_hi = min(C, c_lo + R);
+    auto at = [&](int c) { return static_cast<long long>(c) * NL + gl; };
+
+    // This range as a product P and (backward) as the map h -> V + M (x) h.
+    float4 P = q_ident(), M = q_ident(), V = q_zero();
+    for (int c0 = c_lo; c0 < c_hi; c0 += U) {
+        float4 Lb[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) Lb[u] = (c0 + u < c_hi) ? __ldg(aggL + at(c0 + u)) : q_ident();
+#pragma unroll
+        for (int u = 0; u < U; ++u) P = q_mul(Lb[u], P);
+    }
+    if (BWD) {
+        for (int c1 = c_hi; c1 > c_lo; c1 -= U) {
+            float4 Lb[U], Wb[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int cc = c1 - 1 - u;
+                const bool in = cc >= c_lo;
+                Lb[u] = in ? __ldg(aggL + at(cc)) : q_ident();
+                Wb[u] = in ? __ldg(aggW + at(cc)) : q_zero();
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                V = q_add(Wb[u], q_mul_cl(Lb[u], V));
+                M = q_mul_cl(Lb[u], M);
+            }
+        }
+    }
+    // Inclusive scans over the ranges: products of ranges 0..r (later on the
+    // left) and maps of ranges r..255 (range r applied last).
+    sP[r] = P;
+    if (BWD) {
+        sM[r] = M;
+        sV[r] = V;
+    }
+    __syncthreads();
+    for (int d = 1; d < NTHREADS; d <<= 1) {
+        const float4 oP = r >= d ? sP[r - d] : q_ident();
+        float4 oM = q_ident(), oV = q_zero();
+        if (BWD && r + d < NTHREADS) {
+            oM = sM[r + d];
+            oV = sV[r + d];
+        }
+        __syncthreads();
+        if (r >= d) {
+            P = q_mul(P, oP);
+            sP[r] = P;
+        }
+        if (BWD && r + d < NTHREADS) {
+            V = q_add(V, q_mul(M, oV));
+            M = q_mul(M, oM);
+            sM[r] = M;
+            sV[r] = V;
+        }
+        __syncthreads();
+    }
+    const float4 init4 = lane_ok ? IO::get(init[static_cast<long long>(b) * geo.HJ + hj]) : q_ident();
+    float4 carry = r > 0 ? q_mul(sP[r - 1], init4) : init4;   // cum just before range r
+    float4 h = q_zero();                                       // H entering range r from the right
+    if (BWD) {
+        if (r + 1 < NTHREADS) h = sV[r + 1];
+        if (r == 0 && lane_ok) d_init[static_cast<long long>(b) * geo.HJ + hj] = IO::put(sV[0]);
+    }
+    for (int c0 = c_lo; c0 < c_hi; c0 += U) {
+        float4 Lb[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) Lb[u] = (c0 + u < c_hi) ? __ldg(aggL + at(c0 + u)) : q_ident();
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            if (c0 + u < c_hi) carF[at(c0 + u)] = carry;
+            carry = q_mul(Lb[u], carry);
+        }
+    }
+    if (BWD) {
+        for (int c1 = c_hi; c1 > c_lo; c1 -= U) {
+            float4 Lb[U], Wb[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int cc = c1 - 1 - u;
+                const bool in = cc >= c_lo;
+                Lb[u] = in ? __ldg(aggL + at(cc)) : q_ident();
+                Wb[u] = in ? __ldg(aggW + at(cc)) : q_zero();
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int cc = c1 - 1 - u;
+                if (cc >= c_lo) carH[at(cc)] = h;
+                h = q_add(Wb[u], q_mul_cl(Lb[u], h));
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
 // Apply kernel: one tile per CTA, in reverse tile order.  Forward:
 // cum[t] = local_t (x) F_c.  Backward: reverse pass G = d_cum + H,
 // d_q = G (x) conj(cum[t-1]), H = conj(q_t) (x) G.
@@ -1201,7 +1320,14 @@ int launch(bool bwd, const void *q, const void *d_cum, void *out, const void *in
     const int tiles = (int)pl.tiles;
     int lt = pl.v->lt;
     const void *carry_fn;
-    if (bf16) {
+    // Many chunks per lane: one block per lane and a scan over 256 ranges.
+    const bool scan = pl.geo.C > 256;
+    if (scan) {
+        carry_fn = bf16 ? (bwd ? reinterpret_cast<const void *>(qs::quat_carry_scan_kernel<qs::IoBF16, true>)
+                               : reinterpret_cast<const void *>(qs::quat_carry_scan_kernel<qs::IoBF16, false>))
+                        : (bwd ? reinterpret_cast<const void *>(qs::quat_carry_scan_kernel<qs::IoF32, true>)
+                               : reinterpret_cast<const void *>(qs::quat_carry_scan_kernel<qs::IoF32, false>));
+    } else if (bf16) {
         if (pl.carry_lb == 8)
             carry_fn = bwd ? reinterpret_cast<const void *>(qs::quat_carry_kernel<qs::IoBF16, true, 8>)
                            : reinterpret_cast<const void *>(qs::quat_carry_kernel<qs::IoBF16, false, 8>);
@@ -1218,7 +1344,7 @@ int launch(bool bwd, const void *q, const void *d_cum, void *out, const void *in
     void *agg_args[] = {&qmap, &dmap, &aggL, &aggW, &pl.geo, &ctl};
     void *carry_args[] = {&aggL_c, &aggW_c, &init4, &carF, &carH, &dinit4, &pl.geo, &lt};
     void *apply_args[] = {&qmap, &dmap, &carF_c, &carH_c, &out4, &pl.geo, &ctl};
-    const int carry_blocks = (pl.geo.NL + pl.carry_lb - 1) / pl.carry_lb;
+    const int carry_blocks = scan ? pl.geo.NL : (pl.geo.NL + pl.carry_lb - 1) / pl.carry_lb;
     if (cudaLaunchKernel(pl.v->agg, dim3(tiles), dim3(NTHREADS), agg_args, pl.v->smem(), stream) != cudaSuccess ||
         cudaLaunchKernel(carry_fn, dim3(carry_blocks), dim3(NTHREADS), carry_args, 0, stream) != cudaSuccess ||
         cudaLaunchKernel(pl.v->apply, dim3(tiles), dim3(NTHREADS), apply_args, pl.v->smem(), stream) !=

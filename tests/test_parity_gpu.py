@@ -199,6 +199,16 @@ def test_every_compiled_variant(dev, variant, dims):
     check_against_oracle(dev, *workloads.make_inputs(w))
 
 
+@pytest.mark.parametrize("variant", [0, 1])   # 64- and 32-step chunks
+@pytest.mark.parametrize("dims", [(1, 20000, 1, 3), (2, 17000, 2, 5)])
+def test_many_chunks_per_lane_carry_scan(dev, variant, dims):
+    """More than 256 chunks per lane: the carry step scans 256 chunk ranges per lane."""
+    lib = qs.load_library()
+    assert lib.quat_cumprod_debug_set_variant(variant, variant) == qs.QS_OK
+    w = workloads.custom("chunks", *dims, q_kind="rotation", theta_max=0.3, seed=71 + variant)
+    check_against_oracle(dev, *workloads.make_inputs(w))
+
+
 def test_unknown_variant_is_rejected(dev):
     lib = qs.load_library()
     assert lib.quat_cumprod_debug_set_variant(N_FWD_VARIANTS, 0) == qs.QS_ERR_DIMS
