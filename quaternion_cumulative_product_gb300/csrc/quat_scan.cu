@@ -488,6 +488,153 @@ __global__ void __launch_bounds__(NTHREADS)
 }
 
 // ---------------------------------------------------------------------------
+// Chained-scan forward (single pass, one tile per CTA).  Tiles are numbered
+// chunk-major (tile = c * NG + g) and CTAs start in that order, so a tile
+// waits only on tiles that started before it.  Per lane, a tile publishes its
+// chunk product L_c and, once known, its inclusive value cum at its last step
+// (`incl`), each followed by that lane's status word, written with release
+// semantics by the thread that wrote the value; readers acquire the status
+// word before reading the value.  A tile's carry is the product of the
+// aggregates of the chunks before it, back to the nearest published
+// inclusive value (decoupled look-back); the NSEG segment threads of a lane
+// read NSEG predecessors per round.  Status words carry the launch's epoch,
+// so nothing has to be cleared between launches.  Every wait is bounded; a
+// tile whose wait ran out still publishes (NaN), so no successor waits out
+// its own limit because of it.
+// ---------------------------------------------------------------------------
+constexpr uint32_t CH_AGG = 1, CH_INCL = 2;   // status word: (epoch << 2) | state
+
+template <typename IO, int LT, int N>
+__global__ void __launch_bounds__(NTHREADS)
+    quat_chain_fwd_kernel(const __grid_constant__ CUtensorMap qmap, const typename IO::elem *__restrict__ init,
+                          typename IO::elem *__restrict__ out, uint32_t *__restrict__ flags,
+                          float4 *__restrict__ agg, float4 *__restrict__ incl, const Geometry geo,
+                          const Control ctl, uint32_t epoch) {
+    constexpr int NSEG = NTHREADS / LT;
+    constexpr int T = NSEG * N;
+    using E = typename IO::elem;
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char *smem = align128(smem_raw);
+    const E *Qt = reinterpret_cast<const E *>(smem);
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ float4 s_a[NSEG][LT];
+    __shared__ float4 s_lb[NSEG][LT];       // one look-back round: a predecessor per segment
+    __shared__ uint32_t s_st[NSEG][LT];
+    __shared__ float4 s_x[LT];              // carry into the tile
+
+    const int tile = static_cast<int>(blockIdx.x);
+    const int c = tile / geo.NG, g = tile - c * geo.NG;
+    const int lane = threadIdx.x % LT, seg = threadIdx.x / LT;
+    const int b = g / geo.NGb, hj = (g - b * geo.NGb) * LT + lane;
+    const bool lane_ok = hj < geo.HJ;
+    init_tile_bar(&bar);
+    __syncthreads();
+    stage_tile<IO, false, LT, T>(smem, &bar, &qmap, &qmap, geo, c, g, ctl, tile);
+    float4 init4 = q_ident();
+    if (c == 0 && seg == 0 && lane_ok) init4 = IO::get(init[static_cast<long long>(b) * geo.HJ + hj]);
+    wait_tile(&bar, ctl, tile);
+
+    const int cell0 = seg * N * LT + lane;
+    float4 x[N];
+    float4 loc = q_ident();
+#pragma unroll
+    for (int k = 0; k < N; ++k) {
+        loc = q_mul(IO::get(Qt[cell0 + k * LT]), loc);
+        x[k] = loc;
+    }
+    s_a[seg][lane] = loc;
+    __syncthreads();
+    const uint32_t tag = epoch << 2;
+    const long long me = static_cast<long long>(tile) * LT + lane;
+    float4 L = q_ident();
+    if (seg == 0) {
+#pragma unroll
+        for (int k = 0; k < NSEG; ++k) L = q_mul(s_a[k][lane], L);
+        if (c > 0) {   // the aggregate first: successors can use it before the carry is known
+            __stcg(agg + me, L);
+            st_release_u32(flags + me, tag | CH_AGG);
+        }
+    }
+    // Look-back: acc = L_{c-1} (x) L_{c-2} (x) ... (x) incl_p.  Per round the
+    // NSEG segment threads of a lane read NSEG * LB consecutive predecessors,
+    // LB each (segment k: chunks base - k*LB .. base - k*LB - LB + 1), fold
+    // them locally up to the first inclusive value, and segment 0 combines the
+    // NSEG partial products in order.
+    constexpr int LB = 4;
+    float4 acc = init4;   // chunk 0: the carry is init
+    bool done = c == 0;
+    if (c > 0) {
+        acc = q_ident();
+        for (int base = c - 1;; base -= NSEG * LB) {
+            float4 part = q_ident();
+            uint32_t pst = 0;   // CH_INCL once the fold reached an inclusive value
+#pragma unroll 1
+            for (int j = 0; j < LB && pst != CH_INCL; ++j) {
+                const int p = base - seg * LB - j;
+                if (p < 0) break;   // chunk 0 publishes an inclusive value, so this is never needed
+                const long long idx = (static_cast<long long>(p) * geo.NG + g) * LT + lane;
+                uint32_t f = ld_acquire_u32(flags + idx);
+                bool lost = false;
+                if ((f & ~3u) != tag) {
+                    const unsigned long long t0 = global_timer_ns();
+                    do {
+                        if (global_timer_ns() - t0 > ctl.timeout_ns) {
+                            record_error(ctl.hdr, tile);
+                            lost = true;
+                            break;
+                        }
+                        f = ld_acquire_u32(flags + idx);
+                    } while ((f & ~3u) != tag);
+                }
+                if (lost) {
+                    part = q_nan();
+                    pst = CH_INCL;
+                } else if ((f & 3u) == CH_INCL) {
+                    part = q_mul(part, __ldcg(incl + idx));
+                    pst = CH_INCL;
+                } else {
+                    part = q_mul(part, __ldcg(agg + idx));
+                }
+            }
+            s_lb[seg][lane] = part;
+            s_st[seg][lane] = pst;
+            __syncthreads();
+            if (seg == 0 && !done) {
+#pragma unroll 1
+                for (int k = 0; k < NSEG; ++k) {
+                    acc = q_mul(acc, s_lb[k][lane]);
+                    if (s_st[k][lane] == CH_INCL) {
+                        done = true;
+                        break;
+                    }
+                }
+            }
+            if (!__syncthreads_or(seg == 0 && !done)) break;
+        }
+    }
+    if (seg == 0) {
+        __stcg(incl + me, q_mul(L, acc));
+        st_release_u32(flags + me, tag | CH_INCL);
+        s_x[lane] = acc;
+    }
+    __syncthreads();
+    float4 X = s_x[lane];   // cum just before this segment
+#pragma unroll
+    for (int k = 0; k < NSEG - 1; ++k)
+        if (k < seg) X = q_mul(s_a[k][lane], X);
+    const long long t0 = static_cast<long long>(c) * T + seg * N;
+    E *dst = out + (static_cast<long long>(b) * geo.S + t0) * geo.HJ + hj;
+    if (lane_ok && t0 + N <= geo.S) {
+#pragma unroll
+        for (int k = 0; k < N; ++k) __stcs(dst + static_cast<long long>(k) * geo.HJ, IO::put(q_mul(x[k], X)));
+    } else if (lane_ok) {
+#pragma unroll
+        for (int k = 0; k < N; ++k)
+            if (t0 + k < geo.S) __stcs(dst + static_cast<long long>(k) * geo.HJ, IO::put(q_mul(x[k], X)));
+    }
+}
+
+// ---------------------------------------------------------------------------
 // Walk kernels.  One CTA walks one lane group (LT lanes of one batch entry)
 // along the whole sequence, chunk by chunk: chunk c = T steps x LT lanes is
 // staged by one TMA load per operand through an NST-deep ring, thread
@@ -867,7 +1014,7 @@ constexpr unsigned long long DEFAULT_TIMEOUT_NS = 2000000000ull;
 // One compiled configuration: lane-group width LT, segments per chunk NSEG
 // (threads per CTA = LT * NSEG), steps per thread N.
 struct Variant {
-    bool walk;           // walk kernel (else aggregate / carry / apply)
+    bool walk;           // walk kernel (else aggregate / carry / apply, or chain)
     const void *agg;     // the walk kernel, or the aggregate kernel
     const void *apply;   // the apply kernel (three-kernel variants)
     bool bwd;
@@ -876,6 +1023,7 @@ struct Variant {
     int T() const { return nseg * n; }
     int threads() const { return lt * nseg; }
     size_t smem() const { return smem_bytes; }
+    bool chain = false;  // single-pass chained scan (forward): `agg` is the kernel
 };
 
 #define QS_VARIANT(B, LT, N)                                                                        \
@@ -903,6 +1051,8 @@ const Variant kFwdVariants[] = {
     QS_WALK_FWD(16, 8, 8, 3),          // 5: walk, 16 lanes x 64 steps (128 threads), 3 x 16 KiB
     QS_WALK_FWD(16, 16, 8, 3),         // 6: walk, 16 lanes x 128 steps (256 threads), 3 x 32 KiB
     QS_WALK_FWD(32, 8, 4, 6),          // 7: walk, 32 lanes x 32 steps, 6 x 16 KiB
+    Variant{false, reinterpret_cast<const void *>(qs::quat_chain_fwd_kernel<qs::IoF32, 32, 8>), nullptr, false,
+            32, NTHREADS / 32, 8, qs::tile_smem_bytes(false, 32, 8), true},   // 8: chained scan, 64-step tiles
 };
 const Variant kBwdVariants[] = {
     QS_VARIANT(true, 32, 8),           // 0: three kernels, 64-step chunks, 64 KiB tiles
@@ -995,8 +1145,12 @@ std::map<int, DevInfo> g_dev;
 struct Workspace {
     unsigned char *base = nullptr;
     size_t bytes = 0;
+    uint32_t epoch = 0;   // status words only: last epoch used
 };
 std::map<std::pair<int, uintptr_t>, Workspace> g_ws;
+// Status words of the chained scan, per (device, stream): an allocation of
+// their own that no other kernel writes, zeroed when allocated.
+std::map<std::pair<int, uintptr_t>, Workspace> g_flags;
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
                                    const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
@@ -1125,6 +1279,56 @@ int ensure_workspace(int dev, cudaStream_t stream, size_t need, unsigned char **
     return QS_OK;
 }
 
+// Status words of at least `need` bytes for a chained scan on (device,
+// stream), and the epoch this launch writes into them (epoch << 2 | state).
+// The words are zero when allocated; when the epochs run out they are
+// cleared on the stream and the count starts again.
+int chain_flags(int dev, cudaStream_t stream, size_t need, uint32_t **out, uint32_t *epoch) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    Workspace &w = g_flags[{dev, reinterpret_cast<uintptr_t>(stream)}];
+    if (w.bytes < need) {
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) {
+            cudaGetLastError();
+            return QS_ERR_CUDA;
+        }
+        if (cs != cudaStreamCaptureStatusNone) return QS_ERR_NOMEM;
+        if (w.base) {
+            if (cudaStreamSynchronize(stream) != cudaSuccess) {
+                cudaGetLastError();
+                return QS_ERR_CUDA;
+            }
+            cudaFree(w.base);
+            w.base = nullptr;
+            w.bytes = 0;
+        }
+        const size_t bytes = align_up(need + need / 4, 1 << 20);
+        void *p = nullptr;
+        if (cudaMalloc(&p, bytes) != cudaSuccess) {
+            cudaGetLastError();
+            return QS_ERR_NOMEM;
+        }
+        if (cudaMemsetAsync(p, 0, bytes, stream) != cudaSuccess) {
+            cudaGetLastError();
+            cudaFree(p);
+            return QS_ERR_CUDA;
+        }
+        w.base = static_cast<unsigned char *>(p);
+        w.bytes = bytes;
+        w.epoch = 0;
+    }
+    if (w.epoch >= (1u << 30) - 1) {
+        if (cudaMemsetAsync(w.base, 0, w.bytes, stream) != cudaSuccess) {
+            cudaGetLastError();
+            return QS_ERR_CUDA;
+        }
+        w.epoch = 0;
+    }
+    *epoch = ++w.epoch;
+    *out = reinterpret_cast<uint32_t *>(w.base);
+    return QS_OK;
+}
+
 // 3-D view [B][S][HJ*4 floats] of a [B,S,H,J,4] tensor for TMA boxes of `lt`
 // lanes x `boxh` steps.  Boxes may reach past the tensor: TMA fills those
 // cells with zeros.
@@ -1196,6 +1400,10 @@ int make_plan(bool bwd, int64_t B, int64_t S, int64_t HJ, int sms, Plan *pl, Mod
     }
     const Variant *v = bf16 ? (bwd ? &kBwdBf16Variants[vi] : &kFwdBf16Variants[vi])
                             : bwd ? &kBwdVariants[vi] : &kFwdVariants[vi];
+    if (mode != Mode::PLAIN && v->chain) {   // carries come from the other designs
+        vi = kThreeFwd;
+        v = &kFwdVariants[vi];
+    }
     if (mode != Mode::PLAIN && v->T() != QS_CARRY_STEPS) {
         // The carries are defined on QS_CARRY_STEPS-step chunks: keep the
         // design, take its default configuration (which has that chunk).
@@ -1219,6 +1427,17 @@ int make_plan(bool bwd, int64_t B, int64_t S, int64_t HJ, int sms, Plan *pl, Mod
     g.NL = (int)(NG * LT);
     const size_t per = (size_t)pl->tiles * LT * 16;
     size_t off = sizeof(qs::WsHeader);
+    if (pl->v->chain) {
+        // Chained scan: status block, then per tile and lane the chunk product
+        // and the inclusive value (the status words live apart, see chain_flags).
+        pl->o_L = (size_t)pl->tiles * LT * 4;   // bytes of status words (their own allocation)
+        pl->o_W = off;   // chunk products
+        off = align_up(off + per, 256);
+        pl->o_F = off;   // inclusive values
+        off = align_up(off + per, 256);
+        pl->ws_bytes = off;
+        return QS_OK;
+    }
     if (pl->v->walk) {
         // Walk kernels: status block, then (backward) the carries F_c.
         if (bwd && mode != Mode::FROM_CARRIES) {
@@ -1269,6 +1488,29 @@ int launch(bool bwd, const void *q, const void *d_cum, void *out, const void *in
     rc = make_map(&qmap, q, B, S, HJ, pl.v->lt, pl.v->T(), eb);
     if (rc == QS_OK) rc = make_map(&dmap, bwd ? d_cum : q, B, S, HJ, pl.v->lt, pl.v->T(), eb);
     if (rc != QS_OK) return rc;
+    if (pl.v->chain) {
+        uint32_t epoch = 0, *flags = nullptr;
+        rc = chain_flags(dev, stream, pl.o_L, &flags, &epoch);
+        if (rc != QS_OK) return rc;
+        qs::Control ctl;
+        {
+            std::lock_guard<std::mutex> lk(g_mu);
+            ctl.timeout_ns = g_timeout_ns;
+            ctl.stall_tile = g_stall_tile;
+        }
+        ctl.hdr = reinterpret_cast<qs::WsHeader *>(ws);
+        const void *init4 = init;
+        void *out4 = out;
+        float4 *aggv = reinterpret_cast<float4 *>(ws + pl.o_W);
+        float4 *inclv = reinterpret_cast<float4 *>(ws + pl.o_F);
+        void *args[] = {&qmap, &init4, &out4, &flags, &aggv, &inclv, &pl.geo, &ctl, &epoch};
+        if (cudaLaunchKernel(pl.v->agg, dim3((unsigned)pl.tiles), dim3(NTHREADS), args, pl.v->smem(), stream) !=
+            cudaSuccess) {
+            cudaGetLastError();
+            return QS_ERR_CUDA;
+        }
+        return QS_OK;
+    }
     if (pl.v->walk) {
         float4 *carF = bwd ? reinterpret_cast<float4 *>(ws + pl.o_F) : nullptr;
         qs::Control ctl;
@@ -1555,7 +1797,7 @@ extern "C" int quat_cumprod_plan(int call, int64_t B, int64_t S, int64_t H, int6
     rc = make_plan(bwd, B, S, H * J, di->sms, &pl, mode, bf16);
     if (rc != QS_OK) return rc;
     *variant = pl.vi;
-    *kernels = pl.v->walk ? 1 : (mode == Mode::SAVE_CARRIES ? 4 : 3);
+    *kernels = (pl.v->walk || pl.v->chain) ? 1 : (mode == Mode::SAVE_CARRIES ? 4 : 3);
     return QS_OK;
 }
 

@@ -179,7 +179,7 @@ def test_empty_sizes(dev):
 
 
 # Variants 0-3: aggregate / carry / apply kernels; the rest: walk kernels.
-N_FWD_VARIANTS, N_BWD_VARIANTS = 8, 10
+N_FWD_VARIANTS, N_BWD_VARIANTS = 9, 10
 
 
 @pytest.mark.parametrize("variant", range(max(N_FWD_VARIANTS, N_BWD_VARIANTS)))
@@ -267,10 +267,12 @@ def test_binding_rejects_bad_tensors(dev):
 # runs out its bounded wait; the call reports QS_ERR_TIMEOUT (no hang) and the
 # next call is clean.
 # ---------------------------------------------------------------------------
-@pytest.mark.parametrize("variant", [0, 4])   # aggregate / carry / apply, and walk
+@pytest.mark.parametrize("variant", [0, 4, 8])   # aggregate / carry / apply, walk, chained scan (fwd)
 @pytest.mark.parametrize("which", ["fwd", "bwd"])
 def test_stalled_tile_reports_timeout_then_recovers(dev, which, variant):
     lib = qs.load_library()
+    if which == "bwd" and variant == 8:
+        variant = 4   # the chained scan is a forward design
     assert lib.quat_cumprod_debug_set_variant(variant, variant) == qs.QS_OK
     w = workloads.custom("stall", 2, 600, 2, 16, seed=21)
     q, init, d_cum = workloads.make_inputs(w)
