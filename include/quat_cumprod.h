@@ -36,13 +36,16 @@
  * happens on the device (a wait that ran out) is recorded in a per-stream
  * device word and reported by quat_cumprod_status().
  *
- * Scratch memory: both calls use a library-owned workspace per (device,
- * stream) for per-chunk aggregates and carries (32 bytes per lane and chunk
- * of 64 steps forward, 64 bytes backward).  The first call on a stream, and
- * any later call that needs a larger workspace, allocates it (cudaMalloc) and
- * synchronizes that stream; issue such a call before capturing the stream
- * into a CUDA graph.  Calls on one stream are ordered by the stream; calls on
- * different streams use different workspaces and may run concurrently.
+ * Scratch memory: the calls use a library-owned workspace per (device,
+ * stream) for a status block and per-chunk aggregates and carries.  Per lane
+ * and 64-step chunk this is nothing for a forward walk, 16 bytes for a
+ * backward walk, and 32 (forward) or 64 (backward) bytes for the aggregate /
+ * carry / apply kernels (see quat_cumprod_plan for which a call uses).  The
+ * first call on a stream, and any later call that needs a larger workspace,
+ * allocates it (cudaMalloc) and synchronizes that stream; issue such a call
+ * before capturing the stream into a CUDA graph.  Calls on one stream are
+ * ordered by the stream; calls on different streams use different workspaces
+ * and may run concurrently.
  *
  * Sizes: B, S, H, J >= 0.  Any zero size makes the call a no-op that returns
  * QS_OK (except that quat_cumprod_bwd with S == 0 writes d_init = 0).

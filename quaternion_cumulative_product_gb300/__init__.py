@@ -10,6 +10,13 @@ Operation (burn-mamba ``mamba3/quat_scan/backward.rs``, "Gradient math"):
 ``cum[t] = q_t (x) cum[t-1]`` with ``cum[-1] = init`` over ``[B,S,H,J,4]``
 fp32 tensors, and its vector-Jacobian product ``(d_q, d_init)`` recomputed
 from ``(q, init, d_cum)``.
+
+Calls: ``quat_cumprod_fwd`` / ``quat_cumprod_bwd`` (the page's operation),
+``quat_cumprod_fwd_carries`` / ``quat_cumprod_bwd_carries`` (keep the 64-step
+chunk carries between the two), ``quat_cumprod_fwd_bf16`` /
+``quat_cumprod_bwd_bf16`` (bfloat16 tensors), ``quat_cumprod_bwd_noalloc``
+(no allocation), ``quat_cumprod_plan`` and ``quat_cumprod_status``.  The
+autograd wrapper is in :mod:`quaternion_cumulative_product_gb300.autograd`.
 """
 from __future__ import annotations
 

@@ -38,10 +38,16 @@
 //    fill the GPU: every chunk is an independent tile --
 //      aggregate: one tile per CTA -> L_c (and W_c);
 //      carry:     per lane, chunk aggregates -> carries F_c (and H_{c+1},
-//                 d_init), with 8 to 32 threads per lane over chunk ranges;
+//                 d_init): 32 lanes per block over 8 chunk ranges, or for
+//                 many chunks one block per lane with a scan over 256 ranges;
 //      apply:     one tile per CTA, tiles in reverse order (the most recently
 //                 read tiles are still in L2) -> cum (or d_q).
-//    No kernel waits on another CTA.
+//    None of these kernels waits on another CTA.  A third, single-pass
+//    forward (chained scan with decoupled look-back across CTAs) is compiled
+//    as a configuration to force; it measured slower than both designs.
+//
+//  * Every tensor layout is [B, S, H, J, 4]; the kernels are templated on the
+//    element type in memory (four fp32, or four bfloat16), and compute in fp32.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -58,7 +64,7 @@
 
 namespace qs {
 
-constexpr int NTHREADS = 256;   // threads per CTA of the aggregate, carry and apply kernels
+constexpr int NTHREADS = 256;   // threads per CTA of every kernel but the walks
 
 // Device status of one (device, stream) workspace.
 struct __align__(256) WsHeader {
