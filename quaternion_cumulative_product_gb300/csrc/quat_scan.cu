@@ -60,953 +60,9 @@
 #include <utility>
 
 #include "quat_cumprod.h"
-#include "quat_device.cuh"
-
-namespace qs {
-
-constexpr int NTHREADS = 256;   // threads per CTA of every kernel but the walks
-
-// Device status of one (device, stream) workspace.
-struct __align__(256) WsHeader {
-    unsigned int err_code;        // 1 once a wait ran out (cleared by quat_cumprod_status)
-    unsigned int err_count;       // number of waits that ran out
-    unsigned long long err_item;  // first tile whose wait ran out
-};
-
-struct Geometry {
-    long long S;   // sequence length
-    int HJ;        // lanes per batch entry (H*J)
-    int NGb;       // lane groups per batch entry
-    int NG;        // lane groups in total
-    int C;         // chunks along the sequence
-    int NL;        // padded lanes (NG * LT): aggregates of chunk c start at c * NL
-};
-
-struct Control {
-    WsHeader *hdr;
-    int stall_tile;                  // test hook: this tile's wait never completes
-    unsigned long long timeout_ns;   // limit of every device-side wait
-};
-
-__device__ __forceinline__ unsigned char *align128(unsigned char *p) {
-    return reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(p) + 127) & ~uintptr_t(127));
-}
-
-__device__ void record_error(WsHeader *h, int item) {
-    if (atomicCAS(&h->err_code, 0u, 1u) == 0u) h->err_item = static_cast<unsigned long long>(item);
-    atomicAdd(&h->err_count, 1u);
-}
-
-// Waits for the tile's TMA copies.  Bounded: after ctl.timeout_ns the error is
-// recorded and the CTA carries on with whatever the stage holds (its outputs
-// are then invalid, and quat_cumprod_status reports QS_ERR_TIMEOUT).
-__device__ __forceinline__ void wait_tile(uint64_t *bar, const Control &ctl, int tile) {
-    if (mbar_try_wait(bar, 0)) return;
-    const unsigned long long t0 = global_timer_ns();
-    while (!mbar_try_wait(bar, 0)) {
-        if (global_timer_ns() - t0 > ctl.timeout_ns) {
-            if (threadIdx.x == 0) record_error(ctl.hdr, tile);
-            return;
-        }
-    }
-}
-
-// Thread 0 initialises the tile's barrier; the barrier must be visible to the
-// whole CTA (and to the TMA unit) before the copy is issued.
-__device__ __forceinline__ void init_tile_bar(uint64_t *bar) {
-    if (threadIdx.x == 0) {
-        mbar_init(bar, 1);
-        fence_mbar_init();
-    }
-}
-
-// Thread 0 stages the tile (q, and d_cum for the backward) of lane group g,
-// chunk c.  The test hook makes the barrier of tile `tile` (>= 0; the apply
-// kernel passes -1) expect 16 bytes that never come.
-template <typename IO, bool BWD, int LT, int T>
-__device__ __forceinline__ void stage_tile(unsigned char *dst, uint64_t *bar, const CUtensorMap *qmap,
-                                           const CUtensorMap *dmap, const Geometry &geo, int c, int g,
-                                           const Control &ctl, int tile) {
-    constexpr uint32_t BYTES = T * LT * IO::bytes;
-    if (threadIdx.x == 0) {
-        const int b = g / geo.NGb, x = (g - b * geo.NGb) * LT * 4;
-        const uint32_t extra = (tile >= 0 && tile == ctl.stall_tile) ? 16u : 0u;
-        mbar_arrive_expect_tx(bar, (BWD ? 2 : 1) * BYTES + extra);
-        tma_load_3d(dst, qmap, x, c * T, b, bar);
-        if (BWD) tma_load_3d(dst + BYTES, dmap, x, c * T, b, bar);
-    }
-}
-
-// ---------------------------------------------------------------------------
-// Aggregate kernel: one tile per CTA -> L_c (and W_c) of its LT lanes.
-// Tiles are numbered chunk-major: tile = c * NG + g.
-// ---------------------------------------------------------------------------
-template <typename IO, bool BWD, int LT, int N>
-__global__ void __launch_bounds__(NTHREADS)
-    quat_agg_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap dmap,
-                    float4 *__restrict__ aggL, float4 *__restrict__ aggW, const Geometry geo, const Control ctl) {
-    constexpr int NSEG = NTHREADS / LT;
-    constexpr int T = NSEG * N;
-    extern __shared__ unsigned char smem_raw[];
-    unsigned char *smem = align128(smem_raw);
-    using E = typename IO::elem;
-    const E *Qt = reinterpret_cast<const E *>(smem);
-    const E *Dt = Qt + T * LT;
-    __shared__ __align__(8) uint64_t bar;
-    __shared__ float4 s_a[NSEG][LT];
-    __shared__ float4 s_w[BWD ? NSEG : 1][LT];
-
-    const int tile = blockIdx.x;
-    const int c = tile / geo.NG, g = tile - c * geo.NG;
-    const int lane = threadIdx.x % LT, seg = threadIdx.x / LT;
-    init_tile_bar(&bar);
-    __syncthreads();
-    stage_tile<IO, BWD, LT, T>(smem, &bar, &qmap, &dmap, geo, c, g, ctl, tile);
-    wait_tile(&bar, ctl, tile);
-
-    const int cell0 = seg * N * LT + lane;
-    float4 loc = q_ident(), W = q_zero();
-#pragma unroll
-    for (int i = 0; i < N; ++i) {
-        loc = q_mul(IO::get(Qt[cell0 + i * LT]), loc);
-        if (BWD) W = q_add(W, q_mul_cl(loc, IO::get(Dt[cell0 + i * LT])));
-    }
-    s_a[seg][lane] = loc;
-    if (BWD) s_w[seg][lane] = W;
-    __syncthreads();
-    if (seg == 0) {
-        float4 L = q_ident();
-#pragma unroll
-        for (int k = 0; k < NSEG; ++k) L = q_mul(s_a[k][lane], L);
-        const long long o = static_cast<long long>(c) * geo.NL + static_cast<long long>(g) * LT + lane;
-        aggL[o] = L;
-        if (BWD) {
-            float4 V = q_zero();
-#pragma unroll
-            for (int k = NSEG - 1; k >= 0; --k) V = q_add(s_w[k][lane], q_mul_cl(s_a[k][lane], V));
-            aggW[o] = V;
-        }
-    }
-}
-
-// ---------------------------------------------------------------------------
-// Carry kernel: per padded lane, chunk aggregates -> carries.  Block = LB
-// lanes x RT = 256/LB chunk ranges; thread (r, l) folds its range, the ranges
-// are combined through shared memory, then each thread writes the carries of
-// its range.  carF[c] = cum[t0-1]; carH[c] = H entering chunk c from the
-// right (H_{c+1}); d_init = H_0.
-// ---------------------------------------------------------------------------
-template <typename IO, bool BWD, int LB>
-__global__ void __launch_bounds__(NTHREADS)
-    quat_carry_kernel(const float4 *__restrict__ aggL, const float4 *__restrict__ aggW,
-                      const typename IO::elem *__restrict__ init, float4 *__restrict__ carF,
-                      float4 *__restrict__ carH, typename IO::elem *__restrict__ d_init, const Geometry geo, int LT) {
-    constexpr int RT = NTHREADS / LB;
-    constexpr int U = 8;   // aggregates loaded per batch (independent loads)
-    __shared__ float4 xa[RT][LB];
-    __shared__ float4 xm[BWD ? RT : 1][LB];
-    __shared__ float4 xv[BWD ? RT : 1][LB];
-    const int l = threadIdx.x % LB, r = threadIdx.x / LB;
-    const int gl = blockIdx.x * LB + l;   // padded lane
-    const bool in_range = gl < geo.NL;
-    const int g = gl / LT, lig = gl - g * LT;
-    const int b = g / geo.NGb, hj = (g - b * geo.NGb) * LT + lig;
-    const bool lane_ok = in_range && hj < geo.HJ;
-    const int C = geo.C;
-    const long long NL = geo.NL;
-    const int R = (C + RT - 1) / RT;
-    const int c_lo = min(C, r * R), c_hi = min(C, c_lo + R);
-    auto at = [&](int c) { return static_cast<long long>(c) * NL + gl; };
-
-    float4 P = q_ident(), M = q_ident(), V = q_zero();
-    if (in_range) {
-        for (int c0 = c_lo; c0 < c_hi; c0 += U) {
-            float4 Lb[U];
-#pragma unroll
-            for (int u = 0; u < U; ++u) Lb[u] = (c0 + u < c_hi) ? __ldg(aggL + at(c0 + u)) : q_ident();
-#pragma unroll
-            for (int u = 0; u < U; ++u) P = q_mul(Lb[u], P);
-        }
-        if (BWD) {
-            for (int c1 = c_hi; c1 > c_lo; c1 -= U) {
-                float4 Lb[U], Wb[U];
-#pragma unroll
-                for (int u = 0; u < U; ++u) {
-                    const int cc = c1 - 1 - u;
-                    const bool in = cc >= c_lo;
-                    Lb[u] = in ? __ldg(aggL + at(cc)) : q_ident();
-                    Wb[u] = in ? __ldg(aggW + at(cc)) : q_zero();
-                }
-#pragma unroll
-                for (int u = 0; u < U; ++u) {
-                    V = q_add(Wb[u], q_mul_cl(Lb[u], V));
-                    M = q_mul_cl(Lb[u], M);
-                }
-            }
-        }
-    }
-    xa[r][l] = P;
-    if (BWD) {
-        xm[r][l] = M;
-        xv[r][l] = V;
-    }
-    __syncthreads();
-    if (!in_range) return;
-    float4 carry = lane_ok ? IO::get(init[static_cast<long long>(b) * geo.HJ + hj]) : q_ident();
-    for (int k = 0; k < r; ++k) carry = q_mul(xa[k][l], carry);
-    float4 h = q_zero();
-    if (BWD) {
-        for (int k = RT - 1; k > r; --k) h = q_add(xv[k][l], q_mul(xm[k][l], h));
-        if (r == 0 && lane_ok) d_init[static_cast<long long>(b) * geo.HJ + hj] = IO::put(q_add(V, q_mul(M, h)));
-    }
-    for (int c0 = c_lo; c0 < c_hi; c0 += U) {
-        float4 Lb[U];
-#pragma unroll
-        for (int u = 0; u < U; ++u) Lb[u] = (c0 + u < c_hi) ? __ldg(aggL + at(c0 + u)) : q_ident();
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            if (c0 + u < c_hi) carF[at(c0 + u)] = carry;
-            carry = q_mul(Lb[u], carry);
-        }
-    }
-    if (BWD) {
-        for (int c1 = c_hi; c1 > c_lo; c1 -= U) {
-            float4 Lb[U], Wb[U];
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int cc = c1 - 1 - u;
-                const bool in = cc >= c_lo;
-                Lb[u] = in ? __ldg(aggL + at(cc)) : q_ident();
-                Wb[u] = in ? __ldg(aggW + at(cc)) : q_zero();
-            }
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int cc = c1 - 1 - u;
-                if (cc >= c_lo) carH[at(cc)] = h;
-                h = q_add(Wb[u], q_mul_cl(Lb[u], h));
-            }
-        }
-    }
-}
-
-// ---------------------------------------------------------------------------
-// Carry kernel for many chunks per lane: one block per padded lane, thread r
-// folds the chunk range r (about C / 256 chunks); the 256 range products (and
-// affine range maps) are combined by a log-depth scan in shared memory, then
-// every thread writes the carries of its range.  Same outputs as
-// quat_carry_kernel.
-// ---------------------------------------------------------------------------
-template <typename IO, bool BWD>
-__global__ void __launch_bounds__(NTHREADS)
-    quat_carry_scan_kernel(const float4 *__restrict__ aggL, const float4 *__restrict__ aggW,
-                           const typename IO::elem *__restrict__ init, float4 *__restrict__ carF,
-                           float4 *__restrict__ carH, typename IO::elem *__restrict__ d_init, const Geometry geo,
-                           int LT) {
-    constexpr int U = 8;   // aggregates loaded per batch (independent loads)
-    __shared__ float4 sP[NTHREADS];
-    __shared__ float4 sM[BWD ? NTHREADS : 1];
-    __shared__ float4 sV[BWD ? NTHREADS : 1];
-    const int gl = static_cast<int>(blockIdx.x);   // padded lane
-    const int r = threadIdx.x;
-    const int g = gl / LT, lig = gl - g * LT;
-    const int b = g / geo.NGb, hj = (g - b * geo.NGb) * LT + lig;
-    const bool lane_ok = hj < geo.HJ;
-    const int C = geo.C;
-    const long long NL = geo.NL;
-    const int R = (C + NTHREADS - 1) / NTHREADS;
-    const int c_lo = min(C, r * R), c_hi = min(C, c_lo + R);
-    auto at = [&](int c) { return static_cast<long long>(c) * NL + gl; };
-
-    // This range as a product P and (backward) as the map h -> V + M (x) h.
-    float4 P = q_ident(), M = q_ident(), V = q_zero();
-    for (int c0 = c_lo; c0 < c_hi; c0 += U) {
-        float4 Lb[U];
-#pragma unroll
-        for (int u = 0; u < U; ++u) Lb[u] = (c0 + u < c_hi) ? __ldg(aggL + at(c0 + u)) : q_ident();
-#pragma unroll
-        for (int u = 0; u < U; ++u) P = q_mul(Lb[u], P);
-    }
-    if (BWD) {
-        for (int c1 = c_hi; c1 > c_lo; c1 -= U) {
-            float4 Lb[U], Wb[U];
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int cc = c1 - 1 - u;
-                const bool in = cc >= c_lo;
-                Lb[u] = in ? __ldg(aggL + at(cc)) : q_ident();
-                Wb[u] = in ? __ldg(aggW + at(cc)) : q_zero();
-            }
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                V = q_add(Wb[u], q_mul_cl(Lb[u], V));
-                M = q_mul_cl(Lb[u], M);
-            }
-        }
-    }
-    // Inclusive scans over the ranges: products of ranges 0..r (later on the
-    // left) and maps of ranges r..255 (range r applied last).
-    sP[r] = P;
-    if (BWD) {
-        sM[r] = M;
-        sV[r] = V;
-    }
-    __syncthreads();
-    for (int d = 1; d < NTHREADS; d <<= 1) {
-        const float4 oP = r >= d ? sP[r - d] : q_ident();
-        float4 oM = q_ident(), oV = q_zero();
-        if (BWD && r + d < NTHREADS) {
-            oM = sM[r + d];
-            oV = sV[r + d];
-        }
-        __syncthreads();
-        if (r >= d) {
-            P = q_mul(P, oP);
-            sP[r] = P;
-        }
-        if (BWD && r + d < NTHREADS) {
-            V = q_add(V, q_mul(M, oV));
-            M = q_mul(M, oM);
-            sM[r] = M;
-            sV[r] = V;
-        }
-        __syncthreads();
-    }
-    const float4 init4 = lane_ok ? IO::get(init[static_cast<long long>(b) * geo.HJ + hj]) : q_ident();
-    float4 carry = r > 0 ? q_mul(sP[r - 1], init4) : init4;   // cum just before range r
-    float4 h = q_zero();                                       // H entering range r from the right
-    if (BWD) {
-        if (r + 1 < NTHREADS) h = sV[r + 1];
-        if (r == 0 && lane_ok) d_init[static_cast<long long>(b) * geo.HJ + hj] = IO::put(sV[0]);
-    }
-    for (int c0 = c_lo; c0 < c_hi; c0 += U) {
-        float4 Lb[U];
-#pragma unroll
-        for (int u = 0; u < U; ++u) Lb[u] = (c0 + u < c_hi) ? __ldg(aggL + at(c0 + u)) : q_ident();
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            if (c0 + u < c_hi) carF[at(c0 + u)] = carry;
-            carry = q_mul(Lb[u], carry);
-        }
-    }
-    if (BWD) {
-        for (int c1 = c_hi; c1 > c_lo; c1 -= U) {
-            float4 Lb[U], Wb[U];
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int cc = c1 - 1 - u;
-                const bool in = cc >= c_lo;
-                Lb[u] = in ? __ldg(aggL + at(cc)) : q_ident();
-                Wb[u] = in ? __ldg(aggW + at(cc)) : q_zero();
-            }
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int cc = c1 - 1 - u;
-                if (cc >= c_lo) carH[at(cc)] = h;
-                h = q_add(Wb[u], q_mul_cl(Lb[u], h));
-            }
-        }
-    }
-}
-
-// ---------------------------------------------------------------------------
-// Apply kernel: one tile per CTA, in reverse tile order.  Forward:
-// cum[t] = local_t (x) F_c.  Backward: reverse pass G = d_cum + H,
-// d_q = G (x) conj(cum[t-1]), H = conj(q_t) (x) G.
-// ---------------------------------------------------------------------------
-template <typename IO, bool BWD, int LT, int N>
-__global__ void __launch_bounds__(NTHREADS)
-    quat_apply_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap dmap,
-                      const float4 *__restrict__ carF, const float4 *__restrict__ carH,
-                      typename IO::elem *__restrict__ out,
-                      const Geometry geo, const Control ctl) {
-    constexpr int NSEG = NTHREADS / LT;
-    constexpr int T = NSEG * N;
-    extern __shared__ unsigned char smem_raw[];
-    unsigned char *smem = align128(smem_raw);
-    using E = typename IO::elem;
-    const E *Qt = reinterpret_cast<const E *>(smem);
-    const E *Dt = Qt + T * LT;
-    __shared__ __align__(8) uint64_t bar;
-    __shared__ float4 s_a[NSEG][LT];
-    __shared__ float4 s_w[BWD ? NSEG : 1][LT];
-    __shared__ float4 s_cf[LT];
-    __shared__ float4 s_ch[BWD ? LT : 1];
-
-    const int tile = static_cast<int>(gridDim.x) - 1 - static_cast<int>(blockIdx.x);   // reverse order
-    const int c = tile / geo.NG, g = tile - c * geo.NG;
-    const int lane = threadIdx.x % LT, seg = threadIdx.x / LT;
-    init_tile_bar(&bar);
-    __syncthreads();
-    stage_tile<IO, BWD, LT, T>(smem, &bar, &qmap, &dmap, geo, c, g, ctl, -1);
-    const long long o = static_cast<long long>(c) * geo.NL + static_cast<long long>(g) * LT + lane;
-    if (seg == 0) {   // carries of this chunk (their loads overlap the tile load)
-        s_cf[lane] = __ldg(carF + o);
-        if (BWD) s_ch[lane] = __ldg(carH + o);
-    }
-    wait_tile(&bar, ctl, tile);
-
-    const int b = g / geo.NGb, hj = (g - b * geo.NGb) * LT + lane;
-    const bool lane_ok = hj < geo.HJ;
-    const long long t0 = static_cast<long long>(c) * T + seg * N;
-    const int cell0 = seg * N * LT + lane;
-    E *dst = out + (static_cast<long long>(b) * geo.S + t0) * geo.HJ + hj;
-    if (!BWD) {
-        float4 x[N];
-        float4 loc = q_ident();
-#pragma unroll
-        for (int i = 0; i < N; ++i) {
-            loc = q_mul(IO::get(Qt[cell0 + i * LT]), loc);
-            x[i] = loc;
-        }
-        s_a[seg][lane] = loc;
-        __syncthreads();
-        float4 X = s_cf[lane];   // cum just before this segment
-        for (int k = 0; k < seg; ++k) X = q_mul(s_a[k][lane], X);
-        if (lane_ok) {
-#pragma unroll
-            for (int i = 0; i < N; ++i)
-                if (t0 + i < geo.S) __stcs(dst + static_cast<long long>(i) * geo.HJ, IO::put(q_mul(x[i], X)));
-        }
-    } else {
-        float4 lp[N];
-        float4 loc = q_ident(), W = q_zero();
-#pragma unroll
-        for (int i = 0; i < N; ++i) {
-            lp[i] = loc;
-            loc = q_mul(IO::get(Qt[cell0 + i * LT]), loc);
-            W = q_add(W, q_mul_cl(loc, IO::get(Dt[cell0 + i * LT])));
-        }
-        s_a[seg][lane] = loc;
-        s_w[seg][lane] = W;
-        __syncthreads();
-        float4 X = s_cf[lane];
-        for (int k = 0; k < seg; ++k) X = q_mul(s_a[k][lane], X);
-        float4 Hn = s_ch[lane];
-        for (int k = NSEG - 1; k > seg; --k) Hn = q_add(s_w[k][lane], q_mul_cl(s_a[k][lane], Hn));
-#pragma unroll
-        for (int i = N - 1; i >= 0; --i) {
-            const float4 G = q_add(IO::get(Dt[cell0 + i * LT]), Hn);
-            if (lane_ok && t0 + i < geo.S)
-                __stcs(dst + static_cast<long long>(i) * geo.HJ, IO::put(q_mul_cr(G, q_mul(lp[i], X))));
-            Hn = q_mul_cl(IO::get(Qt[cell0 + i * LT]), G);
-        }
-    }
-}
-
-// ---------------------------------------------------------------------------
-// Chained-scan forward (single pass, one tile per CTA).  Tiles are numbered
-// chunk-major (tile = c * NG + g) and CTAs start in that order, so a tile
-// waits only on tiles that started before it.  Per lane, a tile publishes its
-// chunk product L_c and, once known, its inclusive value cum at its last step
-// (`incl`), each followed by that lane's status word, written with release
-// semantics by the thread that wrote the value; readers acquire the status
-// word before reading the value.  A tile's carry is the product of the
-// aggregates of the chunks before it, back to the nearest published
-// inclusive value (decoupled look-back); the NSEG segment threads of a lane
-// read NSEG predecessors per round.  Status words carry the launch's epoch,
-// so nothing has to be cleared between launches.  Every wait is bounded; a
-// tile whose wait ran out still publishes (NaN), so no successor waits out
-// its own limit because of it.
-// ---------------------------------------------------------------------------
-constexpr uint32_t CH_AGG = 1, CH_INCL = 2;   // status word: (epoch << 2) | state
-
-template <typename IO, int LT, int N>
-__global__ void __launch_bounds__(NTHREADS)
-    quat_chain_fwd_kernel(const __grid_constant__ CUtensorMap qmap, const typename IO::elem *__restrict__ init,
-                          typename IO::elem *__restrict__ out, uint32_t *__restrict__ flags,
-                          float4 *__restrict__ agg, float4 *__restrict__ incl, const Geometry geo,
-                          const Control ctl, uint32_t epoch) {
-    constexpr int NSEG = NTHREADS / LT;
-    constexpr int T = NSEG * N;
-    using E = typename IO::elem;
-    extern __shared__ unsigned char smem_raw[];
-    unsigned char *smem = align128(smem_raw);
-    const E *Qt = reinterpret_cast<const E *>(smem);
-    __shared__ __align__(8) uint64_t bar;
-    __shared__ float4 s_a[NSEG][LT];
-    __shared__ float4 s_lb[NSEG][LT];       // one look-back round: a predecessor per segment
-    __shared__ uint32_t s_st[NSEG][LT];
-    __shared__ float4 s_x[LT];              // carry into the tile
-
-    const int tile = static_cast<int>(blockIdx.x);
-    const int c = tile / geo.NG, g = tile - c * geo.NG;
-    const int lane = threadIdx.x % LT, seg = threadIdx.x / LT;
-    const int b = g / geo.NGb, hj = (g - b * geo.NGb) * LT + lane;
-    const bool lane_ok = hj < geo.HJ;
-    init_tile_bar(&bar);
-    __syncthreads();
-    stage_tile<IO, false, LT, T>(smem, &bar, &qmap, &qmap, geo, c, g, ctl, tile);
-    float4 init4 = q_ident();
-    if (c == 0 && seg == 0 && lane_ok) init4 = IO::get(init[static_cast<long long>(b) * geo.HJ + hj]);
-    wait_tile(&bar, ctl, tile);
-
-    const int cell0 = seg * N * LT + lane;
-    float4 x[N];
-    float4 loc = q_ident();
-#pragma unroll
-    for (int k = 0; k < N; ++k) {
-        loc = q_mul(IO::get(Qt[cell0 + k * LT]), loc);
-        x[k] = loc;
-    }
-    s_a[seg][lane] = loc;
-    __syncthreads();
-    const uint32_t tag = epoch << 2;
-    const long long me = static_cast<long long>(tile) * LT + lane;
-    float4 L = q_ident();
-    if (seg == 0) {
-#pragma unroll
-        for (int k = 0; k < NSEG; ++k) L = q_mul(s_a[k][lane], L);
-        if (c > 0) {   // the aggregate first: successors can use it before the carry is known
-            __stcg(agg + me, L);
-            st_release_u32(flags + me, tag | CH_AGG);
-        }
-    }
-    // Look-back: acc = L_{c-1} (x) L_{c-2} (x) ... (x) incl_p.  Per round the
-    // NSEG segment threads of a lane read NSEG * LB consecutive predecessors,
-    // LB each (segment k: chunks base - k*LB .. base - k*LB - LB + 1), fold
-    // them locally up to the first inclusive value, and segment 0 combines the
-    // NSEG partial products in order.
-    constexpr int LB = 4;
-    float4 acc = init4;   // chunk 0: the carry is init
-    bool done = c == 0;
-    if (c > 0) {
-        acc = q_ident();
-        for (int base = c - 1;; base -= NSEG * LB) {
-            float4 part = q_ident();
-            uint32_t pst = 0;   // CH_INCL once the fold reached an inclusive value
-#pragma unroll 1
-            for (int j = 0; j < LB && pst != CH_INCL; ++j) {
-                const int p = base - seg * LB - j;
-                if (p < 0) break;   // chunk 0 publishes an inclusive value, so this is never needed
-                const long long idx = (static_cast<long long>(p) * geo.NG + g) * LT + lane;
-                uint32_t f = ld_acquire_u32(flags + idx);
-                bool lost = false;
-                if ((f & ~3u) != tag) {
-                    const unsigned long long t0 = global_timer_ns();
-                    do {
-                        if (global_timer_ns() - t0 > ctl.timeout_ns) {
-                            record_error(ctl.hdr, tile);
-                            lost = true;
-                            break;
-                        }
-                        f = ld_acquire_u32(flags + idx);
-                    } while ((f & ~3u) != tag);
-                }
-                if (lost) {
-                    part = q_nan();
-                    pst = CH_INCL;
-                } else if ((f & 3u) == CH_INCL) {
-                    part = q_mul(part, __ldcg(incl + idx));
-                    pst = CH_INCL;
-                } else {
-                    part = q_mul(part, __ldcg(agg + idx));
-                }
-            }
-            s_lb[seg][lane] = part;
-            s_st[seg][lane] = pst;
-            __syncthreads();
-            if (seg == 0 && !done) {
-#pragma unroll 1
-                for (int k = 0; k < NSEG; ++k) {
-                    acc = q_mul(acc, s_lb[k][lane]);
-                    if (s_st[k][lane] == CH_INCL) {
-                        done = true;
-                        break;
-                    }
-                }
-            }
-            if (!__syncthreads_or(seg == 0 && !done)) break;
-        }
-    }
-    if (seg == 0) {
-        __stcg(incl + me, q_mul(L, acc));
-        st_release_u32(flags + me, tag | CH_INCL);
-        s_x[lane] = acc;
-    }
-    __syncthreads();
-    float4 X = s_x[lane];   // cum just before this segment
-#pragma unroll
-    for (int k = 0; k < NSEG - 1; ++k)
-        if (k < seg) X = q_mul(s_a[k][lane], X);
-    const long long t0 = static_cast<long long>(c) * T + seg * N;
-    E *dst = out + (static_cast<long long>(b) * geo.S + t0) * geo.HJ + hj;
-    if (lane_ok && t0 + N <= geo.S) {
-#pragma unroll
-        for (int k = 0; k < N; ++k) __stcs(dst + static_cast<long long>(k) * geo.HJ, IO::put(q_mul(x[k], X)));
-    } else if (lane_ok) {
-#pragma unroll
-        for (int k = 0; k < N; ++k)
-            if (t0 + k < geo.S) __stcs(dst + static_cast<long long>(k) * geo.HJ, IO::put(q_mul(x[k], X)));
-    }
-}
-
-// ---------------------------------------------------------------------------
-// Walk kernels.  One CTA walks one lane group (LT lanes of one batch entry)
-// along the whole sequence, chunk by chunk: chunk c = T steps x LT lanes is
-// staged by one TMA load per operand through an NST-deep ring, thread
-// (seg, lane) owns N consecutive steps of one lane (NSEG segments per chunk),
-// and the carry between chunks stays in the CTA.  Nothing waits on another
-// CTA.  One block barrier per chunk: what a chunk needs from the one before
-// it (the carry, and in the backward the right-hand cotangent) is published
-// one chunk ahead in double-buffered shared slots, and the segment aggregates
-// are double-buffered as well.
-//
-// Forward: one pass, cum[t] = local_t (x) F_c, 32 bytes per element.
-// Backward: a forward walk over q that stores the carries F_c (q loaded with
-// the L2 evict-last policy), then a reverse walk over q and d_cum
-// (evict-first) that folds the affine chunk maps H_c = W_c + conj(L_c) (x)
-// H_{c+1} and writes d_q.  The reverse walk starts with the chunks the
-// forward walk read last, so as much of q as L2 holds is read from L2 the
-// second time: 48 to 64 bytes of DRAM traffic per element.
-// ---------------------------------------------------------------------------
-
-// Bounded wait on one stage of a ring; false if the wait ran out (the error is
-// recorded by thread 0).
-__device__ __forceinline__ bool wait_stage(uint64_t *bar, uint32_t parity, const Control &ctl, int item) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const unsigned long long t0 = global_timer_ns();
-    while (!mbar_try_wait(bar, parity)) {
-        if (global_timer_ns() - t0 > ctl.timeout_ns) {
-            if (threadIdx.x == 0) record_error(ctl.hdr, item);
-            return false;
-        }
-    }
-    return true;
-}
-
-__device__ __forceinline__ int ld_volatile_int(const int *p) { return *reinterpret_cast<const volatile int *>(p); }
-
-// After a wait ran out, the ring's barriers are no longer in step with the
-// loads; the kernel stops issuing loads and, before it exits, gives the loads
-// it did issue a bounded time to land (so that none writes into the shared
-// memory of a later CTA).
-template <int NS>
-__device__ __forceinline__ void drain_ring(uint64_t *bars, const int *issued, const Control &ctl) {
-    if (threadIdx.x != 0) return;
-    for (int s = 0; s < NS; ++s) {
-        if (issued[s] == 0) continue;
-        const uint32_t parity = static_cast<uint32_t>(issued[s] - 1) & 1u;
-        const unsigned long long t0 = global_timer_ns();
-        while (!mbar_try_wait(&bars[s], parity) && global_timer_ns() - t0 <= ctl.timeout_ns) {
-        }
-    }
-}
-
-// `carries` (optional, may be null): [B, C, H*J] float4, the state entering
-// every chunk, carries[b, c] = cum[b, c*T - 1] (init for c = 0).
-template <typename IO, int LT, int NSEG, int N, int NST>
-__global__ void __launch_bounds__(LT *NSEG)
-    quat_walk_fwd_kernel(const __grid_constant__ CUtensorMap qmap, const typename IO::elem *__restrict__ init,
-                         typename IO::elem *__restrict__ out, float4 *__restrict__ carries, const Geometry geo,
-                         const Control ctl) {
-    using E = typename IO::elem;
-    constexpr int T = NSEG * N;
-    constexpr uint32_t BYTES = T * LT * IO::bytes;
-    extern __shared__ unsigned char smem_raw[];
-    unsigned char *ring = align128(smem_raw);
-    __shared__ __align__(8) uint64_t full[NST];
-    __shared__ int issued[NST];   // loads issued per stage (thread 0)
-    __shared__ int s_broken;
-    __shared__ float4 s_a[2][NSEG][LT];   // segment products of chunk i (slot i & 1)
-    __shared__ float4 s_x[2][LT];         // carry into chunk i (slot i & 1)
-
-    const int g = static_cast<int>(blockIdx.x);
-    const int b = g / geo.NGb, x0 = (g - b * geo.NGb) * LT * 4;
-    const int lane = threadIdx.x % LT, seg = threadIdx.x / LT;
-    const int hj = (g - b * geo.NGb) * LT + lane;
-    const bool lane_ok = hj < geo.HJ;
-    const int C = geo.C;
-
-    float4 R = q_ident();   // carry into the next chunk (segment-0 threads)
-    if (seg == 0 && lane_ok) R = IO::get(init[static_cast<long long>(b) * geo.HJ + hj]);
-    if (seg == 0) s_x[0][lane] = R;
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < NST; ++s) {
-            mbar_init(&full[s], 1);
-            issued[s] = 0;
-        }
-        fence_mbar_init();
-        s_broken = 0;
-    }
-    __syncthreads();
-    auto issue = [&](int c) {   // thread 0: chunk c into stage c % NST
-        const int st = c % NST;
-        ++issued[st];
-        mbar_arrive_expect_tx(&full[st], BYTES + (c * geo.NG + g == ctl.stall_tile ? 16u : 0u));
-        tma_load_3d(ring + st * BYTES, &qmap, x0, c * T, b, &full[st]);
-    };
-    if (threadIdx.x == 0)
-        for (int c = 0; c < NST && c < C; ++c) issue(c);
-
-    const long long row0 = static_cast<long long>(b) * geo.S;
-    for (int c = 0; c < C; ++c) {
-        const int st = c % NST, sl = c & 1;
-        const E *Qt = reinterpret_cast<const E *>(ring + st * BYTES);
-        if (!ld_volatile_int(&s_broken) && !wait_stage(&full[st], (c / NST) & 1, ctl, c * geo.NG + g))
-            s_broken = 1;
-        float4 x[N];
-        float4 loc = q_ident();
-#pragma unroll
-        for (int k = 0; k < N; ++k) {
-            loc = q_mul(IO::get(Qt[(seg * N + k) * LT + lane]), loc);
-            x[k] = loc;
-        }
-        s_a[sl][seg][lane] = loc;
-        __syncthreads();
-        if (threadIdx.x == 0 && !s_broken && c + NST < C) issue(c + NST);
-        float4 P = q_ident();   // product of the earlier segments of the chunk
-#pragma unroll
-        for (int k = 0; k < NSEG - 1; ++k)
-            if (k < seg) P = q_mul(s_a[sl][k][lane], P);
-        const float4 Y = q_mul(P, s_x[sl][lane]);
-        if (seg == 0) {
-            if (carries != nullptr && lane_ok)
-                carries[(static_cast<long long>(b) * C + c) * geo.HJ + hj] = R;   // state entering chunk c
-            float4 L = q_ident();
-#pragma unroll
-            for (int k = 0; k < NSEG; ++k) L = q_mul(s_a[sl][k][lane], L);
-            R = q_mul(L, R);
-            s_x[sl ^ 1][lane] = R;
-        }
-        const long long t0 = static_cast<long long>(c) * T + seg * N;
-        E *dst = out + (row0 + t0) * geo.HJ + hj;
-        if (lane_ok && t0 + N <= geo.S) {
-#pragma unroll
-            for (int k = 0; k < N; ++k) __stcs(dst + static_cast<long long>(k) * geo.HJ, IO::put(q_mul(x[k], Y)));
-        } else if (lane_ok) {
-#pragma unroll
-            for (int k = 0; k < N; ++k)
-                if (t0 + k < geo.S) __stcs(dst + static_cast<long long>(k) * geo.HJ, IO::put(q_mul(x[k], Y)));
-        }
-    }
-    if (s_broken) drain_ring<NST>(full, issued, ctl);
-}
-
-// SELF = false: after a chunk's segment aggregates are in shared memory, the
-// segment-0 thread of each lane folds them once (two chains of NSEG products)
-// and a second block barrier hands each segment its carry and cotangent.
-// SELF = true: every thread folds its own carry (through the earlier
-// segments) and cotangent (through the later ones), about NSEG-1 products,
-// and the chunk needs no second barrier; segment 0 publishes the cotangent
-// entering the next chunk one chunk ahead.
-//
-// GIVEN = true: the chunk carries come from the caller, `given` = [B, C, H*J]
-// float4 with given[b, c] = cum[b, c*T - 1] (what the forward walk writes as
-// `carries`); the forward walk is skipped and `init` and `carF` are unused.
-template <typename IO, int LT, int NSEG, int N, int NSTF, int NSTB, bool SELF, bool GIVEN>
-__global__ void __launch_bounds__(LT *NSEG)
-    quat_walk_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap dmap,
-                         const typename IO::elem *__restrict__ init, float4 *__restrict__ carF,
-                         const float4 *__restrict__ given, typename IO::elem *__restrict__ d_q,
-                         typename IO::elem *__restrict__ d_init, const Geometry geo, const Control ctl) {
-    using E = typename IO::elem;
-    constexpr int T = NSEG * N;
-    constexpr uint32_t BQ = T * LT * IO::bytes;   // one operand of one chunk
-    extern __shared__ unsigned char smem_raw[];
-    unsigned char *ring = align128(smem_raw);
-    __shared__ __align__(8) uint64_t fullF[NSTF];
-    __shared__ __align__(8) uint64_t fullB[NSTB];
-    __shared__ int issuedF[NSTF], issuedB[NSTB];
-    __shared__ int s_broken;
-    __shared__ float4 s_a[2][NSEG][LT];             // segment products (slot: chunk parity)
-    __shared__ float4 s_w[SELF ? 2 : 1][NSEG][LT];  // segment weighted sums (reverse walk)
-    __shared__ float4 s_x[SELF ? 1 : NSEG][LT];     // cum just before each segment
-    __shared__ float4 s_h[SELF ? 2 : NSEG][LT];     // H entering each segment / the next chunk
-
-    const int g = static_cast<int>(blockIdx.x);
-    const int b = g / geo.NGb, x0 = (g - b * geo.NGb) * LT * 4;
-    const int lane = threadIdx.x % LT, seg = threadIdx.x / LT;
-    const int hj = (g - b * geo.NGb) * LT + lane;
-    const bool lane_ok = hj < geo.HJ;
-    const int C = geo.C;
-    const long long NL = geo.NL;
-    const long long col = static_cast<long long>(g) * LT + lane;   // padded lane of this thread
-
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < NSTF; ++s) {
-            mbar_init(&fullF[s], 1);
-            issuedF[s] = 0;
-        }
-        for (int s = 0; s < NSTB; ++s) {
-            mbar_init(&fullB[s], 1);
-            issuedB[s] = 0;
-        }
-        fence_mbar_init();
-        s_broken = 0;
-    }
-    __syncthreads();
-    const uint64_t drop = l2_policy_evict_first();
-
-    if constexpr (!GIVEN) {
-        // ---- forward walk over q: carries F_c --------------------------------
-        const uint64_t keep = l2_policy_evict_last();
-        auto issueF = [&](int c) {
-            const int st = c % NSTF;
-            ++issuedF[st];
-            mbar_arrive_expect_tx(&fullF[st], BQ + (c * geo.NG + g == ctl.stall_tile ? 16u : 0u));
-            tma_load_3d_hint(ring + st * BQ, &qmap, x0, c * T, b, &fullF[st], keep);
-        };
-        if (threadIdx.x == 0)
-            for (int c = 0; c < NSTF && c < C; ++c) issueF(c);
-
-        float4 R = q_ident();
-        if (seg == 0 && lane_ok) R = IO::get(init[static_cast<long long>(b) * geo.HJ + hj]);
-        for (int c = 0; c < C; ++c) {
-            const int st = c % NSTF, sl = c & 1;
-            const E *Qt = reinterpret_cast<const E *>(ring + st * BQ);
-            if (!ld_volatile_int(&s_broken) && !wait_stage(&fullF[st], (c / NSTF) & 1, ctl, c * geo.NG + g))
-                s_broken = 1;
-            float4 loc = q_ident();
-#pragma unroll
-            for (int k = 0; k < N; ++k) loc = q_mul(IO::get(Qt[(seg * N + k) * LT + lane]), loc);
-            s_a[sl][seg][lane] = loc;
-            __syncthreads();
-            if (threadIdx.x == 0 && !s_broken && c + NSTF < C) issueF(c + NSTF);
-            if (seg == 0) {   // segment 0 carries the lane through the chunk
-                carF[static_cast<long long>(c) * NL + col] = R;
-#pragma unroll
-                for (int k = 0; k < NSEG; ++k) R = q_mul(s_a[sl][k][lane], R);
-            }
-        }
-    }
-    __syncthreads();   // every read of the forward ring is done before the reverse ring reuses it
-
-    // ---- reverse walk over q and d_cum: d_q, d_init --------------------------
-    auto issueB = [&](int j) {   // reverse step j covers chunk C-1-j
-        const int st = j % NSTB, c = C - 1 - j;
-        ++issuedB[st];
-        unsigned char *dst = ring + st * 2 * BQ;
-        mbar_arrive_expect_tx(&fullB[st], 2 * BQ);
-        tma_load_3d_hint(dst, &qmap, x0, c * T, b, &fullB[st], drop);
-        tma_load_3d_hint(dst + BQ, &dmap, x0, c * T, b, &fullB[st], drop);
-    };
-    if (threadIdx.x == 0 && !s_broken)
-        for (int j = 0; j < NSTB && j < C; ++j) issueB(j);
-
-    float4 Hc = q_zero();   // H entering the current chunk from the right (segment-0 threads)
-    // Carry into the chunk, written by this lane's segment-0 thread in the
-    // forward walk; loaded one chunk ahead.
-    auto carry_of = [&](int c) -> float4 {
-        if constexpr (GIVEN) return lane_ok ? given[(static_cast<long long>(b) * C + c) * geo.HJ + hj] : q_ident();
-        else return carF[static_cast<long long>(c) * NL + col];
-    };
-    float4 F_next = q_ident();
-    if (SELF || seg == 0) F_next = carry_of(C - 1);
-    if (SELF && seg == 0) s_h[0][lane] = Hc;
-    if (SELF) __syncthreads();
-    const long long row0 = static_cast<long long>(b) * geo.S;
-    for (int j = 0; j < C; ++j) {
-        const int c = C - 1 - j;
-        const int st = j % NSTB, sl = j & 1;
-        const float4 F = F_next;
-        if ((SELF || seg == 0) && c > 0) F_next = carry_of(c - 1);
-        const E *Qt = reinterpret_cast<const E *>(ring + st * 2 * BQ);
-        const E *Dt = Qt + T * LT;
-        if (!ld_volatile_int(&s_broken) && !wait_stage(&fullB[st], (j / NSTB) & 1, ctl, c * geo.NG + g))
-            s_broken = 1;
-        const int cell0 = seg * N * LT + lane;
-        float4 qv[N], dv[N], lp[N];
-        float4 loc = q_ident(), W = q_zero();
-#pragma unroll
-        for (int k = 0; k < N; ++k) {
-            qv[k] = IO::get(Qt[cell0 + k * LT]);
-            dv[k] = IO::get(Dt[cell0 + k * LT]);
-            lp[k] = loc;
-            loc = q_mul(qv[k], loc);
-            W = q_fma_cl(W, loc, dv[k]);
-        }
-        const int ws = SELF ? sl : 0;
-        s_a[sl][seg][lane] = loc;
-        s_w[ws][seg][lane] = W;
-        __syncthreads();
-        if (threadIdx.x == 0 && !s_broken && j + NSTB < C) issueB(j + NSTB);
-        float4 X, Hn;
-        if constexpr (SELF) {
-            X = F;   // through the earlier segments
-#pragma unroll
-            for (int k = 0; k < NSEG - 1; ++k)
-                if (k < seg) X = q_mul(s_a[sl][k][lane], X);
-            Hn = s_h[sl][lane];   // through the later segments
-#pragma unroll
-            for (int k = NSEG - 1; k > 0; --k)
-                if (k > seg) Hn = q_fma_cl(s_w[ws][k][lane], s_a[sl][k][lane], Hn);
-            if (seg == 0) {
-                Hc = q_fma_cl(s_w[ws][0][lane], s_a[sl][0][lane], Hn);
-                s_h[sl ^ 1][lane] = Hc;
-                if (c == 0 && lane_ok) d_init[static_cast<long long>(b) * geo.HJ + hj] = IO::put(Hc);
-            }
-        } else {
-            if (seg == 0) {
-                // The carry forward through the segments, and H backward
-                // through them: two independent chains of NSEG products.
-                float4 Xs = F, h = Hc;
-#pragma unroll
-                for (int k = 0; k < NSEG; ++k) {
-                    const int kr = NSEG - 1 - k;
-                    s_x[k][lane] = Xs;
-                    s_h[kr][lane] = h;
-                    Xs = q_mul(s_a[sl][k][lane], Xs);
-                    h = q_fma_cl(s_w[0][kr][lane], s_a[sl][kr][lane], h);
-                }
-                Hc = h;
-                if (c == 0 && lane_ok) d_init[static_cast<long long>(b) * geo.HJ + hj] = IO::put(Hc);
-            }
-            __syncthreads();
-            X = s_x[seg][lane];    // cum just before this segment
-            Hn = s_h[seg][lane];   // H entering this segment from the right
-        }
-        const long long t0 = static_cast<long long>(c) * T + seg * N;
-        E *dst = d_q + (row0 + t0) * geo.HJ + hj;
-        if (lane_ok && t0 + N <= geo.S) {
-#pragma unroll
-            for (int k = N - 1; k >= 0; --k) {
-                const float4 G = q_add(dv[k], Hn);
-                __stcs(dst + static_cast<long long>(k) * geo.HJ, IO::put(q_mul_cr(G, q_mul(lp[k], X))));
-                Hn = q_mul_cl(qv[k], G);
-            }
-        } else if (lane_ok) {
-#pragma unroll
-            for (int k = N - 1; k >= 0; --k) {
-                const float4 G = q_add(dv[k], Hn);
-                if (t0 + k < geo.S) __stcs(dst + static_cast<long long>(k) * geo.HJ, IO::put(q_mul_cr(G, q_mul(lp[k], X))));
-                Hn = q_mul_cl(qv[k], G);
-            }
-        }
-    }
-    if (s_broken) {
-        drain_ring<NSTF>(fullF, issuedF, ctl);
-        drain_ring<NSTB>(fullB, issuedB, ctl);
-    }
-}
-
-// Copies the chunk carries the carry kernel left in the workspace
-// (chunk-major, padded lanes) to the caller's [B, C, H*J] layout.
-__global__ void __launch_bounds__(NTHREADS)
-    quat_export_carries_kernel(const float4 *__restrict__ carF, float4 *__restrict__ carries, const Geometry geo,
-                               int LT, long long total) {
-    const long long i = static_cast<long long>(blockIdx.x) * NTHREADS + threadIdx.x;
-    if (i >= total) return;
-    const long long bc = i / geo.HJ;
-    const int hj = static_cast<int>(i - bc * geo.HJ);
-    const int b = static_cast<int>(bc / geo.C), c = static_cast<int>(bc - static_cast<long long>(b) * geo.C);
-    const long long g = static_cast<long long>(b) * geo.NGb + hj / LT;
-    carries[i] = carF[static_cast<long long>(c) * geo.NL + g * LT + hj % LT];
-}
-
-// Shared memory of a tile kernel (dynamic part).
-__host__ __device__ constexpr size_t tile_smem_bytes(bool bwd, int lt, int n, int eb = 16) {
-    return 128 + size_t(bwd ? 2 : 1) * (NTHREADS / lt) * n * lt * eb;
-}
-
-// Dynamic shared memory of the walk kernels: the forward ring, or the larger
-// of the backward's two rings (one operand per stage forward, two reverse).
-__host__ __device__ constexpr size_t walk_fwd_smem_bytes(int lt, int nseg, int n, int nst, int eb = 16) {
-    return 128 + size_t(nst) * nseg * n * lt * eb;
-}
-__host__ __device__ constexpr size_t walk_bwd_smem_bytes(int lt, int nseg, int n, int nstf, int nstb, int eb = 16) {
-    return 128 + size_t(nstf > 2 * nstb ? nstf : 2 * nstb) * nseg * n * lt * eb;
-}
-}  // namespace qs
+#include "quat_chain.cuh"
+#include "quat_tiles.cuh"
+#include "quat_walk.cuh"
 
 // ===========================================================================
 // Host side: argument checks, workspace, tensor maps, launches, C ABI.
