@@ -238,12 +238,16 @@ const char *quat_cumprod_strerror(int status);
  * wait runs out its limit and the call reports QS_ERR_TIMEOUT instead of
  * hanging.  quat_cumprod_debug_set_variant selects a compiled tile
  * configuration for each direction (index into the library's variant table,
- * -1 = default; QS_ERR_DIMS for an unknown index).  All three are
+ * -1 = default; QS_ERR_DIMS for an unknown index).
+ * quat_cumprod_debug_set_walk_cap(n) caps the CTAs of the backward walk
+ * kernels at n (n <= 0 restores each configuration's own cap); the lane
+ * groups are then walked in equal waves of at most n.  All four are
  * process-wide settings and return QS_OK unless stated.
  */
 int quat_cumprod_debug_set_timeout_ns(int64_t ns);
 int quat_cumprod_debug_stall_tile(int64_t tile);
 int quat_cumprod_debug_set_variant(int fwd_variant, int bwd_variant);
+int quat_cumprod_debug_set_walk_cap(int64_t ctas);
 /* The same for the bfloat16 calls (their own table of configurations). */
 int quat_cumprod_debug_set_variant_bf16(int fwd_variant, int bwd_variant);
 

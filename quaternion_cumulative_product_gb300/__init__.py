@@ -107,6 +107,8 @@ def load_library():
         lib.quat_cumprod_debug_stall_tile.restype = ctypes.c_int
         lib.quat_cumprod_debug_set_variant.argtypes = [ctypes.c_int, ctypes.c_int]
         lib.quat_cumprod_debug_set_variant.restype = ctypes.c_int
+        lib.quat_cumprod_debug_set_walk_cap.argtypes = [ctypes.c_int64]
+        lib.quat_cumprod_debug_set_walk_cap.restype = ctypes.c_int
         lib.quat_cumprod_debug_set_variant_bf16.argtypes = [ctypes.c_int, ctypes.c_int]
         lib.quat_cumprod_debug_set_variant_bf16.restype = ctypes.c_int
         _lib = lib

@@ -71,7 +71,7 @@ __global__ void __launch_bounds__(LT *NSEG)
     extern __shared__ unsigned char smem_raw[];
     unsigned char *ring = align128(smem_raw);
     __shared__ __align__(8) uint64_t full[NST];
-    __shared__ int issued[NST];   // loads issued per stage (thread 0)
+    __shared__ int issued[NST];   // loads issued per stage (by the producer thread)
     __shared__ int s_broken;
     __shared__ float4 s_a[2][NSEG][LT];   // segment products of chunk i (slot i & 1)
     __shared__ float4 s_x[2][LT];         // carry into chunk i (slot i & 1)
@@ -101,7 +101,13 @@ __global__ void __launch_bounds__(LT *NSEG)
         mbar_arrive_expect_tx(&full[st], BYTES + (c * geo.NG + g == ctl.stall_tile ? 16u : 0u));
         tma_load_3d(ring + st * BYTES, &qmap, x0, c * T, b, &full[st]);
     };
-    if (threadIdx.x == 0)
+    // The loads are issued by the first thread of the first warp without
+    // segment-0 threads (segment 0 carries the lane after the barrier; the
+    // low segments have the fewest products to fold): a stall on a full TMA
+    // queue then delays no thread on the chunk's critical path.
+    constexpr int kWarp1 = (LT + 31) / 32 * 32;
+    const bool producer = threadIdx.x == (kWarp1 < LT * NSEG ? kWarp1 : LT * NSEG - 1);
+    if (producer)
         for (int c = 0; c < NST && c < C; ++c) issue(c);
 
     const long long row0 = static_cast<long long>(b) * geo.S;
@@ -119,7 +125,7 @@ __global__ void __launch_bounds__(LT *NSEG)
         }
         s_a[sl][seg][lane] = loc;
         __syncthreads();
-        if (threadIdx.x == 0 && !s_broken && c + NST < C) issue(c + NST);
+        if (producer && !s_broken && c + NST < C) issue(c + NST);
         float4 P = q_ident();   // product of the earlier segments of the chunk
 #pragma unroll
         for (int k = 0; k < NSEG - 1; ++k)
@@ -159,6 +165,11 @@ __global__ void __launch_bounds__(LT *NSEG)
 // GIVEN = true: the chunk carries come from the caller, `given` = [B, C, H*J]
 // float4 with given[b, c] = cum[b, c*T - 1] (what the forward walk writes as
 // `carries`); the forward walk is skipped and `init` and `carF` are unused.
+//
+// A CTA walks lane groups blockIdx.x, blockIdx.x + gridDim.x, ... one after
+// the other (both walks of one group before the next group), so the grid
+// sets how many groups are in flight at once; the rings and shared slots
+// carry over from one group to the next.
 template <typename IO, int LT, int NSEG, int N, int NSTF, int NSTB, bool SELF, bool GIVEN>
 __global__ void __launch_bounds__(LT *NSEG)
     quat_walk_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap dmap,
@@ -170,6 +181,7 @@ __global__ void __launch_bounds__(LT *NSEG)
     constexpr uint32_t BQ = T * LT * IO::bytes;   // one operand of one chunk
     extern __shared__ unsigned char smem_raw[];
     unsigned char *ring = align128(smem_raw);
+    const int tid = static_cast<int>(threadIdx.x);
     __shared__ __align__(8) uint64_t fullF[NSTF];
     __shared__ __align__(8) uint64_t fullB[NSTB];
     __shared__ int issuedF[NSTF], issuedB[NSTB];
@@ -179,16 +191,11 @@ __global__ void __launch_bounds__(LT *NSEG)
     __shared__ float4 s_x[SELF ? 1 : NSEG][LT];     // cum just before each segment
     __shared__ float4 s_h[SELF ? 2 : NSEG][LT];     // H entering each segment / the next chunk
 
-    const int g = static_cast<int>(blockIdx.x);
-    const int b = g / geo.NGb, x0 = (g - b * geo.NGb) * LT * 4;
-    const int lane = threadIdx.x % LT, seg = threadIdx.x / LT;
-    const int hj = (g - b * geo.NGb) * LT + lane;
-    const bool lane_ok = hj < geo.HJ;
+    const int lane = tid % LT, seg = tid / LT;
     const int C = geo.C;
     const long long NL = geo.NL;
-    const long long col = static_cast<long long>(g) * LT + lane;   // padded lane of this thread
 
-    if (threadIdx.x == 0) {
+    if (tid == 0) {
         for (int s = 0; s < NSTF; ++s) {
             mbar_init(&fullF[s], 1);
             issuedF[s] = 0;
@@ -203,141 +210,173 @@ __global__ void __launch_bounds__(LT *NSEG)
     __syncthreads();
     const uint64_t drop = l2_policy_evict_first();
 
-    if constexpr (!GIVEN) {
-        // ---- forward walk over q: carries F_c --------------------------------
-        const uint64_t keep = l2_policy_evict_last();
-        auto issueF = [&](int c) {
-            const int st = c % NSTF;
-            ++issuedF[st];
-            mbar_arrive_expect_tx(&fullF[st], BQ + (c * geo.NG + g == ctl.stall_tile ? 16u : 0u));
-            tma_load_3d_hint(ring + st * BQ, &qmap, x0, c * T, b, &fullF[st], keep);
-        };
-        if (threadIdx.x == 0)
-            for (int c = 0; c < NSTF && c < C; ++c) issueF(c);
+    // Ring items (chunks) of the groups this CTA walked before the current
+    // one: stage = item % ring depth, phase parity = (item / depth) & 1.
+    int baseF = 0, baseB = 0;
+    const bool producer = tid == LT * NSEG - 1;   // issues every load (it never folds)
+    for (int g = static_cast<int>(blockIdx.x); g < geo.NG; g += static_cast<int>(gridDim.x)) {
+        const int b = g / geo.NGb, x0 = (g - b * geo.NGb) * LT * 4;
+        const int hj = (g - b * geo.NGb) * LT + lane;
+        const bool lane_ok = hj < geo.HJ;
+        const long long col = static_cast<long long>(g) * LT + lane;   // padded lane of this thread
 
-        float4 R = q_ident();
-        if (seg == 0 && lane_ok) R = IO::get(init[static_cast<long long>(b) * geo.HJ + hj]);
-        for (int c = 0; c < C; ++c) {
-            const int st = c % NSTF, sl = c & 1;
-            const E *Qt = reinterpret_cast<const E *>(ring + st * BQ);
-            if (!ld_volatile_int(&s_broken) && !wait_stage(&fullF[st], (c / NSTF) & 1, ctl, c * geo.NG + g))
-                s_broken = 1;
-            float4 loc = q_ident();
-#pragma unroll
-            for (int k = 0; k < N; ++k) loc = q_mul(IO::get(Qt[(seg * N + k) * LT + lane]), loc);
-            s_a[sl][seg][lane] = loc;
-            __syncthreads();
-            if (threadIdx.x == 0 && !s_broken && c + NSTF < C) issueF(c + NSTF);
-            if (seg == 0) {   // segment 0 carries the lane through the chunk
-                carF[static_cast<long long>(c) * NL + col] = R;
-#pragma unroll
-                for (int k = 0; k < NSEG; ++k) R = q_mul(s_a[sl][k][lane], R);
-            }
-        }
-    }
-    __syncthreads();   // every read of the forward ring is done before the reverse ring reuses it
+        if constexpr (!GIVEN) {
+            // ---- forward walk over q: carries F_c ----------------------------
+            const uint64_t keep = l2_policy_evict_last();
+            auto issueF = [&](int c) {
+                const int st = (baseF + c) % NSTF;
+                ++issuedF[st];
+                mbar_arrive_expect_tx(&fullF[st], BQ + (c * geo.NG + g == ctl.stall_tile ? 16u : 0u));
+                tma_load_3d_hint(ring + st * BQ, &qmap, x0, c * T, b, &fullF[st], keep);
+            };
+            if (producer && !s_broken)
+                for (int c = 0; c < NSTF && c < C; ++c) issueF(c);
 
-    // ---- reverse walk over q and d_cum: d_q, d_init --------------------------
-    auto issueB = [&](int j) {   // reverse step j covers chunk C-1-j
-        const int st = j % NSTB, c = C - 1 - j;
-        ++issuedB[st];
-        unsigned char *dst = ring + st * 2 * BQ;
-        mbar_arrive_expect_tx(&fullB[st], 2 * BQ);
-        tma_load_3d_hint(dst, &qmap, x0, c * T, b, &fullB[st], drop);
-        tma_load_3d_hint(dst + BQ, &dmap, x0, c * T, b, &fullB[st], drop);
-    };
-    if (threadIdx.x == 0 && !s_broken)
-        for (int j = 0; j < NSTB && j < C; ++j) issueB(j);
-
-    float4 Hc = q_zero();   // H entering the current chunk from the right (segment-0 threads)
-    // Carry into the chunk, written by this lane's segment-0 thread in the
-    // forward walk; loaded one chunk ahead.
-    auto carry_of = [&](int c) -> float4 {
-        if constexpr (GIVEN) return lane_ok ? given[(static_cast<long long>(b) * C + c) * geo.HJ + hj] : q_ident();
-        else return carF[static_cast<long long>(c) * NL + col];
-    };
-    float4 F_next = q_ident();
-    if (SELF || seg == 0) F_next = carry_of(C - 1);
-    if (SELF && seg == 0) s_h[0][lane] = Hc;
-    if (SELF) __syncthreads();
-    const long long row0 = static_cast<long long>(b) * geo.S;
-    for (int j = 0; j < C; ++j) {
-        const int c = C - 1 - j;
-        const int st = j % NSTB, sl = j & 1;
-        const float4 F = F_next;
-        if ((SELF || seg == 0) && c > 0) F_next = carry_of(c - 1);
-        const E *Qt = reinterpret_cast<const E *>(ring + st * 2 * BQ);
-        const E *Dt = Qt + T * LT;
-        if (!ld_volatile_int(&s_broken) && !wait_stage(&fullB[st], (j / NSTB) & 1, ctl, c * geo.NG + g))
-            s_broken = 1;
-        const int cell0 = seg * N * LT + lane;
-        float4 qv[N], dv[N], lp[N];
-        float4 loc = q_ident(), W = q_zero();
+            float4 R = q_ident();
+            if (seg == 0 && lane_ok) R = IO::get(init[static_cast<long long>(b) * geo.HJ + hj]);
+            for (int c = 0; c < C; ++c) {
+                const int it = baseF + c, st = it % NSTF, sl = c & 1;
+                const E *Qt = reinterpret_cast<const E *>(ring + st * BQ);
+                if (!ld_volatile_int(&s_broken) && !wait_stage(&fullF[st], (it / NSTF) & 1, ctl, c * geo.NG + g))
+                    s_broken = 1;
+                float4 loc = q_ident();
 #pragma unroll
-        for (int k = 0; k < N; ++k) {
-            qv[k] = IO::get(Qt[cell0 + k * LT]);
-            dv[k] = IO::get(Dt[cell0 + k * LT]);
-            lp[k] = loc;
-            loc = q_mul(qv[k], loc);
-            W = q_fma_cl(W, loc, dv[k]);
-        }
-        const int ws = SELF ? sl : 0;
-        s_a[sl][seg][lane] = loc;
-        s_w[ws][seg][lane] = W;
-        __syncthreads();
-        if (threadIdx.x == 0 && !s_broken && j + NSTB < C) issueB(j + NSTB);
-        float4 X, Hn;
-        if constexpr (SELF) {
-            X = F;   // through the earlier segments
+                for (int k = 0; k < N; ++k) loc = q_mul(IO::get(Qt[(seg * N + k) * LT + lane]), loc);
+                s_a[sl][seg][lane] = loc;
+                __syncthreads();
+                if (producer && !s_broken && c + NSTF < C) issueF(c + NSTF);
+                if (seg == 0) {   // segment 0 carries the lane through the chunk
+                    carF[static_cast<long long>(c) * NL + col] = R;
 #pragma unroll
-            for (int k = 0; k < NSEG - 1; ++k)
-                if (k < seg) X = q_mul(s_a[sl][k][lane], X);
-            Hn = s_h[sl][lane];   // through the later segments
-#pragma unroll
-            for (int k = NSEG - 1; k > 0; --k)
-                if (k > seg) Hn = q_fma_cl(s_w[ws][k][lane], s_a[sl][k][lane], Hn);
-            if (seg == 0) {
-                Hc = q_fma_cl(s_w[ws][0][lane], s_a[sl][0][lane], Hn);
-                s_h[sl ^ 1][lane] = Hc;
-                if (c == 0 && lane_ok) d_init[static_cast<long long>(b) * geo.HJ + hj] = IO::put(Hc);
-            }
-        } else {
-            if (seg == 0) {
-                // The carry forward through the segments, and H backward
-                // through them: two independent chains of NSEG products.
-                float4 Xs = F, h = Hc;
-#pragma unroll
-                for (int k = 0; k < NSEG; ++k) {
-                    const int kr = NSEG - 1 - k;
-                    s_x[k][lane] = Xs;
-                    s_h[kr][lane] = h;
-                    Xs = q_mul(s_a[sl][k][lane], Xs);
-                    h = q_fma_cl(s_w[0][kr][lane], s_a[sl][kr][lane], h);
+                    for (int k = 0; k < NSEG; ++k) R = q_mul(s_a[sl][k][lane], R);
                 }
-                Hc = h;
-                if (c == 0 && lane_ok) d_init[static_cast<long long>(b) * geo.HJ + hj] = IO::put(Hc);
             }
+            baseF += C;
+        }
+        __syncthreads();   // every read of the forward ring is done before the reverse ring reuses it
+
+        // ---- reverse walk over q and d_cum: d_q, d_init ----------------------
+        auto issueB = [&](int j) {   // reverse step j covers chunk C-1-j
+            const int st = (baseB + j) % NSTB, c = C - 1 - j;
+            ++issuedB[st];
+            unsigned char *dst = ring + st * 2 * BQ;
+            mbar_arrive_expect_tx(&fullB[st], 2 * BQ);
+            tma_load_3d_hint(dst, &qmap, x0, c * T, b, &fullB[st], drop);
+            tma_load_3d_hint(dst + BQ, &dmap, x0, c * T, b, &fullB[st], drop);
+        };
+        if (producer && !s_broken)
+            for (int j = 0; j < NSTB && j < C; ++j) issueB(j);
+
+        float4 Hc = q_zero();   // H entering the current chunk from the right (segment-1 threads; every thread if SELF)
+        // Carry into the chunk, written by this lane's segment-0 thread in the
+        // forward walk; loaded one chunk ahead.
+        auto carry_of = [&](int c) -> float4 {
+            if constexpr (GIVEN) return lane_ok ? given[(static_cast<long long>(b) * C + c) * geo.HJ + hj] : q_ident();
+            else return carF[static_cast<long long>(c) * NL + col];
+        };
+        float4 F_next = q_ident();
+        if (SELF || seg == 0) F_next = carry_of(C - 1);
+        if (SELF && seg == 0) s_h[0][lane] = Hc;
+        if (SELF) __syncthreads();
+        const long long row0 = static_cast<long long>(b) * geo.S;
+        for (int j = 0; j < C; ++j) {
+            const int c = C - 1 - j;
+            const int it = baseB + j, st = it % NSTB, sl = j & 1;
+            const float4 F = F_next;
+            if ((SELF || seg == 0) && c > 0) F_next = carry_of(c - 1);
+            const E *Qt = reinterpret_cast<const E *>(ring + st * 2 * BQ);
+            const E *Dt = Qt + T * LT;
+            if (!ld_volatile_int(&s_broken) && !wait_stage(&fullB[st], (it / NSTB) & 1, ctl, c * geo.NG + g))
+                s_broken = 1;
+            const int cell0 = seg * N * LT + lane;
+            float4 qv[N], dv[N], lp[N];
+            float4 loc = q_ident(), W = q_zero();
+#pragma unroll
+            for (int k = 0; k < N; ++k) {
+                qv[k] = IO::get(Qt[cell0 + k * LT]);
+                dv[k] = IO::get(Dt[cell0 + k * LT]);
+                lp[k] = loc;
+                loc = q_mul(qv[k], loc);
+                W = q_fma_cl(W, loc, dv[k]);
+            }
+            const int ws = SELF ? sl : 0;
+            s_a[sl][seg][lane] = loc;
+            s_w[ws][seg][lane] = W;
             __syncthreads();
-            X = s_x[seg][lane];    // cum just before this segment
-            Hn = s_h[seg][lane];   // H entering this segment from the right
-        }
-        const long long t0 = static_cast<long long>(c) * T + seg * N;
-        E *dst = d_q + (row0 + t0) * geo.HJ + hj;
-        if (lane_ok && t0 + N <= geo.S) {
+            if (producer && !s_broken && j + NSTB < C) issueB(j + NSTB);
+            float4 X, Hn;
+            if constexpr (SELF) {
+                X = F;   // through the earlier segments
 #pragma unroll
-            for (int k = N - 1; k >= 0; --k) {
-                const float4 G = q_add(dv[k], Hn);
-                __stcs(dst + static_cast<long long>(k) * geo.HJ, IO::put(q_mul_cr(G, q_mul(lp[k], X))));
-                Hn = q_mul_cl(qv[k], G);
-            }
-        } else if (lane_ok) {
+                for (int k = 0; k < NSEG - 1; ++k)
+                    if (k < seg) X = q_mul(s_a[sl][k][lane], X);
+                Hn = s_h[sl][lane];   // through the later segments
 #pragma unroll
-            for (int k = N - 1; k >= 0; --k) {
-                const float4 G = q_add(dv[k], Hn);
-                if (t0 + k < geo.S) __stcs(dst + static_cast<long long>(k) * geo.HJ, IO::put(q_mul_cr(G, q_mul(lp[k], X))));
-                Hn = q_mul_cl(qv[k], G);
+                for (int k = NSEG - 1; k > 0; --k)
+                    if (k > seg) Hn = q_fma_cl(s_w[ws][k][lane], s_a[sl][k][lane], Hn);
+                if (seg == 0) {
+                    Hc = q_fma_cl(s_w[ws][0][lane], s_a[sl][0][lane], Hn);
+                    s_h[sl ^ 1][lane] = Hc;
+                    if (c == 0 && lane_ok) d_init[static_cast<long long>(b) * geo.HJ + hj] = IO::put(Hc);
+                }
+            } else {
+                if (seg < 2) {
+                    // Two chains of NSEG steps y <- Q + A (x) y: the carry
+                    // forward through the segments on the segment-0 threads
+                    // (A = s_a[k], Q = 0) and H backward through them on the
+                    // segment-1 threads (A = conj(s_a[k]), Q = s_w[k], k
+                    // descending).  Written as one instruction stream, so the
+                    // two segments run side by side when they share a warp.
+                    const bool back = seg == 1;
+                    const float sg = back ? -1.f : 1.f;
+                    float4(*out)[LT] = back ? s_h : s_x;
+                    float4 y = back ? Hc : F;
+                    int idx = back ? NSEG - 1 : 0;
+                    const int step = back ? -1 : 1;
+#pragma unroll
+                    for (int k = 0; k < NSEG; ++k, idx += step) {
+                        out[idx][lane] = y;
+                        float4 A = s_a[sl][idx][lane];
+                        const float4 Wk = s_w[0][idx][lane];
+                        A.y *= sg;
+                        A.z *= sg;
+                        A.w *= sg;
+                        const float4 Q = make_float4(back ? Wk.x : 0.f, back ? Wk.y : 0.f, back ? Wk.z : 0.f,
+                                                     back ? Wk.w : 0.f);
+                        y = q_fma(Q, A, y);
+                    }
+                    if (back) {
+                        Hc = y;
+                        if (c == 0 && lane_ok) d_init[static_cast<long long>(b) * geo.HJ + hj] = IO::put(Hc);
+                    }
+                }
+                __syncthreads();
+                X = s_x[seg][lane];    // cum just before this segment
+                Hn = s_h[seg][lane];   // H entering this segment from the right
+            }
+            const long long t0 = static_cast<long long>(c) * T + seg * N;
+            E *dst = d_q + (row0 + t0) * geo.HJ + hj;
+            if (lane_ok && t0 + N <= geo.S) {
+#pragma unroll
+                for (int k = N - 1; k >= 0; --k) {
+                    const float4 G = q_add(dv[k], Hn);
+                    __stcs(dst + static_cast<long long>(k) * geo.HJ, IO::put(q_mul_cr(G, q_mul(lp[k], X))));
+                    Hn = q_mul_cl(qv[k], G);
+                }
+            } else if (lane_ok) {
+#pragma unroll
+                for (int k = N - 1; k >= 0; --k) {
+                    const float4 G = q_add(dv[k], Hn);
+                    if (t0 + k < geo.S)
+                        __stcs(dst + static_cast<long long>(k) * geo.HJ, IO::put(q_mul_cr(G, q_mul(lp[k], X))));
+                    Hn = q_mul_cl(qv[k], G);
+                }
             }
         }
+        baseB += C;
+        // Every read of this group's ring stages and shared slots is done
+        // before the next group's loads and writes reuse them.
+        __syncthreads();
     }
     if (s_broken) {
         drain_ring<NSTF>(fullF, issuedF, ctl);

@@ -126,6 +126,8 @@ def test_debug_hooks_return_ok(lib):
     assert lib.quat_cumprod_debug_set_variant(1, 2) == qs.QS_OK
     assert lib.quat_cumprod_debug_set_variant(-1, -1) == qs.QS_OK
     assert lib.quat_cumprod_debug_set_variant(99, 0) == qs.QS_ERR_DIMS
+    assert lib.quat_cumprod_debug_set_walk_cap(100) == qs.QS_OK
+    assert lib.quat_cumprod_debug_set_walk_cap(-1) == qs.QS_OK
 
 
 def test_workload_generator_is_seeded_and_shaped():

@@ -40,6 +40,7 @@ def reset_hooks():
     lib.quat_cumprod_debug_set_timeout_ns(0)
     lib.quat_cumprod_debug_stall_tile(-1)
     lib.quat_cumprod_debug_set_variant(-1, -1)
+    lib.quat_cumprod_debug_set_walk_cap(-1)
 
 
 def normwise(got, ref):
@@ -178,8 +179,9 @@ def test_empty_sizes(dev):
     del z
 
 
-# Variants 0-3: aggregate / carry / apply kernels; the rest: walk kernels.
-N_FWD_VARIANTS, N_BWD_VARIANTS = 9, 10
+# Variants 0-3: aggregate / carry / apply kernels; the rest: walk kernels
+# (backward 10: at most two CTAs per SM, more lane groups in waves).
+N_FWD_VARIANTS, N_BWD_VARIANTS = 9, 11
 
 
 @pytest.mark.parametrize("variant", range(max(N_FWD_VARIANTS, N_BWD_VARIANTS)))
@@ -207,6 +209,52 @@ def test_many_chunks_per_lane_carry_scan(dev, variant, dims):
     assert lib.quat_cumprod_debug_set_variant(variant, variant) == qs.QS_OK
     w = workloads.custom("chunks", *dims, q_kind="rotation", theta_max=0.3, seed=71 + variant)
     check_against_oracle(dev, *workloads.make_inputs(w))
+
+
+@pytest.mark.parametrize("cap", [1, 2, 3, 5])
+@pytest.mark.parametrize("variant", [4, 8, 10])   # fold by segments 0 and 1, every thread folds, capped
+def test_backward_walk_in_waves(dev, variant, cap):
+    """A CTA walks several lane groups one after another (grid capped below the group count).
+
+    3 x 48 lanes: 9 groups of 16 lanes; caps 1, 2, 3, 5 give one CTA
+    walking every group, and waves whose last one is ragged.  The backward from
+    saved carries (the reverse walk alone) runs under the same cap.
+    """
+    lib = qs.load_library()
+    assert lib.quat_cumprod_debug_set_variant(-1, variant) == qs.QS_OK
+    assert lib.quat_cumprod_debug_set_walk_cap(cap) == qs.QS_OK
+    w = workloads.custom("waves", 3, 333, 2, 24, q_kind="rotation", theta_max=0.6, seed=80 + cap)
+    q, init, d_cum = workloads.make_inputs(w)
+    check_against_oracle(dev, q, init, d_cum)
+    tq, ti, td = (torch.from_numpy(a).to(dev) for a in (q, init, d_cum))
+    _, carries = qs.quat_cumprod_fwd_carries(tq, ti)
+    d_q, d_init = qs.quat_cumprod_bwd_carries(tq, carries, td)
+    assert qs.quat_cumprod_status(device=dev) == qs.QS_OK
+    rq, ri = oracle.bwd(q, init, d_cum)
+    assert_parity(d_q.cpu().numpy(), rq, "d_q (from carries)")
+    assert_parity(d_init.cpu().numpy(), ri, "d_init (from carries)")
+
+
+def test_stall_in_a_later_wave_reports_timeout_then_recovers(dev):
+    """2 x 32 lanes = 4 groups of 16, cap 3: two CTAs walk two groups each.
+
+    The stalled tile is chunk 0 of group 2, the second group of CTA 0.
+    """
+    lib = qs.load_library()
+    assert lib.quat_cumprod_debug_set_variant(-1, 4) == qs.QS_OK
+    assert lib.quat_cumprod_debug_set_walk_cap(3) == qs.QS_OK
+    w = workloads.custom("stall_wave", 2, 600, 2, 16, seed=22)
+    q, init, d_cum = workloads.make_inputs(w)
+    tq, ti, td = (torch.from_numpy(a).to(dev) for a in (q, init, d_cum))
+    assert qs.quat_cumprod_status(device=dev) == qs.QS_OK
+    lib.quat_cumprod_debug_set_timeout_ns(50_000_000)    # 50 ms
+    lib.quat_cumprod_debug_stall_tile(2)                 # item c * NG + g = 0 * 4 + 2
+    qs.quat_cumprod_bwd(tq, ti, td)
+    assert qs.quat_cumprod_status(device=dev) == qs.QS_ERR_TIMEOUT
+    assert qs.quat_cumprod_status(device=dev) == qs.QS_OK
+    lib.quat_cumprod_debug_stall_tile(-1)
+    lib.quat_cumprod_debug_set_timeout_ns(0)
+    check_against_oracle(dev, q, init, d_cum)
 
 
 def test_unknown_variant_is_rejected(dev):
