@@ -14,7 +14,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(HERE)
 SOURCES = [os.path.join(HERE, "csrc", "quat_scan.cu")]
 HEADERS = [os.path.join(HERE, "csrc", f) for f in
-           ("quat_device.cuh", "quat_common.cuh", "quat_tiles.cuh", "quat_chain.cuh", "quat_walk.cuh")]
+           ("quat_device.cuh", "quat_common.cuh", "quat_tiles.cuh", "quat_chain.cuh", "quat_walk.cuh",
+            "quat_segwalk.cuh")]
 DEPS = SOURCES + HEADERS + [os.path.join(ROOT, "include", "quat_cumprod.h")]
 LIB = os.path.join(HERE, "libquatscan.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -180,8 +180,10 @@ def test_empty_sizes(dev):
 
 
 # Variants 0-3: aggregate / carry / apply kernels; the rest: walk kernels
-# (backward 10: at most two CTAs per SM, more lane groups in waves).
-N_FWD_VARIANTS, N_BWD_VARIANTS = 9, 11
+# (forward 8: chained scan; 9-13: segmented chained walk; backward 10: at most
+# two CTAs per SM, more lane groups in waves).
+N_FWD_VARIANTS, N_BWD_VARIANTS = 14, 11
+SEGWALK_FWD = [9, 10, 11, 12, 13]
 
 
 @pytest.mark.parametrize("variant", range(max(N_FWD_VARIANTS, N_BWD_VARIANTS)))
@@ -255,6 +257,40 @@ def test_stall_in_a_later_wave_reports_timeout_then_recovers(dev):
     lib.quat_cumprod_debug_stall_tile(-1)
     lib.quat_cumprod_debug_set_timeout_ns(0)
     check_against_oracle(dev, q, init, d_cum)
+
+
+@pytest.mark.parametrize("variant", SEGWALK_FWD)
+@pytest.mark.parametrize("dims", [(1, 20000, 1, 3), (2, 17000, 2, 5), (1, 131072 // 8, 2, 16)])
+def test_segmented_walk_long_sequences(dev, variant, dims):
+    """Many segments per lane (up to 40): the look-back chains over segments."""
+    lib = qs.load_library()
+    assert lib.quat_cumprod_debug_set_variant(variant, -1) == qs.QS_OK
+    w = workloads.custom("segwalk", *dims, q_kind="rotation", theta_max=0.3, seed=90 + variant)
+    q, init, d_cum = workloads.make_inputs(w)
+    tq, ti = (torch.from_numpy(a).to(dev) for a in (q, init))
+    for _ in range(2):   # a second launch reuses the status words and the ticket counter
+        cum = qs.quat_cumprod_fwd(tq, ti)
+        assert qs.quat_cumprod_status(device=dev) == qs.QS_OK
+        assert_parity(cum.cpu().numpy(), oracle.fwd(q, init), "cum")
+
+
+def test_segmented_walk_stall_reports_timeout_then_recovers(dev):
+    lib = qs.load_library()
+    assert lib.quat_cumprod_debug_set_variant(9, -1) == qs.QS_OK
+    w = workloads.custom("segstall", 2, 3000, 2, 16, seed=23)
+    q, init, d_cum = workloads.make_inputs(w)
+    tq, ti = (torch.from_numpy(a).to(dev) for a in (q, init))
+    assert qs.quat_cumprod_status(device=dev) == qs.QS_OK
+    lib.quat_cumprod_debug_set_timeout_ns(50_000_000)    # 50 ms
+    lib.quat_cumprod_debug_stall_tile(1)                 # chunk 0 of lane group 1
+    qs.quat_cumprod_fwd(tq, ti)
+    assert qs.quat_cumprod_status(device=dev) == qs.QS_ERR_TIMEOUT
+    assert qs.quat_cumprod_status(device=dev) == qs.QS_OK
+    lib.quat_cumprod_debug_stall_tile(-1)
+    lib.quat_cumprod_debug_set_timeout_ns(0)
+    cum = qs.quat_cumprod_fwd(tq, ti)
+    assert qs.quat_cumprod_status(device=dev) == qs.QS_OK
+    assert_parity(cum.cpu().numpy(), oracle.fwd(q, init), "cum")
 
 
 def test_unknown_variant_is_rejected(dev):
@@ -349,5 +385,9 @@ def test_plan_picks_the_design_by_lane_groups(dev, name, walk):
     w = workloads.WORKLOADS[name]
     for bwd in (False, True):
         variant, kernels = qs.quat_cumprod_plan(bwd, w.B, w.S, w.H, w.J, device=dev)
-        assert kernels == (1 if walk else 3), (name, bwd, variant, kernels)
+        # few lane groups: the segmented chained walk forward (one kernel),
+        # aggregate / carry / apply backward
+        assert kernels == (1 if walk or not bwd else 3), (name, bwd, variant, kernels)
+        if not walk and not bwd:
+            assert variant in SEGWALK_FWD
     assert qs.quat_cumprod_plan(True, 2, 0, 3, 4, device=dev) == (-1, 0)
