@@ -29,13 +29,17 @@
 //    The forward carry into chunk c is F_c = cum[t0-1] = L_{c-1} (x) F_{c-1},
 //    F_0 = init.
 //
-//  * Two designs; each call picks one from the number of lane groups.
+//  * Each call picks its design from the number of lane groups.
 //    Walk (one kernel): one CTA per lane group streams the whole sequence
 //    through a TMA ring and keeps the carries between chunks itself -- the
 //    forward reads q once and writes cum once; the backward walks forward
 //    over q for the carries, then backward over q and d_cum.
-//    Aggregate / carry / apply (three kernels), for too few lane groups to
-//    fill the GPU: every chunk is an independent tile --
+//    For too few lane groups to fill the GPU, the forward is the segmented
+//    chained walk (one kernel, quat_segwalk.cuh): persistent CTAs take
+//    (segment, lane group) units in order, walk a segment twice (the second
+//    time from L2) and chain the segments by decoupled look-back.  The
+//    backward, and the bf16 forward, use aggregate / carry / apply (three
+//    kernels): every chunk is an independent tile --
 //      aggregate: one tile per CTA -> L_c (and W_c);
 //      carry:     per lane, chunk aggregates -> carries F_c (and H_{c+1},
 //                 d_init): 32 lanes per block over 8 chunk ranges, or for
