@@ -19,6 +19,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import json
 import os
 import statistics
@@ -46,15 +47,29 @@ KERNEL_SOURCES = [os.path.join(ROOT, "quaternion_cumulative_product_gb300", "csr
                             "quat_chain.cuh", "quat_walk.cuh", "quat_segwalk.cuh")]
 
 
-def design_name(call: str, kernels: int) -> str:
-    return f"{call} ({'walk kernel' if kernels == 1 else 'aggregate + carry + apply kernels'})"
+# Forward configurations of the segmented chained walk in the library's table.
+SEGWALK_FWD_VARIANTS = (9, 10, 11, 12, 13)
+
+
+def design_name(call: str, kernels: int, variant: int = -1) -> str:
+    if kernels != 1:
+        return f"{call} (aggregate + carry + apply kernels)"
+    segmented = call == "quat_cumprod_fwd" and variant in SEGWALK_FWD_VARIANTS
+    return f"{call} ({'segmented chained walk kernel' if segmented else 'walk kernel'})"
+
+
+def _code_only(text: str) -> str:
+    """The source without comments and blank lines (a comment edit changes no kernel)."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    lines = (re.sub(r"//.*$", "", ln).rstrip() for ln in text.splitlines())
+    return "\n".join(ln for ln in lines if ln)
 
 
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
     for p in KERNEL_SOURCES:
-        with open(p, "rb") as f:
-            h.update(f.read())
+        with open(p, encoding="utf-8") as f:
+            h.update(_code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 
@@ -475,14 +490,14 @@ def run_ours(args, w, world, rank, local):
                           f"inputs larger than L2 ({tensor_bytes / 1e6:.0f} MB per tensor > 126 MB), no flush"),
                    "parallelism": ("one independent batch per GPU, no collective" if world > 1
                                    else "single GPU")},
-        "roofline": {"bound": "hbm", "kernel": design_name("quat_cumprod_bwd", bwd_kernels),
+        "roofline": {"bound": "hbm", "kernel": design_name("quat_cumprod_bwd", bwd_kernels, bwd_variant),
                      "variant": bwd_variant,
                      "achieved": bwd_gbs, "peak": peak,
                      "unit": "GB/s", "frac": bwd_gbs / peak, "peak_source": peak_src,
                      "traffic": recorded_traffic("quat_cumprod_bwd", w.name),
                      "algorithmic_bytes_per_launch": BWD_BYTES_PER_ELEMENT * E,
                      "avg_launch_ms": bwd_avg},
-        "roofline_fwd": {"bound": "hbm", "kernel": design_name("quat_cumprod_fwd", fwd_kernels),
+        "roofline_fwd": {"bound": "hbm", "kernel": design_name("quat_cumprod_fwd", fwd_kernels, fwd_variant),
                          "variant": fwd_variant,
                          "achieved": fwd_gbs, "peak": peak,
                          "unit": "GB/s", "frac": fwd_gbs / peak,

@@ -95,3 +95,9 @@ def test_reference_arm_runs_on_rank_zero_only(monkeypatch, capsys):
 def test_warmup_below_three_is_rejected():
     with pytest.raises(SystemExit):
         bench.main(["--warmup", "2"])
+
+
+def test_source_hash_ignores_comments_and_blank_lines():
+    import bench
+    assert bench._code_only("a = 1; // note\n\n/* block\n comment */ b = 2;\n") == "a = 1;\n b = 2;"
+    assert bench._code_only("x\n// only a comment\ny") == "x\ny"
