@@ -66,6 +66,7 @@
 #include "quat_cumprod.h"
 #include "quat_chain.cuh"
 #include "quat_segwalk.cuh"
+#include "quat_segwalk_ws.cuh"
 #include "quat_tiles.cuh"
 #include "quat_walk.cuh"
 
@@ -88,7 +89,7 @@ struct Variant {
     int lt, nseg, n;
     size_t smem_bytes;   // dynamic shared memory per CTA
     int T() const { return nseg * n; }
-    int threads() const { return lt * nseg; }
+    int threads() const { return lt * nseg + extra; }
     size_t smem() const { return smem_bytes; }
     bool chain = false;  // single-pass chained scan (forward): `agg` is the kernel
     // Backward walk: most CTAs in flight, per SM x 4 (0: one CTA per lane
@@ -97,6 +98,7 @@ struct Variant {
     // Segmented chained walk (forward): segments of `segk` chunks, persistent
     // CTAs; `agg` is the kernel (0: another design).
     int segk = 0;
+    int extra = 0;   // threads besides the LT * NSEG compute threads (warp-specialised kernels)
 };
 
 #define QS_VARIANT(B, LT, N)                                                                        \
@@ -115,6 +117,11 @@ struct Variant {
         false, reinterpret_cast<const void *>(qs::quat_segwalk_fwd_kernel<qs::IoF32, LT, NSEG, N, NST, K>), \
             nullptr, false, LT, NSEG, N, qs::segwalk_smem_bytes(LT, NSEG, N, NST), false, 0, K      \
     }
+#define QS_SEGWALK_WS_FWD(LT, NSEG, N, NST, K)                                                      \
+    Variant {                                                                                       \
+        false, reinterpret_cast<const void *>(qs::quat_segwalk_ws_fwd_kernel<qs::IoF32, LT, NSEG, N, NST, K>), \
+            nullptr, false, LT, NSEG, N, qs::segwalk_smem_bytes(LT, NSEG, N, NST), false, 0, K, 64  \
+    }
 #define QS_WALK_BWD(LT, NSEG, N, NSTF, NSTB, SELF)                                                  \
     Variant {                                                                                       \
         true, reinterpret_cast<const void *>(qs::quat_walk_bwd_kernel<qs::IoF32, LT, NSEG, N, NSTF, NSTB, SELF, false>), \
@@ -131,11 +138,9 @@ const Variant kFwdVariants[] = {
     QS_WALK_FWD(32, 8, 4, 6),          // 7: walk, 32 lanes x 32 steps, 6 x 16 KiB
     Variant{false, reinterpret_cast<const void *>(qs::quat_chain_fwd_kernel<qs::IoF32, 32, 8>), nullptr, false,
             32, NTHREADS / 32, 8, qs::tile_smem_bytes(false, 32, 8), true},   // 8: chained scan, 64-step tiles
-    QS_SEGWALK_FWD(32, 8, 8, 4, 8),    // 9: segmented chained walk, 32 lanes, segments of 8 x 64 steps
-    QS_SEGWALK_FWD(32, 8, 8, 3, 8),    // 10: the same, 3 x 32 KiB ring (two CTAs per SM)
-    QS_SEGWALK_FWD(16, 8, 8, 4, 8),    // 11: 16 lanes (128 threads), segments of 8 x 64 steps
-    QS_SEGWALK_FWD(32, 8, 8, 3, 4),    // 12: 32 lanes, segments of 4 x 64 steps
-    QS_SEGWALK_FWD(16, 8, 8, 4, 16),   // 13: 16 lanes, segments of 16 x 64 steps
+    QS_SEGWALK_FWD(32, 8, 8, 3, 4),      // 9: segmented chained walk, 32 lanes, segments of 4 x 64 steps
+    QS_SEGWALK_WS_FWD(32, 8, 8, 4, 4),   // 10: the same, warp-specialised (producer and look-back warps)
+    QS_SEGWALK_WS_FWD(16, 8, 8, 6, 4),   // 11: warp-specialised, 16 lanes, 6 x 16 KiB ring
 };
 #define QS_WALK_BWD_CAP(LT, NSEG, N, NSTF, NSTB, CAPX4)                                             \
     Variant {                                                                                       \
@@ -183,12 +188,18 @@ const Variant kBwdGiven = Variant{true,
             reinterpret_cast<const void *>(qs::quat_apply_kernel<qs::IoBF16, B, LT, N>), B, LT,     \
             NTHREADS / (LT), N, qs::tile_smem_bytes(B, LT, N, 8)                                    \
     }
+#define QS_SEGWALK_FWD16(LT, NSEG, N, NST, K)                                                       \
+    Variant {                                                                                       \
+        false, reinterpret_cast<const void *>(qs::quat_segwalk_fwd_kernel<qs::IoBF16, LT, NSEG, N, NST, K>), \
+            nullptr, false, LT, NSEG, N, qs::segwalk_smem_bytes(LT, NSEG, N, NST, 8), false, 0, K   \
+    }
 const Variant kFwdBf16Variants[] = {
     QS_WALK_FWD16(32, 8, 8, 6),            // 0: 32 lanes x 64 steps, 6 x 16 KiB ring
     QS_WALK_FWD16(16, 8, 8, 6),            // 1: 16 lanes x 64 steps (128 threads), 6 x 8 KiB
     QS_WALK_FWD16(16, 16, 8, 4),           // 2: 16 lanes x 128 steps (256 threads), 4 x 16 KiB
     QS_WALK_FWD16(32, 16, 4, 6),           // 3: 32 lanes x 64 steps (512 threads), 6 x 16 KiB
-    QS_VARIANT16(false, 32, 8),            // 4: three kernels, 64-step chunks (few lane groups)
+    QS_VARIANT16(false, 32, 8),            // 4: three kernels, 64-step chunks
+    QS_SEGWALK_FWD16(32, 8, 8, 3, 4),      // 5: segmented chained walk (few lane groups)
 };
 const Variant kBwdBf16Variants[] = {
     QS_WALK_BWD16(16, 8, 8, 8, 4, false),  // 0: 16 lanes x 64 steps (128 threads), 64 KiB rings
@@ -198,14 +209,16 @@ const Variant kBwdBf16Variants[] = {
     QS_VARIANT16(true, 32, 8),             // 4: three kernels, 64-step chunks (few lane groups)
 };
 #undef QS_VARIANT16
+#undef QS_SEGWALK_FWD16
 #undef QS_WALK_FWD16
 #undef QS_WALK_BWD16
 constexpr int kNumFwdBf16 = sizeof(kFwdBf16Variants) / sizeof(kFwdBf16Variants[0]);
 constexpr int kFwdBf16Default = 1, kBwdBf16Default = 0;   // walks; fastest measured on 8x4096x16x32
-constexpr int kFwdBf16Three = 4, kBwdBf16Three = 4;       // for too few lane groups
+constexpr int kFwdBf16Few = 5, kBwdBf16Few = 4;       // for too few lane groups (forward: segmented walk)
 constexpr int kNumBwdBf16 = sizeof(kBwdBf16Variants) / sizeof(kBwdBf16Variants[0]);
 #undef QS_VARIANT
 #undef QS_SEGWALK_FWD
+#undef QS_SEGWALK_WS_FWD
 #undef QS_WALK_FWD
 #undef QS_WALK_BWD
 #undef QS_WALK_BWD_CAP
@@ -223,7 +236,9 @@ constexpr int kWalkFwd = 4, kWalkBwd = 10, kThreeFwd = 0, kThreeBwd = 0;
 // Forward with too few lane groups for a walk: the segmented chained walk
 // (segments of 4 chunks), measured 10-20% faster than aggregate / carry /
 // apply on 1 x 131072 x 16 x 16, 2 x 65536 x 32 x 32 and 2 x 32768 x 16 x 16.
-constexpr int kSegFwd = 12;
+// (The warp-specialised configurations are faster on the last two and 2%
+// slower on the first.)
+constexpr int kSegFwd = 9;
 constexpr int kNumFwd = sizeof(kFwdVariants) / sizeof(kFwdVariants[0]);
 constexpr int kNumBwd = sizeof(kBwdVariants) / sizeof(kBwdVariants[0]);
 
@@ -517,7 +532,7 @@ int make_plan(bool bwd, int64_t B, int64_t S, int64_t HJ, int sms, Plan *pl, Mod
             const Variant &w = bwd ? kBwdBf16Variants[wi] : kFwdBf16Variants[wi];
             const long long groups = (long long)B * ((HJ + w.lt - 1) / w.lt);
             const long long need = bwd ? 3ll * sms / 2 : 3ll * sms / 4;
-            vi = groups >= need ? wi : (bwd ? kBwdBf16Three : kFwdBf16Three);
+            vi = groups >= need ? wi : (bwd ? kBwdBf16Few : kFwdBf16Few);
         }
     } else {
         vi = pick_variant(bwd, B, HJ, sms);

@@ -53,7 +53,9 @@ def bf16_inputs(dev, w):
     return tb, exact
 
 
-N_BF16_VARIANTS = 5   # compiled configurations per direction (0-3 walks, 4 three kernels)
+# Compiled configurations: forward 0-3 walks, 4 three kernels, 5 segmented
+# chained walk; backward 0-3 walks, 4 three kernels.
+N_BF16_FWD, N_BF16_BWD = 6, 5
 
 
 @pytest.fixture(autouse=True)
@@ -62,11 +64,13 @@ def reset_bf16_variant():
     qs.load_library().quat_cumprod_debug_set_variant_bf16(-1, -1)
 
 
-@pytest.mark.parametrize("variant", range(N_BF16_VARIANTS))
+@pytest.mark.parametrize("variant", range(max(N_BF16_FWD, N_BF16_BWD)))
 @pytest.mark.parametrize("dims", [(1, 64, 2, 4), (2, 333, 3, 16), (3, 1100, 1, 40), (1, 70, 5, 2),
-                                  (2, 1, 1, 2)])
+                                  (2, 1, 1, 2), (1, 5000, 2, 32)])
 def test_bf16_matches_oracle(dev, dims, variant):
-    assert qs.load_library().quat_cumprod_debug_set_variant_bf16(variant, variant) == qs.QS_OK
+    fv = variant if variant < N_BF16_FWD else -1
+    bv = variant if variant < N_BF16_BWD else -1
+    assert qs.load_library().quat_cumprod_debug_set_variant_bf16(fv, bv) == qs.QS_OK
     w = workloads.custom("bf16", *dims, q_kind="rotation", theta_max=0.6, seed=61)
     (tq, ti, td), (q, init, d_cum) = bf16_inputs(dev, w)
     cum = qs.quat_cumprod_fwd_bf16(tq, ti)
@@ -109,11 +113,12 @@ def test_bf16_rounding_is_the_only_difference_from_fp32(dev):
         assert normwise(a.cpu().numpy(), b.cpu().numpy().astype(np.float64)) <= 2.0 ** -8 + 1e-5
 
 
-@pytest.mark.parametrize("name,kernels", [("mamba3", 1), ("large", 1), ("long", 3), ("small", 3)])
-def test_bf16_plan_picks_the_design_by_lane_groups(dev, name, kernels):
+@pytest.mark.parametrize("name,walk", [("mamba3", True), ("large", True), ("long", False), ("small", False)])
+def test_bf16_plan_picks_the_design_by_lane_groups(dev, name, walk):
+    """Walks for many lane groups; else the segmented walk forward, three kernels backward."""
     w = workloads.WORKLOADS[name]
-    for call in ("fwd_bf16", "bwd_bf16"):
-        assert qs.quat_cumprod_plan(call, w.B, w.S, w.H, w.J, device=dev)[1] == kernels
+    assert qs.quat_cumprod_plan("fwd_bf16", w.B, w.S, w.H, w.J, device=dev)[1] == 1
+    assert qs.quat_cumprod_plan("bwd_bf16", w.B, w.S, w.H, w.J, device=dev)[1] == (1 if walk else 3)
 
 
 def test_bf16_long_sequence_sampled_lanes(dev):
@@ -135,8 +140,8 @@ def test_bf16_long_sequence_sampled_lanes(dev):
 
 def test_bf16_unknown_variant_is_rejected(dev):
     lib = qs.load_library()
-    assert lib.quat_cumprod_debug_set_variant_bf16(N_BF16_VARIANTS, 0) == qs.QS_ERR_DIMS
-    assert lib.quat_cumprod_debug_set_variant_bf16(0, N_BF16_VARIANTS) == qs.QS_ERR_DIMS
+    assert lib.quat_cumprod_debug_set_variant_bf16(N_BF16_FWD, 0) == qs.QS_ERR_DIMS
+    assert lib.quat_cumprod_debug_set_variant_bf16(0, N_BF16_BWD) == qs.QS_ERR_DIMS
 
 
 def test_bf16_rejects_odd_lane_count_and_wrong_dtype(dev):

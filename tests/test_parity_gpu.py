@@ -180,10 +180,11 @@ def test_empty_sizes(dev):
 
 
 # Variants 0-3: aggregate / carry / apply kernels; the rest: walk kernels
-# (forward 8: chained scan; 9-13: segmented chained walk; backward 10: at most
-# two CTAs per SM, more lane groups in waves).
-N_FWD_VARIANTS, N_BWD_VARIANTS = 14, 11
-SEGWALK_FWD = [9, 10, 11, 12, 13]
+# (forward 8: chained scan; 9: segmented chained walk; 10, 11: the same,
+# warp-specialised; backward 10: at most two CTAs per SM, more lane groups in
+# waves).
+N_FWD_VARIANTS, N_BWD_VARIANTS = 12, 11
+SEGWALK_FWD = [9, 10, 11]
 
 
 @pytest.mark.parametrize("variant", range(max(N_FWD_VARIANTS, N_BWD_VARIANTS)))
@@ -274,9 +275,10 @@ def test_segmented_walk_long_sequences(dev, variant, dims):
         assert_parity(cum.cpu().numpy(), oracle.fwd(q, init), "cum")
 
 
-def test_segmented_walk_stall_reports_timeout_then_recovers(dev):
+@pytest.mark.parametrize("variant", [9, 10])   # one CTA role for all, warp-specialised
+def test_segmented_walk_stall_reports_timeout_then_recovers(dev, variant):
     lib = qs.load_library()
-    assert lib.quat_cumprod_debug_set_variant(9, -1) == qs.QS_OK
+    assert lib.quat_cumprod_debug_set_variant(variant, -1) == qs.QS_OK
     w = workloads.custom("segstall", 2, 3000, 2, 16, seed=23)
     q, init, d_cum = workloads.make_inputs(w)
     tq, ti = (torch.from_numpy(a).to(dev) for a in (q, init))
