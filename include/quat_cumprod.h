@@ -205,6 +205,28 @@ int quat_cumprod_bwd_bf16(const uint16_t *q, const uint16_t *init, const uint16_
                           int64_t B, int64_t S, int64_t H, int64_t J, void *stream);
 
 /*
+ * One forward + backward step on HOST buffers: cum = the forward scan of
+ * (q, init), and (d_q, d_init) = its backward from d_cum, exactly what
+ * quat_cumprod_fwd and quat_cumprod_bwd compute, with the same layouts, but
+ * every pointer is host memory (page-locked memory lets the copies overlap;
+ * other host memory works, with the copies serialised).  No alignment is
+ * required.  The batch is processed in slices of whole batch entries:
+ * the copy of slice i to the device, the kernels of slice i-1 (on `stream`)
+ * and the copy of slice i-2 back overlap, through library-owned device
+ * staging (grown as needed, kept for later calls).
+ * Ordering is that of cudaMemcpyAsync: nothing starts before the work
+ * already on `stream`, and the host outputs are complete once `stream` has
+ * been synchronized (quat_cumprod_status(stream) does that and reports
+ * device-side errors of the step).  The caller must not touch the host
+ * buffers before then.
+ * Errors as for quat_cumprod_bwd, except QS_ERR_MISALIGNED; QS_ERR_ALIAS if
+ * an output overlaps an input or another output.
+ */
+int quat_cumprod_fwd_bwd_host(const float *q, const float *init, const float *d_cum,
+                              float *cum, float *d_q, float *d_init,
+                              int64_t B, int64_t S, int64_t H, int64_t J, void *stream);
+
+/*
  * Synchronizes `stream`, then returns QS_ERR_TIMEOUT if any call enqueued on it
  * since the previous quat_cumprod_status() recorded a device-side timeout
  * (its outputs are then invalid), QS_ERR_CUDA if the synchronization failed,

@@ -15,7 +15,9 @@ Calls: ``quat_cumprod_fwd`` / ``quat_cumprod_bwd`` (the page's operation),
 ``quat_cumprod_fwd_carries`` / ``quat_cumprod_bwd_carries`` (keep the 64-step
 chunk carries between the two), ``quat_cumprod_fwd_bf16`` /
 ``quat_cumprod_bwd_bf16`` (bfloat16 tensors), ``quat_cumprod_bwd_noalloc``
-(no allocation), ``quat_cumprod_plan`` and ``quat_cumprod_status``.  The
+(no allocation), ``quat_cumprod_fwd_bwd_host`` (a whole step on host
+tensors, copies overlapped with the kernels), ``quat_cumprod_plan`` and
+``quat_cumprod_status``.  The
 autograd wrapper is in :mod:`quaternion_cumulative_product_gb300.autograd`.
 """
 from __future__ import annotations
@@ -30,7 +32,8 @@ __all__ = [
     "QS_NOALLOC_MAX_TILES", "QS_CARRY_STEPS", "QuatScanError", "library_path", "load_library",
     "quat_cumprod_fwd", "quat_cumprod_bwd", "quat_cumprod_fwd_carries", "quat_cumprod_bwd_carries",
     "quat_cumprod_fwd_bf16", "quat_cumprod_bwd_bf16",
-    "quat_cumprod_bwd_noalloc", "quat_cumprod_plan", "quat_cumprod_status", "quat_cumprod_strerror",
+    "quat_cumprod_bwd_noalloc", "quat_cumprod_fwd_bwd_host", "quat_cumprod_plan", "quat_cumprod_status",
+    "quat_cumprod_strerror",
 ]
 
 QS_OK = 0
@@ -86,6 +89,8 @@ def load_library():
         lib.quat_cumprod_bwd.restype = ctypes.c_int
         lib.quat_cumprod_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, vp]
         lib.quat_cumprod_bwd_noalloc.restype = ctypes.c_int
+        lib.quat_cumprod_fwd_bwd_host.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, vp]
+        lib.quat_cumprod_fwd_bwd_host.restype = ctypes.c_int
         lib.quat_cumprod_fwd_bf16.argtypes = [vp, vp, vp, i64, i64, i64, i64, vp]
         lib.quat_cumprod_fwd_bf16.restype = ctypes.c_int
         lib.quat_cumprod_bwd_bf16.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, vp]
@@ -329,6 +334,59 @@ def quat_cumprod_bwd_noalloc(q, init, d_cum, d_q, d_init, stream=None):
     if rc != QS_OK:
         raise QuatScanError(rc, "quat_cumprod_bwd_noalloc")
     return d_q, d_init
+
+
+def _check_host(name, t, shape):
+    torch = _torch()
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != torch.float32:
+        raise TypeError(f"{name} must be float32, got {t.dtype}")
+    if t.device.type != "cpu":
+        raise ValueError(f"{name} must be a host (CPU) tensor, got {t.device}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def quat_cumprod_fwd_bwd_host(q, init, d_cum, cum=None, d_q=None, d_init=None, device=None, stream=None,
+                              synchronize=True):
+    """One forward + backward step on host tensors: ``(cum, d_q, d_init)``.
+
+    ``q``, ``init``, ``d_cum``: CPU float32 tensors ([B,S,H,J,4], [B,H,J,4],
+    [B,S,H,J,4]); page-locked (``pin_memory()``) tensors let the copies to
+    and from the GPU overlap the kernels.  Outputs are allocated page-locked
+    when not given.  The step runs on ``device`` (default: the current CUDA
+    device) and is enqueued on ``stream``; with ``synchronize`` (default) the
+    call returns once the outputs are complete, otherwise the caller
+    synchronizes ``stream`` before touching any of the six tensors.
+    """
+    torch = _torch()
+    if q.dim() != 5 or q.shape[-1] != 4:
+        raise ValueError(f"q must be [B,S,H,J,4], got {tuple(q.shape)}")
+    B, S, H, J, _ = q.shape
+    _check_host("q", q, q.shape)
+    _check_host("init", init, (B, H, J, 4))
+    _check_host("d_cum", d_cum, q.shape)
+    cum = torch.empty(q.shape, dtype=torch.float32).pin_memory() if cum is None else cum
+    d_q = torch.empty(q.shape, dtype=torch.float32).pin_memory() if d_q is None else d_q
+    d_init = torch.empty(init.shape, dtype=torch.float32).pin_memory() if d_init is None else d_init
+    _check_host("cum", cum, q.shape)
+    _check_host("d_q", d_q, q.shape)
+    _check_host("d_init", d_init, init.shape)
+    device = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    with torch.cuda.device(device):
+        handle = _stream_handle(stream, device)
+        rc = load_library().quat_cumprod_fwd_bwd_host(
+            ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(init.data_ptr()), ctypes.c_void_p(d_cum.data_ptr()),
+            ctypes.c_void_p(cum.data_ptr()), ctypes.c_void_p(d_q.data_ptr()), ctypes.c_void_p(d_init.data_ptr()),
+            B, S, H, J, handle)
+        if rc != QS_OK:
+            raise QuatScanError(rc, "quat_cumprod_fwd_bwd_host")
+        if synchronize:
+            (torch.cuda.current_stream(device) if stream is None else stream).synchronize()
+    return cum, d_q, d_init
 
 
 _PLAN_CALLS = {"fwd": 0, "bwd": 1, "fwd_carries": 2, "bwd_carries": 3, "fwd_bf16": 4, "bwd_bf16": 5}

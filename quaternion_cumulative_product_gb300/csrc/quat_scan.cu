@@ -942,6 +942,193 @@ extern "C" int quat_cumprod_bwd_bf16(const uint16_t *q, const uint16_t *init, co
     return launch(true, q, d_cum, d_q, init, d_init, B, S, HJ, stream, Mode::PLAIN, nullptr, true);
 }
 
+// ===========================================================================
+// quat_cumprod_fwd_bwd_host: one forward + backward step on host buffers.
+// The work is cut into slices (whole batch entries, or lane ranges of one
+// entry when an entry is large; lanes are independent); slice i is copied in
+// on an internal stream while slice i-1 is computed on the caller's stream
+// and slice i-2 is copied out on a second internal stream, through NSLOT
+// device staging slots (a slot is reused once its copy-out is done).  The
+// caller's stream waits for the last copy-out, so the call is ordered like
+// cudaMemcpyAsync: prior work on `stream` first, and the host outputs are
+// ready once `stream` has been synchronized.
+// ===========================================================================
+namespace {
+
+constexpr int NSLOT = 3;
+constexpr size_t kSliceBytes = 32u << 20;   // about this much of one tensor per slice
+
+struct HostPipe {
+    bool ready = false;
+    cudaStream_t s_in = nullptr, s_out = nullptr;
+    cudaEvent_t start = nullptr, end = nullptr;
+    cudaEvent_t in_done[NSLOT] = {}, comp_done[NSLOT] = {}, out_done[NSLOT] = {};
+    unsigned char *stage = nullptr;
+    size_t bytes = 0;
+};
+std::map<int, HostPipe> g_pipe;
+std::mutex g_pipe_mu;   // one host-buffer step enqueued at a time per process
+
+int pipe_of(int dev, size_t slot_bytes, HostPipe **out) {
+    HostPipe &p = g_pipe[dev];
+    if (!p.ready) {
+        bool ok = cudaStreamCreateWithFlags(&p.s_in, cudaStreamNonBlocking) == cudaSuccess &&
+                  cudaStreamCreateWithFlags(&p.s_out, cudaStreamNonBlocking) == cudaSuccess &&
+                  cudaEventCreateWithFlags(&p.start, cudaEventDisableTiming) == cudaSuccess &&
+                  cudaEventCreateWithFlags(&p.end, cudaEventDisableTiming) == cudaSuccess;
+        for (int i = 0; ok && i < NSLOT; ++i)
+            ok = cudaEventCreateWithFlags(&p.in_done[i], cudaEventDisableTiming) == cudaSuccess &&
+                 cudaEventCreateWithFlags(&p.comp_done[i], cudaEventDisableTiming) == cudaSuccess &&
+                 cudaEventCreateWithFlags(&p.out_done[i], cudaEventDisableTiming) == cudaSuccess;
+        if (!ok) {
+            cudaGetLastError();
+            return QS_ERR_CUDA;
+        }
+        p.ready = true;
+    }
+    const size_t need = slot_bytes * NSLOT;
+    if (p.bytes < need) {
+        // Earlier steps may still copy out of the old staging: wait for them.
+        if (cudaStreamSynchronize(p.s_in) != cudaSuccess || cudaStreamSynchronize(p.s_out) != cudaSuccess) {
+            cudaGetLastError();
+            return QS_ERR_CUDA;
+        }
+        if (p.stage) cudaFree(p.stage);
+        p.stage = nullptr;
+        p.bytes = 0;
+        void *m = nullptr;
+        if (cudaMalloc(&m, need) != cudaSuccess) {
+            cudaGetLastError();
+            return QS_ERR_NOMEM;
+        }
+        p.stage = static_cast<unsigned char *>(m);
+        p.bytes = need;
+    }
+    *out = &p;
+    return QS_OK;
+}
+
+}  // namespace
+
+extern "C" int quat_cumprod_fwd_bwd_host(const float *q, const float *init, const float *d_cum, float *cum,
+                                         float *d_q, float *d_init, int64_t B, int64_t S, int64_t H, int64_t J,
+                                         void *stream_) {
+    const int dc = check_dims(B, S, H, J);
+    if (dc != QS_OK && dc != 1) return dc;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+    const int64_t HJ = H * J;
+    if (dc == 1) {
+        // No steps but some lanes: the gradient of init is zero (written once
+        // the work already on the stream is done).
+        if (S == 0 && B > 0 && HJ > 0) {
+            if (!d_init) return QS_ERR_NULL;
+            if (cudaStreamSynchronize(stream) != cudaSuccess) {
+                cudaGetLastError();
+                return QS_ERR_CUDA;
+            }
+            std::memset(d_init, 0, (size_t)B * HJ * 16);
+        }
+        return QS_OK;
+    }
+    if (!q || !init || !d_cum || !cum || !d_q || !d_init) return QS_ERR_NULL;
+    const size_t big = (size_t)B * S * HJ * 16, small = (size_t)B * HJ * 16;
+    const void *ins[3] = {q, init, d_cum};
+    const size_t insz[3] = {big, small, big};
+    const void *outs[3] = {cum, d_q, d_init};
+    const size_t outsz[3] = {big, big, small};
+    for (int o = 0; o < 3; ++o) {
+        for (int i = 0; i < 3; ++i)
+            if (overlaps(outs[o], outsz[o], ins[i], insz[i])) return QS_ERR_ALIAS;
+        for (int o2 = o + 1; o2 < 3; ++o2)
+            if (overlaps(outs[o], outsz[o], outs[o2], outsz[o2])) return QS_ERR_ALIAS;
+    }
+    DevInfo *di = nullptr;
+    int dev = 0;
+    int rc = device_info(&di, &dev);
+    if (rc != QS_OK) return rc;
+
+    // Slices: whole batch entries, about kSliceBytes of a tensor each.  With
+    // fewer than kMinEntries entries there would be too little to overlap:
+    // then lane ranges of one entry (pitched copies) of at least kMinLanes
+    // lanes (narrower rows copy slowly), up to kRanges ranges per entry.
+    constexpr int64_t kMinEntries = 4, kMinLanes = 64, kRanges = 8;
+    const size_t per_b = (size_t)S * HJ * 16;
+    const bool by_lanes = B < kMinEntries && HJ >= 2 * kMinLanes;
+    const int64_t sb = by_lanes ? 1 : std::max<int64_t>(1, std::min<int64_t>(B, (int64_t)(kSliceBytes / per_b)));
+    int64_t sl_even = HJ;
+    if (by_lanes) {
+        const int64_t ranges = std::min<int64_t>(kRanges / B < 2 ? 2 : kRanges / B, HJ / kMinLanes);
+        sl_even = (HJ + ranges - 1) / ranges;
+        sl_even = (sl_even + 15) / 16 * 16;   // 256-byte rows
+    }
+    // One staging slot: q, d_cum, cum, d_q of a slice, then init and d_init.
+    const size_t big_s = align_up((size_t)sb * S * sl_even * 16, 256), small_s = align_up((size_t)sb * sl_even * 16, 256);
+    const size_t slot_bytes = 4 * big_s + 2 * small_s;
+
+    std::lock_guard<std::mutex> lk(g_pipe_mu);
+    HostPipe *p = nullptr;
+    rc = pipe_of(dev, slot_bytes, &p);
+    if (rc != QS_OK) return rc;
+    auto fail = [&]() {
+        cudaGetLastError();
+        return QS_ERR_CUDA;
+    };
+    // Nothing starts before the work already on the caller's stream.
+    if (cudaEventRecord(p->start, stream) != cudaSuccess || cudaStreamWaitEvent(p->s_in, p->start, 0) != cudaSuccess ||
+        cudaStreamWaitEvent(p->s_out, p->start, 0) != cudaSuccess)
+        return fail();
+    const unsigned char *hq = reinterpret_cast<const unsigned char *>(q);
+    const unsigned char *hi = reinterpret_cast<const unsigned char *>(init);
+    const unsigned char *hd = reinterpret_cast<const unsigned char *>(d_cum);
+    unsigned char *hc = reinterpret_cast<unsigned char *>(cum);
+    unsigned char *hg = reinterpret_cast<unsigned char *>(d_q);
+    unsigned char *hgi = reinterpret_cast<unsigned char *>(d_init);
+    const size_t row = (size_t)HJ * 16;   // one step of one batch entry in the host tensors
+    int i = 0;
+    for (int64_t b0 = 0; b0 < B; b0 += sb) {
+        const int64_t nb = std::min<int64_t>(sb, B - b0);
+        for (int64_t l0 = 0; l0 < HJ; l0 += sl_even, ++i) {
+            const int64_t nl = std::min<int64_t>(sl_even, HJ - l0);
+            const int slot = i % NSLOT;
+            unsigned char *base = p->stage + (size_t)slot * slot_bytes;
+            float *sq = reinterpret_cast<float *>(base), *sd = reinterpret_cast<float *>(base + big_s);
+            float *sc = reinterpret_cast<float *>(base + 2 * big_s), *sg = reinterpret_cast<float *>(base + 3 * big_s);
+            float *si = reinterpret_cast<float *>(base + 4 * big_s);
+            float *sgi = reinterpret_cast<float *>(base + 4 * big_s + small_s);
+            const size_t w = (size_t)nl * 16;                  // bytes of one step of the slice
+            const size_t hoff = (size_t)b0 * S * row + (size_t)l0 * 16;
+            const size_t ioff = (size_t)b0 * row + (size_t)l0 * 16;
+            const size_t rows = (size_t)nb * S;                // whole entries: rows of `row` bytes
+            // in: once the slot's previous copy-out is done
+            auto in2d = [&](void *dst, const unsigned char *src, size_t height) {
+                return cudaMemcpy2DAsync(dst, w, src, row, w, height, cudaMemcpyHostToDevice, p->s_in) == cudaSuccess;
+            };
+            auto out2d = [&](unsigned char *dst, const void *src, size_t height) {
+                return cudaMemcpy2DAsync(dst, row, src, w, w, height, cudaMemcpyDeviceToHost, p->s_out) == cudaSuccess;
+            };
+            if (cudaStreamWaitEvent(p->s_in, p->out_done[slot], 0) != cudaSuccess || !in2d(sq, hq + hoff, rows) ||
+                !in2d(si, hi + ioff, (size_t)nb) || !in2d(sd, hd + hoff, rows) ||
+                cudaEventRecord(p->in_done[slot], p->s_in) != cudaSuccess)
+                return fail();
+            // compute on the caller's stream: nb entries of nl lanes
+            if (cudaStreamWaitEvent(stream, p->in_done[slot], 0) != cudaSuccess) return fail();
+            rc = launch(false, sq, nullptr, sc, si, nullptr, nb, S, nl, stream);
+            if (rc == QS_OK) rc = launch(true, sq, sd, sg, si, sgi, nb, S, nl, stream);
+            if (rc != QS_OK) return rc;
+            if (cudaEventRecord(p->comp_done[slot], stream) != cudaSuccess) return fail();
+            // out
+            if (cudaStreamWaitEvent(p->s_out, p->comp_done[slot], 0) != cudaSuccess || !out2d(hc + hoff, sc, rows) ||
+                !out2d(hg + hoff, sg, rows) || !out2d(hgi + ioff, sgi, (size_t)nb) ||
+                cudaEventRecord(p->out_done[slot], p->s_out) != cudaSuccess)
+                return fail();
+        }
+    }
+    // The caller's stream waits for the last copy-out (s_out runs in order).
+    if (cudaEventRecord(p->end, p->s_out) != cudaSuccess || cudaStreamWaitEvent(stream, p->end, 0) != cudaSuccess)
+        return fail();
+    return QS_OK;
+}
+
 extern "C" int quat_cumprod_status(void *stream_) {
     cudaStream_t stream = static_cast<cudaStream_t>(stream_);
     if (cudaStreamSynchronize(stream) != cudaSuccess) {

@@ -12,6 +12,7 @@ import os
 import re
 import subprocess
 
+import numpy as np
 import pytest
 
 import quaternion_cumulative_product_gb300 as qs
@@ -206,3 +207,27 @@ def test_bf16_calls_argument_checks_before_any_cuda_call(lib):
     assert f(_p(q), _p(i), _p(q + 64), 1, 16, 2, 2, None) == qs.QS_ERR_ALIAS    # 1*16*4 quats * 8 B
     assert g(None, None, None, None, None, 2, 0, 2, 2, None) == qs.QS_ERR_NULL
     assert g(_p(q), _p(i), _p(d), _p(d + 256), _p(gi), 1, 16, 2, 2, None) == qs.QS_ERR_ALIAS
+
+
+def test_host_step_argument_checks(lib):
+    """quat_cumprod_fwd_bwd_host rejects bad arguments before any CUDA call (host buffers)."""
+    f = lib.quat_cumprod_fwd_bwd_host
+    big = np.zeros((1, 4, 1, 1, 4), np.float32)
+    small = np.zeros((1, 1, 1, 4), np.float32)
+    bufs = [big, small, big.copy(), big.copy(), big.copy(), small.copy()]
+    ptrs = [b.ctypes.data for b in bufs]
+    assert f(*ptrs, 1, -1, 1, 1, None) == qs.QS_ERR_DIMS
+    for k in range(6):
+        p = list(ptrs)
+        p[k] = None
+        assert f(*p, 1, 4, 1, 1, None) == qs.QS_ERR_NULL
+    p = list(ptrs)
+    p[3] = ptrs[0]              # cum over q
+    assert f(*p, 1, 4, 1, 1, None) == qs.QS_ERR_ALIAS
+    p = list(ptrs)
+    p[4] = ptrs[3]              # d_q over cum
+    assert f(*p, 1, 4, 1, 1, None) == qs.QS_ERR_ALIAS
+    p = list(ptrs)
+    p[5] = ptrs[1]              # d_init over init
+    assert f(*p, 1, 4, 1, 1, None) == qs.QS_ERR_ALIAS
+    assert f(*ptrs, 0, 4, 1, 1, None) == qs.QS_OK   # no lanes: nothing to do
