@@ -331,6 +331,13 @@ def run_ours(args, w, world, rank, local):
     st = qs.quat_cumprod_status(device=dev)
     if st != qs.QS_OK:
         raise RuntimeError(f"device status after warm-up: {qs.quat_cumprod_strerror(st)}")
+    # Whether a second step on the same inputs gives bitwise the same outputs
+    # (outside the timed region).
+    first = (cum.clone(), d_q.clone(), d_init.clone())
+    step()
+    torch.cuda.synchronize(dev)
+    repeatable = all(torch.equal(a, b) for a, b in zip(first, (cum, d_q, d_init)))
+    del first
 
     # ---- device-timed region -------------------------------------------------
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
@@ -522,6 +529,7 @@ def run_ours(args, w, world, rank, local):
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "steps": e2e_steps,
                 "call": "quat_cumprod_fwd_bwd_host (pinned host buffers; batch slices whose copies "
                         "overlap the kernels)"},
+        "bitwise_repeatable": repeatable,
         "gpu_launches": launches[0],
         "clocks": clocks,
     }
