@@ -39,6 +39,7 @@ UNIT = "elements/s"
 DEFAULT_WORKLOAD = "mamba3"
 FWD_BYTES_PER_ELEMENT = 32      # read q, write cum
 BWD_BYTES_PER_ELEMENT = 48      # read q and d_cum, write d_q
+STEP_BYTES = FWD_BYTES_PER_ELEMENT + BWD_BYTES_PER_ELEMENT
 L2_BYTES = 126 * (1 << 20)
 FALLBACK_HBM_GBS = 6800.0
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.txt")
@@ -371,6 +372,41 @@ def run_ours(args, w, world, rank, local):
     E = w.elements
     value = weak_scaling_value(world, E, step_ms)
 
+    # ---- each call alone: median over reps, with L2 flushed before every rep
+    # by READING a buffer of twice its size, so that no dirty line of earlier
+    # work is left for the timed call to write back ---------------------------
+    flushbuf = torch.ones(2 * L2_BYTES // 4, device=dev)
+    alone_reps = max(20, args.steps)
+
+    def alone(calls):
+        ms = []
+        a0 = torch.cuda.Event(enable_timing=True)
+        a1 = torch.cuda.Event(enable_timing=True)
+        for _ in range(alone_reps):
+            flushbuf.sum()
+            a0.record(stream)
+            for c in calls:
+                c()
+            a1.record(stream)
+            a1.synchronize()
+            ms.append(a0.elapsed_time(a1))
+        return statistics.median(ms)
+
+    def run_fwd():
+        qs.quat_cumprod_fwd(q, init, cum)
+
+    def run_bwd():
+        qs.quat_cumprod_bwd(q, init, d_cum, d_q, d_init)
+
+    torch.cuda.synchronize(dev)
+    barrier(dev)
+    alone_ms = {"fwd": alone([run_fwd]), "bwd": alone([run_bwd]), "fwd_bwd": alone([run_fwd, run_bwd])}
+    st = qs.quat_cumprod_status(device=dev)
+    if st != qs.QS_OK:
+        raise RuntimeError(f"device status after the calls alone: {qs.quat_cumprod_strerror(st)}")
+    alone_ms = {k: reduce_max(v, dev) for k, v in alone_ms.items()}
+    del flushbuf
+
     # ---- the same step with saved chunk carries (forward writes them, the
     # backward starts from them instead of recomputing the forward) ----------
     carries = torch.empty((w.B, (w.S + qs.QS_CARRY_STEPS - 1) // qs.QS_CARRY_STEPS, w.H, w.J, 4),
@@ -507,6 +543,19 @@ def run_ours(args, w, world, rank, local):
                          "traffic": recorded_traffic("quat_cumprod_fwd", w.name),
                          "algorithmic_bytes_per_launch": FWD_BYTES_PER_ELEMENT * E,
                          "avg_launch_ms": fwd_avg},
+        "roofline_step": {"bound": "hbm", "unit": "GB/s", "peak": peak,
+                          "achieved": STEP_BYTES * E / (step_ms * 1e-3) / 1e9,
+                          "frac": STEP_BYTES * E / (step_ms * 1e-3) / 1e9 / peak,
+                          "algorithmic_bytes_per_step": STEP_BYTES * E},
+        "alone": {
+            "note": f"each call timed by itself: median of {alone_reps} reps, L2 flushed before every rep "
+                    "by reading a 2x126 MB buffer (no dirty lines left behind)",
+            "reps": alone_reps,
+            **{k: {"ms": v, "achieved_gbs": nbytes * E / (v * 1e-3) / 1e9,
+                   "frac": nbytes * E / (v * 1e-3) / 1e9 / peak}
+               for k, v, nbytes in (("fwd", alone_ms["fwd"], FWD_BYTES_PER_ELEMENT),
+                                    ("bwd", alone_ms["bwd"], BWD_BYTES_PER_ELEMENT),
+                                    ("fwd_bwd", alone_ms["fwd_bwd"], STEP_BYTES))}},
         "saved_carries": {
             "note": "forward also writes the 64-step chunk carries; backward starts from them "
                     "(the page's node keeps only q and init: this is the measured alternative)",
