@@ -222,6 +222,9 @@ constexpr int kNumBwdBf16 = sizeof(kBwdBf16Variants) / sizeof(kBwdBf16Variants[0
 #undef QS_WALK_FWD
 #undef QS_WALK_BWD
 #undef QS_WALK_BWD_CAP
+// Lanes per block of the carry scan (sequences of more than 256 chunks).
+constexpr int kCarryScanLanes = 2;
+
 // Automatic choice between the two designs.  A walk keeps one CTA per lane
 // group for the whole sequence, so it needs enough lane groups to keep every
 // SM streaming (measured: 128 groups of 32 lanes forward and 256 groups of 16
@@ -760,13 +763,15 @@ int launch(bool bwd, const void *q, const void *d_cum, void *out, const void *in
     const int tiles = (int)pl.tiles;
     int lt = pl.v->lt;
     const void *carry_fn;
-    // Many chunks per lane: one block per lane and a scan over 256 ranges.
+    // Many chunks per lane: kCarryScanLanes lanes per block and a scan over
+    // 256 / kCarryScanLanes chunk ranges per lane.
+    constexpr int LPB = kCarryScanLanes;
     const bool scan = pl.geo.C > 256;
     if (scan) {
-        carry_fn = bf16 ? (bwd ? reinterpret_cast<const void *>(qs::quat_carry_scan_kernel<qs::IoBF16, true>)
-                               : reinterpret_cast<const void *>(qs::quat_carry_scan_kernel<qs::IoBF16, false>))
-                        : (bwd ? reinterpret_cast<const void *>(qs::quat_carry_scan_kernel<qs::IoF32, true>)
-                               : reinterpret_cast<const void *>(qs::quat_carry_scan_kernel<qs::IoF32, false>));
+        carry_fn = bf16 ? (bwd ? reinterpret_cast<const void *>(qs::quat_carry_scan_kernel<qs::IoBF16, true, LPB>)
+                               : reinterpret_cast<const void *>(qs::quat_carry_scan_kernel<qs::IoBF16, false, LPB>))
+                        : (bwd ? reinterpret_cast<const void *>(qs::quat_carry_scan_kernel<qs::IoF32, true, LPB>)
+                               : reinterpret_cast<const void *>(qs::quat_carry_scan_kernel<qs::IoF32, false, LPB>));
     } else if (bf16) {
         if (pl.carry_lb == 8)
             carry_fn = bwd ? reinterpret_cast<const void *>(qs::quat_carry_kernel<qs::IoBF16, true, 8>)
@@ -784,7 +789,7 @@ int launch(bool bwd, const void *q, const void *d_cum, void *out, const void *in
     void *agg_args[] = {&qmap, &dmap, &aggL, &aggW, &pl.geo, &ctl};
     void *carry_args[] = {&aggL_c, &aggW_c, &init4, &carF, &carH, &dinit4, &pl.geo, &lt};
     void *apply_args[] = {&qmap, &dmap, &carF_c, &carH_c, &out4, &pl.geo, &ctl};
-    const int carry_blocks = scan ? pl.geo.NL : (pl.geo.NL + pl.carry_lb - 1) / pl.carry_lb;
+    const int carry_blocks = scan ? (pl.geo.NL + LPB - 1) / LPB : (pl.geo.NL + pl.carry_lb - 1) / pl.carry_lb;
     if (cudaLaunchKernel(pl.v->agg, dim3(tiles), dim3(NTHREADS), agg_args, pl.v->smem(), stream) != cudaSuccess ||
         cudaLaunchKernel(carry_fn, dim3(carry_blocks), dim3(NTHREADS), carry_args, 0, stream) != cudaSuccess ||
         cudaLaunchKernel(pl.v->apply, dim3(tiles), dim3(NTHREADS), apply_args, pl.v->smem(), stream) !=

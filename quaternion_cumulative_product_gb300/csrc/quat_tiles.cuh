@@ -160,31 +160,35 @@ __global__ void __launch_bounds__(NTHREADS)
 }
 
 // ---------------------------------------------------------------------------
-// Carry kernel for many chunks per lane: one block per padded lane, thread r
-// folds the chunk range r (about C / 256 chunks); the 256 range products (and
-// affine range maps) are combined by a log-depth scan in shared memory, then
-// every thread writes the carries of its range.  Same outputs as
-// quat_carry_kernel.
+// Carry kernel for many chunks per lane: a block takes LPB adjacent padded
+// lanes, and thread (r, l) folds chunk range r (about C / (256 / LPB) chunks)
+// of lane l; the 256 / LPB range products (and affine range maps) of a lane
+// are combined by a log-depth scan in shared memory, then every thread writes
+// the carries of its range.  Same outputs as quat_carry_kernel.  The
+// aggregates are stored [chunk][lane], so adjacent lanes share the 32-byte
+// sectors a warp's loads touch.
 // ---------------------------------------------------------------------------
-template <typename IO, bool BWD>
+template <typename IO, bool BWD, int LPB>
 __global__ void __launch_bounds__(NTHREADS)
     quat_carry_scan_kernel(const float4 *__restrict__ aggL, const float4 *__restrict__ aggW,
                            const typename IO::elem *__restrict__ init, float4 *__restrict__ carF,
                            float4 *__restrict__ carH, typename IO::elem *__restrict__ d_init, const Geometry geo,
                            int LT) {
-    constexpr int U = 8;   // aggregates loaded per batch (independent loads)
-    __shared__ float4 sP[NTHREADS];
-    __shared__ float4 sM[BWD ? NTHREADS : 1];
-    __shared__ float4 sV[BWD ? NTHREADS : 1];
-    const int gl = static_cast<int>(blockIdx.x);   // padded lane
-    const int r = threadIdx.x;
+    constexpr int U = 8;                // aggregates loaded per batch (independent loads)
+    constexpr int RT = NTHREADS / LPB;  // chunk ranges per lane
+    __shared__ float4 sP[RT][LPB];
+    __shared__ float4 sM[BWD ? RT : 1][LPB];
+    __shared__ float4 sV[BWD ? RT : 1][LPB];
+    const int l = static_cast<int>(threadIdx.x) % LPB, r = static_cast<int>(threadIdx.x) / LPB;
+    const int gl = static_cast<int>(blockIdx.x) * LPB + l;   // padded lane
+    const bool in_range = gl < geo.NL;
     const int g = gl / LT, lig = gl - g * LT;
     const int b = g / geo.NGb, hj = (g - b * geo.NGb) * LT + lig;
-    const bool lane_ok = hj < geo.HJ;
+    const bool lane_ok = in_range && hj < geo.HJ;
     const int C = geo.C;
     const long long NL = geo.NL;
-    const int R = (C + NTHREADS - 1) / NTHREADS;
-    const int c_lo = min(C, r * R), c_hi = min(C, c_lo + R);
+    const int R = (C + RT - 1) / RT;
+    const int c_lo = in_range ? min(C, r * R) : 0, c_hi = in_range ? min(C, c_lo + R) : 0;
     auto at = [&](int c) { return static_cast<long long>(c) * NL + gl; };
 
     // This range as a product P and (backward) as the map h -> V + M (x) h.
@@ -213,40 +217,41 @@ __global__ void __launch_bounds__(NTHREADS)
             }
         }
     }
-    // Inclusive scans over the ranges: products of ranges 0..r (later on the
-    // left) and maps of ranges r..255 (range r applied last).
-    sP[r] = P;
+    // Inclusive scans over the ranges of a lane: products of ranges 0..r
+    // (later on the left) and maps of ranges r..RT-1 (range r applied last).
+    sP[r][l] = P;
     if (BWD) {
-        sM[r] = M;
-        sV[r] = V;
+        sM[r][l] = M;
+        sV[r][l] = V;
     }
     __syncthreads();
-    for (int d = 1; d < NTHREADS; d <<= 1) {
-        const float4 oP = r >= d ? sP[r - d] : q_ident();
+    for (int d = 1; d < RT; d <<= 1) {
+        const float4 oP = r >= d ? sP[r - d][l] : q_ident();
         float4 oM = q_ident(), oV = q_zero();
-        if (BWD && r + d < NTHREADS) {
-            oM = sM[r + d];
-            oV = sV[r + d];
+        if (BWD && r + d < RT) {
+            oM = sM[r + d][l];
+            oV = sV[r + d][l];
         }
         __syncthreads();
         if (r >= d) {
             P = q_mul(P, oP);
-            sP[r] = P;
+            sP[r][l] = P;
         }
-        if (BWD && r + d < NTHREADS) {
+        if (BWD && r + d < RT) {
             V = q_add(V, q_mul(M, oV));
             M = q_mul(M, oM);
-            sM[r] = M;
-            sV[r] = V;
+            sM[r][l] = M;
+            sV[r][l] = V;
         }
         __syncthreads();
     }
+    if (!in_range) return;   // (after the last barrier)
     const float4 init4 = lane_ok ? IO::get(init[static_cast<long long>(b) * geo.HJ + hj]) : q_ident();
-    float4 carry = r > 0 ? q_mul(sP[r - 1], init4) : init4;   // cum just before range r
-    float4 h = q_zero();                                       // H entering range r from the right
+    float4 carry = r > 0 ? q_mul(sP[r - 1][l], init4) : init4;   // cum just before range r
+    float4 h = q_zero();                                          // H entering range r from the right
     if (BWD) {
-        if (r + 1 < NTHREADS) h = sV[r + 1];
-        if (r == 0 && lane_ok) d_init[static_cast<long long>(b) * geo.HJ + hj] = IO::put(sV[0]);
+        if (r + 1 < RT) h = sV[r + 1][l];
+        if (r == 0 && lane_ok) d_init[static_cast<long long>(b) * geo.HJ + hj] = IO::put(sV[0][l]);
     }
     for (int c0 = c_lo; c0 < c_hi; c0 += U) {
         float4 Lb[U];
