@@ -40,13 +40,14 @@ def host(a, pinned):
     return t.pin_memory() if pinned else t
 
 
-# Slices are about 16 MB of one tensor: (6, 8192, 4, 32) has 16.8 MB per batch
-# entry, so one lane range per entry (6 slices, every staging slot reused);
-# (1, 2048, 8, 100): lane ranges of 512 and 288 lanes (pitched copies, a
-# ragged last range); (7, 6000, 4, 32): one entry per slice; (2, 333, 3, 16):
-# one slice; (1, 64, 2, 4): one entry.
-@pytest.mark.parametrize("dims", [(6, 8192, 4, 32), (1, 2048, 8, 100), (7, 6000, 4, 32), (2, 333, 3, 16),
-                                  (1, 64, 2, 4)])
+# Slices hold about 32 MB of one tensor.  (6, 8192, 4, 32): 16.8 MB per batch
+# entry, two entries per slice (3 slices); (7, 6000, 4, 32): two entries per
+# slice and a ragged last one (4 slices, a staging slot reused); (1, 2048, 8,
+# 100): 8 lane ranges of 112 lanes and a ragged last range of 16 (pitched
+# copies); (3, 5000, 2, 32): two ranges of 32 lanes per entry (6 slices);
+# (2, 333, 3, 16): one slice; (1, 64, 2, 4): one entry.
+@pytest.mark.parametrize("dims", [(6, 8192, 4, 32), (1, 2048, 8, 100), (7, 6000, 4, 32), (3, 5000, 2, 32),
+                                  (2, 333, 3, 16), (1, 64, 2, 4)])
 @pytest.mark.parametrize("pinned", [True, False])
 def test_host_step_matches_oracle(dev, dims, pinned):
     w = workloads.custom("host", *dims, q_kind="rotation", theta_max=0.4, seed=101)
