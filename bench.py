@@ -49,14 +49,15 @@ KERNEL_SOURCES = [os.path.join(ROOT, "quaternion_cumulative_product_gb300", "csr
 
 
 # Forward configurations of the segmented chained walk in the library's table.
-SEGWALK_FWD_VARIANTS = (9, 10, 11)
+SEGWALK_FWD_VARIANTS = (9, 10, 11, 12)
 
 
 def design_name(call: str, kernels: int, variant: int = -1) -> str:
+    if call == "quat_cumprod_fwd" and variant in SEGWALK_FWD_VARIANTS:
+        return f"{call} (segmented chained walk kernel)"
     if kernels != 1:
         return f"{call} (aggregate + carry + apply kernels)"
-    segmented = call == "quat_cumprod_fwd" and variant in SEGWALK_FWD_VARIANTS
-    return f"{call} ({'segmented chained walk kernel' if segmented else 'walk kernel'})"
+    return f"{call} (walk kernel)"
 
 
 def _code_only(text: str) -> str:

@@ -99,6 +99,9 @@ struct Variant {
     // CTAs; `agg` is the kernel (0: another design).
     int segk = 0;
     int extra = 0;   // threads besides the LT * NSEG compute threads (warp-specialised kernels)
+    // Segmented walk whose look-back values carry their own state (reset for
+    // the next launch by the kernel itself; see LbValues).
+    bool sent = false;
 };
 
 #define QS_VARIANT(B, LT, N)                                                                        \
@@ -116,6 +119,11 @@ struct Variant {
     Variant {                                                                                       \
         false, reinterpret_cast<const void *>(qs::quat_segwalk_fwd_kernel<qs::IoF32, LT, NSEG, N, NST, K>), \
             nullptr, false, LT, NSEG, N, qs::segwalk_smem_bytes(LT, NSEG, N, NST), false, 0, K      \
+    }
+#define QS_SEGWALK_SENT_FWD(LT, NSEG, N, NST, K)                                                    \
+    Variant {                                                                                       \
+        false, reinterpret_cast<const void *>(qs::quat_segwalk_fwd_kernel<qs::IoF32, LT, NSEG, N, NST, K, true>), \
+            nullptr, false, LT, NSEG, N, qs::segwalk_smem_bytes(LT, NSEG, N, NST), false, 0, K, 0, true \
     }
 #define QS_SEGWALK_WS_FWD(LT, NSEG, N, NST, K)                                                      \
     Variant {                                                                                       \
@@ -141,6 +149,7 @@ const Variant kFwdVariants[] = {
     QS_SEGWALK_FWD(32, 8, 8, 3, 4),      // 9: segmented chained walk, 32 lanes, segments of 4 x 64 steps
     QS_SEGWALK_WS_FWD(32, 8, 8, 4, 4),   // 10: the same, warp-specialised (producer and look-back warps)
     QS_SEGWALK_WS_FWD(16, 8, 8, 6, 4),   // 11: warp-specialised, 16 lanes, 6 x 16 KiB ring
+    QS_SEGWALK_SENT_FWD(32, 8, 8, 3, 4),   // 12: as 9, one-latency look-back rounds (few lane groups)
 };
 #define QS_WALK_BWD_CAP(LT, NSEG, N, NSTF, NSTB, CAPX4)                                             \
     Variant {                                                                                       \
@@ -188,6 +197,11 @@ const Variant kBwdGiven = Variant{true,
             reinterpret_cast<const void *>(qs::quat_apply_kernel<qs::IoBF16, B, LT, N>), B, LT,     \
             NTHREADS / (LT), N, qs::tile_smem_bytes(B, LT, N, 8)                                    \
     }
+#define QS_SEGWALK_SENT_FWD16(LT, NSEG, N, NST, K)                                                  \
+    Variant {                                                                                       \
+        false, reinterpret_cast<const void *>(qs::quat_segwalk_fwd_kernel<qs::IoBF16, LT, NSEG, N, NST, K, true>), \
+            nullptr, false, LT, NSEG, N, qs::segwalk_smem_bytes(LT, NSEG, N, NST, 8), false, 0, K, 0, true \
+    }
 #define QS_SEGWALK_FWD16(LT, NSEG, N, NST, K)                                                       \
     Variant {                                                                                       \
         false, reinterpret_cast<const void *>(qs::quat_segwalk_fwd_kernel<qs::IoBF16, LT, NSEG, N, NST, K>), \
@@ -200,6 +214,7 @@ const Variant kFwdBf16Variants[] = {
     QS_WALK_FWD16(32, 16, 4, 6),           // 3: 32 lanes x 64 steps (512 threads), 6 x 16 KiB
     QS_VARIANT16(false, 32, 8),            // 4: three kernels, 64-step chunks
     QS_SEGWALK_FWD16(32, 8, 8, 3, 4),      // 5: segmented chained walk (few lane groups)
+    QS_SEGWALK_SENT_FWD16(32, 8, 8, 3, 4), // 6: as 5, one-latency look-back rounds
 };
 const Variant kBwdBf16Variants[] = {
     QS_WALK_BWD16(16, 8, 8, 8, 4, false),  // 0: 16 lanes x 64 steps (128 threads), 64 KiB rings
@@ -210,15 +225,22 @@ const Variant kBwdBf16Variants[] = {
 };
 #undef QS_VARIANT16
 #undef QS_SEGWALK_FWD16
+#undef QS_SEGWALK_SENT_FWD16
 #undef QS_WALK_FWD16
 #undef QS_WALK_BWD16
 constexpr int kNumFwdBf16 = sizeof(kFwdBf16Variants) / sizeof(kFwdBf16Variants[0]);
 constexpr int kFwdBf16Default = 1, kBwdBf16Default = 0;   // walks; fastest measured on 8x4096x16x32
-constexpr int kFwdBf16Few = 5, kBwdBf16Few = 4;       // for too few lane groups (forward: segmented walk)
+// For too few lane groups (forward: segmented walk).  The bf16 forward keeps
+// status words (5): with half the bytes its time is the walk's own latency, and
+// the self-describing look-back values (6) measured 1.5-2.4% slower on
+// 1 x 131072 x 16 x 16, 2 x 65536 x 32 x 32 and 2 x 32768 x 16 x 16 (18%
+// faster on 4 x 8192 x 8 x 16).
+constexpr int kFwdBf16Few = 5, kBwdBf16Few = 4;
 constexpr int kNumBwdBf16 = sizeof(kBwdBf16Variants) / sizeof(kBwdBf16Variants[0]);
 #undef QS_VARIANT
 #undef QS_SEGWALK_FWD
 #undef QS_SEGWALK_WS_FWD
+#undef QS_SEGWALK_SENT_FWD
 #undef QS_WALK_FWD
 #undef QS_WALK_BWD
 #undef QS_WALK_BWD_CAP
@@ -237,11 +259,13 @@ constexpr int kCarryScanLanes = 2;
 // faster than one CTA per group in the hardware's own waves.
 constexpr int kWalkFwd = 4, kWalkBwd = 10, kThreeFwd = 0, kThreeBwd = 0;
 // Forward with too few lane groups for a walk: the segmented chained walk
-// (segments of 4 chunks), measured 10-20% faster than aggregate / carry /
-// apply on 1 x 131072 x 16 x 16, 2 x 65536 x 32 x 32 and 2 x 32768 x 16 x 16.
-// (The warp-specialised configurations are faster on the last two and 2%
-// slower on the first.)
-constexpr int kSegFwd = 9;
+// (segments of 4 chunks) whose look-back values carry their own state, so a
+// look-back round takes one memory latency.  It measured 0.76 / 0.82 / 0.73 of
+// the copy bandwidth on 1 x 131072 x 16 x 16, 2 x 65536 x 32 x 32 and
+// 2 x 32768 x 16 x 16, against 0.71 / 0.73 / 0.68 with status words
+// (configuration 9), 0.68 / 0.81 / 0.70 warp-specialised (configuration 10)
+// and 0.59 / 0.65 / 0.52 for aggregate / carry / apply.
+constexpr int kSegFwd = 12;
 constexpr int kNumFwd = sizeof(kFwdVariants) / sizeof(kFwdVariants[0]);
 constexpr int kNumBwd = sizeof(kBwdVariants) / sizeof(kBwdVariants[0]);
 
@@ -397,9 +421,81 @@ int ensure_workspace(int dev, cudaStream_t stream, size_t need, unsigned char **
     return QS_OK;
 }
 
-// Head of the status-word allocation: the two ticket counters of the
-// segmented chained walk, padded; status words start after it.
+// Head of the status-word allocation: the counters of the segmented chained
+// walk (tickets taken, CTAs finished, units done), padded; status words start
+// after it.
 constexpr size_t kFlagsHead = 256;
+
+// Look-back values of the segmented walk that carry their own state (Variant
+// `sent`): per (device, stream) an allocation no other kernel writes, holding
+// two pairs of buffers (segment products, inclusive values) of `n` entries.
+// A launch reads the pair `next` and resets the other one for the launch
+// after it; the host clears both when the entry layout changes (and when the
+// allocation is new, or a launch failed to be enqueued).
+struct LbValues {
+    unsigned char *base = nullptr;
+    size_t bytes = 0;
+    long long n = -1;   // entries per buffer of the layout the buffers are clean for; -1: none
+    int next = 0;       // the pair the next launch reads
+};
+std::map<std::pair<int, uintptr_t>, LbValues> g_lbv;
+
+// The pair of buffers a launch of `n` entries reads (agg, incl) and the pair
+// it resets (agg_next, incl_next); enqueues the clearing memset if needed.
+int lb_values(int dev, cudaStream_t stream, long long n, float4 **agg, float4 **incl, float4 **agg_next,
+              float4 **incl_next) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    LbValues &w = g_lbv[{dev, reinterpret_cast<uintptr_t>(stream)}];
+    const size_t arr = align_up((size_t)n * 16, 256), need = 4 * arr;
+    if (w.bytes < need) {
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) {
+            cudaGetLastError();
+            return QS_ERR_CUDA;
+        }
+        if (cs != cudaStreamCaptureStatusNone) return QS_ERR_NOMEM;
+        if (w.base) {
+            if (cudaStreamSynchronize(stream) != cudaSuccess) {
+                cudaGetLastError();
+                return QS_ERR_CUDA;
+            }
+            cudaFree(w.base);
+            w.base = nullptr;
+            w.bytes = 0;
+        }
+        const size_t bytes = align_up(need + need / 4, 1 << 20);
+        void *p = nullptr;
+        if (cudaMalloc(&p, bytes) != cudaSuccess) {
+            cudaGetLastError();
+            return QS_ERR_NOMEM;
+        }
+        w.base = static_cast<unsigned char *>(p);
+        w.bytes = bytes;
+        w.n = -1;
+    }
+    if (w.n != n) {
+        if (cudaMemsetAsync(w.base, 0xff, need, stream) != cudaSuccess) {
+            cudaGetLastError();
+            w.n = -1;
+            return QS_ERR_CUDA;
+        }
+        w.n = n;
+        w.next = 0;
+    }
+    const int b = w.next;
+    *agg = reinterpret_cast<float4 *>(w.base + (size_t)(2 * b) * arr);
+    *incl = reinterpret_cast<float4 *>(w.base + (size_t)(2 * b + 1) * arr);
+    *agg_next = reinterpret_cast<float4 *>(w.base + (size_t)(2 * (b ^ 1)) * arr);
+    *incl_next = reinterpret_cast<float4 *>(w.base + (size_t)(2 * (b ^ 1) + 1) * arr);
+    w.next = b ^ 1;
+    return QS_OK;
+}
+
+// After a launch that was not enqueued: the next one starts from cleared buffers.
+void lb_values_invalidate(int dev, cudaStream_t stream) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    g_lbv[{dev, reinterpret_cast<uintptr_t>(stream)}].n = -1;
+}
 
 // CTAs of a persistent kernel: as many as are resident at once on the device
 // (per (device, kernel), computed once).
@@ -675,14 +771,21 @@ int launch(bool bwd, const void *q, const void *d_cum, void *out, const void *in
         ctl.hdr = reinterpret_cast<qs::WsHeader *>(ws);
         const void *init4 = init;
         void *out4 = out;
-        unsigned int *tickets = flags;   // two counters, zero between launches
+        unsigned int *tickets = flags;   // counters, zero between launches
         uint32_t *status = flags + kFlagsHead / 4;
         float4 *aggv = reinterpret_cast<float4 *>(ws + pl.o_W);
         float4 *inclv = reinterpret_cast<float4 *>(ws + pl.o_F);
-        void *args[] = {&qmap, &init4, &out4, &status, &tickets, &aggv, &inclv, &pl.geo, &ctl, &epoch};
+        float4 *agg_next = nullptr, *incl_next = nullptr;
+        if (pl.v->sent) {
+            rc = lb_values(dev, stream, units * pl.v->lt, &aggv, &inclv, &agg_next, &incl_next);
+            if (rc != QS_OK) return rc;
+        }
+        void *args[] = {&qmap, &init4, &out4, &status, &tickets, &aggv, &inclv, &agg_next, &incl_next,
+                        &pl.geo, &ctl, &epoch};
         if (cudaLaunchKernel(pl.v->agg, dim3((unsigned)grid), dim3(pl.v->threads()), args, pl.v->smem(), stream) !=
             cudaSuccess) {
             cudaGetLastError();
+            if (pl.v->sent) lb_values_invalidate(dev, stream);
             return QS_ERR_CUDA;
         }
         return QS_OK;

@@ -38,12 +38,35 @@ namespace qs {
 // one per lane and unit.  A unit whose wait ran out still publishes (NaN).
 // ---------------------------------------------------------------------------
 
-template <typename IO, int LT, int NSEG, int N, int NST, int K>
+// A value the look-back reads is published once none of its four words holds
+// the all-ones pattern the arrays are reset to before each launch (SENT);
+// arithmetic never yields that pattern (a NaN result is the canonical one).
+__device__ __forceinline__ bool lb_published(const float4 v) {
+    return __float_as_uint(v.x) != 0xffffffffu && __float_as_uint(v.y) != 0xffffffffu &&
+           __float_as_uint(v.z) != 0xffffffffu && __float_as_uint(v.w) != 0xffffffffu;
+}
+
+// SENT: the segment products and inclusive values carry their own state: a
+// launch reads buffers (agg, incl) that hold all-ones bits wherever nothing is
+// published yet, so a look-back round loads the predecessors' products and
+// inclusive values together (one memory latency) and the status words go
+// unused.  Each unit, once published, resets its entries of the other pair of
+// buffers (agg_next, incl_next), which the next launch reads; if a wait ran
+// out and units were left undone, the last CTA resets all of them.  Otherwise
+// the values are published behind epoch-tagged status words (two latencies
+// per round) and agg_next / incl_next are unused.
+__device__ __forceinline__ float4 lb_unpublished() {
+    const float n = __uint_as_float(0xffffffffu);
+    return make_float4(n, n, n, n);
+}
+
+template <typename IO, int LT, int NSEG, int N, int NST, int K, bool SENT = false>
 __global__ void __launch_bounds__(LT *NSEG)
     quat_segwalk_fwd_kernel(const __grid_constant__ CUtensorMap qmap, const typename IO::elem *__restrict__ init,
                             typename IO::elem *__restrict__ out, uint32_t *__restrict__ flags,
                             unsigned int *__restrict__ ctr, float4 *__restrict__ agg,
-                            float4 *__restrict__ incl, const Geometry geo, const Control ctl, uint32_t epoch) {
+                            float4 *__restrict__ incl, float4 *__restrict__ agg_next, float4 *__restrict__ incl_next,
+                            const Geometry geo, const Control ctl, uint32_t epoch) {
     using E = typename IO::elem;
     constexpr int T = NSEG * N;
     constexpr int NT = LT * NSEG;
@@ -163,7 +186,7 @@ __global__ void __launch_bounds__(LT *NSEG)
             if (seg == 0 && lane_ok) acc = IO::get(init[static_cast<long long>(b) * geo.HJ + hj]);
         } else if (seg == 0) {   // the product first: later segments can use it before the carry is known
             __stcg(agg + me, A);
-            st_release_u32(flags + me, tag | CH_AGG);
+            if constexpr (!SENT) st_release_u32(flags + me, tag | CH_AGG);
         }
         // acc = A_{p-1} (x) A_{p-2} (x) ... (x) incl.  Per round the NSEG
         // segment threads of a lane take LB predecessors each (segment k:
@@ -174,54 +197,100 @@ __global__ void __launch_bounds__(LT *NSEG)
         constexpr int LB = 4;
         if (p > 0) {
             for (int base = p - 1;; base -= NSEG * LB) {
-                uint32_t f[LB];
-                long long idx[LB];
-#pragma unroll
-                for (int j = 0; j < LB; ++j) {
-                    const int pp = base - seg * LB - j;
-                    idx[j] = (static_cast<long long>(pp < 0 ? 0 : pp) * NG + g) * LT + lane;
-                    // before segment 0 there is nothing to fold: an inclusive identity
-                    f[j] = pp < 0 ? (tag | CH_INCL) : ld_acquire_u32(flags + idx[j]);
-                }
-                bool lost = false;
-#pragma unroll
-                for (int j = 0; j < LB; ++j) {
-                    if ((f[j] & ~3u) == tag || lost) continue;
-                    const unsigned long long t0 = global_timer_ns();
-                    do {
-                        if (global_timer_ns() - t0 > ctl.timeout_ns) {
-                            record_error(ctl.hdr, c0 * NG + g);
-                            lost = true;
-                            break;
-                        }
-                        f[j] = ld_acquire_u32(flags + idx[j]);
-                    } while ((f[j] & ~3u) != tag);
-                }
                 float4 part = q_ident();
                 uint32_t pst = 0;   // CH_INCL once the fold reached an inclusive value
-                if (lost) {
-                    part = q_nan();
-                    pst = CH_INCL;
-                } else {
-                    float4 v[LB];
-                    bool stop = false;
+                if constexpr (SENT) {
+                    float4 av[LB], iv[LB];
+                    long long idx[LB];
+                    bool real[LB];
 #pragma unroll
-                    for (int j = 0; j < LB; ++j) {   // the values to fold, loaded together
-                        const bool use = !stop;
-                        const bool inc = (f[j] & 3u) == CH_INCL;
-                        const bool real = base - seg * LB - j >= 0;
-                        v[j] = q_ident();
-                        if (use && real) v[j] = inc ? __ldcg(incl + idx[j]) : __ldcg(agg + idx[j]);
-                        stop = stop || inc;
+                    for (int j = 0; j < LB; ++j) {   // products and inclusive values, loaded together
+                        const int pp = base - seg * LB - j;
+                        real[j] = pp >= 0;
+                        idx[j] = (static_cast<long long>(pp < 0 ? 0 : pp) * NG + g) * LT + lane;
+                        av[j] = q_ident();
+                        iv[j] = q_ident();   // before segment 0: an inclusive identity
+                        if (real[j]) {
+                            av[j] = __ldcg(agg + idx[j]);
+                            iv[j] = __ldcg(incl + idx[j]);
+                        }
                     }
-                    stop = false;
+                    bool lost = false, stop = false;
 #pragma unroll
                     for (int j = 0; j < LB; ++j) {
                         if (stop) break;
-                        part = q_mul(part, v[j]);
-                        if ((f[j] & 3u) == CH_INCL) {
+                        if (real[j] && !lb_published(iv[j]) && !lb_published(av[j]) && !lost) {
+                            const unsigned long long t0 = global_timer_ns();
+                            do {
+                                if (global_timer_ns() - t0 > ctl.timeout_ns) {
+                                    record_error(ctl.hdr, c0 * NG + g);
+                                    lost = true;
+                                    break;
+                                }
+                                av[j] = __ldcg(agg + idx[j]);
+                                iv[j] = __ldcg(incl + idx[j]);
+                            } while (!lb_published(iv[j]) && !lb_published(av[j]));
+                        }
+                        if (lost) {
+                            part = q_nan();
                             pst = CH_INCL;
                             stop = true;
+                        } else if (!real[j] || lb_published(iv[j])) {
+                            part = q_mul(part, iv[j]);
+                            pst = CH_INCL;
+                            stop = true;
+                        } else {
+                            part = q_mul(part, av[j]);
+                        }
+                    }
+                } else {
+                    uint32_t f[LB];
+                    long long idx[LB];
+#pragma unroll
+                    for (int j = 0; j < LB; ++j) {
+                        const int pp = base - seg * LB - j;
+                        idx[j] = (static_cast<long long>(pp < 0 ? 0 : pp) * NG + g) * LT + lane;
+                        // before segment 0 there is nothing to fold: an inclusive identity
+                        f[j] = pp < 0 ? (tag | CH_INCL) : ld_acquire_u32(flags + idx[j]);
+                    }
+                    bool lost = false;
+#pragma unroll
+                    for (int j = 0; j < LB; ++j) {
+                        if ((f[j] & ~3u) == tag || lost) continue;
+                        const unsigned long long t0 = global_timer_ns();
+                        do {
+                            if (global_timer_ns() - t0 > ctl.timeout_ns) {
+                                record_error(ctl.hdr, c0 * NG + g);
+                                lost = true;
+                                break;
+                            }
+                            f[j] = ld_acquire_u32(flags + idx[j]);
+                        } while ((f[j] & ~3u) != tag);
+                    }
+                    if (lost) {
+                        part = q_nan();
+                        pst = CH_INCL;
+                    } else {
+                        float4 v[LB];
+                        bool stop = false;
+#pragma unroll
+                        for (int j = 0; j < LB; ++j) {   // the values to fold, loaded together
+                            const bool use = !stop;
+                            const bool inc = (f[j] & 3u) == CH_INCL;
+                            const bool real = base - seg * LB - j >= 0;
+                            v[j] = q_ident();
+                            if (use && real) v[j] = inc ? __ldcg(incl + idx[j]) : __ldcg(agg + idx[j]);
+                            stop = stop || inc;
+                        }
+                        stop = false;
+#pragma unroll
+                        for (int j = 0; j < LB; ++j) {
+                            if (stop) break;
+                            part = q_mul(part, v[j]);
+                            if ((f[j] & 3u) == CH_INCL) {
+                                pst = CH_INCL;
+                                stop = true;
+                            }
                         }
                     }
                 }
@@ -243,7 +312,11 @@ __global__ void __launch_bounds__(LT *NSEG)
         }
         if (seg == 0) {
             __stcg(incl + me, q_mul(A, acc));
-            st_release_u32(flags + me, tag | CH_INCL);
+            if constexpr (!SENT) st_release_u32(flags + me, tag | CH_INCL);
+            if constexpr (SENT) {   // this unit's entries of the next launch's buffers
+                __stcg(agg_next + me, lb_unpublished());
+                __stcg(incl_next + me, lb_unpublished());
+            }
             s_x[it & 1][lane] = acc;   // carry into the first item of the second walk
         }
         __syncthreads();
@@ -290,15 +363,34 @@ __global__ void __launch_bounds__(LT *NSEG)
                     if (t0 + kk < geo.S) __stcs(dst + static_cast<long long>(kk) * geo.HJ, IO::put(q_mul(x[kk], Y)));
             }
         }
-        if (tid == 0) s_unit[k % NU] = -1;   // (the producer is fewer than NU units ahead)
+        if (tid == 0) {
+            s_unit[k % NU] = -1;   // (the producer is fewer than NU units ahead)
+            if constexpr (SENT) atomicAdd(ctr + 2, 1u);   // units done
+        }
         __syncthreads();   // the unit's shared slots are read before the next unit writes them
     }
     if (s_broken) drain_ring<NST>(full, issued, ctl);
-    if (tid == 0) {   // the last CTA to finish resets the ticket counters for the next launch
+    // The last CTA to finish resets the counters for the next launch (and,
+    // SENT, the next buffers if units were left undone).
+    __shared__ int s_last, s_short;
+    if (tid == 0) {
         __threadfence();
-        if (atomicAdd(ctr + 1, 1u) == gridDim.x - 1) {
+        s_last = atomicAdd(ctr + 1, 1u) == gridDim.x - 1;
+        s_short = s_last && atomicAdd(ctr + 2, 0u) != static_cast<unsigned int>(U);
+    }
+    __syncthreads();
+    if (s_last) {
+        if (SENT && s_short) {
+            const long long n = static_cast<long long>(U) * LT;
+            for (long long i = tid; i < n; i += NT) {
+                __stcg(agg_next + i, lb_unpublished());
+                __stcg(incl_next + i, lb_unpublished());
+            }
+        }
+        if (tid == 0) {
             atomicExch(ctr, 0u);
             atomicExch(ctr + 1, 0u);
+            atomicExch(ctr + 2, 0u);
         }
     }
 }

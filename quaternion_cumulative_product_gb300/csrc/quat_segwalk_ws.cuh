@@ -59,7 +59,9 @@ __global__ void __launch_bounds__(LT *NSEG + 64)
     quat_segwalk_ws_fwd_kernel(const __grid_constant__ CUtensorMap qmap, const typename IO::elem *__restrict__ init,
                                typename IO::elem *__restrict__ out, uint32_t *__restrict__ flags,
                                unsigned int *__restrict__ ctr, float4 *__restrict__ agg,
-                               float4 *__restrict__ incl, const Geometry geo, const Control ctl, uint32_t epoch) {
+                               float4 *__restrict__ incl, float4 *__restrict__ /*agg_next*/,
+                               float4 *__restrict__ /*incl_next*/, const Geometry geo, const Control ctl,
+                               uint32_t epoch) {
     using E = typename IO::elem;
     constexpr int T = NSEG * N;
     constexpr int NT = LT * NSEG;   // compute threads

@@ -101,3 +101,11 @@ def test_source_hash_ignores_comments_and_blank_lines():
     import bench
     assert bench._code_only("a = 1; // note\n\n/* block\n comment */ b = 2;\n") == "a = 1;\n b = 2;"
     assert bench._code_only("x\n// only a comment\ny") == "x\ny"
+
+
+def test_design_names_follow_the_plan():
+    """The forward for few lane groups is one segmented-walk kernel."""
+    assert bench.design_name("quat_cumprod_fwd", 1, 12) == "quat_cumprod_fwd (segmented chained walk kernel)"
+    assert bench.design_name("quat_cumprod_fwd", 1, 9) == "quat_cumprod_fwd (segmented chained walk kernel)"
+    assert bench.design_name("quat_cumprod_bwd", 3, 0) == "quat_cumprod_bwd (aggregate + carry + apply kernels)"
+    assert bench.design_name("quat_cumprod_fwd", 1, 4) == "quat_cumprod_fwd (walk kernel)"

@@ -181,10 +181,10 @@ def test_empty_sizes(dev):
 
 # Variants 0-3: aggregate / carry / apply kernels; the rest: walk kernels
 # (forward 8: chained scan; 9: segmented chained walk; 10, 11: the same,
-# warp-specialised; backward 10: at most two CTAs per SM, more lane groups in
-# waves).
-N_FWD_VARIANTS, N_BWD_VARIANTS = 12, 11
-SEGWALK_FWD = [9, 10, 11]
+# warp-specialised; 12: as 9, look-back values that carry their own state, read
+# in one round trip; backward 10: at most two CTAs per SM, more lane groups in waves).
+N_FWD_VARIANTS, N_BWD_VARIANTS = 13, 11
+SEGWALK_FWD = [9, 10, 11, 12]
 
 
 @pytest.mark.parametrize("variant", range(max(N_FWD_VARIANTS, N_BWD_VARIANTS)))
@@ -275,7 +275,25 @@ def test_segmented_walk_long_sequences(dev, variant, dims):
         assert_parity(cum.cpu().numpy(), oracle.fwd(q, init), "cum")
 
 
-@pytest.mark.parametrize("variant", [9, 10])   # one CTA role for all, warp-specialised
+def test_segmented_walk_alternating_layouts(dev):
+    """Configuration 12 keeps its look-back values between launches on a stream
+    (two buffers, each launch resetting the one the next reads): shapes that
+    alternate change the layout, repeats reuse it, and every result must match."""
+    lib = qs.load_library()
+    assert lib.quat_cumprod_debug_set_variant(12, -1) == qs.QS_OK
+    cases = []
+    for i, dims in enumerate([(1, 20000, 1, 3), (2, 17000, 2, 5), (1, 9000, 2, 16)]):
+        w = workloads.custom("seg_alt", *dims, q_kind="rotation", theta_max=0.3, seed=110 + i)
+        q, init, _ = workloads.make_inputs(w)
+        cases.append((q, init, oracle.fwd(q, init)))
+    for k in [0, 0, 1, 0, 2, 2, 2, 1, 1, 0]:
+        q, init, ref = cases[k]
+        cum = qs.quat_cumprod_fwd(*(torch.from_numpy(a).to(dev) for a in (q, init)))
+        assert qs.quat_cumprod_status(device=dev) == qs.QS_OK
+        assert_parity(cum.cpu().numpy(), ref, f"cum (case {k})")
+
+
+@pytest.mark.parametrize("variant", [9, 10, 12])   # one CTA role for all, warp-specialised, self-describing values
 def test_segmented_walk_stall_reports_timeout_then_recovers(dev, variant):
     lib = qs.load_library()
     assert lib.quat_cumprod_debug_set_variant(variant, -1) == qs.QS_OK
