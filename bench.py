@@ -49,7 +49,7 @@ KERNEL_SOURCES = [os.path.join(ROOT, "quaternion_cumulative_product_gb300", "csr
 
 
 # Forward configurations of the segmented chained walk in the library's table.
-SEGWALK_FWD_VARIANTS = (9, 10, 11, 12)
+SEGWALK_FWD_VARIANTS = (9, 10, 11, 12, 13, 14)
 
 
 def design_name(call: str, kernels: int, variant: int = -1) -> str:

@@ -125,6 +125,11 @@ struct Variant {
         false, reinterpret_cast<const void *>(qs::quat_segwalk_fwd_kernel<qs::IoF32, LT, NSEG, N, NST, K, true>), \
             nullptr, false, LT, NSEG, N, qs::segwalk_smem_bytes(LT, NSEG, N, NST), false, 0, K, 0, true \
     }
+#define QS_SEGWALK_WS_SENT_FWD(LT, NSEG, N, NST, K)                                                 \
+    Variant {                                                                                       \
+        false, reinterpret_cast<const void *>(qs::quat_segwalk_ws_fwd_kernel<qs::IoF32, LT, NSEG, N, NST, K, true>), \
+            nullptr, false, LT, NSEG, N, qs::segwalk_smem_bytes(LT, NSEG, N, NST), false, 0, K, 64, true \
+    }
 #define QS_SEGWALK_WS_FWD(LT, NSEG, N, NST, K)                                                      \
     Variant {                                                                                       \
         false, reinterpret_cast<const void *>(qs::quat_segwalk_ws_fwd_kernel<qs::IoF32, LT, NSEG, N, NST, K>), \
@@ -150,6 +155,8 @@ const Variant kFwdVariants[] = {
     QS_SEGWALK_WS_FWD(32, 8, 8, 4, 4),   // 10: the same, warp-specialised (producer and look-back warps)
     QS_SEGWALK_WS_FWD(16, 8, 8, 6, 4),   // 11: warp-specialised, 16 lanes, 6 x 16 KiB ring
     QS_SEGWALK_SENT_FWD(32, 8, 8, 3, 4),   // 12: as 9, one-latency look-back rounds (few lane groups)
+    QS_SEGWALK_WS_SENT_FWD(32, 8, 8, 4, 4),   // 13: as 10, one-latency look-back rounds
+    QS_SEGWALK_WS_SENT_FWD(16, 8, 8, 6, 4),   // 14: as 11, one-latency look-back rounds
 };
 #define QS_WALK_BWD_CAP(LT, NSEG, N, NSTF, NSTB, CAPX4)                                             \
     Variant {                                                                                       \
@@ -241,6 +248,7 @@ constexpr int kNumBwdBf16 = sizeof(kBwdBf16Variants) / sizeof(kBwdBf16Variants[0
 #undef QS_SEGWALK_FWD
 #undef QS_SEGWALK_WS_FWD
 #undef QS_SEGWALK_SENT_FWD
+#undef QS_SEGWALK_WS_SENT_FWD
 #undef QS_WALK_FWD
 #undef QS_WALK_BWD
 #undef QS_WALK_BWD_CAP
@@ -266,6 +274,11 @@ constexpr int kWalkFwd = 4, kWalkBwd = 10, kThreeFwd = 0, kThreeBwd = 0;
 // (configuration 9), 0.68 / 0.81 / 0.70 warp-specialised (configuration 10)
 // and 0.59 / 0.65 / 0.52 for aggregate / carry / apply.
 constexpr int kSegFwd = 12;
+// From 2^24 elements on, the warp-specialised form with the same values (16
+// lanes, 6-stage ring) measured faster: 0.79 / 0.84 / 0.73-0.74 on the three
+// shapes above; on 4 x 8192 x 8 x 16 it measured 0.50 against 0.53.
+constexpr int kSegFwdLarge = 14;
+constexpr long long kSegFwdLargeElements = 1ll << 24;
 constexpr int kNumFwd = sizeof(kFwdVariants) / sizeof(kFwdVariants[0]);
 constexpr int kNumBwd = sizeof(kBwdVariants) / sizeof(kBwdVariants[0]);
 
@@ -584,7 +597,7 @@ int make_map(CUtensorMap *m, const void *ptr, int64_t B, int64_t S, int64_t HJ, 
     return r == CUDA_SUCCESS ? QS_OK : QS_ERR_CUDA;
 }
 
-int pick_variant(bool bwd, int64_t B, int64_t HJ, int sms) {
+int pick_variant(bool bwd, int64_t B, int64_t S, int64_t HJ, int sms) {
     {
         std::lock_guard<std::mutex> lk(g_mu);
         const int forced = bwd ? g_bwd_variant : g_fwd_variant;
@@ -594,7 +607,8 @@ int pick_variant(bool bwd, int64_t B, int64_t HJ, int sms) {
     const long long groups = (long long)B * ((HJ + w.lt - 1) / w.lt);
     const long long need = bwd ? 3ll * sms / 2 : 3ll * sms / 4;
     if (groups >= need) return bwd ? kWalkBwd : kWalkFwd;
-    return bwd ? kThreeBwd : kSegFwd;
+    if (bwd) return kThreeBwd;
+    return (long long)B * S * HJ >= kSegFwdLargeElements ? kSegFwdLarge : kSegFwd;
 }
 
 // Everything a call needs, derived from the sizes alone (no device calls).
@@ -634,7 +648,7 @@ int make_plan(bool bwd, int64_t B, int64_t S, int64_t HJ, int sms, Plan *pl, Mod
             vi = groups >= need ? wi : (bwd ? kBwdBf16Few : kFwdBf16Few);
         }
     } else {
-        vi = pick_variant(bwd, B, HJ, sms);
+        vi = pick_variant(bwd, B, S, HJ, sms);
     }
     const Variant *v = bf16 ? (bwd ? &kBwdBf16Variants[vi] : &kFwdBf16Variants[vi])
                             : bwd ? &kBwdVariants[vi] : &kFwdVariants[vi];

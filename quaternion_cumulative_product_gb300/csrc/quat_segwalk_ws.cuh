@@ -54,13 +54,55 @@ __device__ __forceinline__ void compute_sync() {
     asm volatile("bar.sync 1, %0;" ::"n"(NT) : "memory");
 }
 
-template <typename IO, int LT, int NSEG, int N, int NST, int K>
+// The carry entering segment p of lane group g for one lane, from look-back
+// values that carry their own state (see quat_segwalk_fwd_kernel, SENT): per
+// round the LB predecessors' products and inclusive values are loaded
+// together, one memory latency.  NaN if a wait ran out (recorded as `item`).
+template <int LB>
+__device__ __forceinline__ float4 segment_lookback_values(const float4 *agg, const float4 *incl, int p, int g, int NG,
+                                                          int LT, int lane, const Control &ctl, int item) {
+    float4 acc = q_ident();
+    for (int base = p - 1;; base -= LB) {
+        float4 av[LB], iv[LB];
+        long long idx[LB];
+#pragma unroll
+        for (int j = 0; j < LB; ++j) {
+            const int pp = base - j;
+            idx[j] = (static_cast<long long>(pp < 0 ? 0 : pp) * NG + g) * LT + lane;
+            av[j] = q_ident();
+            iv[j] = q_ident();
+            if (pp >= 0) {
+                av[j] = __ldcg(agg + idx[j]);
+                iv[j] = __ldcg(incl + idx[j]);
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < LB; ++j) {
+            if (base - j < 0) return acc;   // before segment 0: an inclusive identity
+            if (!lb_published(iv[j]) && !lb_published(av[j])) {
+                const unsigned long long t0 = global_timer_ns();
+                do {
+                    if (global_timer_ns() - t0 > ctl.timeout_ns) {
+                        record_error(ctl.hdr, item);
+                        return q_nan();
+                    }
+                    av[j] = __ldcg(agg + idx[j]);
+                    iv[j] = __ldcg(incl + idx[j]);
+                } while (!lb_published(iv[j]) && !lb_published(av[j]));
+            }
+            if (lb_published(iv[j])) return q_mul(acc, iv[j]);
+            acc = q_mul(acc, av[j]);
+        }
+    }
+}
+
+template <typename IO, int LT, int NSEG, int N, int NST, int K, bool SENT = false>
 __global__ void __launch_bounds__(LT *NSEG + 64)
     quat_segwalk_ws_fwd_kernel(const __grid_constant__ CUtensorMap qmap, const typename IO::elem *__restrict__ init,
                                typename IO::elem *__restrict__ out, uint32_t *__restrict__ flags,
                                unsigned int *__restrict__ ctr, float4 *__restrict__ agg,
-                               float4 *__restrict__ incl, float4 *__restrict__ /*agg_next*/,
-                               float4 *__restrict__ /*incl_next*/, const Geometry geo, const Control ctl,
+                               float4 *__restrict__ incl, float4 *__restrict__ agg_next,
+                               float4 *__restrict__ incl_next, const Geometry geo, const Control ctl,
                                uint32_t epoch) {
     using E = typename IO::elem;
     constexpr int T = NSEG * N;
@@ -122,6 +164,9 @@ __global__ void __launch_bounds__(LT *NSEG + 64)
                 float4 acc = q_ident();
                 if (p == 0) {
                     if (hj < geo.HJ) acc = IO::get(init[static_cast<long long>(b) * geo.HJ + hj]);
+                } else if constexpr (SENT) {
+                    __stcg(agg + me, A);   // the product first: later segments can use it now
+                    acc = segment_lookback_values<8>(agg, incl, p, g, NG, LT, lane, ctl, p * K * NG + g);
                 } else {
                     __stcg(agg + me, A);   // the product first: later segments can use it now
                     st_release_u32(flags + me, tag | CH_AGG);
@@ -174,11 +219,19 @@ __global__ void __launch_bounds__(LT *NSEG + 64)
                     }
                 }
                 __stcg(incl + me, q_mul(A, acc));
-                st_release_u32(flags + me, tag | CH_INCL);
+                if constexpr (SENT) {   // this unit's entries of the next launch's buffers
+                    __stcg(agg_next + me, lb_unpublished());
+                    __stcg(incl_next + me, lb_unpublished());
+                } else {
+                    st_release_u32(flags + me, tag | CH_INCL);
+                }
                 s_X[k & 1][lane] = acc;
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(&carry_ready[k & 1]);
+            if (lane == 0) {
+                mbar_arrive(&carry_ready[k & 1]);
+                if constexpr (SENT) atomicAdd(ctr + 2, 1u);   // units done
+            }
         }
     } else if (tid >= NT) {
         // ======================= producer warp ================================
@@ -352,11 +405,27 @@ __global__ void __launch_bounds__(LT *NSEG + 64)
         }
     }
     __syncthreads();
-    if (tid == 0) {   // the last CTA to finish resets the ticket counters for the next launch
+    // The last CTA to finish resets the counters for the next launch (and,
+    // SENT, the next buffers if units were left undone).
+    __shared__ int s_last, s_short;
+    if (tid == 0) {
         __threadfence();
-        if (atomicAdd(ctr + 1, 1u) == gridDim.x - 1) {
+        s_last = atomicAdd(ctr + 1, 1u) == gridDim.x - 1;
+        s_short = s_last && atomicAdd(ctr + 2, 0u) != static_cast<unsigned int>(U);
+    }
+    __syncthreads();
+    if (s_last) {
+        if (SENT && s_short) {
+            const long long n = static_cast<long long>(U) * LT;
+            for (long long i = tid; i < n; i += static_cast<long long>(blockDim.x)) {
+                __stcg(agg_next + i, lb_unpublished());
+                __stcg(incl_next + i, lb_unpublished());
+            }
+        }
+        if (tid == 0) {
             atomicExch(ctr, 0u);
             atomicExch(ctr + 1, 0u);
+            atomicExch(ctr + 2, 0u);
         }
     }
 }

@@ -182,9 +182,10 @@ def test_empty_sizes(dev):
 # Variants 0-3: aggregate / carry / apply kernels; the rest: walk kernels
 # (forward 8: chained scan; 9: segmented chained walk; 10, 11: the same,
 # warp-specialised; 12: as 9, look-back values that carry their own state, read
-# in one round trip; backward 10: at most two CTAs per SM, more lane groups in waves).
-N_FWD_VARIANTS, N_BWD_VARIANTS = 13, 11
-SEGWALK_FWD = [9, 10, 11, 12]
+# in one round trip; 13, 14: as 10, 11 with those values; backward 10: at most
+# two CTAs per SM, more lane groups in waves).
+N_FWD_VARIANTS, N_BWD_VARIANTS = 15, 11
+SEGWALK_FWD = [9, 10, 11, 12, 13, 14]
 
 
 @pytest.mark.parametrize("variant", range(max(N_FWD_VARIANTS, N_BWD_VARIANTS)))
@@ -293,7 +294,7 @@ def test_segmented_walk_alternating_layouts(dev):
         assert_parity(cum.cpu().numpy(), ref, f"cum (case {k})")
 
 
-@pytest.mark.parametrize("variant", [9, 10, 12])   # one CTA role for all, warp-specialised, self-describing values
+@pytest.mark.parametrize("variant", [9, 10, 12, 13])   # one CTA role, warp-specialised, each with self-describing values
 def test_segmented_walk_stall_reports_timeout_then_recovers(dev, variant):
     lib = qs.load_library()
     assert lib.quat_cumprod_debug_set_variant(variant, -1) == qs.QS_OK
