@@ -331,19 +331,26 @@ __global__ void __launch_bounds__(LT *NSEG)
                     const float sg = back ? -1.f : 1.f;
                     float4(*out)[LT] = back ? s_h : s_x;
                     float4 y = back ? Hc : F;
-                    int idx = back ? NSEG - 1 : 0;
                     const int step = back ? -1 : 1;
+                    // Every step's operands are loaded before the chain starts, so
+                    // no shared-memory latency sits between two of its steps.
+                    float4 Ak[NSEG], Qk[NSEG];
+                    int idx = back ? NSEG - 1 : 0;
 #pragma unroll
                     for (int k = 0; k < NSEG; ++k, idx += step) {
-                        out[idx][lane] = y;
                         float4 A = s_a[sl][idx][lane];
                         const float4 Wk = s_w[0][idx][lane];
                         A.y *= sg;
                         A.z *= sg;
                         A.w *= sg;
-                        const float4 Q = make_float4(back ? Wk.x : 0.f, back ? Wk.y : 0.f, back ? Wk.z : 0.f,
-                                                     back ? Wk.w : 0.f);
-                        y = q_fma(Q, A, y);
+                        Ak[k] = A;
+                        Qk[k] = make_float4(back ? Wk.x : 0.f, back ? Wk.y : 0.f, back ? Wk.z : 0.f, back ? Wk.w : 0.f);
+                    }
+                    idx = back ? NSEG - 1 : 0;
+#pragma unroll
+                    for (int k = 0; k < NSEG; ++k, idx += step) {
+                        out[idx][lane] = y;
+                        y = q_fma(Qk[k], Ak[k], y);
                     }
                     if (back) {
                         Hc = y;
