@@ -198,6 +198,13 @@ const Variant kBwdGiven = Variant{true,
                 qs::quat_walk_bwd_kernel<qs::IoBF16, LT, NSEG, N, NSTF, NSTB, SELF, false>),        \
             nullptr, true, LT, NSEG, N, qs::walk_bwd_smem_bytes(LT, NSEG, N, NSTF, NSTB, 8)         \
     }
+#define QS_WALK_BWD16_MINB(LT, NSEG, N, NSTF, NSTB, MINB)                                           \
+    Variant {                                                                                       \
+        true,                                                                                       \
+            reinterpret_cast<const void *>(                                                         \
+                qs::quat_walk_bwd_kernel<qs::IoBF16, LT, NSEG, N, NSTF, NSTB, false, false, MINB>), \
+            nullptr, true, LT, NSEG, N, qs::walk_bwd_smem_bytes(LT, NSEG, N, NSTF, NSTB, 8)         \
+    }
 #define QS_VARIANT16(B, LT, N)                                                                      \
     Variant {                                                                                       \
         false, reinterpret_cast<const void *>(qs::quat_agg_kernel<qs::IoBF16, B, LT, N>),           \
@@ -229,12 +236,14 @@ const Variant kBwdBf16Variants[] = {
     QS_WALK_BWD16(16, 16, 4, 8, 4, false), // 2: 16 lanes x 64 steps (256 threads), 64 KiB rings
     QS_WALK_BWD16(32, 8, 8, 8, 4, false),  // 3: 32 lanes x 64 steps (256 threads), 128 KiB rings
     QS_VARIANT16(true, 32, 8),             // 4: three kernels, 64-step chunks (few lane groups)
+    QS_WALK_BWD16_MINB(16, 8, 8, 8, 4, 3), // 5: as 0, registers capped for 3 CTAs per SM (many lane groups)
 };
 #undef QS_VARIANT16
 #undef QS_SEGWALK_FWD16
 #undef QS_SEGWALK_SENT_FWD16
 #undef QS_WALK_FWD16
 #undef QS_WALK_BWD16
+#undef QS_WALK_BWD16_MINB
 constexpr int kNumFwdBf16 = sizeof(kFwdBf16Variants) / sizeof(kFwdBf16Variants[0]);
 constexpr int kFwdBf16Default = 1, kBwdBf16Default = 0;   // walks; fastest measured on 8x4096x16x32
 // For too few lane groups (forward: segmented walk).  The bf16 forward keeps
@@ -243,6 +252,11 @@ constexpr int kFwdBf16Default = 1, kBwdBf16Default = 0;   // walks; fastest meas
 // 1 x 131072 x 16 x 16, 2 x 65536 x 32 x 32 and 2 x 32768 x 16 x 16 (18%
 // faster on 4 x 8192 x 8 x 16).
 constexpr int kFwdBf16Few = 5, kBwdBf16Few = 4;
+// The bf16 backward walk with more lane groups than two CTAs per SM hold: its
+// registers capped so that three fit (168 instead of 205 a thread).  On
+// 16 x 8192 x 32 x 32 (1024 groups) it measured 0.528 against 0.497 of the copy
+// bandwidth; on 8 x 4096 x 16 x 32 (256 groups) 0.401 against 0.418.
+constexpr int kBwdBf16Many = 5;
 constexpr int kNumBwdBf16 = sizeof(kBwdBf16Variants) / sizeof(kBwdBf16Variants[0]);
 #undef QS_VARIANT
 #undef QS_SEGWALK_FWD
@@ -646,6 +660,7 @@ int make_plan(bool bwd, int64_t B, int64_t S, int64_t HJ, int sms, Plan *pl, Mod
             const long long groups = (long long)B * ((HJ + w.lt - 1) / w.lt);
             const long long need = bwd ? 3ll * sms / 2 : 3ll * sms / 4;
             vi = groups >= need ? wi : (bwd ? kBwdBf16Few : kFwdBf16Few);
+            if (bwd && groups > 2ll * sms) vi = kBwdBf16Many;
         }
     } else {
         vi = pick_variant(bwd, B, S, HJ, sms);

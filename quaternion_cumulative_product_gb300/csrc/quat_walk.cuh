@@ -170,8 +170,10 @@ __global__ void __launch_bounds__(LT *NSEG)
 // the other (both walks of one group before the next group), so the grid
 // sets how many groups are in flight at once; the rings and shared slots
 // carry over from one group to the next.
-template <typename IO, int LT, int NSEG, int N, int NSTF, int NSTB, bool SELF, bool GIVEN>
-__global__ void __launch_bounds__(LT *NSEG)
+// MINB: CTAs per SM the register allocation must allow (ptxas caps the
+// registers per thread accordingly).
+template <typename IO, int LT, int NSEG, int N, int NSTF, int NSTB, bool SELF, bool GIVEN, int MINB = 1>
+__global__ void __launch_bounds__(LT *NSEG, MINB)
     quat_walk_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap dmap,
                          const typename IO::elem *__restrict__ init, float4 *__restrict__ carF,
                          const float4 *__restrict__ given, typename IO::elem *__restrict__ d_q,

@@ -55,7 +55,7 @@ def bf16_inputs(dev, w):
 
 # Compiled configurations: forward 0-3 walks, 4 three kernels, 5 segmented
 # chained walk; backward 0-3 walks, 4 three kernels.
-N_BF16_FWD, N_BF16_BWD = 7, 5
+N_BF16_FWD, N_BF16_BWD = 7, 6
 
 
 @pytest.fixture(autouse=True)
