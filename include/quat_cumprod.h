@@ -41,11 +41,18 @@
  * and 64-step chunk this is nothing for a forward walk, 16 bytes for a
  * backward walk, and 32 (forward) or 64 (backward) bytes for the aggregate /
  * carry / apply kernels (see quat_cumprod_plan for which a call uses).  The
- * first call on a stream, and any later call that needs a larger workspace,
- * allocates it (cudaMalloc) and synchronizes that stream; issue such a call
- * before capturing the stream into a CUDA graph.  Calls on one stream are
- * ordered by the stream; calls on different streams use different workspaces
- * and may run concurrently.
+ * segmented chained walk (the forward for few lane groups) keeps, per lane
+ * and segment of 4 chunks, two copies of 32 bytes of look-back values plus a
+ * few counters in further per-stream allocations, and reserves the aggregate
+ * / carry / apply forward's workspace as well.  The first call on a stream,
+ * and any later call that needs more scratch, allocates it (cudaMalloc) and
+ * synchronizes that stream; issue such a call before capturing the stream
+ * into a CUDA graph.  While a stream is being captured the forward uses the
+ * aggregate / carry / apply kernels, which keep no state from one launch to
+ * the next (the segmented walk's look-back values are tied to the launch
+ * that reads them), so a captured graph may be replayed any number of
+ * times.  Calls on one stream are ordered by the stream; calls on different
+ * streams use different workspaces and may run concurrently.
  *
  * Sizes: B, S, H, J >= 0.  Any zero size makes the call a no-op that returns
  * QS_OK (except that quat_cumprod_bwd with S == 0 writes d_init = 0).

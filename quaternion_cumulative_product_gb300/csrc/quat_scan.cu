@@ -252,6 +252,7 @@ constexpr int kFwdBf16Default = 1, kBwdBf16Default = 0;   // walks; fastest meas
 // 1 x 131072 x 16 x 16, 2 x 65536 x 32 x 32 and 2 x 32768 x 16 x 16 (18%
 // faster on 4 x 8192 x 8 x 16).
 constexpr int kFwdBf16Few = 5, kBwdBf16Few = 4;
+constexpr int kFwdBf16Three = 4;   // the aggregate / carry / apply forward
 // The bf16 backward walk with more lane groups than two CTAs per SM hold: its
 // registers capped so that three fit (168 instead of 205 a thread).  On
 // 16 x 8192 x 32 x 32 (1024 groups) it measured 0.528 against 0.497 of the copy
@@ -643,8 +644,18 @@ struct Plan {
     size_t o_L = 0, o_W = 0, o_F = 0, o_H = 0, o_I = 0, ws_bytes = 0;
 };
 
+int layout_plan(bool bwd, int64_t B, int64_t S, int64_t HJ, int sms, Plan *pl, Mode mode);
+
+// `capturing`: the call is being captured into a CUDA graph, whose launches
+// are replayed with the same arguments.  The segmented walk and the chained
+// scan keep state from one launch to the next (the epoch of their status
+// words, or which buffers of self-describing values a launch reads), so a
+// replay would take the previous replay's values for published ones; under
+// capture the forward therefore uses the aggregate / carry / apply kernels,
+// which keep none.  Eager plans of those designs reserve the workspace of that
+// forward as well, so a call before the capture sizes it.
 int make_plan(bool bwd, int64_t B, int64_t S, int64_t HJ, int sms, Plan *pl, Mode mode = Mode::PLAIN,
-              bool bf16 = false) {
+              bool bf16 = false, bool capturing = false) {
     int vi = 0;
     if (bf16) {
         int forced;
@@ -678,8 +689,27 @@ int make_plan(bool bwd, int64_t B, int64_t S, int64_t HJ, int sms, Plan *pl, Mod
         v = bwd ? &kBwdVariants[vi] : &kFwdVariants[vi];
     }
     if (mode == Mode::FROM_CARRIES && v->walk) v = &kBwdGiven;
+    const bool stateful = v->chain || v->segk > 0;
+    const int vthree = bf16 ? kFwdBf16Three : kThreeFwd;
+    const Variant *three = bf16 ? &kFwdBf16Variants[vthree] : &kFwdVariants[vthree];
+    if (capturing && stateful) {
+        vi = vthree;
+        v = three;
+    }
     pl->vi = vi;
     pl->v = v;
+    int rc = layout_plan(bwd, B, S, HJ, sms, pl, mode);
+    if (rc != QS_OK || capturing || !stateful) return rc;
+    Plan p3;
+    p3.vi = vthree;
+    p3.v = three;
+    rc = layout_plan(bwd, B, S, HJ, sms, &p3, mode);
+    if (rc == QS_OK && p3.ws_bytes > pl->ws_bytes) pl->ws_bytes = p3.ws_bytes;
+    return rc;
+}
+
+// Geometry and workspace layout of the configuration pl->v.
+int layout_plan(bool bwd, int64_t B, int64_t S, int64_t HJ, int sms, Plan *pl, Mode mode) {
     const int LT = pl->v->lt, T = pl->v->T();
     qs::Geometry &g = pl->geo;
     g.S = S;
@@ -771,8 +801,13 @@ int launch(bool bwd, const void *q, const void *d_cum, void *out, const void *in
     int dev = 0;
     int rc = device_info(&di, &dev);
     if (rc != QS_OK) return rc;
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) {
+        cudaGetLastError();
+        return QS_ERR_CUDA;
+    }
     Plan pl;
-    rc = make_plan(bwd, B, S, HJ, di->sms, &pl, mode, bf16);
+    rc = make_plan(bwd, B, S, HJ, di->sms, &pl, mode, bf16, cs != cudaStreamCaptureStatusNone);
     if (rc != QS_OK) return rc;
     unsigned char *ws = nullptr;
     rc = ensure_workspace(dev, stream, pl.ws_bytes, &ws);

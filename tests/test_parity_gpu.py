@@ -314,6 +314,47 @@ def test_segmented_walk_stall_reports_timeout_then_recovers(dev, variant):
     assert_parity(cum.cpu().numpy(), oracle.fwd(q, init), "cum")
 
 
+def test_graph_capture_replays_match_the_oracle(dev):
+    """A forward and a backward captured into a CUDA graph, replayed on new inputs.
+
+    The shape has few lane groups, so an eager forward is the segmented walk,
+    whose look-back values are tied to the launch that reads them; under
+    capture the library takes the aggregate / carry / apply forward instead,
+    and every replay must match the oracle."""
+    lib = qs.load_library()
+    assert lib.quat_cumprod_debug_set_variant(-1, -1) == qs.QS_OK
+    dims = (1, 20000, 2, 16)
+
+    def inputs(seed):
+        return workloads.make_inputs(workloads.custom("graph", *dims, q_kind="rotation", theta_max=0.3, seed=seed))
+
+    q, init, d_cum = inputs(130)
+    tq, ti, td = (torch.from_numpy(a).to(dev) for a in (q, init, d_cum))
+    cum, dq, di = torch.empty_like(tq), torch.empty_like(tq), torch.empty_like(ti)
+    s = torch.cuda.Stream(device=dev)
+    s.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(s):   # sizes the capture stream's scratch
+        qs.quat_cumprod_fwd(tq, ti, cum)
+        qs.quat_cumprod_bwd(tq, ti, td, dq, di)
+    assert qs.quat_cumprod_status(stream=s, device=dev) == qs.QS_OK
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        qs.quat_cumprod_fwd(tq, ti, cum)
+        qs.quat_cumprod_bwd(tq, ti, td, dq, di)
+    for seed in (131, 132, 133):
+        q, init, d_cum = inputs(seed)
+        tq.copy_(torch.from_numpy(q))
+        ti.copy_(torch.from_numpy(init))
+        td.copy_(torch.from_numpy(d_cum))
+        g.replay()
+        torch.cuda.synchronize(dev)
+        assert qs.quat_cumprod_status(stream=s, device=dev) == qs.QS_OK
+        assert_parity(cum.cpu().numpy(), oracle.fwd(q, init), "cum (replay)")
+        rq, ri = oracle.bwd(q, init, d_cum)
+        assert_parity(dq.cpu().numpy(), rq, "d_q (replay)")
+        assert_parity(di.cpu().numpy(), ri, "d_init (replay)")
+
+
 def test_unknown_variant_is_rejected(dev):
     lib = qs.load_library()
     assert lib.quat_cumprod_debug_set_variant(N_FWD_VARIANTS, 0) == qs.QS_ERR_DIMS
