@@ -467,6 +467,9 @@ struct LbValues {
     int next = 0;       // the pair the next launch reads
 };
 std::map<std::pair<int, uintptr_t>, LbValues> g_lbv;
+// Held from choosing a launch's pair to enqueueing it, so that launches on a
+// stream are enqueued in the order their pairs were handed out.
+std::mutex g_lbv_launch_mu;
 
 // The pair of buffers a launch of `n` entries reads (agg, incl) and the pair
 // it resets (agg_next, incl_next); enqueues the clearing memset if needed.
@@ -840,7 +843,9 @@ int launch(bool bwd, const void *q, const void *d_cum, void *out, const void *in
         float4 *aggv = reinterpret_cast<float4 *>(ws + pl.o_W);
         float4 *inclv = reinterpret_cast<float4 *>(ws + pl.o_F);
         float4 *agg_next = nullptr, *incl_next = nullptr;
+        std::unique_lock<std::mutex> order(g_lbv_launch_mu, std::defer_lock);
         if (pl.v->sent) {
+            order.lock();
             rc = lb_values(dev, stream, units * pl.v->lt, &aggv, &inclv, &agg_next, &incl_next);
             if (rc != QS_OK) return rc;
         }
