@@ -54,7 +54,8 @@ def bf16_inputs(dev, w):
 
 
 # Compiled configurations: forward 0-3 walks, 4 three kernels, 5 segmented
-# chained walk; backward 0-3 walks, 4 three kernels.
+# chained walk, 6 the same with self-describing look-back values; backward 0-3
+# walks, 4 three kernels, 5 walk with registers capped for three CTAs per SM.
 N_BF16_FWD, N_BF16_BWD = 7, 6
 
 
@@ -163,3 +164,39 @@ def test_bf16_rejects_odd_lane_count_and_wrong_dtype(dev):
     _, di = qs.quat_cumprod_bwd_bf16(q0, i0, q0.clone())
     torch.cuda.synchronize(dev)
     assert float(di.float().abs().max()) == 0.0
+
+
+def test_bf16_graph_capture_replays_match_the_oracle(dev):
+    """A bf16 forward and backward captured into a CUDA graph, replayed on new inputs.
+
+    Eagerly the forward for few lane groups is the segmented walk, whose status
+    words are tied to one launch; under capture it is the three-kernel forward."""
+    dims = (1, 20000, 2, 16)
+
+    def inputs(seed):
+        return bf16_inputs(dev, workloads.custom("graph16", *dims, q_kind="rotation", theta_max=0.3, seed=seed))
+
+    (tq, ti, td), _ = inputs(140)
+    cum, dq, di = torch.empty_like(tq), torch.empty_like(tq), torch.empty_like(ti)
+    s = torch.cuda.Stream(device=dev)
+    s.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(s):   # sizes the capture stream's scratch
+        qs.quat_cumprod_fwd_bf16(tq, ti, cum)
+        qs.quat_cumprod_bwd_bf16(tq, ti, td, dq, di)
+    assert qs.quat_cumprod_status(stream=s, device=dev) == qs.QS_OK
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        qs.quat_cumprod_fwd_bf16(tq, ti, cum)
+        qs.quat_cumprod_bwd_bf16(tq, ti, td, dq, di)
+    for seed in (141, 142):
+        (nq, ni, nd), (eq, ei, ed) = inputs(seed)
+        tq.copy_(nq)
+        ti.copy_(ni)
+        td.copy_(nd)
+        g.replay()
+        torch.cuda.synchronize(dev)
+        assert qs.quat_cumprod_status(stream=s, device=dev) == qs.QS_OK
+        assert normwise(cum.float().cpu().numpy(), oracle.fwd(eq, ei)) <= TOL_BF16
+        rq, ri = oracle.bwd(eq, ei, ed)
+        assert normwise(dq.float().cpu().numpy(), rq) <= TOL_BF16
+        assert normwise(di.float().cpu().numpy(), ri) <= TOL_BF16
