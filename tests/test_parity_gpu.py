@@ -314,6 +314,44 @@ def test_segmented_walk_stall_reports_timeout_then_recovers(dev, variant):
     assert_parity(cum.cpu().numpy(), oracle.fwd(q, init), "cum")
 
 
+def test_segmented_walk_from_concurrent_threads(dev):
+    """Host threads enqueue the segmented-walk forward (few lane groups) on
+    streams of their own at the same time: each stream keeps its own look-back
+    buffers and workspace, and every result must match the oracle."""
+    import threading
+    lib = qs.load_library()
+    assert lib.quat_cumprod_debug_set_variant(-1, -1) == qs.QS_OK
+    cases = []
+    for i, dims in enumerate([(1, 20000, 2, 16), (2, 9000, 1, 32), (1, 30000, 1, 16)]):
+        w = workloads.custom("seg_threads", *dims, q_kind="rotation", theta_max=0.3, seed=150 + i)
+        q, init, _ = workloads.make_inputs(w)
+        cases.append((torch.from_numpy(q).to(dev), torch.from_numpy(init).to(dev), oracle.fwd(q, init)))
+    torch.cuda.synchronize(dev)
+    errors = []
+
+    def worker(k):
+        try:
+            torch.cuda.set_device(dev)
+            s = torch.cuda.Stream(device=dev)
+            tq, ti, ref = cases[k]
+            with torch.cuda.stream(s):
+                for _ in range(4):
+                    cum = qs.quat_cumprod_fwd(tq, ti)
+                    assert qs.quat_cumprod_status(stream=s, device=dev) == qs.QS_OK
+                    errors.append((k, normwise(cum.cpu().numpy(), ref)))
+        except Exception as e:   # reported below
+            errors.append((k, repr(e)))
+
+    threads = [threading.Thread(target=worker, args=(k,)) for k in range(len(cases))]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert len(errors) == 4 * len(cases), errors
+    for k, e in errors:
+        assert isinstance(e, float) and e <= 1e-4, (k, e)
+
+
 def test_graph_capture_replays_match_the_oracle(dev):
     """A forward and a backward captured into a CUDA graph, replayed on new inputs.
 
