@@ -22,6 +22,7 @@ autograd wrapper is in :mod:`quaternion_cumulative_product_gb300.autograd`.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 import threading
@@ -129,6 +130,14 @@ def _torch():
     return torch
 
 
+def _on_device(device):
+    """The CUDA device context for a call on ``device``; none when it is already current."""
+    torch = _torch()
+    if device.index is None or torch.cuda.current_device() == device.index:
+        return contextlib.nullcontext()
+    return torch.cuda.device(device)
+
+
 def _stream_handle(stream, device):
     torch = _torch()
     if stream is None:
@@ -175,7 +184,7 @@ def quat_cumprod_fwd(q, init, cum=None, stream=None):
         cum = torch.empty_like(q)
     else:
         _check_tensor("cum", cum, q.shape, q.device)
-    with torch.cuda.device(q.device):
+    with _on_device(q.device):
         rc = load_library().quat_cumprod_fwd(
             ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(init.data_ptr()),
             ctypes.c_void_p(cum.data_ptr()), B, S, H, J, _stream_handle(stream, q.device))
@@ -201,7 +210,7 @@ def quat_cumprod_bwd(q, init, d_cum, d_q=None, d_init=None, stream=None):
         d_init = torch.empty_like(init)
     else:
         _check_tensor("d_init", d_init, init.shape, q.device)
-    with torch.cuda.device(q.device):
+    with _on_device(q.device):
         rc = load_library().quat_cumprod_bwd(
             ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(init.data_ptr()),
             ctypes.c_void_p(d_cum.data_ptr()), ctypes.c_void_p(d_q.data_ptr()),
@@ -219,7 +228,7 @@ def quat_cumprod_fwd_bf16(q, init, cum=None, stream=None):
         cum = torch.empty_like(q)
     else:
         _check_tensor("cum", cum, q.shape, q.device, torch.bfloat16)
-    with torch.cuda.device(q.device):
+    with _on_device(q.device):
         rc = load_library().quat_cumprod_fwd_bf16(
             ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(init.data_ptr()),
             ctypes.c_void_p(cum.data_ptr()), B, S, H, J, _stream_handle(stream, q.device))
@@ -241,7 +250,7 @@ def quat_cumprod_bwd_bf16(q, init, d_cum, d_q=None, d_init=None, stream=None):
         d_init = torch.empty_like(init)
     else:
         _check_tensor("d_init", d_init, init.shape, q.device, torch.bfloat16)
-    with torch.cuda.device(q.device):
+    with _on_device(q.device):
         rc = load_library().quat_cumprod_bwd_bf16(
             ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(init.data_ptr()),
             ctypes.c_void_p(d_cum.data_ptr()), ctypes.c_void_p(d_q.data_ptr()),
@@ -272,7 +281,7 @@ def quat_cumprod_fwd_carries(q, init, cum=None, carries=None, stream=None):
         carries = torch.empty(_carries_shape(q), dtype=q.dtype, device=q.device)
     else:
         _check_tensor("carries", carries, _carries_shape(q), q.device)
-    with torch.cuda.device(q.device):
+    with _on_device(q.device):
         rc = load_library().quat_cumprod_fwd_carries(
             ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(init.data_ptr()), ctypes.c_void_p(cum.data_ptr()),
             ctypes.c_void_p(carries.data_ptr()), B, S, H, J, _stream_handle(stream, q.device))
@@ -301,7 +310,7 @@ def quat_cumprod_bwd_carries(q, carries, d_cum, d_q=None, d_init=None, stream=No
         d_init = torch.empty((B, H, J, 4), dtype=q.dtype, device=q.device)
     else:
         _check_tensor("d_init", d_init, (B, H, J, 4), q.device)
-    with torch.cuda.device(q.device):
+    with _on_device(q.device):
         rc = load_library().quat_cumprod_bwd_carries(
             ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(carries.data_ptr()),
             ctypes.c_void_p(d_cum.data_ptr()), ctypes.c_void_p(d_q.data_ptr()),
@@ -326,7 +335,7 @@ def quat_cumprod_bwd_noalloc(q, init, d_cum, d_q, d_init, stream=None):
     _check_tensor("d_cum", d_cum, q.shape, q.device)
     _check_tensor("d_q", d_q, q.shape, q.device)
     _check_tensor("d_init", d_init, init.shape, q.device)
-    with torch.cuda.device(q.device):
+    with _on_device(q.device):
         rc = load_library().quat_cumprod_bwd_noalloc(
             ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(init.data_ptr()),
             ctypes.c_void_p(d_cum.data_ptr()), ctypes.c_void_p(d_q.data_ptr()),
