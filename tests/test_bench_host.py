@@ -109,3 +109,23 @@ def test_design_names_follow_the_plan():
     assert bench.design_name("quat_cumprod_fwd", 1, 9) == "quat_cumprod_fwd (segmented chained walk kernel)"
     assert bench.design_name("quat_cumprod_bwd", 3, 0) == "quat_cumprod_bwd (aggregate + carry + apply kernels)"
     assert bench.design_name("quat_cumprod_fwd", 1, 4) == "quat_cumprod_fwd (walk kernel)"
+
+
+def test_reference_arm_prints_the_contract_line(monkeypatch, capsys):
+    """Rank 0 times the fp64 oracle on a lane sample and prints one JSON line with
+    the base contract's keys, its own cpu_baseline and an e2e without copies."""
+    import json
+    for k in ("WORLD_SIZE", "RANK", "LOCAL_RANK"):
+        monkeypatch.delenv(k, raising=False)
+    assert bench.main(["--impl", "reference", "--workload", "tiny", "--steps", "2", "--warmup", "3",
+                       "--cpu-lanes", "8"]) == 0
+    lines = [ln for ln in capsys.readouterr().out.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["metric"] == bench.METRIC and d["unit"] == bench.UNIT
+    assert d["value"] > 0 and d["higher_is_better"] is True and d["n_gpus"] == 1
+    assert d["steps"] == 2 and d["warmup"] == 3 and d["ms_per_step"] > 0
+    assert d["config"]["workload"].startswith("tiny") and d["config"]["elements"] == 1 * 64 * 2 * 4
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1 and cb["sample"]
+    assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
