@@ -129,3 +129,36 @@ def test_reference_arm_prints_the_contract_line(monkeypatch, capsys):
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1 and cb["sample"]
     assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+
+
+def test_every_timed_loop_is_bracketed_and_starts_on_a_busy_stream():
+    """Each device-timed loop over ``range(args.steps)`` in the bench has a
+    synchronize and a barrier before and after it, and the lead spin right before it (the first
+    step's events then exclude the host's enqueue of its first call)."""
+    import ast
+
+    def call_name(stmt):
+        if isinstance(stmt, ast.Expr) and isinstance(stmt.value, ast.Call):
+            return ast.unparse(stmt.value.func)
+        if isinstance(stmt, ast.Assign) and isinstance(stmt.value, ast.Call):
+            return ast.unparse(stmt.value.func)
+        return None
+
+    tree = ast.parse(open(bench.__file__).read())
+    loops = 0
+    for node in ast.walk(tree):
+        for field in ("body", "orelse"):
+            stmts = getattr(node, field, None)
+            if not isinstance(stmts, list):
+                continue
+            for k, st in enumerate(stmts):
+                if not (isinstance(st, ast.For) and ast.unparse(st.iter) == "range(args.steps)"
+                        and ".record(stream)" in ast.unparse(st)):
+                    continue   # only the device-timed loops (the oracle arm times on the host)
+                loops += 1
+                before = [call_name(s) for s in stmts[max(0, k - 6):k]]
+                after = [call_name(s) for s in stmts[k + 1:k + 4]]
+                assert before[-1] == "lead_spin", ast.unparse(st)[:60]
+                assert "torch.cuda.synchronize" in before and "barrier" in before
+                assert after[0] == "torch.cuda.synchronize" and "barrier" in after
+    assert loops == 3   # the step, the saved-carries step, the bf16 step
