@@ -11,7 +11,7 @@
  *
  *     G[t]   = d_cum[t] + conj(q_{t+1}) (x) G[t+1]               (reverse recurrence)
  *     d_q[t] = G[t] (x) conj(cum[t-1])
- *     d_init = conj(q_0) (x) G[0]   (= the page's S[0] for unit q_0)
+ *     d_init = conj(q_0) (x) G[0]   (= the page's S[0] for every non-zero q_0)
  *
  * which for unit quaternions is the page's closed form with the prefix product
  * P_t = q_t (x) ... (x) q_0 and the suffix sum S[t] = sum_{s>=t} conj(P_s) (x) d_cum[s].

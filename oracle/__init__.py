@@ -24,7 +24,9 @@ library rotation composition, closed forms for commuting single-axis inputs
 against numpy's complex ``cumprod``, norm preservation, linearity in ``init``,
 exact-rational brute force on tiny inputs, central finite differences and an
 adjoint dot test for the backward, equality with the closed form for unit
-quaternions, and the reverse-cumsum special case for identity ``q``.
+quaternions, the closed form generalised to non-unit quaternions
+(``G[t] = P_t (x) S[t] / |P_t|^2``, ``d_init = S[0]``), and the reverse-cumsum
+special case for identity ``q``.
 """
 from __future__ import annotations
 

@@ -21,8 +21,9 @@
  *   - the new factor multiplies on the LEFT (cum[t] = q_t (x) cum[t-1]);
  *   - cum holds cum[0..S-1] (init is not part of the output);
  *   - d_init of the literal recurrence is conj(q_0) (x) G[0], i.e. the VJP rule's
- *     grad_b applied to cum[0] = q_0 (x) init (it equals the page's S[0] when
- *     q_0 is a unit quaternion).
+ *     grad_b applied to cum[0] = q_0 (x) init.  It equals the page's S[0] for
+ *     every non-zero q_0: the cotangent of init is S[0] exactly, since
+ *     cum[s] = P_s (x) init.
  *
  * Layout: q, cum, d_cum, d_q are contiguous row-major [B,S,H,J,4]; init and
  * d_init are [B,H,J,4].  A "lane" is one (b,h,j); lanes are independent, and the

@@ -354,6 +354,39 @@ def test_bwd_recurrence_equals_closed_form_for_unit_q():
     assert np.abs(c_q - d_q2).max() > 1e-3 * np.abs(d_q2).max()
 
 
+def test_bwd_generalised_closed_form_for_any_quaternions():
+    """The page's closed form, extended to non-unit q, against the literal recurrence.
+
+    With M = q_s (x) ... (x) q_{t+1} = P_s (x) P_t^-1 and P^-1 = conj(P) / |P|^2,
+    the cotangent of cum[t] is G[t] = sum_{s>=t} conj(M) (x) d_cum[s]
+    = P_t (x) S[t] / |P_t|^2, S[t] = sum_{s>=t} conj(P_s) (x) d_cum[s], and the
+    cotangent of init is S[0] exactly (cum[s] = P_s (x) init).  So the page's
+    d_init = S[0] holds for every non-zero q, and its G = P (x) S only for unit P.
+    Everything here is computed with the test-side table product.
+    """
+    rng = np.random.default_rng(46)
+    B, S, H, J = 2, 200, 1, 3
+    q = rand_quat(rng, B, S, H, J)
+    q *= (rng.uniform(0.8, 1.25, (B, S, H, J, 1)) / np.linalg.norm(q, axis=-1, keepdims=True))
+    init = rand_quat(rng, B, H, J)
+    d_cum = rand_quat(rng, B, S, H, J)
+    P = np.empty_like(q)
+    acc = np.broadcast_to(np.array([1.0, 0, 0, 0]), (B, H, J, 4))
+    for t in range(S):
+        acc = tmul(q[:, t], acc)
+        P[:, t] = acc
+    terms = tmul(tconj(P), d_cum)
+    Ssuf = np.flip(np.cumsum(np.flip(terms, axis=1), axis=1), axis=1)
+    G = tmul(P, Ssuf) / np.sum(P * P, axis=-1, keepdims=True)
+    cum_prev = np.concatenate([init[:, None], tmul(P[:, :-1], init[:, None])], axis=1)
+    want_q = tmul(G, tconj(cum_prev))
+    d_q, d_init = oracle.bwd(q, init, d_cum)
+    assert np.abs(d_q - want_q).max() <= 1e-10 * np.abs(want_q).max()
+    assert np.abs(d_init - Ssuf[:, 0]).max() <= 1e-10 * np.abs(Ssuf[:, 0]).max()
+    # the norms really vary: the unnormalised G = P (x) S would be far off
+    assert np.ptp(np.sum(P * P, axis=-1)) > 1.0
+
+
 def test_bwd_identity_q_is_reverse_cumsum():
     rng = np.random.default_rng(43)
     B, S, H, J = 2, 64, 2, 2
