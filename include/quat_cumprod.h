@@ -52,7 +52,10 @@
  * the next (the segmented walk's look-back values are tied to the launch
  * that reads them), so a captured graph may be replayed any number of
  * times.  Calls on one stream are ordered by the stream; calls on different
- * streams use different workspaces and may run concurrently.
+ * streams use different workspaces and may run concurrently.  A workspace is
+ * found by the stream's handle: before destroying a stream, let its work
+ * finish, so that a new stream given the same handle cannot meet a launch
+ * still running on the old one's workspace.
  *
  * Sizes: B, S, H, J >= 0.  Any zero size makes the call a no-op that returns
  * QS_OK (except that quat_cumprod_bwd with S == 0 writes d_init = 0).
