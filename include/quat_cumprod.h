@@ -59,8 +59,9 @@
  *
  * Sizes: B, S, H, J >= 0.  Any zero size makes the call a no-op that returns
  * QS_OK (except that quat_cumprod_bwd with S == 0 writes d_init = 0).
- * Limits: S*H*J*16 < 2^40 bytes per batch entry, H*J*4 < 2^32, the number of
- * work tiles below 2^31.
+ * Limits: each of B, S, H, J below 2^31, S*H*J*16 < 2^40 bytes per batch
+ * entry, H*J*4 < 2^32, the number of work tiles below 2^31.  A size past a
+ * limit returns QS_ERR_DIMS before anything is enqueued.
  */
 #ifndef QUAT_CUMPROD_H
 #define QUAT_CUMPROD_H

@@ -231,3 +231,30 @@ def test_host_step_argument_checks(lib):
     p[5] = ptrs[1]              # d_init over init
     assert f(*p, 1, 4, 1, 1, None) == qs.QS_ERR_ALIAS
     assert f(*ptrs, 0, 4, 1, 1, None) == qs.QS_OK   # no lanes: nothing to do
+
+
+def test_size_limits_at_their_boundaries(lib):
+    """Just past each documented limit the size check rejects the call; at the
+    limit it passes, and with no device here the call then stops at its first
+    CUDA query.  Fake device pointers are far apart so that no range overlaps."""
+    torch = pytest.importorskip("torch")
+    if torch.cuda.is_available():
+        pytest.skip("the accepted calls would reach a GPU with fake device pointers")
+    q, i, c = _p(1 << 44), _p(1 << 46), _p(1 << 45)
+    f = lib.quat_cumprod_fwd
+
+    def accepted(*dims):
+        rc = f(q, i, c, *dims, None)
+        assert rc not in (qs.QS_ERR_DIMS, qs.QS_OK), dims
+        assert rc in (qs.QS_ERR_CUDA, qs.QS_ERR_DEVICE), (dims, rc)
+
+    # S*H*J*16 < 2^40 bytes per batch entry
+    accepted(1, (1 << 26) - 1, 32, 32)
+    assert f(q, i, c, 1, 1 << 26, 32, 32, None) == qs.QS_ERR_DIMS
+    # H*J*4 < 2^32
+    accepted(1, 1, 1 << 15, (1 << 15) - 1)
+    assert f(q, i, c, 1, 1, 1 << 15, 1 << 15, None) == qs.QS_ERR_DIMS
+    # every size below 2^31
+    accepted((1 << 31) - 1, 1, 1, 1)
+    assert f(q, i, c, 1 << 31, 1, 1, 1, None) == qs.QS_ERR_DIMS
+    assert f(q, i, c, 1, 1, 1, 1 << 31, None) == qs.QS_ERR_DIMS
