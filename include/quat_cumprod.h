@@ -114,7 +114,7 @@ int quat_cumprod_bwd(const float *q, const float *init, const float *d_cum,
 /*
  * Backward without allocation: computes exactly what quat_cumprod_bwd
  * computes, with the same arguments, layout, ownership and checks, but never
- * allocates device memory.  The paper has no counterpart: this entry point
+ * allocates device memory.  The page has no counterpart: this entry point
  * exists for callers that cannot call cudaMalloc at the point where they need
  * the gradient, for example
  *   - code whose device memory is all handed out by another allocator (a
