@@ -209,3 +209,29 @@ def test_backward_chain_on_the_wrong_side_is_caught(data):
     d_q, _ = chunked_bwd_affine(lanes(q), init.reshape(-1, 4), lanes(d_cum), 7, swap_chain=True)
     want_q, _ = oracle.bwd(q, init, d_cum)
     assert rel(unlanes(d_q, B, H, J), want_q) > 1e-3
+
+
+def test_chunked_algorithm_on_random_shapes():
+    """Random (B, S, H, J), chunk length and quaternion scale: the chunked forward
+    and the affine-map backward equal the oracle's sequential loops."""
+    hyp = pytest.importorskip("hypothesis")
+    st = pytest.importorskip("hypothesis.strategies")
+
+    @hyp.settings(max_examples=60, deadline=None, derandomize=True)
+    @hyp.given(B=st.integers(1, 3), S=st.integers(1, 90), H=st.integers(1, 2), J=st.integers(1, 3),
+               T=st.integers(1, 100), scale=st.floats(0.5, 1.5), seed=st.integers(0, 2**31 - 1))
+    def check(B, S, H, J, T, scale, seed):
+        rng = np.random.default_rng(seed)
+        q = rand_quat(rng, B, S, H, J)
+        q *= scale / np.linalg.norm(q, axis=-1, keepdims=True)
+        init = rand_quat(rng, B, H, J)
+        d_cum = rand_quat(rng, B, S, H, J)
+        cum, *_ = chunked_fwd(lanes(q), init.reshape(-1, 4), T)
+        want = oracle.fwd(q, init)
+        assert rel(unlanes(cum, B, H, J), want) <= 1e-11
+        d_q, d_init = chunked_bwd_affine(lanes(q), init.reshape(-1, 4), lanes(d_cum), T)
+        want_q, want_i = oracle.bwd(q, init, d_cum)
+        assert rel(unlanes(d_q, B, H, J), want_q) <= 1e-10
+        assert rel(d_init.reshape(want_i.shape), want_i) <= 1e-10
+
+    check()
