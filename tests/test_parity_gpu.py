@@ -10,6 +10,8 @@ are independent, so the oracle on a lane subset is exact).
 from __future__ import annotations
 
 import ctypes
+import json
+import os
 
 import numpy as np
 import pytest
@@ -23,6 +25,10 @@ torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
 
 TOL = 1e-4
+# When set, every comparison against the oracle appends its measured error to
+# this file (one JSON object per line), so that the margins below the tolerance
+# can be reported; unset, nothing is written.
+PARITY_LOG = os.environ.get("QS_PARITY_LOG")
 
 
 @pytest.fixture(scope="module")
@@ -59,6 +65,11 @@ def run_gpu(dev, q, init, d_cum, stream=None):
 
 def assert_parity(got, ref, what):
     err = normwise(got, ref)
+    if PARITY_LOG:
+        test = os.environ.get("PYTEST_CURRENT_TEST", "").split(" ")[0]
+        with open(PARITY_LOG, "a") as f:
+            f.write(json.dumps({"test": test, "tensor": what, "elements": int(ref.size // 4),
+                                "normwise": err, "tol": TOL}) + "\n")
     assert err <= TOL, f"{what}: normwise relative error {err:.3e} > {TOL}"
     return err
 
