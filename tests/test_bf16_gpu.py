@@ -15,6 +15,9 @@ Tolerance, normwise per output tensor:
 """
 from __future__ import annotations
 
+import json
+import os
+
 import numpy as np
 import pytest
 
@@ -27,6 +30,9 @@ torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
 
 TOL_BF16 = 2.0 ** -8 + 1.1e-4
+# When set, every error measured below is appended to this file (one JSON
+# object per line); unset, nothing is written.
+PARITY_LOG = os.environ.get("QS_PARITY_LOG")
 
 
 @pytest.fixture(scope="module")
@@ -42,7 +48,13 @@ def normwise(got, ref):
     if ref.size == 0:
         return 0.0
     scale = float(np.abs(ref).max())
-    return float(np.abs(np.asarray(got, np.float64) - ref).max()) / (scale if scale > 0 else 1.0)
+    err = float(np.abs(np.asarray(got, np.float64) - ref).max()) / (scale if scale > 0 else 1.0)
+    if PARITY_LOG:
+        test = os.environ.get("PYTEST_CURRENT_TEST", "").split(" ")[0]
+        with open(PARITY_LOG, "a") as f:
+            f.write(json.dumps({"test": test, "dtype": "bf16", "elements": int(ref.size // 4),
+                                "normwise": err}) + "\n")
+    return err
 
 
 def bf16_inputs(dev, w):
