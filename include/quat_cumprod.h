@@ -274,7 +274,8 @@ const char *quat_cumprod_strerror(int status);
  * -1 = default; QS_ERR_DIMS for an unknown index).
  * quat_cumprod_debug_set_walk_cap(n) caps the CTAs of the backward walk
  * kernels at n (n <= 0 restores each configuration's own cap); the lane
- * groups are then walked in equal waves of at most n.  All four are
+ * groups are then walked in equal waves of at most n.  It caps the
+ * persistent grid of the backward's segmented walk as well.  All four are
  * process-wide settings and return QS_OK unless stated.
  */
 int quat_cumprod_debug_set_timeout_ns(int64_t ns);

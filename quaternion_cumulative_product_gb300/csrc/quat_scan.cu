@@ -66,6 +66,7 @@
 #include "quat_cumprod.h"
 #include "quat_chain.cuh"
 #include "quat_segwalk.cuh"
+#include "quat_segwalk_bwd.cuh"
 #include "quat_segwalk_ws.cuh"
 #include "quat_tiles.cuh"
 #include "quat_walk.cuh"
@@ -102,6 +103,9 @@ struct Variant {
     // Segmented walk whose look-back values carry their own state (reset for
     // the next launch by the kernel itself; see LbValues).
     bool sent = false;
+    // Backward segmented walk: the carries-only forward pass it starts from
+    // when it recomputes the carries (the same for every backward configuration).
+    const void *prepass = nullptr;
 };
 
 #define QS_VARIANT(B, LT, N)                                                                        \
@@ -163,6 +167,18 @@ const Variant kFwdVariants[] = {
         true, reinterpret_cast<const void *>(qs::quat_walk_bwd_kernel<qs::IoF32, LT, NSEG, N, NSTF, NSTB, false, false>), \
             nullptr, true, LT, NSEG, N, qs::walk_bwd_smem_bytes(LT, NSEG, N, NSTF, NSTB), false, CAPX4 \
     }
+// The carries-only forward pass of the segmented backward (its forward
+// carries, one read of q): 16-lane groups, segments of 4 chunks, 4-stage ring.
+const void *const kCarriesPass =
+    reinterpret_cast<const void *>(qs::quat_carries_pass_kernel<qs::IoF32, 16, 8, 8, 4, 4>);
+const Variant kCarriesPassVariant = Variant{
+    false, kCarriesPass, nullptr, false, 16, 8, 8, qs::carries_pass_smem_bytes(16, 8, 8, 4, 4), false, 0, 4, 64, true};
+#define QS_SEGWALK_BWD(LT, NSEG, N, NST, K, MINB, LB, W2FWD)                                        \
+    Variant {                                                                                       \
+        false, reinterpret_cast<const void *>(qs::quat_segwalk_bwd_kernel<qs::IoF32, LT, NSEG, N, NST, K, MINB, LB, W2FWD>), \
+            nullptr, true, LT, NSEG, N, qs::segwalk_bwd_smem_bytes(LT, NSEG, N, NST, K), false, 0, K, 64, true, \
+            kCarriesPass                                                                            \
+    }
 const Variant kBwdVariants[] = {
     QS_VARIANT(true, 32, 8),           // 0: three kernels, 64-step chunks, 64 KiB tiles
     QS_VARIANT(true, 32, 4),           // 1: three kernels, 32-step chunks
@@ -175,6 +191,16 @@ const Variant kBwdVariants[] = {
     QS_WALK_BWD(16, 8, 8, 4, 2, true),    // 8: walk, 16 lanes x 64 steps, each thread folds its own carries
     QS_WALK_BWD(32, 8, 8, 6, 3, true),    // 9: walk, 32 lanes x 64 steps, each thread folds its own carries
     QS_WALK_BWD_CAP(16, 8, 8, 4, 2, 8),   // 10: as 4, at most 2 CTAs per SM (more groups: equal waves)
+    QS_SEGWALK_BWD(16, 8, 8, 2, 4, 2, 4, false),   // 11: segmented walk (few lane groups), 16 lanes, segments of 4 chunks, 2 x 32 KiB ring
+    QS_SEGWALK_BWD(16, 8, 8, 3, 2, 2, 4, false),   // 12: as 11, segments of 2 chunks, 3 x 32 KiB ring
+    QS_SEGWALK_BWD(32, 8, 8, 2, 4, 1, 4, false),   // 13: 32 lanes, 2 x 64 KiB ring (one CTA per SM)
+    QS_SEGWALK_BWD(16, 8, 8, 2, 2, 2, 4, false),   // 14: as 11, segments of 2 chunks
+    QS_SEGWALK_BWD(16, 8, 8, 2, 4, 2, 8, false),   // 15: as 11, look-back rounds of 8 predecessors
+    QS_SEGWALK_BWD(16, 8, 8, 2, 4, 2, 2, false),   // 16: as 11, look-back rounds of 2 predecessors
+    QS_SEGWALK_BWD(16, 8, 8, 3, 2, 2, 8, false),   // 17: as 12, look-back rounds of 8 predecessors
+    QS_SEGWALK_BWD(16, 8, 8, 2, 4, 2, 4, true),    // 18: as 11, walk 2 left to right
+    QS_SEGWALK_BWD(16, 8, 8, 3, 2, 2, 4, true),    // 19: as 12, walk 2 left to right
+    QS_SEGWALK_BWD(16, 8, 8, 2, 3, 2, 4, true),    // 20: segments of 3 chunks, walk 2 left to right
 };
 // The backward from caller-provided carries: the reverse walk alone.
 const Variant kBwdGiven = Variant{true,
@@ -253,6 +279,7 @@ constexpr int kFwdBf16Default = 1, kBwdBf16Default = 0;   // walks; fastest meas
 // faster on 4 x 8192 x 8 x 16).
 constexpr int kFwdBf16Few = 5, kBwdBf16Few = 4;
 constexpr int kFwdBf16Three = 4;   // the aggregate / carry / apply forward
+constexpr int kBwdBf16Three = 4;   // the aggregate / carry / apply backward
 // The bf16 backward walk with more lane groups than two CTAs per SM hold: its
 // registers capped so that three fit (168 instead of 205 a thread).  On
 // 16 x 8192 x 32 x 32 (1024 groups) it measured 0.528 against 0.497 of the copy
@@ -267,6 +294,7 @@ constexpr int kNumBwdBf16 = sizeof(kBwdBf16Variants) / sizeof(kBwdBf16Variants[0
 #undef QS_WALK_FWD
 #undef QS_WALK_BWD
 #undef QS_WALK_BWD_CAP
+#undef QS_SEGWALK_BWD
 // Lanes per block of the carry scan (sequences of more than 256 chunks).
 constexpr int kCarryScanLanes = 2;
 
@@ -281,6 +309,10 @@ constexpr int kCarryScanLanes = 2;
 // 32 x 32: 1024 groups) each CTA walks several in equal waves, measured 5%
 // faster than one CTA per group in the hardware's own waves.
 constexpr int kWalkFwd = 4, kWalkBwd = 10, kThreeFwd = 0, kThreeBwd = 0;
+// Backward with too few lane groups for a walk: the segmented walk (after a
+// carries-only forward pass when the carries are not saved: 64 bytes per
+// element of DRAM instead of the three kernels' 80), see pick_variant.
+constexpr int kSegBwd = 11;
 // Forward with too few lane groups for a walk: the segmented chained walk
 // (segments of 4 chunks) whose look-back values carry their own state, so a
 // look-back round takes one memory latency.  It measured 0.76 / 0.82 / 0.73 of
@@ -393,6 +425,7 @@ int device_info(DevInfo **out, int *dev_out) {
             for (const Variant &v : kFwdVariants) setup(v);
             for (const Variant &v : kBwdVariants) setup(v);
             setup(kBwdGiven);
+            setup(kCarriesPassVariant);
             for (const Variant &v : kFwdBf16Variants) setup(v);
             for (const Variant &v : kBwdBf16Variants) setup(v);
             if (!ok) {
@@ -454,30 +487,42 @@ int ensure_workspace(int dev, cudaStream_t stream, size_t need, unsigned char **
 // after it.
 constexpr size_t kFlagsHead = 256;
 
-// Look-back values of the segmented walk that carry their own state (Variant
-// `sent`): per (device, stream) an allocation no other kernel writes, holding
-// two pairs of buffers (segment products, inclusive values) of `n` entries.
-// A launch reads the pair `next` and resets the other one for the launch
-// after it; the host clears both when the entry layout changes (and when the
-// allocation is new, or a launch failed to be enqueued).
+// Look-back values of the segmented walks that carry their own state (Variant
+// `sent`): per (device, stream, kind of launch) an allocation no other kernel
+// writes, holding two sets of `narr` buffers of `n` entries each (forward:
+// segment products and inclusive values; backward: the maps' V and A and the
+// inclusive values).  A launch reads the set `next` and resets the other one
+// for the launch after it; the host clears both when the entry layout changes
+// (and when the allocation is new, or a launch failed to be enqueued).  Each
+// kind keeps its own buffers, so that alternating launches of different kinds
+// on a stream (a forward, a backward and its carries pass) need no clearing.
+enum LbKind { LB_FWD = 0, LB_CARRIES = 1, LB_BWD = 2 };
+constexpr int kLbMaxArrays = 3;
 struct LbValues {
     unsigned char *base = nullptr;
     size_t bytes = 0;
     long long n = -1;   // entries per buffer of the layout the buffers are clean for; -1: none
-    int next = 0;       // the pair the next launch reads
+    int next = 0;       // the set the next launch reads
 };
-std::map<std::pair<int, uintptr_t>, LbValues> g_lbv;
-// Held from choosing a launch's pair to enqueueing it, so that launches on a
-// stream are enqueued in the order their pairs were handed out.
+struct LbKey {
+    int dev;
+    uintptr_t stream;
+    int kind;
+    bool operator<(const LbKey &o) const {
+        return dev != o.dev ? dev < o.dev : stream != o.stream ? stream < o.stream : kind < o.kind;
+    }
+};
+std::map<LbKey, LbValues> g_lbv;
+// Held from choosing a launch's set to enqueueing it, so that launches on a
+// stream are enqueued in the order their sets were handed out.
 std::mutex g_lbv_launch_mu;
 
-// The pair of buffers a launch of `n` entries reads (agg, incl) and the pair
-// it resets (agg_next, incl_next); enqueues the clearing memset if needed.
-int lb_values(int dev, cudaStream_t stream, long long n, float4 **agg, float4 **incl, float4 **agg_next,
-              float4 **incl_next) {
+// The `narr` buffers a launch of `n` entries per buffer reads (cur) and the
+// ones it resets (next); enqueues the clearing memset if needed.
+int lb_values(int dev, cudaStream_t stream, int kind, long long n, int narr, float4 **cur, float4 **next) {
     std::lock_guard<std::mutex> lk(g_mu);
-    LbValues &w = g_lbv[{dev, reinterpret_cast<uintptr_t>(stream)}];
-    const size_t arr = align_up((size_t)n * 16, 256), need = 4 * arr;
+    LbValues &w = g_lbv[{dev, reinterpret_cast<uintptr_t>(stream), kind}];
+    const size_t arr = align_up((size_t)n * 16, 256), need = 2 * (size_t)narr * arr;
     if (w.bytes < need) {
         cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
         if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) {
@@ -514,18 +559,18 @@ int lb_values(int dev, cudaStream_t stream, long long n, float4 **agg, float4 **
         w.next = 0;
     }
     const int b = w.next;
-    *agg = reinterpret_cast<float4 *>(w.base + (size_t)(2 * b) * arr);
-    *incl = reinterpret_cast<float4 *>(w.base + (size_t)(2 * b + 1) * arr);
-    *agg_next = reinterpret_cast<float4 *>(w.base + (size_t)(2 * (b ^ 1)) * arr);
-    *incl_next = reinterpret_cast<float4 *>(w.base + (size_t)(2 * (b ^ 1) + 1) * arr);
+    for (int i = 0; i < narr; ++i) {
+        cur[i] = reinterpret_cast<float4 *>(w.base + (size_t)(b * narr + i) * arr);
+        next[i] = reinterpret_cast<float4 *>(w.base + (size_t)((b ^ 1) * narr + i) * arr);
+    }
     w.next = b ^ 1;
     return QS_OK;
 }
 
 // After a launch that was not enqueued: the next one starts from cleared buffers.
-void lb_values_invalidate(int dev, cudaStream_t stream) {
+void lb_values_invalidate(int dev, cudaStream_t stream, int kind) {
     std::lock_guard<std::mutex> lk(g_mu);
-    g_lbv[{dev, reinterpret_cast<uintptr_t>(stream)}].n = -1;
+    g_lbv[{dev, reinterpret_cast<uintptr_t>(stream), kind}].n = -1;
 }
 
 // CTAs of a persistent kernel: as many as are resident at once on the device
@@ -615,20 +660,6 @@ int make_map(CUtensorMap *m, const void *ptr, int64_t B, int64_t S, int64_t HJ, 
     return r == CUDA_SUCCESS ? QS_OK : QS_ERR_CUDA;
 }
 
-int pick_variant(bool bwd, int64_t B, int64_t S, int64_t HJ, int sms) {
-    {
-        std::lock_guard<std::mutex> lk(g_mu);
-        const int forced = bwd ? g_bwd_variant : g_fwd_variant;
-        if (forced >= 0) return forced;
-    }
-    const Variant &w = bwd ? kBwdVariants[kWalkBwd] : kFwdVariants[kWalkFwd];
-    const long long groups = (long long)B * ((HJ + w.lt - 1) / w.lt);
-    const long long need = bwd ? 3ll * sms / 2 : 3ll * sms / 4;
-    if (groups >= need) return bwd ? kWalkBwd : kWalkFwd;
-    if (bwd) return kThreeBwd;
-    return (long long)B * S * HJ >= kSegFwdLargeElements ? kSegFwdLarge : kSegFwd;
-}
-
 // Everything a call needs, derived from the sizes alone (no device calls).
 // What a call computes besides its outputs.
 enum class Mode {
@@ -648,6 +679,41 @@ struct Plan {
 };
 
 int layout_plan(bool bwd, int64_t B, int64_t S, int64_t HJ, int sms, Plan *pl, Mode mode);
+
+// The backward for few lane groups (LT = 16 groups, C 64-step chunks), both
+// measured on one GB300 with L2 flushed before every call (fraction of the
+// copy bandwidth at 48 bytes per element):
+//  * from saved carries, the segmented walk: segments of 4 chunks on long
+//    sequences of few groups (1 x 131072 x 16 x 16: 0.75; with 2 chunks 0.50,
+//    the look-backs run deep), of 2 chunks when the groups are many or the
+//    units few (2 x 65536 x 32 x 32: 0.88 against 0.79; 4 x 1024 x 8 x 16:
+//    0.22 against 0.18); the three kernels measured 0.58 / 0.60 / 0.14;
+//  * recomputing the carries, the segmented walk after its carries pass only
+//    with 64 groups or more (2 x 65536 x 32 x 32: 0.67 against 0.60 for the
+//    three kernels); with fewer the carries pass costs more than the three
+//    kernels' second read (1 x 131072 x 16 x 16: 0.56 against 0.58;
+//    4 x 1024 x 8 x 16: 0.14 against 0.16).
+constexpr int kSegBwdShort = 14;           // segments of 2 chunks
+constexpr long long kSegBwdManyGroups = 64;
+
+int pick_variant(bool bwd, int64_t B, int64_t S, int64_t HJ, int sms, Mode mode) {
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        const int forced = bwd ? g_bwd_variant : g_fwd_variant;
+        if (forced >= 0) return forced;
+    }
+    const Variant &w = bwd ? kBwdVariants[kWalkBwd] : kFwdVariants[kWalkFwd];
+    const long long groups = (long long)B * ((HJ + w.lt - 1) / w.lt);
+    const long long need = bwd ? 3ll * sms / 2 : 3ll * sms / 4;
+    if (groups >= need) return bwd ? kWalkBwd : kWalkFwd;
+    if (bwd) {
+        const long long units4 = groups * ((S + 4 * 64 - 1) / (4 * 64));   // segments of 4 chunks
+        const int seg = (groups >= kSegBwdManyGroups || units4 < 4ll * sms) ? kSegBwdShort : kSegBwd;
+        if (mode == Mode::FROM_CARRIES || groups >= kSegBwdManyGroups) return seg;
+        return kThreeBwd;
+    }
+    return (long long)B * S * HJ >= kSegFwdLargeElements ? kSegFwdLarge : kSegFwd;
+}
 
 // `capturing`: the call is being captured into a CUDA graph, whose launches
 // are replayed with the same arguments.  The segmented walk and the chained
@@ -677,11 +743,11 @@ int make_plan(bool bwd, int64_t B, int64_t S, int64_t HJ, int sms, Plan *pl, Mod
             if (bwd && groups > 2ll * sms) vi = kBwdBf16Many;
         }
     } else {
-        vi = pick_variant(bwd, B, S, HJ, sms);
+        vi = pick_variant(bwd, B, S, HJ, sms, mode);
     }
     const Variant *v = bf16 ? (bwd ? &kBwdBf16Variants[vi] : &kFwdBf16Variants[vi])
                             : bwd ? &kBwdVariants[vi] : &kFwdVariants[vi];
-    if (mode != Mode::PLAIN && (v->chain || v->segk > 0)) {   // carries come from the other designs
+    if (mode != Mode::PLAIN && v->chain) {   // the chained scan writes no carries: take the three kernels
         vi = kThreeFwd;
         v = &kFwdVariants[vi];
     }
@@ -693,8 +759,9 @@ int make_plan(bool bwd, int64_t B, int64_t S, int64_t HJ, int sms, Plan *pl, Mod
     }
     if (mode == Mode::FROM_CARRIES && v->walk) v = &kBwdGiven;
     const bool stateful = v->chain || v->segk > 0;
-    const int vthree = bf16 ? kFwdBf16Three : kThreeFwd;
-    const Variant *three = bf16 ? &kFwdBf16Variants[vthree] : &kFwdVariants[vthree];
+    const int vthree = bf16 ? (bwd ? kBwdBf16Three : kFwdBf16Three) : (bwd ? kThreeBwd : kThreeFwd);
+    const Variant *three = bf16 ? (bwd ? &kBwdBf16Variants[vthree] : &kFwdBf16Variants[vthree])
+                                : (bwd ? &kBwdVariants[vthree] : &kFwdVariants[vthree]);
     if (capturing && stateful) {
         vi = vthree;
         v = three;
@@ -727,6 +794,18 @@ int layout_plan(bool bwd, int64_t B, int64_t S, int64_t HJ, int sms, Plan *pl, M
     g.NL = (int)(NG * LT);
     const size_t per = (size_t)pl->tiles * LT * 16;
     size_t off = sizeof(qs::WsHeader);
+    if (pl->v->segk > 0 && bwd) {
+        // Backward segmented walk: the look-back values live apart (LbValues),
+        // the ticket counters in the head of the status-word allocation; the
+        // workspace holds the carries of the carries-only pass, [B, C, H*J].
+        pl->o_L = kFlagsHead;
+        if (mode != Mode::FROM_CARRIES) {
+            pl->o_F = off;
+            off = align_up(off + (size_t)B * C * HJ * 16, 256);
+        }
+        pl->ws_bytes = off;
+        return QS_OK;
+    }
     if (pl->v->segk > 0) {
         // Segmented chained walk: per unit (segment, lane group) and lane the
         // segment product and the inclusive value; the status words and the
@@ -794,6 +873,101 @@ int layout_plan(bool bwd, int64_t B, int64_t S, int64_t HJ, int sms, Plan *pl, M
     return QS_OK;
 }
 
+// The control block of a launch: the wait limit, the test hook's stalled tile
+// (`stall`: this launch is the first kernel of its call) and the status block.
+qs::Control control_block(unsigned char *ws, bool stall) {
+    qs::Control ctl;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        ctl.timeout_ns = g_timeout_ns;
+        ctl.stall_tile = stall ? g_stall_tile : -1;
+    }
+    ctl.hdr = reinterpret_cast<qs::WsHeader *>(ws);
+    return ctl;
+}
+
+// Geometry of LT-lane groups and T-step chunks.
+qs::Geometry geometry(int64_t B, int64_t S, int64_t HJ, int LT, int T) {
+    qs::Geometry g;
+    g.S = S;
+    g.HJ = (int)HJ;
+    g.NGb = (int)((HJ + LT - 1) / LT);
+    g.NG = (int)(B * g.NGb);
+    g.C = (int)((S + T - 1) / T);
+    g.NL = g.NG * LT;
+    return g;
+}
+
+// The backward segmented walk (pl.v): without saved carries, first the
+// carries-only forward pass writes every chunk's carry into the workspace.
+// Both launches are enqueued under the look-back buffers' ordering lock.
+int launch_segwalk_bwd(const Plan &pl, int dev, unsigned char *ws, const void *q, const void *d_cum, void *d_q,
+                       const void *init, void *d_init, int64_t B, int64_t S, int64_t HJ, cudaStream_t stream,
+                       Mode mode, float *carries, bool bf16) {
+    const Variant *v = pl.v;
+    const int eb = bf16 ? 8 : 16;
+    uint32_t epoch = 0, *flags = nullptr;
+    int rc = chain_flags(dev, stream, pl.o_L, &flags, &epoch);
+    if (rc != QS_OK) return rc;
+    unsigned int *tickets = flags;   // counters, zero between launches (shared: launches on a stream are ordered)
+    std::lock_guard<std::mutex> order(g_lbv_launch_mu);
+    const float4 *car = reinterpret_cast<const float4 *>(carries);
+    const bool pass = mode != Mode::FROM_CARRIES;
+    if (pass) {
+        const Variant &pv = kCarriesPassVariant;
+        qs::Geometry pg = geometry(B, S, HJ, pv.lt, pv.T());
+        CUtensorMap pmap;
+        rc = make_map(&pmap, q, B, S, HJ, pv.lt, pv.T(), eb);
+        if (rc != QS_OK) return rc;
+        int grid = 0;
+        rc = persistent_grid(dev, &pv, &grid);
+        if (rc != QS_OK) return rc;
+        const long long units = (long long)pg.NG * ((pg.C + pv.segk - 1) / pv.segk);
+        if (grid > units) grid = (int)units;
+        float4 *cur[kLbMaxArrays], *nxt[kLbMaxArrays];
+        rc = lb_values(dev, stream, LB_CARRIES, units * pv.lt, 2, cur, nxt);
+        if (rc != QS_OK) return rc;
+        qs::Control ctl = control_block(ws, true);
+        float4 *carw = reinterpret_cast<float4 *>(ws + pl.o_F);
+        const void *init4 = init;
+        void *args[] = {&pmap, &init4, &carw, &tickets, &cur[0], &cur[1], &nxt[0], &nxt[1], &pg, &ctl};
+        if (cudaLaunchKernel(pv.agg, dim3((unsigned)grid), dim3(pv.threads()), args, pv.smem(), stream) !=
+            cudaSuccess) {
+            cudaGetLastError();
+            lb_values_invalidate(dev, stream, LB_CARRIES);
+            return QS_ERR_CUDA;
+        }
+        car = carw;
+    }
+    CUtensorMap qmap, dmap;
+    rc = make_map(&qmap, q, B, S, HJ, v->lt, v->T(), eb);
+    if (rc == QS_OK) rc = make_map(&dmap, d_cum, B, S, HJ, v->lt, v->T(), eb);
+    if (rc != QS_OK) return rc;
+    int grid = 0;
+    rc = persistent_grid(dev, v, &grid);
+    if (rc != QS_OK) return rc;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        if (g_bwd_cap > 0 && grid > g_bwd_cap) grid = g_bwd_cap;   // test hook: fewer CTAs in flight
+    }
+    const long long units = (long long)pl.geo.NG * ((pl.geo.C + v->segk - 1) / v->segk);
+    if (grid > units) grid = (int)units;
+    float4 *cur[kLbMaxArrays], *nxt[kLbMaxArrays];
+    rc = lb_values(dev, stream, LB_BWD, units * v->lt, 3, cur, nxt);
+    if (rc != QS_OK) return rc;
+    qs::Control ctl = control_block(ws, !pass);
+    qs::Geometry geo = pl.geo;
+    void *dq4 = d_q, *dinit4 = d_init;
+    void *args[] = {&qmap, &dmap, &car, &dq4, &dinit4, &tickets, &cur[0], &cur[1], &cur[2], &nxt[0], &nxt[1],
+                    &nxt[2], &geo, &ctl};
+    if (cudaLaunchKernel(v->agg, dim3((unsigned)grid), dim3(v->threads()), args, v->smem(), stream) != cudaSuccess) {
+        cudaGetLastError();
+        lb_values_invalidate(dev, stream, LB_BWD);
+        return QS_ERR_CUDA;
+    }
+    return QS_OK;
+}
+
 // `carries`: written (Mode::SAVE_CARRIES) or read (Mode::FROM_CARRIES),
 // [B, ceil(S / QS_CARRY_STEPS), H*J] float4; unused otherwise.
 // `bf16`: the tensors hold bfloat16 quaternions (8 bytes); walk kernels only.
@@ -820,6 +994,8 @@ int launch(bool bwd, const void *q, const void *d_cum, void *out, const void *in
     rc = make_map(&qmap, q, B, S, HJ, pl.v->lt, pl.v->T(), eb);
     if (rc == QS_OK) rc = make_map(&dmap, bwd ? d_cum : q, B, S, HJ, pl.v->lt, pl.v->T(), eb);
     if (rc != QS_OK) return rc;
+    if (pl.v->segk > 0 && bwd) return launch_segwalk_bwd(pl, dev, ws, q, d_cum, out, init, d_init, B, S, HJ, stream,
+                                                           mode, carries, bf16);
     if (pl.v->segk > 0) {
         uint32_t epoch = 0, *flags = nullptr;
         rc = chain_flags(dev, stream, pl.o_L, &flags, &epoch);
@@ -829,15 +1005,10 @@ int launch(bool bwd, const void *q, const void *d_cum, void *out, const void *in
         if (rc != QS_OK) return rc;
         const long long units = (long long)pl.geo.NG * ((pl.geo.C + pl.v->segk - 1) / pl.v->segk);
         if (grid > units) grid = (int)units;
-        qs::Control ctl;
-        {
-            std::lock_guard<std::mutex> lk(g_mu);
-            ctl.timeout_ns = g_timeout_ns;
-            ctl.stall_tile = g_stall_tile;
-        }
-        ctl.hdr = reinterpret_cast<qs::WsHeader *>(ws);
+        qs::Control ctl = control_block(ws, true);
         const void *init4 = init;
         void *out4 = out;
+        float4 *save4 = mode == Mode::SAVE_CARRIES ? reinterpret_cast<float4 *>(carries) : nullptr;
         unsigned int *tickets = flags;   // counters, zero between launches
         uint32_t *status = flags + kFlagsHead / 4;
         float4 *aggv = reinterpret_cast<float4 *>(ws + pl.o_W);
@@ -846,15 +1017,20 @@ int launch(bool bwd, const void *q, const void *d_cum, void *out, const void *in
         std::unique_lock<std::mutex> order(g_lbv_launch_mu, std::defer_lock);
         if (pl.v->sent) {
             order.lock();
-            rc = lb_values(dev, stream, units * pl.v->lt, &aggv, &inclv, &agg_next, &incl_next);
+            float4 *cur[kLbMaxArrays], *nxt[kLbMaxArrays];
+            rc = lb_values(dev, stream, LB_FWD, units * pl.v->lt, 2, cur, nxt);
             if (rc != QS_OK) return rc;
+            aggv = cur[0];
+            inclv = cur[1];
+            agg_next = nxt[0];
+            incl_next = nxt[1];
         }
-        void *args[] = {&qmap, &init4, &out4, &status, &tickets, &aggv, &inclv, &agg_next, &incl_next,
+        void *args[] = {&qmap, &init4, &out4, &save4, &status, &tickets, &aggv, &inclv, &agg_next, &incl_next,
                         &pl.geo, &ctl, &epoch};
         if (cudaLaunchKernel(pl.v->agg, dim3((unsigned)grid), dim3(pl.v->threads()), args, pl.v->smem(), stream) !=
             cudaSuccess) {
             cudaGetLastError();
-            if (pl.v->sent) lb_values_invalidate(dev, stream);
+            if (pl.v->sent) lb_values_invalidate(dev, stream, LB_FWD);
             return QS_ERR_CUDA;
         }
         return QS_OK;
@@ -1361,7 +1537,8 @@ extern "C" int quat_cumprod_plan(int call, int64_t B, int64_t S, int64_t H, int6
     rc = make_plan(bwd, B, S, H * J, di->sms, &pl, mode, bf16);
     if (rc != QS_OK) return rc;
     *variant = pl.vi;
-    *kernels = (pl.v->walk || pl.v->chain || pl.v->segk > 0) ? 1 : (mode == Mode::SAVE_CARRIES ? 4 : 3);
+    if (pl.v->segk > 0 && bwd) *kernels = mode == Mode::FROM_CARRIES ? 1 : 2;   // (+ the carries-only pass)
+    else *kernels = (pl.v->walk || pl.v->chain || pl.v->segk > 0) ? 1 : (mode == Mode::SAVE_CARRIES ? 4 : 3);
     return QS_OK;
 }
 

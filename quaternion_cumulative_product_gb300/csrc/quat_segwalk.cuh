@@ -60,10 +60,13 @@ __device__ __forceinline__ float4 lb_unpublished() {
     return make_float4(n, n, n, n);
 }
 
+// `carries` (may be null): [B, C, H*J] float4, the state entering every
+// chunk, carries[b, c] = cum[b, c*T - 1] (init for c = 0).
 template <typename IO, int LT, int NSEG, int N, int NST, int K, bool SENT = false>
 __global__ void __launch_bounds__(LT *NSEG)
     quat_segwalk_fwd_kernel(const __grid_constant__ CUtensorMap qmap, const typename IO::elem *__restrict__ init,
-                            typename IO::elem *__restrict__ out, uint32_t *__restrict__ flags,
+                            typename IO::elem *__restrict__ out, float4 *__restrict__ carries,
+                            uint32_t *__restrict__ flags,
                             unsigned int *__restrict__ ctr, float4 *__restrict__ agg,
                             float4 *__restrict__ incl, float4 *__restrict__ agg_next, float4 *__restrict__ incl_next,
                             const Geometry geo, const Control ctl, uint32_t epoch) {
@@ -345,6 +348,8 @@ __global__ void __launch_bounds__(LT *NSEG)
                 if (kk < seg) Pr = q_mul(s_a[sl][kk][lane], Pr);
             const float4 Y = q_mul(Pr, s_x[sl][lane]);
             if (seg == 0) {
+                if (carries != nullptr && lane_ok)   // the state entering chunk c0 + j
+                    carries[(static_cast<long long>(b) * C + c0 + j) * geo.HJ + hj] = R;
                 float4 L = q_ident();
 #pragma unroll
                 for (int kk = 0; kk < NSEG; ++kk) L = q_mul(s_a[sl][kk][lane], L);

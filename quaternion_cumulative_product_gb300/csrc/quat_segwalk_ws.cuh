@@ -54,6 +54,118 @@ __device__ __forceinline__ void compute_sync() {
     asm volatile("bar.sync 1, %0;" ::"n"(NT) : "memory");
 }
 
+// Look-back of one lane (decoupled look-back over the segments of its lane
+// group).  A round loads the LB nearest predecessors not yet folded, together
+// (one memory latency), and folds the published ones in order, up to the
+// first inclusive value; at the first one not yet published it stops and the
+// next round loads afresh from there, so a value loaded before a wait is
+// never used after it.  Only the nearest unfolded predecessor is waited for.
+// A predecessor counts as published once none of its words holds the
+// all-ones pattern.  A wait that runs out is recorded (as `item`) and gives NaN.
+
+// H entering segment p of lane group g from the right: the maps of segments
+// p-1, p-2, ... composed back to the nearest published inclusive value.
+template <int LB>
+__device__ __forceinline__ float4 lookback_maps(const float4 *aggV, const float4 *aggA, const float4 *incl, int p,
+                                                int g, int NG, int LT, int lane, const Control &ctl, int item) {
+    // H_right = aV + aM (x) (what lies further right)
+    float4 aV = q_zero(), aM = q_ident();
+    int base = p - 1;
+    for (;;) {
+        float4 v[LB], a[LB], h[LB];
+#pragma unroll
+        for (int j = 0; j < LB; ++j) {
+            const long long idx = (static_cast<long long>(base - j < 0 ? 0 : base - j) * NG + g) * LT + lane;
+            h[j] = __ldcg(incl + idx);
+            v[j] = __ldcg(aggV + idx);
+            a[j] = __ldcg(aggA + idx);
+        }
+        int folded = 0;
+        bool gap = false;
+#pragma unroll
+        for (int j = 0; j < LB; ++j) {
+            if (gap) continue;
+            if (base - j < 0) return aV;   // past the right end of the sequence: H = 0 there
+            if (lb_published(h[j])) return q_fma(aV, aM, h[j]);
+            if (lb_published(v[j]) && lb_published(a[j])) {
+                aV = q_fma(aV, aM, v[j]);
+                aM = q_mul_cr(aM, a[j]);
+                ++folded;
+            } else {
+                gap = true;
+            }
+        }
+        base -= folded;
+        if (folded > 0) continue;
+        // The nearest predecessor is not published yet: wait for it.
+        const long long idx = (static_cast<long long>(base) * NG + g) * LT + lane;
+        const unsigned long long t0 = global_timer_ns();
+        float4 hv, vv, av;
+        do {
+            if (global_timer_ns() - t0 > ctl.timeout_ns) {
+                record_error(ctl.hdr, item);
+                return q_nan();
+            }
+            hv = __ldcg(incl + idx);
+            vv = __ldcg(aggV + idx);
+            av = __ldcg(aggA + idx);
+        } while (!lb_published(hv) && !(lb_published(vv) && lb_published(av)));
+        if (lb_published(hv)) return q_fma(aV, aM, hv);
+        aV = q_fma(aV, aM, vv);
+        aM = q_mul_cr(aM, av);
+        --base;
+    }
+}
+
+// The carry entering segment p of lane group g from the left (forward): the
+// products of segments p-1, p-2, ... back to the nearest published inclusive
+// value, the product itself included.
+template <int LB>
+__device__ __forceinline__ float4 lookback_products(const float4 *agg, const float4 *incl, int p, int g, int NG,
+                                                    int LT, int lane, const Control &ctl, int item) {
+    float4 acc = q_ident();
+    int base = p - 1;
+    for (;;) {
+        float4 av[LB], iv[LB];
+#pragma unroll
+        for (int j = 0; j < LB; ++j) {
+            const long long idx = (static_cast<long long>(base - j < 0 ? 0 : base - j) * NG + g) * LT + lane;
+            av[j] = __ldcg(agg + idx);
+            iv[j] = __ldcg(incl + idx);
+        }
+        int folded = 0;
+        bool gap = false;
+#pragma unroll
+        for (int j = 0; j < LB; ++j) {
+            if (gap) continue;
+            if (base - j < 0) return acc;   // before segment 0: an inclusive identity
+            if (lb_published(iv[j])) return q_mul(acc, iv[j]);
+            if (lb_published(av[j])) {
+                acc = q_mul(acc, av[j]);
+                ++folded;
+            } else {
+                gap = true;
+            }
+        }
+        base -= folded;
+        if (folded > 0) continue;
+        const long long idx = (static_cast<long long>(base) * NG + g) * LT + lane;
+        const unsigned long long t0 = global_timer_ns();
+        float4 a1, i1;
+        do {
+            if (global_timer_ns() - t0 > ctl.timeout_ns) {
+                record_error(ctl.hdr, item);
+                return q_nan();
+            }
+            a1 = __ldcg(agg + idx);
+            i1 = __ldcg(incl + idx);
+        } while (!lb_published(i1) && !lb_published(a1));
+        if (lb_published(i1)) return q_mul(acc, i1);
+        acc = q_mul(acc, a1);
+        --base;
+    }
+}
+
 // The carry entering segment p of lane group g for one lane, from look-back
 // values that carry their own state (see quat_segwalk_fwd_kernel, SENT): per
 // round the LB predecessors' products and inclusive values are loaded
@@ -96,12 +208,14 @@ __device__ __forceinline__ float4 segment_lookback_values(const float4 *agg, con
     }
 }
 
+// `carries` (may be null): [B, C, H*J] float4, the state entering every
+// chunk, carries[b, c] = cum[b, c*T - 1] (init for c = 0).
 template <typename IO, int LT, int NSEG, int N, int NST, int K, bool SENT = false>
 __global__ void __launch_bounds__(LT *NSEG + 64)
     quat_segwalk_ws_fwd_kernel(const __grid_constant__ CUtensorMap qmap, const typename IO::elem *__restrict__ init,
-                               typename IO::elem *__restrict__ out, uint32_t *__restrict__ flags,
-                               unsigned int *__restrict__ ctr, float4 *__restrict__ agg,
-                               float4 *__restrict__ incl, float4 *__restrict__ agg_next,
+                               typename IO::elem *__restrict__ out, float4 *__restrict__ carries,
+                               uint32_t *__restrict__ flags, unsigned int *__restrict__ ctr,
+                               float4 *__restrict__ agg, float4 *__restrict__ incl, float4 *__restrict__ agg_next,
                                float4 *__restrict__ incl_next, const Geometry geo, const Control ctl,
                                uint32_t epoch) {
     using E = typename IO::elem;
@@ -354,6 +468,8 @@ __global__ void __launch_bounds__(LT *NSEG + 64)
                     if (kk < seg) Pr = q_mul(s_a[sl][kk][lane], Pr);
                 const float4 Y = q_mul(Pr, s_x[sl][lane]);
                 if (seg == 0) {
+                    if (carries != nullptr && lane_ok)   // the state entering chunk c0 + j
+                        carries[(static_cast<long long>(b) * C + c0 + j) * geo.HJ + hj] = R;
                     float4 L = q_ident();
 #pragma unroll
                     for (int kk = 0; kk < NSEG; ++kk) L = q_mul(s_a[sl][kk][lane], L);

@@ -106,11 +106,58 @@ def test_carry_calls_at_full_size_match_the_plain_calls(dev):
     assert normwise(gq, rq) <= TOL and normwise(gi, ri) <= TOL
 
 
-def test_plan_counts_the_export_kernel(dev):
-    # few lanes: aggregate / carry / apply, plus the carry export for the forward
+def test_plan_counts_the_kernels_of_the_carry_calls(dev):
+    # few lanes: the segmented walks, which write and read the carries themselves
+    assert qs.quat_cumprod_plan("fwd_carries", 1, 4096, 1, 4, device=dev)[1] == 1
+    assert qs.quat_cumprod_plan("bwd_carries", 1, 4096, 1, 4, device=dev)[1] == 1
+    assert qs.quat_cumprod_plan("bwd", 1, 4096, 1, 4, device=dev)[1] == 3   # recompute: aggregate / carry / apply
+    assert qs.quat_cumprod_plan("bwd", 1, 4096, 32, 32, device=dev)[1] == 2  # 64 groups: + the carries-only pass
+    assert qs.quat_cumprod_plan("fwd_carries", 8, 4096, 16, 32, device=dev)[1] == 1
+    # forced aggregate / carry / apply: plus the carry export for the forward
+    lib = qs.load_library()
+    assert lib.quat_cumprod_debug_set_variant(0, 0) == qs.QS_OK
     assert qs.quat_cumprod_plan("fwd_carries", 1, 4096, 1, 4, device=dev)[1] == 4
     assert qs.quat_cumprod_plan("bwd_carries", 1, 4096, 1, 4, device=dev)[1] == 3
-    assert qs.quat_cumprod_plan("fwd_carries", 8, 4096, 16, 32, device=dev)[1] == 1
+
+
+# The segmented walks of both directions (forward 12: one role, 14:
+# warp-specialised; backward 11-14) write and read the carries themselves.
+@pytest.mark.parametrize("fv,bv", [(12, 11), (14, 11), (12, 12), (14, 13), (14, 14), (9, 11)])
+@pytest.mark.parametrize("dims", [(2, 333, 3, 16), (1, 63, 1, 1), (1, 20000, 1, 3), (2, 17000, 2, 5)])
+def test_segmented_walks_write_and_read_carries(dev, fv, bv, dims):
+    lib = qs.load_library()
+    assert lib.quat_cumprod_debug_set_variant(fv, bv) == qs.QS_OK
+    assert qs.quat_cumprod_plan("bwd_carries", *dims, device=dev) == (bv, 1)
+    w = workloads.custom("segcarries", *dims, q_kind="rotation", theta_max=0.5, seed=fv * 16 + bv)
+    q, init, d_cum = workloads.make_inputs(w)
+    tq, ti, td = to_dev(dev, q, init, d_cum)
+    cum, carries = qs.quat_cumprod_fwd_carries(tq, ti)
+    d_q, d_init = qs.quat_cumprod_bwd_carries(tq, carries, td)
+    assert qs.quat_cumprod_status(device=dev) == qs.QS_OK
+    ref_cum = oracle.fwd(q, init)
+    ref_dq, ref_di = oracle.bwd(q, init, d_cum)
+    assert normwise(cum.cpu().numpy(), ref_cum) <= TOL
+    assert normwise(carries.cpu().numpy(), expected_carries(ref_cum, init)) <= TOL
+    assert normwise(d_q.cpu().numpy(), ref_dq) <= TOL
+    assert normwise(d_init.cpu().numpy(), ref_di) <= TOL
+
+
+def test_long_from_saved_carries_full_size_sampled_lanes(dev):
+    """The long workload (1 x 131072 x 16 x 16) at full size through the
+    segmented walks of both directions, compared on sampled whole lanes."""
+    w = workloads.WORKLOADS["long"]
+    assert qs.quat_cumprod_plan("bwd_carries", w.B, w.S, w.H, w.J, device=dev) == (11, 1)
+    q, init, d_cum = workloads.make_inputs(w)
+    tq, ti, td = to_dev(dev, q, init, d_cum)
+    _, carries = qs.quat_cumprod_fwd_carries(tq, ti)
+    d_q, d_init = qs.quat_cumprod_bwd_carries(tq, carries, td)
+    assert qs.quat_cumprod_status(device=dev) == qs.QS_OK
+    lanes = np.unique(np.concatenate([[0, 15, 16, w.lanes - 1],
+                                      np.random.default_rng(8).choice(w.lanes, 24, replace=False)]))
+    sq, si, sd = workloads.sample_lanes((q, init, d_cum), lanes, w.H, w.J)
+    rq, ri = oracle.bwd(sq, si, sd)
+    gq, gi = workloads.sample_lanes((d_q.cpu().numpy(), d_init.cpu().numpy()), lanes, w.H, w.J)
+    assert normwise(gq, rq) <= TOL and normwise(gi, ri) <= TOL
 
 
 # ---------------------------------------------------------------------------

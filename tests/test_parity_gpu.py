@@ -194,9 +194,11 @@ def test_empty_sizes(dev):
 # (forward 8: chained scan; 9: segmented chained walk; 10, 11: the same,
 # warp-specialised; 12: as 9, look-back values that carry their own state, read
 # in one round trip; 13, 14: as 10, 11 with those values; backward 10: at most
-# two CTAs per SM, more lane groups in waves).
-N_FWD_VARIANTS, N_BWD_VARIANTS = 15, 11
+# two CTAs per SM, more lane groups in waves; backward 11-14: the segmented
+# walk of the backward, after its carries-only forward pass).
+N_FWD_VARIANTS, N_BWD_VARIANTS = 15, 21
 SEGWALK_FWD = [9, 10, 11, 12, 13, 14]
+SEGWALK_BWD = [11, 12, 13, 14, 15, 16, 17, 18, 19, 20]
 
 
 @pytest.mark.parametrize("variant", range(max(N_FWD_VARIANTS, N_BWD_VARIANTS)))
@@ -457,6 +459,137 @@ def test_binding_rejects_bad_tensors(dev):
     assert ei.value.status == qs.QS_ERR_ALIAS
 
 
+@pytest.mark.parametrize("variant", SEGWALK_BWD)
+@pytest.mark.parametrize("dims", [(1, 20000, 1, 3), (2, 17000, 2, 5), (1, 131072 // 8, 2, 16), (3, 64 * 9 + 1, 1, 33)])
+def test_segmented_backward_long_sequences(dev, variant, dims):
+    """Many segments per lane (up to 79): the backward's look-back chains the
+    segments' affine maps from the right end; ragged last chunk and lane group.
+    Two launches in a row read the two sets of look-back buffers in turn."""
+    lib = qs.load_library()
+    assert lib.quat_cumprod_debug_set_variant(-1, variant) == qs.QS_OK
+    w = workloads.custom("segbwd", *dims, q_kind="rotation", theta_max=0.3, seed=170 + variant)
+    q, init, d_cum = workloads.make_inputs(w)
+    tq, ti, td = (torch.from_numpy(a).to(dev) for a in (q, init, d_cum))
+    rq, ri = oracle.bwd(q, init, d_cum)
+    for _ in range(2):
+        d_q, d_init = qs.quat_cumprod_bwd(tq, ti, td)
+        assert qs.quat_cumprod_status(device=dev) == qs.QS_OK
+        assert_parity(d_q.cpu().numpy(), rq, "d_q")
+        assert_parity(d_init.cpu().numpy(), ri, "d_init")
+    _, carries = qs.quat_cumprod_fwd_carries(tq, ti)   # and from saved carries
+    d_q, d_init = qs.quat_cumprod_bwd_carries(tq, carries, td)
+    assert qs.quat_cumprod_status(device=dev) == qs.QS_OK
+    assert_parity(d_q.cpu().numpy(), rq, "d_q (from carries)")
+    assert_parity(d_init.cpu().numpy(), ri, "d_init (from carries)")
+
+
+def test_segmented_backward_non_unit_quaternions(dev):
+    """The affine segment maps are exact for every quaternion: strongly non-unit
+    q over many segments (norms drift far from one along the sequence)."""
+    rng = np.random.default_rng(9)
+    B, S, H, J = 1, 5000, 2, 8
+    q = rng.standard_normal((B, S, H, J, 4))
+    q /= np.linalg.norm(q, axis=-1, keepdims=True)
+    q *= rng.uniform(0.999, 1.0012, (B, S, H, J, 1))
+    q = q.astype(np.float32)
+    init = (rng.standard_normal((B, H, J, 4)) * 3).astype(np.float32)
+    d_cum = rng.standard_normal(q.shape).astype(np.float32)
+    lib = qs.load_library()
+    assert lib.quat_cumprod_debug_set_variant(-1, 11) == qs.QS_OK
+    check_against_oracle(dev, q, init, d_cum)
+
+
+def test_segmented_backward_alternating_layouts(dev):
+    """Forward, backward and the backward's carries pass each keep their own
+    look-back buffers between launches on a stream: shapes that alternate
+    change the layouts, repeats reuse them, and every result must match."""
+    lib = qs.load_library()
+    assert lib.quat_cumprod_debug_set_variant(-1, 11) == qs.QS_OK
+    cases = []
+    for i, dims in enumerate([(1, 20000, 1, 3), (2, 17000, 2, 5), (1, 9000, 2, 16)]):
+        w = workloads.custom("segbwd_alt", *dims, q_kind="rotation", theta_max=0.3, seed=180 + i)
+        q, init, d_cum = workloads.make_inputs(w)
+        cases.append((q, init, d_cum, oracle.fwd(q, init), *oracle.bwd(q, init, d_cum)))
+    for k in [0, 0, 1, 0, 2, 2, 2, 1, 1, 0]:
+        q, init, d_cum, rc, rq, ri = cases[k]
+        tq, ti, td = (torch.from_numpy(a).to(dev) for a in (q, init, d_cum))
+        cum = qs.quat_cumprod_fwd(tq, ti)
+        d_q, d_init = qs.quat_cumprod_bwd(tq, ti, td)
+        assert qs.quat_cumprod_status(device=dev) == qs.QS_OK
+        assert_parity(cum.cpu().numpy(), rc, f"cum (case {k})")
+        assert_parity(d_q.cpu().numpy(), rq, f"d_q (case {k})")
+        assert_parity(d_init.cpu().numpy(), ri, f"d_init (case {k})")
+
+
+@pytest.mark.parametrize("saved", [False, True])
+def test_segmented_backward_stall_reports_timeout_then_recovers(dev, saved):
+    """The stall hook holds the first kernel of the call: the carries-only pass
+    of the recompute backward, or the segmented backward itself when it starts
+    from saved carries.  Either way the call reports QS_ERR_TIMEOUT, and the
+    next calls (which read the other set of look-back buffers) are clean."""
+    lib = qs.load_library()
+    assert lib.quat_cumprod_debug_set_variant(-1, 11) == qs.QS_OK
+    w = workloads.custom("segbwd_stall", 2, 3000, 2, 16, seed=24)
+    q, init, d_cum = workloads.make_inputs(w)
+    tq, ti, td = (torch.from_numpy(a).to(dev) for a in (q, init, d_cum))
+    assert qs.quat_cumprod_plan(True, 2, 3000, 2, 16, device=dev) == (11, 2)
+    _, carries = qs.quat_cumprod_fwd_carries(tq, ti)
+    assert qs.quat_cumprod_status(device=dev) == qs.QS_OK
+    lib.quat_cumprod_debug_set_timeout_ns(50_000_000)    # 50 ms
+    lib.quat_cumprod_debug_stall_tile(1)                 # chunk 0 of lane group 1
+    if saved:
+        qs.quat_cumprod_bwd_carries(tq, carries, td)
+    else:
+        qs.quat_cumprod_bwd(tq, ti, td)
+    assert qs.quat_cumprod_status(device=dev) == qs.QS_ERR_TIMEOUT
+    assert qs.quat_cumprod_status(device=dev) == qs.QS_OK
+    lib.quat_cumprod_debug_stall_tile(-1)
+    lib.quat_cumprod_debug_set_timeout_ns(0)
+    rq, ri = oracle.bwd(q, init, d_cum)
+    for _ in range(2):
+        d_q, d_init = (qs.quat_cumprod_bwd_carries(tq, carries, td) if saved else qs.quat_cumprod_bwd(tq, ti, td))
+        assert qs.quat_cumprod_status(device=dev) == qs.QS_OK
+        assert_parity(d_q.cpu().numpy(), rq, "d_q")
+        assert_parity(d_init.cpu().numpy(), ri, "d_init")
+
+
+def test_segmented_backward_from_concurrent_threads(dev):
+    """Host threads enqueue the segmented backward on streams of their own at
+    the same time: each stream keeps its own look-back buffers and workspace."""
+    import threading
+    lib = qs.load_library()
+    assert lib.quat_cumprod_debug_set_variant(-1, 11) == qs.QS_OK
+    cases = []
+    for i, dims in enumerate([(1, 20000, 2, 16), (2, 9000, 1, 32), (1, 30000, 1, 16)]):
+        w = workloads.custom("segbwd_threads", *dims, q_kind="rotation", theta_max=0.3, seed=190 + i)
+        q, init, d_cum = workloads.make_inputs(w)
+        cases.append((*(torch.from_numpy(a).to(dev) for a in (q, init, d_cum)), oracle.bwd(q, init, d_cum)[0]))
+    torch.cuda.synchronize(dev)
+    errors = []
+
+    def worker(k):
+        try:
+            torch.cuda.set_device(dev)
+            s = torch.cuda.Stream(device=dev)
+            tq, ti, td, ref = cases[k]
+            with torch.cuda.stream(s):
+                for _ in range(4):
+                    d_q, _ = qs.quat_cumprod_bwd(tq, ti, td)
+                    assert qs.quat_cumprod_status(stream=s, device=dev) == qs.QS_OK
+                    errors.append((k, normwise(d_q.cpu().numpy(), ref)))
+        except Exception as e:   # reported below
+            errors.append((k, repr(e)))
+
+    threads = [threading.Thread(target=worker, args=(k,)) for k in range(len(cases))]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert len(errors) == 4 * len(cases), errors
+    for k, e in errors:
+        assert isinstance(e, float) and e <= 1e-4, (k, e)
+
+
 # ---------------------------------------------------------------------------
 # Failure detection: a tile whose wait is made to expect bytes that never come
 # runs out its bounded wait; the call reports QS_ERR_TIMEOUT (no hang) and the
@@ -496,11 +629,26 @@ def test_plan_picks_the_design_by_lane_groups(dev, name, walk):
     w = workloads.WORKLOADS[name]
     for bwd in (False, True):
         variant, kernels = qs.quat_cumprod_plan(bwd, w.B, w.S, w.H, w.J, device=dev)
-        # few lane groups: the segmented chained walk forward (one kernel),
-        # aggregate / carry / apply backward
+        # few lane groups: the segmented chained walk forward (one kernel); for
+        # fewer than 64 sixteen-lane groups the aggregate / carry / apply backward
         assert kernels == (1 if walk or not bwd else 3), (name, bwd, variant, kernels)
         if not walk and not bwd:
             # the segmented walk with self-describing look-back values: the
             # warp-specialised form (14) from 2^24 elements, else the one-role form (12)
             assert variant == (14 if w.elements >= 1 << 24 else 12), (name, variant)
+        if not walk and bwd:
+            assert variant == 0, (name, variant)
     assert qs.quat_cumprod_plan(True, 2, 0, 3, 4, device=dev) == (-1, 0)
+
+
+def test_plan_picks_the_segmented_backward_for_many_groups(dev):
+    """64 or more 16-lane groups, too few for a walk: the recompute backward is
+    the carries pass and the segmented walk (segments of 2 chunks)."""
+    assert qs.quat_cumprod_plan(True, 1, 4096, 32, 32, device=dev) == (14, 2)   # 64 groups
+    assert qs.quat_cumprod_plan(True, 1, 4096, 31, 32, device=dev) == (0, 3)    # 62 groups
+    # from saved carries: the segmented walk whatever the group count
+    assert qs.quat_cumprod_plan("bwd_carries", 1, 131072, 16, 16, device=dev) == (11, 1)
+    assert qs.quat_cumprod_plan("bwd_carries", 4, 1024, 8, 16, device=dev) == (14, 1)   # few units
+    w = workloads.custom("manygroups", 1, 700, 32, 33, q_kind="rotation", theta_max=0.4, seed=200)
+    assert qs.quat_cumprod_plan(True, w.B, w.S, w.H, w.J, device=dev) == (14, 2)
+    check_against_oracle(dev, *workloads.make_inputs(w))
