@@ -39,12 +39,13 @@
  * Scratch memory: the calls use a library-owned workspace per (device,
  * stream) for a status block and per-chunk aggregates and carries.  Per lane
  * and 64-step chunk this is nothing for a forward walk, 16 bytes for a
- * backward walk, and 32 (forward) or 64 (backward) bytes for the aggregate /
- * carry / apply kernels (see quat_cumprod_plan for which a call uses).  The
- * segmented chained walk (the forward for few lane groups) keeps, per lane
- * and segment of 4 chunks, two copies of 32 bytes of look-back values plus a
- * few counters in further per-stream allocations, and reserves the aggregate
- * / carry / apply forward's workspace as well.  The first call on a stream,
+ * backward walk or the backward's segmented walk, and 32 (forward) or 64
+ * (backward) bytes for the aggregate / carry / apply kernels (see
+ * quat_cumprod_plan for which a call uses).  The segmented chained walks (for
+ * few lane groups) keep, per lane and segment of 2 or 4 chunks, two copies of
+ * 32 (forward) or 48 (backward) bytes of look-back values plus a few counters
+ * in further per-stream allocations, and reserve the aggregate / carry /
+ * apply workspace of the same direction as well.  The first call on a stream,
  * and any later call that needs more scratch, allocates it (cudaMalloc) and
  * synchronizes that stream; issue such a call before capturing the stream
  * into a CUDA graph.  While a stream is being captured the forward uses the
@@ -134,23 +135,26 @@ int quat_cumprod_bwd(const float *q, const float *init, const float *d_cum,
  * work tiles (for example B=8, S=4096, H=16, J=32 fits exactly); larger sizes
  * return QS_ERR_SCRATCH before anything is enqueued.
  *
- * Every call on a device shares that one array.  Each call clears the status
- * block on `stream` before its kernels run; everything else it reads it has
- * written earlier in the same call.  Calls whose work can overlap on the GPU
- * (calls on different streams without an ordering between them, or from
- * several host threads onto unordered streams) RACE on the array and give
- * wrong results; calls on one stream are ordered and safe.
+ * Every call on a device shares that one array.  Everything a call reads
+ * from it (chunk aggregates and carries) it has written earlier in the same
+ * call.  Calls whose work can overlap on the GPU (calls on different streams
+ * without an ordering between them, or from several host threads onto
+ * unordered streams) RACE on the array and give wrong results; calls on one
+ * stream are ordered and safe.
  *
  * Set-up: the first call on each device looks up the array's address on that
  * device (cudaGetSymbolAddress, with that device current) and prepares the
  * kernels' attributes; later calls reuse both.  Make that first call on each
- * device before any stream capture begins.
+ * device before any stream capture begins: a first call on a stream that is
+ * being captured returns QS_ERR_NOMEM and enqueues nothing.
  *
  * Errors as for quat_cumprod_bwd, plus QS_ERR_SCRATCH.  A device-side wait
  * that runs out (possible only if a tile's copy never lands) is recorded in
- * the array's status block, not in the per-stream word that
- * quat_cumprod_status() reads, so quat_cumprod_status() does not report it
- * for this entry point.  The debug stall hook does not apply to it.
+ * the array's own status block, which starts at zero when the library is
+ * loaded on the device and keeps the record across calls:
+ * quat_cumprod_status(stream) reads and clears it (besides the stream's own
+ * record), allocating nothing, so call it with the stream the no-alloc calls
+ * were enqueued on.  The debug stall hook applies as to quat_cumprod_bwd.
  */
 #define QS_NOALLOC_MAX_TILES 8192
 int quat_cumprod_bwd_noalloc(const float *q, const float *init, const float *d_cum,
@@ -186,9 +190,10 @@ int quat_cumprod_fwd_carries(const float *q, const float *init, float *cum, floa
 /*
  * Backward from the carries written by quat_cumprod_fwd_carries for the same
  * q and init: writes d_q and d_init as quat_cumprod_bwd(q, carries[:, 0],
- * d_cum) would.  When the lane groups are too few for a walk (see
- * quat_cumprod_plan) the carries serve only as init and the backward
- * recomputes the rest.  Arguments, layout and errors otherwise as
+ * d_cum) would, reading q and d_cum once (the walk, or for too few lane
+ * groups the segmented walk, takes every chunk's carry from `carries`; the
+ * aggregate / carry / apply kernels, which a debug setting can force, use
+ * them only as init).  Arguments, layout and errors otherwise as
  * quat_cumprod_bwd.
  */
 int quat_cumprod_bwd_carries(const float *q, const float *carries, const float *d_cum,
@@ -241,17 +246,20 @@ int quat_cumprod_fwd_bwd_host(const float *q, const float *init, const float *d_
  * Synchronizes `stream`, then returns QS_ERR_TIMEOUT if any call enqueued on it
  * since the previous quat_cumprod_status() recorded a device-side timeout
  * (its outputs are then invalid), QS_ERR_CUDA if the synchronization failed,
- * and QS_OK otherwise.  Clears the recorded error.
+ * and QS_OK otherwise.  Clears the recorded error.  It also reads and clears
+ * the record of quat_cumprod_bwd_noalloc's scratch on the current device (one
+ * record per device, shared by every stream).  It allocates nothing.
  */
 int quat_cumprod_status(void *stream);
 
 /*
  * Which compiled configuration a call with these sizes would use on the
  * current device, and how many kernels it launches: 1 for a walk (one CTA
- * per lane group streams the whole sequence), 3 for aggregate / carry /
- * apply (the sequence split into independent tiles, chosen when there are
- * too few lane groups to fill the GPU), plus 1 when the forward exports its
- * carries from that path.  `call`: 0 quat_cumprod_fwd, 1 quat_cumprod_bwd,
+ * per lane group streams the whole sequence) or a segmented walk (too few
+ * lane groups: the sequence cut into segments chained by look-back), 2 for
+ * the backward's segmented walk after its carries-only pass, 3 for
+ * aggregate / carry / apply (independent tiles), plus 1 when the forward
+ * exports its carries from that path.  `call`: 0 quat_cumprod_fwd, 1 quat_cumprod_bwd,
  * 2 quat_cumprod_fwd_carries, 3 quat_cumprod_bwd_carries, 4 quat_cumprod_fwd_bf16,
  * 5 quat_cumprod_bwd_bf16.  Writes
  * *variant = -1 and *kernels = 0 when the call would launch nothing.  Returns

@@ -350,6 +350,9 @@ struct Workspace {
     uint32_t epoch = 0;   // status words only: last epoch used
 };
 std::map<std::pair<int, uintptr_t>, Workspace> g_ws;
+// Device -> address of quat_cumprod_bwd_noalloc's fixed scratch array (set up
+// by that call's first use on the device).
+std::map<int, unsigned char *> g_noalloc_ptr;
 // Status words of the chained scan, per (device, stream): an allocation of
 // their own that no other kernel writes, zeroed when allocated.
 std::map<std::pair<int, uintptr_t>, Workspace> g_flags;
@@ -1495,24 +1498,32 @@ extern "C" int quat_cumprod_status(void *stream_) {
         cudaGetLastError();
         return QS_ERR_CUDA;
     }
-    unsigned char *base = nullptr;
+    // The stream's workspace, and the device's no-alloc scratch (set up by a
+    // quat_cumprod_bwd_noalloc call on this device); neither is allocated here.
+    unsigned char *bases[2] = {nullptr, nullptr};
     {
         std::lock_guard<std::mutex> lk(g_mu);
         auto it = g_ws.find({dev, reinterpret_cast<uintptr_t>(stream)});
-        if (it == g_ws.end() || !it->second.base) return QS_OK;
-        base = it->second.base;
+        if (it != g_ws.end()) bases[0] = it->second.base;
+        auto na = g_noalloc_ptr.find(dev);
+        if (na != g_noalloc_ptr.end()) bases[1] = na->second;
     }
-    qs::WsHeader h;
-    if (cudaMemcpy(&h, base, sizeof h, cudaMemcpyDeviceToHost) != cudaSuccess) {
-        cudaGetLastError();
-        return QS_ERR_CUDA;
+    int status = QS_OK;
+    for (unsigned char *base : bases) {
+        if (!base) continue;
+        qs::WsHeader h;
+        if (cudaMemcpy(&h, base, sizeof h, cudaMemcpyDeviceToHost) != cudaSuccess) {
+            cudaGetLastError();
+            return QS_ERR_CUDA;
+        }
+        if (h.err_code == 0) continue;
+        if (cudaMemset(base, 0, sizeof(qs::WsHeader)) != cudaSuccess) {
+            cudaGetLastError();
+            return QS_ERR_CUDA;
+        }
+        status = QS_ERR_TIMEOUT;
     }
-    if (h.err_code == 0) return QS_OK;
-    if (cudaMemset(base, 0, sizeof(qs::WsHeader)) != cudaSuccess) {
-        cudaGetLastError();
-        return QS_ERR_CUDA;
-    }
-    return QS_ERR_TIMEOUT;
+    return status;
 }
 
 extern "C" int quat_cumprod_plan(int call, int64_t B, int64_t S, int64_t H, int64_t J, int *variant, int *kernels) {
@@ -1617,17 +1628,23 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[NA_SCRATCH_BYTE
 
 namespace {
 
-std::map<int, unsigned char *> g_noalloc_ptr;   // device -> address of g_noalloc_scratch
-
 // Address of the scratch on the current device `dev`, looked up once per
-// device (the lookup loads this library's device code on that device).
-int noalloc_scratch(int dev, unsigned char **out) {
+// device (the lookup loads this library's device code on that device).  The
+// lookup is refused while `stream` is being captured (QS_ERR_NOMEM, as for a
+// workspace that would have to be set up during a capture).
+int noalloc_scratch(int dev, cudaStream_t stream, unsigned char **out) {
     std::lock_guard<std::mutex> lk(g_mu);
     auto it = g_noalloc_ptr.find(dev);
     if (it != g_noalloc_ptr.end()) {
         *out = it->second;
         return QS_OK;
     }
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) {
+        cudaGetLastError();
+        return QS_ERR_CUDA;
+    }
+    if (cs != cudaStreamCaptureStatusNone) return QS_ERR_NOMEM;
     void *p = nullptr;
     const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e != cudaSuccess || p == nullptr) {
@@ -1648,12 +1665,32 @@ long long noalloc_tiles(int64_t B, int64_t S, int64_t HJ) {
 
 int noalloc_launch(const float *q, const float *init, const float *d_cum, float *d_q, float *d_init, int64_t B,
                    int64_t S, int64_t HJ, cudaStream_t stream) {
+    // The first call on a device sets up the library there (kernel
+    // attributes, the array's address): not while the stream is captured.
+    int cur = 0;
+    if (cudaGetDevice(&cur) != cudaSuccess) {
+        cudaGetLastError();
+        return QS_ERR_CUDA;
+    }
+    bool ready;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        ready = g_noalloc_ptr.count(cur) != 0;
+    }
+    if (!ready) {
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) {
+            cudaGetLastError();
+            return QS_ERR_CUDA;
+        }
+        if (cs != cudaStreamCaptureStatusNone) return QS_ERR_NOMEM;
+    }
     DevInfo *di = nullptr;
     int dev = 0;
     int rc = device_info(&di, &dev);
     if (rc != QS_OK) return rc;
     unsigned char *ws = nullptr;
-    rc = noalloc_scratch(dev, &ws);
+    rc = noalloc_scratch(dev, stream, &ws);
     if (rc != QS_OK) return rc;
 
     qs::Geometry geo;
@@ -1670,33 +1707,30 @@ int noalloc_launch(const float *q, const float *init, const float *d_cum, float 
     float4 *aggW = carF + per / 16;
     float4 *carH = aggW + per / 16;
 
-    // The status block must start at zero; every aggregate and carry slot a
-    // call reads is written earlier in the same call.
-    if (cudaMemsetAsync(ws, 0, sizeof(qs::WsHeader), stream) != cudaSuccess) {
-        cudaGetLastError();
-        return QS_ERR_CUDA;
-    }
+    // Every aggregate and carry slot a call reads is written earlier in the
+    // same call.  The status block starts at zero (the array is zeroed when
+    // the library's device code is loaded) and keeps a timeout until
+    // quat_cumprod_status reads and clears it, as a stream's workspace does.
     CUtensorMap qmap, dmap;
     rc = make_map(&qmap, q, B, S, HJ, NA_LT, NA_T);
     if (rc == QS_OK) rc = make_map(&dmap, d_cum, B, S, HJ, NA_LT, NA_T);
     if (rc != QS_OK) return rc;
-    qs::Control ctl;
-    {
-        std::lock_guard<std::mutex> lk(g_mu);
-        ctl.timeout_ns = g_timeout_ns;
-    }
-    ctl.stall_tile = -1;
-    ctl.hdr = reinterpret_cast<qs::WsHeader *>(ws);
+    qs::Control ctl = control_block(ws, true);
     const float4 *init4 = reinterpret_cast<const float4 *>(init);
     float4 *dinit4 = reinterpret_cast<float4 *>(d_init);
     float4 *out4 = reinterpret_cast<float4 *>(d_q);
     const float4 *aggL_c = aggL, *aggW_c = aggW, *carF_c = carF, *carH_c = carH;
     int lt = NA_LT;
-    const int carry_lb = geo.C > 256 ? 8 : 32;
+    // The carry step as in quat_cumprod_bwd: 32 lanes per block up to 256
+    // chunks per lane, beyond that the scan over chunk ranges, kCarryScanLanes
+    // lanes per block.
+    const bool scan = geo.C > 256;
+    const int carry_lb = scan ? kCarryScanLanes : 32;
     const void *agg_fn = reinterpret_cast<const void *>(qs::quat_agg_kernel<qs::IoF32, true, NA_LT, NA_N>);
     const void *apply_fn = reinterpret_cast<const void *>(qs::quat_apply_kernel<qs::IoF32, true, NA_LT, NA_N>);
-    const void *carry_fn = carry_lb == 8 ? reinterpret_cast<const void *>(qs::quat_carry_kernel<qs::IoF32, true, 8>)
-                                         : reinterpret_cast<const void *>(qs::quat_carry_kernel<qs::IoF32, true, 32>);
+    const void *carry_fn =
+        scan ? reinterpret_cast<const void *>(qs::quat_carry_scan_kernel<qs::IoF32, true, kCarryScanLanes>)
+             : reinterpret_cast<const void *>(qs::quat_carry_kernel<qs::IoF32, true, 32>);
     const size_t smem = qs::tile_smem_bytes(true, NA_LT, NA_N);
     void *agg_args[] = {&qmap, &dmap, &aggL, &aggW, &geo, &ctl};
     void *carry_args[] = {&aggL_c, &aggW_c, &init4, &carF, &carH, &dinit4, &geo, &lt};

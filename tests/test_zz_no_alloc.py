@@ -191,3 +191,89 @@ def test_noalloc_binding_and_empty_sequence(dev):
     with pytest.raises(qs.QuatScanError) as ei:
         qs.quat_cumprod_bwd_noalloc(qb, ib, qb.clone(), torch.empty_like(qb), torch.empty_like(ib))
     assert ei.value.status == qs.QS_ERR_SCRATCH
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("dims", [(1, 40000, 1, 32), (1, 20000, 1, 33)])
+def test_noalloc_many_chunks_per_lane(dev, dims):
+    """More than 256 chunks per lane (625 and 313 chunks, the second with a
+    ragged lane group) but within the 8192 tiles: the carry step is the scan
+    over chunk ranges, as in quat_cumprod_bwd."""
+    import torch
+    w = workloads.custom("noalloc_long", *dims, q_kind="rotation", theta_max=0.3, seed=sum(dims))
+    arrays = workloads.make_inputs(w)
+    q, init, d_cum = _to_dev(dev, arrays)
+    d_q, d_init = torch.empty_like(q), torch.empty_like(init)
+    stream = torch.cuda.current_stream(dev)
+    rc = _noalloc(q, init, d_cum, d_q, d_init, stream)
+    assert rc == qs.QS_OK, qs.quat_cumprod_strerror(rc)
+    assert qs.quat_cumprod_status(device=dev) == qs.QS_OK
+    ref_dq, ref_di = qs.quat_cumprod_bwd(q, init, d_cum)
+    ora_dq, ora_di = oracle.bwd(*arrays)
+    assert normwise(d_q.cpu().numpy(), ref_dq.cpu().numpy()) <= TOL
+    assert normwise(d_init.cpu().numpy(), ref_di.cpu().numpy()) <= TOL
+    assert normwise(d_q.cpu().numpy(), ora_dq) <= TOL
+    assert normwise(d_init.cpu().numpy(), ora_di) <= TOL
+
+
+@pytest.mark.gpu
+def test_noalloc_timeout_is_reported_then_clears(dev):
+    """A tile whose copy never completes (the stall hook) makes the wait run
+    out; quat_cumprod_status reports it once, and the next call is clean."""
+    import torch
+    lib = qs.load_library()
+    stream = torch.cuda.current_stream(dev)
+    arrays = workloads.make_inputs(RAGGED)
+    q, init, d_cum = _to_dev(dev, arrays)
+    d_q, d_init = torch.empty_like(q), torch.empty_like(init)
+    assert qs.quat_cumprod_status(device=dev) == qs.QS_OK
+    try:
+        lib.quat_cumprod_debug_set_timeout_ns(50_000_000)   # 50 ms
+        lib.quat_cumprod_debug_stall_tile(0)
+        assert _noalloc(q, init, d_cum, d_q, d_init, stream) == qs.QS_OK
+        assert qs.quat_cumprod_status(device=dev) == qs.QS_ERR_TIMEOUT
+        assert qs.quat_cumprod_status(device=dev) == qs.QS_OK   # read once, then cleared
+    finally:
+        lib.quat_cumprod_debug_stall_tile(-1)
+        lib.quat_cumprod_debug_set_timeout_ns(0)
+    assert _noalloc(q, init, d_cum, d_q, d_init, stream) == qs.QS_OK
+    assert qs.quat_cumprod_status(device=dev) == qs.QS_OK
+    ora_dq, ora_di = oracle.bwd(*arrays)
+    assert normwise(d_q.cpu().numpy(), ora_dq) <= TOL
+    assert normwise(d_init.cpu().numpy(), ora_di) <= TOL
+
+
+_CAPTURE_FIRST = r"""
+import ctypes, sys, torch
+sys.path.insert(0, {root!r})
+import quaternion_cumulative_product_gb300 as qs
+lib = qs.load_library()
+dev = torch.device("cuda", 0)
+q = torch.zeros(1, 64, 1, 4, 4, device=dev); q[..., 0] = 1
+init = torch.zeros(1, 1, 4, 4, device=dev); init[..., 0] = 1
+d_cum, d_q, d_init = torch.ones_like(q), torch.empty_like(q), torch.empty_like(init)
+s = torch.cuda.Stream(device=dev)
+g = torch.cuda.CUDAGraph()
+p = lambda t: ctypes.c_void_p(t.data_ptr())
+with torch.cuda.graph(g, stream=s):
+    rc = lib.quat_cumprod_bwd_noalloc(p(q), p(init), p(d_cum), p(d_q), p(d_init), 1, 64, 1, 4,
+                                      ctypes.c_void_p(s.cuda_stream))
+print("first", rc)
+rc2 = lib.quat_cumprod_bwd_noalloc(p(q), p(init), p(d_cum), p(d_q), p(d_init), 1, 64, 1, 4,
+                                   ctypes.c_void_p(s.cuda_stream))
+print("second", rc2, lib.quat_cumprod_status(ctypes.c_void_p(s.cuda_stream)))
+"""
+
+
+@pytest.mark.gpu
+def test_noalloc_first_call_during_capture_is_refused(dev):
+    """In a fresh process, a first call made while its stream is being captured
+    returns QS_ERR_NOMEM (its set-up is not done under a capture) and enqueues
+    nothing; the same call outside the capture then works."""
+    import subprocess
+    import sys
+    r = subprocess.run([sys.executable, "-c", _CAPTURE_FIRST.format(root=ROOT)], capture_output=True, text=True,
+                       timeout=300)
+    assert r.returncode == 0, r.stdout + r.stderr
+    assert f"first {qs.QS_ERR_NOMEM}" in r.stdout, r.stdout
+    assert f"second {qs.QS_OK} {qs.QS_OK}" in r.stdout, r.stdout
