@@ -300,6 +300,96 @@ def run_reference(args, w, world, rank):
     return 0
 
 
+def time_other_workload(qs, torch, name, dev, stream, steps, warmup, peak):
+    """The step, each call alone and the saved-carries step of another workload.
+
+    Inputs are drawn on the device (``workloads.make_inputs_device``: the same
+    distributions as the seeded table, torch's generator); L2 is flushed by a
+    read before every step and every rep when a tensor is smaller than twice
+    the L2 size.
+    """
+    wl = workloads.WORKLOADS[name]
+    E = wl.elements
+    q, init, d_cum = workloads.make_inputs_device(wl, dev)
+    cum, d_q, d_init = torch.empty_like(q), torch.empty_like(q), torch.empty_like(init)
+    carries = torch.empty((wl.B, (wl.S + qs.QS_CARRY_STEPS - 1) // qs.QS_CARRY_STEPS, wl.H, wl.J, 4),
+                          dtype=torch.float32, device=dev)
+    flush = q.numel() * 4 < 2 * L2_BYTES
+    flushbuf = torch.ones(2 * L2_BYTES // 4, device=dev)
+
+    def fwd():
+        qs.quat_cumprod_fwd(q, init, cum)
+
+    def bwd():
+        qs.quat_cumprod_bwd(q, init, d_cum, d_q, d_init)
+
+    def cfwd():
+        qs.quat_cumprod_fwd_carries(q, init, cum, carries)
+
+    def cbwd():
+        qs.quat_cumprod_bwd_carries(q, carries, d_cum, d_q, d_init)
+
+    def steps_of(a, b):
+        for _ in range(warmup):
+            a()
+            b()
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+        torch.cuda.synchronize(dev)
+        lead_spin()
+        for e0, e1, e2 in ev:
+            if flush:
+                flushbuf.sum()
+            e0.record(stream)
+            a()
+            e1.record(stream)
+            b()
+            e2.record(stream)
+        torch.cuda.synchronize(dev)
+        return (statistics.mean(x.elapsed_time(y) for x, y, _ in ev),
+                statistics.mean(y.elapsed_time(z) for _, y, z in ev))
+
+    def alone(calls, reps=20):
+        ms = []
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        for _ in range(reps):
+            flushbuf.sum()
+            a0.record(stream)
+            for c in calls:
+                c()
+            a1.record(stream)
+            a1.synchronize()
+            ms.append(a0.elapsed_time(a1))
+        return statistics.median(ms)
+
+    fwd_ms, bwd_ms = steps_of(fwd, bwd)
+    al = {"fwd": alone([fwd]), "bwd": alone([bwd]), "fwd_bwd": alone([fwd, bwd])}
+    cf_ms, cb_ms = steps_of(cfwd, cbwd)
+    st = qs.quat_cumprod_status(device=dev)
+    if st != qs.QS_OK:
+        raise RuntimeError(f"device status after workload {name}: {qs.quat_cumprod_strerror(st)}")
+
+    def frac(nbytes, ms):
+        return nbytes * E / (ms * 1e-3) / 1e9 / peak
+
+    plans = {c: qs.quat_cumprod_plan(c, wl.B, wl.S, wl.H, wl.J, device=dev)
+             for c in ("fwd", "bwd", "fwd_carries", "bwd_carries")}
+    return {
+        "config": wl.describe(), "elements": E, "steps": steps,
+        "l2": "flushed by a read before every step" if flush else "inputs larger than L2, no flush",
+        "inputs": "drawn on the device (workloads.make_inputs_device, seed %d)" % wl.seed,
+        "step": {"fwd_ms": fwd_ms, "bwd_ms": bwd_ms, "ms": fwd_ms + bwd_ms,
+                 "value": E / ((fwd_ms + bwd_ms) * 1e-3), "unit": UNIT,
+                 "fwd_frac": frac(FWD_BYTES_PER_ELEMENT, fwd_ms), "bwd_frac": frac(BWD_BYTES_PER_ELEMENT, bwd_ms),
+                 "step_frac": frac(STEP_BYTES, fwd_ms + bwd_ms)},
+        "alone": {k: {"ms": v, "frac": frac(nb, v)} for k, v, nb in
+                  (("fwd", al["fwd"], FWD_BYTES_PER_ELEMENT), ("bwd", al["bwd"], BWD_BYTES_PER_ELEMENT),
+                   ("fwd_bwd", al["fwd_bwd"], STEP_BYTES))},
+        "saved_carries": {"fwd_ms": cf_ms, "bwd_ms": cb_ms, "value": E / ((cf_ms + cb_ms) * 1e-3),
+                          "bwd_frac": frac(BWD_BYTES_PER_ELEMENT, cb_ms)},
+        "plan": {c: {"variant": v, "kernels": k} for c, (v, k) in plans.items()},
+    }
+
+
 def run_ours(args, w, world, rank, local):
     import numpy as np
     import torch
@@ -522,9 +612,22 @@ def run_ours(args, w, world, rank, local):
     h2d = (h_q.numel() + h_init.numel() + h_dcum.numel()) * 4
     d2h = (o_cum.numel() + o_dq.numel() + o_di.numel()) * 4
 
+    peak, peak_src = measured_peak_hbm()
+    # The other roofline-judged workloads, on one GPU only (their figures are
+    # per-call fractions, not a job total).
+    others = None
+    if world == 1 and not args.no_workloads:
+        del h_q, h_init, h_dcum, o_cum, o_dq, o_di, q, init, d_cum, d_init, flushbuf
+        torch.cuda.empty_cache()
+        others = {"note": "each workload's step (forward + backward), each call alone (median of 20, "
+                          "L2 flushed by a read before every rep) and the saved-carries step; "
+                          "fractions of the measured copy bandwidth at 32 / 48 / 80 B per element"}
+        for name in ("small", "large", "long"):
+            others[name] = time_other_workload(qs, torch, name, dev, stream, min(args.steps, 10),
+                                               args.warmup, peak)
+            torch.cuda.empty_cache()
     if rank != 0:
         return 0
-    peak, peak_src = measured_peak_hbm()
     bwd_avg = statistics.mean(bwd_ms)
     fwd_avg = statistics.mean(fwd_ms)
     bwd_gbs = BWD_BYTES_PER_ELEMENT * E / (bwd_avg * 1e-3) / 1e9
@@ -594,6 +697,7 @@ def run_ours(args, w, world, rank, local):
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "steps": e2e_steps,
                 "call": "quat_cumprod_fwd_bwd_host (pinned host buffers; batch slices whose copies "
                         "overlap the kernels)"},
+        "workloads": others,
         "bitwise_repeatable": repeatable,
         "gpu_launches": launches[0],
         "clocks": clocks,
@@ -613,6 +717,8 @@ def main(argv=None):
     p.add_argument("--cpu-seconds", type=float, default=10.0)
     p.add_argument("--cpu-lanes", type=int, default=512)
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-workloads", action="store_true",
+                   help="skip timing the small, large and long workloads besides the headline one")
     args = p.parse_args(argv)
     if args.warmup < 3:
         p.error("--warmup must be >= 3")

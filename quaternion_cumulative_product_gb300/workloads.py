@@ -128,6 +128,47 @@ def make_inputs(w: Workload):
     return q, init, d_cum
 
 
+def make_inputs_device(w: Workload, device):
+    """(q, init, d_cum) as float32 torch tensors drawn on ``device``.
+
+    The same distributions as ``make_inputs`` (and the same draw order: q,
+    init, d_cum) from torch's generator on the device seeded with ``w.seed``,
+    so the values differ from ``make_inputs``'s.  For timing only: the kernels
+    do the same work whatever the values, and drawing the largest workloads on
+    the host would take longer than timing them.
+    """
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(w.seed)
+    n = w.elements
+
+    def gauss4(m):
+        v = torch.randn((m, 4), generator=g, device=device, dtype=torch.float64)
+        return v / v.norm(dim=1, keepdim=True)
+
+    if w.q_kind == "gauss4":
+        q = gauss4(n)
+    elif w.q_kind == "rotation":
+        theta = torch.rand(n, generator=g, device=device, dtype=torch.float64) * w.theta_max
+        u = torch.randn((n, 3), generator=g, device=device, dtype=torch.float64)
+        u /= u.norm(dim=1, keepdim=True)
+        q = torch.cat([torch.cos(theta / 2)[:, None], torch.sin(theta / 2)[:, None] * u], dim=1)
+        del theta, u
+    else:
+        raise ValueError(w.q_kind)
+    q = q.float().reshape(w.B, w.S, w.H, w.J, 4)
+    if w.init_kind == "gauss4":
+        init = gauss4(w.lanes).float()
+    elif w.init_kind == "identity":
+        init = torch.zeros((w.lanes, 4), device=device)
+        init[:, 0] = 1.0
+    else:
+        raise ValueError(w.init_kind)
+    init = init.reshape(w.B, w.H, w.J, 4)
+    d_cum = (torch.randn((w.B, w.S, w.H, w.J, 4), generator=g, device=device) * w.dcum_sigma)
+    return q.contiguous(), init.contiguous(), d_cum.contiguous()
+
+
 def sample_lanes(arrays, lanes, H: int, J: int):
     """Gather whole lanes (b,h,j) of [B,S,H,J,4] / [B,H,J,4] arrays.
 

@@ -15,13 +15,11 @@ Tolerance, normwise per output tensor:
 """
 from __future__ import annotations
 
-import json
-import os
-
 import numpy as np
 import pytest
 
 import oracle
+import parity_log
 import quaternion_cumulative_product_gb300 as qs
 from quaternion_cumulative_product_gb300 import workloads
 
@@ -30,9 +28,6 @@ torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
 
 TOL_BF16 = 2.0 ** -8 + 1.1e-4
-# When set, every error measured below is appended to this file (one JSON
-# object per line); unset, nothing is written.
-PARITY_LOG = os.environ.get("QS_PARITY_LOG")
 
 
 @pytest.fixture(scope="module")
@@ -43,17 +38,10 @@ def dev():
     return torch.device("cuda", 0)
 
 
-def normwise(got, ref):
-    ref = np.asarray(ref, np.float64)
-    if ref.size == 0:
-        return 0.0
-    scale = float(np.abs(ref).max())
-    err = float(np.abs(np.asarray(got, np.float64) - ref).max()) / (scale if scale > 0 else 1.0)
-    if PARITY_LOG:
-        test = os.environ.get("PYTEST_CURRENT_TEST", "").split(" ")[0]
-        with open(PARITY_LOG, "a") as f:
-            f.write(json.dumps({"test": test, "dtype": "bf16", "elements": int(ref.size // 4),
-                                "normwise": err}) + "\n")
+def normwise(got, ref, what="", tol=None):
+    """Normwise error; with QS_PARITY_LOG set, both measures are logged."""
+    err = parity_log.normwise(got, ref)
+    parity_log.record(what, "bf16", got, ref, TOL_BF16 if tol is None else tol, err)
     return err
 
 
@@ -93,7 +81,7 @@ def test_bf16_matches_oracle(dev, dims, variant):
     ref_cum = oracle.fwd(q, init)
     ref_dq, ref_di = oracle.bwd(q, init, d_cum)
     for got, ref, name in ((cum, ref_cum, "cum"), (d_q, ref_dq, "d_q"), (d_init, ref_di, "d_init")):
-        err = normwise(got.float().cpu().numpy(), ref)
+        err = normwise(got.float().cpu().numpy(), ref, name)
         assert err <= TOL_BF16, f"{name}: {err:.3e} > {TOL_BF16:.3e}"
 
 
@@ -123,7 +111,8 @@ def test_bf16_rounding_is_the_only_difference_from_fp32(dev):
     g16, i16 = qs.quat_cumprod_bwd_bf16(tq, ti, td)
     g32, i32 = qs.quat_cumprod_bwd(tq.float(), ti.float(), td.float())
     for a, b in ((c16, c32), (g16.float(), g32), (i16.float(), i32)):
-        assert normwise(a.cpu().numpy(), b.cpu().numpy().astype(np.float64)) <= 2.0 ** -8 + 1e-5
+        assert normwise(a.cpu().numpy(), b.cpu().numpy().astype(np.float64), "vs fp32", 2.0 ** -8 + 1e-5) \
+            <= 2.0 ** -8 + 1e-5
 
 
 @pytest.mark.parametrize("name,walk", [("mamba3", True), ("large", True), ("long", False), ("small", False)])
@@ -154,6 +143,31 @@ def test_bf16_long_sequence_sampled_lanes(dev):
     assert normwise(gc, oracle.fwd(sq, si)) <= TOL_BF16
     assert normwise(gq, ref_dq) <= TOL_BF16
     assert normwise(gi, ref_di) <= TOL_BF16
+
+
+@pytest.mark.parametrize("name", ["tiny", "small", "mamba3", "large", "long"])
+def test_bf16_named_workloads(dev, name):
+    """Every workload in bfloat16, in the configuration the library picks: the
+    two smallest compared in full, the others (at full size) on sampled whole
+    lanes."""
+    w = workloads.WORKLOADS[name]
+    (tq, ti, td), exact = bf16_inputs(dev, w)
+    cum = qs.quat_cumprod_fwd_bf16(tq, ti)
+    d_q, d_init = qs.quat_cumprod_bwd_bf16(tq, ti, td)
+    assert qs.quat_cumprod_status(device=dev) == qs.QS_OK
+    got = [t.float().cpu().numpy() for t in (cum, d_q, d_init)]
+    if w.elements <= 1 << 20:
+        q, init, d_cum = exact
+        ref = [oracle.fwd(q, init), *oracle.bwd(q, init, d_cum)]
+    else:
+        lanes = np.unique(np.concatenate([[0, w.lanes - 1],
+                                          np.random.default_rng(5).choice(w.lanes, 12, replace=False)]))
+        sq, si, sd = workloads.sample_lanes(exact, lanes, w.H, w.J)
+        ref = [oracle.fwd(sq, si), *oracle.bwd(sq, si, sd)]
+        got = list(workloads.sample_lanes(got, lanes, w.H, w.J))
+    for g, r, t in zip(got, ref, ("cum", "d_q", "d_init")):
+        err = normwise(g, r, t)
+        assert err <= TOL_BF16, f"{name} {t}: {err:.3e} > {TOL_BF16:.3e}"
 
 
 def test_bf16_unknown_variant_is_rejected(dev):

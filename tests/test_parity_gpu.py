@@ -10,13 +10,12 @@ are independent, so the oracle on a lane subset is exact).
 from __future__ import annotations
 
 import ctypes
-import json
-import os
 
 import numpy as np
 import pytest
 
 import oracle
+import parity_log
 import quaternion_cumulative_product_gb300 as qs
 from quaternion_cumulative_product_gb300 import workloads
 
@@ -25,10 +24,6 @@ torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
 
 TOL = 1e-4
-# When set, every comparison against the oracle appends its measured error to
-# this file (one JSON object per line), so that the margins below the tolerance
-# can be reported; unset, nothing is written.
-PARITY_LOG = os.environ.get("QS_PARITY_LOG")
 
 
 @pytest.fixture(scope="module")
@@ -49,9 +44,7 @@ def reset_hooks():
     lib.quat_cumprod_debug_set_walk_cap(-1)
 
 
-def normwise(got, ref):
-    scale = float(np.abs(ref).max()) if ref.size else 0.0
-    return float(np.abs(got.astype(np.float64) - ref).max()) / (scale if scale > 0 else 1.0) if ref.size else 0.0
+normwise = parity_log.normwise
 
 
 def run_gpu(dev, q, init, d_cum, stream=None):
@@ -64,12 +57,9 @@ def run_gpu(dev, q, init, d_cum, stream=None):
 
 
 def assert_parity(got, ref, what):
+    """The pass criterion (normwise); with QS_PARITY_LOG set, both measures are logged."""
     err = normwise(got, ref)
-    if PARITY_LOG:
-        test = os.environ.get("PYTEST_CURRENT_TEST", "").split(" ")[0]
-        with open(PARITY_LOG, "a") as f:
-            f.write(json.dumps({"test": test, "tensor": what, "elements": int(ref.size // 4),
-                                "normwise": err, "tol": TOL}) + "\n")
+    parity_log.record(what, "fp32", got, ref, TOL, err)
     assert err <= TOL, f"{what}: normwise relative error {err:.3e} > {TOL}"
     return err
 

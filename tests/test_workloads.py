@@ -69,3 +69,29 @@ def test_seeds_give_distinct_streams():
     a = workloads.make_inputs(workloads.custom("a", 1, 8, 1, 2, seed=0))
     b = workloads.make_inputs(workloads.custom("b", 1, 8, 1, 2, seed=1))
     assert not np.array_equal(a[0], b[0])
+
+
+@pytest.mark.parametrize("name", ["tiny", "small", "identity-init"])
+def test_device_draws_follow_the_same_recipe(name):
+    """make_inputs_device (the bench's draws for the other workloads) on the CPU:
+    shapes, unit q and init (or identity init), rotation angles within their
+    bound, d_cum's spread."""
+    torch = pytest.importorskip("torch")
+    w = (workloads.WORKLOADS[name] if name in workloads.WORKLOADS else
+         workloads.custom(name, 2, 4096, 4, 8, q_kind="rotation", theta_max=math.pi / 8,
+                          init_kind="identity", dcum_sigma=0.02, seed=2))
+    q, init, d_cum = workloads.make_inputs_device(w, torch.device("cpu"))
+    assert q.shape == (w.B, w.S, w.H, w.J, 4) and d_cum.shape == q.shape and init.shape == (w.B, w.H, w.J, 4)
+    assert q.dtype == init.dtype == d_cum.dtype == torch.float32
+    assert torch.allclose(q.double().norm(dim=-1), torch.ones(()).double(), atol=1e-6)
+    if w.init_kind == "identity":
+        assert torch.equal(init, torch.tensor([1.0, 0, 0, 0]).expand_as(init))
+    else:
+        assert torch.allclose(init.double().norm(dim=-1), torch.ones(()).double(), atol=1e-6)
+    if w.q_kind == "rotation":
+        theta = 2 * torch.acos(q[..., 0].double().clamp(-1, 1))
+        assert float(theta.max()) <= w.theta_max + 1e-5
+    sd = float(d_cum.double().std())
+    assert abs(sd - w.dcum_sigma) < 0.05 * w.dcum_sigma
+    again = workloads.make_inputs_device(w, torch.device("cpu"))
+    assert all(torch.equal(a, b) for a, b in zip((q, init, d_cum), again))   # seeded
