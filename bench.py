@@ -55,12 +55,19 @@ KERNEL_SOURCES = [os.path.join(ROOT, "quaternion_cumulative_product_gb300", "csr
 
 
 # Forward configurations of the segmented chained walk in the library's table.
-SEGWALK_FWD_VARIANTS = (9, 10, 11, 12, 13, 14)
+SEGWALK_FWD_VARIANTS = (9, 10, 11, 12, 13, 14, 15, 16, 17, 18)
+
+
+# Backward configurations of the segmented walk (after its carries-only pass
+# when the carries are recomputed).
+SEGWALK_BWD_VARIANTS = tuple(range(11, 22))
 
 
 def design_name(call: str, kernels: int, variant: int = -1) -> str:
     if call == "quat_cumprod_fwd" and variant in SEGWALK_FWD_VARIANTS:
         return f"{call} (segmented chained walk kernel)"
+    if call == "quat_cumprod_bwd" and variant in SEGWALK_BWD_VARIANTS:
+        return f"{call} (carries pass + segmented walk kernels)" if kernels == 2 else f"{call} (segmented walk kernel)"
     if kernels != 1:
         return f"{call} (aggregate + carry + apply kernels)"
     return f"{call} (walk kernel)"

@@ -161,6 +161,10 @@ const Variant kFwdVariants[] = {
     QS_SEGWALK_SENT_FWD(32, 8, 8, 3, 4),   // 12: as 9, one-latency look-back rounds (few lane groups)
     QS_SEGWALK_WS_SENT_FWD(32, 8, 8, 4, 4),   // 13: as 10, one-latency look-back rounds
     QS_SEGWALK_WS_SENT_FWD(16, 8, 8, 6, 4),   // 14: as 11, one-latency look-back rounds
+    QS_SEGWALK_SENT_FWD(32, 8, 8, 3, 1),      // 15: as 12, segments of one chunk (short sequences)
+    QS_SEGWALK_SENT_FWD(32, 8, 8, 3, 2),      // 16: as 12, segments of 2 chunks
+    QS_SEGWALK_WS_SENT_FWD(16, 8, 8, 6, 1),   // 17: as 14, segments of one chunk
+    QS_SEGWALK_WS_SENT_FWD(16, 8, 8, 6, 2),   // 18: as 14, segments of 2 chunks
 };
 #define QS_WALK_BWD_CAP(LT, NSEG, N, NSTF, NSTB, CAPX4)                                             \
     Variant {                                                                                       \
@@ -173,6 +177,10 @@ const void *const kCarriesPass =
     reinterpret_cast<const void *>(qs::quat_carries_pass_kernel<qs::IoF32, 16, 8, 8, 4, 4>);
 const Variant kCarriesPassVariant = Variant{
     false, kCarriesPass, nullptr, false, 16, 8, 8, qs::carries_pass_smem_bytes(16, 8, 8, 4, 4), false, 0, 4, 64, true};
+// The same for bfloat16 tensors (the carries stay fp32).
+const Variant kCarriesPassVariantBf16 = Variant{
+    false, reinterpret_cast<const void *>(qs::quat_carries_pass_kernel<qs::IoBF16, 16, 8, 8, 6, 4>), nullptr, false,
+    16, 8, 8, qs::carries_pass_smem_bytes(16, 8, 8, 6, 4, 8), false, 0, 4, 64, true};
 #define QS_SEGWALK_BWD(LT, NSEG, N, NST, K, MINB, LB, W2FWD)                                        \
     Variant {                                                                                       \
         false, reinterpret_cast<const void *>(qs::quat_segwalk_bwd_kernel<qs::IoF32, LT, NSEG, N, NST, K, MINB, LB, W2FWD>), \
@@ -201,6 +209,7 @@ const Variant kBwdVariants[] = {
     QS_SEGWALK_BWD(16, 8, 8, 2, 4, 2, 4, true),    // 18: as 11, walk 2 left to right
     QS_SEGWALK_BWD(16, 8, 8, 3, 2, 2, 4, true),    // 19: as 12, walk 2 left to right
     QS_SEGWALK_BWD(16, 8, 8, 2, 3, 2, 4, true),    // 20: segments of 3 chunks, walk 2 left to right
+    QS_SEGWALK_BWD(16, 8, 8, 2, 1, 2, 4, false),   // 21: as 11, segments of one chunk (short sequences)
 };
 // The backward from caller-provided carries: the reverse walk alone.
 const Variant kBwdGiven = Variant{true,
@@ -237,6 +246,16 @@ const Variant kBwdGiven = Variant{true,
             reinterpret_cast<const void *>(qs::quat_apply_kernel<qs::IoBF16, B, LT, N>), B, LT,     \
             NTHREADS / (LT), N, qs::tile_smem_bytes(B, LT, N, 8)                                    \
     }
+#define QS_SEGWALK_WS_SENT_FWD16(LT, NSEG, N, NST, K)                                               \
+    Variant {                                                                                       \
+        false, reinterpret_cast<const void *>(qs::quat_segwalk_ws_fwd_kernel<qs::IoBF16, LT, NSEG, N, NST, K, true>), \
+            nullptr, false, LT, NSEG, N, qs::segwalk_smem_bytes(LT, NSEG, N, NST, 8), false, 0, K, 64, true \
+    }
+#define QS_SEGWALK_BWD16(LT, NSEG, N, NST, K, MINB)                                                 \
+    Variant {                                                                                       \
+        false, reinterpret_cast<const void *>(qs::quat_segwalk_bwd_kernel<qs::IoBF16, LT, NSEG, N, NST, K, MINB, 4, false>), \
+            nullptr, true, LT, NSEG, N, qs::segwalk_bwd_smem_bytes(LT, NSEG, N, NST, K, 8), false, 0, K, 64, true \
+    }
 #define QS_SEGWALK_SENT_FWD16(LT, NSEG, N, NST, K)                                                  \
     Variant {                                                                                       \
         false, reinterpret_cast<const void *>(qs::quat_segwalk_fwd_kernel<qs::IoBF16, LT, NSEG, N, NST, K, true>), \
@@ -255,6 +274,7 @@ const Variant kFwdBf16Variants[] = {
     QS_VARIANT16(false, 32, 8),            // 4: three kernels, 64-step chunks
     QS_SEGWALK_FWD16(32, 8, 8, 3, 4),      // 5: segmented chained walk (few lane groups)
     QS_SEGWALK_SENT_FWD16(32, 8, 8, 3, 4), // 6: as 5, one-latency look-back rounds
+    QS_SEGWALK_WS_SENT_FWD16(16, 8, 8, 6, 4),   // 7: segmented walk, warp-specialised, 16 lanes
 };
 const Variant kBwdBf16Variants[] = {
     QS_WALK_BWD16(16, 8, 8, 8, 4, false),  // 0: 16 lanes x 64 steps (128 threads), 64 KiB rings
@@ -263,10 +283,14 @@ const Variant kBwdBf16Variants[] = {
     QS_WALK_BWD16(32, 8, 8, 8, 4, false),  // 3: 32 lanes x 64 steps (256 threads), 128 KiB rings
     QS_VARIANT16(true, 32, 8),             // 4: three kernels, 64-step chunks (few lane groups)
     QS_WALK_BWD16_MINB(16, 8, 8, 8, 4, 3), // 5: as 0, registers capped for 3 CTAs per SM (many lane groups)
+    QS_SEGWALK_BWD16(16, 8, 8, 3, 4, 2),   // 6: segmented walk (after the carries pass), segments of 4 chunks
+    QS_SEGWALK_BWD16(16, 8, 8, 3, 2, 2),   // 7: segmented walk, segments of 2 chunks
 };
 #undef QS_VARIANT16
 #undef QS_SEGWALK_FWD16
 #undef QS_SEGWALK_SENT_FWD16
+#undef QS_SEGWALK_WS_SENT_FWD16
+#undef QS_SEGWALK_BWD16
 #undef QS_WALK_FWD16
 #undef QS_WALK_BWD16
 #undef QS_WALK_BWD16_MINB
@@ -326,6 +350,12 @@ constexpr int kSegFwd = 12;
 // shapes above; on 4 x 8192 x 8 x 16 it measured 0.50 against 0.53.
 constexpr int kSegFwdLarge = 14;
 constexpr long long kSegFwdLargeElements = 1ll << 24;
+// Short sequences (at most 64 chunks): segments of 2 chunks, one look-back
+// less deep per unit.  Measured alone, 15.0 against 17.1 us on 4 x 1024 x 8 x 16,
+// 2 x 2048 x 8 x 16 and 1 x 4096 x 4 x 16 (the event clock ticks by about 2 us);
+// 25.2 against 23.2 us on 2 x 8192 x 8 x 16 (128 chunks).
+constexpr int kSegFwdShort = 16;
+constexpr int kSegFwdShortChunks = 64;
 constexpr int kNumFwd = sizeof(kFwdVariants) / sizeof(kFwdVariants[0]);
 constexpr int kNumBwd = sizeof(kBwdVariants) / sizeof(kBwdVariants[0]);
 
@@ -429,6 +459,7 @@ int device_info(DevInfo **out, int *dev_out) {
             for (const Variant &v : kBwdVariants) setup(v);
             setup(kBwdGiven);
             setup(kCarriesPassVariant);
+            setup(kCarriesPassVariantBf16);
             for (const Variant &v : kFwdBf16Variants) setup(v);
             for (const Variant &v : kBwdBf16Variants) setup(v);
             if (!ok) {
@@ -715,7 +746,8 @@ int pick_variant(bool bwd, int64_t B, int64_t S, int64_t HJ, int sms, Mode mode)
         if (mode == Mode::FROM_CARRIES || groups >= kSegBwdManyGroups) return seg;
         return kThreeBwd;
     }
-    return (long long)B * S * HJ >= kSegFwdLargeElements ? kSegFwdLarge : kSegFwd;
+    if ((long long)B * S * HJ >= kSegFwdLargeElements) return kSegFwdLarge;
+    return (S + 63) / 64 <= kSegFwdShortChunks ? kSegFwdShort : kSegFwd;
 }
 
 // `capturing`: the call is being captured into a CUDA graph, whose launches
@@ -917,7 +949,7 @@ int launch_segwalk_bwd(const Plan &pl, int dev, unsigned char *ws, const void *q
     const float4 *car = reinterpret_cast<const float4 *>(carries);
     const bool pass = mode != Mode::FROM_CARRIES;
     if (pass) {
-        const Variant &pv = kCarriesPassVariant;
+        const Variant &pv = bf16 ? kCarriesPassVariantBf16 : kCarriesPassVariant;
         qs::Geometry pg = geometry(B, S, HJ, pv.lt, pv.T());
         CUtensorMap pmap;
         rc = make_map(&pmap, q, B, S, HJ, pv.lt, pv.T(), eb);

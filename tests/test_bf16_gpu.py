@@ -54,9 +54,11 @@ def bf16_inputs(dev, w):
 
 
 # Compiled configurations: forward 0-3 walks, 4 three kernels, 5 segmented
-# chained walk, 6 the same with self-describing look-back values; backward 0-3
-# walks, 4 three kernels, 5 walk with registers capped for three CTAs per SM.
-N_BF16_FWD, N_BF16_BWD = 7, 6
+# chained walk, 6 the same with self-describing look-back values, 7 its
+# warp-specialised form; backward 0-3 walks, 4 three kernels, 5 walk with
+# registers capped for three CTAs per SM, 6 and 7 the segmented walk after its
+# carries pass (segments of 4 and 2 chunks).
+N_BF16_FWD, N_BF16_BWD = 8, 8
 
 
 @pytest.fixture(autouse=True)

@@ -186,9 +186,9 @@ def test_empty_sizes(dev):
 # in one round trip; 13, 14: as 10, 11 with those values; backward 10: at most
 # two CTAs per SM, more lane groups in waves; backward 11-14: the segmented
 # walk of the backward, after its carries-only forward pass).
-N_FWD_VARIANTS, N_BWD_VARIANTS = 15, 21
-SEGWALK_FWD = [9, 10, 11, 12, 13, 14]
-SEGWALK_BWD = [11, 12, 13, 14, 15, 16, 17, 18, 19, 20]
+N_FWD_VARIANTS, N_BWD_VARIANTS = 19, 22
+SEGWALK_FWD = [9, 10, 11, 12, 13, 14, 15, 16, 17, 18]
+SEGWALK_BWD = [11, 12, 13, 14, 15, 16, 17, 18, 19, 20, 21]
 
 
 @pytest.mark.parametrize("variant", range(max(N_FWD_VARIANTS, N_BWD_VARIANTS)))
@@ -624,8 +624,10 @@ def test_plan_picks_the_design_by_lane_groups(dev, name, walk):
         assert kernels == (1 if walk or not bwd else 3), (name, bwd, variant, kernels)
         if not walk and not bwd:
             # the segmented walk with self-describing look-back values: the
-            # warp-specialised form (14) from 2^24 elements, else the one-role form (12)
-            assert variant == (14 if w.elements >= 1 << 24 else 12), (name, variant)
+            # warp-specialised form (14) from 2^24 elements, else the one-role
+            # form, with segments of 2 chunks (16) for at most 64 chunks (12 beyond)
+            short = (w.S + 63) // 64 <= 64
+            assert variant == (14 if w.elements >= 1 << 24 else 16 if short else 12), (name, variant)
         if not walk and bwd:
             assert variant == 0, (name, variant)
     assert qs.quat_cumprod_plan(True, 2, 0, 3, 4, device=dev) == (-1, 0)
