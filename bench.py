@@ -724,6 +724,8 @@ def main(argv=None):
     p.add_argument("--cpu-seconds", type=float, default=10.0)
     p.add_argument("--cpu-lanes", type=int, default=512)
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--batch", type=int, default=None,
+                   help="the workload's recipe with this many batch entries (a smaller case of a large workload)")
     p.add_argument("--no-workloads", action="store_true",
                    help="skip timing the small, large and long workloads besides the headline one")
     args = p.parse_args(argv)
@@ -733,6 +735,11 @@ def main(argv=None):
     if args.gpus != world and world > 1:
         p.error(f"--gpus {args.gpus} does not match WORLD_SIZE {world}")
     w = workloads.WORKLOADS[args.workload]
+    if args.batch is not None:   # the same workload with another batch size
+        if args.batch < 1:
+            p.error("--batch must be >= 1")
+        w = workloads.custom(w.name, args.batch, w.S, w.H, w.J, q_kind=w.q_kind, theta_max=w.theta_max,
+                             init_kind=w.init_kind, dcum_sigma=w.dcum_sigma, seed=w.seed)
     if args.impl == "reference":
         return run_reference(args, w, world, rank)
     return run_ours(args, w, world, rank, local)
