@@ -60,7 +60,7 @@ SEGWALK_FWD_VARIANTS = (9, 10, 11, 12, 13, 14, 15, 16, 17, 18)
 
 # Backward configurations of the segmented walk (after its carries-only pass
 # when the carries are recomputed).
-SEGWALK_BWD_VARIANTS = tuple(range(11, 22))
+SEGWALK_BWD_VARIANTS = tuple(range(11, 25))
 
 
 def design_name(call: str, kernels: int, variant: int = -1) -> str:

@@ -104,8 +104,8 @@ struct Variant {
     // the next launch by the kernel itself; see LbValues).
     bool sent = false;
     // Backward segmented walk: the carries-only forward pass it starts from
-    // when it recomputes the carries (the same for every backward configuration).
-    const void *prepass = nullptr;
+    // when it recomputes the carries.
+    const Variant *pass = nullptr;
 };
 
 #define QS_VARIANT(B, LT, N)                                                                        \
@@ -172,11 +172,14 @@ const Variant kFwdVariants[] = {
             nullptr, true, LT, NSEG, N, qs::walk_bwd_smem_bytes(LT, NSEG, N, NSTF, NSTB), false, CAPX4 \
     }
 // The carries-only forward pass of the segmented backward (its forward
-// carries, one read of q): 16-lane groups, segments of 4 chunks, 4-stage ring.
-const void *const kCarriesPass =
-    reinterpret_cast<const void *>(qs::quat_carries_pass_kernel<qs::IoF32, 16, 8, 8, 4, 4>);
+// carries, one read of q): 16-lane groups, segments of 4 chunks, 4-stage ring;
+// one look-back warp, or two taking alternate units.
 const Variant kCarriesPassVariant = Variant{
-    false, kCarriesPass, nullptr, false, 16, 8, 8, qs::carries_pass_smem_bytes(16, 8, 8, 4, 4), false, 0, 4, 64, true};
+    false, reinterpret_cast<const void *>(qs::quat_carries_pass_kernel<qs::IoF32, 16, 8, 8, 4, 4>), nullptr, false,
+    16, 8, 8, qs::carries_pass_smem_bytes(16, 8, 8, 4, 4), false, 0, 4, 64, true};
+const Variant kCarriesPassVariant2 = Variant{
+    false, reinterpret_cast<const void *>(qs::quat_carries_pass_kernel<qs::IoF32, 16, 8, 8, 4, 4, 4, 2>), nullptr,
+    false, 16, 8, 8, qs::carries_pass_smem_bytes(16, 8, 8, 4, 4), false, 0, 4, 96, true};
 // The same for bfloat16 tensors (the carries stay fp32).
 const Variant kCarriesPassVariantBf16 = Variant{
     false, reinterpret_cast<const void *>(qs::quat_carries_pass_kernel<qs::IoBF16, 16, 8, 8, 6, 4>), nullptr, false,
@@ -185,7 +188,13 @@ const Variant kCarriesPassVariantBf16 = Variant{
     Variant {                                                                                       \
         false, reinterpret_cast<const void *>(qs::quat_segwalk_bwd_kernel<qs::IoF32, LT, NSEG, N, NST, K, MINB, LB, W2FWD>), \
             nullptr, true, LT, NSEG, N, qs::segwalk_bwd_smem_bytes(LT, NSEG, N, NST, K), false, 0, K, 64, true, \
-            kCarriesPass                                                                            \
+            &kCarriesPassVariant                                                                    \
+    }
+#define QS_SEGWALK_BWD2(LT, NSEG, N, NST, K, MINB)                                                  \
+    Variant {                                                                                       \
+        false, reinterpret_cast<const void *>(qs::quat_segwalk_bwd_kernel<qs::IoF32, LT, NSEG, N, NST, K, MINB, 4, false, 2>), \
+            nullptr, true, LT, NSEG, N, qs::segwalk_bwd_smem_bytes(LT, NSEG, N, NST, K), false, 0, K, 96, true, \
+            &kCarriesPassVariant2                                                                   \
     }
 const Variant kBwdVariants[] = {
     QS_VARIANT(true, 32, 8),           // 0: three kernels, 64-step chunks, 64 KiB tiles
@@ -210,6 +219,9 @@ const Variant kBwdVariants[] = {
     QS_SEGWALK_BWD(16, 8, 8, 3, 2, 2, 4, true),    // 19: as 12, walk 2 left to right
     QS_SEGWALK_BWD(16, 8, 8, 2, 3, 2, 4, true),    // 20: segments of 3 chunks, walk 2 left to right
     QS_SEGWALK_BWD(16, 8, 8, 2, 1, 2, 4, false),   // 21: as 11, segments of one chunk (short sequences)
+    QS_SEGWALK_BWD2(16, 8, 8, 2, 4, 2),            // 22: as 11, two look-back warps (alternate units; so is its carries pass)
+    QS_SEGWALK_BWD2(16, 8, 8, 2, 2, 2),            // 23: as 14, two look-back warps
+    QS_SEGWALK_BWD2(16, 8, 8, 3, 2, 2),            // 24: as 12, two look-back warps
 };
 // The backward from caller-provided carries: the reverse walk alone.
 const Variant kBwdGiven = Variant{true,
@@ -254,7 +266,8 @@ const Variant kBwdGiven = Variant{true,
 #define QS_SEGWALK_BWD16(LT, NSEG, N, NST, K, MINB)                                                 \
     Variant {                                                                                       \
         false, reinterpret_cast<const void *>(qs::quat_segwalk_bwd_kernel<qs::IoBF16, LT, NSEG, N, NST, K, MINB, 4, false>), \
-            nullptr, true, LT, NSEG, N, qs::segwalk_bwd_smem_bytes(LT, NSEG, N, NST, K, 8), false, 0, K, 64, true \
+            nullptr, true, LT, NSEG, N, qs::segwalk_bwd_smem_bytes(LT, NSEG, N, NST, K, 8), false, 0, K, 64, true, \
+            &kCarriesPassVariantBf16                                                                \
     }
 #define QS_SEGWALK_SENT_FWD16(LT, NSEG, N, NST, K)                                                  \
     Variant {                                                                                       \
@@ -319,6 +332,7 @@ constexpr int kNumBwdBf16 = sizeof(kBwdBf16Variants) / sizeof(kBwdBf16Variants[0
 #undef QS_WALK_BWD
 #undef QS_WALK_BWD_CAP
 #undef QS_SEGWALK_BWD
+#undef QS_SEGWALK_BWD2
 // Lanes per block of the carry scan (sequences of more than 256 chunks).
 constexpr int kCarryScanLanes = 2;
 
@@ -336,7 +350,7 @@ constexpr int kWalkFwd = 4, kWalkBwd = 10, kThreeFwd = 0, kThreeBwd = 0;
 // Backward with too few lane groups for a walk: the segmented walk (after a
 // carries-only forward pass when the carries are not saved: 64 bytes per
 // element of DRAM instead of the three kernels' 80), see pick_variant.
-constexpr int kSegBwd = 11;
+constexpr int kSegBwd = 22;   // segments of 4 chunks, two look-back warps
 // Forward with too few lane groups for a walk: the segmented chained walk
 // (segments of 4 chunks) whose look-back values carry their own state, so a
 // look-back round takes one memory latency.  It measured 0.76 / 0.82 / 0.73 of
@@ -459,6 +473,7 @@ int device_info(DevInfo **out, int *dev_out) {
             for (const Variant &v : kBwdVariants) setup(v);
             setup(kBwdGiven);
             setup(kCarriesPassVariant);
+            setup(kCarriesPassVariant2);
             setup(kCarriesPassVariantBf16);
             for (const Variant &v : kFwdBf16Variants) setup(v);
             for (const Variant &v : kBwdBf16Variants) setup(v);
@@ -716,18 +731,19 @@ int layout_plan(bool bwd, int64_t B, int64_t S, int64_t HJ, int sms, Plan *pl, M
 
 // The backward for few lane groups (LT = 16 groups, C 64-step chunks), both
 // measured on one GB300 with L2 flushed before every call (fraction of the
-// copy bandwidth at 48 bytes per element):
+// copy bandwidth at 48 bytes per element), the segmented walk with two
+// look-back warps:
 //  * from saved carries, the segmented walk: segments of 4 chunks on long
-//    sequences of few groups (1 x 131072 x 16 x 16: 0.75; with 2 chunks 0.50,
+//    sequences of few groups (1 x 131072 x 16 x 16: 0.75; with 2 chunks 0.58,
 //    the look-backs run deep), of 2 chunks when the groups are many or the
-//    units few (2 x 65536 x 32 x 32: 0.88 against 0.79; 4 x 1024 x 8 x 16:
-//    0.22 against 0.18); the three kernels measured 0.58 / 0.60 / 0.14;
+//    units few (2 x 65536 x 32 x 32: 0.92 against 0.78; 4 x 1024 x 8 x 16:
+//    0.22 against 0.20); the three kernels measured 0.58 / 0.60 / 0.14;
 //  * recomputing the carries, the segmented walk after its carries pass only
-//    with 64 groups or more (2 x 65536 x 32 x 32: 0.67 against 0.60 for the
-//    three kernels); with fewer the carries pass costs more than the three
-//    kernels' second read (1 x 131072 x 16 x 16: 0.56 against 0.58;
-//    4 x 1024 x 8 x 16: 0.14 against 0.16).
-constexpr int kSegBwdShort = 14;           // segments of 2 chunks
+//    with 64 groups or more (2 x 65536 x 32 x 32: 0.70 against 0.60 for the
+//    three kernels); with fewer the carries pass costs about what the three
+//    kernels' second read does (1 x 131072 x 16 x 16: 0.57 against 0.58;
+//    4 x 1024 x 8 x 16: 0.13 against 0.16).
+constexpr int kSegBwdShort = 24;           // segments of 2 chunks, two look-back warps
 constexpr long long kSegBwdManyGroups = 64;
 
 int pick_variant(bool bwd, int64_t B, int64_t S, int64_t HJ, int sms, Mode mode) {
@@ -949,7 +965,7 @@ int launch_segwalk_bwd(const Plan &pl, int dev, unsigned char *ws, const void *q
     const float4 *car = reinterpret_cast<const float4 *>(carries);
     const bool pass = mode != Mode::FROM_CARRIES;
     if (pass) {
-        const Variant &pv = bf16 ? kCarriesPassVariantBf16 : kCarriesPassVariant;
+        const Variant &pv = *v->pass;
         qs::Geometry pg = geometry(B, S, HJ, pv.lt, pv.T());
         CUtensorMap pmap;
         rc = make_map(&pmap, q, B, S, HJ, pv.lt, pv.T(), eb);

@@ -65,8 +65,11 @@ namespace qs {
 // chunks are independent: every thread starts from its table entries), so
 // every chunk is read again the same number of items after its first read;
 // otherwise right to left, starting with the chunk walk 1 read last.
-template <typename IO, int LT, int NSEG, int N, int NST, int K, int MINB = 1, int LB = 4, bool W2FWD = false>
-__global__ void __launch_bounds__(LT *NSEG + 64, MINB)
+// NLB: look-back warps (1 or 2); with two, unit k goes to look-back warp
+// k % 2, so that one unit's look-back overlaps the previous one's.
+template <typename IO, int LT, int NSEG, int N, int NST, int K, int MINB = 1, int LB = 4, bool W2FWD = false,
+          int NLB = 1>
+__global__ void __launch_bounds__(LT *NSEG + 32 + 32 * NLB, MINB)
     quat_segwalk_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap dmap,
                             const float4 *__restrict__ carries, typename IO::elem *__restrict__ d_q,
                             typename IO::elem *__restrict__ d_init, unsigned int *__restrict__ ctr,
@@ -125,11 +128,13 @@ __global__ void __launch_bounds__(LT *NSEG + 64, MINB)
     __syncthreads();
 
     if (tid >= NT + 32) {
-        // ======================= look-back warp ===============================
-        const int wl = tid - (NT + 32);   // lane of the warp; lanes [0, LT) own the lane group's lanes
+        // ======================= look-back warp(s) ============================
+        static_assert(NLB == 1 || NLB == 2, "one look-back warp, or one per unit slot");
+        const int wl = (tid - (NT + 32)) % 32;   // lane of the warp; lanes [0, LT) own the lane group's lanes
+        const int lbw = (tid - (NT + 32)) / 32;  // which look-back warp: units k = lbw, lbw + NLB, ...
         const int lane = wl % LT;
         const bool own = wl < LT;
-        for (int k = 0;; ++k) {
+        for (int k = lbw;; k += NLB) {
             if (!ws_wait(&agg_ready[k & 1], (k >> 1) & 1, ctl, -1, &s_broken)) break;
             const int t = s_lbu[k & 1];
             if (t < 0) break;
@@ -390,9 +395,13 @@ __global__ void __launch_bounds__(LT *NSEG + 64, MINB)
                     walk2(prev, (k - 1) & 1);
                 }
                 __syncwarp();
-                if (lead) {   // the look-back warp ends too
+                if (lead) {   // the look-back warp(s) end too (unit k - 1 is done: its slot is free)
                     if (tid == 0) s_lbu[k & 1] = -1;
                     mbar_arrive(&agg_ready[k & 1]);
+                    if (NLB == 2) {
+                        if (tid == 0) s_lbu[(k + 1) & 1] = -1;
+                        mbar_arrive(&agg_ready[(k + 1) & 1]);
+                    }
                 }
                 break;
             }
@@ -443,8 +452,8 @@ __global__ void __launch_bounds__(LT *NSEG + 64, MINB)
 // entering the unit, publishes A (x) X and writes the unit's carries.  The
 // look-back values and tickets work as in quat_segwalk_bwd_kernel.
 // ---------------------------------------------------------------------------
-template <typename IO, int LT, int NSEG, int N, int NST, int K, int LB = 4>
-__global__ void __launch_bounds__(LT *NSEG + 64)
+template <typename IO, int LT, int NSEG, int N, int NST, int K, int LB = 4, int NLB = 1>
+__global__ void __launch_bounds__(LT *NSEG + 32 + 32 * NLB)
     quat_carries_pass_kernel(const __grid_constant__ CUtensorMap qmap, const typename IO::elem *__restrict__ init,
                              float4 *__restrict__ carries, unsigned int *__restrict__ ctr, float4 *__restrict__ agg,
                              float4 *__restrict__ incl, float4 *__restrict__ agg_next, float4 *__restrict__ incl_next,
@@ -490,11 +499,13 @@ __global__ void __launch_bounds__(LT *NSEG + 64)
     __syncthreads();
 
     if (tid >= NT + 32) {
-        // ======================= look-back warp ===============================
-        const int wl = tid - (NT + 32);
+        // ======================= look-back warp(s) ============================
+        static_assert(NLB == 1 || NLB == 2, "one look-back warp, or one per unit slot");
+        const int wl = (tid - (NT + 32)) % 32;
+        const int lbw = (tid - (NT + 32)) / 32;   // units k = lbw, lbw + NLB, ...
         const int lane = wl % LT;
         const bool own = wl < LT;
-        for (int k = 0;; ++k) {
+        for (int k = lbw;; k += NLB) {
             if (!ws_wait(&agg_ready[k & 1], (k >> 1) & 1, ctl, -1, &s_broken)) break;
             const int t = s_lbu[k & 1];
             if (t < 0) break;
@@ -608,10 +619,16 @@ __global__ void __launch_bounds__(LT *NSEG + 64)
             __syncwarp();
             if (t < 0) {
                 if (got) release();   // the end marker's stage
+                // (two look-back warps: the other slot is free once unit k - 1 is done)
+                if (NLB == 2 && k >= 1) ws_wait(&carry_ready[(k - 1) & 1], ((k - 1) >> 1) & 1, ctl, -1, &s_broken);
                 __syncwarp();
-                if (lead) {   // the look-back warp ends too
+                if (lead) {   // the look-back warp(s) end too
                     if (tid == 0) s_lbu[k & 1] = -1;
                     mbar_arrive(&agg_ready[k & 1]);
+                    if (NLB == 2) {
+                        if (tid == 0) s_lbu[(k + 1) & 1] = -1;
+                        mbar_arrive(&agg_ready[(k + 1) & 1]);
+                    }
                 }
                 break;
             }

@@ -186,9 +186,9 @@ def test_empty_sizes(dev):
 # in one round trip; 13, 14: as 10, 11 with those values; backward 10: at most
 # two CTAs per SM, more lane groups in waves; backward 11-14: the segmented
 # walk of the backward, after its carries-only forward pass).
-N_FWD_VARIANTS, N_BWD_VARIANTS = 19, 22
+N_FWD_VARIANTS, N_BWD_VARIANTS = 19, 25
 SEGWALK_FWD = [9, 10, 11, 12, 13, 14, 15, 16, 17, 18]
-SEGWALK_BWD = [11, 12, 13, 14, 15, 16, 17, 18, 19, 20, 21]
+SEGWALK_BWD = [11, 12, 13, 14, 15, 16, 17, 18, 19, 20, 21, 22, 23, 24]
 
 
 @pytest.mark.parametrize("variant", range(max(N_FWD_VARIANTS, N_BWD_VARIANTS)))
@@ -511,18 +511,19 @@ def test_segmented_backward_alternating_layouts(dev):
         assert_parity(d_init.cpu().numpy(), ri, f"d_init (case {k})")
 
 
+@pytest.mark.parametrize("variant", [11, 22])   # one look-back warp, two
 @pytest.mark.parametrize("saved", [False, True])
-def test_segmented_backward_stall_reports_timeout_then_recovers(dev, saved):
+def test_segmented_backward_stall_reports_timeout_then_recovers(dev, saved, variant):
     """The stall hook holds the first kernel of the call: the carries-only pass
     of the recompute backward, or the segmented backward itself when it starts
     from saved carries.  Either way the call reports QS_ERR_TIMEOUT, and the
     next calls (which read the other set of look-back buffers) are clean."""
     lib = qs.load_library()
-    assert lib.quat_cumprod_debug_set_variant(-1, 11) == qs.QS_OK
+    assert lib.quat_cumprod_debug_set_variant(-1, variant) == qs.QS_OK
     w = workloads.custom("segbwd_stall", 2, 3000, 2, 16, seed=24)
     q, init, d_cum = workloads.make_inputs(w)
     tq, ti, td = (torch.from_numpy(a).to(dev) for a in (q, init, d_cum))
-    assert qs.quat_cumprod_plan(True, 2, 3000, 2, 16, device=dev) == (11, 2)
+    assert qs.quat_cumprod_plan(True, 2, 3000, 2, 16, device=dev) == (variant, 2)
     _, carries = qs.quat_cumprod_fwd_carries(tq, ti)
     assert qs.quat_cumprod_status(device=dev) == qs.QS_OK
     lib.quat_cumprod_debug_set_timeout_ns(50_000_000)    # 50 ms
@@ -636,11 +637,11 @@ def test_plan_picks_the_design_by_lane_groups(dev, name, walk):
 def test_plan_picks_the_segmented_backward_for_many_groups(dev):
     """64 or more 16-lane groups, too few for a walk: the recompute backward is
     the carries pass and the segmented walk (segments of 2 chunks)."""
-    assert qs.quat_cumprod_plan(True, 1, 4096, 32, 32, device=dev) == (14, 2)   # 64 groups
+    assert qs.quat_cumprod_plan(True, 1, 4096, 32, 32, device=dev) == (24, 2)   # 64 groups
     assert qs.quat_cumprod_plan(True, 1, 4096, 31, 32, device=dev) == (0, 3)    # 62 groups
     # from saved carries: the segmented walk whatever the group count
-    assert qs.quat_cumprod_plan("bwd_carries", 1, 131072, 16, 16, device=dev) == (11, 1)
-    assert qs.quat_cumprod_plan("bwd_carries", 4, 1024, 8, 16, device=dev) == (14, 1)   # few units
+    assert qs.quat_cumprod_plan("bwd_carries", 1, 131072, 16, 16, device=dev) == (22, 1)
+    assert qs.quat_cumprod_plan("bwd_carries", 4, 1024, 8, 16, device=dev) == (24, 1)   # few units
     w = workloads.custom("manygroups", 1, 700, 32, 33, q_kind="rotation", theta_max=0.4, seed=200)
-    assert qs.quat_cumprod_plan(True, w.B, w.S, w.H, w.J, device=dev) == (14, 2)
+    assert qs.quat_cumprod_plan(True, w.B, w.S, w.H, w.J, device=dev) == (24, 2)
     check_against_oracle(dev, *workloads.make_inputs(w))
