@@ -51,11 +51,12 @@ FALLBACK_HBM_GBS = 6800.0
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.txt")
 KERNEL_SOURCES = [os.path.join(ROOT, "quaternion_cumulative_product_gb300", "csrc", f)
                   for f in ("quat_scan.cu", "quat_device.cuh", "quat_common.cuh", "quat_tiles.cuh",
-                            "quat_chain.cuh", "quat_walk.cuh", "quat_segwalk.cuh", "quat_segwalk_ws.cuh", "quat_segwalk_bwd.cuh")]
+                            "quat_chain.cuh", "quat_walk.cuh", "quat_segwalk.cuh", "quat_segwalk_ws.cuh", "quat_segwalk_bwd.cuh",
+                            "quat_segwalk_tab.cuh")]
 
 
 # Forward configurations of the segmented chained walk in the library's table.
-SEGWALK_FWD_VARIANTS = (9, 10, 11, 12, 13, 14, 15, 16, 17, 18)
+SEGWALK_FWD_VARIANTS = (9, 10, 11, 12, 13, 14, 15, 16, 17, 18, 19, 20, 21, 22, 23, 24)
 
 
 # Backward configurations of the segmented walk (after its carries-only pass

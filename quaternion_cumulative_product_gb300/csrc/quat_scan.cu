@@ -67,6 +67,7 @@
 #include "quat_chain.cuh"
 #include "quat_segwalk.cuh"
 #include "quat_segwalk_bwd.cuh"
+#include "quat_segwalk_tab.cuh"
 #include "quat_segwalk_ws.cuh"
 #include "quat_tiles.cuh"
 #include "quat_walk.cuh"
@@ -106,6 +107,9 @@ struct Variant {
     // Backward segmented walk: the carries-only forward pass it starts from
     // when it recomputes the carries.
     const Variant *pass = nullptr;
+    // Forward segmented walk with per-unit tables (quat_segwalk_tab_fwd_kernel):
+    // its own argument list.
+    bool tab = false;
 };
 
 #define QS_VARIANT(B, LT, N)                                                                        \
@@ -139,6 +143,12 @@ struct Variant {
         false, reinterpret_cast<const void *>(qs::quat_segwalk_ws_fwd_kernel<qs::IoF32, LT, NSEG, N, NST, K>), \
             nullptr, false, LT, NSEG, N, qs::segwalk_smem_bytes(LT, NSEG, N, NST), false, 0, K, 64  \
     }
+#define QS_SEGWALK_TAB_FWD(LT, NSEG, N, NST, K, NLB)                                                \
+    Variant {                                                                                       \
+        false, reinterpret_cast<const void *>(qs::quat_segwalk_tab_fwd_kernel<qs::IoF32, LT, NSEG, N, NST, K, NLB>), \
+            nullptr, false, LT, NSEG, N, qs::segwalk_tab_smem_bytes(LT, NSEG, N, NST, K), false, 0, K,    \
+            32 + 32 * NLB, true, nullptr, true                                                      \
+    }
 #define QS_WALK_BWD(LT, NSEG, N, NSTF, NSTB, SELF)                                                  \
     Variant {                                                                                       \
         true, reinterpret_cast<const void *>(qs::quat_walk_bwd_kernel<qs::IoF32, LT, NSEG, N, NSTF, NSTB, SELF, false>), \
@@ -165,6 +175,12 @@ const Variant kFwdVariants[] = {
     QS_SEGWALK_SENT_FWD(32, 8, 8, 3, 2),      // 16: as 12, segments of 2 chunks
     QS_SEGWALK_WS_SENT_FWD(16, 8, 8, 6, 1),   // 17: as 14, segments of one chunk
     QS_SEGWALK_WS_SENT_FWD(16, 8, 8, 6, 2),   // 18: as 14, segments of 2 chunks
+    QS_SEGWALK_TAB_FWD(16, 8, 8, 3, 4, 1),    // 19: segmented walk with per-unit tables, no block barrier, 16 lanes
+    QS_SEGWALK_TAB_FWD(16, 8, 8, 3, 4, 2),    // 20: as 19, two look-back warps
+    QS_SEGWALK_TAB_FWD(32, 8, 8, 3, 4, 2),    // 21: as 20, 32 lanes
+    QS_SEGWALK_TAB_FWD(16, 8, 8, 3, 2, 2),    // 22: as 20, segments of 2 chunks
+    QS_SEGWALK_TAB_FWD(16, 8, 8, 3, 1, 2),    // 23: as 20, segments of one chunk
+    QS_SEGWALK_TAB_FWD(32, 8, 8, 3, 2, 2),    // 24: as 22, 32 lanes
 };
 #define QS_WALK_BWD_CAP(LT, NSEG, N, NSTF, NSTB, CAPX4)                                             \
     Variant {                                                                                       \
@@ -172,14 +188,15 @@ const Variant kFwdVariants[] = {
             nullptr, true, LT, NSEG, N, qs::walk_bwd_smem_bytes(LT, NSEG, N, NSTF, NSTB), false, CAPX4 \
     }
 // The carries-only forward pass of the segmented backward (its forward
-// carries, one read of q): 16-lane groups, segments of 4 chunks, 4-stage ring;
-// one look-back warp, or two taking alternate units.
+// carries, one read of q): 16-lane groups, 4-stage ring; segments of 4 chunks
+// and one look-back warp, or segments of 8 chunks and two look-back warps
+// taking alternate units (fewer, longer look-backs).
 const Variant kCarriesPassVariant = Variant{
     false, reinterpret_cast<const void *>(qs::quat_carries_pass_kernel<qs::IoF32, 16, 8, 8, 4, 4>), nullptr, false,
     16, 8, 8, qs::carries_pass_smem_bytes(16, 8, 8, 4, 4), false, 0, 4, 64, true};
 const Variant kCarriesPassVariant2 = Variant{
-    false, reinterpret_cast<const void *>(qs::quat_carries_pass_kernel<qs::IoF32, 16, 8, 8, 4, 4, 4, 2>), nullptr,
-    false, 16, 8, 8, qs::carries_pass_smem_bytes(16, 8, 8, 4, 4), false, 0, 4, 96, true};
+    false, reinterpret_cast<const void *>(qs::quat_carries_pass_kernel<qs::IoF32, 16, 8, 8, 4, 8, 4, 2>), nullptr,
+    false, 16, 8, 8, qs::carries_pass_smem_bytes(16, 8, 8, 4, 8), false, 0, 8, 96, true};
 // The same for bfloat16 tensors (the carries stay fp32).
 const Variant kCarriesPassVariantBf16 = Variant{
     false, reinterpret_cast<const void *>(qs::quat_carries_pass_kernel<qs::IoBF16, 16, 8, 8, 6, 4>), nullptr, false,
@@ -328,6 +345,7 @@ constexpr int kNumBwdBf16 = sizeof(kBwdBf16Variants) / sizeof(kBwdBf16Variants[0
 #undef QS_SEGWALK_WS_FWD
 #undef QS_SEGWALK_SENT_FWD
 #undef QS_SEGWALK_WS_SENT_FWD
+#undef QS_SEGWALK_TAB_FWD
 #undef QS_WALK_FWD
 #undef QS_WALK_BWD
 #undef QS_WALK_BWD_CAP
@@ -351,25 +369,17 @@ constexpr int kWalkFwd = 4, kWalkBwd = 10, kThreeFwd = 0, kThreeBwd = 0;
 // carries-only forward pass when the carries are not saved: 64 bytes per
 // element of DRAM instead of the three kernels' 80), see pick_variant.
 constexpr int kSegBwd = 22;   // segments of 4 chunks, two look-back warps
-// Forward with too few lane groups for a walk: the segmented chained walk
-// (segments of 4 chunks) whose look-back values carry their own state, so a
-// look-back round takes one memory latency.  It measured 0.76 / 0.82 / 0.73 of
-// the copy bandwidth on 1 x 131072 x 16 x 16, 2 x 65536 x 32 x 32 and
-// 2 x 32768 x 16 x 16, against 0.71 / 0.73 / 0.68 with status words
-// (configuration 9), 0.68 / 0.81 / 0.70 warp-specialised (configuration 10)
-// and 0.59 / 0.65 / 0.52 for aggregate / carry / apply.
-constexpr int kSegFwd = 12;
-// From 2^24 elements on, the warp-specialised form with the same values (16
-// lanes, 6-stage ring) measured faster: 0.79 / 0.84 / 0.73-0.74 on the three
-// shapes above; on 4 x 8192 x 8 x 16 it measured 0.50 against 0.53.
-constexpr int kSegFwdLarge = 14;
-constexpr long long kSegFwdLargeElements = 1ll << 24;
-// Short sequences (at most 64 chunks): segments of 2 chunks, one look-back
-// less deep per unit.  Measured alone, 15.0 against 17.1 us on 4 x 1024 x 8 x 16,
-// 2 x 2048 x 8 x 16 and 1 x 4096 x 4 x 16 (the event clock ticks by about 2 us);
-// 25.2 against 23.2 us on 2 x 8192 x 8 x 16 (128 chunks).
-constexpr int kSegFwdShort = 16;
-constexpr int kSegFwdShortChunks = 64;
+// Forward with too few lane groups for a walk: the segmented walk with
+// per-unit tables and two look-back warps (no block barrier), segments of 2
+// chunks; 32-lane groups when there are at most 32 of them.  Measured alone
+// (fraction of the copy bandwidth at 32 bytes per element) against the
+// warp-specialised segmented walk with per-chunk folds (configuration 14):
+// 1 x 131072 x 16 x 16 0.93 (configuration 24) / 0.90 (22) against 0.77;
+// 2 x 65536 x 32 x 32 0.98 (22) / 0.97 (24) against 0.83; 2 x 4096 x 16 x 32
+// 0.68 (24) / 0.63 (22) against 0.49; 4 x 1024 x 8 x 16 0.17 for both against
+// 0.15.  (On 8 x 4096 x 16 x 32 the walk stays ahead: 0.94 against 0.91.)
+constexpr int kSegFwd = 22, kSegFwdFew = 24;
+constexpr long long kSegFwdFewGroups = 32;   // lane groups of 32
 constexpr int kNumFwd = sizeof(kFwdVariants) / sizeof(kFwdVariants[0]);
 constexpr int kNumBwd = sizeof(kBwdVariants) / sizeof(kBwdVariants[0]);
 
@@ -762,8 +772,7 @@ int pick_variant(bool bwd, int64_t B, int64_t S, int64_t HJ, int sms, Mode mode)
         if (mode == Mode::FROM_CARRIES || groups >= kSegBwdManyGroups) return seg;
         return kThreeBwd;
     }
-    if ((long long)B * S * HJ >= kSegFwdLargeElements) return kSegFwdLarge;
-    return (S + 63) / 64 <= kSegFwdShortChunks ? kSegFwdShort : kSegFwd;
+    return groups <= kSegFwdFewGroups ? kSegFwdFew : kSegFwd;
 }
 
 // `capturing`: the call is being captured into a CUDA graph, whose launches
@@ -1078,8 +1087,9 @@ int launch(bool bwd, const void *q, const void *d_cum, void *out, const void *in
         }
         void *args[] = {&qmap, &init4, &out4, &save4, &status, &tickets, &aggv, &inclv, &agg_next, &incl_next,
                         &pl.geo, &ctl, &epoch};
-        if (cudaLaunchKernel(pl.v->agg, dim3((unsigned)grid), dim3(pl.v->threads()), args, pl.v->smem(), stream) !=
-            cudaSuccess) {
+        void *tab_args[] = {&qmap, &init4, &out4, &save4, &tickets, &aggv, &inclv, &agg_next, &incl_next, &pl.geo, &ctl};
+        if (cudaLaunchKernel(pl.v->agg, dim3((unsigned)grid), dim3(pl.v->threads()), pl.v->tab ? tab_args : args,
+                             pl.v->smem(), stream) != cudaSuccess) {
             cudaGetLastError();
             if (pl.v->sent) lb_values_invalidate(dev, stream, LB_FWD);
             return QS_ERR_CUDA;

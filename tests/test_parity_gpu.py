@@ -186,8 +186,8 @@ def test_empty_sizes(dev):
 # in one round trip; 13, 14: as 10, 11 with those values; backward 10: at most
 # two CTAs per SM, more lane groups in waves; backward 11-14: the segmented
 # walk of the backward, after its carries-only forward pass).
-N_FWD_VARIANTS, N_BWD_VARIANTS = 19, 25
-SEGWALK_FWD = [9, 10, 11, 12, 13, 14, 15, 16, 17, 18]
+N_FWD_VARIANTS, N_BWD_VARIANTS = 25, 25
+SEGWALK_FWD = [9, 10, 11, 12, 13, 14, 15, 16, 17, 18, 19, 20, 21, 22, 23, 24]
 SEGWALK_BWD = [11, 12, 13, 14, 15, 16, 17, 18, 19, 20, 21, 22, 23, 24]
 
 
@@ -297,7 +297,7 @@ def test_segmented_walk_alternating_layouts(dev):
         assert_parity(cum.cpu().numpy(), ref, f"cum (case {k})")
 
 
-@pytest.mark.parametrize("variant", [9, 10, 12, 13])   # one CTA role, warp-specialised, each with self-describing values
+@pytest.mark.parametrize("variant", [9, 10, 12, 13, 19, 20])   # one CTA role, warp-specialised, each with self-describing values; per-unit tables
 def test_segmented_walk_stall_reports_timeout_then_recovers(dev, variant):
     lib = qs.load_library()
     assert lib.quat_cumprod_debug_set_variant(variant, -1) == qs.QS_OK
@@ -624,11 +624,10 @@ def test_plan_picks_the_design_by_lane_groups(dev, name, walk):
         # fewer than 64 sixteen-lane groups the aggregate / carry / apply backward
         assert kernels == (1 if walk or not bwd else 3), (name, bwd, variant, kernels)
         if not walk and not bwd:
-            # the segmented walk with self-describing look-back values: the
-            # warp-specialised form (14) from 2^24 elements, else the one-role
-            # form, with segments of 2 chunks (16) for at most 64 chunks (12 beyond)
-            short = (w.S + 63) // 64 <= 64
-            assert variant == (14 if w.elements >= 1 << 24 else 16 if short else 12), (name, variant)
+            # the segmented walk with per-unit tables, segments of 2 chunks:
+            # 32-lane groups (24) when there are at most 32 of them, else 16 (22)
+            groups32 = w.B * ((w.H * w.J + 31) // 32)
+            assert variant == (24 if groups32 <= 32 else 22), (name, variant)
         if not walk and bwd:
             assert variant == 0, (name, variant)
     assert qs.quat_cumprod_plan(True, 2, 0, 3, 4, device=dev) == (-1, 0)
