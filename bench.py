@@ -52,7 +52,7 @@ TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.txt")
 KERNEL_SOURCES = [os.path.join(ROOT, "quaternion_cumulative_product_gb300", "csrc", f)
                   for f in ("quat_scan.cu", "quat_device.cuh", "quat_common.cuh", "quat_tiles.cuh",
                             "quat_chain.cuh", "quat_walk.cuh", "quat_segwalk.cuh", "quat_segwalk_ws.cuh", "quat_segwalk_bwd.cuh",
-                            "quat_segwalk_tab.cuh")]
+                            "quat_segwalk_tab.cuh", "quat_short.cuh")]
 
 
 # Forward configurations of the segmented chained walk in the library's table.

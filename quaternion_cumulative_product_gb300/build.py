@@ -15,7 +15,8 @@ ROOT = os.path.dirname(HERE)
 SOURCES = [os.path.join(HERE, "csrc", "quat_scan.cu")]
 HEADERS = [os.path.join(HERE, "csrc", f) for f in
            ("quat_device.cuh", "quat_common.cuh", "quat_tiles.cuh", "quat_chain.cuh", "quat_walk.cuh",
-            "quat_segwalk.cuh", "quat_segwalk_ws.cuh", "quat_segwalk_bwd.cuh", "quat_segwalk_tab.cuh")]
+            "quat_segwalk.cuh", "quat_segwalk_ws.cuh", "quat_segwalk_bwd.cuh", "quat_segwalk_tab.cuh",
+            "quat_short.cuh")]
 DEPS = SOURCES + HEADERS + [os.path.join(ROOT, "include", "quat_cumprod.h")]
 LIB = os.path.join(HERE, "libquatscan.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

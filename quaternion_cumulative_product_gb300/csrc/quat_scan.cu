@@ -69,6 +69,7 @@
 #include "quat_segwalk_bwd.cuh"
 #include "quat_segwalk_tab.cuh"
 #include "quat_segwalk_ws.cuh"
+#include "quat_short.cuh"
 #include "quat_tiles.cuh"
 #include "quat_walk.cuh"
 
@@ -110,6 +111,9 @@ struct Variant {
     // Forward segmented walk with per-unit tables (quat_segwalk_tab_fwd_kernel):
     // its own argument list.
     bool tab = false;
+    // Short sequences (quat_short_*_kernel): the whole sequence of LT lanes in
+    // one CTA of LT * nseg threads, n steps each; S <= smax (0: another design).
+    int smax = 0;
 };
 
 #define QS_VARIANT(B, LT, N)                                                                        \
@@ -154,6 +158,16 @@ struct Variant {
         true, reinterpret_cast<const void *>(qs::quat_walk_bwd_kernel<qs::IoF32, LT, NSEG, N, NSTF, NSTB, SELF, false>), \
             nullptr, true, LT, NSEG, N, qs::walk_bwd_smem_bytes(LT, NSEG, N, NSTF, NSTB)            \
     }
+#define QS_SHORT_FWD(LT, NS, R)                                                                     \
+    Variant {                                                                                       \
+        false, reinterpret_cast<const void *>(qs::quat_short_fwd_kernel<qs::IoF32, LT, NS, R>), nullptr, false, LT, \
+            NS, R, 0, false, 0, 0, 0, false, nullptr, false, NS * R                                 \
+    }
+#define QS_SHORT_BWD(LT, NS, R)                                                                     \
+    Variant {                                                                                       \
+        false, reinterpret_cast<const void *>(qs::quat_short_bwd_kernel<qs::IoF32, LT, NS, R>), nullptr, true, LT, \
+            NS, R, 0, false, 0, 0, 0, false, nullptr, false, NS * R                                 \
+    }
 const Variant kFwdVariants[] = {
     QS_VARIANT(false, 32, 8),          // 0: three kernels, 64-step chunks, 32 KiB tiles
     QS_VARIANT(false, 32, 4),          // 1: three kernels, 32-step chunks
@@ -181,6 +195,11 @@ const Variant kFwdVariants[] = {
     QS_SEGWALK_TAB_FWD(16, 8, 8, 3, 2, 2),    // 22: as 20, segments of 2 chunks
     QS_SEGWALK_TAB_FWD(16, 8, 8, 3, 1, 2),    // 23: as 20, segments of one chunk
     QS_SEGWALK_TAB_FWD(32, 8, 8, 3, 2, 2),    // 24: as 22, 32 lanes
+    QS_SHORT_FWD(4, 128, 8),                  // 25: short sequences (S <= 1024), 4 lanes a CTA
+    QS_SHORT_FWD(2, 128, 8),                  // 26: as 25, 2 lanes
+    QS_SHORT_FWD(8, 128, 8),                  // 27: as 25, 8 lanes (1024 threads)
+    QS_SHORT_FWD(4, 256, 8),                  // 28: S <= 2048, 4 lanes (1024 threads)
+    QS_SHORT_FWD(16, 32, 8),                  // 29: S <= 256, 16 lanes
 };
 #define QS_WALK_BWD_CAP(LT, NSEG, N, NSTF, NSTB, CAPX4)                                             \
     Variant {                                                                                       \
@@ -239,6 +258,11 @@ const Variant kBwdVariants[] = {
     QS_SEGWALK_BWD2(16, 8, 8, 2, 4, 2),            // 22: as 11, two look-back warps (alternate units; so is its carries pass)
     QS_SEGWALK_BWD2(16, 8, 8, 2, 2, 2),            // 23: as 14, two look-back warps
     QS_SEGWALK_BWD2(16, 8, 8, 3, 2, 2),            // 24: as 12, two look-back warps
+    QS_SHORT_BWD(4, 128, 8),                       // 25: short sequences (S <= 1024), 4 lanes a CTA
+    QS_SHORT_BWD(2, 128, 8),                       // 26: as 25, 2 lanes
+    QS_SHORT_BWD(8, 64, 8),                        // 27: S <= 512, 8 lanes
+    QS_SHORT_BWD(2, 256, 8),                       // 28: S <= 2048, 2 lanes
+    QS_SHORT_BWD(16, 32, 8),                       // 29: S <= 256, 16 lanes
 };
 // The backward from caller-provided carries: the reverse walk alone.
 const Variant kBwdGiven = Variant{true,
@@ -296,6 +320,16 @@ const Variant kBwdGiven = Variant{true,
         false, reinterpret_cast<const void *>(qs::quat_segwalk_fwd_kernel<qs::IoBF16, LT, NSEG, N, NST, K>), \
             nullptr, false, LT, NSEG, N, qs::segwalk_smem_bytes(LT, NSEG, N, NST, 8), false, 0, K   \
     }
+#define QS_SHORT_FWD16(LT, NS, R)                                                                   \
+    Variant {                                                                                       \
+        false, reinterpret_cast<const void *>(qs::quat_short_fwd_kernel<qs::IoBF16, LT, NS, R>), nullptr, false, LT, \
+            NS, R, 0, false, 0, 0, 0, false, nullptr, false, NS * R                                 \
+    }
+#define QS_SHORT_BWD16(LT, NS, R)                                                                   \
+    Variant {                                                                                       \
+        false, reinterpret_cast<const void *>(qs::quat_short_bwd_kernel<qs::IoBF16, LT, NS, R>), nullptr, true, LT, \
+            NS, R, 0, false, 0, 0, 0, false, nullptr, false, NS * R                                 \
+    }
 const Variant kFwdBf16Variants[] = {
     QS_WALK_FWD16(32, 8, 8, 6),            // 0: 32 lanes x 64 steps, 6 x 16 KiB ring
     QS_WALK_FWD16(16, 8, 8, 6),            // 1: 16 lanes x 64 steps (128 threads), 6 x 8 KiB
@@ -305,6 +339,8 @@ const Variant kFwdBf16Variants[] = {
     QS_SEGWALK_FWD16(32, 8, 8, 3, 4),      // 5: segmented chained walk (few lane groups)
     QS_SEGWALK_SENT_FWD16(32, 8, 8, 3, 4), // 6: as 5, one-latency look-back rounds
     QS_SEGWALK_WS_SENT_FWD16(16, 8, 8, 6, 4),   // 7: segmented walk, warp-specialised, 16 lanes
+    QS_SHORT_FWD16(2, 128, 8),             // 8: short sequences (S <= 1024), 2 lanes a CTA
+    QS_SHORT_FWD16(4, 256, 8),             // 9: S <= 2048, 4 lanes (1024 threads)
 };
 const Variant kBwdBf16Variants[] = {
     QS_WALK_BWD16(16, 8, 8, 8, 4, false),  // 0: 16 lanes x 64 steps (128 threads), 64 KiB rings
@@ -315,8 +351,13 @@ const Variant kBwdBf16Variants[] = {
     QS_WALK_BWD16_MINB(16, 8, 8, 8, 4, 3), // 5: as 0, registers capped for 3 CTAs per SM (many lane groups)
     QS_SEGWALK_BWD16(16, 8, 8, 3, 4, 2),   // 6: segmented walk (after the carries pass), segments of 4 chunks
     QS_SEGWALK_BWD16(16, 8, 8, 3, 2, 2),   // 7: segmented walk, segments of 2 chunks
+    QS_SHORT_BWD16(2, 128, 8),             // 8: short sequences (S <= 1024), 2 lanes a CTA
+    QS_SHORT_BWD16(8, 64, 8),              // 9: S <= 512, 8 lanes
+    QS_SHORT_BWD16(2, 256, 8),             // 10: S <= 2048, 2 lanes
 };
 #undef QS_VARIANT16
+#undef QS_SHORT_FWD16
+#undef QS_SHORT_BWD16
 #undef QS_SEGWALK_FWD16
 #undef QS_SEGWALK_SENT_FWD16
 #undef QS_SEGWALK_WS_SENT_FWD16
@@ -351,6 +392,8 @@ constexpr int kNumBwdBf16 = sizeof(kBwdBf16Variants) / sizeof(kBwdBf16Variants[0
 #undef QS_WALK_BWD_CAP
 #undef QS_SEGWALK_BWD
 #undef QS_SEGWALK_BWD2
+#undef QS_SHORT_FWD
+#undef QS_SHORT_BWD
 // Lanes per block of the carry scan (sequences of more than 256 chunks).
 constexpr int kCarryScanLanes = 2;
 
@@ -756,16 +799,41 @@ int layout_plan(bool bwd, int64_t B, int64_t S, int64_t HJ, int sms, Plan *pl, M
 constexpr int kSegBwdShort = 24;           // segments of 2 chunks, two look-back warps
 constexpr long long kSegBwdManyGroups = 64;
 
+// Short sequences with too few lane groups for a walk: the whole sequence of
+// a few lanes in one CTA (no look-back, one launch), the configuration that
+// fits S with the fewest idle segments.  Measured alone on 152 SMs (L2
+// flushed; a trivial kernel timed the same way takes 6.8 us):
+//   4 x 1024 x 8 x 16: forward 10.9 us against 15.0 (segmented walk),
+//                      backward 12.9 us against 23.2 (three kernels);
+//   2 x 2048 x 16 x 16: forward 12.9 against 17.0, backward 23.2 against 31.4;
+//   4 x 512 x 16 x 16: backward 12.9 (8 lanes, S <= 512) against 17.0 (2 lanes)
+//                      and 31.4 (segmented walk).
+// Returns the configuration in the fp32 or bf16 table, or -1 past 2048 steps.
+int short_variant(bool bwd, int64_t S, bool bf16) {
+    if (S > 2048) return -1;
+    if (bf16) {
+        if (bwd) return S <= 512 ? 9 : S <= 1024 ? 8 : 10;
+        return S <= 1024 ? 8 : 9;
+    }
+    if (bwd) return S <= 512 ? 27 : S <= 1024 ? 26 : 28;
+    return S <= 1024 ? 26 : 28;
+}
+
 int pick_variant(bool bwd, int64_t B, int64_t S, int64_t HJ, int sms, Mode mode) {
     {
         std::lock_guard<std::mutex> lk(g_mu);
         const int forced = bwd ? g_bwd_variant : g_fwd_variant;
-        if (forced >= 0) return forced;
+        // (a short-sequence configuration only where the sequence fits it)
+        if (forced >= 0 && (S <= (bwd ? kBwdVariants : kFwdVariants)[forced].smax ||
+                            (bwd ? kBwdVariants : kFwdVariants)[forced].smax == 0))
+            return forced;
     }
     const Variant &w = bwd ? kBwdVariants[kWalkBwd] : kFwdVariants[kWalkFwd];
     const long long groups = (long long)B * ((HJ + w.lt - 1) / w.lt);
     const long long need = bwd ? 3ll * sms / 2 : 3ll * sms / 4;
     if (groups >= need) return bwd ? kWalkBwd : kWalkFwd;
+    const int sv = short_variant(bwd, S, false);
+    if (sv >= 0) return sv;
     if (bwd) {
         const long long units4 = groups * ((S + 4 * 64 - 1) / (4 * 64));   // segments of 4 chunks
         const int seg = (groups >= kSegBwdManyGroups || units4 < 4ll * sms) ? kSegBwdShort : kSegBwd;
@@ -792,7 +860,8 @@ int make_plan(bool bwd, int64_t B, int64_t S, int64_t HJ, int sms, Plan *pl, Mod
             std::lock_guard<std::mutex> lk(g_mu);
             forced = bwd ? g_bwd_variant16 : g_fwd_variant16;
         }
-        if (forced >= 0) {
+        const Variant *fv = forced < 0 ? nullptr : bwd ? &kBwdBf16Variants[forced] : &kFwdBf16Variants[forced];
+        if (fv != nullptr && (fv->smax == 0 || S <= fv->smax)) {
             vi = forced;
         } else {   // the same rule as for fp32: a walk when the lane groups fill the GPU
             const int wi = bwd ? kBwdBf16Default : kFwdBf16Default;
@@ -800,6 +869,7 @@ int make_plan(bool bwd, int64_t B, int64_t S, int64_t HJ, int sms, Plan *pl, Mod
             const long long groups = (long long)B * ((HJ + w.lt - 1) / w.lt);
             const long long need = bwd ? 3ll * sms / 2 : 3ll * sms / 4;
             vi = groups >= need ? wi : (bwd ? kBwdBf16Few : kFwdBf16Few);
+            if (groups < need && short_variant(bwd, S, true) >= 0) vi = short_variant(bwd, S, true);
             if (bwd && groups > 2ll * sms) vi = kBwdBf16Many;
         }
     } else {
@@ -811,7 +881,7 @@ int make_plan(bool bwd, int64_t B, int64_t S, int64_t HJ, int sms, Plan *pl, Mod
         vi = kThreeFwd;
         v = &kFwdVariants[vi];
     }
-    if (mode != Mode::PLAIN && v->T() != QS_CARRY_STEPS) {
+    if (mode != Mode::PLAIN && v->T() != QS_CARRY_STEPS && v->smax == 0) {
         // The carries are defined on QS_CARRY_STEPS-step chunks: keep the
         // design, take its default configuration (which has that chunk).
         vi = v->walk ? (bwd ? kWalkBwd : kWalkFwd) : (bwd ? kThreeBwd : kThreeFwd);
@@ -854,6 +924,10 @@ int layout_plan(bool bwd, int64_t B, int64_t S, int64_t HJ, int sms, Plan *pl, M
     g.NL = (int)(NG * LT);
     const size_t per = (size_t)pl->tiles * LT * 16;
     size_t off = sizeof(qs::WsHeader);
+    if (pl->v->smax > 0) {   // short sequences: one CTA per lane group, nothing but the status block
+        pl->ws_bytes = off;
+        return QS_OK;
+    }
     if (pl->v->segk > 0 && bwd) {
         // Backward segmented walk: the look-back values live apart (LbValues),
         // the ticket counters in the head of the status-word allocation; the
@@ -1028,6 +1102,33 @@ int launch_segwalk_bwd(const Plan &pl, int dev, unsigned char *ws, const void *q
     return QS_OK;
 }
 
+// Short sequences (pl.v->smax > 0): one launch, one CTA per lane group.  From
+// saved carries the backward takes init = carries[:, 0] and recomputes the rest
+// (the whole sequence is in the CTA's registers anyway).
+int launch_short(const Plan &pl, bool bwd, const void *q, const void *d_cum, void *out, const void *init,
+                 void *d_init, int64_t S, int64_t HJ, cudaStream_t stream, Mode mode, float *carries, bool bf16) {
+    const void *init_p = init;
+    long long init_stride = HJ;
+    int init_f32 = bf16 ? 0 : 1;
+    if (mode == Mode::FROM_CARRIES) {
+        init_p = carries;
+        init_stride = ((S + QS_CARRY_STEPS - 1) / QS_CARRY_STEPS) * HJ;
+        init_f32 = 1;
+    }
+    qs::Geometry geo = pl.geo;
+    float4 *save4 = mode == Mode::SAVE_CARRIES ? reinterpret_cast<float4 *>(carries) : nullptr;
+    const void *q4 = q, *d4 = d_cum;
+    void *out4 = out, *dinit4 = d_init;
+    void *fwd_args[] = {&q4, &init_p, &init_stride, &init_f32, &out4, &save4, &geo};
+    void *bwd_args[] = {&q4, &d4, &init_p, &init_stride, &init_f32, &out4, &dinit4, &geo};
+    if (cudaLaunchKernel(pl.v->agg, dim3((unsigned)geo.NG), dim3(pl.v->threads()), bwd ? bwd_args : fwd_args, 0,
+                         stream) != cudaSuccess) {
+        cudaGetLastError();
+        return QS_ERR_CUDA;
+    }
+    return QS_OK;
+}
+
 // `carries`: written (Mode::SAVE_CARRIES) or read (Mode::FROM_CARRIES),
 // [B, ceil(S / QS_CARRY_STEPS), H*J] float4; unused otherwise.
 // `bf16`: the tensors hold bfloat16 quaternions (8 bytes); walk kernels only.
@@ -1049,6 +1150,8 @@ int launch(bool bwd, const void *q, const void *d_cum, void *out, const void *in
     unsigned char *ws = nullptr;
     rc = ensure_workspace(dev, stream, pl.ws_bytes, &ws);
     if (rc != QS_OK) return rc;
+    if (pl.v->smax > 0)
+        return launch_short(pl, bwd, q, d_cum, out, init, d_init, S, HJ, stream, mode, carries, bf16);
     CUtensorMap qmap, dmap;
     const int eb = bf16 ? 8 : 16;
     rc = make_map(&qmap, q, B, S, HJ, pl.v->lt, pl.v->T(), eb);
@@ -1607,7 +1710,7 @@ extern "C" int quat_cumprod_plan(int call, int64_t B, int64_t S, int64_t H, int6
     if (rc != QS_OK) return rc;
     *variant = pl.vi;
     if (pl.v->segk > 0 && bwd) *kernels = mode == Mode::FROM_CARRIES ? 1 : 2;   // (+ the carries-only pass)
-    else *kernels = (pl.v->walk || pl.v->chain || pl.v->segk > 0) ? 1 : (mode == Mode::SAVE_CARRIES ? 4 : 3);
+    else *kernels = (pl.v->walk || pl.v->chain || pl.v->segk > 0 || pl.v->smax > 0) ? 1 : (mode == Mode::SAVE_CARRIES ? 4 : 3);
     return QS_OK;
 }
 

@@ -57,8 +57,10 @@ def bf16_inputs(dev, w):
 # chained walk, 6 the same with self-describing look-back values, 7 its
 # warp-specialised form; backward 0-3 walks, 4 three kernels, 5 walk with
 # registers capped for three CTAs per SM, 6 and 7 the segmented walk after its
-# carries pass (segments of 4 and 2 chunks).
-N_BF16_FWD, N_BF16_BWD = 8, 8
+# carries pass (segments of 4 and 2 chunks); forward 8, 9 and backward 8-10
+# short sequences (the whole sequence of a few lanes in one CTA, up to 1024,
+# 2048 / 1024, 512, 2048 steps).
+N_BF16_FWD, N_BF16_BWD = 10, 11
 
 
 @pytest.fixture(autouse=True)
@@ -69,7 +71,8 @@ def reset_bf16_variant():
 
 @pytest.mark.parametrize("variant", range(max(N_BF16_FWD, N_BF16_BWD)))
 @pytest.mark.parametrize("dims", [(1, 64, 2, 4), (2, 333, 3, 16), (3, 1100, 1, 40), (1, 70, 5, 2),
-                                  (2, 1, 1, 2), (1, 5000, 2, 32)])
+                                  (2, 1, 1, 2), (1, 5000, 2, 32), (1, 512, 1, 6), (1, 1024, 3, 2),
+                                  (1, 2048, 1, 2)])
 def test_bf16_matches_oracle(dev, dims, variant):
     fv = variant if variant < N_BF16_FWD else -1
     bv = variant if variant < N_BF16_BWD else -1
@@ -119,11 +122,14 @@ def test_bf16_rounding_is_the_only_difference_from_fp32(dev):
 
 @pytest.mark.parametrize("name,walk", [("mamba3", True), ("large", True), ("long", False), ("small", False)])
 def test_bf16_plan_picks_the_design_by_lane_groups(dev, name, walk):
-    """Walks for many lane groups; else the segmented walk forward, three kernels backward."""
+    """Walks for many lane groups; else, for short sequences, the whole sequence
+    of a few lanes in one CTA; else the segmented walk forward, three kernels backward."""
     w = workloads.WORKLOADS[name]
     assert qs.quat_cumprod_plan("fwd_bf16", w.B, w.S, w.H, w.J, device=dev)[1] == 1
     variant, kernels = qs.quat_cumprod_plan("bwd_bf16", w.B, w.S, w.H, w.J, device=dev)
-    assert kernels == (1 if walk else 3)
+    assert kernels == (1 if walk or w.S <= 2048 else 3)
+    if not walk and w.S <= 2048:
+        assert variant == (9 if w.S <= 512 else 8 if w.S <= 1024 else 10), (name, variant)
     if walk:   # more lane groups than two CTAs per SM hold: the register-capped walk (5)
         groups = w.B * ((w.H * w.J + 15) // 16)
         sms = torch.cuda.get_device_properties(dev).multi_processor_count

@@ -142,6 +142,29 @@ def test_segmented_walks_write_and_read_carries(dev, fv, bv, dims):
     assert normwise(d_init.cpu().numpy(), ref_di) <= TOL
 
 
+# The short-sequence kernels write the carries (forward) and start from
+# carries[:, 0] (backward, which recomputes the rest).
+@pytest.mark.parametrize("fv,bv", [(25, 25), (26, 26), (27, 27), (28, 28)])
+@pytest.mark.parametrize("dims", [(2, 333, 3, 16), (1, 63, 1, 1), (3, 64, 1, 5), (1, 500, 2, 3)])
+def test_short_sequences_write_and_read_carries(dev, fv, bv, dims):
+    lib = qs.load_library()
+    assert lib.quat_cumprod_debug_set_variant(fv, bv) == qs.QS_OK
+    assert qs.quat_cumprod_plan("fwd_carries", *dims, device=dev) == (fv, 1)
+    assert qs.quat_cumprod_plan("bwd_carries", *dims, device=dev) == (bv, 1)
+    w = workloads.custom("shortcarries", *dims, q_kind="rotation", theta_max=0.5, seed=fv * 16 + bv)
+    q, init, d_cum = workloads.make_inputs(w)
+    tq, ti, td = to_dev(dev, q, init, d_cum)
+    cum, carries = qs.quat_cumprod_fwd_carries(tq, ti)
+    d_q, d_init = qs.quat_cumprod_bwd_carries(tq, carries, td)
+    assert qs.quat_cumprod_status(device=dev) == qs.QS_OK
+    ref_cum = oracle.fwd(q, init)
+    ref_dq, ref_di = oracle.bwd(q, init, d_cum)
+    assert normwise(cum.cpu().numpy(), ref_cum) <= TOL
+    assert normwise(carries.cpu().numpy(), expected_carries(ref_cum, init)) <= TOL
+    assert normwise(d_q.cpu().numpy(), ref_dq) <= TOL
+    assert normwise(d_init.cpu().numpy(), ref_di) <= TOL
+
+
 def test_long_from_saved_carries_full_size_sampled_lanes(dev):
     """The long workload (1 x 131072 x 16 x 16) at full size through the
     segmented walks of both directions, compared on sampled whole lanes."""
