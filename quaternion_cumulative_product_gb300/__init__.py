@@ -74,6 +74,9 @@ def library_path() -> str:
 def load_library():
     """Loads ``libquatscan.so`` (raises if it has not been built)."""
     global _lib
+    lib = _lib
+    if lib is not None:   # loaded: no lock on the per-call path
+        return lib
     with _lock:
         if _lib is not None:
             return _lib
@@ -125,24 +128,36 @@ def quat_cumprod_strerror(status: int) -> str:
     return load_library().quat_cumprod_strerror(int(status)).decode()
 
 
+_torch_mod = None
+_NULL_CONTEXT = contextlib.nullcontext()
+
+
 def _torch():
-    import torch
-    return torch
+    global _torch_mod
+    if _torch_mod is None:
+        import torch
+        _torch_mod = torch
+    return _torch_mod
 
 
 def _on_device(device):
     """The CUDA device context for a call on ``device``; none when it is already current."""
     torch = _torch()
     if device.index is None or torch.cuda.current_device() == device.index:
-        return contextlib.nullcontext()
+        return _NULL_CONTEXT
     return torch.cuda.device(device)
 
 
 def _stream_handle(stream, device):
+    """The cudaStream_t of ``stream``, else of the current torch stream on ``device``."""
     torch = _torch()
-    if stream is None:
-        stream = torch.cuda.current_stream(device)
-    return ctypes.c_void_p(stream.cuda_stream)
+    if stream is not None:
+        return ctypes.c_void_p(stream.cuda_stream)
+    raw = getattr(torch._C, "_cuda_getCurrentRawStream", None)   # no Stream object per call
+    if raw is not None:
+        index = device.index if device.index is not None else torch.cuda.current_device()
+        return ctypes.c_void_p(raw(index))
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
 
 
 def _check_tensor(name, t, shape, device=None, dtype=None):

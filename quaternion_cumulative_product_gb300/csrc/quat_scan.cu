@@ -232,6 +232,12 @@ const Variant kCarriesPassVariantBf16 = Variant{
             nullptr, true, LT, NSEG, N, qs::segwalk_bwd_smem_bytes(LT, NSEG, N, NST, K), false, 0, K, 96, true, \
             &kCarriesPassVariant2                                                                   \
     }
+#define QS_SEGWALK_BWD_LAG(LT, NSEG, N, NST, K, MINB, DL, LB)                                      \
+    Variant {                                                                                       \
+        false, reinterpret_cast<const void *>(qs::quat_segwalk_bwd_kernel<qs::IoF32, LT, NSEG, N, NST, K, MINB, LB, false, 2, DL>), \
+            nullptr, true, LT, NSEG, N, qs::segwalk_bwd_smem_bytes(LT, NSEG, N, NST, K, 16, DL + 1), false, 0, K, 96, \
+            true, &kCarriesPassVariant2                                                             \
+    }
 const Variant kBwdVariants[] = {
     QS_VARIANT(true, 32, 8),           // 0: three kernels, 64-step chunks, 64 KiB tiles
     QS_VARIANT(true, 32, 4),           // 1: three kernels, 32-step chunks
@@ -263,6 +269,10 @@ const Variant kBwdVariants[] = {
     QS_SHORT_BWD(8, 64, 8),                        // 27: S <= 512, 8 lanes
     QS_SHORT_BWD(2, 256, 8),                       // 28: S <= 2048, 2 lanes
     QS_SHORT_BWD(16, 32, 8),                       // 29: S <= 256, 16 lanes
+    QS_SEGWALK_BWD_LAG(16, 8, 8, 2, 2, 2, 3, 4),   // 30: as 23, walk 2 three units behind walk 1
+    QS_SEGWALK_BWD_LAG(16, 8, 8, 2, 2, 2, 2, 4),   // 31: as 23, walk 2 two units behind
+    QS_SEGWALK_BWD_LAG(16, 8, 8, 2, 3, 2, 2, 4),   // 32: as 31, segments of 3 chunks
+    QS_SEGWALK_BWD_LAG(16, 8, 8, 2, 2, 2, 2, 8),   // 33: as 31, look-back batches of 8
 };
 // The backward from caller-provided carries: the reverse walk alone.
 const Variant kBwdGiven = Variant{true,
@@ -392,6 +402,7 @@ constexpr int kNumBwdBf16 = sizeof(kBwdBf16Variants) / sizeof(kBwdBf16Variants[0
 #undef QS_WALK_BWD_CAP
 #undef QS_SEGWALK_BWD
 #undef QS_SEGWALK_BWD2
+#undef QS_SEGWALK_BWD_LAG
 #undef QS_SHORT_FWD
 #undef QS_SHORT_BWD
 // Lanes per block of the carry scan (sequences of more than 256 chunks).
@@ -411,7 +422,7 @@ constexpr int kWalkFwd = 4, kWalkBwd = 10, kThreeFwd = 0, kThreeBwd = 0;
 // Backward with too few lane groups for a walk: the segmented walk (after a
 // carries-only forward pass when the carries are not saved: 64 bytes per
 // element of DRAM instead of the three kernels' 80), see pick_variant.
-constexpr int kSegBwd = 22;   // segments of 4 chunks, two look-back warps
+constexpr int kSegBwdLag = 31;   // segments of 2 chunks, walk 2 two units behind walk 1
 // Forward with too few lane groups for a walk: the segmented walk with
 // per-unit tables and two look-back warps (no block barrier), segments of 2
 // chunks; 32-lane groups when there are at most 32 of them.  Measured alone
@@ -786,17 +797,20 @@ int layout_plan(bool bwd, int64_t B, int64_t S, int64_t HJ, int sms, Plan *pl, M
 // measured on one GB300 with L2 flushed before every call (fraction of the
 // copy bandwidth at 48 bytes per element), the segmented walk with two
 // look-back warps:
-//  * from saved carries, the segmented walk: segments of 4 chunks on long
-//    sequences of few groups (1 x 131072 x 16 x 16: 0.75; with 2 chunks 0.58,
-//    the look-backs run deep), of 2 chunks when the groups are many or the
-//    units few (2 x 65536 x 32 x 32: 0.92 against 0.78; 4 x 1024 x 8 x 16:
-//    0.22 against 0.20); the three kernels measured 0.58 / 0.60 / 0.14;
-//  * recomputing the carries, the segmented walk after its carries pass only
-//    with 64 groups or more (2 x 65536 x 32 x 32: 0.70 against 0.60 for the
-//    three kernels); with fewer the carries pass costs about what the three
-//    kernels' second read does (1 x 131072 x 16 x 16: 0.57 against 0.58;
-//    4 x 1024 x 8 x 16: 0.13 against 0.16).
-constexpr int kSegBwdShort = 24;           // segments of 2 chunks, two look-back warps
+//  * on long sequences of few groups (at least 4 units of 4 chunks per SM),
+//    segments of 2 chunks with walk 2 two units behind walk 1, so that a
+//    unit's look-back (about 3 us, running deep) ends before its second walk
+//    is due: from saved carries 1 x 131072 x 16 x 16 0.79 (0.75 with segments
+//    of 4 chunks and walk 2 one unit behind, 0.58 with 2 chunks one unit
+//    behind), 1 x 262144 x 16 x 16 0.80, 2 x 65536 x 16 x 16 0.78; recomputing
+//    the carries (the carries pass first) 0.61 / 0.63 / 0.61 against 0.58 /
+//    0.60 / 0.58 for the three kernels;
+//  * with 64 groups or more, segments of 2 chunks one unit behind, one CTA
+//    per SM (2 x 65536 x 32 x 32: 0.92 from saved carries, 0.71 recomputing
+//    against 0.60 for the three kernels; 4 x 32768 x 16 x 16: 0.80 / 0.62);
+//  * with few units, from saved carries the same (4 x 4096 x 8 x 16), and
+//    recomputing the three kernels.
+constexpr int kSegBwdShort = 24;           // segments of 2 chunks, two look-back warps, one CTA per SM
 constexpr long long kSegBwdManyGroups = 64;
 
 // Short sequences with too few lane groups for a walk: the whole sequence of
@@ -836,9 +850,9 @@ int pick_variant(bool bwd, int64_t B, int64_t S, int64_t HJ, int sms, Mode mode)
     if (sv >= 0) return sv;
     if (bwd) {
         const long long units4 = groups * ((S + 4 * 64 - 1) / (4 * 64));   // segments of 4 chunks
-        const int seg = (groups >= kSegBwdManyGroups || units4 < 4ll * sms) ? kSegBwdShort : kSegBwd;
-        if (mode == Mode::FROM_CARRIES || groups >= kSegBwdManyGroups) return seg;
-        return kThreeBwd;
+        if (groups >= kSegBwdManyGroups) return kSegBwdShort;
+        if (units4 >= 4ll * sms) return kSegBwdLag;
+        return mode == Mode::FROM_CARRIES ? kSegBwdShort : kThreeBwd;
     }
     return groups <= kSegFwdFewGroups ? kSegFwdFew : kSegFwd;
 }

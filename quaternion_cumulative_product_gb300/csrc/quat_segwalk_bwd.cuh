@@ -67,8 +67,11 @@ namespace qs {
 // otherwise right to left, starting with the chunk walk 1 read last.
 // NLB: look-back warps (1 or 2); with two, unit k goes to look-back warp
 // k % 2, so that one unit's look-back overlaps the previous one's.
+// DL: walk 2 of unit k follows walk 1 of unit k + DL (items W1(u_k),
+// W2(u_{k-DL})), so a unit's look-back has DL first walks (and DL - 1 second
+// walks) of later units to finish in; DL + 1 unit slots of the tables.
 template <typename IO, int LT, int NSEG, int N, int NST, int K, int MINB = 1, int LB = 4, bool W2FWD = false,
-          int NLB = 1>
+          int NLB = 1, int DL = 1>
 __global__ void __launch_bounds__(LT *NSEG + 32 + 32 * NLB, MINB)
     quat_segwalk_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap dmap,
                             const float4 *__restrict__ carries, typename IO::elem *__restrict__ d_q,
@@ -83,28 +86,30 @@ __global__ void __launch_bounds__(LT *NSEG + 32 + 32 * NLB, MINB)
     static_assert(NT % 32 == 0 && LT <= 32, "compute threads are whole warps; one look-back thread per lane");
     constexpr uint32_t BQ = T * LT * IO::bytes;   // one operand of one chunk
     constexpr int TAB = K * NSEG * LT;            // entries of one unit's table
-    constexpr int NU = 16;          // unit slots (the producer is at most NST items = NST units ahead)
-    static_assert(NST + 3 <= NU, "unit slots");
-    static_assert(NST <= 3, "walk 1 of unit k + 2 ends at least 3 items after that of unit k");
+    constexpr int NSL = DL + 1;     // unit slots of the tables and of agg_ready / carry_ready
+    constexpr int NU = 16;          // ticket slots (the producer is at most NST items = NST units ahead)
+    static_assert(DL >= 1 && DL <= 3, "walk 2 lags walk 1 by one to three units");
+    static_assert(NST + DL + 2 <= NU, "ticket slots: unit k - DL's is still held when unit k + NST's is written");
+    static_assert(NST <= 3, "walk 1 of unit k + NSL ends at least 3 items after that of unit k");
     extern __shared__ unsigned char smem_raw[];
     unsigned char *ring = align128(smem_raw);
-    // Per unit (slot k & 1), entry (chunk j, segment, lane): walk 1 writes the
+    // Per unit (slot k % NSL), entry (chunk j, segment, lane): walk 1 writes the
     // segment's product into tab_a and its weighted sum into tab_w; the
     // look-back warp replaces them by the cum just before the segment (tab_a)
     // and the H entering it from the right (tab_w), which walk 2 reads.  An
     // entry is written and read by the same compute thread.
     float4 *tab_a = reinterpret_cast<float4 *>(ring + NST * 2 * BQ);
-    float4 *tab_w = tab_a + 2 * TAB;
+    float4 *tab_w = tab_a + NSL * TAB;
     __shared__ __align__(8) uint64_t full[NST], empty[NST];
-    __shared__ __align__(8) uint64_t agg_ready[2], carry_ready[2];
+    __shared__ __align__(8) uint64_t agg_ready[NSL], carry_ready[NSL];
     __shared__ int issued[NST];
     __shared__ int s_broken;
     __shared__ int s_unit[NU];      // producer -> compute: ticket of the CTA's k-th unit (slot k % NU), -1: end
-    __shared__ int s_lbu[2];        // compute -> look-back: ticket of unit k (slot k & 1), -1: end
+    __shared__ int s_lbu[NSL];      // compute -> look-back: ticket of unit k (slot k % NSL), -1: end
     // Look-back warp: the carries entering unit k's chunks, copied into shared
     // memory while the look-back runs (K > 2), or held in registers.
     constexpr bool kFsmem = K > 2;
-    __shared__ __align__(16) float4 s_F[kFsmem ? 2 : 1][kFsmem ? K : 1][LT];
+    __shared__ __align__(16) float4 s_F[kFsmem ? NSL : 1][kFsmem ? K : 1][LT];
 
     const int tid = static_cast<int>(threadIdx.x);
     const int NG = geo.NG, C = geo.C;
@@ -117,7 +122,7 @@ __global__ void __launch_bounds__(LT *NSEG + 32 + 32 * NLB, MINB)
             mbar_init(&empty[s], NW);
             issued[s] = 0;
         }
-        for (int s = 0; s < 2; ++s) {
+        for (int s = 0; s < NSL; ++s) {
             mbar_init(&agg_ready[s], NW);
             mbar_init(&carry_ready[s], 1);
         }
@@ -135,16 +140,17 @@ __global__ void __launch_bounds__(LT *NSEG + 32 + 32 * NLB, MINB)
         const int lane = wl % LT;
         const bool own = wl < LT;
         for (int k = lbw;; k += NLB) {
-            if (!ws_wait(&agg_ready[k & 1], (k >> 1) & 1, ctl, -1, &s_broken)) break;
-            const int t = s_lbu[k & 1];
+            const int sl = k % NSL;
+            if (!ws_wait(&agg_ready[sl], (k / NSL) & 1, ctl, -1, &s_broken)) break;
+            const int t = s_lbu[sl];
             if (t < 0) break;
             const int p = t / NG, g = t - p * NG;
             const int b = g / geo.NGb;
             const int hj = (g - b * geo.NGb) * LT + lane;
             const int c_hi = C - p * K, c_lo = max(0, c_hi - K), n = c_hi - c_lo;
             if (own) {
-                float4 *ta = tab_a + (k & 1) * TAB + lane, *tw = tab_w + (k & 1) * TAB + lane;
-                float4 *sF = &s_F[kFsmem ? (k & 1) : 0][0][lane];
+                float4 *ta = tab_a + sl * TAB + lane, *tw = tab_w + sl * TAB + lane;
+                float4 *sF = &s_F[kFsmem ? sl : 0][0][lane];
                 float4 F[kFsmem ? 1 : K];
                 // The carries entering the unit's chunks, fetched while the look-back runs.
 #pragma unroll
@@ -224,7 +230,7 @@ __global__ void __launch_bounds__(LT *NSEG + 32 + 32 * NLB, MINB)
             }
             __syncwarp();
             if (wl == 0) {
-                mbar_arrive(&carry_ready[k & 1]);
+                mbar_arrive(&carry_ready[sl]);
                 atomicAdd(ctr + 2, 1u);   // units done
             }
         }
@@ -258,22 +264,21 @@ __global__ void __launch_bounds__(LT *NSEG + 32 + 32 * NLB, MINB)
                 }
                 return true;
             };
-            int prev = -1;
             bool ok = true;
             for (int k = 0; ok; ++k) {
                 const int t = ld_volatile_int(&s_broken) ? U : static_cast<int>(atomicAdd(ctr, 1u));
-                if (t >= U) {   // end marker where unit k's first load would be
+                if (t >= U) {   // end marker where unit k's first load would be, then the pending second walks
                     if (claim(-1)) {
                         s_unit[k % NU] = -1;
                         mbar_arrive(&full[it % NST]);
                         ++it;
-                        if (prev >= 0) walk(prev, false);
+                        for (int j = max(0, k - DL); j < k && walk(s_unit[j % NU], false); ++j) {
+                        }
                     }
                     break;
                 }
                 s_unit[k % NU] = t;   // read by the compute warps after the wait on this unit's first load
-                ok = walk(t, true) && (prev < 0 || walk(prev, false));
-                prev = t;
+                ok = walk(t, true) && (k < DL || walk(s_unit[(k - DL) % NU], false));
             }
             if (ld_volatile_int(&s_broken)) {   // the loads issued get a bounded time to land
                 for (int st = 0; st < NST; ++st) {
@@ -383,34 +388,31 @@ __global__ void __launch_bounds__(LT *NSEG + 32 + 32 * NLB, MINB)
                 }
             }
         };
-        int prev = -1;
+        // Walk 2 of unit j, once its look-back is done.
+        auto second = [&](int j) {
+            ws_wait(&carry_ready[j % NSL], (j / NSL) & 1, ctl, -1, &s_broken);
+            walk2(ld_volatile_int(&s_unit[j % NU]), j % NSL);
+        };
         for (int k = 0;; ++k) {
             // Unit k: its first load (or the end marker) carries its ticket.
             const bool got = ws_wait(&full[it % NST], (it / NST) & 1, ctl, -1, &s_broken);
             const int t = got ? ld_volatile_int(&s_unit[k % NU]) : -1;
             if (t < 0) {
                 if (got) release();   // the end marker's stage
-                if (prev >= 0) {
-                    ws_wait(&carry_ready[(k - 1) & 1], ((k - 1) >> 1) & 1, ctl, -1, &s_broken);
-                    walk2(prev, (k - 1) & 1);
-                }
+                for (int j = max(0, k - DL); j < k; ++j) second(j);
                 __syncwarp();
-                if (lead) {   // the look-back warp(s) end too (unit k - 1 is done: its slot is free)
-                    if (tid == 0) s_lbu[k & 1] = -1;
-                    mbar_arrive(&agg_ready[k & 1]);
+                if (lead) {   // the look-back warp(s) end too (every unit is done: the slots are free)
+                    if (tid == 0) s_lbu[k % NSL] = -1;
+                    mbar_arrive(&agg_ready[k % NSL]);
                     if (NLB == 2) {
-                        if (tid == 0) s_lbu[(k + 1) & 1] = -1;
-                        mbar_arrive(&agg_ready[(k + 1) & 1]);
+                        if (tid == 0) s_lbu[(k + 1) % NSL] = -1;
+                        mbar_arrive(&agg_ready[(k + 1) % NSL]);
                     }
                 }
                 break;
             }
-            walk1(t, k & 1);
-            if (prev >= 0) {
-                ws_wait(&carry_ready[(k - 1) & 1], ((k - 1) >> 1) & 1, ctl, -1, &s_broken);
-                walk2(prev, (k - 1) & 1);
-            }
-            prev = t;
+            walk1(t, k % NSL);
+            if (k >= DL) second(k - DL);
         }
     }
     __syncthreads();
@@ -683,10 +685,11 @@ __host__ __device__ constexpr size_t carries_pass_smem_bytes(int lt, int nseg, i
     return 128 + size_t(nst) * nseg * n * lt * eb + size_t(2) * k * nseg * lt * 16;
 }
 
-// Dynamic shared memory: the ring (two operands per stage), then the two
-// unit slots of the two tables.
-__host__ __device__ constexpr size_t segwalk_bwd_smem_bytes(int lt, int nseg, int n, int nst, int k, int eb = 16) {
-    return 128 + size_t(nst) * 2 * nseg * n * lt * eb + size_t(4) * k * nseg * lt * 16;
+// Dynamic shared memory: the ring (two operands per stage), then the nsl
+// unit slots of the two tables (nsl = DL + 1).
+__host__ __device__ constexpr size_t segwalk_bwd_smem_bytes(int lt, int nseg, int n, int nst, int k, int eb = 16,
+                                                            int nsl = 2) {
+    return 128 + size_t(nst) * 2 * nseg * n * lt * eb + size_t(2) * nsl * k * nseg * lt * 16;
 }
 
 }  // namespace qs

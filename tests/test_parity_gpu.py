@@ -187,9 +187,9 @@ def test_empty_sizes(dev):
 # two CTAs per SM, more lane groups in waves; backward 11-14: the segmented
 # walk of the backward, after its carries-only forward pass; forward and
 # backward 25-29: short sequences, a lane group's whole sequence in one CTA).
-N_FWD_VARIANTS, N_BWD_VARIANTS = 30, 30
+N_FWD_VARIANTS, N_BWD_VARIANTS = 30, 34
 SEGWALK_FWD = [9, 10, 11, 12, 13, 14, 15, 16, 17, 18, 19, 20, 21, 22, 23, 24]
-SEGWALK_BWD = [11, 12, 13, 14, 15, 16, 17, 18, 19, 20, 21, 22, 23, 24]
+SEGWALK_BWD = [11, 12, 13, 14, 15, 16, 17, 18, 19, 20, 21, 22, 23, 24, 30, 31, 32, 33]
 
 
 @pytest.mark.parametrize("variant", range(max(N_FWD_VARIANTS, N_BWD_VARIANTS)))
@@ -546,7 +546,7 @@ def test_segmented_backward_alternating_layouts(dev):
         assert_parity(d_init.cpu().numpy(), ri, f"d_init (case {k})")
 
 
-@pytest.mark.parametrize("variant", [11, 22])   # one look-back warp, two
+@pytest.mark.parametrize("variant", [11, 22, 31])   # one look-back warp, two; walk 2 two units behind
 @pytest.mark.parametrize("saved", [False, True])
 def test_segmented_backward_stall_reports_timeout_then_recovers(dev, saved, variant):
     """The stall hook holds the first kernel of the call: the carries-only pass
@@ -661,16 +661,20 @@ def test_plan_picks_the_design_by_lane_groups(dev, name, walk):
             assert kernels == 1, (name, bwd, variant, kernels)
             assert variant == ((27 if w.S <= 512 else 26) if bwd else 26), (name, bwd, variant)
             continue
-        # few lane groups: the segmented chained walk forward (one kernel); for
-        # fewer than 64 sixteen-lane groups the aggregate / carry / apply backward
-        assert kernels == (1 if walk or not bwd else 3), (name, bwd, variant, kernels)
+        # few lane groups: the segmented chained walk forward (one kernel); the
+        # backward: on long sequences (at least 4 units of 4 chunks per SM) the
+        # carries pass and the segmented walk with walk 2 two units behind (31)
+        units4 = w.B * ((w.H * w.J + 15) // 16) * ((w.S + 255) // 256)
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        seg = bwd and not walk and units4 >= 4 * sms
+        assert kernels == (1 if walk or not bwd else 2 if seg else 3), (name, bwd, variant, kernels)
         if not walk and not bwd:
             # the segmented walk with per-unit tables, segments of 2 chunks:
             # 32-lane groups (24) when there are at most 32 of them, else 16 (22)
             groups32 = w.B * ((w.H * w.J + 31) // 32)
             assert variant == (24 if groups32 <= 32 else 22), (name, variant)
         if not walk and bwd:
-            assert variant == 0, (name, variant)
+            assert variant == (31 if seg else 0), (name, variant)
     assert qs.quat_cumprod_plan(True, 2, 0, 3, 4, device=dev) == (-1, 0)
 
 
@@ -678,9 +682,10 @@ def test_plan_picks_the_segmented_backward_for_many_groups(dev):
     """64 or more 16-lane groups, too few for a walk: the recompute backward is
     the carries pass and the segmented walk (segments of 2 chunks)."""
     assert qs.quat_cumprod_plan(True, 1, 4096, 32, 32, device=dev) == (24, 2)   # 64 groups
-    assert qs.quat_cumprod_plan(True, 1, 4096, 31, 32, device=dev) == (0, 3)    # 62 groups
+    assert qs.quat_cumprod_plan(True, 1, 4096, 31, 32, device=dev) == (31, 2)   # 62 groups, 992 units
+    assert qs.quat_cumprod_plan(True, 1, 4096, 16, 16, device=dev) == (0, 3)    # 16 groups, 256 units
     # from saved carries: the segmented walk whatever the group count
-    assert qs.quat_cumprod_plan("bwd_carries", 1, 131072, 16, 16, device=dev) == (22, 1)
+    assert qs.quat_cumprod_plan("bwd_carries", 1, 131072, 16, 16, device=dev) == (31, 1)
     assert qs.quat_cumprod_plan("bwd_carries", 4, 4096, 8, 16, device=dev) == (24, 1)   # few units
     assert qs.quat_cumprod_plan("bwd_carries", 4, 1024, 8, 16, device=dev) == (26, 1)   # short sequences
     w = workloads.custom("manygroups", 1, 2100, 32, 33, q_kind="rotation", theta_max=0.4, seed=200)
