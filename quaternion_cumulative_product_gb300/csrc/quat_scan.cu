@@ -320,6 +320,12 @@ const Variant kBwdGiven = Variant{true,
             nullptr, true, LT, NSEG, N, qs::segwalk_bwd_smem_bytes(LT, NSEG, N, NST, K, 8), false, 0, K, 64, true, \
             &kCarriesPassVariantBf16                                                                \
     }
+#define QS_SEGWALK_TAB_FWD16(LT, NSEG, N, NST, K, NLB)                                              \
+    Variant {                                                                                       \
+        false, reinterpret_cast<const void *>(qs::quat_segwalk_tab_fwd_kernel<qs::IoBF16, LT, NSEG, N, NST, K, NLB>), \
+            nullptr, false, LT, NSEG, N, qs::segwalk_tab_smem_bytes(LT, NSEG, N, NST, K, 8), false, 0, K, \
+            32 + 32 * NLB, true, nullptr, true                                                      \
+    }
 #define QS_SEGWALK_SENT_FWD16(LT, NSEG, N, NST, K)                                                  \
     Variant {                                                                                       \
         false, reinterpret_cast<const void *>(qs::quat_segwalk_fwd_kernel<qs::IoBF16, LT, NSEG, N, NST, K, true>), \
@@ -351,6 +357,7 @@ const Variant kFwdBf16Variants[] = {
     QS_SEGWALK_WS_SENT_FWD16(16, 8, 8, 6, 4),   // 7: segmented walk, warp-specialised, 16 lanes
     QS_SHORT_FWD16(2, 128, 8),             // 8: short sequences (S <= 1024), 2 lanes a CTA
     QS_SHORT_FWD16(4, 256, 8),             // 9: S <= 2048, 4 lanes (1024 threads)
+    QS_SEGWALK_TAB_FWD16(32, 8, 8, 3, 2, 2),   // 10: segmented walk with per-unit tables, 32 lanes
 };
 const Variant kBwdBf16Variants[] = {
     QS_WALK_BWD16(16, 8, 8, 8, 4, false),  // 0: 16 lanes x 64 steps (128 threads), 64 KiB rings
@@ -370,19 +377,23 @@ const Variant kBwdBf16Variants[] = {
 #undef QS_SHORT_BWD16
 #undef QS_SEGWALK_FWD16
 #undef QS_SEGWALK_SENT_FWD16
+#undef QS_SEGWALK_TAB_FWD16
 #undef QS_SEGWALK_WS_SENT_FWD16
 #undef QS_SEGWALK_BWD16
 #undef QS_WALK_FWD16
 #undef QS_WALK_BWD16
 #undef QS_WALK_BWD16_MINB
 constexpr int kNumFwdBf16 = sizeof(kFwdBf16Variants) / sizeof(kFwdBf16Variants[0]);
-constexpr int kFwdBf16Default = 1, kBwdBf16Default = 0;   // walks; fastest measured on 8x4096x16x32
-// For too few lane groups (forward: segmented walk).  The bf16 forward keeps
-// status words (5): with half the bytes its time is the walk's own latency, and
-// the self-describing look-back values (6) measured 1.5-2.4% slower on
-// 1 x 131072 x 16 x 16, 2 x 65536 x 32 x 32 and 2 x 32768 x 16 x 16 (18%
-// faster on 4 x 8192 x 8 x 16).
-constexpr int kFwdBf16Few = 5, kBwdBf16Few = 4;
+constexpr int kFwdBf16Default = 1, kBwdBf16Default = 0;   // walks
+// The bf16 forward walk only from three lane groups of 16 per SM: with half
+// the bytes a walk's time is its own latency, which only many CTAs per SM hide
+// (16 x 8192 x 32 x 32, 1024 groups: walk 0.86 of the copy bandwidth at 16
+// bytes per element, against 0.72).  With fewer, the segmented walk with
+// per-unit tables and 32-lane groups (8 x 4096 x 16 x 32: 0.61 against the
+// walk's 0.53; 1 x 131072 x 16 x 16: 0.61 against 0.49 for the segmented walk
+// with status words; 2 x 65536 x 32 x 32: 0.71 against 0.56).
+constexpr int kFwdBf16Few = 10, kBwdBf16Few = 4;
+constexpr int kFwdBf16WalkGroupsPerSm = 3;
 constexpr int kFwdBf16Three = 4;   // the aggregate / carry / apply forward
 constexpr int kBwdBf16Three = 4;   // the aggregate / carry / apply backward
 // The bf16 backward walk with more lane groups than two CTAs per SM hold: its
@@ -881,7 +892,7 @@ int make_plan(bool bwd, int64_t B, int64_t S, int64_t HJ, int sms, Plan *pl, Mod
             const int wi = bwd ? kBwdBf16Default : kFwdBf16Default;
             const Variant &w = bwd ? kBwdBf16Variants[wi] : kFwdBf16Variants[wi];
             const long long groups = (long long)B * ((HJ + w.lt - 1) / w.lt);
-            const long long need = bwd ? 3ll * sms / 2 : 3ll * sms / 4;
+            const long long need = bwd ? 3ll * sms / 2 : (long long)kFwdBf16WalkGroupsPerSm * sms;
             vi = groups >= need ? wi : (bwd ? kBwdBf16Few : kFwdBf16Few);
             if (groups < need && short_variant(bwd, S, true) >= 0) vi = short_variant(bwd, S, true);
             if (bwd && groups > 2ll * sms) vi = kBwdBf16Many;

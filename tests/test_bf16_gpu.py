@@ -59,8 +59,9 @@ def bf16_inputs(dev, w):
 # registers capped for three CTAs per SM, 6 and 7 the segmented walk after its
 # carries pass (segments of 4 and 2 chunks); forward 8, 9 and backward 8-10
 # short sequences (the whole sequence of a few lanes in one CTA, up to 1024,
-# 2048 / 1024, 512, 2048 steps).
-N_BF16_FWD, N_BF16_BWD = 10, 11
+# 2048 / 1024, 512, 2048 steps); forward 10 the segmented walk with per-unit
+# tables (32 lanes).
+N_BF16_FWD, N_BF16_BWD = 11, 11
 
 
 @pytest.fixture(autouse=True)
@@ -122,17 +123,22 @@ def test_bf16_rounding_is_the_only_difference_from_fp32(dev):
 
 @pytest.mark.parametrize("name,walk", [("mamba3", True), ("large", True), ("long", False), ("small", False)])
 def test_bf16_plan_picks_the_design_by_lane_groups(dev, name, walk):
-    """Walks for many lane groups; else, for short sequences, the whole sequence
-    of a few lanes in one CTA; else the segmented walk forward, three kernels backward."""
+    """Walks for many lane groups (the forward only from three 16-lane groups per
+    SM: large, not mamba3); else, for short sequences, the whole sequence of a
+    few lanes in one CTA; else the segmented walk with per-unit tables forward
+    (10), three kernels backward."""
     w = workloads.WORKLOADS[name]
-    assert qs.quat_cumprod_plan("fwd_bf16", w.B, w.S, w.H, w.J, device=dev)[1] == 1
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    fvariant, fkernels = qs.quat_cumprod_plan("fwd_bf16", w.B, w.S, w.H, w.J, device=dev)
+    assert fkernels == 1
+    fwalk = w.B * ((w.H * w.J + 15) // 16) >= 3 * sms
+    assert fvariant == (1 if fwalk else 8 if w.S <= 1024 else 9 if w.S <= 2048 else 10), (name, fvariant)
     variant, kernels = qs.quat_cumprod_plan("bwd_bf16", w.B, w.S, w.H, w.J, device=dev)
     assert kernels == (1 if walk or w.S <= 2048 else 3)
     if not walk and w.S <= 2048:
         assert variant == (9 if w.S <= 512 else 8 if w.S <= 1024 else 10), (name, variant)
     if walk:   # more lane groups than two CTAs per SM hold: the register-capped walk (5)
         groups = w.B * ((w.H * w.J + 15) // 16)
-        sms = torch.cuda.get_device_properties(dev).multi_processor_count
         assert variant == (5 if groups > 2 * sms else 0), (name, variant, groups)
 
 
