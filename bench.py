@@ -62,11 +62,11 @@ SEGWALK_FWD_VARIANTS = (9, 10, 11, 12, 13, 14, 15, 16, 17, 18, 19, 20, 21, 22, 2
 # Backward configurations of the segmented walk (after its carries-only pass
 # when the carries are recomputed).
 SEGWALK_BWD_VARIANTS = tuple(range(11, 25)) + (30, 31, 32, 33)
-SHORT_VARIANTS = tuple(range(25, 30))   # forward and backward
+SHORT_FWD_VARIANTS = SHORT_BWD_VARIANTS = (25, 26, 27, 28, 29)
 
 
 def design_name(call: str, kernels: int, variant: int = -1) -> str:
-    if variant in SHORT_VARIANTS:
+    if variant in (SHORT_BWD_VARIANTS if call.startswith("quat_cumprod_bwd") else SHORT_FWD_VARIANTS):
         return f"{call} (short-sequence kernel: the whole sequence of a few lanes in one CTA)"
     if call == "quat_cumprod_fwd" and variant in SEGWALK_FWD_VARIANTS:
         return f"{call} (segmented chained walk kernel)"

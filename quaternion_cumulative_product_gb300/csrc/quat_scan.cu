@@ -831,8 +831,10 @@ constexpr long long kSegBwdManyGroups = 64;
 //   4 x 1024 x 8 x 16: forward 10.9 us against 15.0 (segmented walk),
 //                      backward 12.9 us against 23.2 (three kernels);
 //   2 x 2048 x 16 x 16: forward 12.9 against 17.0, backward 23.2 against 31.4;
-//   4 x 512 x 16 x 16: backward 12.9 (8 lanes, S <= 512) against 17.0 (2 lanes)
-//                      and 31.4 (segmented walk).
+//   4 x 512 x 16 x 16: backward 12.9 (8 lanes, S <= 512) against 17.0 (2 or 4
+//                      lanes) and 31.4 (segmented walk).
+// (4 steps a thread instead of 8, with twice the segments: slower, 19.1 us
+// against 13.0 for the backward of 4 x 1024 x 8 x 16.)
 // Returns the configuration in the fp32 or bf16 table, or -1 past 2048 steps.
 int short_variant(bool bwd, int64_t S, bool bf16) {
     if (S > 2048) return -1;
@@ -840,7 +842,7 @@ int short_variant(bool bwd, int64_t S, bool bf16) {
         if (bwd) return S <= 512 ? 9 : S <= 1024 ? 8 : 10;
         return S <= 1024 ? 8 : 9;
     }
-    if (bwd) return S <= 512 ? 27 : S <= 1024 ? 26 : 28;
+    if (bwd) return S <= 512 ? 27 : S <= 1024 ? 25 : 28;
     return S <= 1024 ? 26 : 28;
 }
 

@@ -144,7 +144,7 @@ def test_segmented_walks_write_and_read_carries(dev, fv, bv, dims):
 
 # The short-sequence kernels write the carries (forward) and start from
 # carries[:, 0] (backward, which recomputes the rest).
-@pytest.mark.parametrize("fv,bv", [(25, 25), (26, 26), (27, 27), (28, 28)])
+@pytest.mark.parametrize("fv,bv", [(25, 25), (26, 26), (27, 27), (28, 28), (26, 25)])
 @pytest.mark.parametrize("dims", [(2, 333, 3, 16), (1, 63, 1, 1), (3, 64, 1, 5), (1, 500, 2, 3)])
 def test_short_sequences_write_and_read_carries(dev, fv, bv, dims):
     lib = qs.load_library()

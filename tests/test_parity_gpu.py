@@ -186,7 +186,9 @@ def test_empty_sizes(dev):
 # in one round trip; 13, 14: as 10, 11 with those values; backward 10: at most
 # two CTAs per SM, more lane groups in waves; backward 11-14: the segmented
 # walk of the backward, after its carries-only forward pass; forward and
-# backward 25-29: short sequences, a lane group's whole sequence in one CTA).
+# backward 25-29: short sequences, a lane group's whole sequence in one CTA;
+# backward 30-33: the segmented walk of the backward with walk 2 two or three
+# units behind).
 N_FWD_VARIANTS, N_BWD_VARIANTS = 30, 34
 SEGWALK_FWD = [9, 10, 11, 12, 13, 14, 15, 16, 17, 18, 19, 20, 21, 22, 23, 24]
 SEGWALK_BWD = [11, 12, 13, 14, 15, 16, 17, 18, 19, 20, 21, 22, 23, 24, 30, 31, 32, 33]
@@ -450,37 +452,37 @@ def test_binding_rejects_bad_tensors(dev):
     assert ei.value.status == qs.QS_ERR_ALIAS
 
 
-# Short-sequence configurations: (lanes a CTA, longest sequence).
-SHORT = {25: (4, 1024, 4, 1024), 26: (2, 1024, 2, 1024), 27: (8, 1024, 8, 512), 28: (4, 2048, 2, 2048),
-         29: (16, 256, 16, 256)}   # variant: (forward lanes, forward S max, backward lanes, backward S max)
+# Short-sequence configurations: variant -> longest sequence.
+SHORT_FWD = {25: 1024, 26: 1024, 27: 1024, 28: 2048, 29: 256}
+SHORT_BWD = {25: 1024, 26: 1024, 27: 512, 28: 2048, 29: 256}
+SHORT_PAIRS = [(25, 25), (26, 26), (27, 27), (28, 28), (29, 29), (26, 25)]
 
 
-@pytest.mark.parametrize("variant", sorted(SHORT))
+@pytest.mark.parametrize("fv,bv", SHORT_PAIRS)
 @pytest.mark.parametrize("at", ["one", "chunk-1", "chunk", "chunk+1", "max-1", "max"])
-def test_short_sequences(dev, variant, at):
+def test_short_sequences(dev, fv, bv, at):
     """A lane group's whole sequence in one CTA: lengths from one step to the
     configuration's longest (one chunk of the carries and one step either side),
     lane groups ragged on both sides (H*J = 3 x 7 is no multiple of the lanes)."""
     lib = qs.load_library()
-    flt, fmax, blt, bmax = SHORT[variant]
-    smax = min(fmax, bmax)
+    smax = min(SHORT_FWD[fv], SHORT_BWD[bv])
     S = {"one": 1, "chunk-1": 63, "chunk": 64, "chunk+1": 65, "max-1": smax - 1, "max": smax}[at]
-    assert lib.quat_cumprod_debug_set_variant(variant, variant) == qs.QS_OK
-    assert qs.quat_cumprod_plan("fwd", 2, S, 3, 7, device=dev) == (variant, 1)
-    assert qs.quat_cumprod_plan("bwd", 2, S, 3, 7, device=dev) == (variant, 1)
-    w = workloads.custom("short", 2, S, 3, 7, q_kind="gauss4", seed=variant * 8 + len(at))
+    assert lib.quat_cumprod_debug_set_variant(fv, bv) == qs.QS_OK
+    assert qs.quat_cumprod_plan("fwd", 2, S, 3, 7, device=dev) == (fv, 1)
+    assert qs.quat_cumprod_plan("bwd", 2, S, 3, 7, device=dev) == (bv, 1)
+    w = workloads.custom("short", 2, S, 3, 7, q_kind="gauss4", seed=fv * 8 + len(at))
     check_against_oracle(dev, *workloads.make_inputs(w))
 
 
-@pytest.mark.parametrize("variant", [25, 28])
-def test_short_sequences_past_their_length_take_another_design(dev, variant):
+@pytest.mark.parametrize("fv,bv", [(25, 25), (28, 28)])
+def test_short_sequences_past_their_length_take_another_design(dev, fv, bv):
     """A short-sequence configuration asked for a longer sequence is not used."""
     lib = qs.load_library()
-    _, fmax, _, bmax = SHORT[variant]
-    assert lib.quat_cumprod_debug_set_variant(variant, variant) == qs.QS_OK
-    assert qs.quat_cumprod_plan("fwd", 1, fmax + 1, 2, 4, device=dev)[0] != variant
-    assert qs.quat_cumprod_plan("bwd", 1, bmax + 1, 2, 4, device=dev)[0] != variant
-    w = workloads.custom("short-past", 1, bmax + 1, 2, 4, q_kind="rotation", theta_max=0.5, seed=variant)
+    fmax, bmax = SHORT_FWD[fv], SHORT_BWD[bv]
+    assert lib.quat_cumprod_debug_set_variant(fv, bv) == qs.QS_OK
+    assert qs.quat_cumprod_plan("fwd", 1, fmax + 1, 2, 4, device=dev)[0] != fv
+    assert qs.quat_cumprod_plan("bwd", 1, bmax + 1, 2, 4, device=dev)[0] != bv
+    w = workloads.custom("short-past", 1, bmax + 1, 2, 4, q_kind="rotation", theta_max=0.5, seed=fv)
     check_against_oracle(dev, *workloads.make_inputs(w))
 
 
@@ -659,7 +661,7 @@ def test_plan_picks_the_design_by_lane_groups(dev, name, walk):
             # short sequences: the whole sequence of a few lanes in one CTA,
             # the configuration that fits S (backward: 8 lanes up to 512 steps)
             assert kernels == 1, (name, bwd, variant, kernels)
-            assert variant == ((27 if w.S <= 512 else 26) if bwd else 26), (name, bwd, variant)
+            assert variant == ((27 if w.S <= 512 else 25) if bwd else 26), (name, bwd, variant)
             continue
         # few lane groups: the segmented chained walk forward (one kernel); the
         # backward: on long sequences (at least 4 units of 4 chunks per SM) the
@@ -687,7 +689,7 @@ def test_plan_picks_the_segmented_backward_for_many_groups(dev):
     # from saved carries: the segmented walk whatever the group count
     assert qs.quat_cumprod_plan("bwd_carries", 1, 131072, 16, 16, device=dev) == (31, 1)
     assert qs.quat_cumprod_plan("bwd_carries", 4, 4096, 8, 16, device=dev) == (24, 1)   # few units
-    assert qs.quat_cumprod_plan("bwd_carries", 4, 1024, 8, 16, device=dev) == (26, 1)   # short sequences
+    assert qs.quat_cumprod_plan("bwd_carries", 4, 1024, 8, 16, device=dev) == (25, 1)   # short sequences
     w = workloads.custom("manygroups", 1, 2100, 32, 33, q_kind="rotation", theta_max=0.4, seed=200)
     assert qs.quat_cumprod_plan(True, w.B, w.S, w.H, w.J, device=dev) == (24, 2)
     check_against_oracle(dev, *workloads.make_inputs(w))
