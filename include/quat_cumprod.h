@@ -38,21 +38,23 @@
  *
  * Scratch memory: the calls use a library-owned workspace per (device,
  * stream) for a status block and per-chunk aggregates and carries.  Per lane
- * and 64-step chunk this is nothing for a forward walk, 16 bytes for a
- * backward walk or the backward's segmented walk, and 32 (forward) or 64
- * (backward) bytes for the aggregate / carry / apply kernels (see
- * quat_cumprod_plan for which a call uses).  The segmented chained walks (for
- * few lane groups) keep, per lane and segment of 2 or 4 chunks, two copies of
- * 32 (forward) or 48 (backward) bytes of look-back values plus a few counters
- * in further per-stream allocations, and reserve the aggregate / carry /
- * apply workspace of the same direction as well.  The first call on a stream,
- * and any later call that needs more scratch, allocates it (cudaMalloc) and
- * synchronizes that stream; issue such a call before capturing the stream
- * into a CUDA graph.  While a stream is being captured the forward uses the
- * aggregate / carry / apply kernels, which keep no state from one launch to
- * the next (the segmented walk's look-back values are tied to the launch
- * that reads them), so a captured graph may be replayed any number of
- * times.  Calls on one stream are ordered by the stream; calls on different
+ * and 64-step chunk this is nothing for a forward walk or the short-sequence
+ * kernels (at most 2048 steps, the whole sequence of a few lanes in one CTA),
+ * 16 bytes for a backward walk or the backward's segmented walk, and 32
+ * (forward) or 64 (backward) bytes for the aggregate / carry / apply kernels
+ * (see quat_cumprod_plan for which a call uses).  The segmented chained walks
+ * (for few lane groups) keep, per lane and segment of 2 to 8 chunks, two copies
+ * of 32 (forward) or 48 (backward) bytes of look-back values plus a few
+ * counters in further per-stream allocations, and reserve the aggregate /
+ * carry / apply workspace of the same direction as well.  The first call on a
+ * stream, and any later call that needs more scratch, allocates it
+ * (cudaMalloc) and synchronizes that stream; issue such a call before
+ * capturing the stream into a CUDA graph.  While a stream is being captured
+ * the segmented walks give way to the aggregate / carry / apply kernels,
+ * which keep no state from one launch to the next (the segmented walks'
+ * look-back values are tied to the launch that reads them), so a captured
+ * graph may be replayed any number of times; the walks and the
+ * short-sequence kernels keep no state either.  Calls on one stream are ordered by the stream; calls on different
  * streams use different workspaces and may run concurrently.  A workspace is
  * found by the stream's handle: before destroying a stream, let its work
  * finish, so that a new stream given the same handle cannot meet a launch
@@ -192,6 +194,7 @@ int quat_cumprod_fwd_carries(const float *q, const float *init, float *cum, floa
  * q and init: writes d_q and d_init as quat_cumprod_bwd(q, carries[:, 0],
  * d_cum) would, reading q and d_cum once (the walk, or for too few lane
  * groups the segmented walk, takes every chunk's carry from `carries`; the
+ * short-sequence kernels, which hold the whole sequence anyway, and the
  * aggregate / carry / apply kernels, which a debug setting can force, use
  * them only as init).  Arguments, layout and errors otherwise as
  * quat_cumprod_bwd.
@@ -210,7 +213,8 @@ int quat_cumprod_bwd_carries(const float *q, const float *carries, const float *
  * half a bfloat16 ulp (2^-8 of its magnitude) plus the fp32 error of the fp32
  * calls.  Requires
  * H*J even (TMA row strides are multiples of 16 bytes; QS_ERR_DIMS
- * otherwise); pointers 16-byte aligned.  Uses the walk kernels for every size.
+ * otherwise); pointers 16-byte aligned.  The designs follow the fp32 calls'
+ * choice by size (quat_cumprod_plan, calls 4 and 5).
  * The pages define the scan in full precision; this halves the bytes moved
  * (8 bytes per quaternion instead of 16).
  */
@@ -255,11 +259,12 @@ int quat_cumprod_status(void *stream);
 /*
  * Which compiled configuration a call with these sizes would use on the
  * current device, and how many kernels it launches: 1 for a walk (one CTA
- * per lane group streams the whole sequence) or a segmented walk (too few
- * lane groups: the sequence cut into segments chained by look-back), 2 for
- * the backward's segmented walk after its carries-only pass, 3 for
- * aggregate / carry / apply (independent tiles), plus 1 when the forward
- * exports its carries from that path.  `call`: 0 quat_cumprod_fwd, 1 quat_cumprod_bwd,
+ * per lane group streams the whole sequence), a segmented walk (too few
+ * lane groups: the sequence cut into segments chained by look-back) or the
+ * short-sequence kernels (at most 2048 steps: the whole sequence of a few
+ * lanes in one CTA), 2 for the backward's segmented walk after its
+ * carries-only pass, 3 for aggregate / carry / apply (independent tiles),
+ * plus 1 when the forward exports its carries from that path.  `call`: 0 quat_cumprod_fwd, 1 quat_cumprod_bwd,
  * 2 quat_cumprod_fwd_carries, 3 quat_cumprod_bwd_carries, 4 quat_cumprod_fwd_bf16,
  * 5 quat_cumprod_bwd_bf16.  Writes
  * *variant = -1 and *kernels = 0 when the call would launch nothing.  Returns
