@@ -22,16 +22,16 @@ namespace qs {
 // LT adjacent lanes: every load and store of a step is LT * 16 contiguous
 // bytes per segment.
 //
-// The scan across segments runs on threads (l2, s2) = (tid / NS, tid % NS):
-// a warp holds 32 consecutive segments of one lane and scans them with
-// shuffles; the warp totals (NS / 32 per lane) are folded serially.  The
-// per-lane tables are padded by one entry so that both thread layouts read
-// and write them without bank conflicts.
+// The scan across segments runs on one warp per lane (warps 0 .. LT - 1):
+// thread j of lane l2's warp composes segments [j * SPT, (j + 1) * SPT),
+// SPT = NS / 32, serially, the 32 compositions are scanned with five shuffle
+// rounds, and the thread writes the prefix entering each of its segments back
+// into the table.  The other warps wait at the block barrier.
 // ---------------------------------------------------------------------------
 template <int LT, int NS>
 struct ShortShape {
-    static constexpr int NT = LT * NS;   // threads
-    static constexpr int NWL = NS / 32;  // scan warps per lane
+    static constexpr int NT = LT * NS;    // threads
+    static constexpr int SPT = NS / 32;   // segments a scan thread composes
     static_assert(NS % 32 == 0 && NT % 32 == 0 && NT <= 1024, "segments per lane: whole warps; at most 1024 threads");
 };
 
@@ -64,7 +64,6 @@ __global__ void __launch_bounds__(ShortShape<LT, NS>::NT)
     using SH = ShortShape<LT, NS>;
     static_assert(QS_CARRY_STEPS % R == 0, "a chunk of the carries is whole segments");
     __shared__ float4 tab[LT][NS + 1];
-    __shared__ float4 wtot[LT][SH::NWL];
     const int tid = static_cast<int>(threadIdx.x);
     const int g = static_cast<int>(blockIdx.x), b = g / geo.NGb;
     const int hj0 = (g - b * geo.NGb) * LT;
@@ -89,20 +88,27 @@ __global__ void __launch_bounds__(ShortShape<LT, NS>::NT)
 
     // Scan across the segments of each lane: tab[l][s] becomes the cum just
     // before segment s.
-    {
-        const int l2 = tid / NS, s2 = tid % NS, wl = tid & 31, w2 = s2 / 32;
-        float4 a = tab[l2][s2];
+    if (tid < LT * 32) {
+        constexpr int SPT = SH::SPT;
+        const int l2 = tid >> 5, j = tid & 31;
+        float4 *row = &tab[l2][j * SPT];
+        float4 a = row[0];   // the thread's segments, composed
 #pragma unroll
-        for (int d = 1; d < 32; d <<= 1) {   // a = A[s2] (x) ... (x) A[first segment of the warp]
+        for (int i = 1; i < SPT; ++i) a = q_mul(row[i], a);
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {   // a = composition of threads 0 .. j
             const float4 y = shfl_up4(a, d);
-            if (wl >= d) a = q_mul(a, y);
+            if (j >= d) a = q_mul(a, y);
         }
-        if (wl == 31) wtot[l2][w2] = a;
-        __syncthreads();
-        float4 X = hj0 + l2 < HJ ? short_init<IO>(init, init_stride, init_f32 != 0, b, hj0 + l2) : q_ident();
-        for (int w = 0; w < w2; ++w) X = q_mul(wtot[l2][w], X);   // the cum entering the warp's segments
         const float4 e = shfl_up4(a, 1);
-        tab[l2][s2] = wl == 0 ? X : q_mul(e, X);
+        float4 X = hj0 + l2 < HJ ? short_init<IO>(init, init_stride, init_f32 != 0, b, hj0 + l2) : q_ident();
+        if (j > 0) X = q_mul(e, X);   // the cum entering the thread's first segment
+#pragma unroll
+        for (int i = 0; i < SPT; ++i) {
+            const float4 ai = row[i];
+            row[i] = X;
+            X = q_mul(ai, X);
+        }
     }
     __syncthreads();
 
@@ -133,7 +139,6 @@ __global__ void __launch_bounds__(ShortShape<LT, NS>::NT)
     using E = typename IO::elem;
     using SH = ShortShape<LT, NS>;
     __shared__ float4 tabA[LT][NS + 1], tabV[LT][NS + 1];
-    __shared__ float4 wA[LT][SH::NWL], wV[LT][SH::NWL], wM[LT][SH::NWL];
     const int tid = static_cast<int>(threadIdx.x);
     const int g = static_cast<int>(blockIdx.x), b = g / geo.NGb;
     const int hj0 = (g - b * geo.NGb) * LT;
@@ -167,38 +172,51 @@ __global__ void __launch_bounds__(ShortShape<LT, NS>::NT)
 
     // Scans across the segments of each lane: tabA[l][s] becomes the cum just
     // before segment s, tabV[l][s] the H entering its last step from the right.
-    {
-        const int l2 = tid / NS, s2 = tid % NS, wl = tid & 31, w2 = s2 / 32;
-        float4 a = tabA[l2][s2], v = tabV[l2][s2], m = q_conj(a);
+    if (tid < LT * 32) {
+        constexpr int SPT = SH::SPT;
+        const int l2 = tid >> 5, j = tid & 31;
+        float4 *rowA = &tabA[l2][j * SPT], *rowV = &tabV[l2][j * SPT];
+        // The thread's segments composed: product a, and map (v, m) from the H
+        // entering the last one to the H leaving the first (m = conj(a)).
+        float4 a = rowA[0], v = rowV[0], m = q_conj(a);
+#pragma unroll
+        for (int i = 1; i < SPT; ++i) {
+            const float4 ai = rowA[i];
+            a = q_mul(ai, a);
+            v = q_fma(v, m, rowV[i]);
+            m = q_mul(m, q_conj(ai));
+        }
 #pragma unroll
         for (int d = 1; d < 32; d <<= 1) {
             const float4 y = shfl_up4(a, d);
-            if (wl >= d) a = q_mul(a, y);
-            // (v, m) = map of segments [s2, s2 + 2d) of the warp: this segment's
-            // part, then the part d segments to the right.
+            if (j >= d) a = q_mul(a, y);   // threads 0 .. j
+            // (v, m) = map of threads [j, j + 2d): this thread's part, then
+            // the part d threads to the right.
             const float4 vr = shfl_down4(v, d), mr = shfl_down4(m, d);
-            if (wl + d < 32) {
+            if (j + d < 32) {
                 v = q_fma(v, m, vr);
                 m = q_mul(m, mr);
             }
         }
-        if (wl == 31) wA[l2][w2] = a;
-        if (wl == 0) {
-            wV[l2][w2] = v;
-            wM[l2][w2] = m;
-        }
-        __syncthreads();
+        const float4 e = shfl_up4(a, 1), vn = shfl_down4(v, 1);
         const bool own = hj0 + l2 < HJ;
         float4 X = own ? short_init<IO>(init, init_stride, init_f32 != 0, b, hj0 + l2) : q_ident();
-        for (int w = 0; w < w2; ++w) X = q_mul(wA[l2][w], X);   // the cum entering the warp's segments
-        float4 H = q_zero();                                       // H entering the warp's last segment
-        for (int w = SH::NWL - 1; w > w2; --w) H = q_fma(wV[l2][w], wM[l2][w], H);
-        const float4 e = shfl_up4(a, 1);
-        const float4 vr = shfl_down4(v, 1), mr = shfl_down4(m, 1);
-        tabA[l2][s2] = wl == 0 ? X : q_mul(e, X);
-        tabV[l2][s2] = wl == 31 ? H : q_fma(vr, mr, H);
-        if (s2 == 0 && own)   // H leaving the first step to the left
-            d_init[static_cast<long long>(b) * HJ + hj0 + l2] = IO::put(q_fma(v, m, H));
+        if (j > 0) X = q_mul(e, X);             // the cum entering the thread's first segment
+        float4 H = j < 31 ? vn : q_zero();      // the H entering its last segment: the maps to its right applied to nothing
+#pragma unroll
+        for (int i = SPT - 1; i >= 0; --i) {   // (reads each segment's product before it is replaced)
+            const float4 vi = rowV[i];
+            rowV[i] = H;
+            H = q_fma(vi, q_conj(rowA[i]), H);
+        }
+#pragma unroll
+        for (int i = 0; i < SPT; ++i) {
+            const float4 ai = rowA[i];
+            rowA[i] = X;
+            X = q_mul(ai, X);
+        }
+        if (j == 0 && own)   // H leaving the first step to the left
+            d_init[static_cast<long long>(b) * HJ + hj0 + l2] = IO::put(H);
     }
     __syncthreads();
 
