@@ -49,6 +49,9 @@ L2_BYTES = 126 * (1 << 20)
 LEAD_SPIN_CYCLES = 600_000
 FALLBACK_HBM_GBS = 6800.0
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+TRAFFIC_NOTE = ("dram__bytes_read.sum + dram__bytes_write.sum of one launch of the call's kernels, each captured "
+                "alone by ncu (profiles/dram_traffic.txt, null unless the kernel sources hash to the captured "
+                "source); inside the step the backward also writes back the lines the forward left dirty in L2")
 KERNEL_SOURCES = [os.path.join(ROOT, "quaternion_cumulative_product_gb300", "csrc", f)
                   for f in ("quat_scan.cu", "quat_device.cuh", "quat_common.cuh", "quat_tiles.cuh",
                             "quat_chain.cuh", "quat_walk.cuh", "quat_segwalk.cuh", "quat_segwalk_ws.cuh", "quat_segwalk_bwd.cuh",
@@ -664,6 +667,7 @@ def run_ours(args, w, world, rank, local):
                      "achieved": bwd_gbs, "peak": peak,
                      "unit": "GB/s", "frac": bwd_gbs / peak, "peak_source": peak_src,
                      "traffic": recorded_traffic("quat_cumprod_bwd", w.name),
+                     "traffic_source": TRAFFIC_NOTE,
                      "algorithmic_bytes_per_launch": BWD_BYTES_PER_ELEMENT * E,
                      "avg_launch_ms": bwd_avg},
         "roofline_fwd": {"bound": "hbm", "kernel": design_name("quat_cumprod_fwd", fwd_kernels, fwd_variant),
