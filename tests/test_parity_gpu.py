@@ -474,6 +474,25 @@ def test_short_sequences(dev, fv, bv, at):
     check_against_oracle(dev, *workloads.make_inputs(w))
 
 
+@pytest.mark.parametrize("fv,bv", SHORT_PAIRS)
+def test_short_sequences_non_unit_quaternions(dev, fv, bv):
+    """The scans compose segment products and affine cotangent maps exactly for
+    every quaternion: norms drifting along the configuration's longest sequence,
+    a large init, and ragged lane groups."""
+    lib = qs.load_library()
+    S = min(SHORT_FWD[fv], SHORT_BWD[bv])
+    rng = np.random.default_rng(fv * 31 + bv)
+    q = rng.standard_normal((2, S, 3, 5, 4))
+    q /= np.linalg.norm(q, axis=-1, keepdims=True)
+    q *= rng.uniform(0.999, 1.001, (2, S, 3, 5, 1))
+    init = (rng.standard_normal((2, 3, 5, 4)) * 3).astype(np.float32)
+    d_cum = rng.standard_normal(q.shape).astype(np.float32)
+    assert lib.quat_cumprod_debug_set_variant(fv, bv) == qs.QS_OK
+    assert qs.quat_cumprod_plan("fwd", 2, S, 3, 5, device=dev) == (fv, 1)
+    assert qs.quat_cumprod_plan("bwd", 2, S, 3, 5, device=dev) == (bv, 1)
+    check_against_oracle(dev, q.astype(np.float32), init, d_cum)
+
+
 @pytest.mark.parametrize("fv,bv", [(25, 25), (28, 28)])
 def test_short_sequences_past_their_length_take_another_design(dev, fv, bv):
     """A short-sequence configuration asked for a longer sequence is not used."""
@@ -510,9 +529,11 @@ def test_segmented_backward_long_sequences(dev, variant, dims):
     assert_parity(d_init.cpu().numpy(), ri, "d_init (from carries)")
 
 
-def test_segmented_backward_non_unit_quaternions(dev):
+@pytest.mark.parametrize("fv,bv", [(-1, 11), (24, 31), (22, 24)])
+def test_segmented_backward_non_unit_quaternions(dev, fv, bv):
     """The affine segment maps are exact for every quaternion: strongly non-unit
-    q over many segments (norms drift far from one along the sequence)."""
+    q over many segments (norms drift far from one along the sequence); the
+    table forward and the backward with walk 2 two units behind as well."""
     rng = np.random.default_rng(9)
     B, S, H, J = 1, 5000, 2, 8
     q = rng.standard_normal((B, S, H, J, 4))
@@ -522,7 +543,7 @@ def test_segmented_backward_non_unit_quaternions(dev):
     init = (rng.standard_normal((B, H, J, 4)) * 3).astype(np.float32)
     d_cum = rng.standard_normal(q.shape).astype(np.float32)
     lib = qs.load_library()
-    assert lib.quat_cumprod_debug_set_variant(-1, 11) == qs.QS_OK
+    assert lib.quat_cumprod_debug_set_variant(fv, bv) == qs.QS_OK
     check_against_oracle(dev, q, init, d_cum)
 
 
