@@ -529,6 +529,27 @@ def test_segmented_backward_long_sequences(dev, variant, dims):
     assert_parity(d_init.cpu().numpy(), ri, "d_init (from carries)")
 
 
+@pytest.mark.parametrize("cap", [1, 2, 5])
+@pytest.mark.parametrize("variant", [22, 24, 31])
+def test_segmented_backward_few_ctas(dev, variant, cap):
+    """The persistent grid capped below the units in flight (one CTA takes every
+    unit in ticket order): a unit waits only on units taken before it, also with
+    walk 2 two units behind walk 1; recomputing and from saved carries."""
+    lib = qs.load_library()
+    assert lib.quat_cumprod_debug_set_variant(-1, variant) == qs.QS_OK
+    assert lib.quat_cumprod_debug_set_walk_cap(cap) == qs.QS_OK
+    w = workloads.custom("segbwd_cap", 2, 3000, 2, 16, q_kind="rotation", theta_max=0.4, seed=90 + cap)
+    q, init, d_cum = workloads.make_inputs(w)
+    check_against_oracle(dev, q, init, d_cum)
+    tq, ti, td = (torch.from_numpy(a).to(dev) for a in (q, init, d_cum))
+    _, carries = qs.quat_cumprod_fwd_carries(tq, ti)
+    d_q, d_init = qs.quat_cumprod_bwd_carries(tq, carries, td)
+    assert qs.quat_cumprod_status(device=dev) == qs.QS_OK
+    rq, ri = oracle.bwd(q, init, d_cum)
+    assert_parity(d_q.cpu().numpy(), rq, "d_q (from carries)")
+    assert_parity(d_init.cpu().numpy(), ri, "d_init (from carries)")
+
+
 @pytest.mark.parametrize("fv,bv", [(-1, 11), (24, 31), (22, 24)])
 def test_segmented_backward_non_unit_quaternions(dev, fv, bv):
     """The affine segment maps are exact for every quaternion: strongly non-unit
