@@ -300,7 +300,7 @@ def test_segmented_walk_alternating_layouts(dev):
         assert_parity(cum.cpu().numpy(), ref, f"cum (case {k})")
 
 
-@pytest.mark.parametrize("variant", [9, 10, 12, 13, 19, 20])   # one CTA role, warp-specialised, each with self-describing values; per-unit tables
+@pytest.mark.parametrize("variant", [9, 10, 12, 13, 19, 20, 22, 24])   # one CTA role, warp-specialised, each with self-describing values; per-unit tables
 def test_segmented_walk_stall_reports_timeout_then_recovers(dev, variant):
     lib = qs.load_library()
     assert lib.quat_cumprod_debug_set_variant(variant, -1) == qs.QS_OK
