@@ -358,16 +358,18 @@ def test_segmented_walk_from_concurrent_threads(dev):
         assert isinstance(e, float) and e <= 1e-4, (k, e)
 
 
-def test_graph_capture_replays_match_the_oracle(dev):
+@pytest.mark.parametrize("dims", [(1, 20000, 2, 16), (2, 1000, 3, 8)])
+def test_graph_capture_replays_match_the_oracle(dev, dims):
     """A forward and a backward captured into a CUDA graph, replayed on new inputs.
 
-    The shape has few lane groups, so an eager forward is the segmented walk,
-    whose look-back values are tied to the launch that reads them; under
-    capture the library takes the aggregate / carry / apply forward instead,
-    and every replay must match the oracle."""
+    Both shapes have few lane groups.  On the long one an eager forward is the
+    segmented walk, whose look-back values are tied to the launch that reads
+    them; under capture the library takes the aggregate / carry / apply
+    forward instead.  The short one runs the short-sequence kernels, which keep
+    no state and are captured as they are.  Every replay must match the
+    oracle."""
     lib = qs.load_library()
     assert lib.quat_cumprod_debug_set_variant(-1, -1) == qs.QS_OK
-    dims = (1, 20000, 2, 16)
 
     def inputs(seed):
         return workloads.make_inputs(workloads.custom("graph", *dims, q_kind="rotation", theta_max=0.3, seed=seed))
